@@ -1,0 +1,476 @@
+"""Throughput of one decode step of query-aware block-sparse paged attention.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload llama8b_bf16|fp8_g32|ragged_bf16|offload_bf16]
+
+A step = the whole per-step path of one layer over the batch: summary refresh
+of the block holding the newest token, bound scoring + top-k selection,
+[swap-in for the offload workload], gather-attention with split-K, LSE merge.
+The default workload is the Llama-3-8B-like bf16 layer (8 requests x 32768
+tokens, 32 q / 4 kv heads, head_dim 128, 64-token blocks, 2048-token budget).
+Consecutive steps read distinct layer copies (32 layers, ~17 GB) so every step
+streams its K/V from HBM, not L2.  Steps are replayed from a CUDA graph.
+
+Prints ONE JSON line (rank 0).  Multi-GPU: replicas (every rank runs the same
+per-GPU workload; no data-path collective), launched by torchrun.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+# the CPU baseline times the oracle single-threaded; set before numpy loads
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "sparse decode-attn steps/s (batch×heads) and achieved HBM GB/s vs ~8 TB/s peak"
+UNIT = "head-steps/s"
+
+
+# ----------------------------------------------------------------------------
+# algorithmic bytes (what the method must move; no implementation overheads)
+# ----------------------------------------------------------------------------
+
+def kv_bytes_per_token(num_layers: int, num_kv_heads: int, head_dim: int, elem_bytes: float) -> float:
+    """K and V of one token across the model (SparDA article §1.1 arithmetic)."""
+    return 2 * num_layers * num_kv_heads * head_dim * elem_bytes
+
+
+def token_bytes(w) -> float:
+    """K+V bytes of one token of one kv head as stored (e4m3: codes + scales)."""
+    if w.kv_dtype == "fp8":
+        return 2 * (w.head_dim + (w.head_dim // 32) * 4)
+    return 2 * w.head_dim * (4 if w.kv_dtype == "f32" else 2)
+
+
+def summary_bytes_per_block(w) -> int:
+    return 2 * w.head_dim * (4 if w.kv_dtype == "f32" else 2)
+
+
+def attn_bytes(w, selected_tokens: int, pairs_blocks: int) -> int:
+    """Algorithmic bytes of one attention launch: the selected K/V, q, out,
+    the selection indices and the page-table entries they resolve."""
+    qb = w.batch * w.num_q_heads * w.head_dim * (4 if w.kv_dtype == "f32" else 2)
+    return int(selected_tokens * token_bytes(w) + 2 * qb + 8 * pairs_blocks)
+
+
+def select_bytes(w, total_blocks: int) -> int:
+    """Summaries of every block read once, q, the selection written."""
+    qb = w.batch * w.num_q_heads * w.head_dim * (4 if w.kv_dtype == "f32" else 2)
+    return int(total_blocks * summary_bytes_per_block(w) + qb + 4 * w.batch * w.num_kv_heads * w.capacity)
+
+
+# ----------------------------------------------------------------------------
+# helpers
+# ----------------------------------------------------------------------------
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = [r.split(", ") for r in out.strip().splitlines() if r.strip()]
+        if not rows:
+            once = subprocess.run(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                   "--format=csv,noheader,nounits"], capture_output=True, text=True).stdout
+            rows = [r.split(", ") for r in once.strip().splitlines() if r.strip()]
+        sm = [float(r[1]) for r in rows if len(r) > 2 and r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if len(r) > 2 and r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if len(r) > 5 + i and r[5 + i].strip() == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def max_over_ranks(value: float, world: int, device) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------
+# CPU baseline / reference arm: the oracle as it stands, one (request, kv head)
+# pair of the same workload per step, single thread
+# ----------------------------------------------------------------------------
+
+class OracleStep:
+    def __init__(self, w, pairs: int = 4):
+        import numpy as np
+        import torch
+        import oracle as O
+        from synth import make_inputs
+        self.O, self.np = O, np
+        self.w = w
+        wb = w.scaled(batch=1)  # the sampled pairs come from one request of the workload
+        x = make_inputs(wb, device="cpu")
+        self.pairs = []
+        B = w.block_size
+        for kvh in range(min(pairs, w.num_kv_heads)):
+            row = x["page_table"][0, kvh].numpy()
+            L = int(x["seq_lens"][0])
+            if w.kv_dtype == "fp8":
+                D = w.head_dim
+                kc, ks = O.quantize_e4m3_g32(x["k_pages"].float().numpy().reshape(-1, D))
+                vc, vs = O.quantize_e4m3_g32(x["v_pages"].float().numpy().reshape(-1, D))
+                P = x["k_pages"].shape[0]
+                K = O.kv_values("fp8", O.gather_rows(kc.reshape(P, B, D), row, L, B),
+                                O.gather_rows(ks.reshape(P, B, D // 32), row, L, B))
+                V = O.kv_values("fp8", O.gather_rows(vc.reshape(P, B, D), row, L, B),
+                                O.gather_rows(vs.reshape(P, B, D // 32), row, L, B))
+            else:
+                K = O.kv_values(w.kv_dtype, O.gather_rows(x["k_pages"].float().numpy(), row, L, B))
+                V = O.kv_values(w.kv_dtype, O.gather_rows(x["v_pages"].float().numpy(), row, L, B))
+            smin, smax = O.stored_summaries(*O.block_summaries(K, B), w.kv_dtype)
+            g = w.group
+            qg = x["q"][0, kvh * g:(kvh + 1) * g].float().numpy().astype(np.float64)
+            self.pairs.append((K, V, smin, smax, qg, L))
+        self.i = 0
+
+    def step(self):
+        """One pair's per-step work: refresh the newest block's summary, score,
+        select, attend."""
+        O, w = self.O, self.w
+        K, V, smin, smax, qg, L = self.pairs[self.i % len(self.pairs)]
+        self.i += 1
+        B = w.block_size
+        j = (L - 1) // B
+        lo, hi = O.stored_summaries(*O.block_summaries(K[j * B:L], B), w.kv_dtype)
+        smin[j], smax[j] = lo[0], hi[0]
+        _, score = O.bound_scores(qg, smin, smax)
+        sel = O.select_blocks(score, O.forced_blocks(L, B, w.sink_tokens, w.window_tokens), w.k_scored)
+        O.sparse_attention(qg, K, V, sel, B, 1.0 / math.sqrt(w.head_dim))
+        return w.group  # query heads served
+
+
+def cpu_baseline(w, seconds: float = 12.0) -> dict:
+    st = OracleStep(w)
+    st.step()
+    t0 = time.perf_counter()
+    heads, n = 0, 0
+    while time.perf_counter() - t0 < seconds:
+        heads += st.step()
+        n += 1
+    dt = time.perf_counter() - t0
+    return {"value": heads / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{n} single-(request, kv head) steps of {w.name} (8 query heads each, "
+                      f"{w.ctx_max} tokens, summary refresh + bound + selection + attention), "
+                      f"numpy float64, 1 thread, {dt:.1f} s"}
+
+
+def run_reference(args, w):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    st = OracleStep(w)
+    for _ in range(args.warmup):
+        st.step()
+    t0 = time.perf_counter()
+    heads = 0
+    for _ in range(args.steps):
+        heads += st.step()
+    dt = time.perf_counter() - t0
+    value = heads / dt
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / max(args.steps, 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(w, layers=1),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": f"each step = one (request, kv head) pair of {w.name}, numpy float64, 1 thread"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(w, layers: int) -> dict:
+    return {"workload": w.name, "batch": w.batch, "num_q_heads": w.num_q_heads,
+            "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size,
+            "kv_dtype": w.kv_dtype,
+            "context": w.ctx_max if w.ctx_min == w.ctx_max else [w.ctx_min, w.ctx_max],
+            "sink_tokens": w.sink_tokens, "window_tokens": w.window_tokens, "k_scored": w.k_scored,
+            "layer_copies": layers,
+            "l2": f"inputs larger than L2: {layers} distinct layer copies rotate step to step",
+            "parallelism": "replicas"}
+
+
+# ----------------------------------------------------------------------------
+# GPU arm
+# ----------------------------------------------------------------------------
+
+def run_ours(args, w):
+    import numpy as np
+    import torch
+
+    from query_aware_sparse_hs_gb300 import hs
+    from query_aware_sparse_hs_gb300.decode import SparseDecode
+    from synth import make_layer, make_layout
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    layers = args.layers
+    layout = make_layout(w, dev)
+    lens, table = layout["seq_lens"], layout["page_table"]
+    B, D = w.block_size, w.head_dim
+    L_last_block = int(((lens.max().item() - 1) // B))
+    decs, kvs, qs, keep = [], [], [], []
+    for layer in range(layers):
+        x = make_layer(w, layout, dev, layer)
+        k, v, q = x["k_pages"], x["v_pages"], x["q"]
+        ks = vs = None
+        if w.kv_dtype == "fp8":
+            kc = torch.empty(k.shape, dtype=torch.uint8, device=dev)
+            vc = torch.empty_like(kc)
+            ks = torch.empty(k.shape[:-1] + (D // 32,), dtype=torch.float32, device=dev)
+            vs = torch.empty_like(ks)
+            hs.hs_quantize_e4m3_g32(k, kc, ks)
+            hs.hs_quantize_e4m3_g32(v, vc, vs)
+            del k, v
+            k, v = kc, vc
+        kv = hs.paged_kv(k, v, table, lens, ks, vs)
+        dec = SparseDecode(num_q_heads=w.num_q_heads, num_kv_heads=w.num_kv_heads, head_dim=D,
+                           block_size=B, kv_dtype=w.kv_dtype, batch=w.batch, max_blocks=w.max_blocks,
+                           sink_tokens=w.sink_tokens, window_tokens=w.window_tokens,
+                           k_scored=w.k_scored, device=dev)
+        dec.build_summaries(kv)
+        decs.append(dec)
+        kvs.append(kv)
+        qs.append(q)
+        keep.append((k, v, ks, vs))
+    torch.cuda.synchronize()
+    st_, bits = hs.hs_get_device_error()
+    assert st_ == hs.HS_OK, (st_, bits)
+
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.current_stream().wait_stream(stream)
+
+    def one_step(i, q_override=None):
+        d = decs[i % layers]
+        d.step(kvs[i % layers], qs[i % layers] if q_override is None else q_override,
+               refresh_from_block=L_last_block, stream=stream)
+
+    # eager warm-up (module load, cluster attributes) before capture
+    with torch.cuda.stream(stream):
+        for i in range(layers):
+            one_step(i)
+    stream.synchronize()
+
+    def capture(fn, n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n):
+                fn(i)
+        return g
+
+    g_step = capture(one_step, layers)
+
+    def replay(g, reps):
+        for _ in range(reps):
+            g.replay()
+
+    reps = max(1, math.ceil(args.steps / layers))
+    steps = reps * layers
+    wreps = max(1, math.ceil(args.warmup / layers))
+    with torch.cuda.stream(stream):
+        replay(g_step, wreps)
+    stream.synchronize()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        replay(g_step, reps)
+        e1.record(stream)
+    stream.synchronize()
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1)
+    ms = max_over_ranks(ms, world, dev)
+    ms_per_step = ms / steps
+    value = world * steps * w.batch * w.num_q_heads / (ms / 1e3)
+
+    # ---- per-kernel times (each kernel alone, the same rotating layers) ----
+    def timed_graph(fn, n=layers, rr=None):
+        g = capture(fn, n)
+        with torch.cuda.stream(stream):
+            replay(g, 2)
+        stream.synchronize()
+        rr = rr or max(3, min(reps, 200))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            replay(g, rr)
+            b.record(stream)
+        stream.synchronize()
+        return a.elapsed_time(b) * 1e3 / (rr * n)  # microseconds per launch
+
+    t_attn = timed_graph(lambda i: decs[i % layers].attend(kvs[i % layers], qs[i % layers], stream))
+    t_sel = timed_graph(lambda i: decs[i % layers].select(kvs[i % layers], qs[i % layers], stream=stream))
+    t_ref = timed_graph(lambda i: decs[i % layers].build_summaries(kvs[i % layers], L_last_block, stream))
+    t_sum_full = timed_graph(lambda i: decs[i % layers].build_summaries(kvs[i % layers], 0, stream), rr=3)
+
+    # algorithmic bytes from the actual selection
+    d0 = decs[0]
+    cnt = d0.sel_count.cpu().numpy()
+    sel = d0.sel.cpu().numpy()
+    lens_np = lens.cpu().numpy()
+    sel_tokens = 0
+    for b in range(w.batch):
+        L = int(lens_np[b])
+        for kvh in range(w.num_kv_heads):
+            for j in sel[b, kvh, :cnt[b, kvh]]:
+                sel_tokens += min(B, L - int(j) * B)
+    pairs_blocks = int(cnt.sum())
+    total_blocks = int(sum(w.num_kv_heads * ((int(L) + B - 1) // B) for L in lens_np))
+    a_bytes = attn_bytes(w, sel_tokens, pairs_blocks)
+    s_bytes = select_bytes(w, total_blocks)
+    refresh_bytes = w.batch * w.num_kv_heads * (B * token_bytes(w) / 2 + summary_bytes_per_block(w))
+    step_bytes = a_bytes + s_bytes + refresh_bytes
+    full_sum_bytes = total_blocks * (B * token_bytes(w) / 2 + summary_bytes_per_block(w))
+    peak, peak_kind = load_peaks()
+    attn_gbs = a_bytes / (t_attn * 1e-6) / 1e9
+
+    # ---- end to end through the C ABI with host buffers ----
+    q_host = [torch.empty_like(qs[i], device="cpu").pin_memory() for i in range(layers)]
+    for i in range(layers):
+        q_host[i].copy_(qs[i].cpu())
+    q_dev = [torch.empty_like(qs[i]) for i in range(layers)]
+    out_host = torch.empty((layers,) + tuple(d0.out.shape), dtype=d0.out.dtype).pin_memory()
+    lse_host = torch.empty((layers,) + tuple(d0.lse.shape), dtype=torch.float32).pin_memory()
+
+    def e2e_step(i):
+        li = i % layers
+        q_dev[li].copy_(q_host[li], non_blocking=True)
+        one_step(i, q_dev[li])
+        out_host[li].copy_(decs[li].out, non_blocking=True)
+        lse_host[li].copy_(decs[li].lse, non_blocking=True)
+
+    g_e2e = capture(e2e_step, layers)
+    with torch.cuda.stream(stream):
+        replay(g_e2e, 2)
+    stream.synchronize()
+    barrier(world)
+    a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        a.record(stream)
+        replay(g_e2e, reps)
+        b_.record(stream)
+    stream.synchronize()
+    ms_e2e = max_over_ranks(a.elapsed_time(b_), world, dev)
+    e2e_value = world * steps * w.batch * w.num_q_heads / (ms_e2e / 1e3)
+    h2d = qs[0].numel() * qs[0].element_size()
+    d2h = d0.out.numel() * d0.out.element_size() + d0.lse.numel() * 4
+
+    st_, bits = hs.hs_get_device_error()
+    assert st_ == hs.HS_OK, (st_, bits)
+
+    if rank != 0:
+        return
+    cpu = cpu_baseline(w, seconds=args.cpu_seconds) if (world == 1 and args.cpu_seconds > 0) else None
+    launches_per_step = 4  # summary refresh, score+select, attention, merge
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
+        "warmup": wreps * layers, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.kv_dtype, "data": "synthetic",
+        "config": workload_config(w, layers),
+        "hbm_gbs_step": step_bytes / (ms_per_step * 1e-3) / 1e9,
+        "roofline": {"bound": "hbm", "kernel": "sparse_paged_decode_attn", "achieved": attn_gbs,
+                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": attn_gbs / peak,
+                     "traffic": None, "algorithmic_bytes_per_launch": a_bytes,
+                     "avg_launch_us": t_attn},
+        "kernels_us": {"summary_refresh": t_ref, "score_select": t_sel, "attention_with_merge": t_attn,
+                       "summary_build_full": t_sum_full},
+        "kernels_gbs": {"score_select": s_bytes / (t_sel * 1e-6) / 1e9,
+                        "attention_with_merge": attn_gbs,
+                        "summary_build_full": full_sum_bytes / (t_sum_full * 1e-6) / 1e9},
+        "bytes_per_step": {"attention": a_bytes, "score_select": s_bytes, "summary_refresh": int(refresh_bytes)},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": ms_e2e / steps},
+        "gpu_launches": launches_per_step * steps,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=32000)
+    ap.add_argument("--warmup", type=int, default=640)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="llama8b_bf16")
+    ap.add_argument("--layers", type=int, default=32)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    from synth import WORKLOADS
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

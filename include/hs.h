@@ -1,0 +1,267 @@
+/*
+ * hs.h - C ABI of a GB300 (sm_103a) library for one decode step of query-aware
+ * block-sparse attention over a paged KV cache, with a HiSparse-style hot
+ * device buffer.
+ *
+ * The operations follow these pages:
+ *   [KVS] "KV 稀疏化" (KV-cache sparsity wiki): §2 attention sink + sliding
+ *         window, §5 Quest (per-block min/max summary, coarse filter of the
+ *         query against the summaries, top-k blocks, full attention on the
+ *         chosen blocks only), §7 HiSparse (hot device buffer, host inactive KV,
+ *         swap-in kernel that detects misses, updates the page table and brings
+ *         KV back).
+ *   [SPD] "SparDA：把KV選擇提前一層，長上下文推理顯存帶寬雙優化": §4.2 the
+ *         selector keeps sink + local window + remote top-k; §4.3 the sparse
+ *         index lives on top of PagedAttention blocks.
+ *   [FLL] "分块稀疏注意力与KV Cache量化：长文本推理显存优化实践": §2.2 tiled
+ *         attention carrying a running max and normaliser across tiles, §2.4
+ *         grouped KV quantisation with a per-group scale, §3.2 group size 32.
+ *
+ * Conventions shared by every call
+ *   - Every buffer is owned by the caller.  Device pointers must point to
+ *     memory of the current CUDA device; the library never allocates, frees or
+ *     synchronises (except hs_get_device_error).
+ *   - Calls are asynchronous and ordered on `stream` (a cudaStream_t; NULL is
+ *     the legacy default stream).
+ *   - Arguments are checked on the host before anything is launched; a failed
+ *     check returns HS_ERR_INVALID_ARG / HS_ERR_UNSUPPORTED and launches
+ *     nothing.  Errors found by a kernel (a page id outside the pool, a block
+ *     index outside the request, a selection larger than a capacity) set bits
+ *     in a per-device error word read by hs_get_device_error(); the kernel
+ *     skips the offending item and carries on.
+ *   - No C++ exception crosses this interface.
+ *
+ * Layouts (row-major, innermost last)
+ *   B = block_size tokens per block (= per page), D = head_dim,
+ *   Hq / Hkv query / kv heads, g = Hq / Hkv query heads per kv head,
+ *   N_b = ceil(seq_lens[b] / B) blocks of request b.
+ *   k_pages, v_pages  [num_pages][B][D]   f32 | bf16 | e4m3 (one byte)
+ *   k_scales,v_scales [num_pages][B][D/32] f32 (e4m3 only, else NULL)
+ *   page_table        [batch][Hkv][max_blocks] int32: physical page of block j
+ *                     of (b, kvh); only entries j < N_b are read.
+ *   seq_lens          [batch] int32 tokens of each request, including the
+ *                     token being decoded.
+ *   q                 [batch][Hq][D]  f32 for f32 K/V, bf16 otherwise.
+ *   smin, smax        [batch][Hkv][max_blocks][D]  f32 for f32 K/V, bf16
+ *                     otherwise.
+ *   sel               [batch][Hkv][capacity] int32 ascending block indices,
+ *                     entries past sel_count are -1.
+ *   sel_count         [batch][Hkv] int32.
+ *   out               [batch][Hq][D]  bf16, or f32 when out_is_fp32.
+ *   lse               [batch][Hq] f32 natural-log sum of exp of the logits.
+ */
+#ifndef HS_H_
+#define HS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define HS_API __attribute__((visibility("default")))
+#else
+#define HS_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* hs_stream_t; /* cudaStream_t */
+
+typedef enum hs_status {
+  HS_OK = 0,
+  HS_ERR_INVALID_ARG = 1,  /* null pointer, bad size, bad layout */
+  HS_ERR_UNSUPPORTED = 2,  /* valid but not built: head_dim, group size, ... */
+  HS_ERR_CUDA = 3,         /* a CUDA runtime call failed */
+  HS_ERR_OUT_OF_RANGE = 4, /* device: page id or block index outside its range */
+  HS_ERR_CAPACITY = 5,     /* device: selection larger than capacity / hot slots */
+  HS_ERR_TIMEOUT = 6,      /* device: a bounded wait gave up */
+  HS_ERR_WORKSPACE = 7     /* workspace missing or smaller than hs_workspace_bytes */
+} hs_status;
+
+/* Bits of the per-device error word. */
+#define HS_EBIT_PAGE_RANGE 0x1u  /* page id < 0 or >= num_pages */
+#define HS_EBIT_CAPACITY 0x2u    /* count > capacity, or > hot-buffer slots */
+#define HS_EBIT_TIMEOUT 0x4u     /* a bounded device wait expired */
+#define HS_EBIT_BLOCK_RANGE 0x8u /* selected block index outside [0, N_b) */
+
+typedef enum hs_kv_dtype {
+  HS_KV_F32 = 0,         /* fp32 K/V, fp32 q, fp32 summaries */
+  HS_KV_BF16 = 1,        /* bf16 K/V, bf16 q, bf16 summaries */
+  HS_KV_FP8E4M3_G32 = 2  /* e4m3 K/V + one fp32 scale per 32 channels per token;
+                            bf16 q; bf16 summaries rounded outward */
+} hs_kv_dtype;
+
+/* Attention geometry.  head_dim in {64, 128}; num_q_heads / num_kv_heads in
+ * {1, 2, 4, 8, 16}; block_size in [1, 256] (the tensor-core attention path
+ * needs block_size in {16, 32, 64, 128}). */
+typedef struct hs_attn_shape {
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t block_size;
+  int32_t kv_dtype; /* hs_kv_dtype */
+} hs_attn_shape;
+
+/* A paged KV cache (device memory, or mapped pinned host memory for reads). */
+typedef struct hs_paged_kv {
+  const void* k_pages;
+  const void* v_pages;
+  const float* k_scales; /* e4m3 only */
+  const float* v_scales; /* e4m3 only */
+  const int32_t* page_table;
+  const int32_t* seq_lens;
+  int32_t batch;
+  int32_t max_blocks; /* row length of page_table, smin/smax and scores */
+  int64_t num_pages;  /* pages in k_pages / v_pages: valid ids are [0, num_pages) */
+} hs_paged_kv;
+
+/* Which blocks are forced and how many more are chosen by score
+ * ([KVS] §2, [SPD] §4.2): a block is forced when it overlaps the first
+ * sink_tokens tokens or the last window_tokens tokens of its request; k_scored
+ * further blocks are the best-scoring of the rest (ties -> lower index).
+ * capacity is the row length of sel and must be >= the largest possible
+ * selection, ceil(sink/B) + ceil(window/B) + 1 + k_scored (or max_blocks if
+ * smaller). */
+typedef struct hs_select_params {
+  int32_t sink_tokens;
+  int32_t window_tokens;
+  int32_t k_scored;
+  int32_t capacity;
+} hs_select_params;
+
+/* Attention options.  scale multiplies q.k (usually 1/sqrt(head_dim)).
+ * blocks_per_split: selected blocks handled by one CTA before the LSE merge;
+ * 0 = chosen by the library from the device's SM count.  algo: 0 = automatic,
+ * 1 = CUDA-core kernel (every dtype), 2 = tensor-core (tcgen05) kernel (bf16 and
+ * e4m3 only; HS_ERR_UNSUPPORTED otherwise). */
+typedef struct hs_attn_params {
+  float scale;
+  int32_t out_is_fp32;
+  int32_t blocks_per_split;
+  int32_t algo;
+} hs_attn_params;
+
+/* HiSparse hot buffer ([KVS] §7).  One stream per (request, kv head) owns
+ * slots_per_stream consecutive pages of the slot pool; global slot id of
+ * (pair p = b*Hkv + kvh, slot s) is p*slots_per_stream + s, and that id is what
+ * page_table holds, so the attention call reads the slot pool with this table.
+ *   page_table  [batch][Hkv][max_blocks] device int32: slot id or -1
+ *   slot_owner  [batch][Hkv][slots_per_stream] device int32: block or -1
+ *   last_used   [batch][Hkv][slots_per_stream] device int32: step or -1
+ *   k_slots, v_slots            device [batch*Hkv*slots_per_stream][B][D]
+ *   k_slot_scales,v_slot_scales device [..][B][D/32] (e4m3 only)
+ *   host_k, host_v        pinned, mapped host memory [batch][Hkv][max_blocks][B][D]
+ *   host_k_scales, host_v_scales  pinned host [..][B][D/32] (e4m3 only)
+ * Start state: page_table, slot_owner and last_used all -1. */
+typedef struct hs_hot_buffer {
+  int32_t* page_table;
+  int32_t* slot_owner;
+  int32_t* last_used;
+  void* k_slots;
+  void* v_slots;
+  float* k_slot_scales;
+  float* v_slot_scales;
+  const void* host_k;
+  const void* host_v;
+  const float* host_k_scales;
+  const float* host_v_scales;
+  int32_t batch;
+  int32_t max_blocks;
+  int32_t slots_per_stream;
+} hs_hot_buffer;
+
+/* Counters accumulated (atomically added) by hs_swapin_misses; device memory. */
+typedef struct hs_swap_stats {
+  unsigned long long hits;
+  unsigned long long misses;
+  unsigned long long evictions;
+  unsigned long long bytes_in;
+} hs_swap_stats;
+
+HS_API const char* hs_status_string(hs_status s);
+HS_API int32_t hs_version(void);
+
+/* Bytes of device workspace that hs_sparse_paged_decode_attn needs for this
+ * geometry on the current device (split partials: per query head and split, D
+ * floats of output and one float of log-sum-exp).  0 on invalid input. */
+HS_API size_t hs_workspace_bytes(const hs_attn_shape* shape, int32_t batch, int32_t capacity,
+                          const hs_attn_params* params);
+
+/* Per-block key summaries, [KVS] §5 Quest: for every request b, kv head kvh and
+ * block j with first_block <= j < N_b, smin/smax[b][kvh][j][d] = min/max over
+ * the block's valid tokens t in [jB, min((j+1)B, L_b)) of K[t][d].  e4m3 K is
+ * dequantised (code * scale in fp32) first and the results rounded outward to
+ * bf16 (min toward -inf, max toward +inf).  Other entries are not written.
+ * Reading a page id outside [0, num_pages) sets HS_EBIT_PAGE_RANGE and skips
+ * that block. */
+HS_API hs_status hs_build_block_summaries(const hs_attn_shape* shape, const hs_paged_kv* kv,
+                                   int32_t first_block, void* smin, void* smax,
+                                   hs_stream_t stream);
+
+/* Bound scoring and block selection, [KVS] §5 Quest + §2 sink/window:
+ *   U[b][h][j] = sum_d max(q[b][h][d] * smax[b][kvh][j][d],
+ *                          q[b][h][d] * smin[b][kvh][j][d])
+ *   score[b][kvh][j] = max of U over the g query heads of kv head kvh
+ * then sel = forced blocks + the k_scored best other blocks (score descending,
+ * lower index first on ties, NaN last), ascending; all N_b blocks when that
+ * covers them.  sel_count = number selected; sel entries up to capacity past
+ * the count are -1.  scores_opt (nullable) [batch][Hkv][max_blocks] f32
+ * receives the scores of blocks j < N_b.  No workspace is needed
+ * (workspace/ws_bytes may be NULL/0).  Requires max_blocks <= 16384. */
+HS_API hs_status hs_score_select_topk(const hs_attn_shape* shape, const hs_paged_kv* kv, const void* q,
+                               const void* smin, const void* smax,
+                               const hs_select_params* params, int32_t* sel,
+                               int32_t* sel_count, float* scores_opt, void* workspace,
+                               size_t ws_bytes, hs_stream_t stream);
+
+/* Attention over the selected blocks, [KVS] §5 (full attention on the chosen
+ * blocks) with the tiled running-max/normaliser softmax of [FLL] §2.2, split
+ * over CTAs and combined by a log-sum-exp merge:
+ *   for query head h (kv head kvh = h / g) and the valid tokens t of the blocks
+ *   in sel[b][kvh][0 .. sel_count):
+ *     s_t = (q[b][h] . K[t]) * scale,  out = sum_t softmax(s)_t V[t],
+ *     lse = log sum_t exp(s_t)
+ * An empty selection gives out = 0 and lse = -inf.  Tokens past seq_lens[b] in
+ * the last block are never read into the result.  workspace must hold
+ * hs_workspace_bytes(shape, batch, capacity, params) bytes.  lse_opt nullable. */
+HS_API hs_status hs_sparse_paged_decode_attn(const hs_attn_shape* shape, const hs_paged_kv* kv,
+                                      const void* q, const int32_t* sel,
+                                      const int32_t* sel_count, int32_t capacity,
+                                      const hs_attn_params* params, void* out, float* lse_opt,
+                                      void* workspace, size_t ws_bytes, hs_stream_t stream);
+
+/* HiSparse swap-in, [KVS] §7: for every (b, kvh), make each selected block
+ * resident in the stream's hot slots.  Hits set last_used = step.  Misses are
+ * taken in ascending block order; each goes to the lowest free slot, else to
+ * the slot whose block is not in the current selection with the smallest
+ * last_used (ties -> lowest slot), whose block's page_table entry becomes -1.
+ * The missing page (K, V and, for e4m3, their scales) is then copied from the
+ * host pool into its slot.  A selection larger than slots_per_stream sets
+ * HS_EBIT_CAPACITY and leaves that stream untouched.  stats_opt (nullable,
+ * device) accumulates hits, misses, evictions and bytes copied. */
+HS_API hs_status hs_swapin_misses(const hs_attn_shape* shape, const hs_hot_buffer* hb,
+                           const int32_t* sel, const int32_t* sel_count, int32_t capacity,
+                           int32_t step, hs_swap_stats* stats_opt, hs_stream_t stream);
+
+/* Grouped e4m3 quantisation of K or V rows, [FLL] §2.4 + §3.2: for each row
+ * of head_dim values and each 32-channel group, scale = amax / 448 (fp32; 1
+ * when amax == 0) and code = e4m3(x / scale), nearest-even, saturated to
+ * +-448.  src [rows][head_dim] f32 (src_is_fp32) or bf16; codes
+ * [rows][head_dim] bytes; scales [rows][head_dim/32] f32. */
+HS_API hs_status hs_quantize_e4m3_g32(const void* src, int32_t src_is_fp32, int64_t rows,
+                               int32_t head_dim, uint8_t* codes, float* scales,
+                               hs_stream_t stream);
+
+/* Synchronises `stream`, then reads and clears the current device's error
+ * word.  Returns HS_OK when no bit was set, else, in this order of priority:
+ * HS_ERR_OUT_OF_RANGE (PAGE_RANGE or BLOCK_RANGE), HS_ERR_CAPACITY,
+ * HS_ERR_TIMEOUT.  bits_opt (nullable) receives the raw bits.  A failed
+ * synchronisation (an earlier kernel fault) returns HS_ERR_CUDA. */
+HS_API hs_status hs_get_device_error(hs_stream_t stream, uint32_t* bits_opt);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HS_H_ */

@@ -1,0 +1,353 @@
+// C-ABI layer: argument checks, launch geometry, the per-device error word.
+// Nothing here allocates device memory or synchronises, except
+// hs_get_device_error.
+#include <mutex>
+
+#include "hs_internal.h"
+
+namespace hs {
+namespace {
+
+__device__ unsigned int g_error_word;  // HS_EBIT_* bits, cleared by hs_get_device_error
+
+constexpr int kMaxDevices = 64;
+unsigned* g_err_ptr[kMaxDevices];
+int g_sm_count[kMaxDevices];
+std::mutex g_mu;
+
+struct Device {
+  int id;
+  unsigned* err;
+  int sms;
+};
+
+hs_status current_device(Device* d) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return HS_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return HS_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return HS_ERR_CUDA;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return HS_ERR_CUDA;
+    g_sm_count[dev] = sms;
+    g_err_ptr[dev] = static_cast<unsigned*>(p);
+  }
+  d->id = dev;
+  d->err = g_err_ptr[dev];
+  d->sms = g_sm_count[dev];
+  return HS_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+hs_status check_shape(const hs_attn_shape* s) {
+  if (!s) return HS_ERR_INVALID_ARG;
+  if (s->num_q_heads <= 0 || s->num_kv_heads <= 0 || s->num_q_heads % s->num_kv_heads != 0)
+    return HS_ERR_INVALID_ARG;
+  const int g = s->num_q_heads / s->num_kv_heads;
+  if (g != 1 && g != 2 && g != 4 && g != 8 && g != 16) return HS_ERR_UNSUPPORTED;
+  if (s->head_dim != 64 && s->head_dim != 128) return HS_ERR_UNSUPPORTED;
+  if (s->block_size < 1 || s->block_size > 256) return HS_ERR_UNSUPPORTED;
+  if (s->kv_dtype < HS_KV_F32 || s->kv_dtype > HS_KV_FP8E4M3_G32) return HS_ERR_INVALID_ARG;
+  return HS_OK;
+}
+
+int elem_bytes(int kv_dtype) { return kv_dtype == HS_KV_F32 ? 4 : (kv_dtype == HS_KV_BF16 ? 2 : 1); }
+
+hs_status check_kv(const hs_attn_shape* s, const hs_paged_kv* kv, bool need_v) {
+  if (!kv || !kv->k_pages || !kv->page_table || !kv->seq_lens) return HS_ERR_INVALID_ARG;
+  if (need_v && !kv->v_pages) return HS_ERR_INVALID_ARG;
+  if (s->kv_dtype == HS_KV_FP8E4M3_G32 && (!kv->k_scales || (need_v && !kv->v_scales)))
+    return HS_ERR_INVALID_ARG;
+  if (kv->batch < 0 || kv->max_blocks < 1 || kv->num_pages < 0 || kv->num_pages > INT32_MAX)
+    return HS_ERR_INVALID_ARG;
+  if (!aligned(kv->k_pages, 16) || (need_v && !aligned(kv->v_pages, 16))) return HS_ERR_INVALID_ARG;
+  if (!aligned(kv->page_table, 4) || !aligned(kv->seq_lens, 4)) return HS_ERR_INVALID_ARG;
+  return HS_OK;
+}
+
+KvView make_view(const hs_attn_shape* s, const hs_paged_kv* kv) {
+  KvView v;
+  v.k_pages = kv->k_pages;
+  v.v_pages = kv->v_pages;
+  v.k_scales = kv->k_scales;
+  v.v_scales = kv->v_scales;
+  v.page_table = kv->page_table;
+  v.seq_lens = kv->seq_lens;
+  v.num_pages = kv->num_pages;
+  v.batch = kv->batch;
+  v.max_blocks = kv->max_blocks;
+  v.hq = s->num_q_heads;
+  v.hkv = s->num_kv_heads;
+  v.group = s->num_q_heads / s->num_kv_heads;
+  v.head_dim = s->head_dim;
+  v.block = s->block_size;
+  v.kv_dtype = s->kv_dtype;
+  return v;
+}
+
+int max_selected(const hs_attn_shape* s, int max_blocks, int sink, int window, int k) {
+  const int64_t B = s->block_size;
+  const int64_t forced = (sink + B - 1) / B + (window > 0 ? (window + B - 1) / B + 1 : 0);
+  const int64_t m = forced + k;
+  return static_cast<int>(m < max_blocks ? m : max_blocks);
+}
+
+// Split-K geometry: about two CTAs per SM over all (request, kv head) pairs,
+// each split a whole number of 128-token chunks where blocks are shorter.
+void split_geometry(const hs_attn_shape* s, int batch, int capacity, const hs_attn_params* p,
+                    int sms, int* bps_out, int* splits_out) {
+  const int cap = capacity > 0 ? capacity : 1;
+  int bps = p ? p->blocks_per_split : 0;
+  if (bps <= 0) {
+    const int64_t pairs = static_cast<int64_t>(batch) * s->num_kv_heads;
+    int64_t want = pairs > 0 ? (2LL * (sms > 0 ? sms : 148) + pairs - 1) / pairs : 1;
+    if (want < 1) want = 1;
+    if (want > cap) want = cap;
+    bps = static_cast<int>((cap + want - 1) / want);
+    const int per_chunk = s->block_size < 128 ? 128 / s->block_size : 1;
+    bps = ((bps + per_chunk - 1) / per_chunk) * per_chunk;
+  }
+  *bps_out = bps;
+  *splits_out = (cap + bps - 1) / bps;
+}
+
+size_t workspace_for(const hs_attn_shape* s, int batch, int splits) {
+  const size_t rows = static_cast<size_t>(batch) * s->num_q_heads * splits;
+  const size_t bytes = rows * (s->head_dim + 1) * sizeof(float);
+  return (bytes + 255) & ~static_cast<size_t>(255);
+}
+
+hs_status from_cuda(cudaError_t e) { return e == cudaSuccess ? HS_OK : HS_ERR_CUDA; }
+
+}  // namespace
+}  // namespace hs
+
+using namespace hs;
+
+extern "C" {
+
+const char* hs_status_string(hs_status s) {
+  switch (s) {
+    case HS_OK: return "ok";
+    case HS_ERR_INVALID_ARG: return "invalid argument";
+    case HS_ERR_UNSUPPORTED: return "unsupported configuration";
+    case HS_ERR_CUDA: return "CUDA runtime error";
+    case HS_ERR_OUT_OF_RANGE: return "page id or block index out of range";
+    case HS_ERR_CAPACITY: return "selection larger than capacity";
+    case HS_ERR_TIMEOUT: return "device wait timed out";
+    case HS_ERR_WORKSPACE: return "workspace too small";
+  }
+  return "unknown status";
+}
+
+int32_t hs_version(void) { return 1; }
+
+size_t hs_workspace_bytes(const hs_attn_shape* shape, int32_t batch, int32_t capacity,
+                          const hs_attn_params* params) {
+  if (check_shape(shape) != HS_OK || batch < 0 || capacity < 0) return 0;
+  Device d{};
+  int sms = 148;
+  if (current_device(&d) == HS_OK) sms = d.sms;
+  int bps, splits;
+  split_geometry(shape, batch, capacity, params, sms, &bps, &splits);
+  return workspace_for(shape, batch, splits);
+}
+
+hs_status hs_build_block_summaries(const hs_attn_shape* shape, const hs_paged_kv* kv,
+                                   int32_t first_block, void* smin, void* smax,
+                                   hs_stream_t stream) {
+  hs_status st = check_shape(shape);
+  if (st != HS_OK) return st;
+  if ((st = check_kv(shape, kv, false)) != HS_OK) return st;
+  if (!smin || !smax || !aligned(smin, 16) || !aligned(smax, 16)) return HS_ERR_INVALID_ARG;
+  if (first_block < 0 || first_block > kv->max_blocks) return HS_ERR_INVALID_ARG;
+  Device d;
+  if ((st = current_device(&d)) != HS_OK) return st;
+  const KvView v = make_view(shape, kv);
+  return from_cuda(launch_summaries(v, first_block, smin, smax, d.err,
+                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
+hs_status hs_score_select_topk(const hs_attn_shape* shape, const hs_paged_kv* kv, const void* q,
+                               const void* smin, const void* smax,
+                               const hs_select_params* params, int32_t* sel,
+                               int32_t* sel_count, float* scores_opt, void* workspace,
+                               size_t ws_bytes, hs_stream_t stream) {
+  (void)workspace;
+  (void)ws_bytes;
+  hs_status st = check_shape(shape);
+  if (st != HS_OK) return st;
+  if (!kv || !kv->seq_lens || kv->batch < 0 || kv->max_blocks < 1) return HS_ERR_INVALID_ARG;
+  if (!q || !smin || !smax || !sel || !sel_count || !params) return HS_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(smin, 16) || !aligned(smax, 16) || !aligned(sel, 4) ||
+      !aligned(sel_count, 4) || (scores_opt && !aligned(scores_opt, 4)))
+    return HS_ERR_INVALID_ARG;
+  if (params->sink_tokens < 0 || params->window_tokens < 0 || params->k_scored < 0 ||
+      params->capacity < 1)
+    return HS_ERR_INVALID_ARG;
+  if (kv->max_blocks > kMaxSelectBlocks) return HS_ERR_UNSUPPORTED;
+  if (params->capacity < max_selected(shape, kv->max_blocks, params->sink_tokens,
+                                      params->window_tokens, params->k_scored))
+    return HS_ERR_CAPACITY;
+  Device d;
+  if ((st = current_device(&d)) != HS_OK) return st;
+  KvView v = make_view(shape, kv);
+  SelectArgs a;
+  a.q = q;
+  a.smin = smin;
+  a.smax = smax;
+  a.sel = sel;
+  a.sel_count = sel_count;
+  a.scores = scores_opt;
+  a.sink_tokens = params->sink_tokens;
+  a.window_tokens = params->window_tokens;
+  a.k_scored = params->k_scored;
+  a.capacity = params->capacity;
+  return from_cuda(launch_score_select(v, a, d.err, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+hs_status hs_sparse_paged_decode_attn(const hs_attn_shape* shape, const hs_paged_kv* kv,
+                                      const void* q, const int32_t* sel,
+                                      const int32_t* sel_count, int32_t capacity,
+                                      const hs_attn_params* params, void* out, float* lse_opt,
+                                      void* workspace, size_t ws_bytes, hs_stream_t stream) {
+  hs_status st = check_shape(shape);
+  if (st != HS_OK) return st;
+  if ((st = check_kv(shape, kv, true)) != HS_OK) return st;
+  if (!q || !sel || !sel_count || !out || !params || capacity < 1) return HS_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(sel, 4) || !aligned(sel_count, 4))
+    return HS_ERR_INVALID_ARG;
+  if (params->algo < 0 || params->algo > 2 || params->blocks_per_split < 0) return HS_ERR_INVALID_ARG;
+  Device d;
+  if ((st = current_device(&d)) != HS_OK) return st;
+  const KvView v = make_view(shape, kv);
+  bool use_tc;
+  if (params->algo == 1) {
+    use_tc = false;
+  } else if (params->algo == 2) {
+    if (!attn_tc_supported(v)) return HS_ERR_UNSUPPORTED;
+    use_tc = true;
+  } else {
+    use_tc = attn_tc_supported(v);
+  }
+  AttnArgs a;
+  split_geometry(shape, kv->batch, capacity, params, d.sms, &a.blocks_per_split, &a.splits);
+  const size_t need = workspace_for(shape, kv->batch, a.splits);
+  if (need > 0 && (!workspace || ws_bytes < need || !aligned(workspace, 16))) return HS_ERR_WORKSPACE;
+  a.q = q;
+  a.sel = sel;
+  a.sel_count = sel_count;
+  a.capacity = capacity;
+  a.scale = params->scale;
+  a.out_is_fp32 = params->out_is_fp32 ? 1 : 0;
+  a.out = out;
+  a.lse = lse_opt;
+  a.ws_o = static_cast<float*>(workspace);
+  a.ws_lse = a.ws_o + static_cast<size_t>(kv->batch) * shape->num_q_heads * a.splits * shape->head_dim;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = use_tc ? launch_attn_tc(v, a, d.err, s) : launch_attn_simt(v, a, d.err, s);
+  if (e != cudaSuccess) return HS_ERR_CUDA;
+  return from_cuda(launch_merge(v, a, s));
+}
+
+static hs_status device_address(const void* p, const void** out) {
+  if (!p) {
+    *out = nullptr;
+    return HS_OK;
+  }
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return HS_ERR_INVALID_ARG;
+  }
+  if (at.type == cudaMemoryTypeHost || at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) {
+    if (!at.devicePointer) return HS_ERR_INVALID_ARG;
+    *out = at.devicePointer;
+    return HS_OK;
+  }
+  return HS_ERR_INVALID_ARG;  // pageable memory that was never pinned
+}
+
+hs_status hs_swapin_misses(const hs_attn_shape* shape, const hs_hot_buffer* hb,
+                           const int32_t* sel, const int32_t* sel_count, int32_t capacity,
+                           int32_t step, hs_swap_stats* stats_opt, hs_stream_t stream) {
+  hs_status st = check_shape(shape);
+  if (st != HS_OK) return st;
+  if (!hb || !sel || !sel_count || capacity < 1) return HS_ERR_INVALID_ARG;
+  if (!hb->page_table || !hb->slot_owner || !hb->last_used || !hb->k_slots || !hb->v_slots ||
+      !hb->host_k || !hb->host_v)
+    return HS_ERR_INVALID_ARG;
+  const bool fp8 = shape->kv_dtype == HS_KV_FP8E4M3_G32;
+  if (fp8 && (!hb->k_slot_scales || !hb->v_slot_scales || !hb->host_k_scales || !hb->host_v_scales))
+    return HS_ERR_INVALID_ARG;
+  if (hb->batch < 0 || hb->max_blocks < 1 || hb->slots_per_stream < 1 || hb->slots_per_stream > 1024)
+    return HS_ERR_INVALID_ARG;
+  const int64_t page_bytes = static_cast<int64_t>(shape->block_size) * shape->head_dim * elem_bytes(shape->kv_dtype);
+  if (page_bytes % 16 != 0) return HS_ERR_UNSUPPORTED;
+  if (!aligned(hb->k_slots, 16) || !aligned(hb->v_slots, 16) || !aligned(hb->host_k, 16) ||
+      !aligned(hb->host_v, 16))
+    return HS_ERR_INVALID_ARG;
+  Device d;
+  if ((st = current_device(&d)) != HS_OK) return st;
+  HotView v;
+  v.page_table = hb->page_table;
+  v.slot_owner = hb->slot_owner;
+  v.last_used = hb->last_used;
+  v.k_slots = hb->k_slots;
+  v.v_slots = hb->v_slots;
+  v.k_slot_scales = hb->k_slot_scales;
+  v.v_slot_scales = hb->v_slot_scales;
+  const void* p;
+  if ((st = device_address(hb->host_k, &p)) != HS_OK) return st;
+  v.host_k = p;
+  if ((st = device_address(hb->host_v, &p)) != HS_OK) return st;
+  v.host_v = p;
+  if ((st = device_address(hb->host_k_scales, &p)) != HS_OK) return st;
+  v.host_k_scales = static_cast<const float*>(p);
+  if ((st = device_address(hb->host_v_scales, &p)) != HS_OK) return st;
+  v.host_v_scales = static_cast<const float*>(p);
+  v.batch = hb->batch;
+  v.hkv = shape->num_kv_heads;
+  v.max_blocks = hb->max_blocks;
+  v.slots = hb->slots_per_stream;
+  v.block = shape->block_size;
+  v.head_dim = shape->head_dim;
+  v.kv_dtype = shape->kv_dtype;
+  return from_cuda(launch_swapin(v, sel, sel_count, capacity, step, stats_opt, d.err,
+                                 reinterpret_cast<cudaStream_t>(stream)));
+}
+
+hs_status hs_quantize_e4m3_g32(const void* src, int32_t src_is_fp32, int64_t rows,
+                               int32_t head_dim, uint8_t* codes, float* scales,
+                               hs_stream_t stream) {
+  if (!src || !codes || !scales || rows < 0) return HS_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128 && head_dim != 256) return HS_ERR_UNSUPPORTED;
+  if (rows / 8 >= INT32_MAX) return HS_ERR_UNSUPPORTED;
+  Device d;
+  hs_status st = current_device(&d);
+  if (st != HS_OK) return st;
+  return from_cuda(launch_quantize(src, src_is_fp32 != 0, rows, head_dim, codes, scales,
+                                   reinterpret_cast<cudaStream_t>(stream)));
+}
+
+hs_status hs_get_device_error(hs_stream_t stream, uint32_t* bits_opt) {
+  Device d;
+  hs_status st = current_device(&d);
+  if (st != HS_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return HS_ERR_CUDA;
+  unsigned bits = 0;
+  if (cudaMemcpyAsync(&bits, d.err, sizeof(bits), cudaMemcpyDeviceToHost, s) != cudaSuccess) return HS_ERR_CUDA;
+  if (cudaMemsetAsync(d.err, 0, sizeof(unsigned), s) != cudaSuccess) return HS_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return HS_ERR_CUDA;
+  if (bits_opt) *bits_opt = bits;
+  if (bits & (HS_EBIT_PAGE_RANGE | HS_EBIT_BLOCK_RANGE)) return HS_ERR_OUT_OF_RANGE;
+  if (bits & HS_EBIT_CAPACITY) return HS_ERR_CAPACITY;
+  if (bits & HS_EBIT_TIMEOUT) return HS_ERR_TIMEOUT;
+  return HS_OK;
+}
+
+}  // extern "C"

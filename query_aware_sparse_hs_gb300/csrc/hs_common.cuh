@@ -1,0 +1,71 @@
+// Shared device helpers and the launch descriptors passed from the C-ABI layer
+// to the kernels.  sm_103a only.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/hs.h"
+
+namespace hs {
+
+constexpr int kQuantGroup = 32;          // channels per e4m3 scale
+constexpr int kMaxSelectBlocks = 16384;  // blocks per request the selector holds in smem
+constexpr int kSelectCluster = 8;        // CTAs scoring one (request, kv head)
+
+// Everything a kernel needs to address the paged cache of one call.
+struct KvView {
+  const void* k_pages;
+  const void* v_pages;
+  const float* k_scales;
+  const float* v_scales;
+  const int32_t* page_table;
+  const int32_t* seq_lens;
+  int64_t num_pages;
+  int32_t batch;
+  int32_t max_blocks;
+  int32_t hq, hkv, group, head_dim, block;
+  int32_t kv_dtype;
+};
+
+__device__ __forceinline__ void set_error(unsigned* err, unsigned bit) {
+  if (err) atomicOr(err, bit);
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+// Two e4m3 codes (low byte first) to two floats: the conversion is exact.
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t two) {
+  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two), __NV_E4M3);
+  return __half22float2(*reinterpret_cast<__half2*>(&h));
+}
+
+// fp32 score -> unsigned key whose integer order is the float order (-0 and +0
+// are one key); NaN is mapped below every number (key 0).
+__device__ __forceinline__ uint32_t score_key(float s) {
+  if (isnan(s)) return 0u;
+  uint32_t u = (s == 0.0f) ? 0u : __float_as_uint(s);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+template <typename T>
+__device__ __forceinline__ T warp_sum(T v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__host__ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+}  // namespace hs

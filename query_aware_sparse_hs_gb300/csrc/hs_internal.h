@@ -1,0 +1,63 @@
+// Launchers implemented by the kernel translation units and called by the
+// C-ABI layer (hs_api.cu) after argument checks.
+#pragma once
+
+#include "hs_common.cuh"
+
+namespace hs {
+
+struct SelectArgs {
+  const void* q;
+  const void* smin;
+  const void* smax;
+  int32_t* sel;
+  int32_t* sel_count;
+  float* scores;  // nullable
+  int32_t sink_tokens, window_tokens, k_scored, capacity;
+};
+
+struct AttnArgs {
+  const void* q;
+  const int32_t* sel;
+  const int32_t* sel_count;
+  int32_t capacity;
+  float scale;
+  int32_t out_is_fp32;
+  void* out;
+  float* lse;   // nullable
+  float* ws_o;  // [batch][hq][splits][D]
+  float* ws_lse;  // [batch][hq][splits]
+  int32_t blocks_per_split;
+  int32_t splits;
+};
+
+struct HotView {
+  int32_t* page_table;
+  int32_t* slot_owner;
+  int32_t* last_used;
+  void* k_slots;
+  void* v_slots;
+  float* k_slot_scales;
+  float* v_slot_scales;
+  const void* host_k;
+  const void* host_v;
+  const float* host_k_scales;
+  const float* host_v_scales;
+  int32_t batch, hkv, max_blocks, slots, block, head_dim, kv_dtype;
+};
+
+cudaError_t launch_summaries(const KvView& kv, int first_block, void* smin, void* smax,
+                             unsigned* err, cudaStream_t st);
+cudaError_t launch_score_select(const KvView& kv, const SelectArgs& a, unsigned* err,
+                                cudaStream_t st);
+cudaError_t launch_attn_simt(const KvView& kv, const AttnArgs& a, unsigned* err, cudaStream_t st);
+cudaError_t launch_attn_tc(const KvView& kv, const AttnArgs& a, unsigned* err, cudaStream_t st);
+bool attn_tc_supported(const KvView& kv);
+cudaError_t launch_merge(const KvView& kv, const AttnArgs& a, cudaStream_t st);
+cudaError_t launch_swapin(const HotView& hb, const int32_t* sel, const int32_t* sel_count,
+                          int capacity, int step, hs_swap_stats* stats, unsigned* err,
+                          cudaStream_t st);
+cudaError_t launch_quantize(const void* src, bool src_f32, int64_t rows, int head_dim,
+                            uint8_t* codes, float* scales, cudaStream_t st);
+
+}  // namespace hs

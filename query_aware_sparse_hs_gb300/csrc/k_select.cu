@@ -1,0 +1,272 @@
+// Bound scoring + block selection ("KV 稀疏化" wiki §5 Quest, §2 sink/window;
+// SparDA §4.2 selector).
+//
+// One thread-block cluster of kSelectCluster CTAs per (request, kv head).  Each
+// CTA scores a contiguous slice of the request's blocks against the g query
+// heads of the kv head and stores the scores straight into the shared memory
+// of CTA rank 0 (distributed shared memory), so the selection never round-trips
+// through global memory.  After the cluster barrier, rank 0 finds the k-th
+// largest score of the non-forced blocks with a 4-pass 8-bit radix select in
+// shared memory, then writes forced + chosen blocks in ascending order with two
+// block-wide scans (equal-score ranks for the lower-index tie rule, then output
+// positions).
+//
+// Bound:  U_h(j) = sum_d max(q_hd * smax_jd, q_hd * smin_jd)
+//               = sum_d q+_hd * smax_jd + q-_hd * smin_jd,  q+ = max(q,0), q- = min(q,0)
+// (term by term identical in floating point because smax >= smin and rounding
+// is monotonic); the block score is the max of U over the kv head's query heads.
+#include <cooperative_groups.h>
+
+#include "hs_internal.h"
+
+namespace cg = cooperative_groups;
+
+namespace hs {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+
+// Exclusive prefix sum over the CTA; `total` receives the CTA-wide sum.
+__device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int n = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (lane == 31) s_warp[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < kWarps ? s_warp[lane] : 0;
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int n = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += n;
+    }
+    if (lane < kWarps) s_warp[lane] = wi - w;
+    if (lane == kWarps - 1) s_warp[kWarps] = wi;
+  }
+  __syncthreads();
+  const int excl = s_warp[warp] + incl - v;
+  total = s_warp[kWarps];
+  __syncthreads();
+  return excl;
+}
+
+template <int C, bool F32>
+__device__ __forceinline__ void load_summary(const void* base, int64_t off, float (&x)[C]) {
+  if constexpr (F32) {
+    const float* p = static_cast<const float*>(base) + off;
+    if constexpr (C == 4) {
+      float4 v = __ldg(reinterpret_cast<const float4*>(p));
+      x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+    } else {
+      float2 v = __ldg(reinterpret_cast<const float2*>(p));
+      x[0] = v.x; x[1] = v.y;
+    }
+  } else {
+    const uint16_t* p = static_cast<const uint16_t*>(base) + off;
+    if constexpr (C == 4) {
+      uint2 v = __ldg(reinterpret_cast<const uint2*>(p));
+      x[0] = __uint_as_float(v.x << 16); x[1] = __uint_as_float(v.x & 0xffff0000u);
+      x[2] = __uint_as_float(v.y << 16); x[3] = __uint_as_float(v.y & 0xffff0000u);
+    } else {
+      uint32_t v = __ldg(reinterpret_cast<const uint32_t*>(p));
+      x[0] = __uint_as_float(v << 16); x[1] = __uint_as_float(v & 0xffff0000u);
+    }
+  }
+}
+
+template <int C, int G, bool F32>
+__global__ void __cluster_dims__(kSelectCluster, 1, 1) __launch_bounds__(kThreads)
+    score_select_kernel(KvView kv, SelectArgs a, unsigned* err) {
+  extern __shared__ float s_scores[];  // [max_blocks]; rank 0's copy holds every score
+  __shared__ uint32_t s_hist[256];
+  __shared__ int s_warp[kWarps + 1];
+  __shared__ int s_pick[2];
+
+  cg::cluster_group cluster = cg::this_cluster();
+  const unsigned rank = cluster.block_rank();
+  const int b = blockIdx.z, kvh = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tid = threadIdx.x;
+  const int B = kv.block;
+  const int L = max(kv.seq_lens[b], 0);
+  int nb = ceil_div(L, B);
+  if (nb > kv.max_blocks) {
+    if (tid == 0 && rank == 0) set_error(err, HS_EBIT_BLOCK_RANGE);
+    nb = kv.max_blocks;
+  }
+  const int64_t pair = static_cast<int64_t>(b) * kv.hkv + kvh;
+  const int D = C * 32;
+
+  // ---- scoring: this CTA's slice of blocks, one warp per block ----
+  {
+    float qp[G][C], qn[G][C];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const int64_t qo = (static_cast<int64_t>(b) * kv.hq + kvh * G + h) * D + lane * C;
+#pragma unroll
+      for (int c = 0; c < C; ++c) {
+        float x = F32 ? static_cast<const float*>(a.q)[qo + c]
+                      : __bfloat162float(static_cast<const __nv_bfloat16*>(a.q)[qo + c]);
+        qp[h][c] = fmaxf(x, 0.0f);
+        qn[h][c] = fminf(x, 0.0f);
+      }
+    }
+    float* dst = cluster.map_shared_rank(s_scores, 0);
+    const int per = ceil_div(nb, kSelectCluster);
+    const int jb = static_cast<int>(rank) * per, je = min(nb, jb + per);
+    for (int j = jb + warp; j < je; j += kWarps) {
+      const int64_t off = (pair * kv.max_blocks + j) * D + lane * C;
+      float mx[C], mn[C];
+      load_summary<C, F32>(a.smax, off, mx);
+      load_summary<C, F32>(a.smin, off, mn);
+      float best = -INFINITY;
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        float acc = 0.0f;
+#pragma unroll
+        for (int c = 0; c < C; ++c) {
+          acc = fmaf(qp[h][c], mx[c], acc);
+          acc = fmaf(qn[h][c], mn[c], acc);
+        }
+        acc = warp_sum(acc);
+        best = fmaxf(best, acc);
+      }
+      if (lane == 0) {
+        dst[j] = best;
+        if (a.scores) a.scores[pair * kv.max_blocks + j] = best;
+      }
+    }
+  }
+  cluster.sync();
+  if (rank != 0) return;
+
+  // ---- selection in rank 0 ----
+  const int sink = a.sink_tokens, win = a.window_tokens, k = a.k_scored, cap = a.capacity;
+  auto forced = [&](int j) -> bool {
+    const int lo = j * B, hi = min(lo + B, L);
+    return lo < sink || (win > 0 && hi > L - win);
+  };
+  int nf_local = 0;
+  for (int j = tid; j < nb; j += kThreads) nf_local += forced(j) ? 1 : 0;
+  int nf;
+  block_exclusive_scan(nf_local, s_warp, nf);
+  const bool take_all = nf + k >= nb;
+  const bool use_threshold = !take_all && k > 0;
+
+  uint32_t T = 0;
+  int need_eq = 0;
+  if (use_threshold) {
+    uint32_t prefix = 0, mask = 0;
+    int kk = k;  // rank (1-based) of the wanted key among keys matching `prefix`
+    for (int shift = 24; shift >= 0; shift -= 8) {
+      for (int i = tid; i < 256; i += kThreads) s_hist[i] = 0;
+      __syncthreads();
+      for (int j = tid; j < nb; j += kThreads) {
+        if (forced(j)) continue;
+        const uint32_t key = score_key(s_scores[j]);
+        if ((key & mask) == prefix) atomicAdd(&s_hist[(key >> shift) & 255u], 1u);
+      }
+      __syncthreads();
+      if (tid == 0) {
+        int acc = 0, d = 255;
+        for (; d > 0; --d) {
+          const int c = static_cast<int>(s_hist[d]);
+          if (acc + c >= kk) break;
+          acc += c;
+        }
+        s_pick[0] = d;
+        s_pick[1] = kk - acc;
+      }
+      __syncthreads();
+      prefix |= static_cast<uint32_t>(s_pick[0]) << shift;
+      mask |= 255u << shift;
+      kk = s_pick[1];
+      __syncthreads();
+    }
+    T = prefix;
+    need_eq = kk;
+  }
+
+  // contiguous index range per thread keeps the output ascending
+  const int per_t = ceil_div(nb, kThreads);
+  const int j0 = min(nb, tid * per_t), j1 = min(nb, j0 + per_t);
+  int eq_local = 0;
+  if (use_threshold)
+    for (int j = j0; j < j1; ++j)
+      if (!forced(j) && score_key(s_scores[j]) == T) ++eq_local;
+  int eq_total;
+  const int eq_base = block_exclusive_scan(eq_local, s_warp, eq_total);
+
+  auto chosen = [&](int j, int& eqr) -> bool {
+    if (take_all || forced(j)) return true;
+    if (!use_threshold) return false;
+    const uint32_t key = score_key(s_scores[j]);
+    if (key > T) return true;
+    if (key == T) return eqr++ < need_eq;
+    return false;
+  };
+  int cnt_local = 0;
+  {
+    int eqr = eq_base;
+    for (int j = j0; j < j1; ++j) cnt_local += chosen(j, eqr) ? 1 : 0;
+  }
+  int total;
+  int pos = block_exclusive_scan(cnt_local, s_warp, total);
+  int32_t* out = a.sel + pair * cap;
+  {
+    int eqr = eq_base;
+    for (int j = j0; j < j1; ++j)
+      if (chosen(j, eqr)) {
+        if (pos < cap) out[pos] = j;
+        ++pos;
+      }
+  }
+  for (int i = total + tid; i < cap; i += kThreads) out[i] = -1;
+  if (tid == 0) {
+    if (total > cap) set_error(err, HS_EBIT_CAPACITY);
+    a.sel_count[pair] = min(total, cap);
+  }
+}
+
+template <int C, int G, bool F32>
+cudaError_t launch_t(const KvView& kv, const SelectArgs& a, unsigned* err, cudaStream_t st) {
+  const size_t smem = static_cast<size_t>(kv.max_blocks) * sizeof(float);
+  auto kern = score_select_kernel<C, G, F32>;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
+  dim3 grid(kSelectCluster, kv.hkv, kv.batch);
+  kern<<<grid, kThreads, smem, st>>>(kv, a, err);
+  return cudaGetLastError();
+}
+
+template <int C, bool F32>
+cudaError_t launch_g(const KvView& kv, const SelectArgs& a, unsigned* err, cudaStream_t st) {
+  switch (kv.group) {
+    case 1: return launch_t<C, 1, F32>(kv, a, err, st);
+    case 2: return launch_t<C, 2, F32>(kv, a, err, st);
+    case 4: return launch_t<C, 4, F32>(kv, a, err, st);
+    case 8: return launch_t<C, 8, F32>(kv, a, err, st);
+    default: return launch_t<C, 16, F32>(kv, a, err, st);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_score_select(const KvView& kv, const SelectArgs& a, unsigned* err,
+                                cudaStream_t st) {
+  if (kv.batch == 0 || kv.hkv == 0) return cudaSuccess;
+  const bool f32 = kv.kv_dtype == HS_KV_F32;
+  if (kv.head_dim == 128) return f32 ? launch_g<4, true>(kv, a, err, st) : launch_g<4, false>(kv, a, err, st);
+  return f32 ? launch_g<2, true>(kv, a, err, st) : launch_g<2, false>(kv, a, err, st);
+}
+
+}  // namespace hs

@@ -1,0 +1,76 @@
+"""Decode-step driver: owns the per-step device buffers and issues the library
+calls of one step in order (summary refresh -> score/select -> [swap-in] ->
+attention).  All buffers are torch allocations made once in the constructor;
+a step itself allocates nothing, so it can be captured in a CUDA graph.
+"""
+
+from __future__ import annotations
+
+import math
+
+import torch
+
+from . import hs
+
+_SUMMARY_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16, "fp8": torch.bfloat16}
+_Q_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16, "fp8": torch.bfloat16}
+
+
+class SparseDecode:
+    def __init__(self, *, num_q_heads, num_kv_heads, head_dim, block_size, kv_dtype, batch,
+                 max_blocks, sink_tokens, window_tokens, k_scored, capacity=None, scale=None,
+                 out_is_fp32=False, algo="auto", blocks_per_split=0, device="cuda"):
+        self.kv_dtype = kv_dtype
+        self.shape = hs.attn_shape(num_q_heads, num_kv_heads, head_dim, block_size, kv_dtype)
+        self.batch, self.max_blocks = int(batch), int(max_blocks)
+        if capacity is None:
+            forced = -(-sink_tokens // block_size) + ((-(-window_tokens // block_size) + 1) if window_tokens > 0 else 0)
+            capacity = min(self.max_blocks, forced + k_scored)
+        self.capacity = int(capacity)
+        self.sel_params = hs.select_params(sink_tokens, window_tokens, k_scored, self.capacity)
+        self.attn_params = hs.attn_params(scale if scale is not None else 1.0 / math.sqrt(head_dim),
+                                          out_is_fp32, blocks_per_split, algo)
+        dev = torch.device(device)
+        sdt = _SUMMARY_DTYPE[kv_dtype]
+        self.smin = torch.empty((batch, num_kv_heads, max_blocks, head_dim), dtype=sdt, device=dev)
+        self.smax = torch.empty_like(self.smin)
+        self.sel = torch.full((batch, num_kv_heads, self.capacity), -1, dtype=torch.int32, device=dev)
+        self.sel_count = torch.zeros((batch, num_kv_heads), dtype=torch.int32, device=dev)
+        self.scores = torch.empty((batch, num_kv_heads, max_blocks), dtype=torch.float32, device=dev)
+        self.out = torch.empty((batch, num_q_heads, head_dim),
+                               dtype=torch.float32 if out_is_fp32 else torch.bfloat16, device=dev)
+        self.lse = torch.empty((batch, num_q_heads), dtype=torch.float32, device=dev)
+        ws = hs.hs_workspace_bytes(self.shape, batch, self.capacity, self.attn_params)
+        self.workspace = torch.empty((max(ws, 256),), dtype=torch.uint8, device=dev)
+
+    def build_summaries(self, kv: hs.PagedKV, first_block: int = 0, stream=None):
+        hs.hs_build_block_summaries(self.shape, kv, first_block, self.smin, self.smax, stream)
+
+    def select(self, kv: hs.PagedKV, q: torch.Tensor, keep_scores: bool = False, stream=None):
+        hs.hs_score_select_topk(self.shape, kv, q, self.smin, self.smax, self.sel_params, self.sel,
+                                self.sel_count, self.scores if keep_scores else None, None, stream)
+
+    def attend(self, kv: hs.PagedKV, q: torch.Tensor, stream=None):
+        hs.hs_sparse_paged_decode_attn(self.shape, kv, q, self.sel, self.sel_count, self.capacity,
+                                       self.attn_params, self.out, self.lse, self.workspace, stream)
+
+    def swap_in(self, hb: hs.HotBuffer, step: int, stats=None, stream=None):
+        hs.hs_swapin_misses(self.shape, hb, self.sel, self.sel_count, self.capacity, step, stats, stream)
+
+    def step(self, kv: hs.PagedKV, q: torch.Tensor, refresh_from_block: int | None = None,
+             hot: tuple | None = None, stream=None):
+        """One decode step.  ``refresh_from_block``: rebuild summaries of blocks
+        from there on (the block holding the newest token) before selecting.
+        ``hot``: (hot_buffer, slot_kv_view, step, stats) for the offload path:
+        the selection is made against ``kv`` (summaries), pages are swapped into
+        the hot slots and attention reads ``slot_kv_view``."""
+        if refresh_from_block is not None:
+            self.build_summaries(kv, refresh_from_block, stream)
+        self.select(kv, q, stream=stream)
+        if hot is not None:
+            hb, slot_kv, step_idx, stats = hot
+            self.swap_in(hb, step_idx, stats, stream)
+            self.attend(slot_kv, q, stream)
+        else:
+            self.attend(kv, q, stream)
+        return self.out, self.lse

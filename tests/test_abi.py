@@ -1,0 +1,74 @@
+"""The C-ABI library loads and exports every function that include/hs.h
+declares; host-side argument checks answer without a GPU.  CPU only (no
+compute call is made)."""
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "hs.h")).read()
+    return re.findall(r"HS_API\s+[\w\s\*]+?\b(hs_\w+)\s*\(", src)
+
+
+def test_header_declares_the_four_entry_points():
+    names = set(_declared())
+    for n in ("hs_build_block_summaries", "hs_score_select_topk", "hs_sparse_paged_decode_attn",
+              "hs_swapin_misses"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    from query_aware_sparse_hs_gb300 import hs
+    lib = hs.library()
+    for name in _declared():
+        assert hasattr(lib, name), name
+        assert name in hs.SYMBOLS, name
+    out = subprocess.run(["nm", "-D", "--defined-only", hs.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r" T (\w+)$", out, re.M))
+    assert exported == set(_declared())
+
+
+def test_status_strings_and_version():
+    from query_aware_sparse_hs_gb300 import hs
+    assert hs.hs_version() >= 1
+    assert hs.hs_status_string(0) == "ok"
+    assert "capacity" in hs.hs_status_string(hs.HS_ERR_CAPACITY)
+    assert hs.hs_status_string(99) == "unknown status"
+
+
+def test_host_checks_reject_bad_arguments_without_a_gpu():
+    from query_aware_sparse_hs_gb300 import hs
+    lib = hs.library()
+    shape = hs.attn_shape(32, 4, 128, 64, "bf16")
+    assert lib.hs_build_block_summaries(ctypes.byref(shape), None, 0, None, None, None) == hs.HS_ERR_INVALID_ARG
+    bad = hs.attn_shape(32, 5, 128, 64, "bf16")
+    assert lib.hs_build_block_summaries(ctypes.byref(bad), None, 0, None, None, None) == hs.HS_ERR_INVALID_ARG
+    odd_dim = hs.attn_shape(32, 4, 80, 64, "bf16")
+    assert lib.hs_build_block_summaries(ctypes.byref(odd_dim), None, 0, None, None, None) == hs.HS_ERR_UNSUPPORTED
+    g3 = hs.attn_shape(12, 4, 128, 64, "bf16")
+    assert lib.hs_build_block_summaries(ctypes.byref(g3), None, 0, None, None, None) == hs.HS_ERR_UNSUPPORTED
+    # a selection capacity below the largest possible selection is refused before launch
+    kv = hs.PagedKV()
+    kv.seq_lens = 0x1000
+    kv.batch, kv.max_blocks = 1, 512
+    params = hs.select_params(4, 256, 27, 31)  # needs 1 + 5 + 27 = 33
+    st = lib.hs_score_select_topk(ctypes.byref(shape), ctypes.byref(kv), 0x1000, 0x1000, 0x1000,
+                                  ctypes.byref(params), 0x1000, 0x1000, None, None, 0, None)
+    assert st == hs.HS_ERR_CAPACITY
+    assert lib.hs_quantize_e4m3_g32(0x1000, 0, 10, 96, 0x1000, 0x1000, None) == hs.HS_ERR_UNSUPPORTED
+    assert lib.hs_workspace_bytes(ctypes.byref(bad), 8, 33, None) == 0
+
+
+def test_workspace_size_formula():
+    from query_aware_sparse_hs_gb300 import hs
+    shape = hs.attn_shape(32, 4, 128, 64, "bf16")
+    p = hs.attn_params(0.1, blocks_per_split=4)
+    # 9 splits of 4 blocks cover 33; (D + 1) floats per (request, q head, split)
+    assert hs.hs_workspace_bytes(shape, 8, 33, p) == ((8 * 32 * 9 * 129 * 4 + 255) // 256) * 256

@@ -1,0 +1,74 @@
+"""Error reporting: host-side argument checks return a status and launch
+nothing; device-detected problems set bits of the error word and the kernels
+skip the offending item.  No test here faults the GPU: every planted error is
+a value the kernels check before using it.  GPU only."""
+
+import numpy as np
+import pytest
+import torch
+
+from synth import WORKLOADS, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def _case():
+    from _parity import Case
+    w = WORKLOADS["llama8b_bf16"].scaled(batch=2, ctx_min=1024, ctx_max=1024, k_scored=4)
+    return Case(w, make_inputs(w))
+
+
+def test_bad_page_id_sets_page_range_bit():
+    from query_aware_sparse_hs_gb300 import hs
+    c = _case()
+    dec = c.decoder(out_is_fp32=True)
+    dec.build_summaries(c.kv)
+    dec.select(c.kv, c.q)
+    assert hs.hs_get_device_error()[0] == hs.HS_OK
+    bad_table = c.page_table.clone()
+    j = int(dec.sel[0, 1, 2])
+    bad_table[0, 1, j] = 1 << 30  # outside the pool: checked before any read
+    kv_bad = hs.paged_kv(c.k_pages, c.v_pages, bad_table, c.seq_lens)
+    dec.attend(kv_bad, c.q)
+    st, bits = hs.hs_get_device_error()
+    assert st == hs.HS_ERR_OUT_OF_RANGE and bits & hs.HS_EBIT_PAGE_RANGE
+    assert np.isfinite(dec.out.cpu().numpy()).all()
+    # the error word is cleared by the read
+    assert hs.hs_get_device_error() == (hs.HS_OK, 0)
+
+
+def test_selected_block_past_the_request_sets_block_range_bit():
+    from query_aware_sparse_hs_gb300 import hs
+    c = _case()
+    dec = c.decoder(out_is_fp32=True)
+    dec.build_summaries(c.kv)
+    dec.select(c.kv, c.q)
+    dec.sel[1, 0, 0] = 10_000
+    dec.attend(c.kv, c.q)
+    st, bits = hs.hs_get_device_error()
+    assert st == hs.HS_ERR_OUT_OF_RANGE and bits & hs.HS_EBIT_BLOCK_RANGE
+
+
+def test_host_side_checks():
+    from query_aware_sparse_hs_gb300 import hs
+    c = _case()
+    dec = c.decoder()
+    small = torch.empty(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(hs.HSError) as e:
+        hs.hs_sparse_paged_decode_attn(dec.shape, c.kv, c.q, dec.sel, dec.sel_count, dec.capacity,
+                                       dec.attn_params, dec.out, dec.lse, small)
+    assert e.value.status == hs.HS_ERR_WORKSPACE
+    tight = hs.select_params(4, 256, 4, 5)  # 5 < 1 + 4 + 1 + 4
+    with pytest.raises(hs.HSError) as e:
+        hs.hs_score_select_topk(dec.shape, c.kv, c.q, dec.smin, dec.smax, tight, dec.sel, dec.sel_count)
+    assert e.value.status == hs.HS_ERR_CAPACITY
+    odd = hs.attn_shape(32, 4, 96, 64, "bf16")
+    with pytest.raises(hs.HSError) as e:
+        hs.hs_build_block_summaries(odd, c.kv, 0, dec.smin, dec.smax)
+    assert e.value.status == hs.HS_ERR_UNSUPPORTED
+    f32shape = hs.attn_shape(32, 4, 128, 64, "f32")
+    with pytest.raises(hs.HSError) as e:
+        hs.hs_sparse_paged_decode_attn(f32shape, c.kv, c.q, dec.sel, dec.sel_count, dec.capacity,
+                                       hs.attn_params(0.1, algo="tcgen05"), dec.out, dec.lse, dec.workspace)
+    assert e.value.status == hs.HS_ERR_UNSUPPORTED
+    assert hs.hs_get_device_error() == (hs.HS_OK, 0)

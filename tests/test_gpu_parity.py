@@ -1,0 +1,266 @@
+"""CUDA path vs the oracle, element by element, on seeded inputs small enough for
+the oracle (several tiles and a ragged tail).  GPU only."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from synth import WORKLOADS, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+CASES = {
+    "tiny_f32": WORKLOADS["tiny_f32"],
+    "llama_bf16_tail": WORKLOADS["llama8b_bf16"].scaled(batch=2, ctx_min=4133, ctx_max=4133, k_scored=20),
+    "ragged_bf16": WORKLOADS["ragged_bf16"].scaled(batch=5, ctx_min=300, ctx_max=5000, k_scored=40),
+    "fp8_tail": WORKLOADS["fp8_g32"].scaled(batch=2, ctx_min=4133, ctx_max=4133, k_scored=20),
+    "d64_g16_bf16": WORKLOADS["llama8b_bf16"].scaled(batch=2, num_q_heads=32, num_kv_heads=2,
+                                                     head_dim=64, block_size=32, ctx_min=1000,
+                                                     ctx_max=1500, k_scored=9),
+}
+
+
+@pytest.fixture(scope="module")
+def cases():
+    from _parity import Case
+    out = {}
+    for name, w in CASES.items():
+        out[name] = Case(w, make_inputs(w))
+    return out
+
+
+def _err_clear():
+    from query_aware_sparse_hs_gb300 import hs
+    st, bits = hs.hs_get_device_error()
+    assert st == 0 and bits == 0, (st, bits)
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_summaries_bit_exact(cases, name):
+    c = cases[name]
+    dec = c.decoder()
+    dec.build_summaries(c.kv)
+    _err_clear()
+    smin, smax = dec.smin.float().cpu().numpy(), dec.smax.float().cpu().numpy()
+    w = c.w
+    for b in range(w.batch):
+        nb = O.num_blocks(c.lens[b], w.block_size)
+        for kvh in range(w.num_kv_heads):
+            K = c.logical(b, kvh, "k")
+            lo, hi = O.stored_summaries(*O.block_summaries(K, w.block_size), w.kv_dtype)
+            assert np.array_equal(smin[b, kvh, :nb], lo.astype(np.float32)), (b, kvh)
+            assert np.array_equal(smax[b, kvh, :nb], hi.astype(np.float32)), (b, kvh)
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_scores_and_selection(cases, name):
+    from _parity import tie_window_ok
+    c = cases[name]
+    w = c.w
+    dec = c.decoder()
+    dec.build_summaries(c.kv)
+    dec.select(c.kv, c.q, keep_scores=True)
+    _err_clear()
+    scores = dec.scores.cpu().numpy()
+    sel = dec.sel.cpu().numpy()
+    cnt = dec.sel_count.cpu().numpy()
+    for b in range(w.batch):
+        for kvh in range(w.num_kv_heads):
+            r = c.oracle_pair(b, kvh)
+            nb = len(r["score"])
+            q = c.q_group(b, kvh)
+            mag = (np.abs(q)[:, None, :] * np.maximum(np.abs(r["smin"]), np.abs(r["smax"]))[None]).sum(-1).max(0)
+            assert np.all(np.abs(scores[b, kvh, :nb] - r["score"]) <= 1e-5 * mag + 1e-30), (b, kvh)
+            n = int(cnt[b, kvh])
+            got = sel[b, kvh, :n].tolist()
+            assert got == sorted(got) and np.all(sel[b, kvh, n:] == -1)
+            assert tie_window_ok(r["score"], r["forced"], got, r["sel"], w.k_scored), (b, kvh, got, r["sel"])
+
+
+@pytest.mark.parametrize("algo", ["simt", "tcgen05"])
+@pytest.mark.parametrize("bps", [0, 1, 3])
+@pytest.mark.parametrize("name", list(CASES))
+def test_attention_on_oracle_selection(cases, name, bps, algo):
+    """Attention with the oracle's own selection fed to the GPU call."""
+    from _parity import TOL
+    c = cases[name]
+    w = c.w
+    dec = c.decoder(out_is_fp32=True, blocks_per_split=bps, algo=algo)
+    from query_aware_sparse_hs_gb300 import hs
+    sel = np.full((w.batch, w.num_kv_heads, dec.capacity), -1, dtype=np.int32)
+    cnt = np.zeros((w.batch, w.num_kv_heads), dtype=np.int32)
+    ref_out = np.zeros((w.batch, w.num_q_heads, w.head_dim))
+    ref_lse = np.zeros((w.batch, w.num_q_heads))
+    ref_raw = np.zeros_like(ref_out)
+    g = w.group
+    for b in range(w.batch):
+        for kvh in range(w.num_kv_heads):
+            r = c.oracle_pair(b, kvh)
+            sel[b, kvh, :len(r["sel"])] = r["sel"]
+            cnt[b, kvh] = len(r["sel"])
+            ref_out[b, kvh * g:(kvh + 1) * g] = r["out"]
+            ref_lse[b, kvh * g:(kvh + 1) * g] = r["lse"]
+            if w.kv_dtype == "fp8":
+                ref_raw[b, kvh * g:(kvh + 1) * g] = c.oracle_pair(b, kvh, dequant=False)["out"]
+    dec.sel.copy_(torch.from_numpy(sel))
+    dec.sel_count.copy_(torch.from_numpy(cnt))
+    try:
+        dec.attend(c.kv, c.q)
+    except hs.HSError as e:
+        if algo == "tcgen05" and e.status == hs.HS_ERR_UNSUPPORTED:
+            pytest.skip("tensor-core path does not take this shape/dtype")
+        raise
+    _err_clear()
+    out = dec.out.cpu().numpy()
+    lse = dec.lse.cpu().numpy()
+    tol = TOL["fp8_dequant"] if w.kv_dtype == "fp8" else TOL[w.kv_dtype]
+    assert np.abs(out - ref_out).max() <= tol
+    assert np.abs(lse - ref_lse).max() <= 1e-4
+    if w.kv_dtype == "fp8":
+        assert np.abs(out - ref_raw).max() <= TOL["fp8"]
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_end_to_end_bf16_output(cases, name):
+    """Full step on the GPU (its own selection), bf16 output, against the oracle."""
+    from _parity import TOL, tie_window_ok
+    c = cases[name]
+    w = c.w
+    if w.kv_dtype == "f32":
+        pytest.skip("fp32 K/V writes fp32 output in this test suite's convention")
+    dec = c.decoder(out_is_fp32=False)
+    dec.build_summaries(c.kv)
+    dec.select(c.kv, c.q, keep_scores=True)
+    dec.attend(c.kv, c.q)
+    _err_clear()
+    out = dec.out.float().cpu().numpy()
+    sel = dec.sel.cpu().numpy()
+    cnt = dec.sel_count.cpu().numpy()
+    g = w.group
+    for b in range(w.batch):
+        for kvh in range(w.num_kv_heads):
+            r = c.oracle_pair(b, kvh)
+            got = sel[b, kvh, :cnt[b, kvh]].tolist()
+            assert tie_window_ok(r["score"], r["forced"], got, r["sel"], w.k_scored)
+            if set(got) != set(r["sel"]):
+                continue
+            ref = r["out"]
+            ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(ref), 1e-30))) - 7)
+            tol = np.maximum(TOL["fp8_dequant"] if w.kv_dtype == "fp8" else TOL["bf16"], ulp)
+            assert np.all(np.abs(out[b, kvh * g:(kvh + 1) * g] - ref) <= tol), (b, kvh)
+
+
+def test_k_covers_everything_is_dense_attention():
+    """With k at least the block count the result is dense softmax attention."""
+    from _parity import Case
+    w = WORKLOADS["tiny_f32"].scaled(k_scored=1000)
+    c = Case(w, make_inputs(w))
+    dec = c.decoder(out_is_fp32=True)
+    dec.build_summaries(c.kv)
+    dec.select(c.kv, c.q)
+    dec.attend(c.kv, c.q)
+    _err_clear()
+    assert dec.sel_count.cpu().tolist() == [[128, 128]]
+    out = dec.out.cpu().numpy()
+    for kvh in range(2):
+        K, V = c.logical(0, kvh, "k"), c.logical(0, kvh, "v")
+        q = torch.from_numpy(c.q_group(0, kvh))[None, :, None, :]
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            q, torch.from_numpy(K)[None, None].expand(1, 4, -1, -1),
+            torch.from_numpy(V)[None, None].expand(1, 4, -1, -1), scale=1 / 8.0)[0, :, 0].numpy()
+        assert np.abs(out[0, kvh * 4:(kvh + 1) * 4] - ref).max() <= 1e-5
+
+
+def test_zero_query_selects_lowest_blocks_and_averages_v():
+    from _parity import Case
+    w = WORKLOADS["llama8b_bf16"].scaled(batch=1, ctx_min=2048, ctx_max=2048, k_scored=3)
+    x = make_inputs(w)
+    x["q"] = torch.zeros_like(x["q"])
+    c = Case(w, x)
+    dec = c.decoder(out_is_fp32=True)
+    dec.build_summaries(c.kv)
+    dec.select(c.kv, c.q)
+    dec.attend(c.kv, c.q)
+    _err_clear()
+    for kvh in range(4):
+        n = int(dec.sel_count[0, kvh])
+        assert dec.sel[0, kvh, :n].tolist() == [0, 1, 2, 3, 28, 29, 30, 31]
+        V = c.logical(0, kvh, "v")
+        toks = O.selected_tokens([0, 1, 2, 3, 28, 29, 30, 31], 2048, 64)
+        mean = V[toks].mean(0)
+        assert np.abs(dec.out[0, kvh * 8].cpu().numpy() - mean).max() <= 2e-3
+
+
+def test_ties_break_to_lower_index_exactly():
+    """Integer-valued summaries and queries make every score exact in fp32, so
+    the selection with many exact ties must equal the oracle's bit for bit."""
+    from query_aware_sparse_hs_gb300.decode import SparseDecode
+    gen = np.random.default_rng(7)
+    batch, hkv, g, D, B, L = 3, 2, 4, 64, 16, 16 * 300
+    nb = L // B
+    dec = SparseDecode(num_q_heads=hkv * g, num_kv_heads=hkv, head_dim=D, block_size=B, kv_dtype="bf16",
+                       batch=batch, max_blocks=nb, sink_tokens=16, window_tokens=32, k_scored=37)
+    smin = gen.integers(-2, 1, (batch, hkv, nb, D)).astype(np.float32)
+    smax = smin + gen.integers(0, 2, (batch, hkv, nb, D)).astype(np.float32)
+    q = gen.integers(-1, 2, (batch, hkv * g, D)).astype(np.float32)
+    dec.smin.copy_(torch.from_numpy(smin).to(torch.bfloat16))
+    dec.smax.copy_(torch.from_numpy(smax).to(torch.bfloat16))
+    qd = torch.from_numpy(q).to(torch.bfloat16).cuda()
+    lens = torch.full((batch,), L, dtype=torch.int32, device="cuda")
+    table = torch.zeros((batch, hkv, nb), dtype=torch.int32, device="cuda")
+    dummy = torch.zeros((1, B, D), dtype=torch.bfloat16, device="cuda")
+    from query_aware_sparse_hs_gb300 import hs
+    kv = hs.paged_kv(dummy, dummy, table, lens)
+    dec.select(kv, qd, keep_scores=True)
+    _err_clear()
+    for b in range(batch):
+        for kvh in range(hkv):
+            _, score = O.bound_scores(q[b, kvh * g:(kvh + 1) * g].astype(np.float64), smin[b, kvh], smax[b, kvh])
+            assert np.array_equal(dec.scores[b, kvh].cpu().numpy(), score.astype(np.float32))
+            F = O.forced_blocks(L, B, 16, 32)
+            want = O.select_blocks(score, F, 37)
+            n = int(dec.sel_count[b, kvh])
+            assert dec.sel[b, kvh, :n].tolist() == want
+
+
+def test_empty_and_tiny_requests():
+    from _parity import Case
+    w = WORKLOADS["ragged_bf16"].scaled(batch=4, ctx_min=1, ctx_max=40, k_scored=2)
+    x = make_inputs(w)
+    x["seq_lens"] = torch.tensor([0, 1, 17, 40], dtype=torch.int32)
+    c = Case(w, x)
+    dec = c.decoder(out_is_fp32=True)
+    dec.build_summaries(c.kv)
+    dec.select(c.kv, c.q)
+    dec.attend(c.kv, c.q)
+    _err_clear()
+    cnt = dec.sel_count.cpu().numpy()
+    assert np.all(cnt[0] == 0) and np.all(cnt[1] == 1)
+    out, lse = dec.out.cpu().numpy(), dec.lse.cpu().numpy()
+    assert np.all(out[0] == 0) and np.all(np.isneginf(lse[0]))
+    for b in (1, 2, 3):
+        for kvh in range(w.num_kv_heads):
+            r = c.oracle_pair(b, kvh)
+            g = w.group
+            assert np.abs(out[b, kvh * g:(kvh + 1) * g] - r["out"]).max() <= 2e-3
+
+
+def test_quantize_bit_exact():
+    from query_aware_sparse_hs_gb300 import hs
+    gen = np.random.default_rng(3)
+    for D in (64, 128):
+        x = (gen.standard_normal((999, D)) * np.exp2(gen.integers(-20, 20, (999, 1)))).astype(np.float32)
+        x[5] = 0.0
+        x[6, :32] = 1e-30
+        x[7, 3] = 3e38
+        for src in (torch.from_numpy(x), torch.from_numpy(x).to(torch.bfloat16)):
+            xs = src.float().numpy()
+            codes = torch.empty((999, D), dtype=torch.uint8, device="cuda")
+            scales = torch.empty((999, D // 32), dtype=torch.float32, device="cuda")
+            hs.hs_quantize_e4m3_g32(src.cuda().contiguous(), codes, scales)
+            rc, rs = O.quantize_e4m3_g32(xs)
+            assert np.array_equal(scales.cpu().numpy(), rs)
+            assert np.array_equal(codes.cpu().numpy(), rc)
