@@ -237,6 +237,7 @@ hs_status hs_sparse_paged_decode_attn(const hs_attn_shape* shape, const hs_paged
   split_geometry(shape, kv->batch, capacity, params, d.sms, &a.blocks_per_split, &a.splits);
   const size_t need = workspace_for(shape, kv->batch, a.splits);
   if (need > 0 && (!workspace || ws_bytes < need || !aligned(workspace, 16))) return HS_ERR_WORKSPACE;
+  a.sms = d.sms;
   a.q = q;
   a.sel = sel;
   a.sel_count = sel_count;

@@ -29,6 +29,7 @@ struct AttnArgs {
   float* ws_lse;  // [batch][hq][splits]
   int32_t blocks_per_split;
   int32_t splits;
+  int32_t sms;  // multiprocessors of the current device (persistent grid size)
 };
 
 struct HotView {

@@ -1,12 +1,515 @@
-// Tensor-core (tcgen05) gather-attention: not built yet.
+// Tensor-core gather-attention over the selected blocks (bf16 K/V, head_dim
+// 128): "KV 稀疏化" wiki §5 (full attention on the chosen blocks only) with the
+// tiled running-max / normaliser softmax of "分块稀疏注意力与KV Cache量化" §2.2.
+//
+// The g query heads that share a kv head make the decode step a real small GEMM
+// per 128-token chunk:
+//   S^T[128 tok x 16]   = K[128 tok x 128 d] . Qpad^T[128 d x 16]     (tcgen05, M=128 N=16)
+//   O^T[128 d x 2*NH]   = V^T[128 d x 128 tok] . [P_hi | P_lo][128 tok x 2*NH]
+// P is split into a bf16 high part and a bf16 remainder so the probabilities
+// keep ~16 significant bits through the bf16 MMA; both accumulate in fp32 TMEM.
+//
+// Persistent, warp-specialised CTA (one per SM):
+//   warp 4      TMA producer: cp.async.bulk.tensor of each selected page's K
+//               and V rows (two 64-channel halves, 128-byte swizzle) into a
+//               3-stage ring, completion tracked by mbarrier transaction bytes.
+//   warp 5      MMA issuer (one thread): GEMM1 of chunk c+1 is issued before
+//               GEMM2 of chunk c; TMEM double-buffers S and O.
+//   warps 0-3   softmax / correction: thread t owns TMEM lane t = token t of
+//               the chunk for S, and channel t for O; running max and sum per
+//               head, P written to shared memory for GEMM2, O accumulated in
+//               registers with the online-softmax rescale.
+// Every wait is bounded (2 s); on a time-out the CTA sets HS_EBIT_TIMEOUT,
+// stops all roles, lets in-flight copies land and frees its TMEM.
+#include <cuda.h>
+
 #include "hs_internal.h"
+#include "tc_ptx.cuh"
 
 namespace hs {
+namespace {
 
-bool attn_tc_supported(const KvView&) { return false; }
+using namespace tc;
 
-cudaError_t launch_attn_tc(const KvView&, const AttnArgs&, unsigned*, cudaStream_t) {
-  return cudaErrorNotSupported;
+constexpr int kD = 128;
+constexpr int kChunk = 128;
+constexpr int kStages = 3;
+constexpr int kThreads = 192;
+constexpr int kProducerWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr int kHalfBytes = kChunk * 128;   // 128 rows x 64 bf16
+constexpr int kTileBytes = 2 * kHalfBytes;  // one K or V chunk
+constexpr int kStageBytes = 2 * kTileBytes;
+constexpr int kQHalfBytes = 16 * 128;       // 16 (padded) head rows x 64 bf16
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+struct TcArgs {
+  const int32_t* sel;
+  const int32_t* sel_count;
+  const int32_t* page_table;
+  const int32_t* seq_lens;
+  const __nv_bfloat16* q;
+  float* ws_o;
+  float* ws_lse;
+  int64_t num_pages;
+  int hkv, hq, group, block, max_blocks, capacity, bps, splits, items;
+  float scale_log2;
+};
+
+template <int NH>
+struct Layout {
+  static constexpr int kPBytes = kChunk * 2 * NH * 2;
+  static constexpr int kOffQ = kStages * kStageBytes;
+  static constexpr int kOffP = kOffQ + 2 * kQHalfBytes;
+  static constexpr int kOffBar = kOffP + 2 * kPBytes;
+  static constexpr int kNumBars = 2 * kStages + 11;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kOffRed = kOffMisc + 16;
+  static constexpr int kBytes = kOffRed + 4 * NH * 4;
+  // the whole per-block maximum: one CTA per SM, and operand reads through a
+  // descriptor can never leave this CTA's own shared memory
+  static constexpr int kAlloc = 232448;
+  static_assert(kBytes + 1024 <= kAlloc, "shared memory layout too large");
+  static constexpr int kTmemCols = NH == 8 ? 64 : 128;
+  static constexpr int kColO = 32;  // S uses columns [0, 32)
+};
+
+struct Item {
+  int pair, split, b, kvh, s0, s1, nch, L, nb;
+};
+
+__device__ __forceinline__ Item item_geom(const TcArgs& a, int item, int bpc) {
+  Item it;
+  it.pair = item / a.splits;
+  it.split = item - it.pair * a.splits;
+  it.b = it.pair / a.hkv;
+  it.kvh = it.pair - it.b * a.hkv;
+  int cnt = a.sel_count[it.pair];
+  cnt = max(0, min(cnt, a.capacity));
+  it.s0 = it.split * a.bps;
+  it.s1 = min(cnt, it.s0 + a.bps);
+  const int nblk = it.s1 - it.s0;
+  it.nch = nblk > 0 ? (nblk + bpc - 1) / bpc : 0;
+  it.L = a.seq_lens[it.b];
+  it.nb = min((max(it.L, 0) + a.block - 1) / a.block, a.max_blocks);
+  return it;
+}
+
+// physical page of selected position `pos` of the item, or -1; *vt = valid tokens
+__device__ __forceinline__ int resolve(const TcArgs& a, const Item& it, int pos, int* vt, unsigned* bad) {
+  if (pos >= it.s1) return -1;
+  const int j = a.sel[static_cast<int64_t>(it.pair) * a.capacity + pos];
+  if (j < 0 || j >= it.nb) {
+    *bad |= HS_EBIT_BLOCK_RANGE;
+    return -1;
+  }
+  const int page = a.page_table[static_cast<int64_t>(it.pair) * a.max_blocks + j];
+  if (page < 0 || page >= a.num_pages) {
+    *bad |= HS_EBIT_PAGE_RANGE;
+    return -1;
+  }
+  *vt = min(a.block, it.L - j * a.block);
+  return page;
+}
+
+template <int NH>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                   TcArgs a, unsigned* err) {
+  using Ly = Layout<NH>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + Ly::kOffBar;
+  auto full_bar = [&](int s) { return bar0 + 8 * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8 * (kStages + s); };
+  auto s_full = [&](int b) { return bar0 + 8 * (2 * kStages + b); };
+  auto s_free = [&](int b) { return bar0 + 8 * (2 * kStages + 2 + b); };
+  auto p_full = [&](int b) { return bar0 + 8 * (2 * kStages + 4 + b); };
+  auto o_full = [&](int b) { return bar0 + 8 * (2 * kStages + 6 + b); };
+  auto o_free = [&](int b) { return bar0 + 8 * (2 * kStages + 8 + b); };
+  const uint32_t q_full = bar0 + 8 * (2 * kStages + 10);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Ly::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Ly::kOffMisc + 4);
+  float* red = reinterpret_cast<float*>(smem + Ly::kOffRed);  // [4 warps][NH]
+  auto k_half = [&](int s, int h) { return sbase + s * kStageBytes + h * kHalfBytes; };
+  auto v_half = [&](int s, int h) { return sbase + s * kStageBytes + kTileBytes + h * kHalfBytes; };
+  auto q_half = [&](int h) { return sbase + Ly::kOffQ + h * kQHalfBytes; };
+  auto p_buf = [&](int b) { return sbase + Ly::kOffP + b * Ly::kPBytes; };
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int B = a.block;
+  const int bpc = kChunk / B;
+
+  // ---- set-up: barriers, zeroed operand buffers, TMEM ----
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(s_full(b), 1);
+      mbar_init(s_free(b), 128);
+      mbar_init(p_full(b), 128);
+      mbar_init(o_full(b), 1);
+      mbar_init(o_free(b), 128);
+    }
+    mbar_init(q_full, 128);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  {
+    uint4 z = make_uint4(0, 0, 0, 0);
+    uint4* p = reinterpret_cast<uint4*>(smem);
+    for (int i = tid; i < Ly::kOffBar / 16; i += kThreads) p[i] = z;
+  }
+  fence_async_smem();
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), Ly::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kProducerWarp) {
+    // ================= TMA producer =================
+    if (lane == 0) {
+      unsigned bad = 0;
+      int c = 0;
+      for (int item = blockIdx.x; item < a.items && !*abort_flag; item += gridDim.x) {
+        const Item it = item_geom(a, item, bpc);
+        for (int ci = 0; ci < it.nch; ++ci, ++c) {
+          const int s = c % kStages;
+          if (c >= kStages && !mbar_wait(empty_bar(s), ((c / kStages) + 1) & 1, abort_flag)) goto producer_done;
+          uint32_t tx = 0;
+          for (int bi = 0; bi < bpc; ++bi) {
+            int vt;
+            if (resolve(a, it, it.s0 + ci * bpc + bi, &vt, &bad) >= 0) tx += 4u * B * 128u;
+          }
+          mbar_arrive_tx(full_bar(s), tx);
+          unsigned dummy = 0;
+          for (int bi = 0; bi < bpc; ++bi) {
+            int vt;
+            const int page = resolve(a, it, it.s0 + ci * bpc + bi, &vt, &dummy);
+            if (page < 0) continue;
+            const uint32_t row_off = bi * B * 128;
+            const int y = page * B;
+            tma_load_2d(k_half(s, 0) + row_off, &tm_k, 0, y, full_bar(s));
+            tma_load_2d(k_half(s, 1) + row_off, &tm_k, 64, y, full_bar(s));
+            tma_load_2d(v_half(s, 0) + row_off, &tm_v, 0, y, full_bar(s));
+            tma_load_2d(v_half(s, 1) + row_off, &tm_v, 64, y, full_bar(s));
+          }
+        }
+      }
+    producer_done:
+      if (bad) set_error(err, bad);
+      // let every copy this CTA issued land before the CTA can exit
+      for (int s = 0; s < kStages && s < c; ++s) {
+        const int last = c - 1 - ((c - 1 - s) % kStages);
+        mbar_wait(full_bar(s), (last / kStages) & 1, abort_flag, 500000000ull);
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ================= MMA issuer =================
+    if (lane == 0) {
+      constexpr uint32_t idesc1 = idesc_bf16(128, 16, false, false);
+      constexpr uint32_t idesc2 = idesc_bf16(128, 2 * NH, true, true);
+      constexpr uint32_t kPLbo = 8 * 2 * NH * 2;  // bytes between 8-token groups of P
+      int c = 0, qi = 0;
+      auto gemm1 = [&](int cc) -> bool {
+        const int s = cc % kStages, bb = cc & 1;
+        if (!mbar_wait(full_bar(s), (cc / kStages) & 1, abort_flag)) return false;
+        if (cc >= 2 && !mbar_wait(s_free(bb), ((cc >> 1) + 1) & 1, abort_flag)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < kD / 16; ++k) {
+          const int h = k >> 2, kk = k & 3;
+          const uint64_t ad = smem_desc(k_half(s, h) + kk * 32, 16, 1024, 2);
+          const uint64_t bd = smem_desc(q_half(h) + kk * 32, 16, 1024, 2);
+          mma_f16(tmem + bb * 16, ad, bd, idesc1, k > 0 ? 1u : 0u);
+        }
+        mma_commit(s_full(bb));
+        return true;
+      };
+      auto gemm2 = [&](int cc) -> bool {
+        const int s = cc % kStages, bb = cc & 1;
+        if (!mbar_wait(p_full(bb), (cc >> 1) & 1, abort_flag)) return false;
+        if (cc >= 2 && !mbar_wait(o_free(bb), ((cc >> 1) + 1) & 1, abort_flag)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < kChunk / 16; ++k) {
+          const uint64_t ad = smem_desc(v_half(s, 0) + k * 2048, kHalfBytes, 1024, 2);
+          const uint64_t bd = smem_desc(p_buf(bb) + k * 2 * kPLbo, kPLbo, 128, 0);
+          mma_f16(tmem + Ly::kColO + bb * 2 * NH, ad, bd, idesc2, k > 0 ? 1u : 0u);
+        }
+        mma_commit(o_full(bb));
+        mma_commit(empty_bar(s));
+        return true;
+      };
+      for (int item = blockIdx.x; item < a.items && !*abort_flag; item += gridDim.x) {
+        const Item it = item_geom(a, item, bpc);
+        if (it.nch == 0) continue;
+        if (!mbar_wait(q_full, qi & 1, abort_flag)) break;
+        ++qi;
+        tc_fence_after();
+        if (!gemm1(c)) break;
+        bool ok = true;
+        for (int ci = 0; ci < it.nch && ok; ++ci, ++c) {
+          if (ci + 1 < it.nch) ok = gemm1(c + 1);
+          if (ok) ok = gemm2(c);
+        }
+        if (!ok) break;
+      }
+      // every commit has landed before TMEM is released
+      for (int s = 0; s < kStages && s < c; ++s) {
+        const int last = c - 1 - ((c - 1 - s) % kStages);
+        mbar_wait(empty_bar(s), (last / kStages) & 1, abort_flag, 500000000ull);
+      }
+    }
+  } else {
+    // ================= softmax / correction (warps 0-3) =================
+    const int t = tid;  // token row of S, channel of O
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const int g = a.group;
+    int c = 0;
+    for (int item = blockIdx.x; item < a.items && !*abort_flag; item += gridDim.x) {
+      const Item it = item_geom(a, item, bpc);
+      const int64_t row0 = (static_cast<int64_t>(it.b) * a.hq + it.kvh * g) * a.splits + it.split;
+      if (it.nch == 0) {
+        for (int h = 0; h < g; ++h) {
+          a.ws_o[(row0 + static_cast<int64_t>(h) * a.splits) * kD + t] = 0.0f;
+          if (t == 0) a.ws_lse[row0 + static_cast<int64_t>(h) * a.splits] = -INFINITY;
+        }
+        continue;
+      }
+      // Q operand of this kv head: 16 rows (heads, zero past g) x 128 channels, 128-byte swizzle
+      {
+        const int n = t >> 3, ch = t & 7;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint4 v = make_uint4(0, 0, 0, 0);
+          if (n < g)
+            v = *reinterpret_cast<const uint4*>(a.q + (static_cast<int64_t>(it.b) * a.hq + it.kvh * g + n) * kD +
+                                                h * 64 + ch * 8);
+          *reinterpret_cast<uint4*>(smem + Ly::kOffQ + h * kQHalfBytes + n * 128 + ((ch ^ (n & 7)) << 4)) = v;
+        }
+      }
+      fence_async_smem();
+      mbar_arrive(q_full);
+
+      float m[NH], lsum[NH], oacc[NH], alpha_prev[NH];
+#pragma unroll
+      for (int h = 0; h < NH; ++h) {
+        m[h] = -INFINITY;
+        lsum[h] = 0.0f;
+        oacc[h] = 0.0f;
+        alpha_prev[h] = 1.0f;
+      }
+      bool ok = true;
+      auto take_o = [&](int cc) -> bool {
+        const int bb = cc & 1;
+        if (!mbar_wait(o_full(bb), (cc >> 1) & 1, abort_flag)) return false;
+        tc_fence_after();
+        float ov[2 * NH];
+        if constexpr (NH == 8) {
+          tmem_ld16(tmem + lane_base + Ly::kColO + bb * 16, *reinterpret_cast<float(*)[16]>(ov));
+        } else {
+          tmem_ld16(tmem + lane_base + Ly::kColO + bb * 32, *reinterpret_cast<float(*)[16]>(ov));
+          tmem_ld16(tmem + lane_base + Ly::kColO + bb * 32 + 16, *reinterpret_cast<float(*)[16]>(ov + 16));
+        }
+        tc_fence_before();
+        mbar_arrive(o_free(bb));
+#pragma unroll
+        for (int h = 0; h < NH; ++h) oacc[h] = fmaf(oacc[h], alpha_prev[h], ov[h] + ov[NH + h]);
+        return true;
+      };
+      for (int ci = 0; ci < it.nch && ok; ++ci, ++c) {
+        const int bb = c & 1, s = c % kStages;
+        const int bi = t / B, tok = t - bi * B;
+        unsigned dummy = 0;
+        int vt = 0;
+        const int page = resolve(a, it, it.s0 + ci * bpc + bi, &vt, &dummy);
+        const bool loaded = page >= 0;
+        const bool valid = loaded && tok < vt;
+        if (!mbar_wait(s_full(bb), (c >> 1) & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        float sv[16];
+        tmem_ld16(tmem + lane_base + bb * 16, sv);
+        tc_fence_before();
+        mbar_arrive(s_free(bb));
+        float x[NH];
+#pragma unroll
+        for (int h = 0; h < NH; ++h) x[h] = (valid && h < g) ? sv[h] * a.scale_log2 : -INFINITY;
+        // chunk max per head over the 128 rows
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {
+          const float mx = warp_max(x[h]);
+          if (lane == 0) red[warp * NH + h] = mx;
+        }
+        named_barrier(1, 128);
+        float alpha[NH];
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {
+          const float cm = fmaxf(fmaxf(red[h], red[NH + h]), fmaxf(red[2 * NH + h], red[3 * NH + h]));
+          const float mn = fmaxf(m[h], cm);
+          alpha[h] = (mn == -INFINITY) ? 1.0f : exp2f(m[h] - mn);
+          m[h] = mn;
+        }
+        named_barrier(1, 128);
+        // probabilities, split into bf16 high part + bf16 remainder
+        uint32_t hi2[NH / 2], lo2[NH / 2];
+#pragma unroll
+        for (int h = 0; h < NH; h += 2) {
+          float p0 = x[h] == -INFINITY ? 0.0f : exp2f(x[h] - m[h]);
+          float p1 = x[h + 1] == -INFINITY ? 0.0f : exp2f(x[h + 1] - m[h + 1]);
+          lsum[h] = fmaf(lsum[h], alpha[h], p0);
+          lsum[h + 1] = fmaf(lsum[h + 1], alpha[h + 1], p1);
+          const __nv_bfloat162 hi = __floats2bfloat162_rn(p0, p1);
+          const float2 hf = __bfloat1622float2(hi);
+          const __nv_bfloat162 lo = __floats2bfloat162_rn(p0 - hf.x, p1 - hf.y);
+          hi2[h / 2] = *reinterpret_cast<const uint32_t*>(&hi);
+          lo2[h / 2] = *reinterpret_cast<const uint32_t*>(&lo);
+        }
+        {
+          constexpr int kPLbo = 8 * 2 * NH * 2;
+          uint8_t* prow = smem + Ly::kOffP + bb * Ly::kPBytes + (t >> 3) * kPLbo + (t & 7) * 16;
+#pragma unroll
+          for (int gi = 0; gi < NH / 8; ++gi) {
+            *reinterpret_cast<uint4*>(prow + gi * 128) =
+                make_uint4(hi2[gi * 4], hi2[gi * 4 + 1], hi2[gi * 4 + 2], hi2[gi * 4 + 3]);
+            *reinterpret_cast<uint4*>(prow + (NH / 8 + gi) * 128) =
+                make_uint4(lo2[gi * 4], lo2[gi * 4 + 1], lo2[gi * 4 + 2], lo2[gi * 4 + 3]);
+          }
+        }
+        if (loaded && !valid) {
+          // rows past the request's end inside its last page: zero V so they
+          // contribute exactly nothing (P is 0 there, the stored bytes may not be finite)
+          if (!mbar_wait(full_bar(s), (c / kStages) & 1, abort_flag)) { ok = false; break; }
+          uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint4* row = reinterpret_cast<uint4*>(smem + s * kStageBytes + kTileBytes + h * kHalfBytes + t * 128);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) row[i] = z;
+          }
+        }
+        fence_async_smem();
+        mbar_arrive(p_full(bb));
+        if (ci > 0 && !take_o(c - 1)) { ok = false; break; }
+#pragma unroll
+        for (int h = 0; h < NH; ++h) alpha_prev[h] = alpha[h];
+      }
+      if (!ok || !take_o(c - 1)) break;
+      // total normaliser per head
+#pragma unroll
+      for (int h = 0; h < NH; ++h) {
+        const float s_ = warp_sum(lsum[h]);
+        if (lane == 0) red[warp * NH + h] = s_;
+      }
+      named_barrier(1, 128);
+      for (int h = 0; h < g && h < NH; ++h) {
+        const float lt = red[h] + red[NH + h] + red[2 * NH + h] + red[3 * NH + h];
+        const int64_t row = row0 + static_cast<int64_t>(h) * a.splits;
+        a.ws_o[row * kD + t] = lt > 0.0f ? oacc[h] / lt : 0.0f;
+        if (t == 0) a.ws_lse[row] = lt > 0.0f ? (m[h] + log2f(lt)) * kLn2 : -INFINITY;
+      }
+      named_barrier(1, 128);
+    }
+  }
+
+  // ---- tear-down ----
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag && tid == 0) set_error(err, HS_EBIT_TIMEOUT);
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, Ly::kTmemCols);
+  }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// 2-D view of a page pool [num_pages*B rows][128 channels] bf16; box = one
+// page of rows x 64 channels (128 bytes), 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, int64_t rows, int block) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kD) * 2};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(block)};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int NH>
+cudaError_t launch_nh(const KvView& kv, const AttnArgs& aa, unsigned* err, cudaStream_t st) {
+  using Ly = Layout<NH>;
+  CUtensorMap mk, mv;
+  const int64_t rows = kv.num_pages * kv.block;
+  if (rows <= 0) return cudaErrorInvalidValue;
+  if (!make_map(&mk, kv.k_pages, rows, kv.block) || !make_map(&mv, kv.v_pages, rows, kv.block))
+    return cudaErrorInvalidValue;
+  TcArgs a;
+  a.sel = aa.sel;
+  a.sel_count = aa.sel_count;
+  a.page_table = kv.page_table;
+  a.seq_lens = kv.seq_lens;
+  a.q = static_cast<const __nv_bfloat16*>(aa.q);
+  a.ws_o = aa.ws_o;
+  a.ws_lse = aa.ws_lse;
+  a.num_pages = kv.num_pages;
+  a.hkv = kv.hkv;
+  a.hq = kv.hq;
+  a.group = kv.group;
+  a.block = kv.block;
+  a.max_blocks = kv.max_blocks;
+  a.capacity = aa.capacity;
+  a.bps = aa.blocks_per_split;
+  a.splits = aa.splits;
+  a.items = kv.batch * kv.hkv * aa.splits;
+  a.scale_log2 = aa.scale * kLog2e;
+  if (a.items == 0) return cudaSuccess;
+  auto kern = attn_tc_kernel<NH>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::kAlloc);
+  if (e != cudaSuccess) return e;
+  const int grid = a.items < aa.sms ? a.items : aa.sms;
+  kern<<<grid, kThreads, Ly::kAlloc, st>>>(mk, mv, a, err);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool attn_tc_supported(const KvView& kv) {
+  if (kv.kv_dtype != HS_KV_BF16 || kv.head_dim != kD) return false;
+  if (kv.block != 16 && kv.block != 32 && kv.block != 64 && kv.block != 128) return false;
+  if (kv.group > 16) return false;
+  if (kv.num_pages * kv.block >= (int64_t(1) << 31)) return false;
+  return encode_fn() != nullptr;
+}
+
+cudaError_t launch_attn_tc(const KvView& kv, const AttnArgs& a, unsigned* err, cudaStream_t st) {
+  return kv.group <= 8 ? launch_nh<8>(kv, a, err, st) : launch_nh<16>(kv, a, err, st);
 }
 
 }  // namespace hs
