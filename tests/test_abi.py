@@ -72,3 +72,12 @@ def test_workspace_size_formula():
     p = hs.attn_params(0.1, blocks_per_split=4)
     # 9 splits of 4 blocks cover 33; (D + 1) floats per (request, q head, split)
     assert hs.hs_workspace_bytes(shape, 8, 33, p) == ((8 * 32 * 9 * 129 * 4 + 255) // 256) * 256
+
+
+def test_kv_bytes_per_token_of_an_8b_gqa_model():
+    """64 KB per token and 2 GiB at 32K context for 32 layers x 4 kv heads x 128 x fp16
+    (SparDA article, §1.1) from the bench's layout arithmetic."""
+    import bench
+    assert bench.kv_bytes_per_token(32, 4, 128, 2) == 65536
+    assert bench.kv_bytes_per_token(32, 4, 128, 2) * 32768 == 2 * 1024 ** 3
+    assert bench.kv_bytes_per_token(32, 4, 128, 2) * 131072 == 8 * 1024 ** 3
