@@ -76,7 +76,8 @@ typedef enum hs_status {
   HS_ERR_OUT_OF_RANGE = 4, /* device: page id or block index outside its range */
   HS_ERR_CAPACITY = 5,     /* device: selection larger than capacity / hot slots */
   HS_ERR_TIMEOUT = 6,      /* device: a bounded wait gave up */
-  HS_ERR_WORKSPACE = 7     /* workspace missing or smaller than hs_workspace_bytes */
+  HS_ERR_WORKSPACE = 7,    /* workspace missing or smaller than hs_workspace_bytes */
+  HS_ERR_SCRATCH_LIMIT = 8 /* needs more than the fixed scratch of the _noalloc call */
 } hs_status;
 
 /* Bits of the per-device error word. */
@@ -252,6 +253,32 @@ HS_API hs_status hs_swapin_misses(const hs_attn_shape* shape, const hs_hot_buffe
 HS_API hs_status hs_quantize_e4m3_g32(const void* src, int32_t src_is_fp32, int64_t rows,
                                int32_t head_dim, uint8_t* codes, float* scales,
                                hs_stream_t stream);
+
+/* Same computation, arguments and results as hs_sparse_paged_decode_attn, for
+ * callers that cannot allocate device memory.  (The pages have no counterpart
+ * of this call; it exists for integration.)  Some hosts hand an operator only
+ * its input and output buffers and keep the device allocator to themselves -
+ * plugin and custom-operator interfaces of serving engines that plan all
+ * memory ahead, or C programs that load this library without any allocator -
+ * so they cannot provide the split-K workspace.  This variant keeps that
+ * workspace in a fixed array of HS_NOALLOC_SCRATCH_BYTES inside the library:
+ * every GPU that loads the library holds it until the process exits.
+ *   - Calls whose workspace (hs_workspace_bytes for the same arguments) is
+ *     larger are refused with HS_ERR_SCRATCH_LIMIT before anything runs.
+ *   - The first call on a device looks up the array's device address (a
+ *     cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - No cudaMalloc, cudaFree or other allocating routine is ever called.
+ *   - All calls on a device share the one array and it keeps the last call's
+ *     contents; the kernels overwrite every entry they read, so nothing needs
+ *     clearing, but two calls that overlap on the GPU (different streams
+ *     without ordering) race on it and give wrong results. */
+#define HS_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u)
+HS_API hs_status hs_sparse_paged_decode_attn_noalloc(const hs_attn_shape* shape, const hs_paged_kv* kv,
+                                                     const void* q, const int32_t* sel,
+                                                     const int32_t* sel_count, int32_t capacity,
+                                                     const hs_attn_params* params, void* out,
+                                                     float* lse_opt, hs_stream_t stream);
 
 /* Synchronises `stream`, then reads and clears the current device's error
  * word.  Returns HS_OK when no bit was set, else, in this order of priority:

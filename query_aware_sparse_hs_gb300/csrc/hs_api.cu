@@ -139,6 +139,7 @@ const char* hs_status_string(hs_status s) {
     case HS_ERR_CAPACITY: return "selection larger than capacity";
     case HS_ERR_TIMEOUT: return "device wait timed out";
     case HS_ERR_WORKSPACE: return "workspace too small";
+    case HS_ERR_SCRATCH_LIMIT: return "needs more than the fixed scratch of the no-allocation call";
   }
   return "unknown status";
 }
@@ -352,3 +353,53 @@ hs_status hs_get_device_error(hs_stream_t stream, uint32_t* bits_opt) {
 }
 
 }  // extern "C"
+
+// ---- attention without caller-provided workspace ----------------------------
+// For hosts that cannot allocate device memory: the split-K workspace lives in
+// this fixed device array instead.  Host code must not use the array's name as
+// a pointer (it is only a host-side stand-in); its device address is looked up
+// once per device with cudaGetSymbolAddress and passed to the kernels.
+namespace hs {
+namespace {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[HS_NOALLOC_SCRATCH_BYTES];
+void* g_scratch_ptr[kMaxDevices];
+std::mutex g_scratch_mu;
+
+hs_status scratch_address(int dev, void** out) {
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+      cudaGetLastError();
+      return HS_ERR_CUDA;
+    }
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return HS_OK;
+}
+
+}  // namespace
+}  // namespace hs
+
+extern "C" hs_status hs_sparse_paged_decode_attn_noalloc(const hs_attn_shape* shape, const hs_paged_kv* kv,
+                                                         const void* q, const int32_t* sel,
+                                                         const int32_t* sel_count, int32_t capacity,
+                                                         const hs_attn_params* params, void* out,
+                                                         float* lse_opt, hs_stream_t stream) {
+  hs_status st = check_shape(shape);
+  if (st != HS_OK) return st;
+  if (!kv || !params || capacity < 1 || kv->batch < 0) return HS_ERR_INVALID_ARG;
+  if (params->blocks_per_split < 0) return HS_ERR_INVALID_ARG;
+  Device d;
+  if ((st = current_device(&d)) != HS_OK) return st;
+  int bps = 0, splits = 0;
+  split_geometry(shape, kv->batch, capacity, params, d.sms, &bps, &splits);
+  const size_t need = workspace_for(shape, kv->batch, splits);
+  if (need > HS_NOALLOC_SCRATCH_BYTES) return HS_ERR_SCRATCH_LIMIT;
+  void* scratch = nullptr;
+  if ((st = scratch_address(d.id, &scratch)) != HS_OK) return st;
+  return hs_sparse_paged_decode_attn(shape, kv, q, sel, sel_count, capacity, params, out, lse_opt, scratch,
+                                     HS_NOALLOC_SCRATCH_BYTES, stream);
+}

@@ -19,6 +19,8 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "lib
 
 HS_OK, HS_ERR_INVALID_ARG, HS_ERR_UNSUPPORTED, HS_ERR_CUDA = 0, 1, 2, 3
 HS_ERR_OUT_OF_RANGE, HS_ERR_CAPACITY, HS_ERR_TIMEOUT, HS_ERR_WORKSPACE = 4, 5, 6, 7
+HS_ERR_SCRATCH_LIMIT = 8
+HS_NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
 HS_EBIT_PAGE_RANGE, HS_EBIT_CAPACITY, HS_EBIT_TIMEOUT, HS_EBIT_BLOCK_RANGE = 0x1, 0x2, 0x4, 0x8
 KV_DTYPES = {"f32": 0, "bf16": 1, "fp8": 2}
 ALGO = {"auto": 0, "simt": 1, "tcgen05": 2}
@@ -76,6 +78,9 @@ SYMBOLS = {
     "hs_sparse_paged_decode_attn": (c_int32, [POINTER(AttnShape), POINTER(PagedKV), c_void_p, c_void_p,
                                               c_void_p, c_int32, POINTER(AttnParams), c_void_p, c_void_p,
                                               c_void_p, c_size_t, c_void_p]),
+    "hs_sparse_paged_decode_attn_noalloc": (c_int32, [POINTER(AttnShape), POINTER(PagedKV), c_void_p,
+                                                      c_void_p, c_void_p, c_int32, POINTER(AttnParams),
+                                                      c_void_p, c_void_p, c_void_p]),
     "hs_swapin_misses": (c_int32, [POINTER(AttnShape), POINTER(HotBuffer), c_void_p, c_void_p, c_int32,
                                    c_int32, c_void_p, c_void_p]),
     "hs_quantize_e4m3_g32": (c_int32, [c_void_p, c_int32, c_int64, c_int32, c_void_p, c_void_p,
@@ -182,6 +187,17 @@ def hs_sparse_paged_decode_attn(shape, kv, q, sel, sel_count, capacity, params, 
                                             _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes,
                                             _stream(stream)),
            "hs_sparse_paged_decode_attn")
+
+
+def hs_sparse_paged_decode_attn_noalloc(shape, kv, q, sel, sel_count, capacity, params, out, lse=None,
+                                        stream=None):
+    """hs_sparse_paged_decode_attn without a workspace argument, for callers that
+    cannot allocate device memory: the library's own fixed scratch array
+    (HS_NOALLOC_SCRATCH_BYTES per GPU) holds the split partials."""
+    _check(_lib.hs_sparse_paged_decode_attn_noalloc(ctypes.byref(shape), ctypes.byref(kv), _ptr(q), _ptr(sel),
+                                                    _ptr(sel_count), int(capacity), ctypes.byref(params),
+                                                    _ptr(out), _ptr(lse), _stream(stream)),
+           "hs_sparse_paged_decode_attn_noalloc")
 
 
 def hot_buffer(page_table, slot_owner, last_used, k_slots, v_slots, host_k, host_v,
