@@ -263,8 +263,11 @@ def run_ours(args, w):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
 
-    layers = args.layers
     layout = make_layout(w, dev)
+    layers = args.layers
+    if layers <= 0:  # as many distinct layer copies as fit in ~24 GB, at most 32
+        per_layer = layout["num_pages"] * w.block_size * token_bytes(w)
+        layers = int(max(1, min(32, (24 << 30) // max(per_layer, 1))))
     lens, table = layout["seq_lens"], layout["page_table"]
     B, D = w.block_size, w.head_dim
     L_last_block = int(((lens.max().item() - 1) // B))
@@ -460,7 +463,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=640)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="llama8b_bf16")
-    ap.add_argument("--layers", type=int, default=32)
+    ap.add_argument("--layers", type=int, default=0, help="distinct layer copies (0 = fit ~24 GB, max 32)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)

@@ -44,6 +44,8 @@ template <int C, int G, int KIND>
 __global__ __launch_bounds__(kWarps * 32) void attn_simt_kernel(KvView kv, AttnArgs a,
                                                                 unsigned* err) {
   constexpr int D = C * 32;
+  pdl_trigger();
+  pdl_wait();
   const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int B = kv.block;
@@ -150,11 +152,11 @@ cudaError_t launch_g(const KvView& kv, const AttnArgs& a, unsigned* err, cudaStr
   dim3 grid(a.splits, kv.hkv, kv.batch);
   dim3 block(kWarps * 32);
   switch (kv.group) {
-    case 1: attn_simt_kernel<C, 1, KIND><<<grid, block, 0, st>>>(kv, a, err); break;
-    case 2: attn_simt_kernel<C, 2, KIND><<<grid, block, 0, st>>>(kv, a, err); break;
-    case 4: attn_simt_kernel<C, 4, KIND><<<grid, block, 0, st>>>(kv, a, err); break;
-    case 8: attn_simt_kernel<C, 8, KIND><<<grid, block, 0, st>>>(kv, a, err); break;
-    default: attn_simt_kernel<C, 16, KIND><<<grid, block, 0, st>>>(kv, a, err); break;
+    case 1: return launch_pdl(attn_simt_kernel<C, 1, KIND>, grid, block, 0, st, kv, a, err);
+    case 2: return launch_pdl(attn_simt_kernel<C, 2, KIND>, grid, block, 0, st, kv, a, err);
+    case 4: return launch_pdl(attn_simt_kernel<C, 4, KIND>, grid, block, 0, st, kv, a, err);
+    case 8: return launch_pdl(attn_simt_kernel<C, 8, KIND>, grid, block, 0, st, kv, a, err);
+    default: return launch_pdl(attn_simt_kernel<C, 16, KIND>, grid, block, 0, st, kv, a, err);
   }
   return cudaGetLastError();
 }
@@ -172,6 +174,8 @@ cudaError_t launch_c(const KvView& kv, const AttnArgs& a, unsigned* err, cudaStr
 __global__ __launch_bounds__(128) void merge_kernel(int D, int splits, const float* __restrict__ ws_o,
                                                     const float* __restrict__ ws_lse, void* out,
                                                     int out_f32, float* lse_out) {
+  pdl_trigger();
+  pdl_wait();
   const int64_t row = blockIdx.x;
   const float* lse = ws_lse + row * splits;
   float M = -INFINITY;
@@ -207,9 +211,9 @@ cudaError_t launch_attn_simt(const KvView& kv, const AttnArgs& a, unsigned* err,
 cudaError_t launch_merge(const KvView& kv, const AttnArgs& a, cudaStream_t st) {
   const int rows = kv.batch * kv.hq;
   if (rows == 0) return cudaSuccess;
-  merge_kernel<<<rows, 128, 0, st>>>(kv.head_dim, a.splits, a.ws_o, a.ws_lse, a.out, a.out_is_fp32,
-                                     a.lse);
-  return cudaGetLastError();
+  return launch_pdl(merge_kernel, dim3(rows), dim3(128), 0, st, kv.head_dim, a.splits,
+                    static_cast<const float*>(a.ws_o), static_cast<const float*>(a.ws_lse), a.out,
+                    a.out_is_fp32, a.lse);
 }
 
 }  // namespace hs

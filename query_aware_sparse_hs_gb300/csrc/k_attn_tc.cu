@@ -142,7 +142,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int B = a.block;
   const int bpc = kChunk / B;
 
-  // ---- set-up: barriers, zeroed operand buffers, TMEM ----
+  pdl_trigger();
+  // ---- set-up: barriers, zeroed operand buffers, TMEM (overlaps the previous kernel) ----
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(full_bar(s), 1);
@@ -173,6 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait();  // the selection and q of this step are complete from here on
 
   if (warp == kProducerWarp) {
     // ================= TMA producer =================
@@ -494,8 +496,7 @@ cudaError_t launch_nh(const KvView& kv, const AttnArgs& aa, unsigned* err, cudaS
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::kAlloc);
   if (e != cudaSuccess) return e;
   const int grid = a.items < aa.sms ? a.items : aa.sms;
-  kern<<<grid, kThreads, Ly::kAlloc, st>>>(mk, mv, a, err);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(kThreads), Ly::kAlloc, st, mk, mv, a, err);
 }
 
 }  // namespace

@@ -88,6 +88,8 @@ __global__ void __cluster_dims__(kSelectCluster, 1, 1) __launch_bounds__(kThread
   __shared__ int s_warp[kWarps + 1];
   __shared__ int s_pick[2];
 
+  pdl_trigger();
+  pdl_wait();
   cg::cluster_group cluster = cg::this_cluster();
   const unsigned rank = cluster.block_rank();
   const int b = blockIdx.z, kvh = blockIdx.y;
@@ -120,26 +122,68 @@ __global__ void __cluster_dims__(kSelectCluster, 1, 1) __launch_bounds__(kThread
     float* dst = cluster.map_shared_rank(s_scores, 0);
     const int per = ceil_div(nb, kSelectCluster);
     const int jb = static_cast<int>(rank) * per, je = min(nb, jb + per);
-    for (int j = jb + warp; j < je; j += kWarps) {
-      const int64_t off = (pair * kv.max_blocks + j) * D + lane * C;
-      float mx[C], mn[C];
-      load_summary<C, F32>(a.smax, off, mx);
-      load_summary<C, F32>(a.smin, off, mn);
-      float best = -INFINITY;
+    // Each warp scores kNB consecutive blocks per round: all their summaries are
+    // loaded first (memory-level parallelism), then the kNB x G partial dot
+    // products of every lane are summed across the warp by a transpose
+    // reduction (each round halves the values a lane holds), so a block costs
+    // about 8 shuffles instead of 5 per head.
+    constexpr int kNB = (64 / G) < 8 ? (64 / G) : 8;
+    constexpr int kV = kNB * G;                    // partial sums per lane
+    constexpr int kVPL = kV >= 32 ? kV / 32 : 1;   // values per lane after the reduction
+    constexpr int kLPV = kV >= 32 ? 1 : 32 / kV;   // lanes holding one value
+    constexpr int kLanesPerBlock = G * kLPV / kVPL;
+    for (int base = jb + warp * kNB; base < je; base += kWarps * kNB) {
+      float mx[kNB][C], mn[kNB][C];
 #pragma unroll
-      for (int h = 0; h < G; ++h) {
-        float acc = 0.0f;
-#pragma unroll
-        for (int c = 0; c < C; ++c) {
-          acc = fmaf(qp[h][c], mx[c], acc);
-          acc = fmaf(qn[h][c], mn[c], acc);
-        }
-        acc = warp_sum(acc);
-        best = fmaxf(best, acc);
+      for (int u = 0; u < kNB; ++u) {
+        const int j = min(base + u, je - 1);  // clamp: re-reads a valid block, result unused
+        const int64_t off = (pair * kv.max_blocks + j) * D + lane * C;
+        load_summary<C, F32>(a.smax, off, mx[u]);
+        load_summary<C, F32>(a.smin, off, mn[u]);
       }
-      if (lane == 0) {
-        dst[j] = best;
-        if (a.scores) a.scores[pair * kv.max_blocks + j] = best;
+      float v[kV];
+#pragma unroll
+      for (int u = 0; u < kNB; ++u)
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          float acc = 0.0f;
+#pragma unroll
+          for (int c = 0; c < C; ++c) {
+            acc = fmaf(qp[h][c], mx[u][c], acc);
+            acc = fmaf(qn[h][c], mn[u][c], acc);
+          }
+          v[u * G + h] = acc;
+        }
+      int cur = kV;
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) {
+        if (cur > 1) {
+          const bool upper = (lane & o) != 0;
+          const int half = cur / 2;
+#pragma unroll
+          for (int i = 0; i < kV / 2; ++i) {
+            if (i < half) {
+              const float send = upper ? v[i] : v[i + half];
+              const float keep = upper ? v[i + half] : v[i];
+              v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+            }
+          }
+          cur = half;
+        } else {
+          v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
+        }
+      }
+      // lane now holds values [first, first + kVPL) of index u*G + h
+      float best = v[0];
+#pragma unroll
+      for (int i = 1; i < kVPL; ++i) best = fmaxf(best, v[i]);
+#pragma unroll
+      for (int o = 1; o < kLanesPerBlock; o <<= 1) best = fmaxf(best, __shfl_xor_sync(0xffffffffu, best, o));
+      const int first = kV >= 32 ? lane * kVPL : lane / kLPV;
+      const int u = first / G;
+      if ((lane % kLanesPerBlock) == 0 && base + u < je) {
+        dst[base + u] = best;
+        if (a.scores) a.scores[pair * kv.max_blocks + base + u] = best;
       }
     }
   }
@@ -173,15 +217,17 @@ __global__ void __cluster_dims__(kSelectCluster, 1, 1) __launch_bounds__(kThread
         if ((key & mask) == prefix) atomicAdd(&s_hist[(key >> shift) & 255u], 1u);
       }
       __syncthreads();
-      if (tid == 0) {
-        int acc = 0, d = 255;
-        for (; d > 0; --d) {
-          const int c = static_cast<int>(s_hist[d]);
-          if (acc + c >= kk) break;
-          acc += c;
+      {
+        // thread t owns digit 255 - t: an inclusive scan from the top digit finds
+        // the bucket that holds the kk-th largest key
+        const int digit = 255 - tid;
+        const int h = static_cast<int>(s_hist[digit]);
+        int tot;
+        const int above = block_exclusive_scan(h, s_warp, tot);
+        if (above < kk && kk <= above + h) {
+          s_pick[0] = digit;
+          s_pick[1] = kk - above;
         }
-        s_pick[0] = d;
-        s_pick[1] = kk - acc;
       }
       __syncthreads();
       prefix |= static_cast<uint32_t>(s_pick[0]) << shift;
@@ -244,8 +290,7 @@ cudaError_t launch_t(const KvView& kv, const SelectArgs& a, unsigned* err, cudaS
     if (e != cudaSuccess) return e;
   }
   dim3 grid(kSelectCluster, kv.hkv, kv.batch);
-  kern<<<grid, kThreads, smem, st>>>(kv, a, err);
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, dim3(kThreads), smem, st, kv, a, err);
 }
 
 template <int C, bool F32>

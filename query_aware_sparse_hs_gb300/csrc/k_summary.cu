@@ -1,7 +1,7 @@
 // Per-block key summaries (Quest, "KV 稀疏化" wiki §5): channel-wise min and
-// max of K over each block's valid tokens.  One warp per block; each lane owns
-// D/32 consecutive channels, so every token row is one coalesced warp load.
-// HBM-bound: one pass over the K pages of the blocks asked for.
+// max of K over each block's valid tokens.  Each lane owns D/32 consecutive
+// channels, so every token row is one coalesced warp load.  HBM-bound: one pass
+// over the K pages of the blocks asked for.
 #include "hs_internal.h"
 
 namespace hs {
@@ -61,14 +61,22 @@ struct RowLoad<C, HS_KV_FP8E4M3_G32> {
 };
 
 constexpr int kWarps = 8;
+constexpr int kRowsPerRound = 8;  // rows a warp has in flight
 
+// One CTA per block: warp w takes rows w, w+8, ... with all of its rows of a
+// round loaded before any is used, so a block costs about one memory latency;
+// the 8 partial boxes are then combined in shared memory.
 template <int C, int KIND>
 __global__ __launch_bounds__(kWarps * 32) void summaries_kernel(KvView kv, int first_block,
                                                                void* smin, void* smax,
                                                                unsigned* err) {
+  constexpr int D = C * 32;
+  __shared__ float s_mn[kWarps][D], s_mx[kWarps][D];
+  pdl_trigger();
+  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = blockIdx.z, kvh = blockIdx.y;
-  const int j = first_block + blockIdx.x * kWarps + warp;
+  const int j = first_block + blockIdx.x;
   const int L = kv.seq_lens[b];
   const int B = kv.block;
   const int nb = min(ceil_div(max(L, 0), B), kv.max_blocks);
@@ -76,7 +84,7 @@ __global__ __launch_bounds__(kWarps * 32) void summaries_kernel(KvView kv, int f
   const int64_t pair = static_cast<int64_t>(b) * kv.hkv + kvh;
   const int page = kv.page_table[pair * kv.max_blocks + j];
   if (page < 0 || page >= kv.num_pages) {
-    if (lane == 0) set_error(err, HS_EBIT_PAGE_RANGE);
+    if (threadIdx.x == 0) set_error(err, HS_EBIT_PAGE_RANGE);
     return;
   }
   const int valid = min(B, L - j * B);
@@ -85,38 +93,34 @@ __global__ __launch_bounds__(kWarps * 32) void summaries_kernel(KvView kv, int f
 #pragma unroll
   for (int c = 0; c < C; ++c) { mn[c] = INFINITY; mx[c] = -INFINITY; }
   const int64_t row0 = static_cast<int64_t>(page) * B;
-  int t = 0;
-  for (; t + 4 <= valid; t += 4) {
-    float x[4][C];
+  for (int t0 = warp; t0 < valid; t0 += kWarps * kRowsPerRound) {
+    float x[kRowsPerRound][C];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) RowLoad<C, KIND>::get(kv, row0 + t + u, d0, x[u]);
+    for (int u = 0; u < kRowsPerRound; ++u) {
+      const int t = min(t0 + u * kWarps, valid - 1);  // clamp: a repeated valid row changes nothing
+      RowLoad<C, KIND>::get(kv, row0 + t, d0, x[u]);
+    }
 #pragma unroll
-    for (int u = 0; u < 4; ++u)
+    for (int u = 0; u < kRowsPerRound; ++u)
 #pragma unroll
       for (int c = 0; c < C; ++c) { mn[c] = fminf(mn[c], x[u][c]); mx[c] = fmaxf(mx[c], x[u][c]); }
   }
-  for (; t < valid; ++t) {
-    float x[C];
-    RowLoad<C, KIND>::get(kv, row0 + t, d0, x);
 #pragma unroll
-    for (int c = 0; c < C; ++c) { mn[c] = fminf(mn[c], x[c]); mx[c] = fmaxf(mx[c], x[c]); }
-  }
-  const int64_t o = (pair * kv.max_blocks + j) * kv.head_dim + d0;
-  if constexpr (KIND == HS_KV_F32) {
+  for (int c = 0; c < C; ++c) { s_mn[warp][d0 + c] = mn[c]; s_mx[warp][d0 + c] = mx[c]; }
+  __syncthreads();
+  for (int d = threadIdx.x; d < D; d += kWarps * 32) {
+    float lo = s_mn[0][d], hi = s_mx[0][d];
 #pragma unroll
-    for (int c = 0; c < C; ++c) {
-      static_cast<float*>(smin)[o + c] = mn[c];
-      static_cast<float*>(smax)[o + c] = mx[c];
-    }
-  } else {
-#pragma unroll
-    for (int c = 0; c < C; ++c) {
+    for (int w = 1; w < kWarps; ++w) { lo = fminf(lo, s_mn[w][d]); hi = fmaxf(hi, s_mx[w][d]); }
+    const int64_t o = (pair * kv.max_blocks + j) * D + d;
+    if constexpr (KIND == HS_KV_F32) {
+      static_cast<float*>(smin)[o] = lo;
+      static_cast<float*>(smax)[o] = hi;
+    } else {
       // bf16 K: min/max are bf16 values, the conversion is exact.  e4m3 K:
       // round outward so the stored box still contains every dequantised key.
-      __nv_bfloat16 lo = (KIND == HS_KV_BF16) ? __float2bfloat16_rn(mn[c]) : __float2bfloat16_rd(mn[c]);
-      __nv_bfloat16 hi = (KIND == HS_KV_BF16) ? __float2bfloat16_rn(mx[c]) : __float2bfloat16_ru(mx[c]);
-      static_cast<__nv_bfloat16*>(smin)[o + c] = lo;
-      static_cast<__nv_bfloat16*>(smax)[o + c] = hi;
+      static_cast<__nv_bfloat16*>(smin)[o] = (KIND == HS_KV_BF16) ? __float2bfloat16_rn(lo) : __float2bfloat16_rd(lo);
+      static_cast<__nv_bfloat16*>(smax)[o] = (KIND == HS_KV_BF16) ? __float2bfloat16_rn(hi) : __float2bfloat16_ru(hi);
     }
   }
 }
@@ -124,17 +128,14 @@ __global__ __launch_bounds__(kWarps * 32) void summaries_kernel(KvView kv, int f
 template <int C>
 cudaError_t launch_c(const KvView& kv, int first_block, int nblocks, void* smin, void* smax,
                      unsigned* err, cudaStream_t st) {
-  dim3 grid(ceil_div(nblocks, kWarps), kv.hkv, kv.batch);
+  dim3 grid(nblocks, kv.hkv, kv.batch);
   switch (kv.kv_dtype) {
     case HS_KV_F32:
-      summaries_kernel<C, HS_KV_F32><<<grid, kWarps * 32, 0, st>>>(kv, first_block, smin, smax, err);
-      break;
+      return launch_pdl(summaries_kernel<C, HS_KV_F32>, grid, dim3(kWarps * 32), 0, st, kv, first_block, smin, smax, err);
     case HS_KV_BF16:
-      summaries_kernel<C, HS_KV_BF16><<<grid, kWarps * 32, 0, st>>>(kv, first_block, smin, smax, err);
-      break;
+      return launch_pdl(summaries_kernel<C, HS_KV_BF16>, grid, dim3(kWarps * 32), 0, st, kv, first_block, smin, smax, err);
     default:
-      summaries_kernel<C, HS_KV_FP8E4M3_G32><<<grid, kWarps * 32, 0, st>>>(kv, first_block, smin, smax, err);
-      break;
+      return launch_pdl(summaries_kernel<C, HS_KV_FP8E4M3_G32>, grid, dim3(kWarps * 32), 0, st, kv, first_block, smin, smax, err);
   }
   return cudaGetLastError();
 }

@@ -31,6 +31,8 @@ __global__ __launch_bounds__(kThreads) void swapin_kernel(HotView hb, const int3
   __shared__ int s_copy_s[kMaxSlots];
   __shared__ int s_ncopy, s_hits, s_evict;
 
+  pdl_trigger();
+  pdl_wait();
   const int pair = blockIdx.x;
   const int S = hb.slots;
   const int base = pair * S;
@@ -172,8 +174,8 @@ cudaError_t launch_swapin(const HotView& hb, const int32_t* sel, const int32_t* 
                           cudaStream_t st) {
   const int pairs = hb.batch * hb.hkv;
   if (pairs == 0) return cudaSuccess;
-  swapin_kernel<<<pairs, kThreads, 0, st>>>(hb, sel, sel_count, capacity, step, stats, err);
-  return cudaGetLastError();
+  return launch_pdl(swapin_kernel, dim3(pairs), dim3(kThreads), 0, st, hb, sel, sel_count, capacity, step,
+                    stats, err);
 }
 
 }  // namespace hs
