@@ -1,5 +1,5 @@
-// Tensor-core gather-attention over the selected blocks (bf16 K/V, head_dim
-// 128): "KV 稀疏化" wiki §5 (full attention on the chosen blocks only) with the
+// Tensor-core gather-attention over the selected blocks (bf16 or e4m3 K/V,
+// head_dim 128): "KV 稀疏化" wiki §5 (full attention on the chosen blocks only) with the
 // tiled running-max / normaliser softmax of "分块稀疏注意力与KV Cache量化" §2.2.
 //
 // The g query heads that share a kv head make the decode step a real small GEMM
@@ -50,6 +50,8 @@ struct TcArgs {
   const int32_t* page_table;
   const int32_t* seq_lens;
   const __nv_bfloat16* q;
+  const float* k_scales;  // e4m3 only
+  const float* v_scales;
   float* ws_o;
   float* ws_lse;
   int64_t num_pages;
@@ -432,6 +434,380 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+
+// ============================================================================
+// e4m3 K/V (one fp32 scale per 32 channels per token), head_dim 128, g <= 8.
+//
+// The e4m3 codes are exact in bf16, so the MMAs run on the codes and the scales
+// are applied in fp32 around them:
+//   GEMM1  S'[tok][(grp, h)] = sum_{d in grp} code_k[tok][d] * q[h][d]   (N = 4 groups x 8 heads)
+//          S[tok][h] = sum_grp kscale[tok][grp] * S'[tok][(grp, h)]
+//   GEMM2  O'[d][(grp, hl, h)] = sum_tok code_v[tok][d] * W_hl[tok][(grp, h)],
+//          W = p[tok][h] * vscale[tok][grp] split into bf16 hi + lo (N = 64);
+//          channel d keeps the columns of its own group grp = d / 32.
+// TMA stages the raw codes and scales; the softmax warps convert each chunk's
+// codes to bf16 operand tiles (zero rows for tokens outside the request) and
+// release the stage.  K tile conversion of chunk c+1 overlaps the softmax of
+// chunk c; the V tile of chunk c is converted once GEMM2 of chunk c-1 is done.
+// ============================================================================
+constexpr int kStages8 = 3;
+constexpr int kCodeBytes = kChunk * 128;          // 128 tokens x 128 codes
+constexpr int kScaleBytes = kChunk * 16;          // 128 tokens x 4 scales
+constexpr int kStage8Bytes = 2 * kCodeBytes + 2 * kScaleBytes;
+struct Layout8 {
+  static constexpr int kOffKbf = kStages8 * kStage8Bytes;  // bf16 K tile (2 halves, swizzled)
+  static constexpr int kOffVbf = kOffKbf + kTileBytes;
+  static constexpr int kQHalf = 32 * 128;                   // 32 rows (group x head) x 64 channels
+  static constexpr int kOffQ = kOffVbf + kTileBytes;
+  static constexpr int kPBytes = kChunk * 64 * 2;           // 128 tokens x 64 columns bf16
+  static constexpr int kOffP = kOffQ + 2 * kQHalf;
+  static constexpr int kOffBar = kOffP + 2 * kPBytes;
+  static constexpr int kNumBars = 2 * kStages8 + 12;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kOffRed = kOffMisc + 16;
+  static constexpr int kBytes = kOffRed + 4 * 8 * 4;
+  static constexpr int kAlloc = 232448;
+  static_assert(kBytes + 1024 <= kAlloc, "shared memory layout too large");
+  static_assert(kOffKbf % 1024 == 0 && kOffQ % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+  static constexpr int kTmemCols = 256;
+  static constexpr int kColO = 64;  // S' uses columns [0, 64)
+};
+
+// one token row of e4m3 codes -> bf16 row of a 128-byte-swizzled K-major tile
+__device__ __forceinline__ void convert_row(const uint8_t* codes_row, uint8_t* tile, int t, bool valid) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int ch = (i + t) & 7;  // staggered so a warp's reads spread over the banks
+    uint4 raw = make_uint4(0, 0, 0, 0);
+    if (valid) raw = *reinterpret_cast<const uint4*>(codes_row + ch * 16);
+    const uint32_t words[4] = {raw.x, raw.y, raw.z, raw.w};
+    uint32_t w[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 a = e4m3x2_to_float2(static_cast<uint16_t>(words[j] & 0xffffu));
+      const float2 b = e4m3x2_to_float2(static_cast<uint16_t>(words[j] >> 16));
+      const __nv_bfloat162 ab = __floats2bfloat162_rn(a.x, a.y);
+      const __nv_bfloat162 bb = __floats2bfloat162_rn(b.x, b.y);
+      w[2 * j] = *reinterpret_cast<const uint32_t*>(&ab);
+      w[2 * j + 1] = *reinterpret_cast<const uint32_t*>(&bb);
+    }
+    uint8_t* row = tile + (ch >> 2) * kHalfBytes + t * 128;
+    const int lc = (ch & 3) * 2;
+    *reinterpret_cast<uint4*>(row + (((lc) ^ (t & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint4*>(row + (((lc + 1) ^ (t & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_tc_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                       TcArgs a, unsigned* err) {
+  using Ly = Layout8;
+  constexpr int NH = 8;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + Ly::kOffBar;
+  auto full_bar = [&](int s) { return bar0 + 8 * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8 * (kStages8 + s); };
+  auto s_full = [&](int b) { return bar0 + 8 * (2 * kStages8 + b); };
+  auto s_free = [&](int b) { return bar0 + 8 * (2 * kStages8 + 2 + b); };
+  auto p_full = [&](int b) { return bar0 + 8 * (2 * kStages8 + 4 + b); };
+  auto o_full = [&](int b) { return bar0 + 8 * (2 * kStages8 + 6 + b); };
+  auto o_free = [&](int b) { return bar0 + 8 * (2 * kStages8 + 8 + b); };
+  const uint32_t q_full = bar0 + 8 * (2 * kStages8 + 10);
+  const uint32_t kconv_full = bar0 + 8 * (2 * kStages8 + 11);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Ly::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Ly::kOffMisc + 4);
+  float* red = reinterpret_cast<float*>(smem + Ly::kOffRed);
+  auto kc_stage = [&](int s) { return smem + s * kStage8Bytes; };
+  auto vc_stage = [&](int s) { return smem + s * kStage8Bytes + kCodeBytes; };
+  auto ks_stage = [&](int s) { return smem + s * kStage8Bytes + 2 * kCodeBytes; };
+  auto vs_stage = [&](int s) { return smem + s * kStage8Bytes + 2 * kCodeBytes + kScaleBytes; };
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int B = a.block;
+  const int bpc = kChunk / B;
+
+  pdl_trigger();
+  if (tid == 0) {
+    for (int s = 0; s < kStages8; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 128);  // released by the converting warps
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(s_full(b), 1);
+      mbar_init(s_free(b), 128);
+      mbar_init(p_full(b), 128);
+      mbar_init(o_full(b), 1);
+      mbar_init(o_free(b), 128);
+    }
+    mbar_init(q_full, 128);
+    mbar_init(kconv_full, 128);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), Ly::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  pdl_wait();
+
+  if (warp == kProducerWarp) {
+    if (lane == 0) {
+      unsigned bad = 0;
+      int c = 0;
+      for (int item = blockIdx.x; item < a.items && !*abort_flag; item += gridDim.x) {
+        const Item it = item_geom(a, item, bpc);
+        for (int ci = 0; ci < it.nch; ++ci, ++c) {
+          const int s = c % kStages8;
+          if (c >= kStages8 && !mbar_wait(empty_bar(s), ((c / kStages8) + 1) & 1, abort_flag)) goto producer_done;
+          uint32_t tx = 0;
+          for (int bi = 0; bi < bpc; ++bi) {
+            int vt;
+            if (resolve(a, it, it.s0 + ci * bpc + bi, &vt, &bad) >= 0) tx += 2u * B * 128u + 2u * B * 16u;
+          }
+          mbar_arrive_tx(full_bar(s), tx);
+          unsigned dummy = 0;
+          for (int bi = 0; bi < bpc; ++bi) {
+            int vt;
+            const int page = resolve(a, it, it.s0 + ci * bpc + bi, &vt, &dummy);
+            if (page < 0) continue;
+            const int y = page * B;
+            tma_load_2d(smem_u32(kc_stage(s)) + bi * B * 128, &tm_k, 0, y, full_bar(s));
+            tma_load_2d(smem_u32(vc_stage(s)) + bi * B * 128, &tm_v, 0, y, full_bar(s));
+            bulk_load(smem_u32(ks_stage(s)) + bi * B * 16, a.k_scales + static_cast<int64_t>(y) * 4, B * 16,
+                      full_bar(s));
+            bulk_load(smem_u32(vs_stage(s)) + bi * B * 16, a.v_scales + static_cast<int64_t>(y) * 4, B * 16,
+                      full_bar(s));
+          }
+        }
+      }
+    producer_done:
+      if (bad) set_error(err, bad);
+      for (int s = 0; s < kStages8 && s < c; ++s) {
+        const int last = c - 1 - ((c - 1 - s) % kStages8);
+        mbar_wait(full_bar(s), (last / kStages8) & 1, abort_flag, 500000000ull);
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) {
+      constexpr uint32_t idesc1 = idesc_bf16(128, 32, false, false);
+      constexpr uint32_t idesc2 = idesc_bf16(128, 64, true, true);
+      const uint32_t kbf = sbase + Ly::kOffKbf, vbf = sbase + Ly::kOffVbf;
+      const uint32_t qb = sbase + Ly::kOffQ, pb = sbase + Ly::kOffP;
+      int c = 0, qi = 0, last_g2 = -1;
+      auto gemm1 = [&](int cc) -> bool {
+        const int bb = cc & 1;
+        if (!mbar_wait(kconv_full, cc & 1, abort_flag)) return false;
+        if (cc >= 2 && !mbar_wait(s_free(bb), ((cc >> 1) + 1) & 1, abort_flag)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < kD / 16; ++k) {
+          const int h = k >> 2, kk = k & 3;
+          const uint64_t ad = smem_desc(kbf + h * kHalfBytes + kk * 32, 16, 1024, 2);
+          const uint64_t bd = smem_desc(qb + h * Ly::kQHalf + kk * 32, 16, 1024, 2);
+          mma_f16(tmem + bb * 32, ad, bd, idesc1, k > 0 ? 1u : 0u);
+        }
+        mma_commit(s_full(bb));
+        return true;
+      };
+      auto gemm2 = [&](int cc) -> bool {
+        const int bb = cc & 1;
+        if (!mbar_wait(p_full(bb), (cc >> 1) & 1, abort_flag)) return false;
+        if (cc >= 2 && !mbar_wait(o_free(bb), ((cc >> 1) + 1) & 1, abort_flag)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < kChunk / 16; ++k) {
+          const uint64_t ad = smem_desc(vbf + k * 2048, kHalfBytes, 1024, 2);
+          const uint64_t bd = smem_desc(pb + bb * Ly::kPBytes + k * 2048, 1024, 128, 0);
+          mma_f16(tmem + Ly::kColO + bb * 64, ad, bd, idesc2, k > 0 ? 1u : 0u);
+        }
+        mma_commit(o_full(bb));
+        last_g2 = cc;
+        return true;
+      };
+      for (int item = blockIdx.x; item < a.items && !*abort_flag; item += gridDim.x) {
+        const Item it = item_geom(a, item, bpc);
+        if (it.nch == 0) continue;
+        if (!mbar_wait(q_full, qi & 1, abort_flag)) break;
+        ++qi;
+        tc_fence_after();
+        if (!gemm1(c)) break;
+        bool ok = true;
+        for (int ci = 0; ci < it.nch && ok; ++ci, ++c) {
+          if (ci + 1 < it.nch) ok = gemm1(c + 1);
+          if (ok) ok = gemm2(c);
+        }
+        if (!ok) break;
+      }
+      if (last_g2 >= 0) mbar_wait(o_full(last_g2 & 1), (last_g2 >> 1) & 1, abort_flag, 500000000ull);
+    }
+  } else {
+    const int t = tid;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const int g = a.group;
+    int c = 0;
+    for (int item = blockIdx.x; item < a.items && !*abort_flag; item += gridDim.x) {
+      const Item it = item_geom(a, item, bpc);
+      const int64_t row0 = (static_cast<int64_t>(it.b) * a.hq + it.kvh * g) * a.splits + it.split;
+      if (it.nch == 0) {
+        for (int h = 0; h < g; ++h) {
+          a.ws_o[(row0 + static_cast<int64_t>(h) * a.splits) * kD + t] = 0.0f;
+          if (t == 0) a.ws_lse[row0 + static_cast<int64_t>(h) * a.splits] = -INFINITY;
+        }
+        continue;
+      }
+      // Q' operand: row (grp, h) holds head h's channels of group grp, zeros elsewhere
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int idx = t * 4 + i;
+        const int half = idx >> 8, rem = idx & 255, row = rem >> 3, ch = rem & 7;
+        const int grp = row >> 3, h = row & 7;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (h < g && half * 2 + (ch >> 2) == grp)
+          v = *reinterpret_cast<const uint4*>(a.q + (static_cast<int64_t>(it.b) * a.hq + it.kvh * g + h) * kD +
+                                              half * 64 + ch * 8);
+        *reinterpret_cast<uint4*>(smem + Ly::kOffQ + half * Ly::kQHalf + row * 128 + ((ch ^ (row & 7)) << 4)) = v;
+      }
+      fence_async_smem();
+      mbar_arrive(q_full);
+
+      // row t of a chunk: token t % B of its (t / B)-th block
+      auto row_state = [&](int ci, bool* valid) {
+        const int bi = t / B, tok = t - bi * B;
+        unsigned dummy = 0;
+        int vt = 0;
+        const int page = resolve(a, it, it.s0 + ci * bpc + bi, &vt, &dummy);
+        *valid = page >= 0 && tok < vt;
+      };
+      float ks_cur[4], ks_next[4] = {0.f, 0.f, 0.f, 0.f};
+      bool valid_cur = false, valid_next = false;
+      bool ok = true;
+      auto convert_k = [&](int cc, int ci) -> bool {
+        const int s = cc % kStages8;
+        row_state(ci, &valid_next);
+        if (!mbar_wait(full_bar(s), (cc / kStages8) & 1, abort_flag)) return false;
+        convert_row(kc_stage(s) + t * 128, smem + Ly::kOffKbf, t, valid_next);
+        const float4 sc = valid_next ? *reinterpret_cast<const float4*>(ks_stage(s) + t * 16) : make_float4(0, 0, 0, 0);
+        ks_next[0] = sc.x; ks_next[1] = sc.y; ks_next[2] = sc.z; ks_next[3] = sc.w;
+        fence_async_smem();
+        mbar_arrive(kconv_full);
+        return true;
+      };
+      float m[NH], lsum[NH], oacc[NH], alpha_prev[NH];
+#pragma unroll
+      for (int h = 0; h < NH; ++h) {
+        m[h] = -INFINITY;
+        lsum[h] = 0.0f;
+        oacc[h] = 0.0f;
+        alpha_prev[h] = 1.0f;
+      }
+      auto take_o = [&](int cc) -> bool {
+        const int bb = cc & 1;
+        if (!mbar_wait(o_full(bb), (cc >> 1) & 1, abort_flag)) return false;
+        tc_fence_after();
+        float ov[16];
+        tmem_ld16(tmem + lane_base + Ly::kColO + bb * 64 + warp * 16, ov);  // channel t's group = warp
+        tc_fence_before();
+        mbar_arrive(o_free(bb));
+#pragma unroll
+        for (int h = 0; h < NH; ++h) oacc[h] = fmaf(oacc[h], alpha_prev[h], ov[h] + ov[NH + h]);
+        return true;
+      };
+      if (!convert_k(c, 0)) break;
+      for (int ci = 0; ci < it.nch && ok; ++ci, ++c) {
+        const int bb = c & 1, s = c % kStages8;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) ks_cur[i] = ks_next[i];
+        valid_cur = valid_next;
+        if (!mbar_wait(s_full(bb), (c >> 1) & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        float sv[32];
+        tmem_ld16(tmem + lane_base + bb * 32, *reinterpret_cast<float(*)[16]>(sv));
+        tmem_ld16(tmem + lane_base + bb * 32 + 16, *reinterpret_cast<float(*)[16]>(sv + 16));
+        tc_fence_before();
+        mbar_arrive(s_free(bb));
+        if (ci + 1 < it.nch && !convert_k(c + 1, ci + 1)) { ok = false; break; }
+        float x[NH];
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {
+          const float sc = ks_cur[0] * sv[h] + ks_cur[1] * sv[8 + h] + ks_cur[2] * sv[16 + h] + ks_cur[3] * sv[24 + h];
+          x[h] = (valid_cur && h < g) ? sc * a.scale_log2 : -INFINITY;
+        }
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {
+          const float mx = warp_max(x[h]);
+          if (lane == 0) red[warp * NH + h] = mx;
+        }
+        named_barrier(1, 128);
+        float alpha[NH], p[NH];
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {
+          const float cm = fmaxf(fmaxf(red[h], red[NH + h]), fmaxf(red[2 * NH + h], red[3 * NH + h]));
+          const float mn = fmaxf(m[h], cm);
+          alpha[h] = (mn == -INFINITY) ? 1.0f : exp2f(m[h] - mn);
+          m[h] = mn;
+          p[h] = x[h] == -INFINITY ? 0.0f : exp2f(x[h] - mn);
+          lsum[h] = fmaf(lsum[h], alpha[h], p[h]);
+        }
+        named_barrier(1, 128);
+        if (ci > 0 && !take_o(c - 1)) { ok = false; break; }
+        // V tile of this chunk (GEMM2 of the previous chunk is done with it)
+        convert_row(vc_stage(s) + t * 128, smem + Ly::kOffVbf, t, valid_cur);
+        const float4 vsc = valid_cur ? *reinterpret_cast<const float4*>(vs_stage(s) + t * 16) : make_float4(0, 0, 0, 0);
+        mbar_arrive(empty_bar(s));  // codes and scales of this stage are all consumed
+        const float vs[4] = {vsc.x, vsc.y, vsc.z, vsc.w};
+        uint8_t* prow = smem + Ly::kOffP + bb * Ly::kPBytes + (t >> 3) * 1024 + (t & 7) * 16;
+#pragma unroll
+        for (int grp = 0; grp < 4; ++grp) {
+          uint32_t hi2[4], lo2[4];
+#pragma unroll
+          for (int h = 0; h < NH; h += 2) {
+            const float w0 = p[h] * vs[grp], w1 = p[h + 1] * vs[grp];
+            const __nv_bfloat162 hi = __floats2bfloat162_rn(w0, w1);
+            const float2 hf = __bfloat1622float2(hi);
+            const __nv_bfloat162 lo = __floats2bfloat162_rn(w0 - hf.x, w1 - hf.y);
+            hi2[h / 2] = *reinterpret_cast<const uint32_t*>(&hi);
+            lo2[h / 2] = *reinterpret_cast<const uint32_t*>(&lo);
+          }
+          *reinterpret_cast<uint4*>(prow + (grp * 2) * 128) = make_uint4(hi2[0], hi2[1], hi2[2], hi2[3]);
+          *reinterpret_cast<uint4*>(prow + (grp * 2 + 1) * 128) = make_uint4(lo2[0], lo2[1], lo2[2], lo2[3]);
+        }
+        fence_async_smem();
+        mbar_arrive(p_full(bb));
+#pragma unroll
+        for (int h = 0; h < NH; ++h) alpha_prev[h] = alpha[h];
+      }
+      if (!ok || !take_o(c - 1)) break;
+#pragma unroll
+      for (int h = 0; h < NH; ++h) {
+        const float s_ = warp_sum(lsum[h]);
+        if (lane == 0) red[warp * NH + h] = s_;
+      }
+      named_barrier(1, 128);
+      for (int h = 0; h < g && h < NH; ++h) {
+        const float lt = red[h] + red[NH + h] + red[2 * NH + h] + red[3 * NH + h];
+        const int64_t row = row0 + static_cast<int64_t>(h) * a.splits;
+        a.ws_o[row * kD + t] = lt > 0.0f ? oacc[h] / lt : 0.0f;
+        if (t == 0) a.ws_lse[row] = lt > 0.0f ? (m[h] + log2f(lt)) * kLn2 : -INFINITY;
+      }
+      named_barrier(1, 128);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag && tid == 0) set_error(err, HS_EBIT_TIMEOUT);
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, Ly::kTmemCols);
+  }
+}
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -464,20 +840,28 @@ bool make_map(CUtensorMap* m, const void* base, int64_t rows, int block) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int NH>
-cudaError_t launch_nh(const KvView& kv, const AttnArgs& aa, unsigned* err, cudaStream_t st) {
-  using Ly = Layout<NH>;
-  CUtensorMap mk, mv;
-  const int64_t rows = kv.num_pages * kv.block;
-  if (rows <= 0) return cudaErrorInvalidValue;
-  if (!make_map(&mk, kv.k_pages, rows, kv.block) || !make_map(&mv, kv.v_pages, rows, kv.block))
-    return cudaErrorInvalidValue;
+// e4m3 codes: [rows][128] bytes, box = one page of rows x 128 codes, no swizzle
+bool make_map_codes(CUtensorMap* m, const void* base, int64_t rows, int block) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kD)};
+  const cuuint32_t box[2] = {128, static_cast<cuuint32_t>(block)};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+TcArgs make_args(const KvView& kv, const AttnArgs& aa) {
   TcArgs a;
   a.sel = aa.sel;
   a.sel_count = aa.sel_count;
   a.page_table = kv.page_table;
   a.seq_lens = kv.seq_lens;
   a.q = static_cast<const __nv_bfloat16*>(aa.q);
+  a.k_scales = kv.k_scales;
+  a.v_scales = kv.v_scales;
   a.ws_o = aa.ws_o;
   a.ws_lse = aa.ws_lse;
   a.num_pages = kv.num_pages;
@@ -491,6 +875,33 @@ cudaError_t launch_nh(const KvView& kv, const AttnArgs& aa, unsigned* err, cudaS
   a.splits = aa.splits;
   a.items = kv.batch * kv.hkv * aa.splits;
   a.scale_log2 = aa.scale * kLog2e;
+  return a;
+}
+
+cudaError_t launch_fp8(const KvView& kv, const AttnArgs& aa, unsigned* err, cudaStream_t st) {
+  CUtensorMap mk, mv;
+  const int64_t rows = kv.num_pages * kv.block;
+  if (rows <= 0) return cudaErrorInvalidValue;
+  if (!make_map_codes(&mk, kv.k_pages, rows, kv.block) || !make_map_codes(&mv, kv.v_pages, rows, kv.block))
+    return cudaErrorInvalidValue;
+  const TcArgs a = make_args(kv, aa);
+  if (a.items == 0) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(attn_tc_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       Layout8::kAlloc);
+  if (e != cudaSuccess) return e;
+  const int grid = a.items < aa.sms ? a.items : aa.sms;
+  return launch_pdl(attn_tc_fp8_kernel, dim3(grid), dim3(kThreads), Layout8::kAlloc, st, mk, mv, a, err);
+}
+
+template <int NH>
+cudaError_t launch_nh(const KvView& kv, const AttnArgs& aa, unsigned* err, cudaStream_t st) {
+  using Ly = Layout<NH>;
+  CUtensorMap mk, mv;
+  const int64_t rows = kv.num_pages * kv.block;
+  if (rows <= 0) return cudaErrorInvalidValue;
+  if (!make_map(&mk, kv.k_pages, rows, kv.block) || !make_map(&mv, kv.v_pages, rows, kv.block))
+    return cudaErrorInvalidValue;
+  const TcArgs a = make_args(kv, aa);
   if (a.items == 0) return cudaSuccess;
   auto kern = attn_tc_kernel<NH>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::kAlloc);
@@ -502,14 +913,21 @@ cudaError_t launch_nh(const KvView& kv, const AttnArgs& aa, unsigned* err, cudaS
 }  // namespace
 
 bool attn_tc_supported(const KvView& kv) {
-  if (kv.kv_dtype != HS_KV_BF16 || kv.head_dim != kD) return false;
+  if (kv.head_dim != kD) return false;
+  if (kv.kv_dtype == HS_KV_BF16) {
+    if (kv.group > 16) return false;
+  } else if (kv.kv_dtype == HS_KV_FP8E4M3_G32) {
+    if (kv.group > 8 || !kv.k_scales || !kv.v_scales) return false;
+  } else {
+    return false;
+  }
   if (kv.block != 16 && kv.block != 32 && kv.block != 64 && kv.block != 128) return false;
-  if (kv.group > 16) return false;
   if (kv.num_pages * kv.block >= (int64_t(1) << 31)) return false;
   return encode_fn() != nullptr;
 }
 
 cudaError_t launch_attn_tc(const KvView& kv, const AttnArgs& a, unsigned* err, cudaStream_t st) {
+  if (kv.kv_dtype == HS_KV_FP8E4M3_G32) return launch_fp8(kv, a, err, st);
   return kv.group <= 8 ? launch_nh<8>(kv, a, err, st) : launch_nh<16>(kv, a, err, st);
 }
 
