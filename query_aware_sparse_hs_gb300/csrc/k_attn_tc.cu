@@ -68,7 +68,8 @@ struct Layout {
   static constexpr int kNumBars = 2 * kStages + 11;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kOffRed = kOffMisc + 16;
-  static constexpr int kBytes = kOffRed + 4 * NH * 4;
+  static constexpr int kOffMeta = kOffRed + 4 * NH * 4;  // [stage][8] (page, valid tokens)
+  static constexpr int kBytes = kOffMeta + kStages * 8 * 8;
   // the whole per-block maximum: one CTA per SM, and operand reads through a
   // descriptor can never leave this CTA's own shared memory
   static constexpr int kAlloc = 232448;
@@ -113,6 +114,76 @@ __device__ __forceinline__ int resolve(const TcArgs& a, const Item& it, int pos,
   }
   *vt = min(a.block, it.L - j * a.block);
   return page;
+}
+
+
+// The (item, chunk) sequence every role of a CTA walks, skipping empty items.
+struct Cursor {
+  int item, ci;
+  Item it;
+};
+
+__device__ __forceinline__ bool cursor_seek(const TcArgs& a, int bpc, Cursor& c) {
+  for (; c.item < a.items; c.item += gridDim.x) {
+    c.it = item_geom(a, c.item, bpc);
+    if (c.it.nch > 0) {
+      c.ci = 0;
+      return true;
+    }
+  }
+  return false;
+}
+__device__ __forceinline__ bool cursor_first(const TcArgs& a, int bpc, Cursor& c) {
+  c.item = blockIdx.x;
+  return cursor_seek(a, bpc, c);
+}
+__device__ __forceinline__ bool cursor_next(const TcArgs& a, int bpc, Cursor& c) {
+  if (++c.ci < c.it.nch) return true;
+  c.item += gridDim.x;
+  return cursor_seek(a, bpc, c);
+}
+
+// TMA producer warp (all 32 lanes).  Lane i resolves block i of a chunk (its
+// selected index and physical page) one chunk ahead, so the dependent lookups
+// overlap the wait for a free stage; the chunk's pages and valid-token counts
+// are published in meta[stage][8] for the softmax warps, and each lane issues
+// the copies of its own block.
+template <int STAGES, typename IssueFn>
+__device__ __forceinline__ void run_producer(const TcArgs& a, int bpc, uint32_t full0, uint32_t empty0,
+                                             int2* meta, uint32_t bytes_per_block, volatile int* abort_flag,
+                                             unsigned* err, IssueFn issue) {
+  const int lane = threadIdx.x & 31;
+  unsigned bad = 0;
+  Cursor cur;
+  bool have = cursor_first(a, bpc, cur);
+  int page = -1, vt = 0;
+  if (have && lane < bpc) page = resolve(a, cur.it, cur.it.s0 + cur.ci * bpc + lane, &vt, &bad);
+  int c = 0;
+  for (;; ++c) {
+    int go = 0;
+    if (lane == 0) go = have && !*abort_flag && (c < STAGES || mbar_wait(empty0 + 8 * (c % STAGES), ((c / STAGES) + 1) & 1, abort_flag));
+    if (!__shfl_sync(0xffffffffu, go, 0)) break;
+    const int s = c % STAGES;
+    if (lane < 8) meta[s * 8 + lane] = make_int2(page, vt);
+    const uint32_t tx = __reduce_add_sync(0xffffffffu, page >= 0 ? bytes_per_block : 0u);
+    __syncwarp();
+    if (lane == 0) mbar_arrive_tx(full0 + 8 * s, tx);
+    __syncwarp();
+    if (page >= 0) issue(s, lane, page);
+    have = cursor_next(a, bpc, cur);
+    page = -1;
+    vt = 0;
+    if (have && lane < bpc) page = resolve(a, cur.it, cur.it.s0 + cur.ci * bpc + lane, &vt, &bad);
+  }
+  bad = __reduce_or_sync(0xffffffffu, bad);
+  if (lane == 0) {
+    if (bad) set_error(err, bad);
+    // let every copy this CTA issued land before the CTA can exit
+    for (int s = 0; s < STAGES && s < c; ++s) {
+      const int last = c - 1 - ((c - 1 - s) % STAGES);
+      mbar_wait(full0 + 8 * s, (last / STAGES) & 1, abort_flag, 500000000ull);
+    }
+  }
 }
 
 template <int NH>
@@ -178,44 +249,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   pdl_wait();  // the selection and q of this step are complete from here on
 
+  int2* meta = reinterpret_cast<int2*>(smem + Ly::kOffMeta);
   if (warp == kProducerWarp) {
     // ================= TMA producer =================
-    if (lane == 0) {
-      unsigned bad = 0;
-      int c = 0;
-      for (int item = blockIdx.x; item < a.items && !*abort_flag; item += gridDim.x) {
-        const Item it = item_geom(a, item, bpc);
-        for (int ci = 0; ci < it.nch; ++ci, ++c) {
-          const int s = c % kStages;
-          if (c >= kStages && !mbar_wait(empty_bar(s), ((c / kStages) + 1) & 1, abort_flag)) goto producer_done;
-          uint32_t tx = 0;
-          for (int bi = 0; bi < bpc; ++bi) {
-            int vt;
-            if (resolve(a, it, it.s0 + ci * bpc + bi, &vt, &bad) >= 0) tx += 4u * B * 128u;
-          }
-          mbar_arrive_tx(full_bar(s), tx);
-          unsigned dummy = 0;
-          for (int bi = 0; bi < bpc; ++bi) {
-            int vt;
-            const int page = resolve(a, it, it.s0 + ci * bpc + bi, &vt, &dummy);
-            if (page < 0) continue;
-            const uint32_t row_off = bi * B * 128;
-            const int y = page * B;
-            tma_load_2d(k_half(s, 0) + row_off, &tm_k, 0, y, full_bar(s));
-            tma_load_2d(k_half(s, 1) + row_off, &tm_k, 64, y, full_bar(s));
-            tma_load_2d(v_half(s, 0) + row_off, &tm_v, 0, y, full_bar(s));
-            tma_load_2d(v_half(s, 1) + row_off, &tm_v, 64, y, full_bar(s));
-          }
-        }
-      }
-    producer_done:
-      if (bad) set_error(err, bad);
-      // let every copy this CTA issued land before the CTA can exit
-      for (int s = 0; s < kStages && s < c; ++s) {
-        const int last = c - 1 - ((c - 1 - s) % kStages);
-        mbar_wait(full_bar(s), (last / kStages) & 1, abort_flag, 500000000ull);
-      }
-    }
+    run_producer<kStages>(a, bpc, full_bar(0), empty_bar(0), meta, 4u * B * 128u, abort_flag, err,
+                          [&](int s, int bi, int page) {
+                            const uint32_t row_off = bi * B * 128;
+                            const int y = page * B;
+                            tma_load_2d(k_half(s, 0) + row_off, &tm_k, 0, y, full_bar(s));
+                            tma_load_2d(k_half(s, 1) + row_off, &tm_k, 64, y, full_bar(s));
+                            tma_load_2d(v_half(s, 0) + row_off, &tm_v, 0, y, full_bar(s));
+                            tma_load_2d(v_half(s, 1) + row_off, &tm_v, 64, y, full_bar(s));
+                          });
   } else if (warp == kMmaWarp) {
     // ================= MMA issuer =================
     if (lane == 0) {
@@ -333,11 +378,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int ci = 0; ci < it.nch && ok; ++ci, ++c) {
         const int bb = c & 1, s = c % kStages;
         const int bi = t / B, tok = t - bi * B;
-        unsigned dummy = 0;
-        int vt = 0;
-        const int page = resolve(a, it, it.s0 + ci * bpc + bi, &vt, &dummy);
-        const bool loaded = page >= 0;
-        const bool valid = loaded && tok < vt;
+        if (!mbar_wait(full_bar(s), (c / kStages) & 1, abort_flag)) { ok = false; break; }
+        const int2 md = meta[s * 8 + bi];
+        const bool loaded = md.x >= 0;
+        const bool valid = loaded && tok < md.y;
         if (!mbar_wait(s_full(bb), (c >> 1) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
         float sv[16];
@@ -391,7 +435,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (loaded && !valid) {
           // rows past the request's end inside its last page: zero V so they
           // contribute exactly nothing (P is 0 there, the stored bytes may not be finite)
-          if (!mbar_wait(full_bar(s), (c / kStages) & 1, abort_flag)) { ok = false; break; }
           uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
@@ -465,7 +508,8 @@ struct Layout8 {
   static constexpr int kNumBars = 2 * kStages8 + 12;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kOffRed = kOffMisc + 16;
-  static constexpr int kBytes = kOffRed + 4 * 8 * 4;
+  static constexpr int kOffMeta = kOffRed + 4 * 8 * 4;
+  static constexpr int kBytes = kOffMeta + kStages8 * 8 * 8;
   static constexpr int kAlloc = 232448;
   static_assert(kBytes + 1024 <= kAlloc, "shared memory layout too large");
   static_assert(kOffKbf % 1024 == 0 && kOffQ % 1024 == 0, "swizzled tiles need 1024-byte alignment");
@@ -556,43 +600,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   pdl_wait();
 
+  int2* meta = reinterpret_cast<int2*>(smem + Ly::kOffMeta);
   if (warp == kProducerWarp) {
-    if (lane == 0) {
-      unsigned bad = 0;
-      int c = 0;
-      for (int item = blockIdx.x; item < a.items && !*abort_flag; item += gridDim.x) {
-        const Item it = item_geom(a, item, bpc);
-        for (int ci = 0; ci < it.nch; ++ci, ++c) {
-          const int s = c % kStages8;
-          if (c >= kStages8 && !mbar_wait(empty_bar(s), ((c / kStages8) + 1) & 1, abort_flag)) goto producer_done;
-          uint32_t tx = 0;
-          for (int bi = 0; bi < bpc; ++bi) {
-            int vt;
-            if (resolve(a, it, it.s0 + ci * bpc + bi, &vt, &bad) >= 0) tx += 2u * B * 128u + 2u * B * 16u;
-          }
-          mbar_arrive_tx(full_bar(s), tx);
-          unsigned dummy = 0;
-          for (int bi = 0; bi < bpc; ++bi) {
-            int vt;
-            const int page = resolve(a, it, it.s0 + ci * bpc + bi, &vt, &dummy);
-            if (page < 0) continue;
-            const int y = page * B;
-            tma_load_2d(smem_u32(kc_stage(s)) + bi * B * 128, &tm_k, 0, y, full_bar(s));
-            tma_load_2d(smem_u32(vc_stage(s)) + bi * B * 128, &tm_v, 0, y, full_bar(s));
-            bulk_load(smem_u32(ks_stage(s)) + bi * B * 16, a.k_scales + static_cast<int64_t>(y) * 4, B * 16,
-                      full_bar(s));
-            bulk_load(smem_u32(vs_stage(s)) + bi * B * 16, a.v_scales + static_cast<int64_t>(y) * 4, B * 16,
-                      full_bar(s));
-          }
-        }
-      }
-    producer_done:
-      if (bad) set_error(err, bad);
-      for (int s = 0; s < kStages8 && s < c; ++s) {
-        const int last = c - 1 - ((c - 1 - s) % kStages8);
-        mbar_wait(full_bar(s), (last / kStages8) & 1, abort_flag, 500000000ull);
-      }
-    }
+    run_producer<kStages8>(a, bpc, full_bar(0), empty_bar(0), meta, 2u * B * 128u + 2u * B * 16u, abort_flag, err,
+                           [&](int s, int bi, int page) {
+                             const int y = page * B;
+                             tma_load_2d(smem_u32(kc_stage(s)) + bi * B * 128, &tm_k, 0, y, full_bar(s));
+                             tma_load_2d(smem_u32(vc_stage(s)) + bi * B * 128, &tm_v, 0, y, full_bar(s));
+                             bulk_load(smem_u32(ks_stage(s)) + bi * B * 16, a.k_scales + static_cast<int64_t>(y) * 4,
+                                       B * 16, full_bar(s));
+                             bulk_load(smem_u32(vs_stage(s)) + bi * B * 16, a.v_scales + static_cast<int64_t>(y) * 4,
+                                       B * 16, full_bar(s));
+                           });
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
       constexpr uint32_t idesc1 = idesc_bf16(128, 32, false, false);
@@ -677,20 +696,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(q_full);
 
       // row t of a chunk: token t % B of its (t / B)-th block
-      auto row_state = [&](int ci, bool* valid) {
-        const int bi = t / B, tok = t - bi * B;
-        unsigned dummy = 0;
-        int vt = 0;
-        const int page = resolve(a, it, it.s0 + ci * bpc + bi, &vt, &dummy);
-        *valid = page >= 0 && tok < vt;
-      };
       float ks_cur[4], ks_next[4] = {0.f, 0.f, 0.f, 0.f};
       bool valid_cur = false, valid_next = false;
       bool ok = true;
-      auto convert_k = [&](int cc, int ci) -> bool {
+      auto convert_k = [&](int cc) -> bool {
         const int s = cc % kStages8;
-        row_state(ci, &valid_next);
         if (!mbar_wait(full_bar(s), (cc / kStages8) & 1, abort_flag)) return false;
+        const int bi = t / B, tok = t - bi * B;
+        const int2 md = meta[s * 8 + bi];
+        valid_next = md.x >= 0 && tok < md.y;
         convert_row(kc_stage(s) + t * 128, smem + Ly::kOffKbf, t, valid_next);
         const float4 sc = valid_next ? *reinterpret_cast<const float4*>(ks_stage(s) + t * 16) : make_float4(0, 0, 0, 0);
         ks_next[0] = sc.x; ks_next[1] = sc.y; ks_next[2] = sc.z; ks_next[3] = sc.w;
@@ -718,7 +732,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int h = 0; h < NH; ++h) oacc[h] = fmaf(oacc[h], alpha_prev[h], ov[h] + ov[NH + h]);
         return true;
       };
-      if (!convert_k(c, 0)) break;
+      if (!convert_k(c)) break;
       for (int ci = 0; ci < it.nch && ok; ++ci, ++c) {
         const int bb = c & 1, s = c % kStages8;
 #pragma unroll
@@ -731,7 +745,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld16(tmem + lane_base + bb * 32 + 16, *reinterpret_cast<float(*)[16]>(sv + 16));
         tc_fence_before();
         mbar_arrive(s_free(bb));
-        if (ci + 1 < it.nch && !convert_k(c + 1, ci + 1)) { ok = false; break; }
+        if (ci + 1 < it.nch && !convert_k(c + 1)) { ok = false; break; }
         float x[NH];
 #pragma unroll
         for (int h = 0; h < NH; ++h) {

@@ -63,56 +63,68 @@ struct RowLoad<C, HS_KV_FP8E4M3_G32> {
 constexpr int kWarps = 8;
 constexpr int kRowsPerRound = 8;  // rows a warp has in flight
 
-// One CTA per block: warp w takes rows w, w+8, ... with all of its rows of a
-// round loaded before any is used, so a block costs about one memory latency;
-// the 8 partial boxes are then combined in shared memory.
+// Warps per block: enough that each warp reads about 8 rows (B/8, from 1 to
+// 8); a CTA of 8 warps therefore covers 8 / wpb blocks.  Each warp loads all
+// the rows of a round before using any, so a block costs about one memory
+// latency; the warps' partial boxes are combined in shared memory.
+__host__ __device__ __forceinline__ int warps_per_block(int B) { return B >= 64 ? 8 : (B >= 8 ? B / 8 : 1); }
+
 template <int C, int KIND>
 __global__ __launch_bounds__(kWarps * 32) void summaries_kernel(KvView kv, int first_block,
                                                                void* smin, void* smax,
                                                                unsigned* err) {
   constexpr int D = C * 32;
   __shared__ float s_mn[kWarps][D], s_mx[kWarps][D];
+  __shared__ int s_ok[kWarps];
   pdl_trigger();
   pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = blockIdx.z, kvh = blockIdx.y;
-  const int j = first_block + blockIdx.x;
-  const int L = kv.seq_lens[b];
   const int B = kv.block;
+  const int wpb = warps_per_block(B), per_cta = kWarps / wpb;
+  const int j = first_block + blockIdx.x * per_cta + warp / wpb;
+  const int sub = warp % wpb;
+  const int L = kv.seq_lens[b];
   const int nb = min(ceil_div(max(L, 0), B), kv.max_blocks);
-  if (j >= nb) return;
   const int64_t pair = static_cast<int64_t>(b) * kv.hkv + kvh;
-  const int page = kv.page_table[pair * kv.max_blocks + j];
-  if (page < 0 || page >= kv.num_pages) {
-    if (threadIdx.x == 0) set_error(err, HS_EBIT_PAGE_RANGE);
-    return;
-  }
-  const int valid = min(B, L - j * B);
   const int d0 = lane * C;
   float mn[C], mx[C];
 #pragma unroll
   for (int c = 0; c < C; ++c) { mn[c] = INFINITY; mx[c] = -INFINITY; }
-  const int64_t row0 = static_cast<int64_t>(page) * B;
-  for (int t0 = warp; t0 < valid; t0 += kWarps * kRowsPerRound) {
-    float x[kRowsPerRound][C];
+  bool ok = j < nb;
+  if (ok) {
+    const int page = kv.page_table[pair * kv.max_blocks + j];
+    if (page < 0 || page >= kv.num_pages) {
+      if (lane == 0 && sub == 0) set_error(err, HS_EBIT_PAGE_RANGE);
+      ok = false;
+    } else {
+      const int valid = min(B, L - j * B);
+      const int64_t row0 = static_cast<int64_t>(page) * B;
+      for (int t0 = sub; t0 < valid; t0 += wpb * kRowsPerRound) {
+        float x[kRowsPerRound][C];
 #pragma unroll
-    for (int u = 0; u < kRowsPerRound; ++u) {
-      const int t = min(t0 + u * kWarps, valid - 1);  // clamp: a repeated valid row changes nothing
-      RowLoad<C, KIND>::get(kv, row0 + t, d0, x[u]);
+        for (int u = 0; u < kRowsPerRound; ++u) {
+          const int t = min(t0 + u * wpb, valid - 1);  // clamp: a repeated valid row changes nothing
+          RowLoad<C, KIND>::get(kv, row0 + t, d0, x[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < kRowsPerRound; ++u)
+#pragma unroll
+          for (int c = 0; c < C; ++c) { mn[c] = fminf(mn[c], x[u][c]); mx[c] = fmaxf(mx[c], x[u][c]); }
+      }
     }
-#pragma unroll
-    for (int u = 0; u < kRowsPerRound; ++u)
-#pragma unroll
-      for (int c = 0; c < C; ++c) { mn[c] = fminf(mn[c], x[u][c]); mx[c] = fmaxf(mx[c], x[u][c]); }
   }
 #pragma unroll
   for (int c = 0; c < C; ++c) { s_mn[warp][d0 + c] = mn[c]; s_mx[warp][d0 + c] = mx[c]; }
+  if (lane == 0) s_ok[warp] = ok ? 1 : 0;
   __syncthreads();
-  for (int d = threadIdx.x; d < D; d += kWarps * 32) {
-    float lo = s_mn[0][d], hi = s_mx[0][d];
-#pragma unroll
-    for (int w = 1; w < kWarps; ++w) { lo = fminf(lo, s_mn[w][d]); hi = fmaxf(hi, s_mx[w][d]); }
-    const int64_t o = (pair * kv.max_blocks + j) * D + d;
+  for (int idx = threadIdx.x; idx < per_cta * D; idx += kWarps * 32) {
+    const int bl = idx / D, d = idx - bl * D;
+    const int w0 = bl * wpb;
+    if (!s_ok[w0]) continue;
+    float lo = s_mn[w0][d], hi = s_mx[w0][d];
+    for (int w = 1; w < wpb; ++w) { lo = fminf(lo, s_mn[w0 + w][d]); hi = fmaxf(hi, s_mx[w0 + w][d]); }
+    const int64_t o = (pair * kv.max_blocks + first_block + blockIdx.x * per_cta + bl) * D + d;
     if constexpr (KIND == HS_KV_F32) {
       static_cast<float*>(smin)[o] = lo;
       static_cast<float*>(smax)[o] = hi;
@@ -128,7 +140,8 @@ __global__ __launch_bounds__(kWarps * 32) void summaries_kernel(KvView kv, int f
 template <int C>
 cudaError_t launch_c(const KvView& kv, int first_block, int nblocks, void* smin, void* smax,
                      unsigned* err, cudaStream_t st) {
-  dim3 grid(nblocks, kv.hkv, kv.batch);
+  const int per_cta = kWarps / warps_per_block(kv.block);
+  dim3 grid(ceil_div(nblocks, per_cta), kv.hkv, kv.batch);
   switch (kv.kv_dtype) {
     case HS_KV_F32:
       return launch_pdl(summaries_kernel<C, HS_KV_F32>, grid, dim3(kWarps * 32), 0, st, kv, first_block, smin, smax, err);
