@@ -95,15 +95,18 @@ int max_selected(const hs_attn_shape* s, int max_blocks, int sink, int window, i
   return static_cast<int>(m < max_blocks ? m : max_blocks);
 }
 
-// Split-K geometry: about two CTAs per SM over all (request, kv head) pairs,
-// each split a whole number of 128-token chunks where blocks are shorter.
+// Split-K geometry: how many selected blocks one CTA work item takes, a whole
+// number of 128-token chunks where blocks are shorter.
 void split_geometry(const hs_attn_shape* s, int batch, int capacity, const hs_attn_params* p,
                     int sms, int* bps_out, int* splits_out) {
   const int cap = capacity > 0 ? capacity : 1;
   int bps = p ? p->blocks_per_split : 0;
   if (bps <= 0) {
     const int64_t pairs = static_cast<int64_t>(batch) * s->num_kv_heads;
-    int64_t want = pairs > 0 ? (2LL * (sms > 0 ? sms : 148) + pairs - 1) / pairs : 1;
+    const int64_t n_sm = sms > 0 ? sms : 148;
+    // few (request, kv head) pairs: one wave of CTAs, each pair split evenly;
+    // many pairs: about two items per SM
+    int64_t want = pairs <= 0 ? 1 : (pairs <= n_sm ? n_sm / pairs : (2 * n_sm + pairs - 1) / pairs);
     if (want < 1) want = 1;
     if (want > cap) want = cap;
     bps = static_cast<int>((cap + want - 1) / want);

@@ -233,12 +233,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     fence_barrier_init();
   }
-  {
-    uint4 z = make_uint4(0, 0, 0, 0);
-    uint4* p = reinterpret_cast<uint4*>(smem);
-    for (int i = tid; i < Ly::kOffBar / 16; i += kThreads) p[i] = z;
-  }
-  fence_async_smem();
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(tmem_slot), Ly::kTmemCols);
     tmem_relinquish();
@@ -298,19 +292,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(empty_bar(s));
         return true;
       };
-      for (int item = blockIdx.x; item < a.items && !*abort_flag; item += gridDim.x) {
-        const Item it = item_geom(a, item, bpc);
-        if (it.nch == 0) continue;
-        if (!mbar_wait(q_full, qi & 1, abort_flag)) break;
-        ++qi;
-        tc_fence_after();
-        if (!gemm1(c)) break;
-        bool ok = true;
-        for (int ci = 0; ci < it.nch && ok; ++ci, ++c) {
-          if (ci + 1 < it.nch) ok = gemm1(c + 1);
-          if (ok) ok = gemm2(c);
+      int item = blockIdx.x;
+      Item it = item < a.items ? item_geom(a, item, bpc) : Item{};
+      while (item < a.items && !*abort_flag) {
+        const int next = item + gridDim.x;
+        const Item nit = next < a.items ? item_geom(a, next, bpc) : Item{};  // in flight meanwhile
+        if (it.nch > 0) {
+          if (!mbar_wait(q_full, qi & 1, abort_flag)) break;
+          ++qi;
+          tc_fence_after();
+          if (!gemm1(c)) break;
+          bool ok = true;
+          for (int ci = 0; ci < it.nch && ok; ++ci, ++c) {
+            if (ci + 1 < it.nch) ok = gemm1(c + 1);
+            if (ok) ok = gemm2(c);
+          }
+          if (!ok) break;
         }
-        if (!ok) break;
+        item = next;
+        it = nit;
       }
       // every commit has landed before TMEM is released
       for (int s = 0; s < kStages && s < c; ++s) {
@@ -324,27 +324,52 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     const int g = a.group;
     int c = 0;
-    for (int item = blockIdx.x; item < a.items && !*abort_flag; item += gridDim.x) {
-      const Item it = item_geom(a, item, bpc);
+    // thread t holds 16 bytes of each channel half of head row t/8 of the Q operand
+    auto load_q = [&](int item, uint4 (&v)[2]) {
+      const int pair = item / a.splits, b = pair / a.hkv, kvh = pair - b * a.hkv;
+      const int n = t >> 3, ch = t & 7;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        v[h] = make_uint4(0, 0, 0, 0);
+        if (n < g)
+          v[h] = *reinterpret_cast<const uint4*>(a.q + (static_cast<int64_t>(b) * a.hq + kvh * g + n) * kD + h * 64 +
+                                                 ch * 8);
+      }
+    };
+    int item = blockIdx.x;
+    Item it{};
+    uint4 qv[2];
+    if (item < a.items) {
+      it = item_geom(a, item, bpc);
+      load_q(item, qv);
+    }
+    for (; item < a.items && !*abort_flag;) {
+      // the next item's geometry and query rows are fetched while this one runs
+      const int next = item + gridDim.x;
+      Item nit{};
+      uint4 nqv[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+      if (next < a.items) {
+        nit = item_geom(a, next, bpc);
+        load_q(next, nqv);
+      }
       const int64_t row0 = (static_cast<int64_t>(it.b) * a.hq + it.kvh * g) * a.splits + it.split;
       if (it.nch == 0) {
         for (int h = 0; h < g; ++h) {
           a.ws_o[(row0 + static_cast<int64_t>(h) * a.splits) * kD + t] = 0.0f;
           if (t == 0) a.ws_lse[row0 + static_cast<int64_t>(h) * a.splits] = -INFINITY;
         }
+        item = next;
+        it = nit;
+        qv[0] = nqv[0];
+        qv[1] = nqv[1];
         continue;
       }
       // Q operand of this kv head: 16 rows (heads, zero past g) x 128 channels, 128-byte swizzle
       {
         const int n = t >> 3, ch = t & 7;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint4 v = make_uint4(0, 0, 0, 0);
-          if (n < g)
-            v = *reinterpret_cast<const uint4*>(a.q + (static_cast<int64_t>(it.b) * a.hq + it.kvh * g + n) * kD +
-                                                h * 64 + ch * 8);
-          *reinterpret_cast<uint4*>(smem + Ly::kOffQ + h * kQHalfBytes + n * 128 + ((ch ^ (n & 7)) << 4)) = v;
-        }
+        for (int h = 0; h < 2; ++h)
+          *reinterpret_cast<uint4*>(smem + Ly::kOffQ + h * kQHalfBytes + n * 128 + ((ch ^ (n & 7)) << 4)) = qv[h];
       }
       fence_async_smem();
       mbar_arrive(q_full);
@@ -380,8 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int bi = t / B, tok = t - bi * B;
         if (!mbar_wait(full_bar(s), (c / kStages) & 1, abort_flag)) { ok = false; break; }
         const int2 md = meta[s * 8 + bi];
-        const bool loaded = md.x >= 0;
-        const bool valid = loaded && tok < md.y;
+        const bool valid = md.x >= 0 && tok < md.y;
         if (!mbar_wait(s_full(bb), (c >> 1) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
         float sv[16];
@@ -432,9 +456,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 make_uint4(lo2[gi * 4], lo2[gi * 4 + 1], lo2[gi * 4 + 2], lo2[gi * 4 + 3]);
           }
         }
-        if (loaded && !valid) {
-          // rows past the request's end inside its last page: zero V so they
-          // contribute exactly nothing (P is 0 there, the stored bytes may not be finite)
+        if (!valid) {
+          // rows of no token (past the request's end inside its last page, or of
+          // no loaded block): zero V so they contribute exactly nothing - P is 0
+          // there but the bytes in shared memory need not be finite
           uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
@@ -464,6 +489,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (t == 0) a.ws_lse[row] = lt > 0.0f ? (m[h] + log2f(lt)) * kLn2 : -INFINITY;
       }
       named_barrier(1, 128);
+      item = next;
+      it = nit;
+      qv[0] = nqv[0];
+      qv[1] = nqv[1];
     }
   }
 
@@ -649,19 +678,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         last_g2 = cc;
         return true;
       };
-      for (int item = blockIdx.x; item < a.items && !*abort_flag; item += gridDim.x) {
-        const Item it = item_geom(a, item, bpc);
-        if (it.nch == 0) continue;
-        if (!mbar_wait(q_full, qi & 1, abort_flag)) break;
-        ++qi;
-        tc_fence_after();
-        if (!gemm1(c)) break;
-        bool ok = true;
-        for (int ci = 0; ci < it.nch && ok; ++ci, ++c) {
-          if (ci + 1 < it.nch) ok = gemm1(c + 1);
-          if (ok) ok = gemm2(c);
+      int item = blockIdx.x;
+      Item it = item < a.items ? item_geom(a, item, bpc) : Item{};
+      while (item < a.items && !*abort_flag) {
+        const int next = item + gridDim.x;
+        const Item nit = next < a.items ? item_geom(a, next, bpc) : Item{};
+        if (it.nch > 0) {
+          if (!mbar_wait(q_full, qi & 1, abort_flag)) break;
+          ++qi;
+          tc_fence_after();
+          if (!gemm1(c)) break;
+          bool ok = true;
+          for (int ci = 0; ci < it.nch && ok; ++ci, ++c) {
+            if (ci + 1 < it.nch) ok = gemm1(c + 1);
+            if (ok) ok = gemm2(c);
+          }
+          if (!ok) break;
         }
-        if (!ok) break;
+        item = next;
+        it = nit;
       }
       if (last_g2 >= 0) mbar_wait(o_full(last_g2 & 1), (last_g2 >> 1) & 1, abort_flag, 500000000ull);
     }
@@ -670,27 +705,55 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     const int g = a.group;
     int c = 0;
-    for (int item = blockIdx.x; item < a.items && !*abort_flag; item += gridDim.x) {
-      const Item it = item_geom(a, item, bpc);
+    // Q' operand: row (grp, h) holds head h's channels of group grp, zeros
+    // elsewhere; thread t owns four 16-byte pieces of it
+    auto load_q = [&](int item, uint4 (&v)[4]) {
+      const int pair = item / a.splits, b = pair / a.hkv, kvh = pair - b * a.hkv;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int idx = t * 4 + i;
+        const int half = idx >> 8, rem = idx & 255, row = rem >> 3, ch = rem & 7;
+        const int grp = row >> 3, h = row & 7;
+        v[i] = make_uint4(0, 0, 0, 0);
+        if (h < g && half * 2 + (ch >> 2) == grp)
+          v[i] = *reinterpret_cast<const uint4*>(a.q + (static_cast<int64_t>(b) * a.hq + kvh * g + h) * kD +
+                                                 half * 64 + ch * 8);
+      }
+    };
+    int item = blockIdx.x;
+    Item it{};
+    uint4 qv[4];
+    if (item < a.items) {
+      it = item_geom(a, item, bpc);
+      load_q(item, qv);
+    }
+    for (; item < a.items && !*abort_flag;) {
+      const int next = item + gridDim.x;
+      Item nit{};
+      uint4 nqv[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) nqv[i] = make_uint4(0, 0, 0, 0);
+      if (next < a.items) {
+        nit = item_geom(a, next, bpc);
+        load_q(next, nqv);
+      }
       const int64_t row0 = (static_cast<int64_t>(it.b) * a.hq + it.kvh * g) * a.splits + it.split;
       if (it.nch == 0) {
         for (int h = 0; h < g; ++h) {
           a.ws_o[(row0 + static_cast<int64_t>(h) * a.splits) * kD + t] = 0.0f;
           if (t == 0) a.ws_lse[row0 + static_cast<int64_t>(h) * a.splits] = -INFINITY;
         }
+        item = next;
+        it = nit;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) qv[i] = nqv[i];
         continue;
       }
-      // Q' operand: row (grp, h) holds head h's channels of group grp, zeros elsewhere
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int idx = t * 4 + i;
         const int half = idx >> 8, rem = idx & 255, row = rem >> 3, ch = rem & 7;
-        const int grp = row >> 3, h = row & 7;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (h < g && half * 2 + (ch >> 2) == grp)
-          v = *reinterpret_cast<const uint4*>(a.q + (static_cast<int64_t>(it.b) * a.hq + it.kvh * g + h) * kD +
-                                              half * 64 + ch * 8);
-        *reinterpret_cast<uint4*>(smem + Ly::kOffQ + half * Ly::kQHalf + row * 128 + ((ch ^ (row & 7)) << 4)) = v;
+        *reinterpret_cast<uint4*>(smem + Ly::kOffQ + half * Ly::kQHalf + row * 128 + ((ch ^ (row & 7)) << 4)) = qv[i];
       }
       fence_async_smem();
       mbar_arrive(q_full);
@@ -810,6 +873,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (t == 0) a.ws_lse[row] = lt > 0.0f ? (m[h] + log2f(lt)) * kLn2 : -INFINITY;
       }
       named_barrier(1, 128);
+      item = next;
+      it = nit;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) qv[i] = nqv[i];
     }
   }
 

@@ -81,10 +81,10 @@ __device__ __forceinline__ void load_summary(const void* base, int64_t off, floa
 }
 
 template <int C, int G, bool F32>
-__global__ void __cluster_dims__(kSelectCluster, 1, 1) __launch_bounds__(kThreads)
+__global__ void __cluster_dims__(kSelectCluster, 1, 1) __launch_bounds__(kThreads, (G * C <= 32) ? 2 : 1)
     score_select_kernel(KvView kv, SelectArgs a, unsigned* err) {
   extern __shared__ float s_scores[];  // [max_blocks]; rank 0's copy holds every score
-  __shared__ uint32_t s_hist[256];
+  __shared__ uint32_t s_hist[2][256];
   __shared__ int s_warp[kWarps + 1];
   __shared__ int s_pick[2];
 
@@ -127,7 +127,7 @@ __global__ void __cluster_dims__(kSelectCluster, 1, 1) __launch_bounds__(kThread
     // products of every lane are summed across the warp by a transpose
     // reduction (each round halves the values a lane holds), so a block costs
     // about 8 shuffles instead of 5 per head.
-    constexpr int kNB = (64 / G) < 8 ? (64 / G) : 8;
+    constexpr int kNB = (32 / G) < 4 ? ((32 / G) < 1 ? 1 : 32 / G) : 4;
     constexpr int kV = kNB * G;                    // partial sums per lane
     constexpr int kVPL = kV >= 32 ? kV / 32 : 1;   // values per lane after the reduction
     constexpr int kLPV = kV >= 32 ? 1 : 32 / kV;   // lanes holding one value
@@ -187,6 +187,7 @@ __global__ void __cluster_dims__(kSelectCluster, 1, 1) __launch_bounds__(kThread
       }
     }
   }
+  for (int i = tid; i < 512; i += kThreads) s_hist[i >> 8][i & 255] = 0u;
   cluster.sync();
   if (rank != 0) return;
 
@@ -196,82 +197,111 @@ __global__ void __cluster_dims__(kSelectCluster, 1, 1) __launch_bounds__(kThread
     const int lo = j * B, hi = min(lo + B, L);
     return lo < sink || (win > 0 && hi > L - win);
   };
-  int nf_local = 0;
-  for (int j = tid; j < nb; j += kThreads) nf_local += forced(j) ? 1 : 0;
-  int nf;
-  block_exclusive_scan(nf_local, s_warp, nf);
+  // forced blocks in closed form: [0, sink blocks) and [first window block, nb)
+  const int n_sink = min(nb, ceil_div(sink, B));
+  int w_first = nb;
+  if (win > 0) w_first = (L - win <= 0) ? 0 : min(nb, (L - win) / B);
+  const int nf = n_sink + max(0, nb - max(w_first, n_sink));
   const bool take_all = nf + k >= nb;
   const bool use_threshold = !take_all && k > 0;
+  int32_t* out = a.sel + pair * cap;
 
   uint32_t T = 0;
   int need_eq = 0;
   if (use_threshold) {
+    // 4-pass 8-bit radix select of the k-th largest key among non-forced blocks;
+    // two histogram buffers so that clearing the next one rides on this pass
     uint32_t prefix = 0, mask = 0;
     int kk = k;  // rank (1-based) of the wanted key among keys matching `prefix`
-    for (int shift = 24; shift >= 0; shift -= 8) {
-      for (int i = tid; i < 256; i += kThreads) s_hist[i] = 0;
-      __syncthreads();
+    int buf = 0;
+    for (int shift = 24; shift >= 0; shift -= 8, buf ^= 1) {
+      uint32_t* hist = s_hist[buf];
       for (int j = tid; j < nb; j += kThreads) {
         if (forced(j)) continue;
         const uint32_t key = score_key(s_scores[j]);
-        if ((key & mask) == prefix) atomicAdd(&s_hist[(key >> shift) & 255u], 1u);
+        if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
       }
       __syncthreads();
-      {
-        // thread t owns digit 255 - t: an inclusive scan from the top digit finds
-        // the bucket that holds the kk-th largest key
-        const int digit = 255 - tid;
-        const int h = static_cast<int>(s_hist[digit]);
-        int tot;
-        const int above = block_exclusive_scan(h, s_warp, tot);
-        if (above < kk && kk <= above + h) {
-          s_pick[0] = digit;
-          s_pick[1] = kk - above;
+      if (warp == 0) {
+        // lane l owns digits 255-8l .. 248-8l; a warp scan from the top digit
+        // finds the bucket holding the kk-th largest key
+        uint32_t hv[8];
+        int sum = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          hv[i] = hist[255 - 8 * lane - i];
+          sum += static_cast<int>(hv[i]);
         }
+        int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int n = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += n;
+        }
+        int above = incl - sum;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int h = static_cast<int>(hv[i]);
+          if (above < kk && kk <= above + h) {
+            s_pick[0] = 255 - 8 * lane - i;
+            s_pick[1] = kk - above;
+          }
+          above += h;
+        }
+        uint32_t* other = s_hist[buf ^ 1];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) other[8 * lane + i] = 0u;
       }
       __syncthreads();
       prefix |= static_cast<uint32_t>(s_pick[0]) << shift;
       mask |= 255u << shift;
       kk = s_pick[1];
-      __syncthreads();
     }
     T = prefix;
     need_eq = kk;
   }
 
-  // contiguous index range per thread keeps the output ascending
+  if (take_all) {
+    for (int j = tid; j < cap; j += kThreads) out[j] = j < nb ? j : -1;
+    if (tid == 0) {
+      if (nb > cap) set_error(err, HS_EBIT_CAPACITY);
+      a.sel_count[pair] = min(nb, cap);
+    }
+    return;
+  }
+  // contiguous index range per thread keeps the output ascending.  One packed
+  // scan gives, for every block, how many forced-or-above-threshold blocks and
+  // how many threshold-equal blocks precede it; an equal block is chosen while
+  // fewer than need_eq equal blocks precede it (lower index first).
   const int per_t = ceil_div(nb, kThreads);
   const int j0 = min(nb, tid * per_t), j1 = min(nb, j0 + per_t);
-  int eq_local = 0;
-  if (use_threshold)
-    for (int j = j0; j < j1; ++j)
-      if (!forced(j) && score_key(s_scores[j]) == T) ++eq_local;
-  int eq_total;
-  const int eq_base = block_exclusive_scan(eq_local, s_warp, eq_total);
-
-  auto chosen = [&](int j, int& eqr) -> bool {
-    if (take_all || forced(j)) return true;
-    if (!use_threshold) return false;
-    const uint32_t key = score_key(s_scores[j]);
-    if (key > T) return true;
-    if (key == T) return eqr++ < need_eq;
-    return false;
-  };
-  int cnt_local = 0;
-  {
-    int eqr = eq_base;
-    for (int j = j0; j < j1; ++j) cnt_local += chosen(j, eqr) ? 1 : 0;
+  int gt_local = 0, eq_local = 0;
+  for (int j = j0; j < j1; ++j) {
+    if (forced(j)) {
+      ++gt_local;
+    } else if (use_threshold) {
+      const uint32_t key = score_key(s_scores[j]);
+      gt_local += key > T;
+      eq_local += key == T;
+    }
   }
-  int total;
-  int pos = block_exclusive_scan(cnt_local, s_warp, total);
-  int32_t* out = a.sel + pair * cap;
-  {
-    int eqr = eq_base;
-    for (int j = j0; j < j1; ++j)
-      if (chosen(j, eqr)) {
-        if (pos < cap) out[pos] = j;
-        ++pos;
-      }
+  int packed_total;
+  const int packed = block_exclusive_scan((gt_local << 16) | eq_local, s_warp, packed_total);
+  int gt_b = packed >> 16, eq_b = packed & 0xffff;
+  const int total = (packed_total >> 16) + min(packed_total & 0xffff, need_eq);
+  for (int j = j0; j < j1; ++j) {
+    bool is_gt = forced(j), is_eq = false;
+    if (!is_gt && use_threshold) {
+      const uint32_t key = score_key(s_scores[j]);
+      is_gt = key > T;
+      is_eq = key == T;
+    }
+    if (is_gt || (is_eq && eq_b < need_eq)) {
+      const int pos = gt_b + min(eq_b, need_eq);  // chosen blocks before j
+      if (pos < cap) out[pos] = j;
+    }
+    gt_b += is_gt ? 1 : 0;
+    eq_b += is_eq ? 1 : 0;
   }
   for (int i = total + tid; i < cap; i += kThreads) out[i] = -1;
   if (tid == 0) {
