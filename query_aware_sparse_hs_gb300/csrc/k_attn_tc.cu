@@ -68,7 +68,7 @@ struct Layout {
   static constexpr int kNumBars = 2 * kStages + 11;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kOffRed = kOffMisc + 16;
-  static constexpr int kOffMeta = kOffRed + 4 * NH * 4;  // [stage][8] (page, valid tokens)
+  static constexpr int kOffMeta = kOffRed + 3 * 4 * NH * 4;  // red: [3][4 warps][NH]; meta: [stage][8] (page, valid tokens)
   static constexpr int kBytes = kOffMeta + kStages * 8 * 8;
   // the whole per-block maximum: one CTA per SM, and operand reads through a
   // descriptor can never leave this CTA's own shared memory
@@ -186,6 +186,49 @@ __device__ __forceinline__ void run_producer(const TcArgs& a, int bpc, uint32_t 
   }
 }
 
+
+// Issues GEMM1 and GEMM2 of chunks [c0, c0 + n) as soon as each one's inputs
+// are ready (non-blocking polls), so a TMA stage that lands late does not hold
+// back the P.V product of a chunk whose probabilities are already written.
+// Gives up (sets *abort) after 2 s without progress.
+template <typename R1, typename I1, typename R2, typename I2>
+__device__ __forceinline__ bool issue_chunks(int c0, int n, volatile int* abort_flag, R1 ready1, I1 issue1,
+                                             R2 ready2, I2 issue2) {
+  int g1 = c0, g2 = c0;
+  const int end = c0 + n;
+  uint64_t t0 = 0;
+  uint32_t idle = 0;
+  while (g2 < end) {
+    bool progress = false;
+    if (g1 < end && ready1(g1)) {
+      issue1(g1);
+      ++g1;
+      progress = true;
+    }
+    if (g2 < g1 && ready2(g2)) {
+      issue2(g2);
+      ++g2;
+      progress = true;
+    }
+    if (progress) {
+      idle = 0;
+      t0 = 0;
+    } else {
+      if (*abort_flag) return false;
+      if ((++idle & 255u) == 0) {
+        const uint64_t now = globaltimer_ns();
+        if (t0 == 0) {
+          t0 = now;
+        } else if (now - t0 > 2000000000ull) {
+          *abort_flag = 1;
+          return false;
+        }
+      }
+    }
+  }
+  return true;
+}
+
 template <int NH>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -262,10 +305,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc2 = idesc_bf16(128, 2 * NH, true, true);
       constexpr uint32_t kPLbo = 8 * 2 * NH * 2;  // bytes between 8-token groups of P
       int c = 0, qi = 0;
-      auto gemm1 = [&](int cc) -> bool {
+      auto ready1 = [&](int cc) -> bool {
+        return mbar_try(full_bar(cc % kStages), (cc / kStages) & 1) &&
+               (cc < 2 || mbar_try(s_free(cc & 1), ((cc >> 1) + 1) & 1));
+      };
+      auto gemm1 = [&](int cc) {
         const int s = cc % kStages, bb = cc & 1;
-        if (!mbar_wait(full_bar(s), (cc / kStages) & 1, abort_flag)) return false;
-        if (cc >= 2 && !mbar_wait(s_free(bb), ((cc >> 1) + 1) & 1, abort_flag)) return false;
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < kD / 16; ++k) {
@@ -275,12 +320,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_f16(tmem + bb * 16, ad, bd, idesc1, k > 0 ? 1u : 0u);
         }
         mma_commit(s_full(bb));
-        return true;
       };
-      auto gemm2 = [&](int cc) -> bool {
+      auto ready2 = [&](int cc) -> bool {
+        return mbar_try(p_full(cc & 1), (cc >> 1) & 1) && (cc < 2 || mbar_try(o_free(cc & 1), ((cc >> 1) + 1) & 1));
+      };
+      auto gemm2 = [&](int cc) {
         const int s = cc % kStages, bb = cc & 1;
-        if (!mbar_wait(p_full(bb), (cc >> 1) & 1, abort_flag)) return false;
-        if (cc >= 2 && !mbar_wait(o_free(bb), ((cc >> 1) + 1) & 1, abort_flag)) return false;
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < kChunk / 16; ++k) {
@@ -290,7 +335,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(o_full(bb));
         mma_commit(empty_bar(s));
-        return true;
       };
       int item = blockIdx.x;
       Item it = item < a.items ? item_geom(a, item, bpc) : Item{};
@@ -300,14 +344,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (it.nch > 0) {
           if (!mbar_wait(q_full, qi & 1, abort_flag)) break;
           ++qi;
-          tc_fence_after();
-          if (!gemm1(c)) break;
-          bool ok = true;
-          for (int ci = 0; ci < it.nch && ok; ++ci, ++c) {
-            if (ci + 1 < it.nch) ok = gemm1(c + 1);
-            if (ok) ok = gemm2(c);
-          }
-          if (!ok) break;
+          if (!issue_chunks(c, it.nch, abort_flag, ready1, gemm1, ready2, gemm2)) break;
+          c += it.nch;
         }
         item = next;
         it = nit;
@@ -419,18 +457,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int h = 0; h < NH; ++h) {
           const float mx = warp_max(x[h]);
-          if (lane == 0) red[warp * NH + h] = mx;
+          if (lane == 0) red[(c & 1) * 4 * NH + warp * NH + h] = mx;
         }
         named_barrier(1, 128);
+        const float* rb = red + (c & 1) * 4 * NH;  // alternate buffers: one barrier per chunk
         float alpha[NH];
 #pragma unroll
         for (int h = 0; h < NH; ++h) {
-          const float cm = fmaxf(fmaxf(red[h], red[NH + h]), fmaxf(red[2 * NH + h], red[3 * NH + h]));
+          const float cm = fmaxf(fmaxf(rb[h], rb[NH + h]), fmaxf(rb[2 * NH + h], rb[3 * NH + h]));
           const float mn = fmaxf(m[h], cm);
           alpha[h] = (mn == -INFINITY) ? 1.0f : exp2f(m[h] - mn);
           m[h] = mn;
         }
-        named_barrier(1, 128);
         // probabilities, split into bf16 high part + bf16 remainder
         uint32_t hi2[NH / 2], lo2[NH / 2];
 #pragma unroll
@@ -479,11 +517,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int h = 0; h < NH; ++h) {
         const float s_ = warp_sum(lsum[h]);
-        if (lane == 0) red[warp * NH + h] = s_;
+        if (lane == 0) red[8 * NH + warp * NH + h] = s_;
       }
       named_barrier(1, 128);
+      const float* rs = red + 8 * NH;
       for (int h = 0; h < g && h < NH; ++h) {
-        const float lt = red[h] + red[NH + h] + red[2 * NH + h] + red[3 * NH + h];
+        const float lt = rs[h] + rs[NH + h] + rs[2 * NH + h] + rs[3 * NH + h];
         const int64_t row = row0 + static_cast<int64_t>(h) * a.splits;
         a.ws_o[row * kD + t] = lt > 0.0f ? oacc[h] / lt : 0.0f;
         if (t == 0) a.ws_lse[row] = lt > 0.0f ? (m[h] + log2f(lt)) * kLn2 : -INFINITY;
@@ -537,7 +576,7 @@ struct Layout8 {
   static constexpr int kNumBars = 2 * kStages8 + 12;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kOffRed = kOffMisc + 16;
-  static constexpr int kOffMeta = kOffRed + 4 * 8 * 4;
+  static constexpr int kOffMeta = kOffRed + 3 * 4 * 8 * 4;
   static constexpr int kBytes = kOffMeta + kStages8 * 8 * 8;
   static constexpr int kAlloc = 232448;
   static_assert(kBytes + 1024 <= kAlloc, "shared memory layout too large");
@@ -648,10 +687,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t kbf = sbase + Ly::kOffKbf, vbf = sbase + Ly::kOffVbf;
       const uint32_t qb = sbase + Ly::kOffQ, pb = sbase + Ly::kOffP;
       int c = 0, qi = 0, last_g2 = -1;
-      auto gemm1 = [&](int cc) -> bool {
+      auto ready1 = [&](int cc) -> bool {
+        return mbar_try(kconv_full, cc & 1) && (cc < 2 || mbar_try(s_free(cc & 1), ((cc >> 1) + 1) & 1));
+      };
+      auto gemm1 = [&](int cc) {
         const int bb = cc & 1;
-        if (!mbar_wait(kconv_full, cc & 1, abort_flag)) return false;
-        if (cc >= 2 && !mbar_wait(s_free(bb), ((cc >> 1) + 1) & 1, abort_flag)) return false;
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < kD / 16; ++k) {
@@ -661,12 +701,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_f16(tmem + bb * 32, ad, bd, idesc1, k > 0 ? 1u : 0u);
         }
         mma_commit(s_full(bb));
-        return true;
       };
-      auto gemm2 = [&](int cc) -> bool {
+      auto ready2 = [&](int cc) -> bool {
+        return mbar_try(p_full(cc & 1), (cc >> 1) & 1) && (cc < 2 || mbar_try(o_free(cc & 1), ((cc >> 1) + 1) & 1));
+      };
+      auto gemm2 = [&](int cc) {
         const int bb = cc & 1;
-        if (!mbar_wait(p_full(bb), (cc >> 1) & 1, abort_flag)) return false;
-        if (cc >= 2 && !mbar_wait(o_free(bb), ((cc >> 1) + 1) & 1, abort_flag)) return false;
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < kChunk / 16; ++k) {
@@ -676,7 +716,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(o_full(bb));
         last_g2 = cc;
-        return true;
       };
       int item = blockIdx.x;
       Item it = item < a.items ? item_geom(a, item, bpc) : Item{};
@@ -686,14 +725,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (it.nch > 0) {
           if (!mbar_wait(q_full, qi & 1, abort_flag)) break;
           ++qi;
-          tc_fence_after();
-          if (!gemm1(c)) break;
-          bool ok = true;
-          for (int ci = 0; ci < it.nch && ok; ++ci, ++c) {
-            if (ci + 1 < it.nch) ok = gemm1(c + 1);
-            if (ok) ok = gemm2(c);
-          }
-          if (!ok) break;
+          if (!issue_chunks(c, it.nch, abort_flag, ready1, gemm1, ready2, gemm2)) break;
+          c += it.nch;
         }
         item = next;
         it = nit;
@@ -818,20 +851,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int h = 0; h < NH; ++h) {
           const float mx = warp_max(x[h]);
-          if (lane == 0) red[warp * NH + h] = mx;
+          if (lane == 0) red[(c & 1) * 4 * NH + warp * NH + h] = mx;
         }
         named_barrier(1, 128);
+        const float* rb = red + (c & 1) * 4 * NH;  // alternate buffers: one barrier per chunk
         float alpha[NH], p[NH];
 #pragma unroll
         for (int h = 0; h < NH; ++h) {
-          const float cm = fmaxf(fmaxf(red[h], red[NH + h]), fmaxf(red[2 * NH + h], red[3 * NH + h]));
+          const float cm = fmaxf(fmaxf(rb[h], rb[NH + h]), fmaxf(rb[2 * NH + h], rb[3 * NH + h]));
           const float mn = fmaxf(m[h], cm);
           alpha[h] = (mn == -INFINITY) ? 1.0f : exp2f(m[h] - mn);
           m[h] = mn;
           p[h] = x[h] == -INFINITY ? 0.0f : exp2f(x[h] - mn);
           lsum[h] = fmaf(lsum[h], alpha[h], p[h]);
         }
-        named_barrier(1, 128);
         if (ci > 0 && !take_o(c - 1)) { ok = false; break; }
         // V tile of this chunk (GEMM2 of the previous chunk is done with it)
         convert_row(vc_stage(s) + t * 128, smem + Ly::kOffVbf, t, valid_cur);
@@ -863,11 +896,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int h = 0; h < NH; ++h) {
         const float s_ = warp_sum(lsum[h]);
-        if (lane == 0) red[warp * NH + h] = s_;
+        if (lane == 0) red[8 * NH + warp * NH + h] = s_;
       }
       named_barrier(1, 128);
+      const float* rs = red + 8 * NH;
       for (int h = 0; h < g && h < NH; ++h) {
-        const float lt = red[h] + red[NH + h] + red[2 * NH + h] + red[3 * NH + h];
+        const float lt = rs[h] + rs[NH + h] + rs[2 * NH + h] + rs[3 * NH + h];
         const int64_t row = row0 + static_cast<int64_t>(h) * a.splits;
         a.ws_o[row * kD + t] = lt > 0.0f ? oacc[h] / lt : 0.0f;
         if (t == 0) a.ws_lse[row] = lt > 0.0f ? (m[h] + log2f(lt)) * kLn2 : -INFINITY;
