@@ -117,63 +117,90 @@ __device__ __forceinline__ int resolve(const TcArgs& a, const Item& it, int pos,
 }
 
 
-// The (item, chunk) sequence every role of a CTA walks, skipping empty items.
-struct Cursor {
-  int item, ci;
-  Item it;
-};
-
-__device__ __forceinline__ bool cursor_seek(const TcArgs& a, int bpc, Cursor& c) {
-  for (; c.item < a.items; c.item += gridDim.x) {
-    c.it = item_geom(a, c.item, bpc);
-    if (c.it.nch > 0) {
-      c.ci = 0;
-      return true;
-    }
+// First item at or after `item` (stepping by the grid) that has chunks; a.items if none.
+__device__ __forceinline__ int find_item(const TcArgs& a, int bpc, int item, Item* it) {
+  for (; item < a.items; item += gridDim.x) {
+    *it = item_geom(a, item, bpc);
+    if (it->nch > 0) break;
   }
-  return false;
-}
-__device__ __forceinline__ bool cursor_first(const TcArgs& a, int bpc, Cursor& c) {
-  c.item = blockIdx.x;
-  return cursor_seek(a, bpc, c);
-}
-__device__ __forceinline__ bool cursor_next(const TcArgs& a, int bpc, Cursor& c) {
-  if (++c.ci < c.it.nch) return true;
-  c.item += gridDim.x;
-  return cursor_seek(a, bpc, c);
+  return item;
 }
 
-// TMA producer warp (all 32 lanes).  Lane i resolves block i of a chunk (its
-// selected index and physical page) one chunk ahead, so the dependent lookups
-// overlap the wait for a free stage; the chunk's pages and valid-token counts
-// are published in meta[stage][8] for the softmax warps, and each lane issues
-// the copies of its own block.
+// Lane's block of the group of 32 selected positions starting at `gbase`:
+// (page, valid tokens), page -1 past the item or for a bad entry.  The
+// selection entry is read without waiting for the item's count.
+__device__ __forceinline__ int2 resolve_group(const TcArgs& a, const Item& it, int gbase, unsigned* bad) {
+  const int lane = threadIdx.x & 31;
+  const int pos = it.s0 + gbase + lane;
+  const int64_t row = static_cast<int64_t>(it.pair) * a.capacity;
+  const int j = pos < a.capacity ? a.sel[row + pos] : -1;
+  if (pos >= it.s1) return make_int2(-1, 0);
+  if (j < 0 || j >= it.nb) {
+    *bad |= HS_EBIT_BLOCK_RANGE;
+    return make_int2(-1, 0);
+  }
+  const int page = a.page_table[static_cast<int64_t>(it.pair) * a.max_blocks + j];
+  if (page < 0 || page >= a.num_pages) {
+    *bad |= HS_EBIT_PAGE_RANGE;
+    return make_int2(-1, 0);
+  }
+  return make_int2(page, min(a.block, it.L - j * a.block));
+}
+
+// TMA producer warp (all 32 lanes).  An item's selected blocks are resolved 32
+// at a time (lane i: block i of the group) and the next group - of this item or
+// of the next one - is looked up while the current group's chunks are issued,
+// so page-table lookups stay off the copy stream.  Each chunk's pages and
+// valid-token counts are published in meta[stage][8] for the softmax warps and
+// every lane issues the copies of its own block.
 template <int STAGES, typename IssueFn>
 __device__ __forceinline__ void run_producer(const TcArgs& a, int bpc, uint32_t full0, uint32_t empty0,
                                              int2* meta, uint32_t bytes_per_block, volatile int* abort_flag,
                                              unsigned* err, IssueFn issue) {
   const int lane = threadIdx.x & 31;
   unsigned bad = 0;
-  Cursor cur;
-  bool have = cursor_first(a, bpc, cur);
-  int page = -1, vt = 0;
-  if (have && lane < bpc) page = resolve(a, cur.it, cur.it.s0 + cur.ci * bpc + lane, &vt, &bad);
+  Item it;
+  int item = find_item(a, bpc, blockIdx.x, &it);
+  int2 cur = item < a.items ? resolve_group(a, it, 0, &bad) : make_int2(-1, 0);
   int c = 0;
-  for (;; ++c) {
-    int go = 0;
-    if (lane == 0) go = have && !*abort_flag && (c < STAGES || mbar_wait(empty0 + 8 * (c % STAGES), ((c / STAGES) + 1) & 1, abort_flag));
-    if (!__shfl_sync(0xffffffffu, go, 0)) break;
-    const int s = c % STAGES;
-    if (lane < 8) meta[s * 8 + lane] = make_int2(page, vt);
-    const uint32_t tx = __reduce_add_sync(0xffffffffu, page >= 0 ? bytes_per_block : 0u);
-    __syncwarp();
-    if (lane == 0) mbar_arrive_tx(full0 + 8 * s, tx);
-    __syncwarp();
-    if (page >= 0) issue(s, lane, page);
-    have = cursor_next(a, bpc, cur);
-    page = -1;
-    vt = 0;
-    if (have && lane < bpc) page = resolve(a, cur.it, cur.it.s0 + cur.ci * bpc + lane, &vt, &bad);
+  bool stop = false;
+  while (item < a.items && !stop) {
+    const int nblk = it.s1 - it.s0;
+    const int ngroups = (nblk + 31) / 32;
+    int next_item = item;
+    Item nit = it;
+    for (int g = 0; g < ngroups && !stop; ++g) {
+      int2 nxt = make_int2(-1, 0);
+      if (g + 1 < ngroups) {
+        nxt = resolve_group(a, it, (g + 1) * 32, &bad);
+      } else {
+        next_item = find_item(a, bpc, item + gridDim.x, &nit);
+        if (next_item < a.items) nxt = resolve_group(a, nit, 0, &bad);
+      }
+      const int gchunks = min(32 / bpc, (nblk - g * 32 + bpc - 1) / bpc);
+      for (int k = 0; k < gchunks; ++k, ++c) {
+        int go = 0;
+        if (lane == 0)
+          go = !*abort_flag &&
+               (c < STAGES || mbar_wait(empty0 + 8 * (c % STAGES), ((c / STAGES) + 1) & 1, abort_flag));
+        if (!__shfl_sync(0xffffffffu, go, 0)) {
+          stop = true;
+          break;
+        }
+        const int s = c % STAGES;
+        const int bi = lane - k * bpc;
+        const bool mine = bi >= 0 && bi < bpc;
+        if (mine) meta[s * 8 + bi] = cur;
+        const uint32_t tx = __reduce_add_sync(0xffffffffu, (mine && cur.x >= 0) ? bytes_per_block : 0u);
+        __syncwarp();
+        if (lane == 0) mbar_arrive_tx(full0 + 8 * s, tx);
+        __syncwarp();
+        if (mine && cur.x >= 0) issue(s, bi, cur.x);
+      }
+      cur = nxt;
+    }
+    item = next_item;
+    it = nit;
   }
   bad = __reduce_or_sync(0xffffffffu, bad);
   if (lane == 0) {
@@ -185,7 +212,6 @@ __device__ __forceinline__ void run_producer(const TcArgs& a, int bpc, uint32_t 
     }
   }
 }
-
 
 // Issues GEMM1 and GEMM2 of chunks [c0, c0 + n) as soon as each one's inputs
 // are ready (non-blocking polls), so a TMA stage that lands late does not hold
@@ -306,8 +332,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kPLbo = 8 * 2 * NH * 2;  // bytes between 8-token groups of P
       int c = 0, qi = 0;
       auto ready1 = [&](int cc) -> bool {
-        return mbar_try(full_bar(cc % kStages), (cc / kStages) & 1) &&
-               (cc < 2 || mbar_try(s_free(cc & 1), ((cc >> 1) + 1) & 1));
+        return mbar_test(full_bar(cc % kStages), (cc / kStages) & 1) &&
+               (cc < 2 || mbar_test(s_free(cc & 1), ((cc >> 1) + 1) & 1));
       };
       auto gemm1 = [&](int cc) {
         const int s = cc % kStages, bb = cc & 1;
@@ -322,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(s_full(bb));
       };
       auto ready2 = [&](int cc) -> bool {
-        return mbar_try(p_full(cc & 1), (cc >> 1) & 1) && (cc < 2 || mbar_try(o_free(cc & 1), ((cc >> 1) + 1) & 1));
+        return mbar_test(p_full(cc & 1), (cc >> 1) & 1) && (cc < 2 || mbar_test(o_free(cc & 1), ((cc >> 1) + 1) & 1));
       };
       auto gemm2 = [&](int cc) {
         const int s = cc % kStages, bb = cc & 1;
@@ -512,8 +538,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int h = 0; h < NH; ++h) alpha_prev[h] = alpha[h];
       }
-      if (!ok || !take_o(c - 1)) break;
-      // total normaliser per head
+      if (!ok) break;
+      // the normaliser reduction overlaps the last P.V product
 #pragma unroll
       for (int h = 0; h < NH; ++h) {
         const float s_ = warp_sum(lsum[h]);
@@ -521,6 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       named_barrier(1, 128);
       const float* rs = red + 8 * NH;
+      if (!take_o(c - 1)) break;
       for (int h = 0; h < g && h < NH; ++h) {
         const float lt = rs[h] + rs[NH + h] + rs[2 * NH + h] + rs[3 * NH + h];
         const int64_t row = row0 + static_cast<int64_t>(h) * a.splits;
@@ -688,7 +715,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t qb = sbase + Ly::kOffQ, pb = sbase + Ly::kOffP;
       int c = 0, qi = 0, last_g2 = -1;
       auto ready1 = [&](int cc) -> bool {
-        return mbar_try(kconv_full, cc & 1) && (cc < 2 || mbar_try(s_free(cc & 1), ((cc >> 1) + 1) & 1));
+        return mbar_test(kconv_full, cc & 1) && (cc < 2 || mbar_test(s_free(cc & 1), ((cc >> 1) + 1) & 1));
       };
       auto gemm1 = [&](int cc) {
         const int bb = cc & 1;
@@ -703,7 +730,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(s_full(bb));
       };
       auto ready2 = [&](int cc) -> bool {
-        return mbar_try(p_full(cc & 1), (cc >> 1) & 1) && (cc < 2 || mbar_try(o_free(cc & 1), ((cc >> 1) + 1) & 1));
+        return mbar_test(p_full(cc & 1), (cc >> 1) & 1) && (cc < 2 || mbar_test(o_free(cc & 1), ((cc >> 1) + 1) & 1));
       };
       auto gemm2 = [&](int cc) {
         const int bb = cc & 1;
@@ -892,7 +919,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int h = 0; h < NH; ++h) alpha_prev[h] = alpha[h];
       }
-      if (!ok || !take_o(c - 1)) break;
+      if (!ok) break;
+      // the normaliser reduction overlaps the last P.V product
 #pragma unroll
       for (int h = 0; h < NH; ++h) {
         const float s_ = warp_sum(lsum[h]);
@@ -900,6 +928,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       named_barrier(1, 128);
       const float* rs = red + 8 * NH;
+      if (!take_o(c - 1)) break;
       for (int h = 0; h < g && h < NH; ++h) {
         const float lt = rs[h] + rs[NH + h] + rs[2 * NH + h] + rs[3 * NH + h];
         const int64_t row = row0 + static_cast<int64_t>(h) * a.splits;
