@@ -13,8 +13,8 @@
 //   warp 4      TMA producer: cp.async.bulk.tensor of each selected page's K
 //               and V rows (two 64-channel halves, 128-byte swizzle) into a
 //               3-stage ring, completion tracked by mbarrier transaction bytes.
-//   warp 5      MMA issuer (one thread): GEMM1 of chunk c+1 is issued before
-//               GEMM2 of chunk c; TMEM double-buffers S and O.
+//   warps 5, 6  MMA issuers (one thread each): warp 5 issues S = K.Q^T, warp 6
+//               O = V^T.P; TMEM double-buffers S and O.
 //   warps 0-3   softmax / correction: thread t owns TMEM lane t = token t of
 //               the chunk for S, and channel t for O; running max and sum per
 //               head, P written to shared memory for GEMM2, O accumulated in
@@ -34,9 +34,10 @@ using namespace tc;
 constexpr int kD = 128;
 constexpr int kChunk = 128;
 constexpr int kStages = 3;
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;
 constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
+constexpr int kMmaWarp = 5;   // S = K.Q^T issuer (and TMEM owner)
+constexpr int kMma2Warp = 6;  // O = V^T.P issuer
 constexpr int kHalfBytes = kChunk * 128;   // 128 rows x 64 bf16
 constexpr int kTileBytes = 2 * kHalfBytes;  // one K or V chunk
 constexpr int kStageBytes = 2 * kTileBytes;
@@ -98,24 +99,6 @@ __device__ __forceinline__ Item item_geom(const TcArgs& a, int item, int bpc) {
   it.nb = min((max(it.L, 0) + a.block - 1) / a.block, a.max_blocks);
   return it;
 }
-
-// physical page of selected position `pos` of the item, or -1; *vt = valid tokens
-__device__ __forceinline__ int resolve(const TcArgs& a, const Item& it, int pos, int* vt, unsigned* bad) {
-  if (pos >= it.s1) return -1;
-  const int j = a.sel[static_cast<int64_t>(it.pair) * a.capacity + pos];
-  if (j < 0 || j >= it.nb) {
-    *bad |= HS_EBIT_BLOCK_RANGE;
-    return -1;
-  }
-  const int page = a.page_table[static_cast<int64_t>(it.pair) * a.max_blocks + j];
-  if (page < 0 || page >= a.num_pages) {
-    *bad |= HS_EBIT_PAGE_RANGE;
-    return -1;
-  }
-  *vt = min(a.block, it.L - j * a.block);
-  return page;
-}
-
 
 // First item at or after `item` (stepping by the grid) that has chunks; a.items if none.
 __device__ __forceinline__ int find_item(const TcArgs& a, int bpc, int item, Item* it) {
@@ -213,48 +196,6 @@ __device__ __forceinline__ void run_producer(const TcArgs& a, int bpc, uint32_t 
   }
 }
 
-// Issues GEMM1 and GEMM2 of chunks [c0, c0 + n) as soon as each one's inputs
-// are ready (non-blocking polls), so a TMA stage that lands late does not hold
-// back the P.V product of a chunk whose probabilities are already written.
-// Gives up (sets *abort) after 2 s without progress.
-template <typename R1, typename I1, typename R2, typename I2>
-__device__ __forceinline__ bool issue_chunks(int c0, int n, volatile int* abort_flag, R1 ready1, I1 issue1,
-                                             R2 ready2, I2 issue2) {
-  int g1 = c0, g2 = c0;
-  const int end = c0 + n;
-  uint64_t t0 = 0;
-  uint32_t idle = 0;
-  while (g2 < end) {
-    bool progress = false;
-    if (g1 < end && ready1(g1)) {
-      issue1(g1);
-      ++g1;
-      progress = true;
-    }
-    if (g2 < g1 && ready2(g2)) {
-      issue2(g2);
-      ++g2;
-      progress = true;
-    }
-    if (progress) {
-      idle = 0;
-      t0 = 0;
-    } else {
-      if (*abort_flag) return false;
-      if ((++idle & 255u) == 0) {
-        const uint64_t now = globaltimer_ns();
-        if (t0 == 0) {
-          t0 = now;
-        } else if (now - t0 > 2000000000ull) {
-          *abort_flag = 1;
-          return false;
-        }
-      }
-    }
-  }
-  return true;
-}
-
 template <int NH>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -324,62 +265,69 @@ __global__ void __launch_bounds__(kThreads, 1)
                             tma_load_2d(v_half(s, 0) + row_off, &tm_v, 0, y, full_bar(s));
                             tma_load_2d(v_half(s, 1) + row_off, &tm_v, 64, y, full_bar(s));
                           });
-  } else if (warp == kMmaWarp) {
-    // ================= MMA issuer =================
+  } else if (warp == kMmaWarp || warp == kMma2Warp) {
+    // ================= MMA issuers: one thread for S = K.Q^T, one for O = V^T.P =================
+    // (issuing a GEMM's 8 tcgen05.mma takes a few hundred ns, so the two GEMMs
+    // of a chunk are issued from two threads instead of one after the other)
     if (lane == 0) {
+      const bool first = warp == kMmaWarp;
       constexpr uint32_t idesc1 = idesc_bf16(128, 16, false, false);
       constexpr uint32_t idesc2 = idesc_bf16(128, 2 * NH, true, true);
       constexpr uint32_t kPLbo = 8 * 2 * NH * 2;  // bytes between 8-token groups of P
+      const uint64_t kdesc = smem_desc(k_half(0, 0), 16, 1024, 2);
+      const uint64_t qdesc = smem_desc(q_half(0), 16, 1024, 2);
+      const uint64_t vdesc = smem_desc(v_half(0, 0), kHalfBytes, 1024, 2);
+      const uint64_t pdesc = smem_desc(p_buf(0), kPLbo, 128, 0);
       int c = 0, qi = 0;
-      auto ready1 = [&](int cc) -> bool {
-        return mbar_test(full_bar(cc % kStages), (cc / kStages) & 1) &&
-               (cc < 2 || mbar_test(s_free(cc & 1), ((cc >> 1) + 1) & 1));
-      };
-      auto gemm1 = [&](int cc) {
-        const int s = cc % kStages, bb = cc & 1;
-        tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < kD / 16; ++k) {
-          const int h = k >> 2, kk = k & 3;
-          const uint64_t ad = smem_desc(k_half(s, h) + kk * 32, 16, 1024, 2);
-          const uint64_t bd = smem_desc(q_half(h) + kk * 32, 16, 1024, 2);
-          mma_f16(tmem + bb * 16, ad, bd, idesc1, k > 0 ? 1u : 0u);
-        }
-        mma_commit(s_full(bb));
-      };
-      auto ready2 = [&](int cc) -> bool {
-        return mbar_test(p_full(cc & 1), (cc >> 1) & 1) && (cc < 2 || mbar_test(o_free(cc & 1), ((cc >> 1) + 1) & 1));
-      };
-      auto gemm2 = [&](int cc) {
-        const int s = cc % kStages, bb = cc & 1;
-        tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < kChunk / 16; ++k) {
-          const uint64_t ad = smem_desc(v_half(s, 0) + k * 2048, kHalfBytes, 1024, 2);
-          const uint64_t bd = smem_desc(p_buf(bb) + k * 2 * kPLbo, kPLbo, 128, 0);
-          mma_f16(tmem + Ly::kColO + bb * 2 * NH, ad, bd, idesc2, k > 0 ? 1u : 0u);
-        }
-        mma_commit(o_full(bb));
-        mma_commit(empty_bar(s));
-      };
       int item = blockIdx.x;
       Item it = item < a.items ? item_geom(a, item, bpc) : Item{};
-      while (item < a.items && !*abort_flag) {
+      bool ok = true;
+      while (ok && item < a.items && !*abort_flag) {
         const int next = item + gridDim.x;
         const Item nit = next < a.items ? item_geom(a, next, bpc) : Item{};  // in flight meanwhile
-        if (it.nch > 0) {
-          if (!mbar_wait(q_full, qi & 1, abort_flag)) break;
+        if (it.nch > 0 && first) {
+          ok = mbar_wait(q_full, qi & 1, abort_flag);
           ++qi;
-          if (!issue_chunks(c, it.nch, abort_flag, ready1, gemm1, ready2, gemm2)) break;
-          c += it.nch;
+        }
+        for (int ci = 0; ok && ci < it.nch; ++ci, ++c) {
+          const int st = c % kStages, bb = c & 1;
+          if (first) {
+            ok = mbar_wait(full_bar(st), (c / kStages) & 1, abort_flag) &&
+                 (c < 2 || mbar_wait(s_free(bb), ((c >> 1) + 1) & 1, abort_flag));
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll
+            for (int k = 0; k < kD / 16; ++k) {
+              const uint32_t koff = st * kStageBytes + (k >> 2) * kHalfBytes + (k & 3) * 32;
+              const uint32_t qoff = (k >> 2) * kQHalfBytes + (k & 3) * 32;
+              mma_f16(tmem + bb * 16, kdesc + (koff >> 4), qdesc + (qoff >> 4), idesc1, k > 0 ? 1u : 0u);
+            }
+            mma_commit(s_full(bb));
+          } else {
+            ok = mbar_wait(p_full(bb), (c >> 1) & 1, abort_flag) &&
+                 (c < 2 || mbar_wait(o_free(bb), ((c >> 1) + 1) & 1, abort_flag));
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll
+            for (int k = 0; k < kChunk / 16; ++k) {
+              const uint32_t voff = st * kStageBytes + k * 2048;
+              const uint32_t poff = bb * Ly::kPBytes + k * 2 * kPLbo;
+              mma_f16(tmem + Ly::kColO + bb * 2 * NH, vdesc + (voff >> 4), pdesc + (poff >> 4), idesc2,
+                      k > 0 ? 1u : 0u);
+            }
+            mma_commit(o_full(bb));
+            mma_commit(empty_bar(st));
+          }
         }
         item = next;
         it = nit;
       }
-      // every commit has landed before TMEM is released
-      for (int s = 0; s < kStages && s < c; ++s) {
-        const int last = c - 1 - ((c - 1 - s) % kStages);
-        mbar_wait(empty_bar(s), (last / kStages) & 1, abort_flag, 500000000ull);
+      if (!first) {
+        // every commit has landed before TMEM is released
+        for (int st = 0; st < kStages && st < c; ++st) {
+          const int last = c - 1 - ((c - 1 - st) % kStages);
+          mbar_wait(empty_bar(st), (last / kStages) & 1, abort_flag, 500000000ull);
+        }
       }
     }
   } else {
@@ -707,58 +655,59 @@ __global__ void __launch_bounds__(kThreads, 1)
                              bulk_load(smem_u32(vs_stage(s)) + bi * B * 16, a.v_scales + static_cast<int64_t>(y) * 4,
                                        B * 16, full_bar(s));
                            });
-  } else if (warp == kMmaWarp) {
+  } else if (warp == kMmaWarp || warp == kMma2Warp) {
     if (lane == 0) {
+      const bool first = warp == kMmaWarp;
       constexpr uint32_t idesc1 = idesc_bf16(128, 32, false, false);
       constexpr uint32_t idesc2 = idesc_bf16(128, 64, true, true);
-      const uint32_t kbf = sbase + Ly::kOffKbf, vbf = sbase + Ly::kOffVbf;
-      const uint32_t qb = sbase + Ly::kOffQ, pb = sbase + Ly::kOffP;
+      const uint64_t kdesc = smem_desc(sbase + Ly::kOffKbf, 16, 1024, 2);
+      const uint64_t qdesc = smem_desc(sbase + Ly::kOffQ, 16, 1024, 2);
+      const uint64_t vdesc = smem_desc(sbase + Ly::kOffVbf, kHalfBytes, 1024, 2);
+      const uint64_t pdesc = smem_desc(sbase + Ly::kOffP, 1024, 128, 0);
       int c = 0, qi = 0, last_g2 = -1;
-      auto ready1 = [&](int cc) -> bool {
-        return mbar_test(kconv_full, cc & 1) && (cc < 2 || mbar_test(s_free(cc & 1), ((cc >> 1) + 1) & 1));
-      };
-      auto gemm1 = [&](int cc) {
-        const int bb = cc & 1;
-        tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < kD / 16; ++k) {
-          const int h = k >> 2, kk = k & 3;
-          const uint64_t ad = smem_desc(kbf + h * kHalfBytes + kk * 32, 16, 1024, 2);
-          const uint64_t bd = smem_desc(qb + h * Ly::kQHalf + kk * 32, 16, 1024, 2);
-          mma_f16(tmem + bb * 32, ad, bd, idesc1, k > 0 ? 1u : 0u);
-        }
-        mma_commit(s_full(bb));
-      };
-      auto ready2 = [&](int cc) -> bool {
-        return mbar_test(p_full(cc & 1), (cc >> 1) & 1) && (cc < 2 || mbar_test(o_free(cc & 1), ((cc >> 1) + 1) & 1));
-      };
-      auto gemm2 = [&](int cc) {
-        const int bb = cc & 1;
-        tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < kChunk / 16; ++k) {
-          const uint64_t ad = smem_desc(vbf + k * 2048, kHalfBytes, 1024, 2);
-          const uint64_t bd = smem_desc(pb + bb * Ly::kPBytes + k * 2048, 1024, 128, 0);
-          mma_f16(tmem + Ly::kColO + bb * 64, ad, bd, idesc2, k > 0 ? 1u : 0u);
-        }
-        mma_commit(o_full(bb));
-        last_g2 = cc;
-      };
       int item = blockIdx.x;
       Item it = item < a.items ? item_geom(a, item, bpc) : Item{};
-      while (item < a.items && !*abort_flag) {
+      bool ok = true;
+      while (ok && item < a.items && !*abort_flag) {
         const int next = item + gridDim.x;
         const Item nit = next < a.items ? item_geom(a, next, bpc) : Item{};
-        if (it.nch > 0) {
-          if (!mbar_wait(q_full, qi & 1, abort_flag)) break;
+        if (it.nch > 0 && first) {
+          ok = mbar_wait(q_full, qi & 1, abort_flag);
           ++qi;
-          if (!issue_chunks(c, it.nch, abort_flag, ready1, gemm1, ready2, gemm2)) break;
-          c += it.nch;
+        }
+        for (int ci = 0; ok && ci < it.nch; ++ci, ++c) {
+          const int bb = c & 1;
+          if (first) {
+            ok = mbar_wait(kconv_full, c & 1, abort_flag) &&
+                 (c < 2 || mbar_wait(s_free(bb), ((c >> 1) + 1) & 1, abort_flag));
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll
+            for (int k = 0; k < kD / 16; ++k) {
+              const uint32_t koff = (k >> 2) * kHalfBytes + (k & 3) * 32;
+              const uint32_t qoff = (k >> 2) * Ly::kQHalf + (k & 3) * 32;
+              mma_f16(tmem + bb * 32, kdesc + (koff >> 4), qdesc + (qoff >> 4), idesc1, k > 0 ? 1u : 0u);
+            }
+            mma_commit(s_full(bb));
+          } else {
+            ok = mbar_wait(p_full(bb), (c >> 1) & 1, abort_flag) &&
+                 (c < 2 || mbar_wait(o_free(bb), ((c >> 1) + 1) & 1, abort_flag));
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll
+            for (int k = 0; k < kChunk / 16; ++k) {
+              const uint32_t poff = bb * Ly::kPBytes + k * 2048;
+              mma_f16(tmem + Ly::kColO + bb * 64, vdesc + ((k * 2048) >> 4), pdesc + (poff >> 4), idesc2,
+                      k > 0 ? 1u : 0u);
+            }
+            mma_commit(o_full(bb));
+            last_g2 = c;
+          }
         }
         item = next;
         it = nit;
       }
-      if (last_g2 >= 0) mbar_wait(o_full(last_g2 & 1), (last_g2 >> 1) & 1, abort_flag, 500000000ull);
+      if (!first && last_g2 >= 0) mbar_wait(o_full(last_g2 & 1), (last_g2 >> 1) & 1, abort_flag, 500000000ull);
     }
   } else {
     const int t = tid;
