@@ -10,15 +10,16 @@
 // keep ~16 significant bits through the bf16 MMA; both accumulate in fp32 TMEM.
 //
 // Persistent, warp-specialised CTA (one per SM):
-//   warp 4      TMA producer: cp.async.bulk.tensor of each selected page's K
-//               and V rows (two 64-channel halves, 128-byte swizzle) into a
-//               3-stage ring, completion tracked by mbarrier transaction bytes.
-//   warps 5, 6  MMA issuers (one thread each): warp 5 issues S = K.Q^T, warp 6
-//               O = V^T.P; TMEM double-buffers S and O.
-//   warps 0-3   softmax / correction: thread t owns TMEM lane t = token t of
-//               the chunk for S, and channel t for O; running max and sum per
-//               head, P written to shared memory for GEMM2, O accumulated in
-//               registers with the online-softmax rescale.
+//   TMA producer warp: cp.async.bulk.tensor of each selected page's K and V
+//               rows (two 64-channel halves, 128-byte swizzle) into a 3-stage
+//               ring, completion tracked by mbarrier transaction bytes.
+//   two MMA issuer warps (one thread each): S = K.Q^T and O = V^T.P; TMEM
+//               double-buffers S and O.
+//   softmax / correction warps: thread t owns TMEM lane t = token t of the
+//               chunk for S, and channel t for O; running max and sum per head,
+//               P written to shared memory for GEMM2, O accumulated in registers
+//               with the online-softmax rescale.  The bf16 kernel has two such
+//               groups working on alternate chunks, merged per work item.
 // Every wait is bounded (2 s); on a time-out the CTA sets HS_EBIT_TIMEOUT,
 // stops all roles, lets in-flight copies land and frees its TMEM.
 #include <cuda.h>
@@ -65,11 +66,12 @@ struct Layout {
   static constexpr int kPBytes = kChunk * 2 * NH * 2;
   static constexpr int kOffQ = kStages * kStageBytes;
   static constexpr int kOffP = kOffQ + 2 * kQHalfBytes;
-  static constexpr int kOffBar = kOffP + 2 * kPBytes;
+  static constexpr int kOffX = kOffP + 2 * kPBytes;           // group exchange: o[NH][128], m[NH], l[NH]
+  static constexpr int kOffBar = kOffX + ((NH * 128 + 2 * NH) * 4 + 15) / 16 * 16;
   static constexpr int kNumBars = 2 * kStages + 11;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kOffRed = kOffMisc + 16;
-  static constexpr int kOffMeta = kOffRed + 3 * 4 * NH * 4;  // red: [3][4 warps][NH]; meta: [stage][8] (page, valid tokens)
+  static constexpr int kOffMeta = kOffRed + 2 * 3 * 4 * NH * 4;  // red: [group][3][4 warps][NH]; meta: [stage][8] (page, valid tokens)
   static constexpr int kBytes = kOffMeta + kStages * 8 * 8;
   // the whole per-block maximum: one CTA per SM, and operand reads through a
   // descriptor can never leave this CTA's own shared memory
@@ -196,8 +198,45 @@ __device__ __forceinline__ void run_producer(const TcArgs& a, int bpc, uint32_t 
   }
 }
 
+// bf16 kernel: warps 0-7 are two softmax groups of 4 warps (group g takes the
+// chunks c with c % 2 == g, so two chunks are in the softmax stage at once),
+// warp 8 is the TMA producer, warps 9 and 10 the MMA issuers.
+constexpr int kGroups = 2;
+constexpr int kThreadsB = 352;
+constexpr int kProdB = 8, kMma1B = 9, kMma2B = 10;
+
+// per-warp max (or sum) of each of the NH values a lane holds, over the warp's
+// 32 lanes, by halving exchanges: afterwards lane l holds the result of value
+// l / (32 / NH) (NH <= 32)
+template <int NH, bool MAX>
+__device__ __forceinline__ float warp_reduce_scatter(float (&v)[NH]) {
+  const int lane = threadIdx.x & 31;
+  int cur = NH;
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    if (cur > 1) {
+      const bool upper = (lane & o) != 0;
+      const int half = cur / 2;
+#pragma unroll
+      for (int i = 0; i < NH / 2; ++i) {
+        if (i < half) {
+          const float send = upper ? v[i] : v[i + half];
+          const float keep = upper ? v[i + half] : v[i];
+          const float got = __shfl_xor_sync(0xffffffffu, send, o);
+          v[i] = MAX ? fmaxf(keep, got) : keep + got;
+        }
+      }
+      cur = half;
+    } else {
+      const float got = __shfl_xor_sync(0xffffffffu, v[0], o);
+      v[0] = MAX ? fmaxf(v[0], got) : v[0] + got;
+    }
+  }
+  return v[0];
+}
+
 template <int NH>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreadsB, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                    TcArgs a, unsigned* err) {
   using Ly = Layout<NH>;
@@ -215,7 +254,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t q_full = bar0 + 8 * (2 * kStages + 10);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Ly::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Ly::kOffMisc + 4);
-  float* red = reinterpret_cast<float*>(smem + Ly::kOffRed);  // [4 warps][NH]
   auto k_half = [&](int s, int h) { return sbase + s * kStageBytes + h * kHalfBytes; };
   auto v_half = [&](int s, int h) { return sbase + s * kStageBytes + kTileBytes + h * kHalfBytes; };
   auto q_half = [&](int h) { return sbase + Ly::kOffQ + h * kQHalfBytes; };
@@ -226,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int bpc = kChunk / B;
 
   pdl_trigger();
-  // ---- set-up: barriers, zeroed operand buffers, TMEM (overlaps the previous kernel) ----
+  // ---- set-up: barriers and TMEM (overlaps the previous kernel) ----
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(full_bar(s), 1);
@@ -243,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == kMmaWarp) {
+  if (warp == kMma1B) {
     tmem_alloc(smem_u32(tmem_slot), Ly::kTmemCols);
     tmem_relinquish();
   }
@@ -254,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_wait();  // the selection and q of this step are complete from here on
 
   int2* meta = reinterpret_cast<int2*>(smem + Ly::kOffMeta);
-  if (warp == kProducerWarp) {
+  if (warp == kProdB) {
     // ================= TMA producer =================
     run_producer<kStages>(a, bpc, full_bar(0), empty_bar(0), meta, 4u * B * 128u, abort_flag, err,
                           [&](int s, int bi, int page) {
@@ -265,12 +303,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                             tma_load_2d(v_half(s, 0) + row_off, &tm_v, 0, y, full_bar(s));
                             tma_load_2d(v_half(s, 1) + row_off, &tm_v, 64, y, full_bar(s));
                           });
-  } else if (warp == kMmaWarp || warp == kMma2Warp) {
+  } else if (warp == kMma1B || warp == kMma2B) {
     // ================= MMA issuers: one thread for S = K.Q^T, one for O = V^T.P =================
     // (issuing a GEMM's 8 tcgen05.mma takes a few hundred ns, so the two GEMMs
     // of a chunk are issued from two threads instead of one after the other)
     if (lane == 0) {
-      const bool first = warp == kMmaWarp;
+      const bool first = warp == kMma1B;
       constexpr uint32_t idesc1 = idesc_bf16(128, 16, false, false);
       constexpr uint32_t idesc2 = idesc_bf16(128, 2 * NH, true, true);
       constexpr uint32_t kPLbo = 8 * 2 * NH * 2;  // bytes between 8-token groups of P
@@ -331,12 +369,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    // ================= softmax / correction (warps 0-3) =================
-    const int t = tid;  // token row of S, channel of O
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    // ================= softmax / correction: two groups of 4 warps =================
+    const int grp = warp >> 2;       // group: owns the chunks with c % 2 == grp, S/P/O buffer grp
+    const int wq = warp & 3;         // TMEM lane quarter
+    const int t = tid & 127;         // token row of S, channel of O
+    const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+    const int bar = 1 + grp;         // named barrier of the group
     const int g = a.group;
-    int c = 0;
-    // thread t holds 16 bytes of each channel half of head row t/8 of the Q operand
+    float* red = reinterpret_cast<float*>(smem + Ly::kOffRed) + grp * 12 * NH;  // [3][4 warps][NH]
+    float* xo = reinterpret_cast<float*>(smem + Ly::kOffX);                    // [NH][128] + m[NH] + l[NH]
     auto load_q = [&](int item, uint4 (&v)[2]) {
       const int pair = item / a.splits, b = pair / a.hkv, kvh = pair - b * a.hkv;
       const int n = t >> 3, ch = t & 7;
@@ -348,12 +389,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                  ch * 8);
       }
     };
+    int c = 0;
     int item = blockIdx.x;
     Item it{};
-    uint4 qv[2];
+    uint4 qv[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
     if (item < a.items) {
       it = item_geom(a, item, bpc);
-      load_q(item, qv);
+      if (grp == 0) load_q(item, qv);
     }
     for (; item < a.items && !*abort_flag;) {
       // the next item's geometry and query rows are fetched while this one runs
@@ -362,147 +404,165 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint4 nqv[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
       if (next < a.items) {
         nit = item_geom(a, next, bpc);
-        load_q(next, nqv);
+        if (grp == 0) load_q(next, nqv);
       }
       const int64_t row0 = (static_cast<int64_t>(it.b) * a.hq + it.kvh * g) * a.splits + it.split;
-      if (it.nch == 0) {
+      if (it.nch > 0) {
+        if (grp == 0) {
+          // Q operand: 16 rows (heads, zero past g) x 128 channels, 128-byte swizzle
+          const int n = t >> 3, ch = t & 7;
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+            *reinterpret_cast<uint4*>(smem + Ly::kOffQ + h * kQHalfBytes + n * 128 + ((ch ^ (n & 7)) << 4)) = qv[h];
+          fence_async_smem();
+          mbar_arrive(q_full);
+        }
+        float m[NH], lsum[NH], oacc[NH], alpha_prev[NH];
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {
+          m[h] = -INFINITY;
+          lsum[h] = 0.0f;
+          oacc[h] = 0.0f;
+          alpha_prev[h] = 1.0f;
+        }
+        bool ok = true;
+        auto take_o = [&](int cc) -> bool {
+          if (!mbar_wait(o_full(grp), (cc >> 1) & 1, abort_flag)) return false;
+          tc_fence_after();
+          float ov[2 * NH];
+          if constexpr (NH == 8) {
+            tmem_ld16(tmem + lane_base + Ly::kColO + grp * 16, *reinterpret_cast<float(*)[16]>(ov));
+          } else {
+            tmem_ld16(tmem + lane_base + Ly::kColO + grp * 32, *reinterpret_cast<float(*)[16]>(ov));
+            tmem_ld16(tmem + lane_base + Ly::kColO + grp * 32 + 16, *reinterpret_cast<float(*)[16]>(ov + 16));
+          }
+          tc_fence_before();
+          mbar_arrive(o_free(grp));
+#pragma unroll
+          for (int h = 0; h < NH; ++h) oacc[h] = fmaf(oacc[h], alpha_prev[h], ov[h] + ov[NH + h]);
+          return true;
+        };
+        const int c0 = c;
+        int last_own = -1;
+        for (int cc = c0 + ((grp - c0) & 1); cc < c0 + it.nch; cc += 2) {
+          const int s = cc % kStages;
+          const int bi = t / B, tok = t - bi * B;
+          if (!mbar_wait(full_bar(s), (cc / kStages) & 1, abort_flag)) { ok = false; break; }
+          const int2 md = meta[s * 8 + bi];
+          const bool valid = md.x >= 0 && tok < md.y;
+          if (!mbar_wait(s_full(grp), (cc >> 1) & 1, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          float sv[16];
+          tmem_ld16(tmem + lane_base + grp * 16, sv);
+          tc_fence_before();
+          mbar_arrive(s_free(grp));
+          float x[NH], r[NH];
+#pragma unroll
+          for (int h = 0; h < NH; ++h) {
+            x[h] = (valid && h < g) ? sv[h] * a.scale_log2 : -INFINITY;
+            r[h] = x[h];
+          }
+          // chunk max per head over the 128 rows: warp reduce-scatter, then the 4 warps
+          float* rb = red + ((cc >> 1) & 1) * 4 * NH;  // alternate buffers: one barrier per chunk
+          const float wmax = warp_reduce_scatter<NH, true>(r);
+          if ((lane % (32 / NH)) == 0) rb[wq * NH + lane / (32 / NH)] = wmax;
+          named_barrier(bar, 128);
+          float alpha[NH], p[NH];
+#pragma unroll
+          for (int h = 0; h < NH; ++h) {
+            const float cm = fmaxf(fmaxf(rb[h], rb[NH + h]), fmaxf(rb[2 * NH + h], rb[3 * NH + h]));
+            const float mn = fmaxf(m[h], cm);
+            alpha[h] = (mn == -INFINITY) ? 1.0f : exp2f(m[h] - mn);
+            m[h] = mn;
+            p[h] = x[h] == -INFINITY ? 0.0f : exp2f(x[h] - mn);
+            lsum[h] = fmaf(lsum[h], alpha[h], p[h]);
+          }
+          // probabilities, split into bf16 high part + bf16 remainder
+          uint32_t hi2[NH / 2], lo2[NH / 2];
+#pragma unroll
+          for (int h = 0; h < NH; h += 2) {
+            const __nv_bfloat162 hi = __floats2bfloat162_rn(p[h], p[h + 1]);
+            const float2 hf = __bfloat1622float2(hi);
+            const __nv_bfloat162 lo = __floats2bfloat162_rn(p[h] - hf.x, p[h + 1] - hf.y);
+            hi2[h / 2] = *reinterpret_cast<const uint32_t*>(&hi);
+            lo2[h / 2] = *reinterpret_cast<const uint32_t*>(&lo);
+          }
+          {
+            constexpr int kPLbo = 8 * 2 * NH * 2;
+            uint8_t* prow = smem + Ly::kOffP + grp * Ly::kPBytes + (t >> 3) * kPLbo + (t & 7) * 16;
+#pragma unroll
+            for (int gi = 0; gi < NH / 8; ++gi) {
+              *reinterpret_cast<uint4*>(prow + gi * 128) =
+                  make_uint4(hi2[gi * 4], hi2[gi * 4 + 1], hi2[gi * 4 + 2], hi2[gi * 4 + 3]);
+              *reinterpret_cast<uint4*>(prow + (NH / 8 + gi) * 128) =
+                  make_uint4(lo2[gi * 4], lo2[gi * 4 + 1], lo2[gi * 4 + 2], lo2[gi * 4 + 3]);
+            }
+          }
+          if (!valid) {
+            // rows of no token (past the request's end inside its last page, or of
+            // no loaded block): zero V so they contribute exactly nothing - P is 0
+            // there but the bytes in shared memory need not be finite
+            uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              uint4* row = reinterpret_cast<uint4*>(smem + s * kStageBytes + kTileBytes + h * kHalfBytes + t * 128);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) row[i] = z;
+            }
+          }
+          fence_async_smem();
+          mbar_arrive(p_full(grp));
+          if (last_own >= 0 && !take_o(last_own)) { ok = false; break; }
+#pragma unroll
+          for (int h = 0; h < NH; ++h) alpha_prev[h] = alpha[h];
+          last_own = cc;
+        }
+        c = c0 + it.nch;
+        if (!ok) break;
+        // the normaliser reduction overlaps the last P.V product
+        float* rs = red + 8 * NH;
+        {
+          float r[NH];
+#pragma unroll
+          for (int h = 0; h < NH; ++h) r[h] = lsum[h];
+          const float wsum = warp_reduce_scatter<NH, false>(r);
+          if ((lane % (32 / NH)) == 0) rs[wq * NH + lane / (32 / NH)] = wsum;
+        }
+        named_barrier(bar, 128);
+        if (last_own >= 0 && !take_o(last_own)) break;
+        // combine the two groups' states: group 1 publishes, group 0 merges and writes
+        float* xm = xo + NH * 128;
+        float* xl = xm + NH;
+        if (grp == 1) {
+#pragma unroll
+          for (int h = 0; h < NH; ++h) xo[h * 128 + t] = oacc[h];
+          if (t < NH) {
+            xm[t] = m[t];
+            xl[t] = rs[t] + rs[NH + t] + rs[2 * NH + t] + rs[3 * NH + t];
+          }
+        }
+        named_barrier(3, 256);
+        if (grp == 0) {
+          for (int h = 0; h < g && h < NH; ++h) {
+            const float l0 = rs[h] + rs[NH + h] + rs[2 * NH + h] + rs[3 * NH + h];
+            const float m1 = xm[h], l1 = xl[h];
+            const float mx = fmaxf(m[h], m1);
+            const float e0 = m[h] == -INFINITY ? 0.0f : exp2f(m[h] - mx);
+            const float e1 = m1 == -INFINITY ? 0.0f : exp2f(m1 - mx);
+            const float lt = l0 * e0 + l1 * e1;
+            const float ot = oacc[h] * e0 + xo[h * 128 + t] * e1;
+            const int64_t row = row0 + static_cast<int64_t>(h) * a.splits;
+            a.ws_o[row * kD + t] = lt > 0.0f ? ot / lt : 0.0f;
+            if (t == 0) a.ws_lse[row] = lt > 0.0f ? (mx + log2f(lt)) * kLn2 : -INFINITY;
+          }
+        }
+        named_barrier(3, 256);  // the exchange buffer is free again
+      } else if (grp == 0) {
         for (int h = 0; h < g; ++h) {
           a.ws_o[(row0 + static_cast<int64_t>(h) * a.splits) * kD + t] = 0.0f;
           if (t == 0) a.ws_lse[row0 + static_cast<int64_t>(h) * a.splits] = -INFINITY;
         }
-        item = next;
-        it = nit;
-        qv[0] = nqv[0];
-        qv[1] = nqv[1];
-        continue;
       }
-      // Q operand of this kv head: 16 rows (heads, zero past g) x 128 channels, 128-byte swizzle
-      {
-        const int n = t >> 3, ch = t & 7;
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-          *reinterpret_cast<uint4*>(smem + Ly::kOffQ + h * kQHalfBytes + n * 128 + ((ch ^ (n & 7)) << 4)) = qv[h];
-      }
-      fence_async_smem();
-      mbar_arrive(q_full);
-
-      float m[NH], lsum[NH], oacc[NH], alpha_prev[NH];
-#pragma unroll
-      for (int h = 0; h < NH; ++h) {
-        m[h] = -INFINITY;
-        lsum[h] = 0.0f;
-        oacc[h] = 0.0f;
-        alpha_prev[h] = 1.0f;
-      }
-      bool ok = true;
-      auto take_o = [&](int cc) -> bool {
-        const int bb = cc & 1;
-        if (!mbar_wait(o_full(bb), (cc >> 1) & 1, abort_flag)) return false;
-        tc_fence_after();
-        float ov[2 * NH];
-        if constexpr (NH == 8) {
-          tmem_ld16(tmem + lane_base + Ly::kColO + bb * 16, *reinterpret_cast<float(*)[16]>(ov));
-        } else {
-          tmem_ld16(tmem + lane_base + Ly::kColO + bb * 32, *reinterpret_cast<float(*)[16]>(ov));
-          tmem_ld16(tmem + lane_base + Ly::kColO + bb * 32 + 16, *reinterpret_cast<float(*)[16]>(ov + 16));
-        }
-        tc_fence_before();
-        mbar_arrive(o_free(bb));
-#pragma unroll
-        for (int h = 0; h < NH; ++h) oacc[h] = fmaf(oacc[h], alpha_prev[h], ov[h] + ov[NH + h]);
-        return true;
-      };
-      for (int ci = 0; ci < it.nch && ok; ++ci, ++c) {
-        const int bb = c & 1, s = c % kStages;
-        const int bi = t / B, tok = t - bi * B;
-        if (!mbar_wait(full_bar(s), (c / kStages) & 1, abort_flag)) { ok = false; break; }
-        const int2 md = meta[s * 8 + bi];
-        const bool valid = md.x >= 0 && tok < md.y;
-        if (!mbar_wait(s_full(bb), (c >> 1) & 1, abort_flag)) { ok = false; break; }
-        tc_fence_after();
-        float sv[16];
-        tmem_ld16(tmem + lane_base + bb * 16, sv);
-        tc_fence_before();
-        mbar_arrive(s_free(bb));
-        float x[NH];
-#pragma unroll
-        for (int h = 0; h < NH; ++h) x[h] = (valid && h < g) ? sv[h] * a.scale_log2 : -INFINITY;
-        // chunk max per head over the 128 rows
-#pragma unroll
-        for (int h = 0; h < NH; ++h) {
-          const float mx = warp_max(x[h]);
-          if (lane == 0) red[(c & 1) * 4 * NH + warp * NH + h] = mx;
-        }
-        named_barrier(1, 128);
-        const float* rb = red + (c & 1) * 4 * NH;  // alternate buffers: one barrier per chunk
-        float alpha[NH];
-#pragma unroll
-        for (int h = 0; h < NH; ++h) {
-          const float cm = fmaxf(fmaxf(rb[h], rb[NH + h]), fmaxf(rb[2 * NH + h], rb[3 * NH + h]));
-          const float mn = fmaxf(m[h], cm);
-          alpha[h] = (mn == -INFINITY) ? 1.0f : exp2f(m[h] - mn);
-          m[h] = mn;
-        }
-        // probabilities, split into bf16 high part + bf16 remainder
-        uint32_t hi2[NH / 2], lo2[NH / 2];
-#pragma unroll
-        for (int h = 0; h < NH; h += 2) {
-          float p0 = x[h] == -INFINITY ? 0.0f : exp2f(x[h] - m[h]);
-          float p1 = x[h + 1] == -INFINITY ? 0.0f : exp2f(x[h + 1] - m[h + 1]);
-          lsum[h] = fmaf(lsum[h], alpha[h], p0);
-          lsum[h + 1] = fmaf(lsum[h + 1], alpha[h + 1], p1);
-          const __nv_bfloat162 hi = __floats2bfloat162_rn(p0, p1);
-          const float2 hf = __bfloat1622float2(hi);
-          const __nv_bfloat162 lo = __floats2bfloat162_rn(p0 - hf.x, p1 - hf.y);
-          hi2[h / 2] = *reinterpret_cast<const uint32_t*>(&hi);
-          lo2[h / 2] = *reinterpret_cast<const uint32_t*>(&lo);
-        }
-        {
-          constexpr int kPLbo = 8 * 2 * NH * 2;
-          uint8_t* prow = smem + Ly::kOffP + bb * Ly::kPBytes + (t >> 3) * kPLbo + (t & 7) * 16;
-#pragma unroll
-          for (int gi = 0; gi < NH / 8; ++gi) {
-            *reinterpret_cast<uint4*>(prow + gi * 128) =
-                make_uint4(hi2[gi * 4], hi2[gi * 4 + 1], hi2[gi * 4 + 2], hi2[gi * 4 + 3]);
-            *reinterpret_cast<uint4*>(prow + (NH / 8 + gi) * 128) =
-                make_uint4(lo2[gi * 4], lo2[gi * 4 + 1], lo2[gi * 4 + 2], lo2[gi * 4 + 3]);
-          }
-        }
-        if (!valid) {
-          // rows of no token (past the request's end inside its last page, or of
-          // no loaded block): zero V so they contribute exactly nothing - P is 0
-          // there but the bytes in shared memory need not be finite
-          uint4 z = make_uint4(0, 0, 0, 0);
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            uint4* row = reinterpret_cast<uint4*>(smem + s * kStageBytes + kTileBytes + h * kHalfBytes + t * 128);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) row[i] = z;
-          }
-        }
-        fence_async_smem();
-        mbar_arrive(p_full(bb));
-        if (ci > 0 && !take_o(c - 1)) { ok = false; break; }
-#pragma unroll
-        for (int h = 0; h < NH; ++h) alpha_prev[h] = alpha[h];
-      }
-      if (!ok) break;
-      // the normaliser reduction overlaps the last P.V product
-#pragma unroll
-      for (int h = 0; h < NH; ++h) {
-        const float s_ = warp_sum(lsum[h]);
-        if (lane == 0) red[8 * NH + warp * NH + h] = s_;
-      }
-      named_barrier(1, 128);
-      const float* rs = red + 8 * NH;
-      if (!take_o(c - 1)) break;
-      for (int h = 0; h < g && h < NH; ++h) {
-        const float lt = rs[h] + rs[NH + h] + rs[2 * NH + h] + rs[3 * NH + h];
-        const int64_t row = row0 + static_cast<int64_t>(h) * a.splits;
-        a.ws_o[row * kD + t] = lt > 0.0f ? oacc[h] / lt : 0.0f;
-        if (t == 0) a.ws_lse[row] = lt > 0.0f ? (m[h] + log2f(lt)) * kLn2 : -INFINITY;
-      }
-      named_barrier(1, 128);
       item = next;
       it = nit;
       qv[0] = nqv[0];
@@ -514,12 +574,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   if (*abort_flag && tid == 0) set_error(err, HS_EBIT_TIMEOUT);
-  if (warp == kMmaWarp) {
+  if (warp == kMma1B) {
     tc_fence_after();
     tmem_dealloc(tmem, Ly::kTmemCols);
   }
 }
-
 
 // ============================================================================
 // e4m3 K/V (one fp32 scale per 32 channels per token), head_dim 128, g <= 8.
@@ -1000,7 +1059,7 @@ cudaError_t launch_nh(const KvView& kv, const AttnArgs& aa, unsigned* err, cudaS
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::kAlloc);
   if (e != cudaSuccess) return e;
   const int grid = a.items < aa.sms ? a.items : aa.sms;
-  return launch_pdl(kern, dim3(grid), dim3(kThreads), Ly::kAlloc, st, mk, mv, a, err);
+  return launch_pdl(kern, dim3(grid), dim3(kThreadsB), Ly::kAlloc, st, mk, mv, a, err);
 }
 
 }  // namespace
