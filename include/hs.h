@@ -200,6 +200,10 @@ HS_API hs_status hs_build_block_summaries(const hs_attn_shape* shape, const hs_p
                                    int32_t first_block, void* smin, void* smax,
                                    hs_stream_t stream);
 
+/* Bytes of workspace hs_score_select_topk needs when scores_opt is NULL: one
+ * fp32 score per block, [batch][Hkv][max_blocks].  0 on invalid input. */
+HS_API size_t hs_select_workspace_bytes(const hs_attn_shape* shape, int32_t batch, int32_t max_blocks);
+
 /* Bound scoring and block selection, [KVS] §5 Quest + §2 sink/window:
  *   U[b][h][j] = sum_d max(q[b][h][d] * smax[b][kvh][j][d],
  *                          q[b][h][d] * smin[b][kvh][j][d])
@@ -208,8 +212,11 @@ HS_API hs_status hs_build_block_summaries(const hs_attn_shape* shape, const hs_p
  * lower index first on ties, NaN last), ascending; all N_b blocks when that
  * covers them.  sel_count = number selected; sel entries up to capacity past
  * the count are -1.  scores_opt (nullable) [batch][Hkv][max_blocks] f32
- * receives the scores of blocks j < N_b.  No workspace is needed
- * (workspace/ws_bytes may be NULL/0).  Requires max_blocks <= 16384. */
+ * receives the scores of blocks j < N_b.  With bf16 summaries and head_dim 128
+ * the bounds are computed on the tensor cores into scores_opt or, when it is
+ * NULL, into workspace (hs_select_workspace_bytes bytes, else
+ * HS_ERR_WORKSPACE); otherwise no workspace is needed.  Requires max_blocks
+ * <= 16384. */
 HS_API hs_status hs_score_select_topk(const hs_attn_shape* shape, const hs_paged_kv* kv, const void* q,
                                const void* smin, const void* smax,
                                const hs_select_params* params, int32_t* sel,

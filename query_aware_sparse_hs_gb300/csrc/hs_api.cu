@@ -180,8 +180,6 @@ hs_status hs_score_select_topk(const hs_attn_shape* shape, const hs_paged_kv* kv
                                const hs_select_params* params, int32_t* sel,
                                int32_t* sel_count, float* scores_opt, void* workspace,
                                size_t ws_bytes, hs_stream_t stream) {
-  (void)workspace;
-  (void)ws_bytes;
   hs_status st = check_shape(shape);
   if (st != HS_OK) return st;
   if (!kv || !kv->seq_lens || kv->batch < 0 || kv->max_blocks < 1) return HS_ERR_INVALID_ARG;
@@ -210,7 +208,25 @@ hs_status hs_score_select_topk(const hs_attn_shape* shape, const hs_paged_kv* kv
   a.window_tokens = params->window_tokens;
   a.k_scored = params->k_scored;
   a.capacity = params->capacity;
-  return from_cuda(launch_score_select(v, a, d.err, reinterpret_cast<cudaStream_t>(stream)));
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (score_tc_supported(v)) {
+    // tensor-core bound scoring into a score buffer, then one CTA per pair selects
+    float* buf = scores_opt;
+    if (!buf) {
+      const size_t need = static_cast<size_t>(kv->batch) * shape->num_kv_heads * kv->max_blocks * sizeof(float);
+      if (!workspace || ws_bytes < need || !aligned(workspace, 16)) return HS_ERR_WORKSPACE;
+      buf = static_cast<float*>(workspace);
+    }
+    if (launch_score_tc(v, q, smin, smax, buf, d.sms, d.err, cs) != cudaSuccess) return HS_ERR_CUDA;
+    return from_cuda(launch_select_only(v, a, buf, d.err, cs));
+  }
+  return from_cuda(launch_score_select(v, a, d.err, cs));
+}
+
+size_t hs_select_workspace_bytes(const hs_attn_shape* shape, int32_t batch, int32_t max_blocks) {
+  if (check_shape(shape) != HS_OK || batch < 0 || max_blocks < 0) return 0;
+  const size_t bytes = static_cast<size_t>(batch) * shape->num_kv_heads * max_blocks * sizeof(float);
+  return (bytes + 255) & ~static_cast<size_t>(255);
 }
 
 hs_status hs_sparse_paged_decode_attn(const hs_attn_shape* shape, const hs_paged_kv* kv,

@@ -80,118 +80,16 @@ __device__ __forceinline__ void load_summary(const void* base, int64_t off, floa
   }
 }
 
-template <int C, int G, bool F32>
-__global__ void __cluster_dims__(kSelectCluster, 1, 1) __launch_bounds__(kThreads, (G * C <= 32) ? 2 : 1)
-    score_select_kernel(KvView kv, SelectArgs a, unsigned* err) {
-  extern __shared__ float s_scores[];  // [max_blocks]; rank 0's copy holds every score
-  __shared__ uint32_t s_hist[2][256];
-  __shared__ int s_warp[kWarps + 1];
-  __shared__ int s_pick[2];
-
-  pdl_trigger();
-  pdl_wait();
-  cg::cluster_group cluster = cg::this_cluster();
-  const unsigned rank = cluster.block_rank();
-  const int b = blockIdx.z, kvh = blockIdx.y;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tid = threadIdx.x;
-  const int B = kv.block;
-  const int L = max(kv.seq_lens[b], 0);
-  int nb = ceil_div(L, B);
-  if (nb > kv.max_blocks) {
-    if (tid == 0 && rank == 0) set_error(err, HS_EBIT_BLOCK_RANGE);
-    nb = kv.max_blocks;
-  }
-  const int64_t pair = static_cast<int64_t>(b) * kv.hkv + kvh;
-  const int D = C * 32;
-
-  // ---- scoring: this CTA's slice of blocks, one warp per block ----
-  {
-    float qp[G][C], qn[G][C];
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      const int64_t qo = (static_cast<int64_t>(b) * kv.hq + kvh * G + h) * D + lane * C;
-#pragma unroll
-      for (int c = 0; c < C; ++c) {
-        float x = F32 ? static_cast<const float*>(a.q)[qo + c]
-                      : __bfloat162float(static_cast<const __nv_bfloat16*>(a.q)[qo + c]);
-        qp[h][c] = fmaxf(x, 0.0f);
-        qn[h][c] = fminf(x, 0.0f);
-      }
-    }
-    float* dst = cluster.map_shared_rank(s_scores, 0);
-    const int per = ceil_div(nb, kSelectCluster);
-    const int jb = static_cast<int>(rank) * per, je = min(nb, jb + per);
-    // Each warp scores kNB consecutive blocks per round: all their summaries are
-    // loaded first (memory-level parallelism), then the kNB x G partial dot
-    // products of every lane are summed across the warp by a transpose
-    // reduction (each round halves the values a lane holds), so a block costs
-    // about 8 shuffles instead of 5 per head.
-    constexpr int kNB = (32 / G) < 4 ? ((32 / G) < 1 ? 1 : 32 / G) : 4;
-    constexpr int kV = kNB * G;                    // partial sums per lane
-    constexpr int kVPL = kV >= 32 ? kV / 32 : 1;   // values per lane after the reduction
-    constexpr int kLPV = kV >= 32 ? 1 : 32 / kV;   // lanes holding one value
-    constexpr int kLanesPerBlock = G * kLPV / kVPL;
-    for (int base = jb + warp * kNB; base < je; base += kWarps * kNB) {
-      float mx[kNB][C], mn[kNB][C];
-#pragma unroll
-      for (int u = 0; u < kNB; ++u) {
-        const int j = min(base + u, je - 1);  // clamp: re-reads a valid block, result unused
-        const int64_t off = (pair * kv.max_blocks + j) * D + lane * C;
-        load_summary<C, F32>(a.smax, off, mx[u]);
-        load_summary<C, F32>(a.smin, off, mn[u]);
-      }
-      float v[kV];
-#pragma unroll
-      for (int u = 0; u < kNB; ++u)
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          float acc = 0.0f;
-#pragma unroll
-          for (int c = 0; c < C; ++c) {
-            acc = fmaf(qp[h][c], mx[u][c], acc);
-            acc = fmaf(qn[h][c], mn[u][c], acc);
-          }
-          v[u * G + h] = acc;
-        }
-      int cur = kV;
-#pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) {
-        if (cur > 1) {
-          const bool upper = (lane & o) != 0;
-          const int half = cur / 2;
-#pragma unroll
-          for (int i = 0; i < kV / 2; ++i) {
-            if (i < half) {
-              const float send = upper ? v[i] : v[i + half];
-              const float keep = upper ? v[i + half] : v[i];
-              v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-            }
-          }
-          cur = half;
-        } else {
-          v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
-        }
-      }
-      // lane now holds values [first, first + kVPL) of index u*G + h
-      float best = v[0];
-#pragma unroll
-      for (int i = 1; i < kVPL; ++i) best = fmaxf(best, v[i]);
-#pragma unroll
-      for (int o = 1; o < kLanesPerBlock; o <<= 1) best = fmaxf(best, __shfl_xor_sync(0xffffffffu, best, o));
-      const int first = kV >= 32 ? lane * kVPL : lane / kLPV;
-      const int u = first / G;
-      if ((lane % kLanesPerBlock) == 0 && base + u < je) {
-        dst[base + u] = best;
-        if (a.scores) a.scores[pair * kv.max_blocks + base + u] = best;
-      }
-    }
-  }
-  for (int i = tid; i < 512; i += kThreads) s_hist[i >> 8][i & 255] = 0u;
-  cluster.sync();
-  if (rank != 0) return;
-
-  // ---- selection in rank 0 ----
+// Selection of one (request, kv head) from its block scores in shared memory,
+// by all kThreads threads of the CTA ("KV 稀疏化" wiki §2 sink/window, §5 top-k):
+// forced blocks in closed form, a 4-pass 8-bit radix select of the k-th largest
+// key among the other blocks (two histogram buffers, which must be zero on
+// entry), then one packed scan that places forced-or-above-threshold blocks and
+// the lowest-index threshold-equal blocks in ascending order.
+__device__ __forceinline__ void select_pair(const float* s_scores, int nb, int L, int B, const SelectArgs& a,
+                                            int64_t pair, uint32_t (*s_hist)[256], int* s_warp, int* s_pick,
+                                            unsigned* err) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int sink = a.sink_tokens, win = a.window_tokens, k = a.k_scored, cap = a.capacity;
   auto forced = [&](int j) -> bool {
     const int lo = j * B, hi = min(lo + B, L);
@@ -311,6 +209,147 @@ __global__ void __cluster_dims__(kSelectCluster, 1, 1) __launch_bounds__(kThread
 }
 
 template <int C, int G, bool F32>
+__global__ void __cluster_dims__(kSelectCluster, 1, 1) __launch_bounds__(kThreads, (G * C <= 32) ? 2 : 1)
+    score_select_kernel(KvView kv, SelectArgs a, unsigned* err) {
+  extern __shared__ float s_scores[];  // [max_blocks]; rank 0's copy holds every score
+  __shared__ uint32_t s_hist[2][256];
+  __shared__ int s_warp[kWarps + 1];
+  __shared__ int s_pick[2];
+
+  pdl_trigger();
+  pdl_wait();
+  cg::cluster_group cluster = cg::this_cluster();
+  const unsigned rank = cluster.block_rank();
+  const int b = blockIdx.z, kvh = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tid = threadIdx.x;
+  const int B = kv.block;
+  const int L = max(kv.seq_lens[b], 0);
+  int nb = ceil_div(L, B);
+  if (nb > kv.max_blocks) {
+    if (tid == 0 && rank == 0) set_error(err, HS_EBIT_BLOCK_RANGE);
+    nb = kv.max_blocks;
+  }
+  const int64_t pair = static_cast<int64_t>(b) * kv.hkv + kvh;
+  const int D = C * 32;
+
+  // ---- scoring: this CTA's slice of blocks, one warp per block ----
+  {
+    float qp[G][C], qn[G][C];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const int64_t qo = (static_cast<int64_t>(b) * kv.hq + kvh * G + h) * D + lane * C;
+#pragma unroll
+      for (int c = 0; c < C; ++c) {
+        float x = F32 ? static_cast<const float*>(a.q)[qo + c]
+                      : __bfloat162float(static_cast<const __nv_bfloat16*>(a.q)[qo + c]);
+        qp[h][c] = fmaxf(x, 0.0f);
+        qn[h][c] = fminf(x, 0.0f);
+      }
+    }
+    float* dst = cluster.map_shared_rank(s_scores, 0);
+    const int per = ceil_div(nb, kSelectCluster);
+    const int jb = static_cast<int>(rank) * per, je = min(nb, jb + per);
+    // Each warp scores kNB consecutive blocks per round: all their summaries are
+    // loaded first (memory-level parallelism), then the kNB x G partial dot
+    // products of every lane are summed across the warp by a transpose
+    // reduction (each round halves the values a lane holds), so a block costs
+    // about 8 shuffles instead of 5 per head.
+    constexpr int kNB = (32 / G) < 4 ? ((32 / G) < 1 ? 1 : 32 / G) : 4;
+    constexpr int kV = kNB * G;                    // partial sums per lane
+    constexpr int kVPL = kV >= 32 ? kV / 32 : 1;   // values per lane after the reduction
+    constexpr int kLPV = kV >= 32 ? 1 : 32 / kV;   // lanes holding one value
+    constexpr int kLanesPerBlock = G * kLPV / kVPL;
+    for (int base = jb + warp * kNB; base < je; base += kWarps * kNB) {
+      float mx[kNB][C], mn[kNB][C];
+#pragma unroll
+      for (int u = 0; u < kNB; ++u) {
+        const int j = min(base + u, je - 1);  // clamp: re-reads a valid block, result unused
+        const int64_t off = (pair * kv.max_blocks + j) * D + lane * C;
+        load_summary<C, F32>(a.smax, off, mx[u]);
+        load_summary<C, F32>(a.smin, off, mn[u]);
+      }
+      float v[kV];
+#pragma unroll
+      for (int u = 0; u < kNB; ++u)
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          float acc = 0.0f;
+#pragma unroll
+          for (int c = 0; c < C; ++c) {
+            acc = fmaf(qp[h][c], mx[u][c], acc);
+            acc = fmaf(qn[h][c], mn[u][c], acc);
+          }
+          v[u * G + h] = acc;
+        }
+      int cur = kV;
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) {
+        if (cur > 1) {
+          const bool upper = (lane & o) != 0;
+          const int half = cur / 2;
+#pragma unroll
+          for (int i = 0; i < kV / 2; ++i) {
+            if (i < half) {
+              const float send = upper ? v[i] : v[i + half];
+              const float keep = upper ? v[i + half] : v[i];
+              v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+            }
+          }
+          cur = half;
+        } else {
+          v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
+        }
+      }
+      // lane now holds values [first, first + kVPL) of index u*G + h
+      float best = v[0];
+#pragma unroll
+      for (int i = 1; i < kVPL; ++i) best = fmaxf(best, v[i]);
+#pragma unroll
+      for (int o = 1; o < kLanesPerBlock; o <<= 1) best = fmaxf(best, __shfl_xor_sync(0xffffffffu, best, o));
+      const int first = kV >= 32 ? lane * kVPL : lane / kLPV;
+      const int u = first / G;
+      if ((lane % kLanesPerBlock) == 0 && base + u < je) {
+        dst[base + u] = best;
+        if (a.scores) a.scores[pair * kv.max_blocks + base + u] = best;
+      }
+    }
+  }
+  for (int i = tid; i < 512; i += kThreads) s_hist[i >> 8][i & 255] = 0u;
+  cluster.sync();
+  if (rank != 0) return;
+
+  select_pair(s_scores, nb, L, B, a, pair, s_hist, s_warp, s_pick, err);
+}
+
+// One CTA per (request, kv head): scores already in global memory (written by
+// the tensor-core scorer) -> selection.
+__global__ __launch_bounds__(kThreads) void select_only_kernel(KvView kv, SelectArgs a, const float* scores,
+                                                               unsigned* err) {
+  extern __shared__ float s_scores[];
+  __shared__ uint32_t s_hist[2][256];
+  __shared__ int s_warp[kWarps + 1];
+  __shared__ int s_pick[2];
+  pdl_trigger();
+  pdl_wait();
+  const int tid = threadIdx.x;
+  const int64_t pair = blockIdx.x;
+  const int b = static_cast<int>(pair / kv.hkv);
+  const int B = kv.block;
+  const int L = max(kv.seq_lens[b], 0);
+  int nb = ceil_div(L, B);
+  if (nb > kv.max_blocks) {
+    if (tid == 0) set_error(err, HS_EBIT_BLOCK_RANGE);
+    nb = kv.max_blocks;
+  }
+  const float* src = scores + pair * kv.max_blocks;
+  for (int j = tid; j < nb; j += kThreads) s_scores[j] = src[j];
+  for (int i = tid; i < 512; i += kThreads) s_hist[i >> 8][i & 255] = 0u;
+  __syncthreads();
+  select_pair(s_scores, nb, L, B, a, pair, s_hist, s_warp, s_pick, err);
+}
+
+template <int C, int G, bool F32>
 cudaError_t launch_t(const KvView& kv, const SelectArgs& a, unsigned* err, cudaStream_t st) {
   const size_t smem = static_cast<size_t>(kv.max_blocks) * sizeof(float);
   auto kern = score_select_kernel<C, G, F32>;
@@ -335,6 +374,19 @@ cudaError_t launch_g(const KvView& kv, const SelectArgs& a, unsigned* err, cudaS
 }
 
 }  // namespace
+
+cudaError_t launch_select_only(const KvView& kv, const SelectArgs& a, const float* scores, unsigned* err,
+                               cudaStream_t st) {
+  const int pairs = kv.batch * kv.hkv;
+  if (pairs == 0) return cudaSuccess;
+  const size_t smem = static_cast<size_t>(kv.max_blocks) * sizeof(float);
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(select_only_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
+  return launch_pdl(select_only_kernel, dim3(pairs), dim3(kThreads), smem, st, kv, a, scores, err);
+}
 
 cudaError_t launch_score_select(const KvView& kv, const SelectArgs& a, unsigned* err,
                                 cudaStream_t st) {

@@ -46,7 +46,7 @@ class SparseDecode:
     def build_summaries(self, kv: hs.PagedKV, first_block: int = 0, stream=None):
         hs.hs_build_block_summaries(self.shape, kv, first_block, self.smin, self.smax, stream)
 
-    def select(self, kv: hs.PagedKV, q: torch.Tensor, keep_scores: bool = False, stream=None):
+    def select(self, kv: hs.PagedKV, q: torch.Tensor, keep_scores: bool = True, stream=None):
         hs.hs_score_select_topk(self.shape, kv, q, self.smin, self.smax, self.sel_params, self.sel,
                                 self.sel_count, self.scores if keep_scores else None, None, stream)
 

@@ -70,6 +70,7 @@ SYMBOLS = {
     "hs_status_string": (ctypes.c_char_p, [c_int32]),
     "hs_version": (c_int32, []),
     "hs_workspace_bytes": (c_size_t, [POINTER(AttnShape), c_int32, c_int32, POINTER(AttnParams)]),
+    "hs_select_workspace_bytes": (c_size_t, [POINTER(AttnShape), c_int32, c_int32]),
     "hs_build_block_summaries": (c_int32, [POINTER(AttnShape), POINTER(PagedKV), c_int32, c_void_p,
                                            c_void_p, c_void_p]),
     "hs_score_select_topk": (c_int32, [POINTER(AttnShape), POINTER(PagedKV), c_void_p, c_void_p,
@@ -162,6 +163,10 @@ def attn_params(scale, out_is_fp32=False, blocks_per_split=0, algo="auto") -> At
 
 def hs_workspace_bytes(shape: AttnShape, batch: int, capacity: int, params: AttnParams) -> int:
     return int(_lib.hs_workspace_bytes(ctypes.byref(shape), batch, capacity, ctypes.byref(params)))
+
+
+def hs_select_workspace_bytes(shape: AttnShape, batch: int, max_blocks: int) -> int:
+    return int(_lib.hs_select_workspace_bytes(ctypes.byref(shape), batch, max_blocks))
 
 
 def hs_build_block_summaries(shape, kv, first_block, smin, smax, stream=None):

@@ -72,3 +72,23 @@ def test_host_side_checks():
                                        hs.attn_params(0.1, algo="tcgen05"), dec.out, dec.lse, dec.workspace)
     assert e.value.status == hs.HS_ERR_UNSUPPORTED
     assert hs.hs_get_device_error() == (hs.HS_OK, 0)
+
+
+def test_select_workspace_when_no_score_buffer():
+    """Tensor-core scoring needs a score buffer: scores_opt or the workspace."""
+    from query_aware_sparse_hs_gb300 import hs
+    c = _case()
+    dec = c.decoder()
+    dec.build_summaries(c.kv)
+    dec.select(c.kv, c.q)
+    ref = dec.sel.clone()
+    with pytest.raises(hs.HSError) as e:
+        hs.hs_score_select_topk(dec.shape, c.kv, c.q, dec.smin, dec.smax, dec.sel_params, dec.sel, dec.sel_count)
+    assert e.value.status == hs.HS_ERR_WORKSPACE
+    ws = torch.empty(hs.hs_select_workspace_bytes(dec.shape, c.w.batch, c.page_table.shape[-1]),
+                     dtype=torch.uint8, device="cuda")
+    dec.sel.fill_(-7)
+    hs.hs_score_select_topk(dec.shape, c.kv, c.q, dec.smin, dec.smax, dec.sel_params, dec.sel, dec.sel_count,
+                            None, ws)
+    assert torch.equal(dec.sel, ref)
+    assert hs.hs_get_device_error() == (hs.HS_OK, 0)

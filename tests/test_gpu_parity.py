@@ -191,12 +191,14 @@ def test_zero_query_selects_lowest_blocks_and_averages_v():
         assert np.abs(dec.out[0, kvh * 8].cpu().numpy() - mean).max() <= 2e-3
 
 
-def test_ties_break_to_lower_index_exactly():
+@pytest.mark.parametrize("D", [64, 128])
+def test_ties_break_to_lower_index_exactly(D):
     """Integer-valued summaries and queries make every score exact in fp32, so
-    the selection with many exact ties must equal the oracle's bit for bit."""
+    the selection with many exact ties must equal the oracle's bit for bit
+    (head_dim 64: CUDA-core scorer; 128: tensor-core scorer)."""
     from query_aware_sparse_hs_gb300.decode import SparseDecode
     gen = np.random.default_rng(7)
-    batch, hkv, g, D, B, L = 3, 2, 4, 64, 16, 16 * 300
+    batch, hkv, g, B, L = 3, 2, 4, 16, 16 * 300
     nb = L // B
     dec = SparseDecode(num_q_heads=hkv * g, num_kv_heads=hkv, head_dim=D, block_size=B, kv_dtype="bf16",
                        batch=batch, max_blocks=nb, sink_tokens=16, window_tokens=32, k_scored=37)
