@@ -30,6 +30,7 @@ struct AttnArgs {
   int32_t blocks_per_split;
   int32_t splits;
   int32_t sms;  // multiprocessors of the current device (persistent grid size)
+  int32_t merged = 0;  // set by a launcher that already wrote out / lse (fused merge)
 };
 
 struct HotView {
@@ -57,7 +58,7 @@ cudaError_t launch_score_tc(const KvView& kv, const void* q, const void* smin, c
 cudaError_t launch_select_only(const KvView& kv, const SelectArgs& a, const float* scores, unsigned* err,
                                cudaStream_t st);
 cudaError_t launch_attn_simt(const KvView& kv, const AttnArgs& a, unsigned* err, cudaStream_t st);
-cudaError_t launch_attn_tc(const KvView& kv, const AttnArgs& a, unsigned* err, cudaStream_t st);
+cudaError_t launch_attn_tc(const KvView& kv, AttnArgs& a, unsigned* err, cudaStream_t st);
 bool attn_tc_supported(const KvView& kv);
 cudaError_t launch_merge(const KvView& kv, const AttnArgs& a, cudaStream_t st);
 cudaError_t launch_swapin(const HotView& hb, const int32_t* sel, const int32_t* sel_count,

@@ -81,7 +81,7 @@ def test_scores_and_selection(cases, name):
 
 
 @pytest.mark.parametrize("algo", ["simt", "tcgen05"])
-@pytest.mark.parametrize("bps", [0, 1, 3])
+@pytest.mark.parametrize("bps", [0, 1, 3, 8])
 @pytest.mark.parametrize("name", list(CASES))
 def test_attention_on_oracle_selection(cases, name, bps, algo):
     """Attention with the oracle's own selection fed to the GPU call."""
