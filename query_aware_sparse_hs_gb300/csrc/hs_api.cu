@@ -106,8 +106,7 @@ void split_geometry(const hs_attn_shape* s, int batch, int capacity, const hs_at
     const int64_t n_sm = sms > 0 ? sms : 148;
     // few (request, kv head) pairs: one wave of CTAs, each pair split evenly;
     // many pairs: about two items per SM
-    // (at most 8 splits in that case, so a pair's splits fit in one cluster)
-    int64_t want = pairs <= 0 ? 1 : (pairs <= n_sm ? (n_sm / pairs < 8 ? n_sm / pairs : 8) : (2 * n_sm + pairs - 1) / pairs);
+    int64_t want = pairs <= 0 ? 1 : (pairs <= n_sm ? n_sm / pairs : (2 * n_sm + pairs - 1) / pairs);
     if (want < 1) want = 1;
     if (want > cap) want = cap;
     bps = static_cast<int>((cap + want - 1) / want);

@@ -22,13 +22,10 @@
 //               groups working on alternate chunks, merged per work item.
 // Every wait is bounded (2 s); on a time-out the CTA sets HS_EBIT_TIMEOUT,
 // stops all roles, lets in-flight copies land and frees its TMEM.
-#include <cooperative_groups.h>
 #include <cuda.h>
 
 #include "hs_internal.h"
 #include "tc_ptx.cuh"
-
-namespace cg = cooperative_groups;
 
 namespace hs {
 namespace {
@@ -59,12 +56,11 @@ struct TcArgs {
   const float* v_scales;
   float* ws_o;
   float* ws_lse;
-  void* out;       // fused merge: final output and lse
+  void* out;       // one split per pair: the final output and lse are written directly
   float* lse_out;
   int64_t num_pages;
   int hkv, hq, group, block, max_blocks, capacity, bps, splits, items;
   int out_f32;
-  int fused;       // 1: one item per CTA, the CTAs of a (request, kv head) form a cluster and merge in it
   float scale_log2;
 };
 
@@ -110,58 +106,22 @@ __device__ __forceinline__ Item item_geom(const TcArgs& a, int item, int bpc) {
 }
 
 
-// A split's result: written to the global partial workspace, or - fused
-// merge - kept in this CTA's shared memory (stage 0, free once the item is
-// done) for the cluster's rank 0 to combine.
-__device__ __forceinline__ void put_partial(const TcArgs& a, uint8_t* smem, int64_t row0, int h, int t, float o,
-                                            float lse) {
-  if (a.fused) {
-    float* part = reinterpret_cast<float*>(smem);  // [16][128] then lse[16]
-    part[h * kD + t] = o;
-    if (t == 0) part[16 * kD + h] = lse;
+// A split's result: with one split per (request, kv head) it is the final
+// output (written directly, no merge pass); otherwise it goes to the partial
+// workspace for the log-sum-exp merge.
+__device__ __forceinline__ void put_partial(const TcArgs& a, int64_t row0, int h, int t, float o, float lse) {
+  if (a.splits == 1) {
+    const int64_t orow = row0 + h;  // row0 = (b * hq + kvh * g) * splits with splits == 1
+    if (a.out_f32)
+      static_cast<float*>(a.out)[orow * kD + t] = o;
+    else
+      static_cast<__nv_bfloat16*>(a.out)[orow * kD + t] = __float2bfloat16_rn(o);
+    if (a.lse_out && t == 0) a.lse_out[orow] = lse;
   } else {
     const int64_t row = row0 + static_cast<int64_t>(h) * a.splits;
     a.ws_o[row * kD + t] = o;
     if (t == 0) a.ws_lse[row] = lse;
   }
-}
-
-// Fused merge: rank 0 of the cluster combines every rank's (o, lse) per head
-// by the log-sum-exp rule and writes out and lse.  All threads of every CTA
-// of the cluster call this after their roles are done.
-__device__ __forceinline__ void cluster_merge(const TcArgs& a, uint8_t* smem) {
-  cg::cluster_group cluster = cg::this_cluster();
-  cluster.sync();  // every rank's partial is in its shared memory
-  const int t = threadIdx.x;
-  if (cluster.block_rank() == 0 && t < kD) {
-    const int nr = static_cast<int>(cluster.num_blocks());
-    const int pair = blockIdx.x / a.splits;
-    const int b = pair / a.hkv, kvh = pair - b * a.hkv;
-    float* part = reinterpret_cast<float*>(smem);
-    for (int h = 0; h < a.group; ++h) {
-      float M = -INFINITY;
-      for (int r = 0; r < nr; ++r) M = fmaxf(M, cluster.map_shared_rank(part, r)[16 * kD + h]);
-      float o = 0.0f, lse = -INFINITY;
-      if (M != -INFINITY) {
-        float tot = 0.0f, acc = 0.0f;
-        for (int r = 0; r < nr; ++r) {
-          const float* pr = cluster.map_shared_rank(part, r);
-          const float w = expf(pr[16 * kD + h] - M);
-          tot += w;
-          acc = fmaf(w, pr[h * kD + t], acc);
-        }
-        o = acc / tot;
-        lse = M + logf(tot);
-      }
-      const int64_t orow = static_cast<int64_t>(b) * a.hq + kvh * a.group + h;
-      if (a.out_f32)
-        static_cast<float*>(a.out)[orow * kD + t] = o;
-      else
-        static_cast<__nv_bfloat16*>(a.out)[orow * kD + t] = __float2bfloat16_rn(o);
-      if (a.lse_out && t == 0) a.lse_out[orow] = lse;
-    }
-  }
-  cluster.sync();  // rank 0 has read every peer before they exit
 }
 
 // First item at or after `item` (stepping by the grid) that has chunks; a.items if none.
@@ -613,13 +573,13 @@ __global__ void __launch_bounds__(kThreadsB, 1)
             const float e1 = m1 == -INFINITY ? 0.0f : exp2f(m1 - mx);
             const float lt = l0 * e0 + l1 * e1;
             const float ot = oacc[h] * e0 + xo[h * 128 + t] * e1;
-            put_partial(a, smem, row0, h, t, lt > 0.0f ? ot / lt : 0.0f,
+            put_partial(a, row0, h, t, lt > 0.0f ? ot / lt : 0.0f,
                         lt > 0.0f ? (mx + log2f(lt)) * kLn2 : -INFINITY);
           }
         }
         named_barrier(3, 256);  // the exchange buffer is free again
       } else if (grp == 0) {
-        for (int h = 0; h < g; ++h) put_partial(a, smem, row0, h, t, 0.0f, -INFINITY);
+        for (int h = 0; h < g; ++h) put_partial(a, row0, h, t, 0.0f, -INFINITY);
       }
       item = next;
       it = nit;
@@ -632,7 +592,6 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   tc_fence_before();
   __syncthreads();
   if (*abort_flag && tid == 0) set_error(err, HS_EBIT_TIMEOUT);
-  if (a.fused) cluster_merge(a, smem);
   if (warp == kMma1B) {
     tc_fence_after();
     tmem_dealloc(tmem, Ly::kTmemCols);
@@ -866,7 +825,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int64_t row0 = (static_cast<int64_t>(it.b) * a.hq + it.kvh * g) * a.splits + it.split;
       if (it.nch == 0) {
-        for (int h = 0; h < g; ++h) put_partial(a, smem, row0, h, t, 0.0f, -INFINITY);
+        for (int h = 0; h < g; ++h) put_partial(a, row0, h, t, 0.0f, -INFINITY);
         item = next;
         it = nit;
 #pragma unroll
@@ -995,7 +954,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!take_o(c - 1)) break;
       for (int h = 0; h < g && h < NH; ++h) {
         const float lt = rs[h] + rs[NH + h] + rs[2 * NH + h] + rs[3 * NH + h];
-        put_partial(a, smem, row0, h, t, lt > 0.0f ? oacc[h] / lt : 0.0f,
+        put_partial(a, row0, h, t, lt > 0.0f ? oacc[h] / lt : 0.0f,
                     lt > 0.0f ? (m[h] + log2f(lt)) * kLn2 : -INFINITY);
       }
       named_barrier(1, 128);
@@ -1009,7 +968,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   if (*abort_flag && tid == 0) set_error(err, HS_EBIT_TIMEOUT);
-  if (a.fused) cluster_merge(a, smem);
   if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, Ly::kTmemCols);
@@ -1085,39 +1043,10 @@ TcArgs make_args(const KvView& kv, const AttnArgs& aa) {
   a.bps = aa.blocks_per_split;
   a.splits = aa.splits;
   a.items = kv.batch * kv.hkv * aa.splits;
-  // one wave of items: the splits of a (request, kv head) run as one cluster
-  // and merge through distributed shared memory (no merge kernel)
-  a.fused = (a.items <= aa.sms && aa.splits <= 8) ? 1 : 0;
   a.scale_log2 = aa.scale * kLog2e;
   return a;
 }
 
-
-// PDL launch, with the cluster of a (request, kv head)'s splits when the merge is fused
-template <typename... KArgs, typename... Args>
-cudaError_t launch_attn(void (*kern)(KArgs...), const TcArgs& a, int sms, int threads, int smem, cudaStream_t st,
-                        Args&&... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.fused ? a.items : (a.items < sms ? a.items : sms));
-  cfg.blockDim = dim3(threads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[2];
-  int n = 0;
-  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[n].val.programmaticStreamSerializationAllowed = 1;
-  ++n;
-  if (a.fused && a.splits > 1) {
-    attr[n].id = cudaLaunchAttributeClusterDimension;
-    attr[n].val.clusterDim.x = a.splits;
-    attr[n].val.clusterDim.y = 1;
-    attr[n].val.clusterDim.z = 1;
-    ++n;
-  }
-  cfg.attrs = attr;
-  cfg.numAttrs = n;
-  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
-}
 
 cudaError_t launch_fp8(const KvView& kv, AttnArgs& aa, unsigned* err, cudaStream_t st) {
   CUtensorMap mk, mv;
@@ -1130,8 +1059,9 @@ cudaError_t launch_fp8(const KvView& kv, AttnArgs& aa, unsigned* err, cudaStream
   cudaError_t e = cudaFuncSetAttribute(attn_tc_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        Layout8::kAlloc);
   if (e != cudaSuccess) return e;
-  aa.merged = a.fused;
-  return launch_attn(attn_tc_fp8_kernel, a, aa.sms, kThreads, Layout8::kAlloc, st, mk, mv, a, err);
+  aa.merged = aa.splits == 1;
+  const int grid = a.items < aa.sms ? a.items : aa.sms;
+  return launch_pdl(attn_tc_fp8_kernel, dim3(grid), dim3(kThreads), Layout8::kAlloc, st, mk, mv, a, err);
 }
 
 template <int NH>
@@ -1147,8 +1077,9 @@ cudaError_t launch_nh(const KvView& kv, AttnArgs& aa, unsigned* err, cudaStream_
   auto kern = attn_tc_kernel<NH>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::kAlloc);
   if (e != cudaSuccess) return e;
-  aa.merged = a.fused;
-  return launch_attn(kern, a, aa.sms, kThreadsB, Ly::kAlloc, st, mk, mv, a, err);
+  aa.merged = aa.splits == 1;
+  const int grid = a.items < aa.sms ? a.items : aa.sms;
+  return launch_pdl(kern, dim3(grid), dim3(kThreadsB), Ly::kAlloc, st, mk, mv, a, err);
 }
 
 }  // namespace
