@@ -125,14 +125,18 @@ def dist_env():
     return rank, world, local
 
 
-def max_over_ranks(value: float, world: int, device) -> float:
+def whole_job_rate(units: float, ms: float, world: int, device) -> tuple:
+    """Replicas: every rank times its own units; the job's rate is all units
+    over the slowest rank's time.  Returns (rate per second, max ms)."""
     if world == 1:
-        return value
+        return units / (ms / 1e3), ms
     import torch
     import torch.distributed as dist
-    t = torch.tensor([value], dtype=torch.float64, device=device)
+    u = torch.tensor([units], dtype=torch.float64, device=device)
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
+    return float(u.item()) / (float(t.item()) / 1e3), float(t.item())
 
 
 def barrier(world: int):
@@ -347,10 +351,8 @@ def run_ours(args, w):
     torch.cuda.synchronize()
     barrier(world)
     clk = clocks.stop()
-    ms = e0.elapsed_time(e1)
-    ms = max_over_ranks(ms, world, dev)
+    value, ms = whole_job_rate(steps * w.batch * w.num_q_heads, e0.elapsed_time(e1), world, dev)
     ms_per_step = ms / steps
-    value = world * steps * w.batch * w.num_q_heads / (ms / 1e3)
 
     # ---- per-kernel times (each kernel alone, the same rotating layers) ----
     def timed_graph(fn, n=layers, rr=None):
@@ -419,8 +421,7 @@ def run_ours(args, w):
         replay(g_e2e, reps)
         b_.record(stream)
     stream.synchronize()
-    ms_e2e = max_over_ranks(a.elapsed_time(b_), world, dev)
-    e2e_value = world * steps * w.batch * w.num_q_heads / (ms_e2e / 1e3)
+    e2e_value, ms_e2e = whole_job_rate(steps * w.batch * w.num_q_heads, a.elapsed_time(b_), world, dev)
     h2d = qs[0].numel() * qs[0].element_size()
     d2h = d0.out.numel() * d0.out.element_size() + d0.lse.numel() * 4
 
@@ -551,10 +552,9 @@ def run_offload(args, w):
     barrier(world)
     clk = clocks.stop()
     st = stats.cpu().tolist()
-    ms = max_over_ranks(ms, world, dev)
     steps = passes * timed_steps
+    value, ms = whole_job_rate(steps * w.batch * w.num_q_heads, ms, world, dev)
     ms_per_step = ms / steps
-    value = world * steps * w.batch * w.num_q_heads / (ms / 1e3)
 
     # per-kernel times over one pass, each kernel bracketed by events (eager)
     ev = {k: [] for k in ("select", "swapin", "attention")}
