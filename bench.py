@@ -252,6 +252,12 @@ def workload_config(w, layers: int) -> dict:
 # GPU arm
 # ----------------------------------------------------------------------------
 
+# DRAM bytes (read + written) of one attention launch from an ncu capture of the
+# current kernel (profiles/ncu_full_llama8b_bf16_1layer.md), per workload;
+# a workload without a capture of the current kernel reports null.
+NCU_TRAFFIC = {"llama8b_bf16": 33_759_232}
+
+
 def run_ours(args, w):
     import numpy as np
     import torch
@@ -440,7 +446,7 @@ def run_ours(args, w):
         "hbm_gbs_step": step_bytes / (ms_per_step * 1e-3) / 1e9,
         "roofline": {"bound": "hbm", "kernel": "sparse_paged_decode_attn", "achieved": attn_gbs,
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": attn_gbs / peak,
-                     "traffic": None, "algorithmic_bytes_per_launch": a_bytes,
+                     "traffic": NCU_TRAFFIC.get(w.name), "algorithmic_bytes_per_launch": a_bytes,
                      "avg_launch_us": t_attn},
         "kernels_us": {"summary_refresh": t_ref, "score_select": t_sel, "attention_with_merge": t_attn,
                        "summary_build_full": t_sum_full},
