@@ -3,8 +3,9 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload llama8b_bf16|fp8_g32|ragged_bf16|offload_bf16]
 
-A step = the whole per-step path of one layer over the batch: summary refresh
-of the block holding the newest token, bound scoring + top-k selection,
+A step = the whole per-step path of one layer over the batch: append of the
+newest token (written into its page, e4m3-quantised for the e4m3 cache, its
+block's summary widened), bound scoring + top-k selection,
 [swap-in for the offload workload], gather-attention with split-K, LSE merge.
 The default workload is the Llama-3-8B-like bf16 layer (8 requests x 32768
 tokens, 32 q / 4 kv heads, head_dim 128, 64-token blocks, 2048-token budget).
@@ -62,6 +63,30 @@ def attn_bytes(w, selected_tokens: int, pairs_blocks: int) -> int:
     the selection indices and the page-table entries they resolve."""
     qb = w.batch * w.num_q_heads * w.head_dim * (4 if w.kv_dtype == "f32" else 2)
     return int(selected_tokens * token_bytes(w) + 2 * qb + 8 * pairs_blocks)
+
+
+def append_bytes_per_step(w) -> int:
+    """The newest token of every (request, kv head): its K/V read in source
+    precision, written as stored, and its block's summary row pair read and
+    written."""
+    src = 2 * w.head_dim * (4 if w.kv_dtype == "f32" else 2)
+    return int(w.batch * w.num_kv_heads * (src + token_bytes(w) + 2 * summary_bytes_per_block(w)))
+
+
+def step_launches(w, dec, hot: bool = False) -> int:
+    """Kernels of one step as the library dispatches them for this workload:
+    append (not on the offload path), bound scoring + selection (two launches
+    with bf16 summaries at head_dim 128, else one), the swap-in (offload),
+    attention, and the split merge unless the tensor-core attention gives
+    every pair a single split."""
+    n = 0 if hot else 1
+    n += 2 if (w.kv_dtype != "f32" and w.head_dim == 128) else 1
+    n += 1 if hot else 0
+    n += 1
+    tc = w.kv_dtype in ("bf16", "fp8") and w.head_dim == 128 and w.block_size in (16, 32, 64, 128)
+    per_split = w.batch * w.num_q_heads * (w.head_dim + 1) * 4
+    splits = dec.workspace.numel() // per_split
+    return n + (0 if tc and splits <= 1 else 1)
 
 
 def select_bytes(w, total_blocks: int) -> int:
@@ -180,16 +205,23 @@ class OracleStep:
             smin, smax = O.stored_summaries(*O.block_summaries(K, B), w.kv_dtype)
             g = w.group
             qg = x["q"][0, kvh * g:(kvh + 1) * g].float().numpy().astype(np.float64)
-            self.pairs.append((K, V, smin, smax, qg, L))
+            newest = (O.gather_rows(x["k_pages"].float().numpy(), row, L, B)[L - 1:],
+                      O.gather_rows(x["v_pages"].float().numpy(), row, L, B)[L - 1:])
+            self.pairs.append((K, V, smin, smax, qg, L, newest))
         self.i = 0
 
     def step(self):
-        """One pair's per-step work: refresh the newest block's summary, score,
-        select, attend."""
+        """One pair's per-step work: append the newest token (e4m3: quantise
+        it) and rebuild its block's summary, score, select, attend."""
         O, w = self.O, self.w
-        K, V, smin, smax, qg, L = self.pairs[self.i % len(self.pairs)]
+        K, V, smin, smax, qg, L, newest = self.pairs[self.i % len(self.pairs)]
         self.i += 1
         B = w.block_size
+        if w.kv_dtype == "fp8":
+            for rows, dst in zip(newest, (K, V)):
+                dst[L - 1:] = O.kv_values("fp8", *O.quantize_e4m3_g32(rows))
+        else:
+            K[L - 1:], V[L - 1:] = O.kv_values(w.kv_dtype, newest[0]), O.kv_values(w.kv_dtype, newest[1])
         j = (L - 1) // B
         lo, hi = O.stored_summaries(*O.block_summaries(K[j * B:L], B), w.kv_dtype)
         smin[j], smax[j] = lo[0], hi[0]
@@ -210,7 +242,7 @@ def cpu_baseline(w, seconds: float = 12.0) -> dict:
     dt = time.perf_counter() - t0
     return {"value": heads / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"{n} single-(request, kv head) steps of {w.name} (8 query heads each, "
-                      f"{w.ctx_max} tokens, summary refresh + bound + selection + attention), "
+                      f"{w.ctx_max} tokens, append + bound + selection + attention), "
                       f"numpy float64, 1 thread, {dt:.1f} s"}
 
 
@@ -280,11 +312,15 @@ def run_ours(args, w):
         layers = int(max(1, min(32, (24 << 30) // max(per_layer, 1))))
     lens, table = layout["seq_lens"], layout["page_table"]
     B, D = w.block_size, w.head_dim
-    L_last_block = int(((lens.max().item() - 1) // B))
-    decs, kvs, qs, keep = [], [], [], []
+    decs, kvs, qs, news, keep = [], [], [], [], []
     for layer in range(layers):
         x = make_layer(w, layout, dev, layer)
         k, v, q = x["k_pages"], x["v_pages"], x["q"]
+        # the newest token's K/V (source precision), appended again every step
+        t_last = (lens.long() - 1)[:, None].expand(w.batch, w.num_kv_heads)
+        pg = table[torch.arange(w.batch, device=dev)[:, None], torch.arange(w.num_kv_heads, device=dev)[None, :],
+                   t_last // w.block_size].long()
+        new_kv = (k[pg, t_last % w.block_size].contiguous(), v[pg, t_last % w.block_size].contiguous())
         ks = vs = None
         if w.kv_dtype == "fp8":
             kc = torch.empty(k.shape, dtype=torch.uint8, device=dev)
@@ -304,6 +340,7 @@ def run_ours(args, w):
         decs.append(dec)
         kvs.append(kv)
         qs.append(q)
+        news.append(new_kv)
         keep.append((k, v, ks, vs))
     torch.cuda.synchronize()
     st_, bits = hs.hs_get_device_error()
@@ -315,7 +352,7 @@ def run_ours(args, w):
     def one_step(i, q_override=None):
         d = decs[i % layers]
         d.step(kvs[i % layers], qs[i % layers] if q_override is None else q_override,
-               refresh_from_block=L_last_block, stream=stream)
+               new_kv=news[i % layers], stream=stream)
 
     # eager warm-up (module load, cluster attributes) before capture
     with torch.cuda.stream(stream):
@@ -377,7 +414,7 @@ def run_ours(args, w):
 
     t_attn = timed_graph(lambda i: decs[i % layers].attend(kvs[i % layers], qs[i % layers], stream))
     t_sel = timed_graph(lambda i: decs[i % layers].select(kvs[i % layers], qs[i % layers], stream=stream))
-    t_ref = timed_graph(lambda i: decs[i % layers].build_summaries(kvs[i % layers], L_last_block, stream))
+    t_app = timed_graph(lambda i: decs[i % layers].append(kvs[i % layers], *news[i % layers], stream))
     t_sum_full = timed_graph(lambda i: decs[i % layers].build_summaries(kvs[i % layers], 0, stream), rr=3)
 
     # algorithmic bytes from the actual selection
@@ -395,8 +432,8 @@ def run_ours(args, w):
     total_blocks = int(sum(w.num_kv_heads * ((int(L) + B - 1) // B) for L in lens_np))
     a_bytes = attn_bytes(w, sel_tokens, pairs_blocks)
     s_bytes = select_bytes(w, total_blocks)
-    refresh_bytes = w.batch * w.num_kv_heads * (B * token_bytes(w) / 2 + summary_bytes_per_block(w))
-    step_bytes = a_bytes + s_bytes + refresh_bytes
+    append_bytes = append_bytes_per_step(w)
+    step_bytes = a_bytes + s_bytes + append_bytes
     full_sum_bytes = total_blocks * (B * token_bytes(w) / 2 + summary_bytes_per_block(w))
     peak, peak_kind = load_peaks()
     attn_gbs = a_bytes / (t_attn * 1e-6) / 1e9
@@ -406,12 +443,15 @@ def run_ours(args, w):
     for i in range(layers):
         q_host[i].copy_(qs[i].cpu())
     q_dev = [torch.empty_like(qs[i]) for i in range(layers)]
+    new_host = [tuple(t.cpu().pin_memory() for t in news[i]) for i in range(layers)]
     out_host = torch.empty((layers,) + tuple(d0.out.shape), dtype=d0.out.dtype).pin_memory()
     lse_host = torch.empty((layers,) + tuple(d0.lse.shape), dtype=torch.float32).pin_memory()
 
     def e2e_step(i):
         li = i % layers
         q_dev[li].copy_(q_host[li], non_blocking=True)
+        news[li][0].copy_(new_host[li][0], non_blocking=True)
+        news[li][1].copy_(new_host[li][1], non_blocking=True)
         one_step(i, q_dev[li])
         out_host[li].copy_(decs[li].out, non_blocking=True)
         lse_host[li].copy_(decs[li].lse, non_blocking=True)
@@ -428,7 +468,7 @@ def run_ours(args, w):
         b_.record(stream)
     stream.synchronize()
     e2e_value, ms_e2e = whole_job_rate(steps * w.batch * w.num_q_heads, a.elapsed_time(b_), world, dev)
-    h2d = qs[0].numel() * qs[0].element_size()
+    h2d = qs[0].numel() * qs[0].element_size() + sum(t.numel() * t.element_size() for t in news[0])
     d2h = d0.out.numel() * d0.out.element_size() + d0.lse.numel() * 4
 
     st_, bits = hs.hs_get_device_error()
@@ -437,7 +477,7 @@ def run_ours(args, w):
     if rank != 0:
         return
     cpu = cpu_baseline(w, seconds=args.cpu_seconds) if (world == 1 and args.cpu_seconds > 0) else None
-    launches_per_step = 4  # summary refresh, score+select, attention, merge
+    launches_per_step = step_launches(w, d0)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
         "warmup": wreps * layers, "ms_per_step": ms_per_step, "higher_is_better": True,
@@ -448,12 +488,12 @@ def run_ours(args, w):
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": attn_gbs / peak,
                      "traffic": NCU_TRAFFIC.get(w.name), "algorithmic_bytes_per_launch": a_bytes,
                      "avg_launch_us": t_attn},
-        "kernels_us": {"summary_refresh": t_ref, "score_select": t_sel, "attention_with_merge": t_attn,
+        "kernels_us": {"append": t_app, "score_select": t_sel, "attention_with_merge": t_attn,
                        "summary_build_full": t_sum_full},
         "kernels_gbs": {"score_select": s_bytes / (t_sel * 1e-6) / 1e9,
                         "attention_with_merge": attn_gbs,
                         "summary_build_full": full_sum_bytes / (t_sum_full * 1e-6) / 1e9},
-        "bytes_per_step": {"attention": a_bytes, "score_select": s_bytes, "summary_refresh": int(refresh_bytes)},
+        "bytes_per_step": {"attention": a_bytes, "score_select": s_bytes, "append": int(append_bytes)},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": ms_e2e / steps},
@@ -624,7 +664,7 @@ def run_offload(args, w):
         "kernels_us": {"score_select": t_us["select"], "swapin": t_us["swapin"], "attention_with_merge": t_us["attention"]},
         "cpu_baseline": cpu_baseline(w, seconds=args.cpu_seconds) if (world == 1 and args.cpu_seconds > 0) else None,
         "e2e": None,
-        "gpu_launches": 4 * steps,
+        "gpu_launches": step_launches(w, dec, hot=True) * steps,
         "clocks": clk,
     }
     print(json.dumps(line), flush=True)

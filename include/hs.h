@@ -200,6 +200,25 @@ HS_API hs_status hs_build_block_summaries(const hs_attn_shape* shape, const hs_p
                                    int32_t first_block, void* smin, void* smax,
                                    hs_stream_t stream);
 
+/* Append step of a decode loop, [KVS] §5 (summaries kept current) with the
+ * grouped e4m3 storage of [FLL] §2.4 + §3.2: for every (b, kvh) with
+ * seq_lens[b] > 0, the token at t = seq_lens[b] - 1 (block j = t / B, row
+ * t % B) is written into page page_table[b][kvh][j], and the summaries of
+ * block j are widened to it, so that afterwards they equal what
+ * hs_build_block_summaries computes over the block.  Row 0 starts the block's
+ * summary afresh; other rows require the summary of tokens jB .. t-1 to be
+ * current.  The caller updates seq_lens (to include the new token) and
+ * page_table (a page for a new block) before the call.
+ *   new_k, new_v  [batch][Hkv][D]  f32 for f32 K/V, bf16 otherwise; an e4m3
+ *                 cache stores them quantised as hs_quantize_e4m3_g32 does
+ *                 (codes into k_pages/v_pages, scales into k_scales/v_scales).
+ *   The call WRITES through kv->k_pages, v_pages, k_scales and v_scales: they
+ *   must point to writable device memory.
+ * A block index >= max_blocks sets HS_EBIT_BLOCK_RANGE, a page id outside
+ * [0, num_pages) sets HS_EBIT_PAGE_RANGE; that stream is left unchanged. */
+HS_API hs_status hs_append_token(const hs_attn_shape* shape, const hs_paged_kv* kv, const void* new_k,
+                                 const void* new_v, void* smin, void* smax, hs_stream_t stream);
+
 /* Bytes of workspace hs_score_select_topk needs when scores_opt is NULL: one
  * fp32 score per block, [batch][Hkv][max_blocks].  0 on invalid input. */
 HS_API size_t hs_select_workspace_bytes(const hs_attn_shape* shape, int32_t batch, int32_t max_blocks);

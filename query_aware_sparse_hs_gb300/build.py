@@ -24,7 +24,7 @@ LIB = os.path.join(OUT_DIR, "libhs.so")
 BUILD = os.path.join(ROOT, "_build")
 
 SOURCES = ["hs_api.cu", "k_summary.cu", "k_select.cu", "k_score_tc.cu", "k_attn_simt.cu", "k_attn_tc.cu",
-           "k_swapin.cu", "k_quant.cu"]
+           "k_swapin.cu", "k_quant.cu", "k_append.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVFLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
            "--expt-relaxed-constexpr"]

@@ -175,6 +175,21 @@ hs_status hs_build_block_summaries(const hs_attn_shape* shape, const hs_paged_kv
                                     reinterpret_cast<cudaStream_t>(stream)));
 }
 
+hs_status hs_append_token(const hs_attn_shape* shape, const hs_paged_kv* kv, const void* new_k,
+                          const void* new_v, void* smin, void* smax, hs_stream_t stream) {
+  hs_status st = check_shape(shape);
+  if (st != HS_OK) return st;
+  if ((st = check_kv(shape, kv, true)) != HS_OK) return st;
+  if (!new_k || !new_v || !smin || !smax) return HS_ERR_INVALID_ARG;
+  if (!aligned(new_k, 16) || !aligned(new_v, 16) || !aligned(smin, 16) || !aligned(smax, 16))
+    return HS_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(kv->batch) * shape->num_kv_heads > INT32_MAX) return HS_ERR_UNSUPPORTED;
+  Device d;
+  if ((st = current_device(&d)) != HS_OK) return st;
+  const KvView v = make_view(shape, kv);
+  return from_cuda(launch_append(v, new_k, new_v, smin, smax, d.err, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 hs_status hs_score_select_topk(const hs_attn_shape* shape, const hs_paged_kv* kv, const void* q,
                                const void* smin, const void* smax,
                                const hs_select_params* params, int32_t* sel,

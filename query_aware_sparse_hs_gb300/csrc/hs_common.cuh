@@ -68,6 +68,30 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
+// Grouped e4m3 quantisation of one row held C consecutive channels per lane
+// ("分块稀疏注意力与KV Cache量化" §2.4 grouped scales, §3.2 group size 32):
+// scale = amax of the 32-channel group / 448 (1 when the group is all zero),
+// code = e4m3(x / scale), nearest-even, saturating.  All 32 lanes must call
+// it.  Returns the lane's group scale.
+template <int C>
+__device__ __forceinline__ float quantize_e4m3_lane(const float (&x)[C], uint8_t (&out)[C]) {
+  constexpr int kLanesPerGroup = kQuantGroup / C;
+  float amax = 0.0f;
+#pragma unroll
+  for (int c = 0; c < C; ++c) amax = fmaxf(amax, fabsf(x[c]));
+#pragma unroll
+  for (int o = kLanesPerGroup / 2; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const float scale = amax > 0.0f ? amax / 448.0f : 1.0f;  // IEEE division
+#pragma unroll
+  for (int c = 0; c < C; c += 2) {
+    float2 y = make_float2(x[c] / scale, x[c + 1] / scale);
+    __nv_fp8x2_storage_t two = __nv_cvt_float2_to_fp8x2(y, __NV_SATFINITE, __NV_E4M3);
+    out[c] = static_cast<uint8_t>(two & 0xff);
+    out[c + 1] = static_cast<uint8_t>(two >> 8);
+  }
+  return scale;
+}
+
 __host__ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
 // Programmatic dependent launch: every kernel of a step lets its successor be

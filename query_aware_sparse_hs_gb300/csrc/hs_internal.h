@@ -48,6 +48,9 @@ struct HotView {
   int32_t batch, hkv, max_blocks, slots, block, head_dim, kv_dtype;
 };
 
+// Newest token of every stream into its page + widening of its block's summary.
+cudaError_t launch_append(const KvView& kv, const void* new_k, const void* new_v, void* smin, void* smax,
+                          unsigned* err, cudaStream_t st);
 cudaError_t launch_summaries(const KvView& kv, int first_block, void* smin, void* smax,
                              unsigned* err, cudaStream_t st);
 cudaError_t launch_score_select(const KvView& kv, const SelectArgs& a, unsigned* err,

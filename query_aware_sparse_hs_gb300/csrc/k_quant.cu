@@ -28,20 +28,8 @@ __global__ __launch_bounds__(kWarps * 32) void quant_kernel(const void* __restri
 #pragma unroll
     for (int c = 0; c < C; ++c) x[c] = bf16_bits_to_float(p[c]);
   }
-  float amax = 0.0f;
-#pragma unroll
-  for (int c = 0; c < C; ++c) amax = fmaxf(amax, fabsf(x[c]));
-#pragma unroll
-  for (int o = kLanesPerGroup / 2; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-  const float scale = amax > 0.0f ? amax / 448.0f : 1.0f;  // IEEE division
   uint8_t out[C];
-#pragma unroll
-  for (int c = 0; c < C; c += 2) {
-    float2 y = make_float2(x[c] / scale, x[c + 1] / scale);
-    __nv_fp8x2_storage_t two = __nv_cvt_float2_to_fp8x2(y, __NV_SATFINITE, __NV_E4M3);
-    out[c] = static_cast<uint8_t>(two & 0xff);
-    out[c + 1] = static_cast<uint8_t>(two >> 8);
-  }
+  const float scale = quantize_e4m3_lane<C>(x, out);
   uint8_t* q = codes + row * D + lane * C;
 #pragma unroll
   for (int c = 0; c < C; ++c) q[c] = out[c];

@@ -1,6 +1,6 @@
 """Decode-step driver: owns the per-step device buffers and issues the library
-calls of one step in order (summary refresh -> score/select -> [swap-in] ->
-attention).  All buffers are torch allocations made once in the constructor;
+calls of one step in order (token append or summary refresh -> score/select
+-> [swap-in] -> attention).  All buffers are torch allocations made once in the constructor;
 a step itself allocates nothing, so it can be captured in a CUDA graph.
 """
 
@@ -46,6 +46,11 @@ class SparseDecode:
     def build_summaries(self, kv: hs.PagedKV, first_block: int = 0, stream=None):
         hs.hs_build_block_summaries(self.shape, kv, first_block, self.smin, self.smax, stream)
 
+    def append(self, kv: hs.PagedKV, new_k: torch.Tensor, new_v: torch.Tensor, stream=None):
+        """Writes the newest token's K/V ([batch][Hkv][D]) at seq_lens - 1 and
+        widens its block's summaries (the caller has advanced seq_lens)."""
+        hs.hs_append_token(self.shape, kv, new_k, new_v, self.smin, self.smax, stream)
+
     def select(self, kv: hs.PagedKV, q: torch.Tensor, keep_scores: bool = True, stream=None):
         hs.hs_score_select_topk(self.shape, kv, q, self.smin, self.smax, self.sel_params, self.sel,
                                 self.sel_count, self.scores if keep_scores else None, None, stream)
@@ -58,12 +63,16 @@ class SparseDecode:
         hs.hs_swapin_misses(self.shape, hb, self.sel, self.sel_count, self.capacity, step, stats, stream)
 
     def step(self, kv: hs.PagedKV, q: torch.Tensor, refresh_from_block: int | None = None,
-             hot: tuple | None = None, stream=None):
-        """One decode step.  ``refresh_from_block``: rebuild summaries of blocks
+             hot: tuple | None = None, new_kv: tuple | None = None, stream=None):
+        """One decode step.  ``new_kv``: (new_k, new_v) of the token at
+        seq_lens - 1, appended to the cache with its summary widened before
+        selecting.  ``refresh_from_block``: instead rebuild summaries of blocks
         from there on (the block holding the newest token) before selecting.
         ``hot``: (hot_buffer, slot_kv_view, step, stats) for the offload path:
         the selection is made against ``kv`` (summaries), pages are swapped into
         the hot slots and attention reads ``slot_kv_view``."""
+        if new_kv is not None:
+            self.append(kv, new_kv[0], new_kv[1], stream)
         if refresh_from_block is not None:
             self.build_summaries(kv, refresh_from_block, stream)
         self.select(kv, q, stream=stream)

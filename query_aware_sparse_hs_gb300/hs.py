@@ -73,6 +73,8 @@ SYMBOLS = {
     "hs_select_workspace_bytes": (c_size_t, [POINTER(AttnShape), c_int32, c_int32]),
     "hs_build_block_summaries": (c_int32, [POINTER(AttnShape), POINTER(PagedKV), c_int32, c_void_p,
                                            c_void_p, c_void_p]),
+    "hs_append_token": (c_int32, [POINTER(AttnShape), POINTER(PagedKV), c_void_p, c_void_p, c_void_p,
+                                  c_void_p, c_void_p]),
     "hs_score_select_topk": (c_int32, [POINTER(AttnShape), POINTER(PagedKV), c_void_p, c_void_p,
                                        c_void_p, POINTER(SelectParams), c_void_p, c_void_p, c_void_p,
                                        c_void_p, c_size_t, c_void_p]),
@@ -173,6 +175,12 @@ def hs_build_block_summaries(shape, kv, first_block, smin, smax, stream=None):
     _check(_lib.hs_build_block_summaries(ctypes.byref(shape), ctypes.byref(kv), int(first_block),
                                          _ptr(smin), _ptr(smax), _stream(stream)),
            "hs_build_block_summaries")
+
+
+def hs_append_token(shape, kv, new_k, new_v, smin, smax, stream=None):
+    _check(_lib.hs_append_token(ctypes.byref(shape), ctypes.byref(kv), _ptr(new_k), _ptr(new_v), _ptr(smin),
+                                _ptr(smax), _stream(stream)),
+           "hs_append_token")
 
 
 def hs_score_select_topk(shape, kv, q, smin, smax, params, sel, sel_count, scores=None,

@@ -63,6 +63,15 @@ def test_host_checks_reject_bad_arguments_without_a_gpu():
                                   ctypes.byref(params), 0x1000, 0x1000, None, None, 0, None)
     assert st == hs.HS_ERR_CAPACITY
     assert lib.hs_quantize_e4m3_g32(0x1000, 0, 10, 96, 0x1000, 0x1000, None) == hs.HS_ERR_UNSUPPORTED
+    # the append call: a missing new token, or an e4m3 cache without scales
+    full = hs.PagedKV()
+    full.k_pages = full.v_pages = full.page_table = full.seq_lens = 0x1000
+    full.batch, full.max_blocks, full.num_pages = 1, 4, 4
+    assert lib.hs_append_token(ctypes.byref(shape), ctypes.byref(full), None, 0x1000, 0x1000, 0x1000,
+                               None) == hs.HS_ERR_INVALID_ARG
+    fp8 = hs.attn_shape(32, 4, 128, 64, "fp8")
+    assert lib.hs_append_token(ctypes.byref(fp8), ctypes.byref(full), 0x1000, 0x1000, 0x1000, 0x1000,
+                               None) == hs.HS_ERR_INVALID_ARG
     assert lib.hs_workspace_bytes(ctypes.byref(bad), 8, 33, None) == 0
 
 
