@@ -73,14 +73,17 @@ def append_bytes_per_step(w) -> int:
     return int(w.batch * w.num_kv_heads * (src + token_bytes(w) + 2 * summary_bytes_per_block(w)))
 
 
-def step_launches(w, dec, hot: bool = False) -> int:
+def step_launches(w, dec, hot: bool = False, overlap: bool = False) -> int:
     """Kernels of one step as the library dispatches them for this workload:
     append (not on the offload path), bound scoring + selection (two launches
-    with bf16 summaries at head_dim 128, else one), the swap-in (offload),
-    attention, and the split merge unless the tensor-core attention gives
-    every pair a single split."""
+    with bf16 summaries at head_dim 128, else one), the swap-in (offload; with
+    the copy overlapped: plan, copy, attention over the hits, attention over
+    the misses and the merge of the two), attention, and the split merge unless
+    the tensor-core attention gives every pair a single split."""
     n = 0 if hot else 1
     n += 2 if (w.kv_dtype != "f32" and w.head_dim == 128) else 1
+    if hot and overlap:
+        return n + 5
     n += 1 if hot else 0
     n += 1
     tc = w.kv_dtype in ("bf16", "fp8") and w.head_dim == 128 and w.block_size in (16, 32, 64, 128)
@@ -312,7 +315,7 @@ def run_ours(args, w):
         layers = int(max(1, min(32, (24 << 30) // max(per_layer, 1))))
     lens, table = layout["seq_lens"], layout["page_table"]
     B, D = w.block_size, w.head_dim
-    decs, kvs, qs, news, keep = [], [], [], [], []
+    decs, kvs, qs, news, inputs, keep = [], [], [], [], [], []
     for layer in range(layers):
         x = make_layer(w, layout, dev, layer)
         k, v, q = x["k_pages"], x["v_pages"], x["q"]
@@ -320,7 +323,17 @@ def run_ours(args, w):
         t_last = (lens.long() - 1)[:, None].expand(w.batch, w.num_kv_heads)
         pg = table[torch.arange(w.batch, device=dev)[:, None], torch.arange(w.num_kv_heads, device=dev)[None, :],
                    t_last // w.block_size].long()
-        new_kv = (k[pg, t_last % w.block_size].contiguous(), v[pg, t_last % w.block_size].contiguous())
+        # q and the new K/V share one device buffer, so the end-to-end step
+        # brings its inputs over in one host-to-device copy
+        nq, nkv = q.numel(), w.batch * w.num_kv_heads * w.head_dim
+        packed = torch.empty(nq + 2 * nkv, dtype=q.dtype, device=dev)
+        packed[:nq].copy_(q.reshape(-1))
+        packed[nq:nq + nkv].copy_(k[pg, t_last % w.block_size].reshape(-1))
+        packed[nq + nkv:].copy_(v[pg, t_last % w.block_size].reshape(-1))
+        q = packed[:nq].view(q.shape)
+        new_kv = (packed[nq:nq + nkv].view(w.batch, w.num_kv_heads, w.head_dim),
+                  packed[nq + nkv:].view(w.batch, w.num_kv_heads, w.head_dim))
+        inputs.append(packed)
         ks = vs = None
         if w.kv_dtype == "fp8":
             kc = torch.empty(k.shape, dtype=torch.uint8, device=dev)
@@ -439,22 +452,16 @@ def run_ours(args, w):
     attn_gbs = a_bytes / (t_attn * 1e-6) / 1e9
 
     # ---- end to end through the C ABI with host buffers ----
-    q_host = [torch.empty_like(qs[i], device="cpu").pin_memory() for i in range(layers)]
-    for i in range(layers):
-        q_host[i].copy_(qs[i].cpu())
-    q_dev = [torch.empty_like(qs[i]) for i in range(layers)]
-    new_host = [tuple(t.cpu().pin_memory() for t in news[i]) for i in range(layers)]
-    out_host = torch.empty((layers,) + tuple(d0.out.shape), dtype=d0.out.dtype).pin_memory()
-    lse_host = torch.empty((layers,) + tuple(d0.lse.shape), dtype=torch.float32).pin_memory()
+    # per step: one copy of the step's inputs (q, new K/V) from pinned host
+    # memory, the step, one copy of its results (out, lse) back
+    in_host = [inputs[i].cpu().pin_memory() for i in range(layers)]
+    res_host = torch.empty((layers, d0.results.numel()), dtype=torch.uint8).pin_memory()
 
     def e2e_step(i):
         li = i % layers
-        q_dev[li].copy_(q_host[li], non_blocking=True)
-        news[li][0].copy_(new_host[li][0], non_blocking=True)
-        news[li][1].copy_(new_host[li][1], non_blocking=True)
-        one_step(i, q_dev[li])
-        out_host[li].copy_(decs[li].out, non_blocking=True)
-        lse_host[li].copy_(decs[li].lse, non_blocking=True)
+        inputs[li].copy_(in_host[li], non_blocking=True)
+        one_step(i)
+        res_host[li].copy_(decs[li].results, non_blocking=True)
 
     g_e2e = capture(e2e_step, layers)
     with torch.cuda.stream(stream):
@@ -468,8 +475,8 @@ def run_ours(args, w):
         b_.record(stream)
     stream.synchronize()
     e2e_value, ms_e2e = whole_job_rate(steps * w.batch * w.num_q_heads, a.elapsed_time(b_), world, dev)
-    h2d = qs[0].numel() * qs[0].element_size() + sum(t.numel() * t.element_size() for t in news[0])
-    d2h = d0.out.numel() * d0.out.element_size() + d0.lse.numel() * 4
+    h2d = inputs[0].numel() * inputs[0].element_size()
+    d2h = d0.results.numel()
 
     st_, bits = hs.hs_get_device_error()
     assert st_ == hs.HS_OK, (st_, bits)
@@ -547,6 +554,8 @@ def run_offload(args, w):
                        batch=w.batch, max_blocks=nb, sink_tokens=w.sink_tokens, window_tokens=w.window_tokens,
                        k_scored=w.k_scored, device=dev)
     dec.build_summaries(pool_kv)  # read over the host link once
+    if args.swap_overlap:
+        dec.enable_swap_overlap(args.swap_copy_ctas, args.swap_attn_ctas)
     stream = torch.cuda.Stream(device=dev)
 
     def reset():
@@ -567,11 +576,18 @@ def run_offload(args, w):
     with torch.cuda.graph(g, stream=stream):
         for t in range(1, steps_seq):
             step(t, stats)
+    # the same steps with the swap-in and attention one after the other
+    side, dec.side_stream = getattr(dec, "side_stream", None), None
+    g_serial = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_serial, stream=stream):
+        for t in range(1, steps_seq):
+            step(t, stats)
+    dec.side_stream = side
     timed_steps = steps_seq - 1
     passes = max(1, math.ceil(args.steps / timed_steps))
     warm_passes = max(1, math.ceil(args.warmup / timed_steps))
 
-    def run_pass(timed):
+    def run_pass(timed, graph=g):
         with torch.cuda.stream(stream):
             reset()
             step(0)  # refills the empty buffer: warm-up, not timed
@@ -579,7 +595,7 @@ def run_offload(args, w):
             if timed:
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a.record(stream)
-            g.replay()
+            graph.replay()
             if timed:
                 b.record(stream)
         stream.synchronize()
@@ -599,6 +615,9 @@ def run_offload(args, w):
     clk = clocks.stop()
     st = stats.cpu().tolist()
     steps = passes * timed_steps
+    serial_passes = max(1, min(passes, 4))
+    run_pass(False, g_serial)
+    ms_serial = sum(run_pass(True, g_serial) for _ in range(serial_passes)) / (serial_passes * timed_steps)
     value, ms = whole_job_rate(steps * w.batch * w.num_q_heads, ms, world, dev)
     ms_per_step = ms / steps
 
@@ -662,9 +681,11 @@ def run_offload(args, w):
                  "link_frac": swap_bytes_step / (t_us["swapin"] * 1e-6) / 1e9 / link,
                  "page_bytes": page_bytes},
         "kernels_us": {"score_select": t_us["select"], "swapin": t_us["swapin"], "attention_with_merge": t_us["attention"]},
+        "swap_overlap": {"overlapped": bool(args.swap_overlap), "copy_ctas": args.swap_copy_ctas,
+                         "attn_ctas": args.swap_attn_ctas, "serial_ms_per_step": ms_serial},
         "cpu_baseline": cpu_baseline(w, seconds=args.cpu_seconds) if (world == 1 and args.cpu_seconds > 0) else None,
         "e2e": None,
-        "gpu_launches": step_launches(w, dec, hot=True) * steps,
+        "gpu_launches": step_launches(w, dec, hot=True, overlap=bool(args.swap_overlap)) * steps,
         "clocks": clk,
     }
     print(json.dumps(line), flush=True)
@@ -679,6 +700,11 @@ def main():
     ap.add_argument("--workload", default="llama8b_bf16")
     ap.add_argument("--layers", type=int, default=0, help="distinct layer copies (0 = fit ~24 GB, max 32)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--swap-overlap", type=int, default=1,
+                    help="offload workload: 1 = page copy overlapped with attention over the hits, 0 = one after the other")
+    ap.add_argument("--swap-copy-ctas", type=int, default=24, help="CTAs (SMs) of the overlapped page copy")
+    ap.add_argument("--swap-attn-ctas", type=int, default=0,
+                    help="CTAs of the attention beside the copy (0 = the SMs the copy leaves)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     from synth import WORKLOADS

@@ -133,14 +133,19 @@ typedef struct hs_select_params {
 
 /* Attention options.  scale multiplies q.k (usually 1/sqrt(head_dim)).
  * blocks_per_split: selected blocks handled by one CTA before the LSE merge;
- * 0 = chosen by the library from the device's SM count.  algo: 0 = automatic,
- * 1 = CUDA-core kernel (every dtype), 2 = tensor-core (tcgen05) kernel (bf16 and
- * e4m3 only; HS_ERR_UNSUPPORTED otherwise). */
+ * 0 = chosen by the library from the SMs the call may use.  algo: 0 =
+ * automatic, 1 = CUDA-core kernel (every dtype), 2 = tensor-core (tcgen05)
+ * kernel (bf16 and e4m3 only; HS_ERR_UNSUPPORTED otherwise).  max_ctas: 0 =
+ * the tensor-core kernel runs one CTA on every SM; n > 0 = at most n CTAs (and
+ * the automatic split for n SMs), leaving the other SMs to work launched
+ * beside it, such as hs_swapin_copy.  Each of its CTAs takes a whole SM's
+ * shared memory, so nothing else fits on an SM it occupies. */
 typedef struct hs_attn_params {
   float scale;
   int32_t out_is_fp32;
   int32_t blocks_per_split;
   int32_t algo;
+  int32_t max_ctas;
 } hs_attn_params;
 
 /* HiSparse hot buffer ([KVS] §7).  One stream per (request, kv head) owns
@@ -270,6 +275,63 @@ HS_API hs_status hs_sparse_paged_decode_attn(const hs_attn_shape* shape, const h
 HS_API hs_status hs_swapin_misses(const hs_attn_shape* shape, const hs_hot_buffer* hb,
                            const int32_t* sel, const int32_t* sel_count, int32_t capacity,
                            int32_t step, hs_swap_stats* stats_opt, hs_stream_t stream);
+
+/* The HiSparse swap-in of hs_swapin_misses in two parts, so that the page
+ * copy can overlap attention over the blocks that were already resident
+ * ([KVS] §7 names the miss path as the risk to decode latency).
+ * hs_swapin_plan applies the same table rule (hits stamped, misses placed in
+ * ascending block order, victims chosen among slots outside the selection)
+ * and writes, in the selection layout [batch][Hkv][capacity] (ascending, -1
+ * padded) with counts [batch][Hkv]:
+ *   hit_sel / hit_count    selected blocks that were resident on entry;
+ *   miss_sel / miss_count  selected blocks just given a slot, whose pages are
+ *                          not yet copied.
+ * It reads no host memory; stats_opt gets hits, misses and evictions.  A
+ * selection larger than slots_per_stream sets HS_EBIT_CAPACITY, leaves the
+ * stream's tables untouched and writes empty lists.  The four outputs must not
+ * alias sel or each other.
+ * hs_swapin_copy copies the K/V pages (and e4m3 scales) of the blocks in a
+ * miss list from the host pool into the slots the page table now gives them,
+ * with at most max_ctas CTAs (0 = one per SM); stats_opt gets bytes_in.
+ * Attention over hit_sel may run concurrently with the copy (the copy writes
+ * only slots outside the selection and reads the page table); attention over
+ * miss_sel must follow the copy.  Their two outputs combine with
+ * hs_merge_attn_partials into the attention over the whole selection. */
+HS_API hs_status hs_swapin_plan(const hs_attn_shape* shape, const hs_hot_buffer* hb, const int32_t* sel,
+                                const int32_t* sel_count, int32_t capacity, int32_t step, int32_t* hit_sel,
+                                int32_t* hit_count, int32_t* miss_sel, int32_t* miss_count,
+                                hs_swap_stats* stats_opt, hs_stream_t stream);
+HS_API hs_status hs_swapin_copy(const hs_attn_shape* shape, const hs_hot_buffer* hb, const int32_t* miss_sel,
+                                const int32_t* miss_count, int32_t capacity, int32_t max_ctas,
+                                hs_swap_stats* stats_opt, hs_stream_t stream);
+
+/* hs_swapin_copy, and besides the attention over the copied blocks: for each
+ * (b, kvh) and each query head h of the group, over the valid tokens t (t <
+ * seq_lens[b]) of the blocks in miss_sel,
+ *   s_t = (q[b][h] . K[t]) * scale, out[b][h] = sum_t softmax(s)_t V[t],
+ *   lse[b][h] = log sum_t exp(s_t)
+ * with K/V read from the slots just filled (e4m3: code * scale).  Streams
+ * with no copied token get lse = -inf and their out rows are not written.
+ * q [batch][Hq][D] (f32 for f32 K/V, bf16 otherwise); out [batch][Hq][D] f32;
+ * lse [batch][Hq] f32.  Together with attention over hit_sel (fp32 output)
+ * and hs_merge_attn_partials this gives the attention over the selection,
+ * with no separate attention launch for the misses. */
+HS_API hs_status hs_swapin_copy_attend(const hs_attn_shape* shape, const hs_hot_buffer* hb, const int32_t* seq_lens,
+                                       const void* q, const int32_t* miss_sel, const int32_t* miss_count,
+                                       int32_t capacity, float scale, int32_t max_ctas, float* out, float* lse,
+                                       hs_swap_stats* stats_opt, hs_stream_t stream);
+
+/* Log-sum-exp merge of attention results over disjoint token sets of the same
+ * queries, [FLL] §2.2 (running max and normaliser carried across tiles):
+ * for each (b, h), with m = max_p lse[p][b][h],
+ *   out = sum_p e^(lse_p - m) out_p / sum_p e^(lse_p - m),  lse = m + log(sum)
+ * (out = 0, lse = -inf when every part is empty).
+ *   outs  [parts][batch][Hq][D] f32 (each part's normalised output)
+ *   lses  [parts][batch][Hq]   f32
+ *   out   [batch][Hq][D] bf16, or f32 when out_is_fp32;  lse_opt [batch][Hq]. */
+HS_API hs_status hs_merge_attn_partials(const hs_attn_shape* shape, int32_t batch, int32_t parts,
+                                        const float* outs, const float* lses, void* out, int32_t out_is_fp32,
+                                        float* lse_opt, hs_stream_t stream);
 
 /* Grouped e4m3 quantisation of K or V rows, [FLL] §2.4 + §3.2: for each row
  * of head_dim values and each 32-channel group, scale = amax / 448 (fp32; 1

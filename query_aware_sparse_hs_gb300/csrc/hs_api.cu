@@ -125,6 +125,12 @@ size_t workspace_for(const hs_attn_shape* s, int batch, int splits) {
 
 hs_status from_cuda(cudaError_t e) { return e == cudaSuccess ? HS_OK : HS_ERR_CUDA; }
 
+// CTAs the tensor-core attention may run at once: the SM count, or fewer when
+// the caller keeps SMs free for concurrent work.
+int attn_ctas(int sms, const hs_attn_params* p) {
+  return (p && p->max_ctas > 0 && p->max_ctas < sms) ? p->max_ctas : sms;
+}
+
 }  // namespace
 }  // namespace hs
 
@@ -156,7 +162,7 @@ size_t hs_workspace_bytes(const hs_attn_shape* shape, int32_t batch, int32_t cap
   int sms = 148;
   if (current_device(&d) == HS_OK) sms = d.sms;
   int bps, splits;
-  split_geometry(shape, batch, capacity, params, sms, &bps, &splits);
+  split_geometry(shape, batch, capacity, params, attn_ctas(sms, params), &bps, &splits);
   return workspace_for(shape, batch, splits);
 }
 
@@ -255,10 +261,12 @@ hs_status hs_sparse_paged_decode_attn(const hs_attn_shape* shape, const hs_paged
   if (!q || !sel || !sel_count || !out || !params || capacity < 1) return HS_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(out, 16) || !aligned(sel, 4) || !aligned(sel_count, 4))
     return HS_ERR_INVALID_ARG;
-  if (params->algo < 0 || params->algo > 2 || params->blocks_per_split < 0) return HS_ERR_INVALID_ARG;
+  if (params->algo < 0 || params->algo > 2 || params->blocks_per_split < 0 || params->max_ctas < 0)
+    return HS_ERR_INVALID_ARG;
   Device d;
   if ((st = current_device(&d)) != HS_OK) return st;
   const KvView v = make_view(shape, kv);
+  const int ctas = attn_ctas(d.sms, params);
   bool use_tc;
   if (params->algo == 1) {
     use_tc = false;
@@ -269,10 +277,10 @@ hs_status hs_sparse_paged_decode_attn(const hs_attn_shape* shape, const hs_paged
     use_tc = attn_tc_supported(v);
   }
   AttnArgs a;
-  split_geometry(shape, kv->batch, capacity, params, d.sms, &a.blocks_per_split, &a.splits);
+  split_geometry(shape, kv->batch, capacity, params, ctas, &a.blocks_per_split, &a.splits);
   const size_t need = workspace_for(shape, kv->batch, a.splits);
   if (need > 0 && (!workspace || ws_bytes < need || !aligned(workspace, 16))) return HS_ERR_WORKSPACE;
-  a.sms = d.sms;
+  a.sms = ctas;
   a.q = q;
   a.sel = sel;
   a.sel_count = sel_count;
@@ -308,12 +316,12 @@ static hs_status device_address(const void* p, const void** out) {
   return HS_ERR_INVALID_ARG;  // pageable memory that was never pinned
 }
 
-hs_status hs_swapin_misses(const hs_attn_shape* shape, const hs_hot_buffer* hb,
-                           const int32_t* sel, const int32_t* sel_count, int32_t capacity,
-                           int32_t step, hs_swap_stats* stats_opt, hs_stream_t stream) {
+// Checks a hot buffer and builds the kernels' view of it (host pool pointers
+// translated to their device addresses).
+static hs_status hot_view(const hs_attn_shape* shape, const hs_hot_buffer* hb, HotView* v) {
   hs_status st = check_shape(shape);
   if (st != HS_OK) return st;
-  if (!hb || !sel || !sel_count || capacity < 1) return HS_ERR_INVALID_ARG;
+  if (!hb) return HS_ERR_INVALID_ARG;
   if (!hb->page_table || !hb->slot_owner || !hb->last_used || !hb->k_slots || !hb->v_slots ||
       !hb->host_k || !hb->host_v)
     return HS_ERR_INVALID_ARG;
@@ -322,39 +330,118 @@ hs_status hs_swapin_misses(const hs_attn_shape* shape, const hs_hot_buffer* hb,
     return HS_ERR_INVALID_ARG;
   if (hb->batch < 0 || hb->max_blocks < 1 || hb->slots_per_stream < 1 || hb->slots_per_stream > 1024)
     return HS_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(hb->batch) * shape->num_kv_heads * hb->slots_per_stream > INT32_MAX)
+    return HS_ERR_UNSUPPORTED;
   const int64_t page_bytes = static_cast<int64_t>(shape->block_size) * shape->head_dim * elem_bytes(shape->kv_dtype);
   if (page_bytes % 16 != 0) return HS_ERR_UNSUPPORTED;
   if (!aligned(hb->k_slots, 16) || !aligned(hb->v_slots, 16) || !aligned(hb->host_k, 16) ||
       !aligned(hb->host_v, 16))
     return HS_ERR_INVALID_ARG;
-  Device d;
-  if ((st = current_device(&d)) != HS_OK) return st;
-  HotView v;
-  v.page_table = hb->page_table;
-  v.slot_owner = hb->slot_owner;
-  v.last_used = hb->last_used;
-  v.k_slots = hb->k_slots;
-  v.v_slots = hb->v_slots;
-  v.k_slot_scales = hb->k_slot_scales;
-  v.v_slot_scales = hb->v_slot_scales;
+  v->page_table = hb->page_table;
+  v->slot_owner = hb->slot_owner;
+  v->last_used = hb->last_used;
+  v->k_slots = hb->k_slots;
+  v->v_slots = hb->v_slots;
+  v->k_slot_scales = hb->k_slot_scales;
+  v->v_slot_scales = hb->v_slot_scales;
   const void* p;
   if ((st = device_address(hb->host_k, &p)) != HS_OK) return st;
-  v.host_k = p;
+  v->host_k = p;
   if ((st = device_address(hb->host_v, &p)) != HS_OK) return st;
-  v.host_v = p;
+  v->host_v = p;
   if ((st = device_address(hb->host_k_scales, &p)) != HS_OK) return st;
-  v.host_k_scales = static_cast<const float*>(p);
+  v->host_k_scales = static_cast<const float*>(p);
   if ((st = device_address(hb->host_v_scales, &p)) != HS_OK) return st;
-  v.host_v_scales = static_cast<const float*>(p);
-  v.batch = hb->batch;
-  v.hkv = shape->num_kv_heads;
-  v.max_blocks = hb->max_blocks;
-  v.slots = hb->slots_per_stream;
-  v.block = shape->block_size;
-  v.head_dim = shape->head_dim;
-  v.kv_dtype = shape->kv_dtype;
+  v->host_v_scales = static_cast<const float*>(p);
+  v->batch = hb->batch;
+  v->hkv = shape->num_kv_heads;
+  v->max_blocks = hb->max_blocks;
+  v->slots = hb->slots_per_stream;
+  v->block = shape->block_size;
+  v->head_dim = shape->head_dim;
+  v->kv_dtype = shape->kv_dtype;
+  return HS_OK;
+}
+
+hs_status hs_swapin_misses(const hs_attn_shape* shape, const hs_hot_buffer* hb,
+                           const int32_t* sel, const int32_t* sel_count, int32_t capacity,
+                           int32_t step, hs_swap_stats* stats_opt, hs_stream_t stream) {
+  if (!sel || !sel_count || capacity < 1) return HS_ERR_INVALID_ARG;
+  HotView v;
+  hs_status st = hot_view(shape, hb, &v);
+  if (st != HS_OK) return st;
+  Device d;
+  if ((st = current_device(&d)) != HS_OK) return st;
   return from_cuda(launch_swapin(v, sel, sel_count, capacity, step, stats_opt, d.err,
                                  reinterpret_cast<cudaStream_t>(stream)));
+}
+
+hs_status hs_swapin_plan(const hs_attn_shape* shape, const hs_hot_buffer* hb, const int32_t* sel,
+                         const int32_t* sel_count, int32_t capacity, int32_t step, int32_t* hit_sel,
+                         int32_t* hit_count, int32_t* miss_sel, int32_t* miss_count,
+                         hs_swap_stats* stats_opt, hs_stream_t stream) {
+  if (!sel || !sel_count || capacity < 1 || !hit_sel || !hit_count || !miss_sel || !miss_count)
+    return HS_ERR_INVALID_ARG;
+  if (hit_sel == sel || miss_sel == sel || hit_sel == miss_sel) return HS_ERR_INVALID_ARG;
+  HotView v;
+  hs_status st = hot_view(shape, hb, &v);
+  if (st != HS_OK) return st;
+  Device d;
+  if ((st = current_device(&d)) != HS_OK) return st;
+  return from_cuda(launch_swapin_plan(v, sel, sel_count, capacity, step, hit_sel, hit_count, miss_sel, miss_count,
+                                      stats_opt, d.err, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+hs_status hs_swapin_copy(const hs_attn_shape* shape, const hs_hot_buffer* hb, const int32_t* miss_sel,
+                         const int32_t* miss_count, int32_t capacity, int32_t max_ctas,
+                         hs_swap_stats* stats_opt, hs_stream_t stream) {
+  if (!miss_sel || !miss_count || capacity < 1 || max_ctas < 0) return HS_ERR_INVALID_ARG;
+  HotView v;
+  hs_status st = hot_view(shape, hb, &v);
+  if (st != HS_OK) return st;
+  Device d;
+  if ((st = current_device(&d)) != HS_OK) return st;
+  const int ctas = max_ctas > 0 ? max_ctas : d.sms;
+  return from_cuda(launch_swapin_copy(v, miss_sel, miss_count, capacity, ctas, nullptr, stats_opt, d.err,
+                                      reinterpret_cast<cudaStream_t>(stream)));
+}
+
+hs_status hs_swapin_copy_attend(const hs_attn_shape* shape, const hs_hot_buffer* hb, const int32_t* seq_lens,
+                                const void* q, const int32_t* miss_sel, const int32_t* miss_count, int32_t capacity,
+                                float scale, int32_t max_ctas, float* out, float* lse, hs_swap_stats* stats_opt,
+                                hs_stream_t stream) {
+  if (!miss_sel || !miss_count || capacity < 1 || max_ctas < 0 || !seq_lens || !q || !out || !lse)
+    return HS_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(lse, 4) || !aligned(seq_lens, 4)) return HS_ERR_INVALID_ARG;
+  HotView v;
+  hs_status st = hot_view(shape, hb, &v);
+  if (st != HS_OK) return st;
+  Device d;
+  if ((st = current_device(&d)) != HS_OK) return st;
+  MissAttnArgs a;
+  a.q = q;
+  a.seq_lens = seq_lens;
+  a.out = out;
+  a.lse = lse;
+  a.scale = scale;
+  a.hq = shape->num_q_heads;
+  const int ctas = max_ctas > 0 ? max_ctas : d.sms;
+  return from_cuda(launch_swapin_copy(v, miss_sel, miss_count, capacity, ctas, &a, stats_opt, d.err,
+                                      reinterpret_cast<cudaStream_t>(stream)));
+}
+
+hs_status hs_merge_attn_partials(const hs_attn_shape* shape, int32_t batch, int32_t parts, const float* outs,
+                                 const float* lses, void* out, int32_t out_is_fp32, float* lse_opt,
+                                 hs_stream_t stream) {
+  hs_status st = check_shape(shape);
+  if (st != HS_OK) return st;
+  if (batch < 0 || parts < 1 || !outs || !lses || !out) return HS_ERR_INVALID_ARG;
+  if (!aligned(outs, 4) || !aligned(lses, 4) || !aligned(out, out_is_fp32 ? 4 : 2)) return HS_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(batch) * shape->num_q_heads > INT32_MAX) return HS_ERR_UNSUPPORTED;
+  Device d;
+  if ((st = current_device(&d)) != HS_OK) return st;
+  return from_cuda(launch_merge_parts(batch * shape->num_q_heads, shape->head_dim, parts, outs, lses, out,
+                                      out_is_fp32 ? 1 : 0, lse_opt, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 hs_status hs_quantize_e4m3_g32(const void* src, int32_t src_is_fp32, int64_t rows,
@@ -430,7 +517,7 @@ extern "C" hs_status hs_sparse_paged_decode_attn_noalloc(const hs_attn_shape* sh
   Device d;
   if ((st = current_device(&d)) != HS_OK) return st;
   int bps = 0, splits = 0;
-  split_geometry(shape, kv->batch, capacity, params, d.sms, &bps, &splits);
+  split_geometry(shape, kv->batch, capacity, params, attn_ctas(d.sms, params), &bps, &splits);
   const size_t need = workspace_for(shape, kv->batch, splits);
   if (need > HS_NOALLOC_SCRATCH_BYTES) return HS_ERR_SCRATCH_LIMIT;
   void* scratch = nullptr;

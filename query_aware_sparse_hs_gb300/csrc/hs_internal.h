@@ -63,10 +63,28 @@ cudaError_t launch_select_only(const KvView& kv, const SelectArgs& a, const floa
 cudaError_t launch_attn_simt(const KvView& kv, const AttnArgs& a, unsigned* err, cudaStream_t st);
 cudaError_t launch_attn_tc(const KvView& kv, AttnArgs& a, unsigned* err, cudaStream_t st);
 bool attn_tc_supported(const KvView& kv);
+// LSE merge of `parts` partial results laid out [parts][rows][D] and [parts][rows].
+cudaError_t launch_merge_parts(int rows, int head_dim, int parts, const float* outs, const float* lses, void* out,
+                               int out_f32, float* lse_out, cudaStream_t st);
 cudaError_t launch_merge(const KvView& kv, const AttnArgs& a, cudaStream_t st);
 cudaError_t launch_swapin(const HotView& hb, const int32_t* sel, const int32_t* sel_count,
                           int capacity, int step, hs_swap_stats* stats, unsigned* err,
                           cudaStream_t st);
+cudaError_t launch_swapin_plan(const HotView& hb, const int32_t* sel, const int32_t* sel_count, int capacity,
+                               int step, int32_t* hit_sel, int32_t* hit_count, int32_t* miss_sel,
+                               int32_t* miss_count, hs_swap_stats* stats, unsigned* err, cudaStream_t st);
+// Attention over the blocks a page copy brings in (q rows of the stream's query heads).
+struct MissAttnArgs {
+  const void* q;
+  const int32_t* seq_lens;
+  float* out;
+  float* lse;
+  float scale;
+  int hq;
+};
+cudaError_t launch_swapin_copy(const HotView& hb, const int32_t* miss_sel, const int32_t* miss_count,
+                               int capacity, int ctas, const MissAttnArgs* attn, hs_swap_stats* stats, unsigned* err,
+                               cudaStream_t st);
 cudaError_t launch_quantize(const void* src, bool src_f32, int64_t rows, int head_dim,
                             uint8_t* codes, float* scales, cudaStream_t st);
 

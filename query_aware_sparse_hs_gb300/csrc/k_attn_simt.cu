@@ -170,35 +170,67 @@ cudaError_t launch_c(const KvView& kv, const AttnArgs& a, unsigned* err, cudaStr
   }
 }
 
-// One CTA per (request, query head); thread d owns output channel d.
-__global__ __launch_bounds__(128) void merge_kernel(int D, int splits, const float* __restrict__ ws_o,
-                                                    const float* __restrict__ ws_lse, void* out,
-                                                    int out_f32, float* lse_out) {
+// Log-sum-exp merge of attention partials over disjoint token sets ("分块稀疏
+// 注意力与KV Cache量化" §2.2: running max and normaliser): with m = max_i lse_i,
+// out = sum_i e^(lse_i - m) o_i / sum_i e^(lse_i - m), lse = m + log of the sum.
+// Partial i of row r sits at o[r * o_row + i * o_part], lse[r * l_row + i * l_part].
+// One warp per (request, query head) row; lane owns C = D/32 consecutive channels.
+constexpr int kMergeWarps = 8;
+
+template <int C>
+__global__ __launch_bounds__(kMergeWarps * 32) void merge_kernel(int rows, int parts, const float* __restrict__ o,
+                                                                 const float* __restrict__ lse, int64_t o_row,
+                                                                 int64_t o_part, int64_t l_row, int64_t l_part,
+                                                                 void* out, int out_f32, float* lse_out) {
+  constexpr int D = C * 32;
   pdl_trigger();
   pdl_wait();
-  const int64_t row = blockIdx.x;
-  const float* lse = ws_lse + row * splits;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * kMergeWarps + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  const int lane = threadIdx.x & 31;
   float M = -INFINITY;
-  for (int i = 0; i < splits; ++i) M = fmaxf(M, lse[i]);
-  float val = 0.0f, lse_v = -INFINITY;
-  const int d = threadIdx.x;
+  for (int i = 0; i < parts; ++i) M = fmaxf(M, lse[row * l_row + i * l_part]);
+  float acc[C];
+#pragma unroll
+  for (int c = 0; c < C; ++c) acc[c] = 0.0f;
+  float lse_v = -INFINITY;
   if (M != -INFINITY) {
-    float tot = 0.0f, acc = 0.0f;
-    for (int i = 0; i < splits; ++i) {
-      const float w = expf(lse[i] - M);
+    float tot = 0.0f;
+    for (int i = 0; i < parts; ++i) {
+      const float w = expf(lse[row * l_row + i * l_part] - M);
       tot += w;
-      if (d < D) acc = fmaf(w, ws_o[(row * splits + i) * D + d], acc);
+      if (w > 0.0f) {
+        const float* src = o + row * o_row + i * o_part + lane * C;
+#pragma unroll
+        for (int c = 0; c < C; ++c) acc[c] = fmaf(w, src[c], acc[c]);
+      }
     }
-    val = acc / tot;
+#pragma unroll
+    for (int c = 0; c < C; ++c) acc[c] = acc[c] / tot;
     lse_v = M + logf(tot);
   }
-  if (d < D) {
-    if (out_f32)
-      static_cast<float*>(out)[row * D + d] = val;
-    else
-      static_cast<__nv_bfloat16*>(out)[row * D + d] = __float2bfloat16_rn(val);
+  if (out_f32) {
+    float* dst = static_cast<float*>(out) + row * D + lane * C;
+#pragma unroll
+    for (int c = 0; c < C; ++c) dst[c] = acc[c];
+  } else {
+    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(out) + row * D + lane * C;
+#pragma unroll
+    for (int c = 0; c < C; ++c) dst[c] = __float2bfloat16_rn(acc[c]);
   }
-  if (lse_out && d == 0) lse_out[row] = lse_v;
+  if (lse_out && lane == 0) lse_out[row] = lse_v;
+}
+
+cudaError_t launch_merge_rows(int rows, int head_dim, int parts, const float* o, const float* lse, int64_t o_row,
+                              int64_t o_part, int64_t l_row, int64_t l_part, void* out, int out_f32,
+                              float* lse_out, cudaStream_t st) {
+  if (rows == 0) return cudaSuccess;
+  const dim3 grid((rows + kMergeWarps - 1) / kMergeWarps);
+  if (head_dim == 128)
+    return launch_pdl(merge_kernel<4>, grid, dim3(kMergeWarps * 32), 0, st, rows, parts, o, lse, o_row, o_part,
+                      l_row, l_part, out, out_f32, lse_out);
+  return launch_pdl(merge_kernel<2>, grid, dim3(kMergeWarps * 32), 0, st, rows, parts, o, lse, o_row, o_part, l_row,
+                    l_part, out, out_f32, lse_out);
 }
 
 }  // namespace
@@ -209,11 +241,16 @@ cudaError_t launch_attn_simt(const KvView& kv, const AttnArgs& a, unsigned* err,
 }
 
 cudaError_t launch_merge(const KvView& kv, const AttnArgs& a, cudaStream_t st) {
-  const int rows = kv.batch * kv.hq;
-  if (rows == 0) return cudaSuccess;
-  return launch_pdl(merge_kernel, dim3(rows), dim3(128), 0, st, kv.head_dim, a.splits,
-                    static_cast<const float*>(a.ws_o), static_cast<const float*>(a.ws_lse), a.out,
-                    a.out_is_fp32, a.lse);
+  const int64_t D = kv.head_dim, S = a.splits;
+  return launch_merge_rows(kv.batch * kv.hq, kv.head_dim, a.splits, static_cast<const float*>(a.ws_o),
+                           static_cast<const float*>(a.ws_lse), S * D, D, S, int64_t(1), a.out, a.out_is_fp32,
+                           a.lse, st);
+}
+
+cudaError_t launch_merge_parts(int rows, int head_dim, int parts, const float* outs, const float* lses, void* out,
+                               int out_f32, float* lse_out, cudaStream_t st) {
+  const int64_t D = head_dim, R = rows;
+  return launch_merge_rows(rows, head_dim, parts, outs, lses, D, R * D, int64_t(1), R, out, out_f32, lse_out, st);
 }
 
 }  // namespace hs

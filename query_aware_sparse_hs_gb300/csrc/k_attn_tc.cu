@@ -76,10 +76,10 @@ struct Layout {
   static constexpr int kOffRed = kOffMisc + 16;
   static constexpr int kOffMeta = kOffRed + 2 * 3 * 4 * NH * 4;  // red: [group][3][4 warps][NH]; meta: [stage][8] (page, valid tokens)
   static constexpr int kBytes = kOffMeta + kStages * 8 * 8;
-  // the whole per-block maximum: one CTA per SM, and operand reads through a
-  // descriptor can never leave this CTA's own shared memory
-  static constexpr int kAlloc = 232448;
-  static_assert(kBytes + 1024 <= kAlloc, "shared memory layout too large");
+  // the layout plus 1 KB to align its base; what is left of the SM's shared
+  // memory can hold a small CTA of another kernel (the overlapped page copy)
+  static constexpr int kAlloc = (kBytes + 1024 + 127) / 128 * 128;
+  static_assert(kAlloc <= 232448, "shared memory layout too large");
   static constexpr int kTmemCols = NH == 8 ? 64 : 128;
   static constexpr int kColO = 32;  // S uses columns [0, 32)
 };
@@ -630,8 +630,8 @@ struct Layout8 {
   static constexpr int kOffRed = kOffMisc + 16;
   static constexpr int kOffMeta = kOffRed + 3 * 4 * 8 * 4;
   static constexpr int kBytes = kOffMeta + kStages8 * 8 * 8;
-  static constexpr int kAlloc = 232448;
-  static_assert(kBytes + 1024 <= kAlloc, "shared memory layout too large");
+  static constexpr int kAlloc = (kBytes + 1024 + 127) / 128 * 128;  // layout + base alignment
+  static_assert(kAlloc <= 232448, "shared memory layout too large");
   static_assert(kOffKbf % 1024 == 0 && kOffQ % 1024 == 0, "swizzled tiles need 1024-byte alignment");
   static constexpr int kTmemCols = 256;
   static constexpr int kColO = 64;  // S' uses columns [0, 64)

@@ -3,11 +3,20 @@
 // current access set, update the page table, and pull the missing pages back
 // from the pinned host pool.
 //
-// One CTA per (request, kv head) stream.  The table logic is sequential by
-// definition (each miss sees the state left by the previous one), so warp 0
-// runs it in ascending block order with a warp-wide argmin over the slots;
-// then the whole CTA streams the missing pages from mapped host memory into
+// The table logic ("plan") is sequential by definition (each miss sees the
+// state left by the previous one): one CTA per (request, kv head) stream, warp
+// 0 walks the misses in ascending block order with a warp-wide argmin over the
+// slots.  The page copy streams the missing pages from mapped host memory into
 // their slots with 16-byte vector loads (zero-copy over the CPU-GPU link).
+//
+// Kernels: swapin_kernel plans and copies one stream per CTA;
+// swapin_plan_kernel only plans, and lists the selection's hits (resident
+// before the call) and misses in the selection layout; swapin_copy_kernel
+// copies the pages of such a miss list on a few SMs, and
+// copied_blocks_attn_kernel computes the attention over the copied blocks,
+// so that both can run beside an attention launch over the hit list on the
+// other SMs (they touch disjoint slots: victims are never in the current
+// selection).
 #include "hs_internal.h"
 
 namespace hs {
@@ -15,56 +24,65 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kMaxSlots = 1024;
+// The copy kernel runs on a few SMs of its own (the attention CTAs beside it
+// fill the SMs' shared memory): large CTAs keep many host loads in flight.
+constexpr int kCopyThreads = 1024;
+constexpr int kCopyUnroll = 4;
+constexpr int kCopyBatch = 1024;  // (block, slot) pairs staged per round
+constexpr int kAttnThreads = 256;
 
 __device__ __forceinline__ unsigned long long umin64(unsigned long long a, unsigned long long b) {
   return a < b ? a : b;
 }
 
-__global__ __launch_bounds__(kThreads) void swapin_kernel(HotView hb, const int32_t* __restrict__ sel,
-                                                          const int32_t* __restrict__ sel_count,
-                                                          int capacity, int step,
-                                                          hs_swap_stats* stats, unsigned* err) {
-  __shared__ int s_owner[kMaxSlots];
-  __shared__ int s_last[kMaxSlots];
-  __shared__ unsigned char s_prot[kMaxSlots];
-  __shared__ int s_copy_j[kMaxSlots];
-  __shared__ int s_copy_s[kMaxSlots];
-  __shared__ int s_ncopy, s_hits, s_evict;
+struct PlanSmem {
+  int owner[kMaxSlots];
+  int last[kMaxSlots];
+  unsigned char prot[kMaxSlots];
+  unsigned char hit[kMaxSlots];  // per selection entry: resident at entry
+  int copy_j[kMaxSlots];
+  int copy_s[kMaxSlots];
+  int ncopy, hits, evict;
+};
 
-  pdl_trigger();
-  pdl_wait();
-  const int pair = blockIdx.x;
+// Runs the victim rule of one stream and updates its tables.  Returns the
+// stream's selection count (entries of `my_sel`), or -1 when the selection
+// does not fit (HS_EBIT_CAPACITY; the stream is left untouched).  Afterwards
+// sm.copy_j/copy_s hold the sm.ncopy (block, slot) pairs to fill and sm.hit[i]
+// says whether entry i was a hit.  All threads of the CTA call it.
+__device__ int plan_stream(const HotView& hb, const int32_t* my_sel, int cnt, int capacity, int step, int pair,
+                           PlanSmem& sm, unsigned* err) {
   const int S = hb.slots;
   const int base = pair * S;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  int cnt = sel_count[pair];
   if (cnt > capacity || cnt > S) {
     if (tid == 0) set_error(err, HS_EBIT_CAPACITY);
-    return;  // the stream is left untouched
+    return -1;
   }
   if (cnt < 0) cnt = 0;
-  const int32_t* my_sel = sel + static_cast<int64_t>(pair) * capacity;
   int32_t* pt = hb.page_table + static_cast<int64_t>(pair) * hb.max_blocks;
 
-  for (int s = tid; s < S; s += kThreads) {
-    s_owner[s] = hb.slot_owner[base + s];
-    s_last[s] = hb.last_used[base + s];
-    s_prot[s] = 0;
+  for (int s = tid; s < S; s += blockDim.x) {
+    sm.owner[s] = hb.slot_owner[base + s];
+    sm.last[s] = hb.last_used[base + s];
+    sm.prot[s] = 0;
   }
-  if (tid == 0) { s_ncopy = 0; s_hits = 0; s_evict = 0; }
+  if (tid == 0) { sm.ncopy = 0; sm.hits = 0; sm.evict = 0; }
   __syncthreads();
 
   // hits: stamp and protect
-  for (int i = tid; i < cnt; i += kThreads) {
+  for (int i = tid; i < cnt; i += blockDim.x) {
     const int j = my_sel[i];
+    sm.hit[i] = 0;
     if (j < 0 || j >= hb.max_blocks) continue;
     const int g = pt[j];
     if (g >= 0) {
       const int s = g - base;
       if (s < 0 || s >= S) { set_error(err, HS_EBIT_PAGE_RANGE); continue; }
-      s_prot[s] = 1;
-      s_last[s] = step;
-      atomicAdd(&s_hits, 1);
+      sm.prot[s] = 1;
+      sm.last[s] = step;
+      sm.hit[i] = 1;
+      atomicAdd(&sm.hits, 1);
     }
   }
   __syncthreads();
@@ -77,18 +95,18 @@ __global__ __launch_bounds__(kThreads) void swapin_kernel(HotView hb, const int3
         if (lane == 0) set_error(err, HS_EBIT_BLOCK_RANGE);
         continue;
       }
-      if (pt[j] >= 0) continue;  // a hit (or a block placed earlier in this loop)
+      if (pt[j] >= 0) continue;  // a hit
       // victim key: (class, last_used, slot); class 0 = free, 1 = evictable, 3 = protected
       unsigned long long best = ~0ull;
       for (int s = lane; s < S; s += 32) {
         unsigned long long key;
-        if (s_owner[s] < 0)
+        if (sm.owner[s] < 0)
           key = static_cast<unsigned long long>(s);
-        else if (s_prot[s])
+        else if (sm.prot[s])
           key = (3ull << 62) | static_cast<unsigned long long>(s);
         else
           key = (1ull << 62) |
-                (static_cast<unsigned long long>(static_cast<uint32_t>(s_last[s]) ^ 0x80000000u) << 20) |
+                (static_cast<unsigned long long>(static_cast<uint32_t>(sm.last[s]) ^ 0x80000000u) << 20) |
                 static_cast<unsigned long long>(s);
         best = umin64(best, key);
       }
@@ -100,74 +118,454 @@ __global__ __launch_bounds__(kThreads) void swapin_kernel(HotView hb, const int3
         break;
       }
       if (lane == 0) {
-        const int old = s_owner[s];
+        const int old = sm.owner[s];
         if (old >= 0) {
           pt[old] = -1;
-          ++s_evict;
+          ++sm.evict;
         }
-        s_owner[s] = j;
-        s_last[s] = step;
-        s_prot[s] = 1;
+        sm.owner[s] = j;
+        sm.last[s] = step;
+        sm.prot[s] = 1;
         pt[j] = base + s;
-        s_copy_j[s_ncopy] = j;
-        s_copy_s[s_ncopy] = s;
-        ++s_ncopy;
+        sm.copy_j[sm.ncopy] = j;
+        sm.copy_s[sm.ncopy] = s;
+        ++sm.ncopy;
       }
       __syncwarp();
     }
   }
   __syncthreads();
-  for (int s = tid; s < S; s += kThreads) {
-    hb.slot_owner[base + s] = s_owner[s];
-    hb.last_used[base + s] = s_last[s];
+  for (int s = tid; s < S; s += blockDim.x) {
+    hb.slot_owner[base + s] = sm.owner[s];
+    hb.last_used[base + s] = sm.last[s];
   }
+  return cnt;
+}
 
-  // copy the missing pages host -> slots
-  const int ncopy = s_ncopy;
+__device__ __forceinline__ int64_t page_bytes_of(const HotView& hb) {
   const int elem = hb.kv_dtype == HS_KV_F32 ? 4 : (hb.kv_dtype == HS_KV_BF16 ? 2 : 1);
-  const int64_t page_bytes = static_cast<int64_t>(hb.block) * hb.head_dim * elem;
-  const int vec_per_page = static_cast<int>(page_bytes / 16);
-  const int64_t total_vec = static_cast<int64_t>(ncopy) * vec_per_page;
+  return static_cast<int64_t>(hb.block) * hb.head_dim * elem;
+}
+
+__device__ __forceinline__ int64_t scale_bytes_of(const HotView& hb) {
+  return hb.kv_dtype == HS_KV_FP8E4M3_G32 ? static_cast<int64_t>(hb.block) * (hb.head_dim / kQuantGroup) * 4 : 0;
+}
+
+// Copies `n` pages of one stream (pool page pool_pair + js[c] -> slot
+// base + ss[c]), K and V and, for e4m3, their scales, with all threads of the
+// CTA; each thread keeps kCopyUnroll 16-byte loads in flight.
+template <typename JS, typename SS>
+__device__ void copy_pages(const HotView& hb, int pair, int n, JS js, SS ss) {
   const int64_t pool_pair = static_cast<int64_t>(pair) * hb.max_blocks;
-  for (int64_t v = tid; v < 2 * total_vec; v += kThreads) {
-    const int which = v >= total_vec;  // 0 = K, 1 = V
-    const int64_t w = v - which * total_vec;
-    const int c = static_cast<int>(w / vec_per_page);
-    const int64_t off = w % vec_per_page;
-    const int64_t src_page = pool_pair + s_copy_j[c];
-    const int64_t dst_page = base + s_copy_s[c];
-    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const char*>(which ? hb.host_v : hb.host_k) + src_page * page_bytes) + off;
-    uint4* dst = reinterpret_cast<uint4*>(static_cast<char*>(which ? hb.v_slots : hb.k_slots) + dst_page * page_bytes) + off;
-    *dst = *src;
+  const int64_t base = static_cast<int64_t>(pair) * hb.slots;
+  const int64_t page_bytes = page_bytes_of(hb);
+  const int64_t vpp = page_bytes / 16;
+  const int64_t total = static_cast<int64_t>(n) * vpp * 2;  // K then V
+  for (int64_t v0 = threadIdx.x; v0 < total; v0 += static_cast<int64_t>(blockDim.x) * kCopyUnroll) {
+    uint4 buf[kCopyUnroll];
+    uint4* dst[kCopyUnroll];
+#pragma unroll
+    for (int u = 0; u < kCopyUnroll; ++u) {
+      const int64_t v = v0 + static_cast<int64_t>(u) * blockDim.x;
+      dst[u] = nullptr;
+      if (v < total) {
+        const int which = v >= n * vpp;  // 0 = K, 1 = V
+        const int64_t w = v - which * n * vpp;
+        const int c = static_cast<int>(w / vpp);
+        const int64_t off = w - c * vpp;
+        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const char*>(which ? hb.host_v : hb.host_k) +
+                                                          (pool_pair + js(c)) * page_bytes) + off;
+        dst[u] = reinterpret_cast<uint4*>(static_cast<char*>(which ? hb.v_slots : hb.k_slots) +
+                                          (base + ss(c)) * page_bytes) + off;
+        buf[u] = __ldcs(src);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kCopyUnroll; ++u)
+      if (dst[u]) *dst[u] = buf[u];
   }
   if (hb.kv_dtype == HS_KV_FP8E4M3_G32) {
     const int sc_per_page = hb.block * (hb.head_dim / kQuantGroup);
-    const int64_t total_sc = static_cast<int64_t>(ncopy) * sc_per_page;
-    for (int64_t v = tid; v < 2 * total_sc; v += kThreads) {
+    const int64_t total_sc = static_cast<int64_t>(n) * sc_per_page;
+    for (int64_t v = threadIdx.x; v < 2 * total_sc; v += blockDim.x) {
       const int which = v >= total_sc;
       const int64_t w = v - which * total_sc;
       const int c = static_cast<int>(w / sc_per_page);
       const int64_t off = w % sc_per_page;
-      const int64_t src_page = pool_pair + s_copy_j[c];
-      const int64_t dst_page = base + s_copy_s[c];
-      const float* src = (which ? hb.host_v_scales : hb.host_k_scales) + src_page * sc_per_page + off;
-      float* dst = (which ? hb.v_slot_scales : hb.k_slot_scales) + dst_page * sc_per_page + off;
-      *dst = *src;
+      const float* src = (which ? hb.host_v_scales : hb.host_k_scales) + (pool_pair + js(c)) * sc_per_page + off;
+      float* dst = (which ? hb.v_slot_scales : hb.k_slot_scales) + (base + ss(c)) * sc_per_page + off;
+      *dst = __ldcs(src);
     }
-  }
-  if (stats && tid == 0) {
-    const int64_t sc_bytes = hb.kv_dtype == HS_KV_FP8E4M3_G32
-                                 ? static_cast<int64_t>(hb.block) * (hb.head_dim / kQuantGroup) * 4
-                                 : 0;
-    atomicAdd(&stats->hits, static_cast<unsigned long long>(s_hits));
-    atomicAdd(&stats->misses, static_cast<unsigned long long>(ncopy));
-    atomicAdd(&stats->evictions, static_cast<unsigned long long>(s_evict));
-    atomicAdd(&stats->bytes_in, static_cast<unsigned long long>(ncopy) * 2ull *
-                                    static_cast<unsigned long long>(page_bytes + sc_bytes));
   }
 }
 
+__global__ __launch_bounds__(kThreads) void swapin_kernel(HotView hb, const int32_t* __restrict__ sel,
+                                                          const int32_t* __restrict__ sel_count,
+                                                          int capacity, int step,
+                                                          hs_swap_stats* stats, unsigned* err) {
+  __shared__ PlanSmem sm;
+  pdl_trigger();
+  pdl_wait();
+  const int pair = blockIdx.x;
+  const int32_t* my_sel = sel + static_cast<int64_t>(pair) * capacity;
+  if (plan_stream(hb, my_sel, sel_count[pair], capacity, step, pair, sm, err) < 0) return;
+  const int ncopy = sm.ncopy;
+  copy_pages(hb, pair, ncopy, [&](int c) { return sm.copy_j[c]; }, [&](int c) { return sm.copy_s[c]; });
+  if (stats && threadIdx.x == 0) {
+    atomicAdd(&stats->hits, static_cast<unsigned long long>(sm.hits));
+    atomicAdd(&stats->misses, static_cast<unsigned long long>(ncopy));
+    atomicAdd(&stats->evictions, static_cast<unsigned long long>(sm.evict));
+    atomicAdd(&stats->bytes_in, static_cast<unsigned long long>(ncopy) * 2ull *
+                                    static_cast<unsigned long long>(page_bytes_of(hb) + scale_bytes_of(hb)));
+  }
+}
+
+// Plan only: tables updated, hit and miss lists written in the selection
+// layout ([pair][capacity], ascending, -1 padded) with their counts.
+__global__ __launch_bounds__(kThreads) void swapin_plan_kernel(HotView hb, const int32_t* __restrict__ sel,
+                                                               const int32_t* __restrict__ sel_count,
+                                                               int capacity, int step, int32_t* hit_sel,
+                                                               int32_t* hit_count, int32_t* miss_sel,
+                                                               int32_t* miss_count, hs_swap_stats* stats,
+                                                               unsigned* err) {
+  __shared__ PlanSmem sm;
+  pdl_trigger();
+  pdl_wait();
+  const int pair = blockIdx.x;
+  const int64_t row = static_cast<int64_t>(pair) * capacity;
+  const int32_t* my_sel = sel + row;
+  const int cnt = plan_stream(hb, my_sel, sel_count[pair], capacity, step, pair, sm, err);
+  int nh = 0, nm = 0;
+  if (cnt > 0 && threadIdx.x < 32) {  // warp 0 compacts hits and misses in selection order
+    const int lane = threadIdx.x;
+    for (int i0 = 0; i0 < cnt; i0 += 32) {
+      const int i = i0 + lane;
+      const int j = i < cnt ? my_sel[i] : -1;
+      const bool valid = i < cnt && j >= 0 && j < hb.max_blocks;
+      const bool h = valid && sm.hit[i];
+      const bool m = valid && !sm.hit[i];
+      const unsigned bh = __ballot_sync(0xffffffffu, h), bm = __ballot_sync(0xffffffffu, m);
+      const unsigned below = (1u << lane) - 1u;
+      if (h) hit_sel[row + nh + __popc(bh & below)] = j;
+      if (m) miss_sel[row + nm + __popc(bm & below)] = j;
+      nh += __popc(bh);
+      nm += __popc(bm);
+    }
+  }
+  __shared__ int s_nh, s_nm;
+  if (threadIdx.x == 0) { s_nh = nh; s_nm = nm; }  // warp 0's lanes all hold the totals
+  __syncthreads();
+  for (int i = s_nh + threadIdx.x; i < capacity; i += blockDim.x) hit_sel[row + i] = -1;
+  for (int i = s_nm + threadIdx.x; i < capacity; i += blockDim.x) miss_sel[row + i] = -1;
+  if (threadIdx.x == 0) {
+    hit_count[pair] = s_nh;
+    miss_count[pair] = s_nm;
+    if (stats && cnt >= 0) {
+      atomicAdd(&stats->hits, static_cast<unsigned long long>(s_nh));
+      atomicAdd(&stats->misses, static_cast<unsigned long long>(sm.ncopy));
+      atomicAdd(&stats->evictions, static_cast<unsigned long long>(sm.evict));
+    }
+  }
+}
+
+// Attention of one stream's query heads over the blocks it has just copied:
+// the part of the selection's attention that the attention over the hits
+// leaves out.  Normalised output and natural-log lse per query head, to be
+// combined with the hits' part by the LSE merge.
+struct MissAttn {
+  const void* q;            // [batch][Hq][D]: f32 for f32 K/V, bf16 otherwise
+  const int32_t* seq_lens;  // [batch]
+  float* out;               // [batch][Hq][D]
+  float* lse;               // [batch][Hq]
+  float scale_log2;         // scale * log2(e)
+  int hq, group;
+};
+
+constexpr int kMaxGroup = 16;
+constexpr int kSub = 64;  // token rows of a block staged in shared memory at a time
+
+template <int KIND>
+constexpr int elem_size() { return KIND == HS_KV_F32 ? 4 : (KIND == HS_KV_BF16 ? 2 : 1); }
+
+// Dynamic shared memory of the attending copy kernel: K and V rows of a
+// sub-block (+ e4m3 scales), q of the group, and the scores/probabilities.
+// K/V rows are staged with a stride of one row plus four elements, so that
+// threads reading four consecutive elements of consecutive rows hit distinct
+// banks.
+template <int C, int KIND>
+struct AttendSmem {
+  static constexpr int D = C * 32;
+  static constexpr int kRowBytes = D * elem_size<KIND>();
+  static constexpr int kStride = kRowBytes + 4 * elem_size<KIND>();
+  static constexpr int kScaleRow = KIND == HS_KV_FP8E4M3_G32 ? (D / kQuantGroup) * 4 : 0;
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kOffK + kSub * kStride;
+  static constexpr int kOffKs = (kOffV + kSub * kStride + 15) / 16 * 16;
+  static constexpr int kOffVs = kOffKs + kSub * kScaleRow;
+  static constexpr int kOffQ = (kOffVs + kSub * kScaleRow + 15) / 16 * 16;
+  static constexpr int kOffP = kOffQ + kMaxGroup * D * 4;
+  static constexpr int kBytes = kOffP + kMaxGroup * kSub * 4;
+};
+
+// Channel d of staged row t, as the attention sees it (e4m3: code * scale).
+template <int C, int KIND>
+__device__ __forceinline__ float staged_val(const uint8_t* rows, const float* scales, int t, int d) {
+  constexpr int D = C * 32;
+  const uint8_t* r = rows + t * AttendSmem<C, KIND>::kStride;
+  if constexpr (KIND == HS_KV_F32) {
+    return reinterpret_cast<const float*>(r)[d];
+  } else if constexpr (KIND == HS_KV_BF16) {
+    return bf16_bits_to_float(reinterpret_cast<const uint16_t*>(r)[d]);
+  } else {
+    return e4m3x2_to_float2(static_cast<uint16_t>(r[d])).x * scales[t * (D / kQuantGroup) + d / kQuantGroup];
+  }
+}
+
+// Channels d0 .. d0+3 of staged row t (d0 a multiple of 4), one load.
+template <int C, int KIND>
+__device__ __forceinline__ float4 staged_val4(const uint8_t* rows, const float* scales, int t, int d0) {
+  constexpr int D = C * 32;
+  const uint8_t* r = rows + t * AttendSmem<C, KIND>::kStride;
+  if constexpr (KIND == HS_KV_F32) {
+    return *reinterpret_cast<const float4*>(r + d0 * 4);
+  } else if constexpr (KIND == HS_KV_BF16) {
+    const uint2 u = *reinterpret_cast<const uint2*>(r + d0 * 2);
+    return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u), __uint_as_float(u.y << 16),
+                       __uint_as_float(u.y & 0xffff0000u));
+  } else {
+    const uint32_t u = *reinterpret_cast<const uint32_t*>(r + d0);
+    const float sc = scales[t * (D / kQuantGroup) + d0 / kQuantGroup];
+    const float2 a = e4m3x2_to_float2(static_cast<uint16_t>(u & 0xffffu));
+    const float2 b = e4m3x2_to_float2(static_cast<uint16_t>(u >> 16));
+    return make_float4(a.x * sc, a.y * sc, b.x * sc, b.y * sc);
+  }
+}
+
+// Copy only: the pages of the miss lists written by swapin_plan_kernel, whose
+// slots the page table now names.  Persistent: CTA c takes streams c, c+grid, ...
+__global__ __launch_bounds__(kCopyThreads, 1) void swapin_copy_kernel(HotView hb, const int32_t* __restrict__ miss_sel,
+                                                                      const int32_t* __restrict__ miss_count,
+                                                                      int capacity, hs_swap_stats* stats,
+                                                                      unsigned* err) {
+  __shared__ int s_j[kCopyBatch];
+  __shared__ int s_s[kCopyBatch];
+  __shared__ int s_n;
+  // No early trigger: CTAs of a dependent launched early would wait on SMs
+  // that the attention running beside the copy needs.
+  pdl_wait();
+  const int pairs = hb.batch * hb.hkv;
+  const int S = hb.slots;
+  unsigned long long pages = 0;
+  for (int pair = blockIdx.x; pair < pairs; pair += gridDim.x) {
+    int n = miss_count[pair];
+    n = n < 0 ? 0 : (n > capacity ? capacity : n);
+    n = n > S ? S : n;
+    const int64_t row = static_cast<int64_t>(pair) * capacity;
+    const int32_t* pt = hb.page_table + static_cast<int64_t>(pair) * hb.max_blocks;
+    for (int i0 = 0; i0 < n; i0 += kCopyBatch) {  // n is uniform across the CTA
+      if (threadIdx.x == 0) s_n = 0;
+      __syncthreads();
+      const int i = i0 + static_cast<int>(threadIdx.x);
+      if (threadIdx.x < kCopyBatch && i < n) {
+        const int j = miss_sel[row + i];
+        if (j < 0 || j >= hb.max_blocks) {
+          set_error(err, HS_EBIT_BLOCK_RANGE);
+        } else {
+          const int sl = pt[j] - pair * S;
+          if (sl < 0 || sl >= S) {
+            set_error(err, HS_EBIT_PAGE_RANGE);
+          } else {
+            const int k = atomicAdd(&s_n, 1);
+            s_j[k] = j;
+            s_s[k] = sl;
+          }
+        }
+      }
+      __syncthreads();
+      const int m = s_n;
+      copy_pages(hb, pair, m, [&](int c) { return s_j[c]; }, [&](int c) { return s_s[c]; });
+      pages += m;
+      __syncthreads();  // s_j/s_s/s_n are refilled next round
+    }
+  }
+  if (stats && threadIdx.x == 0 && pages)
+    atomicAdd(&stats->bytes_in, pages * 2ull * static_cast<unsigned long long>(page_bytes_of(hb) + scale_bytes_of(hb)));
+}
+
+// Attention of one stream's query heads over the blocks of its miss list,
+// read from the slots the copy filled.  One CTA per stream (streams without
+// misses only write lse = -inf).  Per block, in pieces of up to kSub valid
+// tokens: the rows are staged in shared memory (16-byte loads, padded rows);
+// thread (head, token) takes a dot product; one warp per head updates the
+// running max and sum; thread (head, channel) accumulates p * v.
+template <int C, int KIND>
+__global__ __launch_bounds__(kAttnThreads) void copied_blocks_attn_kernel(HotView hb,
+                                                                         const int32_t* __restrict__ miss_sel,
+                                                                         const int32_t* __restrict__ miss_count,
+                                                                         int capacity, MissAttn ma, unsigned* err) {
+  using Ly = AttendSmem<C, KIND>;
+  constexpr int D = C * 32;
+  constexpr int kAcc = (kMaxGroup * D + kAttnThreads - 1) / kAttnThreads;
+  __shared__ float s_m[kMaxGroup], s_l[kMaxGroup], s_alpha[kMaxGroup];
+  extern __shared__ __align__(16) uint8_t dyn[];
+  float* s_q = reinterpret_cast<float*>(dyn + Ly::kOffQ);
+  float* s_p = reinterpret_cast<float*>(dyn + Ly::kOffP);
+  pdl_trigger();
+  pdl_wait();
+  const int pair = blockIdx.x;
+  const int S = hb.slots;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = ma.group;
+  const int b = pair / hb.hkv, kvh = pair - b * hb.hkv;
+  const int64_t qrow0 = static_cast<int64_t>(b) * ma.hq + static_cast<int64_t>(kvh) * g;
+  int n = miss_count[pair];
+  n = n < 0 ? 0 : (n > capacity ? capacity : n);
+  n = n > S ? S : n;
+  if (n == 0) {
+    if (tid < g) ma.lse[qrow0 + tid] = -INFINITY;
+    return;
+  }
+  const int64_t row = static_cast<int64_t>(pair) * capacity;
+  const int32_t* pt = hb.page_table + static_cast<int64_t>(pair) * hb.max_blocks;
+  const int L = ma.seq_lens[b];
+  const int B = hb.block;
+  float acc[kAcc];
+#pragma unroll
+  for (int i = 0; i < kAcc; ++i) acc[i] = 0.0f;
+  if (tid < g) {
+    s_m[tid] = -INFINITY;
+    s_l[tid] = 0.0f;
+  }
+  for (int i = tid; i < g * D; i += kAttnThreads) {
+    const int64_t e = qrow0 * D + i;  // heads of the group are consecutive rows
+    s_q[i] = KIND == HS_KV_F32 ? static_cast<const float*>(ma.q)[e]
+                               : bf16_bits_to_float(static_cast<const uint16_t*>(ma.q)[e]);
+  }
+  const float* ksc = reinterpret_cast<const float*>(dyn + Ly::kOffKs);
+  const float* vsc = reinterpret_cast<const float*>(dyn + Ly::kOffVs);
+  for (int c = 0; c < n; ++c) {
+    const int j = miss_sel[row + c];
+    if (j < 0 || j >= hb.max_blocks) continue;  // reported by the copy
+    const int sl = pt[j] - pair * S;
+    if (sl < 0 || sl >= S) continue;
+    const int nv = min(B, L - j * B);  // valid tokens of the block (uniform)
+    const int64_t row0 = (static_cast<int64_t>(pair) * S + sl) * B;
+    for (int r0 = 0; r0 < nv; r0 += kSub) {
+      const int rows = min(kSub, nv - r0);
+      __syncthreads();  // previous piece done with the staging, s_p and s_alpha
+      {  // stage K and V rows (and scales): 16-byte loads, 4-byte stores into the padded rows
+        constexpr int kVecRow = Ly::kRowBytes / 16;
+        const int vec = rows * kVecRow;
+        const uint4* ks = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(hb.k_slots) +
+                                                         (row0 + r0) * Ly::kRowBytes);
+        const uint4* vs = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(hb.v_slots) +
+                                                         (row0 + r0) * Ly::kRowBytes);
+        for (int v = tid; v < 2 * vec; v += kAttnThreads) {
+          const int w = v < vec ? v : v - vec;
+          const uint4 x = v < vec ? ks[w] : vs[w];
+          uint32_t* dst = reinterpret_cast<uint32_t*>(dyn + (v < vec ? Ly::kOffK : Ly::kOffV) +
+                                                      (w / kVecRow) * Ly::kStride + (w % kVecRow) * 16);
+          dst[0] = x.x;
+          dst[1] = x.y;
+          dst[2] = x.z;
+          dst[3] = x.w;
+        }
+        if constexpr (KIND == HS_KV_FP8E4M3_G32) {
+          constexpr int G = D / kQuantGroup;
+          for (int v = tid; v < 2 * rows * G; v += kAttnThreads) {
+            if (v < rows * G)
+              reinterpret_cast<float*>(dyn + Ly::kOffKs)[v] = hb.k_slot_scales[(row0 + r0) * G + v];
+            else
+              reinterpret_cast<float*>(dyn + Ly::kOffVs)[v - rows * G] = hb.v_slot_scales[(row0 + r0) * G + v - rows * G];
+          }
+        }
+      }
+      __syncthreads();
+      // scores: thread (h, t) takes the dot product of head h with token t
+      for (int idx = tid; idx < g * kSub; idx += kAttnThreads) {
+        const int h = idx / kSub, t = idx - h * kSub;
+        if (t < rows) {
+          const float4* qv = reinterpret_cast<const float4*>(s_q + h * D);
+          float a0 = 0.0f, a1 = 0.0f;
+#pragma unroll 8
+          for (int d4 = 0; d4 < D / 4; ++d4) {
+            const float4 k4 = staged_val4<C, KIND>(dyn + Ly::kOffK, ksc, t, d4 * 4);
+            const float4 q4 = qv[d4];
+            a0 = fmaf(q4.x, k4.x, a0);
+            a1 = fmaf(q4.y, k4.y, a1);
+            a0 = fmaf(q4.z, k4.z, a0);
+            a1 = fmaf(q4.w, k4.w, a1);
+          }
+          s_p[h * kSub + t] = (a0 + a1) * ma.scale_log2;
+        }
+      }
+      __syncthreads();
+      // running max / sum per head; s_p becomes p = 2^(s - m)
+      for (int h = warp; h < g; h += kAttnThreads / 32) {
+        float mb = -INFINITY;
+        for (int t = lane; t < rows; t += 32) mb = fmaxf(mb, s_p[h * kSub + t]);
+        mb = warp_max(mb);
+        const float m_old = s_m[h];
+        const float m_new = fmaxf(m_old, mb);
+        float sum = 0.0f;
+        for (int t = lane; t < rows; t += 32) {
+          const float pv = exp2f(s_p[h * kSub + t] - m_new);
+          s_p[h * kSub + t] = pv;
+          sum += pv;
+        }
+        sum = warp_sum(sum);
+        if (lane == 0) {
+          const float alpha = m_old == -INFINITY ? 0.0f : exp2f(m_old - m_new);
+          s_alpha[h] = alpha;
+          s_l[h] = s_l[h] * alpha + sum;
+          s_m[h] = m_new;
+        }
+      }
+      __syncthreads();
+      // o[h][d] = o[h][d] * alpha_h + sum_t p[h][t] v[t][d]
+#pragma unroll
+      for (int ai = 0; ai < kAcc; ++ai) {
+        const int idx = tid + ai * kAttnThreads;
+        if (idx < g * D) {
+          const int h = idx / D, d = idx - h * D;
+          float a = acc[ai] * s_alpha[h];
+          for (int t = 0; t < rows; ++t) a = fmaf(s_p[h * kSub + t], staged_val<C, KIND>(dyn + Ly::kOffV, vsc, t, d), a);
+          acc[ai] = a;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  // normalised output and lse of every query head of the stream
+#pragma unroll
+  for (int ai = 0; ai < kAcc; ++ai) {
+    const int idx = tid + ai * kAttnThreads;
+    if (idx < g * D) {
+      const int h = idx / D, d = idx - h * D;
+      const float l = s_l[h];
+      if (l > 0.0f) ma.out[(qrow0 + h) * D + d] = acc[ai] / l;
+      if (d == 0) ma.lse[qrow0 + h] = l > 0.0f ? (s_m[h] + log2f(l)) * 0.6931471805599453f : -INFINITY;
+    }
+  }
+  (void)err;
+}
+
 }  // namespace
+
+template <int C, int KIND>
+cudaError_t launch_attend(const HotView& hb, const int32_t* miss_sel, const int32_t* miss_count, int capacity,
+                          const MissAttn& ma, unsigned* err, cudaStream_t st) {
+  constexpr int kBytes = AttendSmem<C, KIND>::kBytes;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(copied_blocks_attn_kernel<C, KIND>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  return launch_pdl(copied_blocks_attn_kernel<C, KIND>, dim3(hb.batch * hb.hkv), dim3(kAttnThreads), kBytes, st, hb,
+                    miss_sel, miss_count, capacity, ma, err);
+}
 
 cudaError_t launch_swapin(const HotView& hb, const int32_t* sel, const int32_t* sel_count,
                           int capacity, int step, hs_swap_stats* stats, unsigned* err,
@@ -176,6 +574,42 @@ cudaError_t launch_swapin(const HotView& hb, const int32_t* sel, const int32_t* 
   if (pairs == 0) return cudaSuccess;
   return launch_pdl(swapin_kernel, dim3(pairs), dim3(kThreads), 0, st, hb, sel, sel_count, capacity, step,
                     stats, err);
+}
+
+cudaError_t launch_swapin_plan(const HotView& hb, const int32_t* sel, const int32_t* sel_count, int capacity,
+                               int step, int32_t* hit_sel, int32_t* hit_count, int32_t* miss_sel,
+                               int32_t* miss_count, hs_swap_stats* stats, unsigned* err, cudaStream_t st) {
+  const int pairs = hb.batch * hb.hkv;
+  if (pairs == 0) return cudaSuccess;
+  return launch_pdl(swapin_plan_kernel, dim3(pairs), dim3(kThreads), 0, st, hb, sel, sel_count, capacity, step,
+                    hit_sel, hit_count, miss_sel, miss_count, stats, err);
+}
+
+cudaError_t launch_swapin_copy(const HotView& hb, const int32_t* miss_sel, const int32_t* miss_count,
+                               int capacity, int ctas, const MissAttnArgs* attn, hs_swap_stats* stats, unsigned* err,
+                               cudaStream_t st) {
+  const int pairs = hb.batch * hb.hkv;
+  if (pairs == 0) return cudaSuccess;
+  const int grid = ctas < pairs ? ctas : pairs;
+  cudaError_t e = launch_pdl(swapin_copy_kernel, dim3(grid), dim3(kCopyThreads), 0, st, hb, miss_sel, miss_count,
+                             capacity, stats, err);
+  if (e != cudaSuccess || !attn) return e;
+  MissAttn ma{};
+  ma.q = attn->q;
+  ma.seq_lens = attn->seq_lens;
+  ma.out = attn->out;
+  ma.lse = attn->lse;
+  ma.scale_log2 = attn->scale * 1.4426950408889634f;
+  ma.hq = attn->hq;
+  ma.group = attn->hq / hb.hkv;
+  if (hb.head_dim == 128) {
+    if (hb.kv_dtype == HS_KV_F32) return launch_attend<4, HS_KV_F32>(hb, miss_sel, miss_count, capacity, ma, err, st);
+    if (hb.kv_dtype == HS_KV_BF16) return launch_attend<4, HS_KV_BF16>(hb, miss_sel, miss_count, capacity, ma, err, st);
+    return launch_attend<4, HS_KV_FP8E4M3_G32>(hb, miss_sel, miss_count, capacity, ma, err, st);
+  }
+  if (hb.kv_dtype == HS_KV_F32) return launch_attend<2, HS_KV_F32>(hb, miss_sel, miss_count, capacity, ma, err, st);
+  if (hb.kv_dtype == HS_KV_BF16) return launch_attend<2, HS_KV_BF16>(hb, miss_sel, miss_count, capacity, ma, err, st);
+  return launch_attend<2, HS_KV_FP8E4M3_G32>(hb, miss_sel, miss_count, capacity, ma, err, st);
 }
 
 }  // namespace hs

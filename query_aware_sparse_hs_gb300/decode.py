@@ -37,9 +37,14 @@ class SparseDecode:
         self.sel = torch.full((batch, num_kv_heads, self.capacity), -1, dtype=torch.int32, device=dev)
         self.sel_count = torch.zeros((batch, num_kv_heads), dtype=torch.int32, device=dev)
         self.scores = torch.empty((batch, num_kv_heads, max_blocks), dtype=torch.float32, device=dev)
-        self.out = torch.empty((batch, num_q_heads, head_dim),
-                               dtype=torch.float32 if out_is_fp32 else torch.bfloat16, device=dev)
-        self.lse = torch.empty((batch, num_q_heads), dtype=torch.float32, device=dev)
+        # out and lse share one byte buffer (out first, 16-byte aligned), so a
+        # host read of a step's results is one transfer of ``results``
+        odt = torch.float32 if out_is_fp32 else torch.bfloat16
+        ob = batch * num_q_heads * head_dim * (4 if out_is_fp32 else 2)
+        ob16 = (ob + 15) // 16 * 16
+        self.results = torch.empty((ob16 + batch * num_q_heads * 4,), dtype=torch.uint8, device=dev)
+        self.out = self.results[:ob].view(odt).view(batch, num_q_heads, head_dim)
+        self.lse = self.results[ob16:].view(torch.float32).view(batch, num_q_heads)
         ws = hs.hs_workspace_bytes(self.shape, batch, self.capacity, self.attn_params)
         self.workspace = torch.empty((max(ws, 256),), dtype=torch.uint8, device=dev)
 
@@ -62,6 +67,52 @@ class SparseDecode:
     def swap_in(self, hb: hs.HotBuffer, step: int, stats=None, stream=None):
         hs.hs_swapin_misses(self.shape, hb, self.sel, self.sel_count, self.capacity, step, stats, stream)
 
+    def enable_swap_overlap(self, copy_ctas: int = 24, attn_ctas: int = 0):
+        """Allocates what the overlapped swap-in step needs: hit and miss lists,
+        two fp32 partial results, a side stream for the page copy.  The copy
+        kernel runs ``copy_ctas`` CTAs, each on an SM of its own; the attention
+        over the hits runs at most ``attn_ctas`` CTAs (0 = the SMs the copy
+        leaves).  The copy kernel also computes the attention over the blocks
+        it brings in."""
+        dev = self.sel.device
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        if not 0 < copy_ctas < sms or attn_ctas < 0:
+            raise ValueError(f"copy_ctas must be in [1, {sms - 1}], attn_ctas >= 0")
+        self.copy_ctas = int(copy_ctas)
+        attn_ctas = int(attn_ctas) if attn_ctas > 0 else sms - self.copy_ctas
+        self.hit_sel = torch.full_like(self.sel, -1)
+        self.miss_sel = torch.full_like(self.sel, -1)
+        self.hit_count = torch.zeros_like(self.sel_count)
+        self.miss_count = torch.zeros_like(self.sel_count)
+        b, hq, d = self.out.shape
+        self.part_out = torch.empty((2, b, hq, d), dtype=torch.float32, device=dev)
+        self.part_lse = torch.empty((2, b, hq), dtype=torch.float32, device=dev)
+        p = self.attn_params
+        self.hit_params = hs.attn_params(p.scale, True, p.blocks_per_split, p.algo, max_ctas=attn_ctas)
+        ws = hs.hs_workspace_bytes(self.shape, self.batch, self.capacity, self.hit_params)
+        if ws > self.workspace.numel():
+            self.workspace = torch.empty((ws,), dtype=torch.uint8, device=dev)
+        self.side_stream = torch.cuda.Stream(device=dev)
+
+    def swap_in_overlapped(self, hb: hs.HotBuffer, slot_kv: hs.PagedKV, q: torch.Tensor, step: int,
+                           stats=None, stream=None):
+        """Swap-in and attention with the page copy overlapped: plan (hit and
+        miss lists) -> [side stream: copy the missed pages and attend over
+        them] | attention over the hits -> LSE merge of the two parts into
+        ``out``/``lse``.  Needs enable_swap_overlap() first."""
+        main = stream if stream is not None else torch.cuda.current_stream(self.sel.device)
+        hs.hs_swapin_plan(self.shape, hb, self.sel, self.sel_count, self.capacity, step, self.hit_sel,
+                          self.hit_count, self.miss_sel, self.miss_count, stats, main)
+        side = self.side_stream
+        side.wait_stream(main)
+        hs.hs_swapin_copy_attend(self.shape, hb, slot_kv.seq_lens, q, self.miss_sel, self.miss_count, self.capacity,
+                                 self.attn_params.scale, self.part_out[1], self.part_lse[1], self.copy_ctas, stats,
+                                 side)
+        hs.hs_sparse_paged_decode_attn(self.shape, slot_kv, q, self.hit_sel, self.hit_count, self.capacity,
+                                       self.hit_params, self.part_out[0], self.part_lse[0], self.workspace, main)
+        main.wait_stream(side)
+        hs.hs_merge_attn_partials(self.shape, self.part_out, self.part_lse, self.out, self.lse, main)
+
     def step(self, kv: hs.PagedKV, q: torch.Tensor, refresh_from_block: int | None = None,
              hot: tuple | None = None, new_kv: tuple | None = None, stream=None):
         """One decode step.  ``new_kv``: (new_k, new_v) of the token at
@@ -70,7 +121,8 @@ class SparseDecode:
         from there on (the block holding the newest token) before selecting.
         ``hot``: (hot_buffer, slot_kv_view, step, stats) for the offload path:
         the selection is made against ``kv`` (summaries), pages are swapped into
-        the hot slots and attention reads ``slot_kv_view``."""
+        the hot slots and attention reads ``slot_kv_view`` (with the page copy
+        overlapped once enable_swap_overlap() was called)."""
         if new_kv is not None:
             self.append(kv, new_kv[0], new_kv[1], stream)
         if refresh_from_block is not None:
@@ -78,8 +130,11 @@ class SparseDecode:
         self.select(kv, q, stream=stream)
         if hot is not None:
             hb, slot_kv, step_idx, stats = hot
-            self.swap_in(hb, step_idx, stats, stream)
-            self.attend(slot_kv, q, stream)
+            if getattr(self, "side_stream", None) is not None:
+                self.swap_in_overlapped(hb, slot_kv, q, step_idx, stats, stream)
+            else:
+                self.swap_in(hb, step_idx, stats, stream)
+                self.attend(slot_kv, q, stream)
         else:
             self.attend(kv, q, stream)
         return self.out, self.lse

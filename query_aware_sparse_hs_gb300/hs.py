@@ -50,7 +50,7 @@ class SelectParams(ctypes.Structure):
 
 class AttnParams(ctypes.Structure):
     _fields_ = [("scale", c_float), ("out_is_fp32", c_int32), ("blocks_per_split", c_int32),
-                ("algo", c_int32)]
+                ("algo", c_int32), ("max_ctas", c_int32)]
 
 
 class HotBuffer(ctypes.Structure):
@@ -86,6 +86,15 @@ SYMBOLS = {
                                                       c_void_p, c_void_p, c_void_p]),
     "hs_swapin_misses": (c_int32, [POINTER(AttnShape), POINTER(HotBuffer), c_void_p, c_void_p, c_int32,
                                    c_int32, c_void_p, c_void_p]),
+    "hs_swapin_plan": (c_int32, [POINTER(AttnShape), POINTER(HotBuffer), c_void_p, c_void_p, c_int32, c_int32,
+                                 c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
+    "hs_swapin_copy": (c_int32, [POINTER(AttnShape), POINTER(HotBuffer), c_void_p, c_void_p, c_int32, c_int32,
+                                 c_void_p, c_void_p]),
+    "hs_swapin_copy_attend": (c_int32, [POINTER(AttnShape), POINTER(HotBuffer), c_void_p, c_void_p, c_void_p,
+                                        c_void_p, c_int32, c_float, c_int32, c_void_p, c_void_p, c_void_p,
+                                        c_void_p]),
+    "hs_merge_attn_partials": (c_int32, [POINTER(AttnShape), c_int32, c_int32, c_void_p, c_void_p, c_void_p,
+                                         c_int32, c_void_p, c_void_p]),
     "hs_quantize_e4m3_g32": (c_int32, [c_void_p, c_int32, c_int64, c_int32, c_void_p, c_void_p,
                                        c_void_p]),
     "hs_get_device_error": (c_int32, [c_void_p, POINTER(c_uint32)]),
@@ -125,8 +134,8 @@ def _check(status: int, where: str):
 
 
 def _ptr(t) -> int | None:
-    if t is None:
-        return None
+    if t is None or isinstance(t, int):  # None, or an address already
+        return t
     if not t.is_contiguous():
         raise ValueError("tensor arguments must be contiguous")
     return t.data_ptr()
@@ -158,9 +167,9 @@ def select_params(sink_tokens, window_tokens, k_scored, capacity) -> SelectParam
     return SelectParams(sink_tokens, window_tokens, k_scored, capacity)
 
 
-def attn_params(scale, out_is_fp32=False, blocks_per_split=0, algo="auto") -> AttnParams:
+def attn_params(scale, out_is_fp32=False, blocks_per_split=0, algo="auto", max_ctas=0) -> AttnParams:
     return AttnParams(float(scale), 1 if out_is_fp32 else 0, int(blocks_per_split),
-                      ALGO[algo] if isinstance(algo, str) else int(algo))
+                      ALGO[algo] if isinstance(algo, str) else int(algo), int(max_ctas))
 
 
 def hs_workspace_bytes(shape: AttnShape, batch: int, capacity: int, params: AttnParams) -> int:
@@ -229,6 +238,37 @@ def hs_swapin_misses(shape, hb, sel, sel_count, capacity, step, stats=None, stre
     _check(_lib.hs_swapin_misses(ctypes.byref(shape), ctypes.byref(hb), _ptr(sel), _ptr(sel_count),
                                  int(capacity), int(step), _ptr(stats), _stream(stream)),
            "hs_swapin_misses")
+
+
+def hs_swapin_plan(shape, hb, sel, sel_count, capacity, step, hit_sel, hit_count, miss_sel, miss_count,
+                   stats=None, stream=None):
+    _check(_lib.hs_swapin_plan(ctypes.byref(shape), ctypes.byref(hb), _ptr(sel), _ptr(sel_count), int(capacity),
+                               int(step), _ptr(hit_sel), _ptr(hit_count), _ptr(miss_sel), _ptr(miss_count),
+                               _ptr(stats), _stream(stream)),
+           "hs_swapin_plan")
+
+
+def hs_swapin_copy(shape, hb, miss_sel, miss_count, capacity, max_ctas=0, stats=None, stream=None):
+    _check(_lib.hs_swapin_copy(ctypes.byref(shape), ctypes.byref(hb), _ptr(miss_sel), _ptr(miss_count),
+                               int(capacity), int(max_ctas), _ptr(stats), _stream(stream)),
+           "hs_swapin_copy")
+
+
+def hs_swapin_copy_attend(shape, hb, seq_lens, q, miss_sel, miss_count, capacity, scale, out, lse, max_ctas=0,
+                          stats=None, stream=None):
+    _check(_lib.hs_swapin_copy_attend(ctypes.byref(shape), ctypes.byref(hb), _ptr(seq_lens), _ptr(q), _ptr(miss_sel),
+                                      _ptr(miss_count), int(capacity), float(scale), int(max_ctas), _ptr(out),
+                                      _ptr(lse), _ptr(stats), _stream(stream)),
+           "hs_swapin_copy_attend")
+
+
+def hs_merge_attn_partials(shape, outs, lses, out, lse=None, stream=None):
+    """outs [parts][batch][Hq][D] f32, lses [parts][batch][Hq] f32 -> out (bf16 or f32), lse."""
+    parts, batch = outs.shape[0], outs.shape[1]
+    _check(_lib.hs_merge_attn_partials(ctypes.byref(shape), int(batch), int(parts), _ptr(outs), _ptr(lses),
+                                       _ptr(out), 1 if out.dtype == torch.float32 else 0, _ptr(lse),
+                                       _stream(stream)),
+           "hs_merge_attn_partials")
 
 
 def hs_quantize_e4m3_g32(src, codes, scales, stream=None):

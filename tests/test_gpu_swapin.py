@@ -37,8 +37,13 @@ def _pool(w, x):
     return x["k_pages"].pin_memory(), x["v_pages"].pin_memory(), None, None
 
 
+@pytest.mark.parametrize("mode", ["one_call", "overlapped"])
 @pytest.mark.parametrize("kv_dtype", ["bf16", "fp8"])
-def test_swapin_tables_bit_exact_and_attention(kv_dtype):
+def test_swapin_tables_bit_exact_and_attention(kv_dtype, mode):
+    """one_call: hs_swapin_misses then attention over the selection.
+    overlapped: plan -> copy on a side stream (3 CTAs, several streams each)
+    beside attention over the hits -> attention over the misses -> LSE merge;
+    the hit and miss lists must be the oracle's partition of the selection."""
     from query_aware_sparse_hs_gb300 import hs
     from query_aware_sparse_hs_gb300.decode import SparseDecode
     w, x = _setup(kv_dtype)
@@ -66,6 +71,8 @@ def test_swapin_tables_bit_exact_and_attention(kv_dtype):
     dec = SparseDecode(num_q_heads=w.num_q_heads, num_kv_heads=hkv, head_dim=D, block_size=B,
                        kv_dtype=kv_dtype, batch=w.batch, max_blocks=nb, sink_tokens=w.sink_tokens,
                        window_tokens=w.window_tokens, k_scored=w.k_scored, out_is_fp32=True)
+    if mode == "overlapped":
+        dec.enable_swap_overlap(copy_ctas=3)
     dec.build_summaries(pool_kv)  # summaries read the pinned pool directly
     st, bits = hs.hs_get_device_error()
     assert st == 0, bits
@@ -94,6 +101,8 @@ def test_swapin_tables_bit_exact_and_attention(kv_dtype):
         sel = np.full((w.batch, hkv, dec.capacity), -1, dtype=np.int32)
         cnt = np.zeros((w.batch, hkv), dtype=np.int32)
         ref = np.zeros((w.batch, w.num_q_heads, D))
+        ref_lse = np.zeros((w.batch, w.num_q_heads))
+        parts = {}
         for b in range(w.batch):
             for kvh in range(hkv):
                 K, V, smin, smax = KV[(b, kvh)]
@@ -103,17 +112,30 @@ def test_swapin_tables_bit_exact_and_attention(kv_dtype):
                                     w.k_scored)
                 sel[b, kvh, :len(s)] = s
                 cnt[b, kvh] = len(s)
+                resident = {j for j, e in enumerate(sim[b * hkv + kvh].page_table) if e >= 0}
+                parts[(b, kvh)] = ([j for j in s if j in resident], [j for j in s if j not in resident])
                 _, st_ = sim[b * hkv + kvh].step(s, t)
                 want += [st_["hits"], st_["misses"], st_["evictions"]]
                 total_misses += st_["misses"]
-                ref[b, kvh * g:(kvh + 1) * g] = O.sparse_attention(qg, K, V, s, B, 1 / math.sqrt(D))[0]
+                o_, l_ = O.sparse_attention(qg, K, V, s, B, 1 / math.sqrt(D))
+                ref[b, kvh * g:(kvh + 1) * g], ref_lse[b, kvh * g:(kvh + 1) * g] = o_, l_
         dec.sel.copy_(torch.from_numpy(sel))
         dec.sel_count.copy_(torch.from_numpy(cnt))
-        dec.swap_in(hb, t, stats)
         qd = q.to(dev)
-        dec.attend(slot_kv, qd)
+        if mode == "one_call":
+            dec.swap_in(hb, t, stats)
+            dec.attend(slot_kv, qd)
+        else:
+            dec.swap_in_overlapped(hb, slot_kv, qd, t, stats)
         st, bits = hs.hs_get_device_error()
         assert st == 0, bits
+        if mode == "overlapped":
+            hs_, hc = dec.hit_sel.cpu().numpy(), dec.hit_count.cpu().numpy()
+            ms_, mc = dec.miss_sel.cpu().numpy(), dec.miss_count.cpu().numpy()
+            for (b, kvh), (hits, misses) in parts.items():
+                assert hc[b, kvh] == len(hits) and mc[b, kvh] == len(misses), (t, b, kvh)
+                assert hs_[b, kvh].tolist() == hits + [-1] * (dec.capacity - len(hits))
+                assert ms_[b, kvh].tolist() == misses + [-1] * (dec.capacity - len(misses))
         gt, go, gl = hot_table.cpu().numpy(), owner.cpu().numpy(), last.cpu().numpy()
         for p in range(pairs):
             b, kvh = divmod(p, hkv)
@@ -122,6 +144,7 @@ def test_swapin_tables_bit_exact_and_attention(kv_dtype):
             assert gl[b, kvh].tolist() == sim[p].last_used, (t, p)
         tol = 2e-3
         assert np.abs(dec.out.cpu().numpy() - ref).max() <= tol, t
+        assert np.abs(dec.lse.cpu().numpy() - ref_lse).max() <= 1e-4, t
     # slot contents equal the pool pages they hold
     ks_np = k_slots.cpu()
     for p in range(pairs):
@@ -155,3 +178,79 @@ def test_swapin_capacity_error_leaves_tables():
     st, bits = hs.hs_get_device_error()
     assert st == hs.HS_ERR_CAPACITY and bits & hs.HS_EBIT_CAPACITY
     assert bool((table == -1).all()) and bool((owner == -1).all())
+
+
+@pytest.mark.parametrize("out_fp32", [True, False])
+def test_merge_attn_partials_matches_the_oracle(out_fp32):
+    """Three partials per row, some of them empty (lse = -inf, out = 0), one
+    row with every part empty; against the oracle's LSE merge row by row."""
+    from query_aware_sparse_hs_gb300 import hs
+    parts, batch, hq, D = 3, 2, 8, 128
+    g = torch.Generator().manual_seed(7)
+    outs = torch.randn((parts, batch, hq, D), generator=g)
+    lses = torch.randn((parts, batch, hq), generator=g) * 4
+    lses[0, 0, 1] = -math.inf
+    lses[1, 1, 2] = lses[2, 1, 2] = -math.inf
+    lses[:, 1, 5] = -math.inf
+    outs[lses == -math.inf] = 0.0
+    shape = hs.attn_shape(hq, 2, D, 64, "bf16")
+    out = torch.empty((batch, hq, D), dtype=torch.float32 if out_fp32 else torch.bfloat16, device="cuda")
+    lse = torch.empty((batch, hq), device="cuda")
+    hs.hs_merge_attn_partials(shape, outs.cuda(), lses.cuda(), out, lse)
+    st, bits = hs.hs_get_device_error()
+    assert st == 0, bits
+    got, got_lse = out.float().cpu().numpy(), lse.cpu().numpy()
+    for b in range(batch):
+        for h in range(hq):
+            ref, ref_lse = O.lse_merge([outs[p, b, h].numpy() for p in range(parts)], lses[:, b, h].numpy())
+            tol = 1e-5 if out_fp32 else np.maximum(1e-5, np.abs(ref) * 2.0 ** -8)
+            assert np.all(np.abs(got[b, h] - ref) <= tol), (b, h)
+            if np.isneginf(ref_lse):
+                assert np.isneginf(got_lse[b, h]) and np.all(got[b, h] == 0)
+            else:
+                assert abs(got_lse[b, h] - ref_lse) <= 1e-5 * max(1.0, abs(ref_lse)), (b, h)
+
+
+def test_plan_then_copy_equals_the_one_call_swapin():
+    """hs_swapin_plan + hs_swapin_copy (2 CTAs) leave the same tables and slot
+    contents as hs_swapin_misses, over several steps of a drifting selection."""
+    from query_aware_sparse_hs_gb300 import hs
+    w, x = _setup("bf16", batch=2, blocks=40, slots=12, k_scored=6)
+    dev = torch.device("cuda")
+    B, D, S, hkv, nb = w.block_size, w.head_dim, w.hot_slots, w.num_kv_heads, w.max_blocks
+    hk, hv, _, _ = _pool(w, x)
+    pairs, cap = w.batch * hkv, 12
+    shape = hs.attn_shape(w.num_q_heads, hkv, D, B, "bf16")
+
+    def buffer():
+        t = torch.full((w.batch, hkv, nb), -1, dtype=torch.int32, device=dev)
+        o = torch.full((w.batch, hkv, S), -1, dtype=torch.int32, device=dev)
+        l = torch.full((w.batch, hkv, S), -1, dtype=torch.int32, device=dev)
+        k = torch.zeros((pairs * S, B, D), dtype=torch.bfloat16, device=dev)
+        v = torch.zeros_like(k)
+        return hs.hot_buffer(t, o, l, k, v, hk, hv, S), (t, o, l, k, v)
+
+    hb1, st1 = buffer()
+    hb2, st2 = buffer()
+    g = torch.Generator().manual_seed(3)
+    lists = [torch.full((w.batch, hkv, cap), -1, dtype=torch.int32, device=dev) for _ in range(2)]
+    counts = [torch.zeros((w.batch, hkv), dtype=torch.int32, device=dev) for _ in range(2)]
+    stats1 = torch.zeros(4, dtype=torch.int64, device=dev)
+    stats2 = torch.zeros(4, dtype=torch.int64, device=dev)
+    for t in range(6):
+        sel = torch.full((w.batch, hkv, cap), -1, dtype=torch.int32)
+        cnt = torch.zeros((w.batch, hkv), dtype=torch.int32)
+        for p in range(pairs):
+            k = int(torch.randint(1, cap + 1, (1,), generator=g))
+            pick = torch.sort(torch.randperm(nb, generator=g)[:k]).values
+            sel.view(pairs, cap)[p, :k] = pick.int()
+            cnt.view(pairs)[p] = k
+        sel, cnt = sel.to(dev), cnt.to(dev)
+        hs.hs_swapin_misses(shape, hb1, sel, cnt, cap, t, stats1)
+        hs.hs_swapin_plan(shape, hb2, sel, cnt, cap, t, lists[0], counts[0], lists[1], counts[1], stats2)
+        hs.hs_swapin_copy(shape, hb2, lists[1], counts[1], cap, 2, stats2)
+        st, bits = hs.hs_get_device_error()
+        assert st == 0, bits
+        for a, b in zip(st1, st2):
+            assert torch.equal(a, b), t
+    assert torch.equal(stats1, stats2)
