@@ -20,7 +20,9 @@ Sources, cited by page title and section:
   offload target driven by the sparse attention's current access set.
 * [SPD] "SparDA：把KV選擇提前一層，長上下文推理顯存帶寬雙優化":
   §1.1 KV bytes per token of an 8B GQA model; §4.2 selector = attention sink +
-  local window + remote top-k; §4.3 sparse index kept over PagedAttention blocks.
+  local window + remote top-k; §4.3 sparse index kept over PagedAttention blocks;
+  §6.1 selection scores smoothed over decode steps, 70% this step's value and
+  30% the previous step's smoothed value.
 * [FLL] "分块稀疏注意力与KV Cache量化：长文本推理显存优化实践":
   §2.2 tiled attention whose partial softmax statistics (running max and
   normaliser) are carried across tiles; §2.4 grouped KV quantisation along the
@@ -48,6 +50,10 @@ Readings where the pages are silent (each is also listed in the design notes):
   smallest ``last_used`` (ties -> lowest slot); the evicted block's page-table
   entry becomes -1; no write-back (the host pool keeps every page).
 * Empty selection (zero-length request): output 0, lse = -inf.
+* Score smoothing ([SPD] §6.1): applied to the per-block selection score
+  (the group bound) of each (request, kv head): s~_t = (1 - w) s_t + w s~_{t-1}
+  with w = 0.3, and s~_t = s_t for a block without history (first step, or a
+  block new since the last step).
 
 Parity pins (``tests/test_oracle.py``): e4m3 decode against torch's
 float8_e4m3fn; e4m3 encode by brute force over all codes and against torch;
@@ -57,7 +63,8 @@ enumeration of every k-subset; attention against
 ``torch.nn.functional.scaled_dot_product_attention`` in float64 and by the
 weights-sum-to-one and single-token cases; LSE merge against the one-pass
 softmax; hot buffer against a hand-worked trace (``tests/golden``) and the
-table invariants.  No function here is unpinned.
+table invariants; score smoothing against its unrolled closed form.  No
+function here is unpinned.
 """
 
 from __future__ import annotations
@@ -250,6 +257,16 @@ def forced_blocks(seq_len: int, block_size: int, sink_tokens: int, window_tokens
         if in_sink or in_window:
             out.append(j)
     return out
+
+
+def smooth_scores(scores, history, weight: float) -> np.ndarray:
+    """Exponential smoothing of selection scores across decode steps ([SPD]
+    §6.1): where ``history`` (the previous step's smoothed scores) is a number,
+    the result is (1 - weight) * score + weight * history; where it is NaN (no
+    history yet) the score itself.  The result is the next step's history."""
+    s = np.asarray(scores, dtype=np.float64)
+    h = np.asarray(history, dtype=np.float64)
+    return np.where(np.isnan(h), s, (1.0 - weight) * s + weight * h)
 
 
 def select_blocks(scores, forced, k_scored: int) -> list:

@@ -363,3 +363,26 @@ def test_hot_buffer_capacity_error():
     hb = O.HotBuffer(10, 2)
     with pytest.raises(O.CapacityError):
         hb.step([1, 2, 3], 0)
+
+
+def test_score_smoothing_matches_its_unrolled_form():
+    """s~_t = 0.7 s_t + 0.3 s~_{t-1} from an empty history unrolls to
+    sum_k 0.7 * 0.3^k s_{t-k} plus 0.3^t s_0 (weights summing to one); blocks
+    whose history is NaN (new blocks) take their raw score."""
+    w, T, N = 0.3, 6, 9
+    seq = RNG.normal(size=(T, N))
+    h = np.full(N, np.nan)
+    for t in range(T):
+        h = O.smooth_scores(seq[t], h, w)
+        closed = sum((1 - w) * w ** k * seq[t - k] for k in range(t)) + w ** t * seq[0]
+        assert np.allclose(h, closed, rtol=1e-12, atol=1e-12)
+    # a constant score is a fixed point; weight 0 is the identity
+    c = np.full(N, 2.5)
+    assert np.array_equal(O.smooth_scores(c, c, w), c)
+    assert np.array_equal(O.smooth_scores(seq[1], seq[0], 0.0), seq[1])
+    # mixed history: NaN entries take the raw score, the others blend
+    hist = seq[0].copy()
+    hist[::2] = np.nan
+    got = O.smooth_scores(seq[1], hist, w)
+    assert np.array_equal(got[::2], seq[1][::2])
+    assert np.allclose(got[1::2], 0.7 * seq[1][1::2] + 0.3 * seq[0][1::2], rtol=1e-12)
