@@ -552,7 +552,7 @@ def run_offload(args, w):
     stats = torch.zeros(4, dtype=torch.int64, device=dev)
     dec = SparseDecode(num_q_heads=w.num_q_heads, num_kv_heads=hkv, head_dim=D, block_size=B, kv_dtype=w.kv_dtype,
                        batch=w.batch, max_blocks=nb, sink_tokens=w.sink_tokens, window_tokens=w.window_tokens,
-                       k_scored=w.k_scored, device=dev)
+                       k_scored=w.k_scored, score_smoothing=args.score_smoothing, device=dev)
     dec.build_summaries(pool_kv)  # read over the host link once
     if args.swap_overlap:
         dec.enable_swap_overlap(args.swap_copy_ctas, args.swap_attn_ctas)
@@ -562,6 +562,7 @@ def run_offload(args, w):
         table.fill_(-1)
         owner.fill_(-1)
         last.fill_(-1)
+        dec.reset_score_history()
 
     def step(t, st=None):
         dec.step(pool_kv, qs[t], hot=(hb, slot_kv, t, st), stream=stream)
@@ -681,6 +682,7 @@ def run_offload(args, w):
                  "link_frac": swap_bytes_step / (t_us["swapin"] * 1e-6) / 1e9 / link,
                  "page_bytes": page_bytes},
         "kernels_us": {"score_select": t_us["select"], "swapin": t_us["swapin"], "attention_with_merge": t_us["attention"]},
+        "score_smoothing": args.score_smoothing,
         "swap_overlap": {"overlapped": bool(args.swap_overlap), "copy_ctas": args.swap_copy_ctas,
                          "attn_ctas": args.swap_attn_ctas, "serial_ms_per_step": ms_serial},
         "cpu_baseline": cpu_baseline(w, seconds=args.cpu_seconds) if (world == 1 and args.cpu_seconds > 0) else None,
@@ -700,6 +702,8 @@ def main():
     ap.add_argument("--workload", default="llama8b_bf16")
     ap.add_argument("--layers", type=int, default=0, help="distinct layer copies (0 = fit ~24 GB, max 32)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--score-smoothing", type=float, default=0.0,
+                    help="offload workload: weight of the previous step's block scores (0.3 in the SparDA article)")
     ap.add_argument("--swap-overlap", type=int, default=1,
                     help="offload workload: 1 = page copy overlapped with attention over the hits, 0 = one after the other")
     ap.add_argument("--swap-copy-ctas", type=int, default=24, help="CTAs (SMs) of the overlapped page copy")

@@ -123,12 +123,22 @@ typedef struct hs_paged_kv {
  * further blocks are the best-scoring of the rest (ties -> lower index).
  * capacity is the row length of sel and must be >= the largest possible
  * selection, ceil(sink/B) + ceil(window/B) + 1 + k_scored (or max_blocks if
- * smaller). */
+ * smaller).
+ * Score smoothing across decode steps ([SPD] §6.1, which blends 70% of the
+ * current score with 30% of the previous one): with history_weight w in
+ * (0, 1), the score a block is ranked by is (1 - w) * score + w * h, where h
+ * is its entry in score_history when that is a number, else the score
+ * itself; the ranked value is then stored back into score_history.
+ * score_history [batch][Hkv][max_blocks] f32, device, read and written for
+ * blocks j < N_b; fill it with NaN before the first step.  w = 0 turns the
+ * smoothing off and score_history may be NULL. */
 typedef struct hs_select_params {
   int32_t sink_tokens;
   int32_t window_tokens;
   int32_t k_scored;
   int32_t capacity;
+  float history_weight;
+  float* score_history;
 } hs_select_params;
 
 /* Attention options.  scale multiplies q.k (usually 1/sqrt(head_dim)).
@@ -234,7 +244,7 @@ HS_API size_t hs_select_workspace_bytes(const hs_attn_shape* shape, int32_t batc
  *   score[b][kvh][j] = max of U over the g query heads of kv head kvh
  * then sel = forced blocks + the k_scored best other blocks (score descending,
  * lower index first on ties, NaN last), ascending; all N_b blocks when that
- * covers them.  sel_count = number selected; sel entries up to capacity past
+ * covers them (ranked by the smoothed score when params->history_weight > 0).  sel_count = number selected; sel entries up to capacity past
  * the count are -1.  scores_opt (nullable) [batch][Hkv][max_blocks] f32
  * receives the scores of blocks j < N_b.  With bf16 summaries and head_dim 128
  * the bounds are computed on the tensor cores into scores_opt or, when it is

@@ -211,6 +211,9 @@ hs_status hs_score_select_topk(const hs_attn_shape* shape, const hs_paged_kv* kv
   if (params->sink_tokens < 0 || params->window_tokens < 0 || params->k_scored < 0 ||
       params->capacity < 1)
     return HS_ERR_INVALID_ARG;
+  if (!(params->history_weight >= 0.0f && params->history_weight < 1.0f)) return HS_ERR_INVALID_ARG;
+  if (params->history_weight > 0.0f && (!params->score_history || !aligned(params->score_history, 4)))
+    return HS_ERR_INVALID_ARG;
   if (kv->max_blocks > kMaxSelectBlocks) return HS_ERR_UNSUPPORTED;
   if (params->capacity < max_selected(shape, kv->max_blocks, params->sink_tokens,
                                       params->window_tokens, params->k_scored))
@@ -229,6 +232,8 @@ hs_status hs_score_select_topk(const hs_attn_shape* shape, const hs_paged_kv* kv
   a.window_tokens = params->window_tokens;
   a.k_scored = params->k_scored;
   a.capacity = params->capacity;
+  a.history_weight = params->history_weight;
+  a.history = params->history_weight > 0.0f ? params->score_history : nullptr;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   if (score_tc_supported(v)) {
     // tensor-core bound scoring into a score buffer, then one CTA per pair selects

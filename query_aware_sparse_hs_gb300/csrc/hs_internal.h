@@ -14,6 +14,8 @@ struct SelectArgs {
   int32_t* sel_count;
   float* scores;  // nullable
   int32_t sink_tokens, window_tokens, k_scored, capacity;
+  float history_weight;  // 0: no smoothing
+  float* history;        // [batch][Hkv][max_blocks] smoothed scores of the previous step (NaN = none)
 };
 
 struct AttnArgs {

@@ -249,8 +249,19 @@ cudaError_t launch_merge(const KvView& kv, const AttnArgs& a, cudaStream_t st) {
 
 cudaError_t launch_merge_parts(int rows, int head_dim, int parts, const float* outs, const float* lses, void* out,
                                int out_f32, float* lse_out, cudaStream_t st) {
+  // A plain launch: the parts usually come from kernels on two streams, and the
+  // merge must wait for all of them, not only for the last kernel of its own
+  // stream.
+  if (rows == 0) return cudaSuccess;
   const int64_t D = head_dim, R = rows;
-  return launch_merge_rows(rows, head_dim, parts, outs, lses, D, R * D, int64_t(1), R, out, out_f32, lse_out, st);
+  const dim3 grid((rows + kMergeWarps - 1) / kMergeWarps);
+  if (head_dim == 128)
+    merge_kernel<4><<<grid, kMergeWarps * 32, 0, st>>>(rows, parts, outs, lses, D, R * D, int64_t(1), R, out, out_f32,
+                                                         lse_out);
+  else
+    merge_kernel<2><<<grid, kMergeWarps * 32, 0, st>>>(rows, parts, outs, lses, D, R * D, int64_t(1), R, out, out_f32,
+                                                         lse_out);
+  return cudaGetLastError();
 }
 
 }  // namespace hs

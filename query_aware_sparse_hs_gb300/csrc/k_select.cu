@@ -80,6 +80,24 @@ __device__ __forceinline__ void load_summary(const void* base, int64_t off, floa
   }
 }
 
+// Score smoothing across decode steps ("SparDA" article §6.1): where the
+// previous step's smoothed score h of a block is a number, the score becomes
+// (1 - w) * s + w * h; a block without history keeps s.  The result is stored
+// as the next step's history.  All threads of the CTA call it.
+__device__ __forceinline__ void smooth_scores(float* s_scores, int nb, int max_blocks, const SelectArgs& a,
+                                              int64_t pair) {
+  if (a.history_weight == 0.0f || a.history == nullptr) return;
+  float* h = a.history + pair * max_blocks;
+  const float w = a.history_weight, keep = 1.0f - a.history_weight;
+  for (int j = threadIdx.x; j < nb; j += blockDim.x) {
+    const float old = h[j];
+    const float v = old == old ? fmaf(w, old, keep * s_scores[j]) : s_scores[j];
+    s_scores[j] = v;
+    h[j] = v;
+  }
+  __syncthreads();
+}
+
 // Selection of one (request, kv head) from its block scores in shared memory,
 // by all kThreads threads of the CTA ("KV 稀疏化" wiki §2 sink/window, §5 top-k):
 // forced blocks in closed form, a 4-pass 8-bit radix select of the k-th largest
@@ -319,6 +337,7 @@ __global__ void __cluster_dims__(kSelectCluster, 1, 1) __launch_bounds__(kThread
   cluster.sync();
   if (rank != 0) return;
 
+  smooth_scores(s_scores, nb, kv.max_blocks, a, pair);
   select_pair(s_scores, nb, L, B, a, pair, s_hist, s_warp, s_pick, err);
 }
 
@@ -346,6 +365,7 @@ __global__ __launch_bounds__(kThreads) void select_only_kernel(KvView kv, Select
   for (int j = tid; j < nb; j += kThreads) s_scores[j] = src[j];
   for (int i = tid; i < 512; i += kThreads) s_hist[i >> 8][i & 255] = 0u;
   __syncthreads();
+  smooth_scores(s_scores, nb, kv.max_blocks, a, pair);
   select_pair(s_scores, nb, L, B, a, pair, s_hist, s_warp, s_pick, err);
 }
 

@@ -352,7 +352,7 @@ __global__ __launch_bounds__(kCopyThreads, 1) void swapin_copy_kernel(HotView hb
   __shared__ int s_n;
   // No early trigger: CTAs of a dependent launched early would wait on SMs
   // that the attention running beside the copy needs.
-  pdl_wait();
+  pdl_wait();  // (a no-op unless launched as a programmatic dependent)
   const int pairs = hb.batch * hb.hkv;
   const int S = hb.slots;
   unsigned long long pages = 0;
@@ -591,8 +591,10 @@ cudaError_t launch_swapin_copy(const HotView& hb, const int32_t* miss_sel, const
   const int pairs = hb.batch * hb.hkv;
   if (pairs == 0) return cudaSuccess;
   const int grid = ctas < pairs ? ctas : pairs;
-  cudaError_t e = launch_pdl(swapin_copy_kernel, dim3(grid), dim3(kCopyThreads), 0, st, hb, miss_sel, miss_count,
-                             capacity, stats, err);
+  // A plain launch: the copy usually follows a wait on another stream's plan,
+  // which it must not overtake.
+  swapin_copy_kernel<<<grid, kCopyThreads, 0, st>>>(hb, miss_sel, miss_count, capacity, stats, err);
+  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || !attn) return e;
   MissAttn ma{};
   ma.q = attn->q;

@@ -19,7 +19,7 @@ _Q_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16, "fp8": torch.bfloat16}
 class SparseDecode:
     def __init__(self, *, num_q_heads, num_kv_heads, head_dim, block_size, kv_dtype, batch,
                  max_blocks, sink_tokens, window_tokens, k_scored, capacity=None, scale=None,
-                 out_is_fp32=False, algo="auto", blocks_per_split=0, device="cuda"):
+                 out_is_fp32=False, algo="auto", blocks_per_split=0, score_smoothing=0.0, device="cuda"):
         self.kv_dtype = kv_dtype
         self.shape = hs.attn_shape(num_q_heads, num_kv_heads, head_dim, block_size, kv_dtype)
         self.batch, self.max_blocks = int(batch), int(max_blocks)
@@ -27,10 +27,14 @@ class SparseDecode:
             forced = -(-sink_tokens // block_size) + ((-(-window_tokens // block_size) + 1) if window_tokens > 0 else 0)
             capacity = min(self.max_blocks, forced + k_scored)
         self.capacity = int(capacity)
-        self.sel_params = hs.select_params(sink_tokens, window_tokens, k_scored, self.capacity)
+        dev = torch.device(device)
+        # scores smoothed across steps (weight of the previous step), NaN = no history
+        self.score_history = (torch.full((batch, num_kv_heads, max_blocks), float("nan"), device=dev)
+                              if score_smoothing > 0 else None)
+        self.sel_params = hs.select_params(sink_tokens, window_tokens, k_scored, self.capacity, score_smoothing,
+                                           self.score_history)
         self.attn_params = hs.attn_params(scale if scale is not None else 1.0 / math.sqrt(head_dim),
                                           out_is_fp32, blocks_per_split, algo)
-        dev = torch.device(device)
         sdt = _SUMMARY_DTYPE[kv_dtype]
         self.smin = torch.empty((batch, num_kv_heads, max_blocks, head_dim), dtype=sdt, device=dev)
         self.smax = torch.empty_like(self.smin)
@@ -47,6 +51,11 @@ class SparseDecode:
         self.lse = self.results[ob16:].view(torch.float32).view(batch, num_q_heads)
         ws = hs.hs_workspace_bytes(self.shape, batch, self.capacity, self.attn_params)
         self.workspace = torch.empty((max(ws, 256),), dtype=torch.uint8, device=dev)
+
+    def reset_score_history(self):
+        """Forget the smoothed scores (a new sequence of decode steps)."""
+        if self.score_history is not None:
+            self.score_history.fill_(float("nan"))
 
     def build_summaries(self, kv: hs.PagedKV, first_block: int = 0, stream=None):
         hs.hs_build_block_summaries(self.shape, kv, first_block, self.smin, self.smax, stream)

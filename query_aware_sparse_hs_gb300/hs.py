@@ -45,7 +45,7 @@ class PagedKV(ctypes.Structure):
 
 class SelectParams(ctypes.Structure):
     _fields_ = [("sink_tokens", c_int32), ("window_tokens", c_int32), ("k_scored", c_int32),
-                ("capacity", c_int32)]
+                ("capacity", c_int32), ("history_weight", c_float), ("score_history", c_void_p)]
 
 
 class AttnParams(ctypes.Structure):
@@ -163,8 +163,11 @@ def paged_kv(k_pages, v_pages, page_table, seq_lens, k_scales=None, v_scales=Non
     return kv
 
 
-def select_params(sink_tokens, window_tokens, k_scored, capacity) -> SelectParams:
-    return SelectParams(sink_tokens, window_tokens, k_scored, capacity)
+def select_params(sink_tokens, window_tokens, k_scored, capacity, history_weight=0.0,
+                  score_history=None) -> SelectParams:
+    p = SelectParams(sink_tokens, window_tokens, k_scored, capacity, float(history_weight), _ptr(score_history))
+    p._keep = score_history
+    return p
 
 
 def attn_params(scale, out_is_fp32=False, blocks_per_split=0, algo="auto", max_ctas=0) -> AttnParams:

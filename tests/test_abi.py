@@ -62,6 +62,13 @@ def test_host_checks_reject_bad_arguments_without_a_gpu():
     st = lib.hs_score_select_topk(ctypes.byref(shape), ctypes.byref(kv), 0x1000, 0x1000, 0x1000,
                                   ctypes.byref(params), 0x1000, 0x1000, None, None, 0, None)
     assert st == hs.HS_ERR_CAPACITY
+    # score smoothing: the weight must be in [0, 1) and needs a history buffer
+    for weight, hist in ((1.0, 0x1000), (-0.1, 0x1000), (0.3, None)):
+        p = hs.select_params(4, 256, 27, 33)
+        p.history_weight, p.score_history = weight, hist
+        st = lib.hs_score_select_topk(ctypes.byref(shape), ctypes.byref(kv), 0x1000, 0x1000, 0x1000,
+                                      ctypes.byref(p), 0x1000, 0x1000, None, None, 0, None)
+        assert st == hs.HS_ERR_INVALID_ARG, (weight, hist)
     assert lib.hs_quantize_e4m3_g32(0x1000, 0, 10, 96, 0x1000, 0x1000, None) == hs.HS_ERR_UNSUPPORTED
     # the append call: a missing new token, or an e4m3 cache without scales
     full = hs.PagedKV()
