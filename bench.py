@@ -363,9 +363,11 @@ def run_ours(args, w):
     torch.cuda.current_stream().wait_stream(stream)
 
     def one_step(i, q_override=None):
-        d = decs[i % layers]
-        d.step(kvs[i % layers], qs[i % layers] if q_override is None else q_override,
-               new_kv=news[i % layers], stream=stream)
+        li = i % layers
+        lead = li - li % args.select_every  # layer whose selection this layer uses
+        d = decs[li]
+        d.step(kvs[li], qs[li] if q_override is None else q_override, new_kv=news[li],
+               reuse=None if lead == li else decs[lead], stream=stream)
 
     # eager warm-up (module load, cluster attributes) before capture
     with torch.cuda.stream(stream):
@@ -425,7 +427,11 @@ def run_ours(args, w):
         stream.synchronize()
         return a.elapsed_time(b) * 1e3 / (rr * n)  # microseconds per launch
 
-    t_attn = timed_graph(lambda i: decs[i % layers].attend(kvs[i % layers], qs[i % layers], stream))
+    def lead_of(li):
+        return decs[li - li % args.select_every]
+
+    t_attn = timed_graph(lambda i: decs[i % layers].attend(kvs[i % layers], qs[i % layers], stream,
+                                                           selection=lead_of(i % layers)))
     t_sel = timed_graph(lambda i: decs[i % layers].select(kvs[i % layers], qs[i % layers], stream=stream))
     t_app = timed_graph(lambda i: decs[i % layers].append(kvs[i % layers], *news[i % layers], stream))
     t_sum_full = timed_graph(lambda i: decs[i % layers].build_summaries(kvs[i % layers], 0, stream), rr=3)
@@ -484,12 +490,14 @@ def run_ours(args, w):
     if rank != 0:
         return
     cpu = cpu_baseline(w, seconds=args.cpu_seconds) if (world == 1 and args.cpu_seconds > 0) else None
-    launches_per_step = step_launches(w, d0)
+    # layers that reuse a selection skip its two (or one) launches
+    sel_launches = 2 if (w.kv_dtype != "f32" and w.head_dim == 128) else 1
+    launches_per_step = step_launches(w, d0) - sel_launches * (1 - 1 / args.select_every)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
         "warmup": wreps * layers, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.kv_dtype, "data": "synthetic",
-        "config": workload_config(w, layers),
+        "config": dict(workload_config(w, layers), select_every=args.select_every),
         "hbm_gbs_step": step_bytes / (ms_per_step * 1e-3) / 1e9,
         "roofline": {"bound": "hbm", "kernel": "sparse_paged_decode_attn", "achieved": attn_gbs,
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": attn_gbs / peak,
@@ -504,7 +512,7 @@ def run_ours(args, w):
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": ms_e2e / steps},
-        "gpu_launches": launches_per_step * steps,
+        "gpu_launches": int(round(launches_per_step * steps)),
         "clocks": clk,
     }
     print(json.dumps(line), flush=True)
@@ -702,6 +710,9 @@ def main():
     ap.add_argument("--workload", default="llama8b_bf16")
     ap.add_argument("--layers", type=int, default=0, help="distinct layer copies (0 = fit ~24 GB, max 32)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--select-every", type=int, default=1,
+                    help="layers per selection: the first layer of each group selects, the others reuse it "
+                         "(SparDA-style cross-layer reuse); 1 = every layer selects")
     ap.add_argument("--score-smoothing", type=float, default=0.0,
                     help="offload workload: weight of the previous step's block scores (0.3 in the SparDA article)")
     ap.add_argument("--swap-overlap", type=int, default=1,
@@ -711,6 +722,8 @@ def main():
                     help="CTAs of the attention beside the copy (0 = the SMs the copy leaves)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.select_every < 1:
+        ap.error("--select-every must be >= 1")
     from synth import WORKLOADS
     w = WORKLOADS[args.workload]
     if args.impl == "reference":

@@ -69,8 +69,15 @@ class SparseDecode:
         hs.hs_score_select_topk(self.shape, kv, q, self.smin, self.smax, self.sel_params, self.sel,
                                 self.sel_count, self.scores if keep_scores else None, None, stream)
 
-    def attend(self, kv: hs.PagedKV, q: torch.Tensor, stream=None):
-        hs.hs_sparse_paged_decode_attn(self.shape, kv, q, self.sel, self.sel_count, self.capacity,
+    def attend(self, kv: hs.PagedKV, q: torch.Tensor, stream=None, selection=None):
+        """Attention over the selected blocks: this decoder's own selection, or
+        ``selection`` = another decoder whose selection is reused (a layer
+        that borrows the block mask of an earlier layer, as SparDA's deep layers
+        reuse the shallow layers' mask, §3.1 of its article)."""
+        src = self if selection is None else selection
+        if src.capacity != self.capacity:
+            raise ValueError("a reused selection must have the same capacity")
+        hs.hs_sparse_paged_decode_attn(self.shape, kv, q, src.sel, src.sel_count, self.capacity,
                                        self.attn_params, self.out, self.lse, self.workspace, stream)
 
     def swap_in(self, hb: hs.HotBuffer, step: int, stats=None, stream=None):
@@ -123,7 +130,7 @@ class SparseDecode:
         hs.hs_merge_attn_partials(self.shape, self.part_out, self.part_lse, self.out, self.lse, main)
 
     def step(self, kv: hs.PagedKV, q: torch.Tensor, refresh_from_block: int | None = None,
-             hot: tuple | None = None, new_kv: tuple | None = None, stream=None):
+             hot: tuple | None = None, new_kv: tuple | None = None, reuse=None, stream=None):
         """One decode step.  ``new_kv``: (new_k, new_v) of the token at
         seq_lens - 1, appended to the cache with its summary widened before
         selecting.  ``refresh_from_block``: instead rebuild summaries of blocks
@@ -131,11 +138,18 @@ class SparseDecode:
         ``hot``: (hot_buffer, slot_kv_view, step, stats) for the offload path:
         the selection is made against ``kv`` (summaries), pages are swapped into
         the hot slots and attention reads ``slot_kv_view`` (with the page copy
-        overlapped once enable_swap_overlap() was called)."""
+        overlapped once enable_swap_overlap() was called).  ``reuse``: skip
+        the scoring and selection and attend over the selection of ``reuse``
+        (another decoder, or ``self`` to keep this decoder's previous one)."""
         if new_kv is not None:
             self.append(kv, new_kv[0], new_kv[1], stream)
         if refresh_from_block is not None:
             self.build_summaries(kv, refresh_from_block, stream)
+        if reuse is not None:
+            if hot is not None:
+                raise ValueError("the offload path selects every step")
+            self.attend(kv, q, stream, selection=reuse)
+            return self.out, self.lse
         self.select(kv, q, stream=stream)
         if hot is not None:
             hb, slot_kv, step_idx, stats = hot
