@@ -149,13 +149,23 @@ typedef struct hs_select_params {
  * the tensor-core kernel runs one CTA on every SM; n > 0 = at most n CTAs (and
  * the automatic split for n SMs), leaving the other SMs to work launched
  * beside it, such as hs_swapin_copy.  Each of its CTAs takes a whole SM's
- * shared memory, so nothing else fits on an SM it occupies. */
+ * shared memory, so nothing else fits on an SM it occupies.
+ * split_counters (nullable): device array of at least batch * Hkv uint32, all
+ * zero before the first call that uses it.  When given, and the tensor-core
+ * kernel runs every work item on a CTA of its own, it merges the splits itself
+ * ([FLL] §2.2 log-sum-exp): each split of a (request, kv head) writes its
+ * partial result and counts itself in, and the split that arrives last merges
+ * them all into out/lse and sets the counter back to zero; no separate merge
+ * kernel is launched (otherwise one is).  Every counter is zero again when the
+ * call has completed; after HS_ERR_TIMEOUT, zero the array before reusing it.
+ * NULL (and the CUDA-core kernel): the merge runs as a separate kernel. */
 typedef struct hs_attn_params {
   float scale;
   int32_t out_is_fp32;
   int32_t blocks_per_split;
   int32_t algo;
   int32_t max_ctas;
+  uint32_t* split_counters;
 } hs_attn_params;
 
 /* HiSparse hot buffer ([KVS] §7).  One stream per (request, kv head) owns

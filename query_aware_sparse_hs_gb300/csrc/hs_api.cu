@@ -286,6 +286,8 @@ hs_status hs_sparse_paged_decode_attn(const hs_attn_shape* shape, const hs_paged
   const size_t need = workspace_for(shape, kv->batch, a.splits);
   if (need > 0 && (!workspace || ws_bytes < need || !aligned(workspace, 16))) return HS_ERR_WORKSPACE;
   a.sms = ctas;
+  if (params->split_counters && !aligned(params->split_counters, 4)) return HS_ERR_INVALID_ARG;
+  a.counters = params->split_counters;
   a.q = q;
   a.sel = sel;
   a.sel_count = sel_count;

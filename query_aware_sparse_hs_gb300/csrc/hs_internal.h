@@ -19,6 +19,7 @@ struct SelectArgs {
 };
 
 struct AttnArgs {
+  uint32_t* counters = nullptr;  // split arrival counters (tensor-core kernel merges in place)
   const void* q;
   const int32_t* sel;
   const int32_t* sel_count;

@@ -58,6 +58,7 @@ struct TcArgs {
   float* ws_lse;
   void* out;       // one split per pair: the final output and lse are written directly
   float* lse_out;
+  unsigned* counters;  // split arrivals per pair (null: a separate merge kernel runs)
   int64_t num_pages;
   int hkv, hq, group, block, max_blocks, capacity, bps, splits, items;
   int out_f32;
@@ -67,9 +68,14 @@ struct TcArgs {
 template <int NH>
 struct Layout {
   static constexpr int kPBytes = kChunk * 2 * NH * 2;
+  // P buffers: two per softmax group where they fit (a group writes P of its
+  // next chunk while the P.V product of its previous one may still read the
+  // other), else one per group, and the group then waits for that product
+  // before rewriting P
+  static constexpr int kPBufs = NH <= 8 ? 4 : 2;
   static constexpr int kOffQ = kStages * kStageBytes;
   static constexpr int kOffP = kOffQ + 2 * kQHalfBytes;
-  static constexpr int kOffX = kOffP + 2 * kPBytes;           // group exchange: o[NH][128], m[NH], l[NH]
+  static constexpr int kOffX = kOffP + kPBufs * kPBytes;      // group exchange: o[NH][128], m[NH], l[NH]
   static constexpr int kOffBar = kOffX + ((NH * 128 + 2 * NH) * 4 + 15) / 16 * 16;
   static constexpr int kNumBars = 2 * kStages + 11;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
@@ -122,6 +128,78 @@ __device__ __forceinline__ void put_partial(const TcArgs& a, int64_t row0, int h
     a.ws_o[row * kD + t] = o;
     if (t == 0) a.ws_lse[row] = lse;
   }
+}
+
+// Split-K completion without a merge launch ("分块稀疏注意力与KV Cache量化"
+// §2.2 log-sum-exp): once the 128 writer threads of an item have stored its
+// partials (a CTA barrier), one thread counts the item in on its pair's
+// counter with an acquire-release atomic, which publishes the CTA's partials
+// and, for the split that arrives last, makes every other split's visible.
+// That split merges them into the output and re-arms the counter.  No thread
+// waits for another CTA.  Thread t merges 8 channels of head t / 16 (heads in
+// rounds of 8), in the same order and arithmetic as the merge kernel.
+// bar_id = the writers' named barrier; s_last = a shared-memory word.
+__device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned* p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+__device__ __forceinline__ void merge_if_last(const TcArgs& a, const Item& it, int t, int bar_id,
+                                              volatile int* s_last) {
+  named_barrier(bar_id, 128);  // every writer's partial stores are issued
+  if (t == 0) *s_last = atom_add_acq_rel_gpu(a.counters + it.pair, 1u) == static_cast<unsigned>(a.splits - 1);
+  named_barrier(bar_id, 128);
+  const bool last = *s_last != 0;
+  named_barrier(bar_id, 128);  // s_last may be rewritten by the next item
+  if (!last) return;
+  const int g = a.group, S = a.splits;
+  const int c0 = (t & 15) * 8;
+  for (int h0 = 0; h0 < g; h0 += 8) {
+    const int h = h0 + (t >> 4);
+    if (h >= g) continue;
+    const int64_t orow = static_cast<int64_t>(it.b) * a.hq + static_cast<int64_t>(it.kvh) * g + h;
+    const int64_t r0 = orow * S;
+    float M = -INFINITY;
+#pragma unroll 4
+    for (int s = 0; s < S; ++s) M = fmaxf(M, __ldcg(a.ws_lse + r0 + s));
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+    float lse = -INFINITY;
+    if (M != -INFINITY) {
+      float tot = 0.0f;
+#pragma unroll 2
+      for (int s = 0; s < S; ++s) {
+        const float w = expf(__ldcg(a.ws_lse + r0 + s) - M);
+        const float4* src = reinterpret_cast<const float4*>(a.ws_o + (r0 + s) * kD + c0);
+        const float4 x0 = __ldcg(src), x1 = __ldcg(src + 1);
+        const float x[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+        tot += w;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = w > 0.0f ? fmaf(w, x[i], acc[i]) : acc[i];
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = acc[i] / tot;
+      lse = M + logf(tot);
+    }
+    if (a.out_f32) {
+      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + orow * kD + c0);
+      dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    } else {
+      uint32_t w4[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const __nv_bfloat162 v = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+        w4[i] = *reinterpret_cast<const uint32_t*>(&v);
+      }
+      *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + orow * kD + c0) =
+          make_uint4(w4[0], w4[1], w4[2], w4[3]);
+    }
+    if (a.lse_out && (t & 15) == 0) a.lse_out[orow] = lse;
+  }
+  if (t == 0) a.counters[it.pair] = 0u;
 }
 
 // First item at or after `item` (stepping by the grid) that has chunks; a.items if none.
@@ -276,6 +354,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   const uint32_t q_full = bar0 + 8 * (2 * kStages + 10);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Ly::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Ly::kOffMisc + 4);
+  volatile int* s_last = reinterpret_cast<volatile int*>(smem + Ly::kOffMisc + 8);  // last split of an item
   auto k_half = [&](int s, int h) { return sbase + s * kStageBytes + h * kHalfBytes; };
   auto v_half = [&](int s, int h) { return sbase + s * kStageBytes + kTileBytes + h * kHalfBytes; };
   auto q_half = [&](int h) { return sbase + Ly::kOffQ + h * kQHalfBytes; };
@@ -371,7 +450,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 #pragma unroll
             for (int k = 0; k < kChunk / 16; ++k) {
               const uint32_t voff = st * kStageBytes + k * 2048;
-              const uint32_t poff = bb * Ly::kPBytes + k * 2 * kPLbo;
+              const uint32_t poff = (c % Ly::kPBufs) * Ly::kPBytes + k * 2 * kPLbo;
               mma_f16(tmem + Ly::kColO + bb * 2 * NH, vdesc + (voff >> 4), pdesc + (poff >> 4), idesc2,
                       k > 0 ? 1u : 0u);
             }
@@ -499,6 +578,10 @@ __global__ void __launch_bounds__(kThreadsB, 1)
             p[h] = x[h] == -INFINITY ? 0.0f : exp2f(x[h] - mn);
             lsum[h] = fmaf(lsum[h], alpha[h], p[h]);
           }
+          // with one P buffer per group, the P.V product of this group's
+          // previous chunk reads it: that product must be complete (and its O
+          // taken) before P is rewritten
+          if (Ly::kPBufs == 2 && last_own >= 0 && !take_o(last_own)) { ok = false; break; }
           // probabilities, split into bf16 high part + bf16 remainder
           uint32_t hi2[NH / 2], lo2[NH / 2];
 #pragma unroll
@@ -511,7 +594,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
           }
           {
             constexpr int kPLbo = 8 * 2 * NH * 2;
-            uint8_t* prow = smem + Ly::kOffP + grp * Ly::kPBytes + (t >> 3) * kPLbo + (t & 7) * 16;
+            uint8_t* prow = smem + Ly::kOffP + (cc % Ly::kPBufs) * Ly::kPBytes + (t >> 3) * kPLbo + (t & 7) * 16;
 #pragma unroll
             for (int gi = 0; gi < NH / 8; ++gi) {
               *reinterpret_cast<uint4*>(prow + gi * 128) =
@@ -534,7 +617,9 @@ __global__ void __launch_bounds__(kThreadsB, 1)
           }
           fence_async_smem();
           mbar_arrive(p_full(grp));
-          if (last_own >= 0 && !take_o(last_own)) { ok = false; break; }
+          // two P buffers per group: the product two own chunks back is done
+          // before its buffer is written again (next own chunk)
+          if (Ly::kPBufs == 4 && last_own >= 0 && !take_o(last_own)) { ok = false; break; }
 #pragma unroll
           for (int h = 0; h < NH; ++h) alpha_prev[h] = alpha[h];
           last_own = cc;
@@ -576,10 +661,12 @@ __global__ void __launch_bounds__(kThreadsB, 1)
             put_partial(a, row0, h, t, lt > 0.0f ? ot / lt : 0.0f,
                         lt > 0.0f ? (mx + log2f(lt)) * kLn2 : -INFINITY);
           }
+          if (a.splits > 1 && a.counters) merge_if_last(a, it, t, bar, s_last);
         }
         named_barrier(3, 256);  // the exchange buffer is free again
       } else if (grp == 0) {
         for (int h = 0; h < g; ++h) put_partial(a, row0, h, t, 0.0f, -INFINITY);
+        if (a.splits > 1 && a.counters) merge_if_last(a, it, t, bar, s_last);
       }
       item = next;
       it = nit;
@@ -682,6 +769,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t kconv_full = bar0 + 8 * (2 * kStages8 + 11);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Ly::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Ly::kOffMisc + 4);
+  volatile int* s_last = reinterpret_cast<volatile int*>(smem + Ly::kOffMisc + 8);  // last split of an item
   float* red = reinterpret_cast<float*>(smem + Ly::kOffRed);
   auto kc_stage = [&](int s) { return smem + s * kStage8Bytes; };
   auto vc_stage = [&](int s) { return smem + s * kStage8Bytes + kCodeBytes; };
@@ -826,6 +914,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t row0 = (static_cast<int64_t>(it.b) * a.hq + it.kvh * g) * a.splits + it.split;
       if (it.nch == 0) {
         for (int h = 0; h < g; ++h) put_partial(a, row0, h, t, 0.0f, -INFINITY);
+        if (a.splits > 1 && a.counters) merge_if_last(a, it, t, 1, s_last);
         item = next;
         it = nit;
 #pragma unroll
@@ -957,6 +1046,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         put_partial(a, row0, h, t, lt > 0.0f ? oacc[h] / lt : 0.0f,
                     lt > 0.0f ? (m[h] + log2f(lt)) * kLn2 : -INFINITY);
       }
+      if (a.splits > 1 && a.counters) merge_if_last(a, it, t, 1, s_last);
       named_barrier(1, 128);
       item = next;
       it = nit;
@@ -1032,6 +1122,7 @@ TcArgs make_args(const KvView& kv, const AttnArgs& aa) {
   a.ws_lse = aa.ws_lse;
   a.out = aa.out;
   a.lse_out = aa.lse;
+  a.counters = aa.counters;
   a.out_f32 = aa.out_is_fp32;
   a.num_pages = kv.num_pages;
   a.hkv = kv.hkv;
@@ -1059,9 +1150,11 @@ cudaError_t launch_fp8(const KvView& kv, AttnArgs& aa, unsigned* err, cudaStream
   cudaError_t e = cudaFuncSetAttribute(attn_tc_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        Layout8::kAlloc);
   if (e != cudaSuccess) return e;
-  aa.merged = aa.splits == 1;
   const int grid = a.items < aa.sms ? a.items : aa.sms;
-  return launch_pdl(attn_tc_fp8_kernel, dim3(grid), dim3(kThreads), Layout8::kAlloc, st, mk, mv, a, err);
+  TcArgs b = a;
+  if (a.items > grid) b.counters = nullptr;  // CTAs with several items: the merge kernel is cheaper
+  aa.merged = aa.splits == 1 || b.counters != nullptr;
+  return launch_pdl(attn_tc_fp8_kernel, dim3(grid), dim3(kThreads), Layout8::kAlloc, st, mk, mv, b, err);
 }
 
 template <int NH>
@@ -1077,9 +1170,11 @@ cudaError_t launch_nh(const KvView& kv, AttnArgs& aa, unsigned* err, cudaStream_
   auto kern = attn_tc_kernel<NH>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::kAlloc);
   if (e != cudaSuccess) return e;
-  aa.merged = aa.splits == 1;
   const int grid = a.items < aa.sms ? a.items : aa.sms;
-  return launch_pdl(kern, dim3(grid), dim3(kThreadsB), Ly::kAlloc, st, mk, mv, a, err);
+  TcArgs b = a;
+  if (a.items > grid) b.counters = nullptr;  // CTAs with several items: the merge kernel is cheaper
+  aa.merged = aa.splits == 1 || b.counters != nullptr;
+  return launch_pdl(kern, dim3(grid), dim3(kThreadsB), Ly::kAlloc, st, mk, mv, b, err);
 }
 
 }  // namespace

@@ -19,7 +19,8 @@ _Q_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16, "fp8": torch.bfloat16}
 class SparseDecode:
     def __init__(self, *, num_q_heads, num_kv_heads, head_dim, block_size, kv_dtype, batch,
                  max_blocks, sink_tokens, window_tokens, k_scored, capacity=None, scale=None,
-                 out_is_fp32=False, algo="auto", blocks_per_split=0, score_smoothing=0.0, device="cuda"):
+                 out_is_fp32=False, algo="auto", blocks_per_split=0, score_smoothing=0.0,
+                 inline_merge=True, device="cuda"):
         self.kv_dtype = kv_dtype
         self.shape = hs.attn_shape(num_q_heads, num_kv_heads, head_dim, block_size, kv_dtype)
         self.batch, self.max_blocks = int(batch), int(max_blocks)
@@ -33,8 +34,11 @@ class SparseDecode:
                               if score_smoothing > 0 else None)
         self.sel_params = hs.select_params(sink_tokens, window_tokens, k_scored, self.capacity, score_smoothing,
                                            self.score_history)
+        # split arrival counters: the tensor-core attention merges its splits itself
+        self.split_counters = (torch.zeros(batch * num_kv_heads, dtype=torch.int32, device=dev)
+                               if inline_merge else None)
         self.attn_params = hs.attn_params(scale if scale is not None else 1.0 / math.sqrt(head_dim),
-                                          out_is_fp32, blocks_per_split, algo)
+                                          out_is_fp32, blocks_per_split, algo, split_counters=self.split_counters)
         sdt = _SUMMARY_DTYPE[kv_dtype]
         self.smin = torch.empty((batch, num_kv_heads, max_blocks, head_dim), dtype=sdt, device=dev)
         self.smax = torch.empty_like(self.smin)

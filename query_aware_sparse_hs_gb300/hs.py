@@ -50,7 +50,7 @@ class SelectParams(ctypes.Structure):
 
 class AttnParams(ctypes.Structure):
     _fields_ = [("scale", c_float), ("out_is_fp32", c_int32), ("blocks_per_split", c_int32),
-                ("algo", c_int32), ("max_ctas", c_int32)]
+                ("algo", c_int32), ("max_ctas", c_int32), ("split_counters", c_void_p)]
 
 
 class HotBuffer(ctypes.Structure):
@@ -170,9 +170,12 @@ def select_params(sink_tokens, window_tokens, k_scored, capacity, history_weight
     return p
 
 
-def attn_params(scale, out_is_fp32=False, blocks_per_split=0, algo="auto", max_ctas=0) -> AttnParams:
-    return AttnParams(float(scale), 1 if out_is_fp32 else 0, int(blocks_per_split),
-                      ALGO[algo] if isinstance(algo, str) else int(algo), int(max_ctas))
+def attn_params(scale, out_is_fp32=False, blocks_per_split=0, algo="auto", max_ctas=0,
+                split_counters=None) -> AttnParams:
+    p = AttnParams(float(scale), 1 if out_is_fp32 else 0, int(blocks_per_split),
+                   ALGO[algo] if isinstance(algo, str) else int(algo), int(max_ctas), _ptr(split_counters))
+    p._keep = split_counters
+    return p
 
 
 def hs_workspace_bytes(shape: AttnShape, batch: int, capacity: int, params: AttnParams) -> int:

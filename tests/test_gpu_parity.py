@@ -263,3 +263,23 @@ def test_quantize_bit_exact():
             rc, rs = O.quantize_e4m3_g32(xs)
             assert np.array_equal(scales.cpu().numpy(), rs)
             assert np.array_equal(codes.cpu().numpy(), rc)
+
+
+@pytest.mark.parametrize("name", ["llama_bf16_tail", "ragged_bf16", "fp8_tail"])
+def test_inline_split_merge_matches_the_merge_kernel(cases, name):
+    """With split counters, and one work item per CTA (the automatic split
+    gives 80-104 items here), the tensor-core kernel merges its splits itself;
+    the result equals the separate merge kernel's (same partials, same
+    arithmetic) and every counter is back to zero after each call."""
+    c = cases[name]
+    outs = []
+    for inline in (True, False):
+        dec = c.decoder(out_is_fp32=True, inline_merge=inline)
+        dec.build_summaries(c.kv)
+        for _ in range(2):
+            dec.step(c.kv, c.q)
+            _err_clear()
+            if inline:
+                assert bool((dec.split_counters == 0).all())
+        outs.append((dec.out.clone(), dec.lse.clone()))
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
