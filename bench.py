@@ -249,6 +249,37 @@ def cpu_baseline(w, seconds: float = 12.0) -> dict:
                       f"numpy float64, 1 thread, {dt:.1f} s"}
 
 
+def _oracle_worker(args):
+    """One host process of the all-cores baseline: the oracle's per-pair step,
+    repeated for `seconds`.  Returns (query heads served, seconds)."""
+    name, seconds, seed = args
+    from synth import WORKLOADS
+    st = OracleStep(WORKLOADS[name])
+    st.i = seed
+    st.step()
+    t0 = time.perf_counter()
+    heads = 0
+    while time.perf_counter() - t0 < seconds:
+        heads += st.step()
+    return heads, time.perf_counter() - t0
+
+
+def cpu_baseline_all_cores(w, seconds: float = 12.0) -> dict:
+    """The same oracle step on every host core: one process per core, each on
+    its own (request, kv head) pairs (the pairs are independent).  Processes are
+    started with 'spawn', so no CUDA state is inherited."""
+    import multiprocessing as mp
+    cores = os.cpu_count() or 1
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(cores) as pool:
+        res = pool.map(_oracle_worker, [(w.name, seconds, i) for i in range(cores)])
+    heads = sum(r[0] for r in res)
+    dt = max(r[1] for r in res)
+    return {"value": heads / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{cores} processes x {seconds:.0f} s of single-(request, kv head) steps of {w.name} "
+                      f"(append + bound + selection + attention), numpy float64, 1 thread each"}
+
+
 def run_reference(args, w):
     rank, world, _ = dist_env()
     if rank != 0:
@@ -290,7 +321,7 @@ def workload_config(w, layers: int) -> dict:
 # DRAM bytes (read + written) of one attention launch from an ncu capture of the
 # current kernel (profiles/ncu_full_llama8b_bf16_1layer.md), per workload;
 # a workload without a capture of the current kernel reports null.
-NCU_TRAFFIC = {"llama8b_bf16": 33_759_232}
+NCU_TRAFFIC: dict = {}
 
 
 def run_ours(args, w):
@@ -490,6 +521,8 @@ def run_ours(args, w):
     if rank != 0:
         return
     cpu = cpu_baseline(w, seconds=args.cpu_seconds) if (world == 1 and args.cpu_seconds > 0) else None
+    cpu_all = (cpu_baseline_all_cores(w, seconds=args.cpu_seconds / 2)
+               if (world == 1 and args.cpu_seconds > 0) else None)
     # layers that reuse a selection skip its two (or one) launches
     sel_launches = 2 if (w.kv_dtype != "f32" and w.head_dim == 128) else 1
     launches_per_step = step_launches(w, d0) - sel_launches * (1 - 1 / args.select_every)
@@ -510,6 +543,7 @@ def run_ours(args, w):
                         "summary_build_full": full_sum_bytes / (t_sum_full * 1e-6) / 1e9},
         "bytes_per_step": {"attention": a_bytes, "score_select": s_bytes, "append": int(append_bytes)},
         "cpu_baseline": cpu,
+        "cpu_baseline_all_cores": cpu_all,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": ms_e2e / steps},
         "gpu_launches": int(round(launches_per_step * steps)),
