@@ -89,7 +89,12 @@ def step_launches(w, dec, hot: bool = False, overlap: bool = False) -> int:
     tc = w.kv_dtype in ("bf16", "fp8") and w.head_dim == 128 and w.block_size in (16, 32, 64, 128)
     per_split = w.batch * w.num_q_heads * (w.head_dim + 1) * 4
     splits = dec.workspace.numel() // per_split
-    return n + (0 if tc and splits <= 1 else 1)
+    # the tensor-core kernel merges its splits itself when it has split
+    # counters and every work item a CTA of its own
+    import torch
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    inline = tc and dec.split_counters is not None and w.batch * w.num_kv_heads * splits <= sms
+    return n + (0 if (tc and splits <= 1) or inline else 1)
 
 
 def select_bytes(w, total_blocks: int) -> int:
@@ -321,7 +326,7 @@ def workload_config(w, layers: int) -> dict:
 # DRAM bytes (read + written) of one attention launch from an ncu capture of the
 # current kernel (profiles/ncu_full_llama8b_bf16_1layer.md), per workload;
 # a workload without a capture of the current kernel reports null.
-NCU_TRAFFIC: dict = {}
+NCU_TRAFFIC = {"llama8b_bf16": 33_775_872}
 
 
 def run_ours(args, w):
