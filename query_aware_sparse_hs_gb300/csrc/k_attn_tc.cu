@@ -35,10 +35,13 @@ using namespace tc;
 constexpr int kD = 128;
 constexpr int kChunk = 128;
 constexpr int kStages = 3;
-constexpr int kThreads = 224;
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;   // S = K.Q^T issuer (and TMEM owner)
-constexpr int kMma2Warp = 6;  // O = V^T.P issuer
+// e4m3 kernel roles: warps 0-3 softmax, 4-7 code conversion, 8 TMA producer,
+// 9 S' = K.Q'^T issuer (and TMEM owner), 10 O' = V^T.P' issuer
+constexpr int kThreads = 352;
+constexpr int kConvWarp0 = 4;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kMma2Warp = 10;
 constexpr int kHalfBytes = kChunk * 128;   // 128 rows x 64 bf16
 constexpr int kTileBytes = 2 * kHalfBytes;  // one K or V chunk
 constexpr int kStageBytes = 2 * kTileBytes;
@@ -712,7 +715,7 @@ struct Layout8 {
   static constexpr int kPBytes = kChunk * 64 * 2;           // 128 tokens x 64 columns bf16
   static constexpr int kOffP = kOffQ + 2 * kQHalf;
   static constexpr int kOffBar = kOffP + 2 * kPBytes;
-  static constexpr int kNumBars = 2 * kStages8 + 12;
+  static constexpr int kNumBars = 2 * kStages8 + 13;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kOffRed = kOffMisc + 16;
   static constexpr int kOffMeta = kOffRed + 3 * 4 * 8 * 4;
@@ -767,6 +770,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto o_free = [&](int b) { return bar0 + 8 * (2 * kStages8 + 8 + b); };
   const uint32_t q_full = bar0 + 8 * (2 * kStages8 + 10);
   const uint32_t kconv_full = bar0 + 8 * (2 * kStages8 + 11);
+  const uint32_t vconv_full = bar0 + 8 * (2 * kStages8 + 12);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Ly::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Ly::kOffMisc + 4);
   volatile int* s_last = reinterpret_cast<volatile int*>(smem + Ly::kOffMisc + 8);  // last split of an item
@@ -784,7 +788,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < kStages8; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 128);  // released by the converting warps
+      mbar_init(empty_bar(s), 256);  // released by the converting and the softmax warps
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(s_full(b), 1);
@@ -795,6 +799,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(q_full, 128);
     mbar_init(kconv_full, 128);
+    mbar_init(vconv_full, 128);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -855,7 +860,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             mma_commit(s_full(bb));
           } else {
-            ok = mbar_wait(p_full(bb), (c >> 1) & 1, abort_flag) &&
+            ok = mbar_wait(p_full(bb), (c >> 1) & 1, abort_flag) && mbar_wait(vconv_full, c & 1, abort_flag) &&
                  (c < 2 || mbar_wait(o_free(bb), ((c >> 1) + 1) & 1, abort_flag));
             if (!ok) break;
             tc_fence_after();
@@ -874,6 +879,45 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!first && last_g2 >= 0) mbar_wait(o_full(last_g2 & 1), (last_g2 >> 1) & 1, abort_flag, 500000000ull);
     }
+  } else if (warp >= kConvWarp0 && warp < kConvWarp0 + 4) {
+    // ================= code conversion: e4m3 rows -> bf16 operand tiles =================
+    // iteration c converts K of chunk c (once the S' product of chunk c-1 is
+    // done with the K tile), then V of chunk c-1 (once the P'.V product of
+    // chunk c-2 is done with the V tile), and releases chunk c-1's stage
+    const int ct = tid - kConvWarp0 * 32;  // row of the chunk
+    auto valid_row = [&](int cc) -> bool {
+      const int2 md = meta[(cc % kStages8) * 8 + ct / B];
+      return md.x >= 0 && (ct % B) < md.y;
+    };
+    auto convert_v = [&](int cc) -> bool {
+      if (cc >= 1 && !mbar_wait(o_full((cc - 1) & 1), ((cc - 1) >> 1) & 1, abort_flag)) return false;
+      convert_row(vc_stage(cc % kStages8) + ct * 128, smem + Ly::kOffVbf, ct, valid_row(cc));
+      fence_async_smem();
+      mbar_arrive(vconv_full);
+      mbar_arrive(empty_bar(cc % kStages8));
+      return true;
+    };
+    int c = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; ok && item < a.items && !*abort_flag; item += gridDim.x) {
+      const Item it = item_geom(a, item, bpc);
+      for (int ci = 0; ci < it.nch; ++ci, ++c) {
+        const int s = c % kStages8;
+        if (!mbar_wait(full_bar(s), (c / kStages8) & 1, abort_flag) ||
+            (c >= 1 && !mbar_wait(s_full((c - 1) & 1), ((c - 1) >> 1) & 1, abort_flag))) {
+          ok = false;
+          break;
+        }
+        convert_row(kc_stage(s) + ct * 128, smem + Ly::kOffKbf, ct, valid_row(c));
+        fence_async_smem();
+        mbar_arrive(kconv_full);
+        if (c >= 1 && !convert_v(c - 1)) {
+          ok = false;
+          break;
+        }
+      }
+    }
+    if (ok && c >= 1) convert_v(c - 1);
   } else {
     const int t = tid;
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
@@ -930,23 +974,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_async_smem();
       mbar_arrive(q_full);
 
-      // row t of a chunk: token t % B of its (t / B)-th block
-      float ks_cur[4], ks_next[4] = {0.f, 0.f, 0.f, 0.f};
-      bool valid_cur = false, valid_next = false;
       bool ok = true;
-      auto convert_k = [&](int cc) -> bool {
-        const int s = cc % kStages8;
-        if (!mbar_wait(full_bar(s), (cc / kStages8) & 1, abort_flag)) return false;
-        const int bi = t / B, tok = t - bi * B;
-        const int2 md = meta[s * 8 + bi];
-        valid_next = md.x >= 0 && tok < md.y;
-        convert_row(kc_stage(s) + t * 128, smem + Ly::kOffKbf, t, valid_next);
-        const float4 sc = valid_next ? *reinterpret_cast<const float4*>(ks_stage(s) + t * 16) : make_float4(0, 0, 0, 0);
-        ks_next[0] = sc.x; ks_next[1] = sc.y; ks_next[2] = sc.z; ks_next[3] = sc.w;
-        fence_async_smem();
-        mbar_arrive(kconv_full);
-        return true;
-      };
       float m[NH], lsum[NH], oacc[NH], alpha_prev[NH];
 #pragma unroll
       for (int h = 0; h < NH; ++h) {
@@ -967,12 +995,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int h = 0; h < NH; ++h) oacc[h] = fmaf(oacc[h], alpha_prev[h], ov[h] + ov[NH + h]);
         return true;
       };
-      if (!convert_k(c)) break;
       for (int ci = 0; ci < it.nch && ok; ++ci, ++c) {
         const int bb = c & 1, s = c % kStages8;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) ks_cur[i] = ks_next[i];
-        valid_cur = valid_next;
+        // row t of the chunk: token t % B of its (t / B)-th block; its K and V
+        // scales come from this chunk's stage
+        if (!mbar_wait(full_bar(s), (c / kStages8) & 1, abort_flag)) { ok = false; break; }
+        const int2 md = meta[s * 8 + t / B];
+        const bool valid_cur = md.x >= 0 && (t % B) < md.y;
+        float ks_cur[4] = {0.f, 0.f, 0.f, 0.f};
+        if (valid_cur) {
+          const float4 sc = *reinterpret_cast<const float4*>(ks_stage(s) + t * 16);
+          ks_cur[0] = sc.x; ks_cur[1] = sc.y; ks_cur[2] = sc.z; ks_cur[3] = sc.w;
+        }
         if (!mbar_wait(s_full(bb), (c >> 1) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
         float sv[32];
@@ -980,7 +1014,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld16(tmem + lane_base + bb * 32 + 16, *reinterpret_cast<float(*)[16]>(sv + 16));
         tc_fence_before();
         mbar_arrive(s_free(bb));
-        if (ci + 1 < it.nch && !convert_k(c + 1)) { ok = false; break; }
         float x[NH];
 #pragma unroll
         for (int h = 0; h < NH; ++h) {
@@ -1005,10 +1038,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           lsum[h] = fmaf(lsum[h], alpha[h], p[h]);
         }
         if (ci > 0 && !take_o(c - 1)) { ok = false; break; }
-        // V tile of this chunk (GEMM2 of the previous chunk is done with it)
-        convert_row(vc_stage(s) + t * 128, smem + Ly::kOffVbf, t, valid_cur);
         const float4 vsc = valid_cur ? *reinterpret_cast<const float4*>(vs_stage(s) + t * 16) : make_float4(0, 0, 0, 0);
-        mbar_arrive(empty_bar(s));  // codes and scales of this stage are all consumed
         const float vs[4] = {vsc.x, vsc.y, vsc.z, vsc.w};
         uint8_t* prow = smem + Ly::kOffP + bb * Ly::kPBytes + (t >> 3) * 1024 + (t & 7) * 16;
 #pragma unroll
@@ -1028,6 +1058,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         fence_async_smem();
         mbar_arrive(p_full(bb));
+        mbar_arrive(empty_bar(s));  // this group is done with the stage's meta and scales
 #pragma unroll
         for (int h = 0; h < NH; ++h) alpha_prev[h] = alpha[h];
       }
