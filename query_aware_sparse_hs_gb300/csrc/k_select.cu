@@ -27,8 +27,11 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 
-// Exclusive prefix sum over the CTA; `total` receives the CTA-wide sum.
+// Exclusive prefix sum over a CTA of THREADS threads (at most 1024); `total`
+// receives the CTA-wide sum.  s_warp holds THREADS / 32 + 1 ints.
+template <int THREADS = kThreads>
 __device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int& total) {
+  constexpr int kWarps = THREADS / 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int incl = v;
 #pragma unroll
@@ -104,6 +107,7 @@ __device__ __forceinline__ void smooth_scores(float* s_scores, int nb, int max_b
 // key among the other blocks (two histogram buffers, which must be zero on
 // entry), then one packed scan that places forced-or-above-threshold blocks and
 // the lowest-index threshold-equal blocks in ascending order.
+template <int THREADS = kThreads>
 __device__ __forceinline__ void select_pair(const float* s_scores, int nb, int L, int B, const SelectArgs& a,
                                             int64_t pair, uint32_t (*s_hist)[256], int* s_warp, int* s_pick,
                                             unsigned* err) {
@@ -132,7 +136,7 @@ __device__ __forceinline__ void select_pair(const float* s_scores, int nb, int L
     int buf = 0;
     for (int shift = 24; shift >= 0; shift -= 8, buf ^= 1) {
       uint32_t* hist = s_hist[buf];
-      for (int j = tid; j < nb; j += kThreads) {
+      for (int j = tid; j < nb; j += THREADS) {
         if (forced(j)) continue;
         const uint32_t key = score_key(s_scores[j]);
         if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
@@ -178,7 +182,7 @@ __device__ __forceinline__ void select_pair(const float* s_scores, int nb, int L
   }
 
   if (take_all) {
-    for (int j = tid; j < cap; j += kThreads) out[j] = j < nb ? j : -1;
+    for (int j = tid; j < cap; j += THREADS) out[j] = j < nb ? j : -1;
     if (tid == 0) {
       if (nb > cap) set_error(err, HS_EBIT_CAPACITY);
       a.sel_count[pair] = min(nb, cap);
@@ -189,7 +193,7 @@ __device__ __forceinline__ void select_pair(const float* s_scores, int nb, int L
   // scan gives, for every block, how many forced-or-above-threshold blocks and
   // how many threshold-equal blocks precede it; an equal block is chosen while
   // fewer than need_eq equal blocks precede it (lower index first).
-  const int per_t = ceil_div(nb, kThreads);
+  const int per_t = ceil_div(nb, THREADS);
   const int j0 = min(nb, tid * per_t), j1 = min(nb, j0 + per_t);
   int gt_local = 0, eq_local = 0;
   for (int j = j0; j < j1; ++j) {
@@ -202,7 +206,7 @@ __device__ __forceinline__ void select_pair(const float* s_scores, int nb, int L
     }
   }
   int packed_total;
-  const int packed = block_exclusive_scan((gt_local << 16) | eq_local, s_warp, packed_total);
+  const int packed = block_exclusive_scan<THREADS>((gt_local << 16) | eq_local, s_warp, packed_total);
   int gt_b = packed >> 16, eq_b = packed & 0xffff;
   const int total = (packed_total >> 16) + min(packed_total & 0xffff, need_eq);
   for (int j = j0; j < j1; ++j) {
@@ -219,7 +223,7 @@ __device__ __forceinline__ void select_pair(const float* s_scores, int nb, int L
     gt_b += is_gt ? 1 : 0;
     eq_b += is_eq ? 1 : 0;
   }
-  for (int i = total + tid; i < cap; i += kThreads) out[i] = -1;
+  for (int i = total + tid; i < cap; i += THREADS) out[i] = -1;
   if (tid == 0) {
     if (total > cap) set_error(err, HS_EBIT_CAPACITY);
     a.sel_count[pair] = min(total, cap);
@@ -343,8 +347,10 @@ __global__ void __cluster_dims__(kSelectCluster, 1, 1) __launch_bounds__(kThread
 
 // One CTA per (request, kv head): scores already in global memory (written by
 // the tensor-core scorer) -> selection.
-__global__ __launch_bounds__(kThreads) void select_only_kernel(KvView kv, SelectArgs a, const float* scores,
-                                                               unsigned* err) {
+template <int THREADS>
+__global__ __launch_bounds__(THREADS) void select_only_kernel(KvView kv, SelectArgs a, const float* scores,
+                                                              unsigned* err) {
+  constexpr int kWarps = THREADS / 32;
   extern __shared__ float s_scores[];
   __shared__ uint32_t s_hist[2][256];
   __shared__ int s_warp[kWarps + 1];
@@ -362,11 +368,11 @@ __global__ __launch_bounds__(kThreads) void select_only_kernel(KvView kv, Select
     nb = kv.max_blocks;
   }
   const float* src = scores + pair * kv.max_blocks;
-  for (int j = tid; j < nb; j += kThreads) s_scores[j] = src[j];
-  for (int i = tid; i < 512; i += kThreads) s_hist[i >> 8][i & 255] = 0u;
+  for (int j = tid; j < nb; j += THREADS) s_scores[j] = src[j];
+  for (int i = tid; i < 512; i += THREADS) s_hist[i >> 8][i & 255] = 0u;
   __syncthreads();
   smooth_scores(s_scores, nb, kv.max_blocks, a, pair);
-  select_pair(s_scores, nb, L, B, a, pair, s_hist, s_warp, s_pick, err);
+  select_pair<THREADS>(s_scores, nb, L, B, a, pair, s_hist, s_warp, s_pick, err);
 }
 
 template <int C, int G, bool F32>
@@ -400,12 +406,15 @@ cudaError_t launch_select_only(const KvView& kv, const SelectArgs& a, const floa
   const int pairs = kv.batch * kv.hkv;
   if (pairs == 0) return cudaSuccess;
   const size_t smem = static_cast<size_t>(kv.max_blocks) * sizeof(float);
+  // long requests: four times the threads, so each radix pass touches a
+  // quarter of the keys per thread
+  auto kern = kv.max_blocks > 2048 ? select_only_kernel<1024> : select_only_kernel<kThreads>;
+  const int threads = kv.max_blocks > 2048 ? 1024 : kThreads;
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(select_only_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
-  return launch_pdl(select_only_kernel, dim3(pairs), dim3(kThreads), smem, st, kv, a, scores, err);
+  return launch_pdl(kern, dim3(pairs), dim3(threads), smem, st, kv, a, scores, err);
 }
 
 cudaError_t launch_score_select(const KvView& kv, const SelectArgs& a, unsigned* err,
