@@ -408,8 +408,8 @@ cudaError_t launch_select_only(const KvView& kv, const SelectArgs& a, const floa
   const size_t smem = static_cast<size_t>(kv.max_blocks) * sizeof(float);
   // long requests: four times the threads, so each radix pass touches a
   // quarter of the keys per thread
-  auto kern = kv.max_blocks > 2048 ? select_only_kernel<1024> : select_only_kernel<kThreads>;
-  const int threads = kv.max_blocks > 2048 ? 1024 : kThreads;
+  auto kern = kv.max_blocks > 1024 ? select_only_kernel<1024> : select_only_kernel<kThreads>;
+  const int threads = kv.max_blocks > 1024 ? 1024 : kThreads;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;

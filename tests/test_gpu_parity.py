@@ -17,7 +17,7 @@ CASES = {
     "llama_bf16_tail": WORKLOADS["llama8b_bf16"].scaled(batch=2, ctx_min=4133, ctx_max=4133, k_scored=20),
     "ragged_bf16": WORKLOADS["ragged_bf16"].scaled(batch=5, ctx_min=300, ctx_max=5000, k_scored=40),
     "fp8_tail": WORKLOADS["fp8_g32"].scaled(batch=2, ctx_min=4133, ctx_max=4133, k_scored=20),
-    # more than 2048 blocks per request: the selection runs on 1024 threads
+    # more than 1024 blocks per request: the selection runs on 1024 threads
     "long_b16_bf16": WORKLOADS["ragged_bf16"].scaled(batch=2, ctx_min=33000, ctx_max=40000, k_scored=64),
     "d64_g16_bf16": WORKLOADS["llama8b_bf16"].scaled(batch=2, num_q_heads=32, num_kv_heads=2,
                                                      head_dim=64, block_size=32, ctx_min=1000,
