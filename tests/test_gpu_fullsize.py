@@ -109,10 +109,13 @@ def test_full_size_step(name, samples):
     _check_pairs(w, x, dec, samples, tol=2e-3)
 
 
-def test_full_size_offload_steps():
+@pytest.mark.parametrize("overlap", [False, True])
+def test_full_size_offload_steps(overlap):
     """256 requests x 32768 tokens with 64 hot slots per (request, kv head): the
     hot-buffer tables of sampled pairs follow the oracle's simulator exactly over
-    several drifting decode steps, and the attention on the hot slots matches."""
+    several drifting decode steps, and the attention on the hot slots matches -
+    with the swap-in in one call, and overlapped (page copy and attention over
+    the copied blocks on 24 SMs beside attention over the resident blocks)."""
     from query_aware_sparse_hs_gb300 import hs
     from query_aware_sparse_hs_gb300.decode import SparseDecode
     from _parity import tie_window_ok
@@ -141,6 +144,8 @@ def test_full_size_offload_steps():
     dec = SparseDecode(num_q_heads=w.num_q_heads, num_kv_heads=hkv, head_dim=D, block_size=B, kv_dtype="bf16",
                        batch=w.batch, max_blocks=nb, sink_tokens=w.sink_tokens, window_tokens=w.window_tokens,
                        k_scored=w.k_scored)
+    if overlap:
+        dec.enable_swap_overlap()
     dec.build_summaries(pool_kv)
     samples = [(0, 0), (100, 2), (255, 3)]
     L = w.ctx_max
