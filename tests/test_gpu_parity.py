@@ -285,3 +285,45 @@ def test_inline_split_merge_matches_the_merge_kernel(cases, name):
                 assert bool((dec.split_counters == 0).all())
         outs.append((dec.out.clone(), dec.lse.clone()))
     assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+
+
+def test_fp8_attention_over_every_code():
+    """K and V codes drawn uniformly from the 254 non-NaN e4m3 codes (zero and
+    subnormal codes included, alone and beside normal codes in the same 4-byte
+    word) with random group scales; the tensor-core e4m3 attention against the
+    oracle on the same codes, over the library's own selection."""
+    from query_aware_sparse_hs_gb300 import hs
+    from query_aware_sparse_hs_gb300.decode import SparseDecode
+    w = WORKLOADS["fp8_g32"].scaled(batch=2, ctx_min=4096, ctx_max=4096, k_scored=20)
+    x = make_inputs(w)
+    B, D, hkv, g = w.block_size, w.head_dim, w.num_kv_heads, w.group
+    P = x["k_pages"].shape[0]
+    gen = torch.Generator().manual_seed(11)
+    allowed = torch.tensor([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=torch.uint8)
+    pages, scales = {}, {}
+    for n in ("k", "v"):
+        pages[n] = allowed[torch.randint(len(allowed), (P, B, D), generator=gen)]
+        scales[n] = torch.rand((P, B, D // 32), generator=gen) * 0.009 + 0.001
+    dev = torch.device("cuda")
+    kv = hs.paged_kv(pages["k"].to(dev), pages["v"].to(dev), x["page_table"].to(dev), x["seq_lens"].to(dev),
+                     scales["k"].to(dev), scales["v"].to(dev))
+    q = x["q"].to(dev)
+    dec = SparseDecode(num_q_heads=w.num_q_heads, num_kv_heads=hkv, head_dim=D, block_size=B, kv_dtype="fp8",
+                       batch=w.batch, max_blocks=w.max_blocks, sink_tokens=w.sink_tokens,
+                       window_tokens=w.window_tokens, k_scored=w.k_scored, out_is_fp32=True, algo="tcgen05")
+    dec.build_summaries(kv)
+    dec.step(kv, q)
+    _err_clear()
+    sel, cnt, out = dec.sel.cpu().numpy(), dec.sel_count.cpu().numpy(), dec.out.cpu().numpy()
+    table = x["page_table"].numpy()
+    for b in range(w.batch):
+        L = int(x["seq_lens"][b])
+        for kvh in range(hkv):
+            row = table[b, kvh]
+            K = O.kv_values("fp8", O.gather_rows(pages["k"].numpy(), row, L, B),
+                            O.gather_rows(scales["k"].numpy(), row, L, B))
+            V = O.kv_values("fp8", O.gather_rows(pages["v"].numpy(), row, L, B),
+                            O.gather_rows(scales["v"].numpy(), row, L, B))
+            qg = x["q"][b, kvh * g:(kvh + 1) * g].float().numpy().astype(np.float64)
+            ref, _ = O.sparse_attention(qg, K, V, sel[b, kvh, :cnt[b, kvh]].tolist(), B, 1 / math.sqrt(D))
+            assert np.abs(out[b, kvh * g:(kvh + 1) * g] - ref).max() <= 2e-3, (b, kvh)
