@@ -35,13 +35,15 @@ using namespace tc;
 constexpr int kD = 128;
 constexpr int kChunk = 128;
 constexpr int kStages = 3;
-// e4m3 kernel roles: warps 0-3 softmax, 4-7 code conversion, 8 TMA producer,
-// 9 S' = K.Q'^T issuer (and TMEM owner), 10 O' = V^T.P' issuer
-constexpr int kThreads = 352;
+// e4m3 kernel roles: warps 0-3 softmax, 4-7 K code conversion, 8-11 V code
+// conversion, 12 TMA producer, 13 S' = K.Q'^T issuer (and TMEM owner),
+// 14 O' = V^T.P' issuer
+constexpr int kThreads = 480;
 constexpr int kConvWarp0 = 4;
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr int kMma2Warp = 10;
+constexpr int kConvVWarp0 = 8;
+constexpr int kProducerWarp = 12;
+constexpr int kMmaWarp = 13;
+constexpr int kMma2Warp = 14;
 constexpr int kHalfBytes = kChunk * 128;   // 128 rows x 64 bf16
 constexpr int kTileBytes = 2 * kHalfBytes;  // one K or V chunk
 constexpr int kStageBytes = 2 * kTileBytes;
@@ -788,7 +790,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < kStages8; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 256);  // released by the converting and the softmax warps
+      mbar_init(empty_bar(s), 384);  // released by both converting warpgroups and the softmax warps
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(s_full(b), 1);
@@ -879,45 +881,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!first && last_g2 >= 0) mbar_wait(o_full(last_g2 & 1), (last_g2 >> 1) & 1, abort_flag, 500000000ull);
     }
-  } else if (warp >= kConvWarp0 && warp < kConvWarp0 + 4) {
+  } else if (warp >= kConvWarp0 && warp < kConvVWarp0 + 4) {
     // ================= code conversion: e4m3 rows -> bf16 operand tiles =================
-    // iteration c converts K of chunk c (once the S' product of chunk c-1 is
-    // done with the K tile), then V of chunk c-1 (once the P'.V product of
-    // chunk c-2 is done with the V tile), and releases chunk c-1's stage
-    const int ct = tid - kConvWarp0 * 32;  // row of the chunk
-    auto valid_row = [&](int cc) -> bool {
-      const int2 md = meta[(cc % kStages8) * 8 + ct / B];
-      return md.x >= 0 && (ct % B) < md.y;
-    };
-    auto convert_v = [&](int cc) -> bool {
-      if (cc >= 1 && !mbar_wait(o_full((cc - 1) & 1), ((cc - 1) >> 1) & 1, abort_flag)) return false;
-      convert_row(vc_stage(cc % kStages8) + ct * 128, smem + Ly::kOffVbf, ct, valid_row(cc));
-      fence_async_smem();
-      mbar_arrive(vconv_full);
-      mbar_arrive(empty_bar(cc % kStages8));
-      return true;
-    };
+    // one warpgroup converts K of chunk c once the S' product of chunk c-1 is
+    // done with the K tile, the other V of chunk c once the P'.V product of
+    // chunk c-1 is done with the V tile; each then releases its part of the stage
+    const bool is_k = warp < kConvVWarp0;
+    const int ct = tid - (is_k ? kConvWarp0 : kConvVWarp0) * 32;  // row of the chunk
     int c = 0;
     bool ok = true;
     for (int item = blockIdx.x; ok && item < a.items && !*abort_flag; item += gridDim.x) {
       const Item it = item_geom(a, item, bpc);
       for (int ci = 0; ci < it.nch; ++ci, ++c) {
         const int s = c % kStages8;
-        if (!mbar_wait(full_bar(s), (c / kStages8) & 1, abort_flag) ||
-            (c >= 1 && !mbar_wait(s_full((c - 1) & 1), ((c - 1) >> 1) & 1, abort_flag))) {
+        const bool prev_done = c == 0 || (is_k ? mbar_wait(s_full((c - 1) & 1), ((c - 1) >> 1) & 1, abort_flag)
+                                               : mbar_wait(o_full((c - 1) & 1), ((c - 1) >> 1) & 1, abort_flag));
+        if (!mbar_wait(full_bar(s), (c / kStages8) & 1, abort_flag) || !prev_done) {
           ok = false;
           break;
         }
-        convert_row(kc_stage(s) + ct * 128, smem + Ly::kOffKbf, ct, valid_row(c));
+        const int2 md = meta[s * 8 + ct / B];
+        const bool valid = md.x >= 0 && (ct % B) < md.y;
+        convert_row((is_k ? kc_stage(s) : vc_stage(s)) + ct * 128, smem + (is_k ? Ly::kOffKbf : Ly::kOffVbf), ct,
+                    valid);
         fence_async_smem();
-        mbar_arrive(kconv_full);
-        if (c >= 1 && !convert_v(c - 1)) {
-          ok = false;
-          break;
-        }
+        mbar_arrive(is_k ? kconv_full : vconv_full);
+        mbar_arrive(empty_bar(s));
       }
     }
-    if (ok && c >= 1) convert_v(c - 1);
   } else {
     const int t = tid;
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
