@@ -97,3 +97,39 @@ def test_kv_bytes_per_token_of_an_8b_gqa_model():
     assert bench.kv_bytes_per_token(32, 4, 128, 2) == 65536
     assert bench.kv_bytes_per_token(32, 4, 128, 2) * 32768 == 2 * 1024 ** 3
     assert bench.kv_bytes_per_token(32, 4, 128, 2) * 131072 == 8 * 1024 ** 3
+
+
+
+def test_host_checks_of_the_overlap_and_merge_calls():
+    """The overlapped swap-in calls and the partial merge refuse missing or
+    aliased buffers before launching anything (no GPU needed)."""
+    from query_aware_sparse_hs_gb300 import hs
+    lib = hs.library()
+    shape = hs.attn_shape(32, 4, 128, 64, "bf16")
+    hb = hs.HotBuffer()
+    P = 0x1000
+    # plan: the hit and miss lists may not alias the selection or each other
+    assert lib.hs_swapin_plan(ctypes.byref(shape), ctypes.byref(hb), P, P, 32, 0, P, P, P + 64, P, None,
+                              None) == hs.HS_ERR_INVALID_ARG
+    assert lib.hs_swapin_plan(ctypes.byref(shape), ctypes.byref(hb), P, P, 32, 0, None, P, P + 64, P, None,
+                              None) == hs.HS_ERR_INVALID_ARG
+    # copy: a negative CTA count; copy+attend: missing query or outputs
+    assert lib.hs_swapin_copy(ctypes.byref(shape), ctypes.byref(hb), P, P, 32, -1, None,
+                              None) == hs.HS_ERR_INVALID_ARG
+    assert lib.hs_swapin_copy_attend(ctypes.byref(shape), ctypes.byref(hb), P, None, P, P, 32, 0.088, 0, P, P,
+                                     None, None) == hs.HS_ERR_INVALID_ARG
+    # an empty hot buffer description is refused
+    assert lib.hs_swapin_copy(ctypes.byref(shape), ctypes.byref(hb), P, P, 32, 0, None,
+                              None) == hs.HS_ERR_INVALID_ARG
+    # merge of partials: no parts, or a misaligned output
+    assert lib.hs_merge_attn_partials(ctypes.byref(shape), 2, 0, P, P, P, 1, None, None) == hs.HS_ERR_INVALID_ARG
+    assert lib.hs_merge_attn_partials(ctypes.byref(shape), 2, 2, P, P, P + 2, 1, None,
+                                      None) == hs.HS_ERR_INVALID_ARG
+    # attention: a negative CTA cap is refused
+    kv = hs.PagedKV()
+    kv.k_pages = kv.v_pages = kv.page_table = kv.seq_lens = P
+    kv.batch, kv.max_blocks, kv.num_pages = 1, 4, 4
+    params = hs.attn_params(0.088, max_ctas=-1)
+    st = lib.hs_sparse_paged_decode_attn(ctypes.byref(shape), ctypes.byref(kv), P, P, P, 8, ctypes.byref(params),
+                                         P, None, None, 0, None)
+    assert st == hs.HS_ERR_INVALID_ARG
