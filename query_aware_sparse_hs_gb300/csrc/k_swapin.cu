@@ -556,13 +556,9 @@ template <int C, int KIND>
 cudaError_t launch_attend(const HotView& hb, const int32_t* miss_sel, const int32_t* miss_count, int capacity,
                           const MissAttn& ma, unsigned* err, cudaStream_t st) {
   constexpr int kBytes = AttendSmem<C, KIND>::kBytes;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(copied_blocks_attn_kernel<C, KIND>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  cudaError_t e = cudaFuncSetAttribute(copied_blocks_attn_kernel<C, KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kBytes);
+  if (e != cudaSuccess) return e;
   return launch_pdl(copied_blocks_attn_kernel<C, KIND>, dim3(hb.batch * hb.hkv), dim3(kAttnThreads), kBytes, st, hb,
                     miss_sel, miss_count, capacity, ma, err);
 }
