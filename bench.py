@@ -73,15 +73,30 @@ def append_bytes_per_step(w) -> int:
     return int(w.batch * w.num_kv_heads * (src + token_bytes(w) + 2 * summary_bytes_per_block(w)))
 
 
+def select_launches(w) -> int:
+    """Launches of bound scoring + selection: one fused cluster launch when
+    every tile of every (request, kv head) fits one wave (tensor-core scoring,
+    at most 8 tiles of 128 blocks per request), two with the tensor-core scorer
+    otherwise, one on the CUDA-core path."""
+    import torch
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    if not (w.kv_dtype != "f32" and w.head_dim == 128):
+        return 1
+    tiles = -(-w.max_blocks // 128)
+    return 1 if tiles <= 8 and w.batch * w.num_kv_heads * tiles <= sms else 2
+
+
 def step_launches(w, dec, hot: bool = False, overlap: bool = False) -> int:
     """Kernels of one step as the library dispatches them for this workload:
-    append (not on the offload path), bound scoring + selection (two launches
-    with bf16 summaries at head_dim 128, else one), the swap-in (offload; with
-    the copy overlapped: plan, copy, attention over the hits, attention over
-    the misses and the merge of the two), attention, and the split merge unless
-    the tensor-core attention gives every pair a single split."""
+    append (not on the offload path), bound scoring + selection
+    (select_launches), the swap-in (offload; with the copy overlapped: plan,
+    page copy, attention over the copied blocks, attention over the resident
+    blocks and the merge of the two), attention, and the split merge unless the
+    tensor-core attention merges in the kernel or gives every pair one split."""
+    import torch
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
     n = 0 if hot else 1
-    n += 2 if (w.kv_dtype != "f32" and w.head_dim == 128) else 1
+    n += select_launches(w)
     if hot and overlap:
         return n + 5
     n += 1 if hot else 0
@@ -91,8 +106,6 @@ def step_launches(w, dec, hot: bool = False, overlap: bool = False) -> int:
     splits = dec.workspace.numel() // per_split
     # the tensor-core kernel merges its splits itself when it has split
     # counters and every work item a CTA of its own
-    import torch
-    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
     inline = tc and dec.split_counters is not None and w.batch * w.num_kv_heads * splits <= sms
     return n + (0 if (tc and splits <= 1) or inline else 1)
 
@@ -538,9 +551,8 @@ def run_ours(args, w):
     cpu = cpu_baseline(w, seconds=args.cpu_seconds) if (world == 1 and args.cpu_seconds > 0) else None
     cpu_all = (cpu_baseline_all_cores(w, seconds=args.cpu_seconds / 2)
                if (world == 1 and args.cpu_seconds > 0) else None)
-    # layers that reuse a selection skip its two (or one) launches
-    sel_launches = 2 if (w.kv_dtype != "f32" and w.head_dim == 128) else 1
-    launches_per_step = step_launches(w, d0) - sel_launches * (1 - 1 / args.select_every)
+    # layers that reuse a selection skip its launches
+    launches_per_step = step_launches(w, d0) - select_launches(w) * (1 - 1 / args.select_every)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
         "warmup": wreps * layers, "ms_per_step": ms_per_step, "higher_is_better": True,

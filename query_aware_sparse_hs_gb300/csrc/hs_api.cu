@@ -243,6 +243,8 @@ hs_status hs_score_select_topk(const hs_attn_shape* shape, const hs_paged_kv* kv
       if (!workspace || ws_bytes < need || !aligned(workspace, 16)) return HS_ERR_WORKSPACE;
       buf = static_cast<float*>(workspace);
     }
+    if (score_select_fused_supported(v, d.sms))  // every tile of every pair in one wave: one launch
+      return from_cuda(launch_score_tc(v, q, smin, smax, buf, d.sms, d.err, cs, &a));
     if (launch_score_tc(v, q, smin, smax, buf, d.sms, d.err, cs) != cudaSuccess) return HS_ERR_CUDA;
     return from_cuda(launch_select_only(v, a, buf, d.err, cs));
   }

@@ -59,8 +59,11 @@ cudaError_t launch_summaries(const KvView& kv, int first_block, void* smin, void
 cudaError_t launch_score_select(const KvView& kv, const SelectArgs& a, unsigned* err,
                                 cudaStream_t st);
 bool score_tc_supported(const KvView& kv);
+// fuse (nullable): score and select in one launch, one cluster per (request,
+// kv head); only where score_select_fused_supported.
 cudaError_t launch_score_tc(const KvView& kv, const void* q, const void* smin, const void* smax, float* scores,
-                            int sms, unsigned* err, cudaStream_t st);
+                            int sms, unsigned* err, cudaStream_t st, const SelectArgs* fuse = nullptr);
+bool score_select_fused_supported(const KvView& kv, int sms);
 cudaError_t launch_select_only(const KvView& kv, const SelectArgs& a, const float* scores, unsigned* err,
                                cudaStream_t st);
 cudaError_t launch_attn_simt(const KvView& kv, const AttnArgs& a, unsigned* err, cudaStream_t st);

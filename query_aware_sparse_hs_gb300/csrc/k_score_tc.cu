@@ -16,10 +16,14 @@
 // with TMA into a 3-stage ring, warp 5 issues the 16 MMAs of a tile into one of
 // two TMEM accumulators, warps 0-3 write the [Q+ | Q-] operand of each tile's
 // (request, kv head) and turn accumulator rows into block scores.
+#include <cooperative_groups.h>
 #include <cuda.h>
 
 #include "hs_internal.h"
+#include "select_pair.cuh"
 #include "tc_ptx.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace hs {
 namespace {
@@ -60,9 +64,13 @@ __device__ __forceinline__ bool tile_valid(const ScoreArgs& a, int item, int* pa
   return *tile * kTile < *nb;
 }
 
+// FUSE: launched as one cluster per (request, kv head) with one CTA per tile
+// (every CTA takes exactly one item); once all tiles' scores are stored, rank
+// 0 of the cluster reads them back and runs the selection itself.
+template <bool FUSE>
 __global__ void __launch_bounds__(kThreads, 1)
     score_tc_kernel(const __grid_constant__ CUtensorMap tm_max, const __grid_constant__ CUtensorMap tm_min,
-                    ScoreArgs a, unsigned* err) {
+                    ScoreArgs a, SelectArgs sa, unsigned* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -227,6 +235,33 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  if constexpr (FUSE) {
+    // every CTA of the cluster has stored its tile's scores (the cluster
+    // barrier orders those global stores before rank 0's loads); the ring's
+    // shared memory is free again and holds the selection's work arrays
+    cg::cluster_group cluster = cg::this_cluster();
+    cluster.sync();
+    if (cluster.block_rank() == 0) {
+      float* s_scores = reinterpret_cast<float*>(smem);                              // <= 16 tiles x 128
+      uint32_t(*s_hist)[256] = reinterpret_cast<uint32_t(*)[256]>(smem + 65536);  // 2 x 256
+      int* s_warp = reinterpret_cast<int*>(smem + 65536 + 2048);                     // kThreads / 32 + 1
+      int* s_pick = s_warp + 16;
+      const int pair = blockIdx.x / a.tiles;
+      const int b = pair / a.hkv;
+      const int L = max(a.seq_lens[b], 0);
+      int nb = (L + a.block - 1) / a.block;
+      if (nb > a.max_blocks) {
+        if (tid == 0) set_error(err, HS_EBIT_BLOCK_RANGE);
+        nb = a.max_blocks;
+      }
+      const float* src = a.scores + static_cast<int64_t>(pair) * a.max_blocks;
+      for (int j = tid; j < nb; j += kThreads) s_scores[j] = __ldcg(src + j);
+      for (int i = tid; i < 512; i += kThreads) s_hist[i >> 8][i & 255] = 0u;
+      __syncthreads();
+      sel::smooth_scores(s_scores, nb, a.max_blocks, sa, pair);
+      sel::select_pair<kThreads>(s_scores, nb, L, a.block, sa, pair, s_hist, s_warp, s_pick, err);
+    }
+  }
   if (*abort_flag && tid == 0) set_error(err, HS_EBIT_TIMEOUT);
   if (warp == kMmaWarp) {
     tc_fence_after();
@@ -274,8 +309,13 @@ bool score_tc_supported(const KvView& kv) {
   return encode_fn() != nullptr;
 }
 
+bool score_select_fused_supported(const KvView& kv, int sms) {
+  const int tiles = (kv.max_blocks + kTile - 1) / kTile;
+  return score_tc_supported(kv) && tiles <= 8 && static_cast<int64_t>(kv.batch) * kv.hkv * tiles <= sms;
+}
+
 cudaError_t launch_score_tc(const KvView& kv, const void* q, const void* smin, const void* smax, float* scores,
-                            int sms, unsigned* err, cudaStream_t st) {
+                            int sms, unsigned* err, cudaStream_t st, const SelectArgs* fuse) {
   const int64_t rows = static_cast<int64_t>(kv.batch) * kv.hkv * kv.max_blocks;
   if (rows == 0) return cudaSuccess;
   CUtensorMap mmax, mmin;
@@ -291,10 +331,31 @@ cudaError_t launch_score_tc(const KvView& kv, const void* q, const void* smin, c
   a.max_blocks = kv.max_blocks;
   a.tiles = (kv.max_blocks + kTile - 1) / kTile;
   a.items = kv.batch * kv.hkv * a.tiles;
-  cudaError_t e = cudaFuncSetAttribute(score_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAlloc);
+  if (!fuse) {
+    cudaError_t e = cudaFuncSetAttribute(score_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kAlloc);
+    if (e != cudaSuccess) return e;
+    const int grid = a.items < sms ? a.items : sms;
+    return launch_pdl(score_tc_kernel<false>, dim3(grid), dim3(kThreads), kAlloc, st, mmax, mmin, a, SelectArgs{},
+                      err);
+  }
+  // one cluster of a.tiles CTAs per (request, kv head), one CTA per tile
+  cudaError_t e = cudaFuncSetAttribute(score_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kAlloc);
   if (e != cudaSuccess) return e;
-  const int grid = a.items < sms ? a.items : sms;
-  return launch_pdl(score_tc_kernel, dim3(grid), dim3(kThreads), kAlloc, st, mmax, mmin, a, err);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.items);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kAlloc;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = a.tiles;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, score_tc_kernel<true>, mmax, mmin, a, *fuse, err);
 }
 
 }  // namespace hs
