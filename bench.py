@@ -86,24 +86,41 @@ def select_launches(w) -> int:
     return 1 if tiles <= 8 and w.batch * w.num_kv_heads * tiles <= sms else 2
 
 
-def step_launches(w, dec, hot: bool = False, overlap: bool = False) -> int:
+def fused_step(w, dec) -> bool:
+    """Whether the decoder's step runs scoring, selection and attention as one
+    launch (the library answers for this geometry on this device)."""
+    from query_aware_sparse_hs_gb300 import hs
+    return bool(dec.fuse_step) and hs.hs_score_select_attend_fused(
+        dec.shape, w.batch, dec.max_blocks, dec.capacity, dec.attn_params) == 1
+
+
+def attn_splits(w, dec) -> int:
+    from query_aware_sparse_hs_gb300 import hs
+    per_split = w.batch * w.num_q_heads * (w.head_dim + 1) * 4
+    return hs.hs_workspace_bytes(dec.shape, w.batch, dec.capacity, dec.attn_params) // per_split
+
+
+def step_launches(w, dec, hot: bool = False, overlap: bool = False, allow_fused: bool = True) -> int:
     """Kernels of one step as the library dispatches them for this workload:
-    append (not on the offload path), bound scoring + selection
+    append (not on the offload path), then either the single scoring +
+    selection + attention launch, or bound scoring + selection
     (select_launches), the swap-in (offload; with the copy overlapped: plan,
     page copy, attention over the copied blocks, attention over the resident
-    blocks and the merge of the two), attention, and the split merge unless the
-    tensor-core attention merges in the kernel or gives every pair one split."""
+    blocks and the merge of the two) and attention; and the split merge unless
+    the tensor-core attention merges in the kernel or gives every pair one
+    split."""
     import torch
     sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
     n = 0 if hot else 1
+    splits = attn_splits(w, dec)
+    if not hot and allow_fused and fused_step(w, dec):
+        return n + 1 + (0 if splits <= 1 or dec.split_counters is not None else 1)
     n += select_launches(w)
     if hot and overlap:
         return n + 5
     n += 1 if hot else 0
     n += 1
     tc = w.kv_dtype in ("bf16", "fp8") and w.head_dim == 128 and w.block_size in (16, 32, 64, 128)
-    per_split = w.batch * w.num_q_heads * (w.head_dim + 1) * 4
-    splits = dec.workspace.numel() // per_split
     # the tensor-core kernel merges its splits itself when it has split
     # counters and every work item a CTA of its own
     inline = tc and dec.split_counters is not None and w.batch * w.num_kv_heads * splits <= sms
@@ -336,10 +353,10 @@ def workload_config(w, layers: int) -> dict:
 # GPU arm
 # ----------------------------------------------------------------------------
 
-# DRAM bytes (read + written) of one attention launch from an ncu capture of the
-# current kernel (profiles/ncu_full_llama8b_bf16_1layer.md), per workload;
-# a workload without a capture of the current kernel reports null.
-NCU_TRAFFIC = {"llama8b_bf16": 33_775_872}
+# DRAM bytes (read + written) of one launch of the dominant kernel from an ncu
+# capture of the current kernel, keyed by (workload, single-launch step); a
+# workload without a capture of the current kernel reports null.
+NCU_TRAFFIC = {}
 
 
 def run_ours(args, w):
@@ -481,6 +498,9 @@ def run_ours(args, w):
 
     t_attn = timed_graph(lambda i: decs[i % layers].attend(kvs[i % layers], qs[i % layers], stream,
                                                            selection=lead_of(i % layers)))
+    fused = fused_step(w, decs[0])
+    t_fused = (timed_graph(lambda i: decs[i % layers].select_attend(kvs[i % layers], qs[i % layers], stream=stream))
+               if fused else None)
     t_sel = timed_graph(lambda i: decs[i % layers].select(kvs[i % layers], qs[i % layers], stream=stream))
     t_app = timed_graph(lambda i: decs[i % layers].append(kvs[i % layers], *news[i % layers], stream))
     t_sum_full = timed_graph(lambda i: decs[i % layers].build_summaries(kvs[i % layers], 0, stream), rr=3)
@@ -505,6 +525,13 @@ def run_ours(args, w):
     full_sum_bytes = total_blocks * (B * token_bytes(w) / 2 + summary_bytes_per_block(w))
     peak, peak_kind = load_peaks()
     attn_gbs = a_bytes / (t_attn * 1e-6) / 1e9
+    # the dominant kernel: the single scoring + selection + attention launch
+    # where the step uses it, else the attention launch (with its merge)
+    if fused:
+        dom = {"kernel": "score_select_attend (one launch)", "bytes": a_bytes + s_bytes, "us": t_fused}
+    else:
+        dom = {"kernel": "sparse_paged_decode_attn", "bytes": a_bytes, "us": t_attn}
+    dom_gbs = dom["bytes"] / (dom["us"] * 1e-6) / 1e9
 
     # ---- end to end through the C ABI with host buffers ----
     # per step: one copy of the step's inputs (q, new K/V) from pinned host
@@ -552,20 +579,23 @@ def run_ours(args, w):
     cpu_all = (cpu_baseline_all_cores(w, seconds=args.cpu_seconds / 2)
                if (world == 1 and args.cpu_seconds > 0) else None)
     # layers that reuse a selection skip its launches
-    launches_per_step = step_launches(w, d0) - select_launches(w) * (1 - 1 / args.select_every)
+    # a layer that reuses a selection runs append + attention (+ merge)
+    reuse_launches = step_launches(w, d0, allow_fused=False) - select_launches(w)
+    launches_per_step = step_launches(w, d0) / args.select_every + reuse_launches * (1 - 1 / args.select_every)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
         "warmup": wreps * layers, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.kv_dtype, "data": "synthetic",
         "config": dict(workload_config(w, layers), select_every=args.select_every),
         "hbm_gbs_step": step_bytes / (ms_per_step * 1e-3) / 1e9,
-        "roofline": {"bound": "hbm", "kernel": "sparse_paged_decode_attn", "achieved": attn_gbs,
-                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": attn_gbs / peak,
-                     "traffic": NCU_TRAFFIC.get(w.name), "algorithmic_bytes_per_launch": a_bytes,
-                     "avg_launch_us": t_attn},
-        "kernels_us": {"append": t_app, "score_select": t_sel, "attention_with_merge": t_attn,
-                       "summary_build_full": t_sum_full},
-        "kernels_gbs": {"score_select": s_bytes / (t_sel * 1e-6) / 1e9,
+        "roofline": {"bound": "hbm", "kernel": dom["kernel"], "achieved": dom_gbs,
+                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": dom_gbs / peak,
+                     "traffic": NCU_TRAFFIC.get((w.name, fused)), "algorithmic_bytes_per_launch": dom["bytes"],
+                     "avg_launch_us": dom["us"]},
+        "kernels_us": {"append": t_app, "score_select_attend": t_fused, "score_select": t_sel,
+                       "attention_with_merge": t_attn, "summary_build_full": t_sum_full},
+        "kernels_gbs": {"score_select_attend": dom_gbs if fused else None,
+                        "score_select": s_bytes / (t_sel * 1e-6) / 1e9,
                         "attention_with_merge": attn_gbs,
                         "summary_build_full": full_sum_bytes / (t_sum_full * 1e-6) / 1e9},
         "bytes_per_step": {"attention": a_bytes, "score_select": s_bytes, "append": int(append_bytes)},

@@ -283,6 +283,44 @@ HS_API hs_status hs_sparse_paged_decode_attn(const hs_attn_shape* shape, const h
                                       const hs_attn_params* params, void* out, float* lse_opt,
                                       void* workspace, size_t ws_bytes, hs_stream_t stream);
 
+/* Bytes of workspace hs_score_select_attend needs: the selection's score
+ * buffer (hs_select_workspace_bytes) followed by the attention's partials
+ * (hs_workspace_bytes).  0 on invalid input. */
+HS_API size_t hs_score_select_attend_workspace_bytes(const hs_attn_shape* shape, int32_t batch,
+                                                     int32_t max_blocks, int32_t capacity,
+                                                     const hs_attn_params* attn_params);
+
+/* Selection and attention of one decode step in one call ([KVS] §5 + §2, [FLL]
+ * §2.2): the same results as
+ * hs_score_select_topk(shape, kv, q, smin, smax, sel_params, sel, sel_count,
+ * scores_opt, ...) followed by hs_sparse_paged_decode_attn(shape, kv, q, sel,
+ * sel_count, sel_params->capacity, attn_params, out, lse_opt, ...), with the
+ * same argument rules, outputs and error bits as those two calls.
+ * With bf16 K/V and summaries, head_dim 128, at most 8 query heads per kv
+ * head, the tensor-core attention and no CTA limit (attn_params->max_ctas 0),
+ * and when every (request, kv head) takes one cluster of at most 8 CTAs (its
+ * 128-block score tiles and its attention splits) and all clusters fit one
+ * wave, it is a single launch: each cluster scores its tiles, one CTA selects
+ * and resolves the selected pages, and each CTA attends over one split of the
+ * selection it received in shared memory.  Otherwise the calls' own launches
+ * run in order.  workspace: hs_score_select_attend_workspace_bytes(shape,
+ * batch, max_blocks, sel_params->capacity, attn_params) bytes, 16-byte
+ * aligned; the selection part is used only without scores_opt. */
+HS_API hs_status hs_score_select_attend(const hs_attn_shape* shape, const hs_paged_kv* kv, const void* q,
+                                        const void* smin, const void* smax,
+                                        const hs_select_params* sel_params, int32_t* sel,
+                                        int32_t* sel_count, float* scores_opt,
+                                        const hs_attn_params* attn_params, void* out, float* lse_opt,
+                                        void* workspace, size_t ws_bytes, hs_stream_t stream);
+
+/* 1 when hs_score_select_attend runs as a single launch (plus the split merge
+ * when attn_params has no split_counters and a pair has several splits) for
+ * this geometry on the current device, 0 when it runs the separate launches,
+ * -1 on invalid input or without a device.  Depends on the shape, batch,
+ * max_blocks, capacity and attn_params only. */
+HS_API int32_t hs_score_select_attend_fused(const hs_attn_shape* shape, int32_t batch, int32_t max_blocks,
+                                            int32_t capacity, const hs_attn_params* attn_params);
+
 /* HiSparse swap-in, [KVS] §7: for every (b, kvh), make each selected block
  * resident in the stream's hot slots.  Hits set last_used = step.  Misses are
  * taken in ascending block order; each goes to the lowest free slot, else to

@@ -131,6 +131,108 @@ int attn_ctas(int sms, const hs_attn_params* p) {
   return (p && p->max_ctas > 0 && p->max_ctas < sms) ? p->max_ctas : sms;
 }
 
+// Argument checks of the selection; fills the launch arguments.
+hs_status prepare_select(const hs_attn_shape* shape, const hs_paged_kv* kv, const void* q, const void* smin,
+                         const void* smax, const hs_select_params* params, int32_t* sel, int32_t* sel_count,
+                         float* scores_opt, SelectArgs* out) {
+  hs_status st = check_shape(shape);
+  if (st != HS_OK) return st;
+  if (!kv || !kv->seq_lens || kv->batch < 0 || kv->max_blocks < 1) return HS_ERR_INVALID_ARG;
+  if (!q || !smin || !smax || !sel || !sel_count || !params) return HS_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(smin, 16) || !aligned(smax, 16) || !aligned(sel, 4) ||
+      !aligned(sel_count, 4) || (scores_opt && !aligned(scores_opt, 4)))
+    return HS_ERR_INVALID_ARG;
+  if (params->sink_tokens < 0 || params->window_tokens < 0 || params->k_scored < 0 ||
+      params->capacity < 1)
+    return HS_ERR_INVALID_ARG;
+  if (!(params->history_weight >= 0.0f && params->history_weight < 1.0f)) return HS_ERR_INVALID_ARG;
+  if (params->history_weight > 0.0f && (!params->score_history || !aligned(params->score_history, 4)))
+    return HS_ERR_INVALID_ARG;
+  if (kv->max_blocks > kMaxSelectBlocks) return HS_ERR_UNSUPPORTED;
+  if (params->capacity < max_selected(shape, kv->max_blocks, params->sink_tokens,
+                                      params->window_tokens, params->k_scored))
+    return HS_ERR_CAPACITY;
+  SelectArgs& a = *out;
+  a.q = q;
+  a.smin = smin;
+  a.smax = smax;
+  a.sel = sel;
+  a.sel_count = sel_count;
+  a.scores = scores_opt;
+  a.sink_tokens = params->sink_tokens;
+  a.window_tokens = params->window_tokens;
+  a.k_scored = params->k_scored;
+  a.capacity = params->capacity;
+  a.history_weight = params->history_weight;
+  a.history = params->history_weight > 0.0f ? params->score_history : nullptr;
+  return HS_OK;
+}
+
+// The selection's launches: tensor-core bound scoring (into scores_opt or the
+// workspace) and selection, fused into one launch where every tile of every
+// pair fits one wave; else the CUDA-core scoring + selection clusters.
+hs_status run_select(const KvView& v, const SelectArgs& a, const Device& d, void* workspace, size_t ws_bytes,
+                     cudaStream_t cs) {
+  if (score_tc_supported(v)) {
+    float* buf = a.scores;
+    if (!buf) {
+      const size_t need = static_cast<size_t>(v.batch) * v.hkv * v.max_blocks * sizeof(float);
+      if (!workspace || ws_bytes < need || !aligned(workspace, 16)) return HS_ERR_WORKSPACE;
+      buf = static_cast<float*>(workspace);
+    }
+    if (score_select_fused_supported(v, d.sms))  // every tile of every pair in one wave: one launch
+      return from_cuda(launch_score_tc(v, a.q, a.smin, a.smax, buf, d.sms, d.err, cs, &a));
+    if (launch_score_tc(v, a.q, a.smin, a.smax, buf, d.sms, d.err, cs) != cudaSuccess) return HS_ERR_CUDA;
+    return from_cuda(launch_select_only(v, a, buf, d.err, cs));
+  }
+  return from_cuda(launch_score_select(v, a, d.err, cs));
+}
+
+// Argument checks of the attention; fills the launch arguments and picks the
+// tensor-core or the CUDA-core kernel.
+hs_status prepare_attn(const hs_attn_shape* shape, const hs_paged_kv* kv, const void* q, const int32_t* sel,
+                       const int32_t* sel_count, int32_t capacity, const hs_attn_params* params, void* out,
+                       float* lse_opt, void* workspace, size_t ws_bytes, Device* dev, AttnArgs* out_args,
+                       bool* use_tc) {
+  hs_status st = check_kv(shape, kv, true);
+  if (st != HS_OK) return st;
+  if (!q || !sel || !sel_count || !out || !params || capacity < 1) return HS_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(sel, 4) || !aligned(sel_count, 4))
+    return HS_ERR_INVALID_ARG;
+  if (params->algo < 0 || params->algo > 2 || params->blocks_per_split < 0 || params->max_ctas < 0)
+    return HS_ERR_INVALID_ARG;
+  if ((st = current_device(dev)) != HS_OK) return st;
+  const Device& d = *dev;
+  const KvView v = make_view(shape, kv);
+  const int ctas = attn_ctas(d.sms, params);
+  if (params->algo == 1) {
+    *use_tc = false;
+  } else if (params->algo == 2) {
+    if (!attn_tc_supported(v)) return HS_ERR_UNSUPPORTED;
+    *use_tc = true;
+  } else {
+    *use_tc = attn_tc_supported(v);
+  }
+  AttnArgs& a = *out_args;
+  split_geometry(shape, kv->batch, capacity, params, ctas, &a.blocks_per_split, &a.splits);
+  const size_t need = workspace_for(shape, kv->batch, a.splits);
+  if (need > 0 && (!workspace || ws_bytes < need || !aligned(workspace, 16))) return HS_ERR_WORKSPACE;
+  a.sms = ctas;
+  if (params->split_counters && !aligned(params->split_counters, 4)) return HS_ERR_INVALID_ARG;
+  a.counters = params->split_counters;
+  a.q = q;
+  a.sel = sel;
+  a.sel_count = sel_count;
+  a.capacity = capacity;
+  a.scale = params->scale;
+  a.out_is_fp32 = params->out_is_fp32 ? 1 : 0;
+  a.out = out;
+  a.lse = lse_opt;
+  a.ws_o = static_cast<float*>(workspace);
+  a.ws_lse = a.ws_o + static_cast<size_t>(kv->batch) * shape->num_q_heads * a.splits * shape->head_dim;
+  return HS_OK;
+}
+
 }  // namespace
 }  // namespace hs
 
@@ -201,54 +303,12 @@ hs_status hs_score_select_topk(const hs_attn_shape* shape, const hs_paged_kv* kv
                                const hs_select_params* params, int32_t* sel,
                                int32_t* sel_count, float* scores_opt, void* workspace,
                                size_t ws_bytes, hs_stream_t stream) {
-  hs_status st = check_shape(shape);
+  SelectArgs a;
+  hs_status st = prepare_select(shape, kv, q, smin, smax, params, sel, sel_count, scores_opt, &a);
   if (st != HS_OK) return st;
-  if (!kv || !kv->seq_lens || kv->batch < 0 || kv->max_blocks < 1) return HS_ERR_INVALID_ARG;
-  if (!q || !smin || !smax || !sel || !sel_count || !params) return HS_ERR_INVALID_ARG;
-  if (!aligned(q, 16) || !aligned(smin, 16) || !aligned(smax, 16) || !aligned(sel, 4) ||
-      !aligned(sel_count, 4) || (scores_opt && !aligned(scores_opt, 4)))
-    return HS_ERR_INVALID_ARG;
-  if (params->sink_tokens < 0 || params->window_tokens < 0 || params->k_scored < 0 ||
-      params->capacity < 1)
-    return HS_ERR_INVALID_ARG;
-  if (!(params->history_weight >= 0.0f && params->history_weight < 1.0f)) return HS_ERR_INVALID_ARG;
-  if (params->history_weight > 0.0f && (!params->score_history || !aligned(params->score_history, 4)))
-    return HS_ERR_INVALID_ARG;
-  if (kv->max_blocks > kMaxSelectBlocks) return HS_ERR_UNSUPPORTED;
-  if (params->capacity < max_selected(shape, kv->max_blocks, params->sink_tokens,
-                                      params->window_tokens, params->k_scored))
-    return HS_ERR_CAPACITY;
   Device d;
   if ((st = current_device(&d)) != HS_OK) return st;
-  KvView v = make_view(shape, kv);
-  SelectArgs a;
-  a.q = q;
-  a.smin = smin;
-  a.smax = smax;
-  a.sel = sel;
-  a.sel_count = sel_count;
-  a.scores = scores_opt;
-  a.sink_tokens = params->sink_tokens;
-  a.window_tokens = params->window_tokens;
-  a.k_scored = params->k_scored;
-  a.capacity = params->capacity;
-  a.history_weight = params->history_weight;
-  a.history = params->history_weight > 0.0f ? params->score_history : nullptr;
-  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  if (score_tc_supported(v)) {
-    // tensor-core bound scoring into a score buffer, then one CTA per pair selects
-    float* buf = scores_opt;
-    if (!buf) {
-      const size_t need = static_cast<size_t>(kv->batch) * shape->num_kv_heads * kv->max_blocks * sizeof(float);
-      if (!workspace || ws_bytes < need || !aligned(workspace, 16)) return HS_ERR_WORKSPACE;
-      buf = static_cast<float*>(workspace);
-    }
-    if (score_select_fused_supported(v, d.sms))  // every tile of every pair in one wave: one launch
-      return from_cuda(launch_score_tc(v, q, smin, smax, buf, d.sms, d.err, cs, &a));
-    if (launch_score_tc(v, q, smin, smax, buf, d.sms, d.err, cs) != cudaSuccess) return HS_ERR_CUDA;
-    return from_cuda(launch_select_only(v, a, buf, d.err, cs));
-  }
-  return from_cuda(launch_score_select(v, a, d.err, cs));
+  return run_select(make_view(shape, kv), a, d, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
 size_t hs_select_workspace_bytes(const hs_attn_shape* shape, int32_t batch, int32_t max_blocks) {
@@ -264,45 +324,77 @@ hs_status hs_sparse_paged_decode_attn(const hs_attn_shape* shape, const hs_paged
                                       void* workspace, size_t ws_bytes, hs_stream_t stream) {
   hs_status st = check_shape(shape);
   if (st != HS_OK) return st;
-  if ((st = check_kv(shape, kv, true)) != HS_OK) return st;
-  if (!q || !sel || !sel_count || !out || !params || capacity < 1) return HS_ERR_INVALID_ARG;
-  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(sel, 4) || !aligned(sel_count, 4))
-    return HS_ERR_INVALID_ARG;
-  if (params->algo < 0 || params->algo > 2 || params->blocks_per_split < 0 || params->max_ctas < 0)
-    return HS_ERR_INVALID_ARG;
   Device d;
-  if ((st = current_device(&d)) != HS_OK) return st;
-  const KvView v = make_view(shape, kv);
-  const int ctas = attn_ctas(d.sms, params);
-  bool use_tc;
-  if (params->algo == 1) {
-    use_tc = false;
-  } else if (params->algo == 2) {
-    if (!attn_tc_supported(v)) return HS_ERR_UNSUPPORTED;
-    use_tc = true;
-  } else {
-    use_tc = attn_tc_supported(v);
-  }
   AttnArgs a;
-  split_geometry(shape, kv->batch, capacity, params, ctas, &a.blocks_per_split, &a.splits);
-  const size_t need = workspace_for(shape, kv->batch, a.splits);
-  if (need > 0 && (!workspace || ws_bytes < need || !aligned(workspace, 16))) return HS_ERR_WORKSPACE;
-  a.sms = ctas;
-  if (params->split_counters && !aligned(params->split_counters, 4)) return HS_ERR_INVALID_ARG;
-  a.counters = params->split_counters;
-  a.q = q;
-  a.sel = sel;
-  a.sel_count = sel_count;
-  a.capacity = capacity;
-  a.scale = params->scale;
-  a.out_is_fp32 = params->out_is_fp32 ? 1 : 0;
-  a.out = out;
-  a.lse = lse_opt;
-  a.ws_o = static_cast<float*>(workspace);
-  a.ws_lse = a.ws_o + static_cast<size_t>(kv->batch) * shape->num_q_heads * a.splits * shape->head_dim;
+  bool use_tc = false;
+  st = prepare_attn(shape, kv, q, sel, sel_count, capacity, params, out, lse_opt, workspace, ws_bytes, &d, &a,
+                    &use_tc);
+  if (st != HS_OK) return st;
+  const KvView v = make_view(shape, kv);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = use_tc ? launch_attn_tc(v, a, d.err, s) : launch_attn_simt(v, a, d.err, s);
   if (e != cudaSuccess) return HS_ERR_CUDA;
+  if (a.merged) return HS_OK;
+  return from_cuda(launch_merge(v, a, s));
+}
+
+size_t hs_score_select_attend_workspace_bytes(const hs_attn_shape* shape, int32_t batch, int32_t max_blocks,
+                                              int32_t capacity, const hs_attn_params* params) {
+  if (check_shape(shape) != HS_OK || batch < 0 || max_blocks < 0 || capacity < 0) return 0;
+  return hs_select_workspace_bytes(shape, batch, max_blocks) + hs_workspace_bytes(shape, batch, capacity, params);
+}
+
+int32_t hs_score_select_attend_fused(const hs_attn_shape* shape, int32_t batch, int32_t max_blocks,
+                                     int32_t capacity, const hs_attn_params* params) {
+  if (check_shape(shape) != HS_OK || batch < 0 || max_blocks < 1 || capacity < 1 || !params) return -1;
+  if (params->algo < 0 || params->algo > 2 || params->blocks_per_split < 0 || params->max_ctas < 0) return -1;
+  Device d;
+  if (current_device(&d) != HS_OK) return -1;
+  if (params->algo == 1 || attn_ctas(d.sms, params) != d.sms) return 0;
+  KvView v{};
+  v.batch = batch;
+  v.max_blocks = max_blocks;
+  v.num_pages = 1;
+  v.hq = shape->num_q_heads;
+  v.hkv = shape->num_kv_heads;
+  v.group = shape->num_q_heads / shape->num_kv_heads;
+  v.head_dim = shape->head_dim;
+  v.block = shape->block_size;
+  v.kv_dtype = shape->kv_dtype;
+  if (!attn_tc_supported(v)) return 0;
+  AttnArgs a;
+  split_geometry(shape, batch, capacity, params, d.sms, &a.blocks_per_split, &a.splits);
+  return score_select_attn_supported(v, a, d.sms) ? 1 : 0;
+}
+
+hs_status hs_score_select_attend(const hs_attn_shape* shape, const hs_paged_kv* kv, const void* q,
+                                 const void* smin, const void* smax, const hs_select_params* sel_params,
+                                 int32_t* sel, int32_t* sel_count, float* scores_opt,
+                                 const hs_attn_params* attn_params, void* out, float* lse_opt, void* workspace,
+                                 size_t ws_bytes, hs_stream_t stream) {
+  SelectArgs sa;
+  hs_status st = prepare_select(shape, kv, q, smin, smax, sel_params, sel, sel_count, scores_opt, &sa);
+  if (st != HS_OK) return st;
+  // workspace: the selection's score buffer first, the attention's partials after it
+  const size_t sw = hs_select_workspace_bytes(shape, kv->batch, kv->max_blocks);
+  if (sw > 0 && (!workspace || ws_bytes < sw || !aligned(workspace, 16))) return HS_ERR_WORKSPACE;
+  void* aws = workspace ? static_cast<uint8_t*>(workspace) + sw : nullptr;
+  const size_t aws_bytes = workspace ? ws_bytes - sw : 0;
+  Device d;
+  AttnArgs a;
+  bool use_tc = false;
+  st = prepare_attn(shape, kv, q, sel, sel_count, sel_params->capacity, attn_params, out, lse_opt, aws, aws_bytes,
+                    &d, &a, &use_tc);
+  if (st != HS_OK) return st;
+  const KvView v = make_view(shape, kv);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (use_tc && a.sms == d.sms && score_select_attn_supported(v, a, d.sms)) {
+    if (launch_score_select_attn(v, smin, smax, sa, a, d.err, s) != cudaSuccess) return HS_ERR_CUDA;
+  } else {
+    if ((st = run_select(v, sa, d, workspace, sw, s)) != HS_OK) return st;
+    cudaError_t e = use_tc ? launch_attn_tc(v, a, d.err, s) : launch_attn_simt(v, a, d.err, s);
+    if (e != cudaSuccess) return HS_ERR_CUDA;
+  }
   if (a.merged) return HS_OK;
   return from_cuda(launch_merge(v, a, s));
 }

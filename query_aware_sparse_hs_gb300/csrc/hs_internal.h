@@ -69,6 +69,11 @@ cudaError_t launch_select_only(const KvView& kv, const SelectArgs& a, const floa
 cudaError_t launch_attn_simt(const KvView& kv, const AttnArgs& a, unsigned* err, cudaStream_t st);
 cudaError_t launch_attn_tc(const KvView& kv, AttnArgs& a, unsigned* err, cudaStream_t st);
 bool attn_tc_supported(const KvView& kv);
+// Bound scoring, selection and tensor-core attention in one cluster launch
+// (bf16, head_dim 128, g <= 8, every pair in one wave of at most 8 CTAs).
+bool score_select_attn_supported(const KvView& kv, const AttnArgs& a, int sms);
+cudaError_t launch_score_select_attn(const KvView& kv, const void* smin, const void* smax, const SelectArgs& sa,
+                                     AttnArgs& a, unsigned* err, cudaStream_t st);
 // LSE merge of `parts` partial results laid out [parts][rows][D] and [parts][rows].
 cudaError_t launch_merge_parts(int rows, int head_dim, int parts, const float* outs, const float* lses, void* out,
                                int out_f32, float* lse_out, cudaStream_t st);

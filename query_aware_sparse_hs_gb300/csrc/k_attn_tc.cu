@@ -22,10 +22,16 @@
 //               groups working on alternate chunks, merged per work item.
 // Every wait is bounded (2 s); on a time-out the CTA sets HS_EBIT_TIMEOUT,
 // stops all roles, lets in-flight copies land and frees its TMEM.
+#include <cooperative_groups.h>
+#include <type_traits>
 #include <cuda.h>
 
+#include "bound_tile.cuh"
 #include "hs_internal.h"
+#include "select_pair.cuh"
 #include "tc_ptx.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace hs {
 namespace {
@@ -99,19 +105,50 @@ struct Item {
   int pair, split, b, kvh, s0, s1, nch, L, nb;
 };
 
-__device__ __forceinline__ Item item_geom(const TcArgs& a, int item, int bpc) {
+// The work items of one CTA and where their selected blocks come from.  A
+// persistent launch takes items first, first + stride, ... and resolves the
+// global selection through the page table; a CTA of the fused scoring +
+// selection + attention launch takes one item, whose (page, valid tokens)
+// list rank 0 of its cluster has already resolved into this CTA's shared
+// memory: list[i] is position s0 + i of the pair's selection, positions
+// [s0, s1) are the item's, and L is the request's length.
+struct Work {
+  int first, stride;
+  const int2* list;
+  int s0, s1, L;
+};
+
+__device__ __forceinline__ Work persistent_work() {
+  return Work{static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), nullptr, 0, 0, 0};
+}
+
+// Selected blocks per split of a pair with cnt selected blocks: its whole
+// 128-token chunks spread evenly over the splits, at most bps.
+__device__ __forceinline__ int split_len(int cnt, int bpc, int splits, int bps) {
+  const int per = ((cnt + bpc - 1) / bpc + splits - 1) / splits * bpc;
+  return min(per, bps);
+}
+
+__device__ __forceinline__ Item item_geom(const TcArgs& a, int item, int bpc, const Work& w) {
   Item it;
   it.pair = item / a.splits;
   it.split = item - it.pair * a.splits;
   it.b = it.pair / a.hkv;
   it.kvh = it.pair - it.b * a.hkv;
-  int cnt = a.sel_count[it.pair];
-  cnt = max(0, min(cnt, a.capacity));
-  it.s0 = it.split * a.bps;
-  it.s1 = min(cnt, it.s0 + a.bps);
+  if (w.list) {
+    it.s0 = w.s0;
+    it.s1 = w.s1;
+    it.L = w.L;
+  } else {
+    int cnt = a.sel_count[it.pair];
+    cnt = max(0, min(cnt, a.capacity));
+    const int per = split_len(cnt, bpc, a.splits, a.bps);
+    it.s0 = it.split * per;
+    it.s1 = min(cnt, it.s0 + per);
+    it.L = a.seq_lens[it.b];
+  }
   const int nblk = it.s1 - it.s0;
   it.nch = nblk > 0 ? (nblk + bpc - 1) / bpc : 0;
-  it.L = a.seq_lens[it.b];
   it.nb = min((max(it.L, 0) + a.block - 1) / a.block, a.max_blocks);
   return it;
 }
@@ -207,10 +244,10 @@ __device__ __forceinline__ void merge_if_last(const TcArgs& a, const Item& it, i
   if (t == 0) a.counters[it.pair] = 0u;
 }
 
-// First item at or after `item` (stepping by the grid) that has chunks; a.items if none.
-__device__ __forceinline__ int find_item(const TcArgs& a, int bpc, int item, Item* it) {
-  for (; item < a.items; item += gridDim.x) {
-    *it = item_geom(a, item, bpc);
+// First item at or after `item` (stepping by w.stride) that has chunks; a.items if none.
+__device__ __forceinline__ int find_item(const TcArgs& a, int bpc, int item, Item* it, const Work& w) {
+  for (; item < a.items; item += w.stride) {
+    *it = item_geom(a, item, bpc, w);
     if (it->nch > 0) break;
   }
   return item;
@@ -219,8 +256,10 @@ __device__ __forceinline__ int find_item(const TcArgs& a, int bpc, int item, Ite
 // Lane's block of the group of 32 selected positions starting at `gbase`:
 // (page, valid tokens), page -1 past the item or for a bad entry.  The
 // selection entry is read without waiting for the item's count.
-__device__ __forceinline__ int2 resolve_group(const TcArgs& a, const Item& it, int gbase, unsigned* bad) {
+__device__ __forceinline__ int2 resolve_group(const TcArgs& a, const Item& it, int gbase, unsigned* bad,
+                                              const Work& w) {
   const int lane = threadIdx.x & 31;
+  if (w.list) return it.s0 + gbase + lane < it.s1 ? w.list[gbase + lane] : make_int2(-1, 0);
   const int pos = it.s0 + gbase + lane;
   const int64_t row = static_cast<int64_t>(it.pair) * a.capacity;
   const int j = pos < a.capacity ? a.sel[row + pos] : -1;
@@ -244,14 +283,14 @@ __device__ __forceinline__ int2 resolve_group(const TcArgs& a, const Item& it, i
 // valid-token counts are published in meta[stage][8] for the softmax warps and
 // every lane issues the copies of its own block.
 template <int STAGES, typename IssueFn>
-__device__ __forceinline__ void run_producer(const TcArgs& a, int bpc, uint32_t full0, uint32_t empty0,
+__device__ __forceinline__ void run_producer(const TcArgs& a, const Work& w, int bpc, uint32_t full0, uint32_t empty0,
                                              int2* meta, uint32_t bytes_per_block, volatile int* abort_flag,
                                              unsigned* err, IssueFn issue) {
   const int lane = threadIdx.x & 31;
   unsigned bad = 0;
   Item it;
-  int item = find_item(a, bpc, blockIdx.x, &it);
-  int2 cur = item < a.items ? resolve_group(a, it, 0, &bad) : make_int2(-1, 0);
+  int item = find_item(a, bpc, w.first, &it, w);
+  int2 cur = item < a.items ? resolve_group(a, it, 0, &bad, w) : make_int2(-1, 0);
   int c = 0;
   bool stop = false;
   while (item < a.items && !stop) {
@@ -262,10 +301,10 @@ __device__ __forceinline__ void run_producer(const TcArgs& a, int bpc, uint32_t 
     for (int g = 0; g < ngroups && !stop; ++g) {
       int2 nxt = make_int2(-1, 0);
       if (g + 1 < ngroups) {
-        nxt = resolve_group(a, it, (g + 1) * 32, &bad);
+        nxt = resolve_group(a, it, (g + 1) * 32, &bad, w);
       } else {
-        next_item = find_item(a, bpc, item + gridDim.x, &nit);
-        if (next_item < a.items) nxt = resolve_group(a, nit, 0, &bad);
+        next_item = find_item(a, bpc, item + w.stride, &nit, w);
+        if (next_item < a.items) nxt = resolve_group(a, nit, 0, &bad, w);
       }
       const int gchunks = min(32 / bpc, (nblk - g * 32 + bpc - 1) / bpc);
       for (int k = 0; k < gchunks; ++k, ++c) {
@@ -340,11 +379,50 @@ __device__ __forceinline__ float warp_reduce_scatter(float (&v)[NH]) {
   return v[0];
 }
 
+// Barrier initialisation (thread 0) and TMEM allocation (warp kMma1B) of a
+// bf16 attention CTA; the caller synchronises the CTA before any role starts.
 template <int NH>
-__global__ void __launch_bounds__(kThreadsB, 1)
-    attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                   TcArgs a, unsigned* err) {
+__device__ __forceinline__ void attn_bf16_setup(uint8_t* smem) {
   using Ly = Layout<NH>;
+  const uint32_t bar0 = smem_u32(smem) + Ly::kOffBar;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar0 + 8 * s, 1);              // full
+      mbar_init(bar0 + 8 * (kStages + s), 1);  // empty
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar0 + 8 * (2 * kStages + b), 1);      // s_full
+      mbar_init(bar0 + 8 * (2 * kStages + 2 + b), 128);  // s_free
+      mbar_init(bar0 + 8 * (2 * kStages + 4 + b), 128);  // p_full
+      mbar_init(bar0 + 8 * (2 * kStages + 6 + b), 1);    // o_full
+      mbar_init(bar0 + 8 * (2 * kStages + 8 + b), 128);  // o_free
+    }
+    mbar_init(bar0 + 8 * (2 * kStages + 10), 128);  // q_full
+    *reinterpret_cast<volatile int*>(smem + Ly::kOffMisc + 4) = 0;  // abort flag
+    fence_barrier_init();
+  }
+  if (warp == kMma1B) {
+    tmem_alloc(smem_u32(smem + Ly::kOffMisc), Ly::kTmemCols);
+    tmem_relinquish();
+  }
+}
+
+struct NoEmit {};
+
+// The whole life of one bf16 attention CTA over the items of w: set-up
+// (unless SETUP is false: the caller ran attn_bf16_setup, synchronised the
+// CTA and waited for its predecessor), roles, tear-down.  An item's result
+// goes to the output (one split) or the partial workspace, or, with an Emit
+// other than NoEmit, to emit(h, channel, o, lse) for the caller's merge.  Run
+// by all kThreadsB threads.
+template <int NH, bool SETUP = true, class Emit = NoEmit>
+__device__ __forceinline__ void attn_bf16_cta(const CUtensorMap* tm_k_, const CUtensorMap* tm_v_, const TcArgs& a,
+                                              const Work& w, unsigned* err, const Emit& emit = Emit{}) {
+  constexpr bool PART_SMEM = !std::is_same<Emit, NoEmit>::value;
+  using Ly = Layout<NH>;
+  const CUtensorMap& tm_k = *tm_k_;
+  const CUtensorMap& tm_v = *tm_v_;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -369,38 +447,25 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   const int B = a.block;
   const int bpc = kChunk / B;
 
-  pdl_trigger();
-  // ---- set-up: barriers and TMEM (overlaps the previous kernel) ----
-  if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
+  if constexpr (SETUP) {
+    pdl_trigger();
+    // ---- set-up: barriers, TMEM, tensor maps (overlaps the previous kernel) ----
+    if (warp == kProdB && lane == 0) {
+      prefetch_tmap(&tm_k);
+      prefetch_tmap(&tm_v);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(s_full(b), 1);
-      mbar_init(s_free(b), 128);
-      mbar_init(p_full(b), 128);
-      mbar_init(o_full(b), 1);
-      mbar_init(o_free(b), 128);
-    }
-    mbar_init(q_full, 128);
-    *abort_flag = 0;
-    fence_barrier_init();
+    attn_bf16_setup<NH>(smem);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    pdl_wait();  // the selection and q of this step are complete from here on
   }
-  if (warp == kMma1B) {
-    tmem_alloc(smem_u32(tmem_slot), Ly::kTmemCols);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  pdl_wait();  // the selection and q of this step are complete from here on
 
   int2* meta = reinterpret_cast<int2*>(smem + Ly::kOffMeta);
   if (warp == kProdB) {
     // ================= TMA producer =================
-    run_producer<kStages>(a, bpc, full_bar(0), empty_bar(0), meta, 4u * B * 128u, abort_flag, err,
+    run_producer<kStages>(a, w, bpc, full_bar(0), empty_bar(0), meta, 4u * B * 128u, abort_flag, err,
                           [&](int s, int bi, int page) {
                             const uint32_t row_off = bi * B * 128;
                             const int y = page * B;
@@ -423,12 +488,12 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       const uint64_t vdesc = smem_desc(v_half(0, 0), kHalfBytes, 1024, 2);
       const uint64_t pdesc = smem_desc(p_buf(0), kPLbo, 128, 0);
       int c = 0, qi = 0;
-      int item = blockIdx.x;
-      Item it = item < a.items ? item_geom(a, item, bpc) : Item{};
+      int item = w.first;
+      Item it = item < a.items ? item_geom(a, item, bpc, w) : Item{};
       bool ok = true;
       while (ok && item < a.items && !*abort_flag) {
-        const int next = item + gridDim.x;
-        const Item nit = next < a.items ? item_geom(a, next, bpc) : Item{};  // in flight meanwhile
+        const int next = item + w.stride;
+        const Item nit = next < a.items ? item_geom(a, next, bpc, w) : Item{};  // in flight meanwhile
         if (it.nch > 0 && first) {
           ok = mbar_wait(q_full, qi & 1, abort_flag);
           ++qi;
@@ -496,20 +561,20 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       }
     };
     int c = 0;
-    int item = blockIdx.x;
+    int item = w.first;
     Item it{};
     uint4 qv[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
     if (item < a.items) {
-      it = item_geom(a, item, bpc);
+      it = item_geom(a, item, bpc, w);
       if (grp == 0) load_q(item, qv);
     }
     for (; item < a.items && !*abort_flag;) {
       // the next item's geometry and query rows are fetched while this one runs
-      const int next = item + gridDim.x;
+      const int next = item + w.stride;
       Item nit{};
       uint4 nqv[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
       if (next < a.items) {
-        nit = item_geom(a, next, bpc);
+        nit = item_geom(a, next, bpc, w);
         if (grp == 0) load_q(next, nqv);
       }
       const int64_t row0 = (static_cast<int64_t>(it.b) * a.hq + it.kvh * g) * a.splits + it.split;
@@ -648,30 +713,45 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         if (grp == 1) {
 #pragma unroll
           for (int h = 0; h < NH; ++h) xo[h * 128 + t] = oacc[h];
-          if (t < NH) {
-            xm[t] = m[t];
-            xl[t] = rs[t] + rs[NH + t] + rs[2 * NH + t] + rs[3 * NH + t];
+#pragma unroll
+          for (int h = 0; h < NH; ++h) {  // compile-time indices keep m[] in registers
+            if (t == h) {
+              xm[h] = m[h];
+              xl[h] = rs[h] + rs[NH + h] + rs[2 * NH + h] + rs[3 * NH + h];
+            }
           }
         }
         named_barrier(3, 256);
         if (grp == 0) {
-          for (int h = 0; h < g && h < NH; ++h) {
-            const float l0 = rs[h] + rs[NH + h] + rs[2 * NH + h] + rs[3 * NH + h];
-            const float m1 = xm[h], l1 = xl[h];
-            const float mx = fmaxf(m[h], m1);
-            const float e0 = m[h] == -INFINITY ? 0.0f : exp2f(m[h] - mx);
-            const float e1 = m1 == -INFINITY ? 0.0f : exp2f(m1 - mx);
-            const float lt = l0 * e0 + l1 * e1;
-            const float ot = oacc[h] * e0 + xo[h * 128 + t] * e1;
-            put_partial(a, row0, h, t, lt > 0.0f ? ot / lt : 0.0f,
-                        lt > 0.0f ? (mx + log2f(lt)) * kLn2 : -INFINITY);
+#pragma unroll
+          for (int h = 0; h < NH; ++h) {  // unrolled: the heads' chains overlap
+            if (h < g) {
+              const float l0 = rs[h] + rs[NH + h] + rs[2 * NH + h] + rs[3 * NH + h];
+              const float m1 = xm[h], l1 = xl[h];
+              const float mx = fmaxf(m[h], m1);
+              const float e0 = m[h] == -INFINITY ? 0.0f : exp2f(m[h] - mx);
+              const float e1 = m1 == -INFINITY ? 0.0f : exp2f(m1 - mx);
+              const float lt = l0 * e0 + l1 * e1;
+              const float ot = oacc[h] * e0 + xo[h * 128 + t] * e1;
+              const float o = lt > 0.0f ? ot / lt : 0.0f;
+              const float lse = lt > 0.0f ? (mx + log2f(lt)) * kLn2 : -INFINITY;
+              if constexpr (PART_SMEM) {
+                emit(h, t, o, lse);
+              } else {
+                put_partial(a, row0, h, t, o, lse);
+              }
+            }
           }
-          if (a.splits > 1 && a.counters) merge_if_last(a, it, t, bar, s_last);
+          if (!PART_SMEM && a.splits > 1 && a.counters) merge_if_last(a, it, t, bar, s_last);
         }
         named_barrier(3, 256);  // the exchange buffer is free again
       } else if (grp == 0) {
-        for (int h = 0; h < g; ++h) put_partial(a, row0, h, t, 0.0f, -INFINITY);
-        if (a.splits > 1 && a.counters) merge_if_last(a, it, t, bar, s_last);
+        if constexpr (PART_SMEM) {
+          for (int h = 0; h < g; ++h) emit(h, t, 0.0f, -INFINITY);
+        } else {
+          for (int h = 0; h < g; ++h) put_partial(a, row0, h, t, 0.0f, -INFINITY);
+          if (a.splits > 1 && a.counters) merge_if_last(a, it, t, bar, s_last);
+        }
       }
       item = next;
       it = nit;
@@ -687,6 +767,294 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   if (warp == kMma1B) {
     tc_fence_after();
     tmem_dealloc(tmem, Ly::kTmemCols);
+  }
+}
+
+template <int NH>
+__global__ void __launch_bounds__(kThreadsB, 1)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                   TcArgs a, unsigned* err) {
+  attn_bf16_cta<NH>(&tm_k, &tm_v, a, persistent_work(), err);
+}
+
+
+// ============================================================================
+// Bound scoring + selection + attention of one decode step in one launch
+// ("KV 稀疏化" wiki §5 Quest and §2 sink/window, then the attention above),
+// bf16 K/V and summaries, head_dim 128, g <= 8, when every (request, kv head)
+// fits one wave: one cluster of F CTAs per (request, kv head), F = max(tiles
+// of 128 blocks, attention splits) <= 8.
+//   phase 1  CTA r scores tile r of the pair (TMA of its summary rows, 16
+//            MMAs, max over the group) and stores the scores (and the range
+//            of their keys) into the shared memory of every CTA of the
+//            cluster, and into scores_opt; meanwhile every CTA stages the
+//            pair's page-table row (and score history), and rank 0 asks L2
+//            for the K/V pages of the forced blocks.
+//   phase 2  after one cluster barrier every CTA smooths and selects on its
+//            own copy - the same selection as the selection kernels; rank 0
+//            stores it (and the history) - and resolves the blocks of its
+//            own split, whole 128-token chunks spread evenly over the splits,
+//            to (page, valid tokens).
+//   phase 3  CTA r is the attention CTA of split r (a one-item Work).
+// Nothing waits on another cluster, and no CTA touches another's shared
+// memory after the cluster barrier.
+constexpr int kFuseMaxCluster = 8;
+constexpr int kFuseList = 256;   // selected blocks of one split held in shared memory
+constexpr int kPushSlots = 13;   // (split, head) results one CTA merges
+constexpr int kFuseMaxBlocks = kFuseMaxCluster * bound::kTile;
+// scratch of phases 1-2 inside the K/V ring, which is unused until phase 3
+constexpr int kFTile = 0;                                       // summary tile
+constexpr int kFQ = kFTile + bound::kTileBytes;                 // [Q+ | Q-]
+constexpr int kFScores = kFQ + bound::kQBytes;                  // the pair's scores
+constexpr int kFPrev = kFScores + kFuseMaxBlocks * 4;           // the pair's score history
+constexpr int kFHist = kFPrev + kFuseMaxBlocks * 4;             // radix histograms
+constexpr int kFWarp = kFHist + 3 * sel::kHistWords * 4;        // per-warp counts
+constexpr int kFRange = kFWarp + 128;                           // key range per scoring warp
+constexpr int kFPt = kFRange + 2 * 4 * kFuseMaxCluster * 4;     // the pair's page-table row
+constexpr int kFSel = kFPt + kFuseMaxBlocks * 4;                // the selection
+static_assert(kFSel + kFuseMaxBlocks * 4 <= kStages * kStageBytes, "scratch exceeds the ring");
+
+template <int NH>
+struct FuseLayout {
+  static constexpr int kOffF = (Layout<NH>::kBytes + 15) / 16 * 16;
+  static constexpr int kOffBar = kOffF;       // tile full, q full, accumulator full
+  static constexpr int kOffMisc = kOffF + 32;  // abort flag
+  static constexpr int kOffList = kOffF + 48;  // int2[kFuseList]: (page, valid tokens) of this CTA's split
+  static constexpr int kOffPush = kOffList + kFuseList * 8;  // [kPushSlots][128] o, then [kPushSlots] lse
+  static constexpr int kBytes = kOffPush + (kPushSlots * 129 * 4 + 15) / 16 * 16;
+  static constexpr int kAlloc = (kBytes + 1024 + 127) / 128 * 128;
+  static_assert(kAlloc <= 232448, "fused shared memory layout too large");
+};
+
+struct FuseArgs {
+  float* scores;  // nullable: the bound scores also go to global memory
+  const uint8_t* k_pages;  // for the L2 prefetch of the forced blocks
+  const uint8_t* v_pages;
+  int tiles;    // 128-block tiles per (request, kv head)
+  int cluster;  // CTAs per (request, kv head)
+};
+
+// Sends a split's result for head h to the CTA that merges it: CTA h / hp,
+// slot (split, h % hp) of its push buffer.
+struct ClusterPush {
+  float* buf;  // the push buffer (same offset in every CTA of the cluster)
+  int hp, split;
+  __device__ __forceinline__ void operator()(int h, int c, float o, float lse) const {
+    float* dst = cg::this_cluster().map_shared_rank(buf, static_cast<unsigned>(h / hp));
+    const int slot = split * hp + h % hp;
+    dst[slot * 128 + c] = o;
+    if (c == 0) dst[kPushSlots * 128 + slot] = lse;
+  }
+};
+
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait;" ::: "memory"); }
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
+               : "memory");
+}
+
+template <int NH>
+__global__ void __launch_bounds__(kThreadsB, 1)
+    score_select_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                             const __grid_constant__ CUtensorMap tm_smax, const __grid_constant__ CUtensorMap tm_smin,
+                             TcArgs a, SelectArgs sa, FuseArgs f, unsigned* err) {
+  using FL = FuseLayout<NH>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t tile_full = sbase + FL::kOffBar, q_full = tile_full + 8, acc_full = tile_full + 16;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + FL::kOffMisc);
+  int2* s_list = reinterpret_cast<int2*>(smem + FL::kOffList);
+  float* s_scores = reinterpret_cast<float*>(smem + kFScores);
+  float* s_prev = reinterpret_cast<float*>(smem + kFPrev);
+  auto s_hist = reinterpret_cast<uint32_t(*)[sel::kHistWords]>(smem + kFHist);
+  int* s_warp = reinterpret_cast<int*>(smem + kFWarp);
+  uint32_t* s_range = reinterpret_cast<uint32_t*>(smem + kFRange);
+  int* s_pt = reinterpret_cast<int*>(smem + kFPt);
+  int* s_sel = reinterpret_cast<int*>(smem + kFSel);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = static_cast<int>(cluster.block_rank());
+  const int pair = blockIdx.x / f.cluster;
+  const int b = pair / a.hkv, kvh = pair - b * a.hkv;
+  const int g = a.group;
+  const bool smoothed = sa.history_weight != 0.0f && sa.history != nullptr;
+
+  pdl_trigger();
+  // barriers of phase 1, and the attention's barriers and TMEM (its S
+  // columns hold the bound accumulator in phase 1); the four tensor maps
+  if (warp == kProdB && lane == 0) {
+    prefetch_tmap(&tm_smax);
+    prefetch_tmap(&tm_smin);
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
+  }
+  if (tid == 0) {
+    mbar_init(tile_full, 1);
+    mbar_init(q_full, 128);
+    mbar_init(acc_full, 1);
+    *abort_flag = 0;
+  }
+  attn_bf16_setup<NH>(smem);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<uint32_t*>(smem + Layout<NH>::kOffMisc);
+  cluster_arrive_relaxed();  // completes once every CTA of the cluster runs
+  pdl_wait();  // q, the summaries, seq_lens, the page table and the history of this step are complete
+
+  // the summary tile is requested before the request's length is known (rows
+  // past its blocks are never used)
+  if (warp == kProdB && lane == 0 && rank < f.tiles) {
+    mbar_arrive_tx(tile_full, bound::kTileBytes);
+    const int y = pair * a.max_blocks + rank * bound::kTile;
+    const uint32_t st = sbase + kFTile;
+    tma_load_2d(st, &tm_smax, 0, y, tile_full);
+    tma_load_2d(st + bound::kHalf, &tm_smax, 64, y, tile_full);
+    tma_load_2d(st + 2 * bound::kHalf, &tm_smin, 0, y, tile_full);
+    tma_load_2d(st + 3 * bound::kHalf, &tm_smin, 64, y, tile_full);
+  }
+  const int L = max(a.seq_lens[b], 0);
+  int nb = (L + a.block - 1) / a.block;
+  if (nb > a.max_blocks) {
+    if (tid == 0 && rank == 0) set_error(err, HS_EBIT_BLOCK_RANGE);
+    nb = a.max_blocks;
+  }
+  const bool has_tile = rank < f.tiles && rank * bound::kTile < nb;
+  const int32_t* pt = a.page_table + static_cast<int64_t>(pair) * a.max_blocks;
+
+  // ---- phase 1: bound scores of tile `rank` ----
+  if (warp == kMma1B) {
+    if (lane == 0 && has_tile && mbar_wait(q_full, 0, abort_flag) && mbar_wait(tile_full, 0, abort_flag)) {
+      tc_fence_after();
+      bound::issue_mmas(tmem, sbase + kFTile, sbase + kFQ);
+      mma_commit(acc_full);
+    }
+  } else if (warp < 4) {
+    if (has_tile) {
+      bound::write_q(smem + kFQ, a.q, static_cast<int64_t>(b) * a.hq + kvh * g, g, tid);
+      fence_async_smem();
+      mbar_arrive(q_full);
+    }
+  } else if (warp < 8) {
+    // the pair's page-table row and score history, cleared histograms
+    const int t = tid - 128;
+    for (int j = t; j < nb; j += 128) s_pt[j] = pt[j];
+    if (smoothed) {
+      const float* h = sa.history + static_cast<int64_t>(pair) * a.max_blocks;
+      for (int j = t; j < nb; j += 128) s_prev[j] = h[j];
+    }
+    for (int i = t; i < sel::kHistWords; i += 128) s_hist[0][i] = 0u;
+  } else if (warp == kMma2B && rank == 0) {
+    // K/V pages of the forced blocks (sink, window) into L2 ahead of phase 3
+    const int B = a.block;
+    const int n_sink = min(nb, ceil_div(sa.sink_tokens, B));
+    int w_first = nb;
+    if (sa.window_tokens > 0) w_first = (L - sa.window_tokens <= 0) ? 0 : min(nb, (L - sa.window_tokens) / B);
+    w_first = max(w_first, n_sink);
+    const int nf = n_sink + (nb - w_first);
+    const uint32_t page_bytes = static_cast<uint32_t>(B) * kD * 2;
+    for (int i = lane; i < nf; i += 32) {
+      const int j = i < n_sink ? i : w_first + (i - n_sink);
+      const int page = pt[j];
+      if (page >= 0 && page < a.num_pages) {
+        prefetch_l2(f.k_pages + static_cast<int64_t>(page) * page_bytes, page_bytes);
+        prefetch_l2(f.v_pages + static_cast<int64_t>(page) * page_bytes, page_bytes);
+      }
+    }
+  }
+  cluster_wait();  // every CTA of the cluster runs: its shared memory is addressable
+  if (warp < 4 && has_tile) {
+    float best = -INFINITY;
+    if (mbar_wait(acc_full, 0, abort_flag)) {
+      tc_fence_after();
+      float u[16];
+      tmem_ld16(tmem + (static_cast<uint32_t>(warp * 32) << 16), u);
+      tc_fence_before();
+#pragma unroll
+      for (int h = 0; h < 16; ++h)
+        if (h < g) best = fmaxf(best, u[h]);
+    }
+    const int j = rank * bound::kTile + tid;
+    if (j < nb && f.scores) f.scores[static_cast<int64_t>(pair) * a.max_blocks + j] = best;
+    for (int r = 0; r < f.cluster; ++r) {  // every CTA of the cluster gets the tile's scores
+      if (j < nb) cluster.map_shared_rank(s_scores, r)[j] = best;
+      sel::warp_key_range(best, j < nb, cluster.map_shared_rank(s_range, r), rank * 4 + warp);
+    }
+  }
+  if (warp == kProdB && lane == 0 && rank < f.tiles)  // the tile has landed before the ring is reused
+    mbar_wait(tile_full, 0, abort_flag, 500000000ull);
+  cluster.sync();  // every CTA holds all scores; no shared memory of another CTA is touched after this
+
+  // ---- phase 2: every CTA selects; rank 0 stores the selection ----
+  if (smoothed) sel::smooth_staged(s_scores, s_prev, nb, a.max_blocks, sa, pair, rank == 0);
+  const int n = sel::select_pair<kThreadsB>(s_scores, nb, L, a.block, sa, pair, s_hist, s_warp, err, s_sel,
+                                            smoothed ? nullptr : s_range, 4 * ceil_div(nb, bound::kTile),
+                                            rank == 0);
+  __syncthreads();  // the shared copy of the selection is complete
+  const int bpc = kChunk / a.block;
+  const int per = split_len(n, bpc, a.splits, a.bps);
+  const int s0 = min(n, rank * per), s1 = min(n, s0 + per);
+  unsigned bad = 0;
+  for (int p = s0 + tid; p < s1 && rank < a.splits; p += kThreadsB) {
+    const int j = s_sel[p];
+    int2 e = make_int2(-1, 0);
+    if (j < 0 || j >= nb) {
+      bad |= HS_EBIT_BLOCK_RANGE;
+    } else {
+      const int page = s_pt[j];
+      if (page < 0 || page >= a.num_pages)
+        bad |= HS_EBIT_PAGE_RANGE;
+      else
+        e = make_int2(page, min(a.block, L - j * a.block));
+    }
+    s_list[p - s0] = e;
+  }
+  if (bad) set_error(err, bad);
+  if (*abort_flag && tid == 0) set_error(err, HS_EBIT_TIMEOUT);
+  fence_async_smem();  // the scratch's generic writes before the ring's TMA writes
+  __syncthreads();
+
+  // ---- phase 3: attention over split `rank`; its result per head goes to
+  // the push buffer of the CTA that merges that head ----
+  const int hp = (g + f.cluster - 1) / f.cluster;  // heads merged per CTA
+  float* push = reinterpret_cast<float*>(smem + FL::kOffPush);
+  const Work w{rank < a.splits ? pair * a.splits + rank : a.items, a.items, s_list, s0, s1, L};
+  attn_bf16_cta<NH, false, ClusterPush>(&tm_k, &tm_v, a, w, err, ClusterPush{push, hp, rank});
+
+  // ---- phase 4: the splits' log-sum-exp merge inside the cluster
+  // ("分块稀疏注意力与KV Cache量化" §2.2), the same arithmetic in the same
+  // order as the merge kernel; CTA r merges heads r*hp .. r*hp+hp-1 from its
+  // own push buffer ----
+  cluster.sync();  // every split's results are in the merging CTAs' push buffers
+  {
+    const int S = a.splits;
+    for (int idx = tid; idx < hp * 128; idx += kThreadsB) {
+      const int hl = idx / 128, c = idx % 128, h = rank * hp + hl;
+      if (h >= g) break;
+      float M = -INFINITY;
+      for (int sp = 0; sp < S; ++sp) M = fmaxf(M, push[kPushSlots * 128 + sp * hp + hl]);
+      float acc = 0.0f, lse = -INFINITY;
+      if (M != -INFINITY) {
+        float tot = 0.0f;
+        for (int sp = 0; sp < S; ++sp) {
+          const float wgt = expf(push[kPushSlots * 128 + sp * hp + hl] - M);
+          tot += wgt;
+          acc = wgt > 0.0f ? fmaf(wgt, push[(sp * hp + hl) * 128 + c], acc) : acc;
+        }
+        acc = acc / tot;
+        lse = M + logf(tot);
+      }
+      const int64_t orow = static_cast<int64_t>(b) * a.hq + static_cast<int64_t>(kvh) * g + h;
+      if (a.out_f32)
+        static_cast<float*>(a.out)[orow * kD + c] = acc;
+      else
+        static_cast<__nv_bfloat16*>(a.out)[orow * kD + c] = __float2bfloat16_rn(acc);
+      if (a.lse_out && c == 0) a.lse_out[orow] = lse;
+    }
   }
 }
 
@@ -759,6 +1127,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                        TcArgs a, unsigned* err) {
   using Ly = Layout8;
   constexpr int NH = 8;
+  const Work w = persistent_work();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -787,6 +1156,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int bpc = kChunk / B;
 
   pdl_trigger();
+  if (warp == kProducerWarp && lane == 0) {
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
+  }
   if (tid == 0) {
     for (int s = 0; s < kStages8; ++s) {
       mbar_init(full_bar(s), 1);
@@ -817,7 +1190,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   int2* meta = reinterpret_cast<int2*>(smem + Ly::kOffMeta);
   if (warp == kProducerWarp) {
-    run_producer<kStages8>(a, bpc, full_bar(0), empty_bar(0), meta, 2u * B * 128u + 2u * B * 16u, abort_flag, err,
+    run_producer<kStages8>(a, w, bpc, full_bar(0), empty_bar(0), meta, 2u * B * 128u + 2u * B * 16u, abort_flag, err,
                            [&](int s, int bi, int page) {
                              const int y = page * B;
                              tma_load_2d(smem_u32(kc_stage(s)) + bi * B * 128, &tm_k, 0, y, full_bar(s));
@@ -837,12 +1210,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t vdesc = smem_desc(sbase + Ly::kOffVbf, kHalfBytes, 1024, 2);
       const uint64_t pdesc = smem_desc(sbase + Ly::kOffP, 1024, 128, 0);
       int c = 0, qi = 0, last_g2 = -1;
-      int item = blockIdx.x;
-      Item it = item < a.items ? item_geom(a, item, bpc) : Item{};
+      int item = w.first;
+      Item it = item < a.items ? item_geom(a, item, bpc, w) : Item{};
       bool ok = true;
       while (ok && item < a.items && !*abort_flag) {
-        const int next = item + gridDim.x;
-        const Item nit = next < a.items ? item_geom(a, next, bpc) : Item{};
+        const int next = item + w.stride;
+        const Item nit = next < a.items ? item_geom(a, next, bpc, w) : Item{};
         if (it.nch > 0 && first) {
           ok = mbar_wait(q_full, qi & 1, abort_flag);
           ++qi;
@@ -890,8 +1263,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ct = tid - (is_k ? kConvWarp0 : kConvVWarp0) * 32;  // row of the chunk
     int c = 0;
     bool ok = true;
-    for (int item = blockIdx.x; ok && item < a.items && !*abort_flag; item += gridDim.x) {
-      const Item it = item_geom(a, item, bpc);
+    for (int item = w.first; ok && item < a.items && !*abort_flag; item += w.stride) {
+      const Item it = item_geom(a, item, bpc, w);
       for (int ci = 0; ci < it.nch; ++ci, ++c) {
         const int s = c % kStages8;
         const bool prev_done = c == 0 || (is_k ? mbar_wait(s_full((c - 1) & 1), ((c - 1) >> 1) & 1, abort_flag)
@@ -929,21 +1302,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                  half * 64 + ch * 8);
       }
     };
-    int item = blockIdx.x;
+    int item = w.first;
     Item it{};
     uint4 qv[4];
     if (item < a.items) {
-      it = item_geom(a, item, bpc);
+      it = item_geom(a, item, bpc, w);
       load_q(item, qv);
     }
     for (; item < a.items && !*abort_flag;) {
-      const int next = item + gridDim.x;
+      const int next = item + w.stride;
       Item nit{};
       uint4 nqv[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) nqv[i] = make_uint4(0, 0, 0, 0);
       if (next < a.items) {
-        nit = item_geom(a, next, bpc);
+        nit = item_geom(a, next, bpc, w);
         load_q(next, nqv);
       }
       const int64_t row0 = (static_cast<int64_t>(it.b) * a.hq + it.kvh * g) * a.splits + it.split;
@@ -1200,6 +1573,56 @@ cudaError_t launch_nh(const KvView& kv, AttnArgs& aa, unsigned* err, cudaStream_
 }
 
 }  // namespace
+
+bool score_select_attn_supported(const KvView& kv, const AttnArgs& aa, int sms) {
+  if (kv.kv_dtype != HS_KV_BF16 || kv.group > 8 || !attn_tc_supported(kv)) return false;
+  const int tiles = (kv.max_blocks + bound::kTile - 1) / bound::kTile;
+  const int f = tiles > aa.splits ? tiles : aa.splits;
+  const int64_t pairs = static_cast<int64_t>(kv.batch) * kv.hkv;
+  if (f > kFuseMaxCluster || pairs * f > sms || aa.blocks_per_split > kFuseList) return false;
+  if (aa.splits * ((kv.group + f - 1) / f) > kPushSlots) return false;  // the merging CTAs' push buffers
+  return pairs * kv.max_blocks < (int64_t(1) << 31);
+}
+
+cudaError_t launch_score_select_attn(const KvView& kv, const void* smin, const void* smax, const SelectArgs& sa,
+                                     AttnArgs& aa, unsigned* err, cudaStream_t st) {
+  using FL = FuseLayout<8>;
+  const int64_t pairs = static_cast<int64_t>(kv.batch) * kv.hkv;
+  if (pairs == 0) return cudaSuccess;
+  CUtensorMap mk, mv, mmax, mmin;
+  const int64_t rows = kv.num_pages * kv.block;
+  if (rows <= 0) return cudaErrorInvalidValue;
+  if (!make_map(&mk, kv.k_pages, rows, kv.block) || !make_map(&mv, kv.v_pages, rows, kv.block) ||
+      !make_map(&mmax, smax, pairs * kv.max_blocks, bound::kTile) ||
+      !make_map(&mmin, smin, pairs * kv.max_blocks, bound::kTile))
+    return cudaErrorInvalidValue;
+  const TcArgs a = make_args(kv, aa);
+  FuseArgs f;
+  f.scores = sa.scores;
+  f.k_pages = static_cast<const uint8_t*>(kv.k_pages);
+  f.v_pages = static_cast<const uint8_t*>(kv.v_pages);
+  f.tiles = (kv.max_blocks + bound::kTile - 1) / bound::kTile;
+  f.cluster = f.tiles > aa.splits ? f.tiles : aa.splits;
+  auto kern = score_select_attn_kernel<8>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, FL::kAlloc);
+  if (e != cudaSuccess) return e;
+  aa.merged = 1;  // the cluster merges its splits
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(pairs * f.cluster));
+  cfg.blockDim = dim3(kThreadsB);
+  cfg.dynamicSmemBytes = FL::kAlloc;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = f.cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kern, mk, mv, mmax, mmin, a, sa, f, err);
+}
 
 bool attn_tc_supported(const KvView& kv) {
   if (kv.head_dim != kD) return false;

@@ -19,6 +19,7 @@
 #include <cooperative_groups.h>
 #include <cuda.h>
 
+#include "bound_tile.cuh"
 #include "hs_internal.h"
 #include "select_pair.cuh"
 #include "tc_ptx.cuh"
@@ -31,14 +32,13 @@ namespace {
 using namespace tc;
 
 constexpr int kD = 128;
-constexpr int kTile = 128;                   // blocks per tile (MMA M)
+constexpr int kTile = bound::kTile;           // blocks per tile (MMA M)
 constexpr int kStages = 3;
 constexpr int kThreads = 192;
 constexpr int kProducerWarp = 4, kMmaWarp = 5;
-constexpr int kHalf = kTile * 128;            // 128 rows x 64 bf16
-constexpr int kStageBytes = 4 * kHalf;        // smax halves, smin halves
-constexpr int kQHalf = 16 * 128;              // 16 heads x 64 bf16
-constexpr int kQBytes = 4 * kQHalf;           // Q+ halves, Q- halves
+constexpr int kHalf = bound::kHalf;
+constexpr int kStageBytes = bound::kTileBytes;
+constexpr int kQBytes = bound::kQBytes;
 constexpr int kOffQ = kStages * kStageBytes;
 constexpr int kOffBar = kOffQ + 2 * kQBytes;
 constexpr int kNumBars = 2 * kStages + 8;
@@ -86,6 +86,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   pdl_trigger();
+  if (warp == kProducerWarp && lane == 0) {
+    prefetch_tmap(&tm_max);
+    prefetch_tmap(&tm_min);
+  }
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(full_bar(s), 1);
@@ -134,9 +138,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16(128, 16, false, false);
-      const uint64_t adesc = smem_desc(sbase, 16, 1024, 2);
-      const uint64_t bdesc = smem_desc(sbase + kOffQ, 16, 1024, 2);
       int n = 0;
       for (int item = blockIdx.x; item < a.items && !*abort_flag; item += gridDim.x) {
         int pair, tile, nb;
@@ -146,13 +147,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(full_bar(s), (n / kStages) & 1, abort_flag)) break;
         if (n >= 2 && !mbar_wait(acc_free(b), ((n >> 1) + 1) & 1, abort_flag)) break;
         tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {  // k < 8: Smax . Q+, k >= 8: Smin . Q-
-          const int part = k >> 3, h = (k >> 2) & 1, kk = k & 3;
-          const uint32_t aoff = s * kStageBytes + (2 * part + h) * kHalf + kk * 32;
-          const uint32_t boff = b * kQBytes + (2 * part + h) * kQHalf + kk * 32;
-          mma_f16(tmem + b * 16, adesc + (aoff >> 4), bdesc + (boff >> 4), idesc, k > 0 ? 1u : 0u);
-        }
+        bound::issue_mmas(tmem + b * 16, sbase + s * kStageBytes, sbase + kOffQ + b * kQBytes);
         mma_commit(acc_full(b));
         mma_commit(empty_bar(s));
         mma_commit(q_free(b));
@@ -165,32 +160,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t = tid;
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     const int g = a.group;
-    // [Q+ | Q-] of a (request, kv head): thread t writes 16-byte pieces of head
-    // row t/8 (zero rows past g), 128-byte swizzle like the TMA tiles
+    // [Q+ | Q-] of a (request, kv head)
     auto write_q = [&](int pair, int b) {
       const int bq = pair / a.hkv, kvh = pair - bq * a.hkv;
-      const int n = t >> 3, ch = t & 7;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (n < g)
-          v = *reinterpret_cast<const uint4*>(a.q + (static_cast<int64_t>(bq) * a.hq + kvh * g + n) * kD + h * 64 +
-                                              ch * 8);
-        uint32_t w[4] = {v.x, v.y, v.z, v.w}, pos[4], neg[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          // bf16 pair: keep the positive (negative) halves, zero the others
-          const uint32_t lo = w[i] & 0xffffu, hi = w[i] >> 16;
-          const bool lneg = (lo & 0x8000u) != 0, hneg = (hi & 0x8000u) != 0;
-          pos[i] = (lneg ? 0u : lo) | ((hneg ? 0u : hi) << 16);
-          neg[i] = (lneg ? lo : 0u) | ((hneg ? hi : 0u) << 16);
-        }
-        const int off = n * 128 + ((ch ^ (n & 7)) << 4);
-        *reinterpret_cast<uint4*>(smem + kOffQ + b * kQBytes + h * kQHalf + off) =
-            make_uint4(pos[0], pos[1], pos[2], pos[3]);
-        *reinterpret_cast<uint4*>(smem + kOffQ + b * kQBytes + (2 + h) * kQHalf + off) =
-            make_uint4(neg[0], neg[1], neg[2], neg[3]);
-      }
+      bound::write_q(smem + kOffQ + b * kQBytes, a.q, static_cast<int64_t>(bq) * a.hq + kvh * g, g, t);
     };
     int n = 0;
     int item = blockIdx.x;
@@ -242,10 +215,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     cg::cluster_group cluster = cg::this_cluster();
     cluster.sync();
     if (cluster.block_rank() == 0) {
-      float* s_scores = reinterpret_cast<float*>(smem);                              // <= 16 tiles x 128
-      uint32_t(*s_hist)[256] = reinterpret_cast<uint32_t(*)[256]>(smem + 65536);  // 2 x 256
-      int* s_warp = reinterpret_cast<int*>(smem + 65536 + 2048);                     // kThreads / 32 + 1
-      int* s_pick = s_warp + 16;
+      float* s_scores = reinterpret_cast<float*>(smem);  // <= 16 tiles x 128
+      auto s_hist = reinterpret_cast<uint32_t(*)[sel::kHistWords]>(smem + 65536);  // 3 buffers
+      int* s_warp = reinterpret_cast<int*>(smem + 65536 + 4096);                    // kThreads / 32
+      uint32_t* s_range = reinterpret_cast<uint32_t*>(smem + 65536 + 4096 + 128);   // 2 per warp
       const int pair = blockIdx.x / a.tiles;
       const int b = pair / a.hkv;
       const int L = max(a.seq_lens[b], 0);
@@ -255,11 +228,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         nb = a.max_blocks;
       }
       const float* src = a.scores + static_cast<int64_t>(pair) * a.max_blocks;
-      for (int j = tid; j < nb; j += kThreads) s_scores[j] = __ldcg(src + j);
-      for (int i = tid; i < 512; i += kThreads) s_hist[i >> 8][i & 255] = 0u;
+      uint32_t lo = 0xffffffffu, hi = 0u;  // per warp: the range of the keys
+      for (int j0 = 0; j0 < nb; j0 += kThreads) {
+        const int j = j0 + tid;
+        if (j < nb) {
+          const float v = __ldcg(src + j);
+          s_scores[j] = v;
+          lo = min(lo, score_key(v));
+          hi = max(hi, score_key(v));
+        }
+      }
+      lo = __reduce_min_sync(0xffffffffu, lo);
+      hi = __reduce_max_sync(0xffffffffu, hi);
+      if (lane == 0) {
+        s_range[2 * warp] = lo;
+        s_range[2 * warp + 1] = hi;
+      }
+      for (int i = tid; i < sel::kHistWords; i += kThreads) s_hist[0][i] = 0u;
       __syncthreads();
+      const bool smoothed = sa.history_weight != 0.0f && sa.history != nullptr;  // the range no longer holds
       sel::smooth_scores(s_scores, nb, a.max_blocks, sa, pair);
-      sel::select_pair<kThreads>(s_scores, nb, L, a.block, sa, pair, s_hist, s_warp, s_pick, err);
+      sel::select_pair<kThreads>(s_scores, nb, L, a.block, sa, pair, s_hist, s_warp, err, nullptr,
+                                 smoothed ? nullptr : s_range, kThreads / 32);
     }
   }
   if (*abort_flag && tid == 0) set_error(err, HS_EBIT_TIMEOUT);

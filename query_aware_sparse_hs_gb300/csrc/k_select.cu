@@ -6,10 +6,8 @@
 // heads of the kv head and stores the scores straight into the shared memory
 // of CTA rank 0 (distributed shared memory), so the selection never round-trips
 // through global memory.  After the cluster barrier, rank 0 finds the k-th
-// largest score of the non-forced blocks with a 4-pass 8-bit radix select in
-// shared memory, then writes forced + chosen blocks in ascending order with two
-// block-wide scans (equal-score ranks for the lower-index tie rule, then output
-// positions).
+// largest score of the non-forced blocks with an 8-bit radix select in shared
+// memory, then writes forced + chosen blocks in ascending order (select_pair.cuh).
 //
 // Bound:  U_h(j) = sum_d max(q_hd * smax_jd, q_hd * smin_jd)
 //               = sum_d q+_hd * smax_jd + q-_hd * smin_jd,  q+ = max(q,0), q- = min(q,0)
@@ -58,9 +56,8 @@ template <int C, int G, bool F32>
 __global__ void __cluster_dims__(kSelectCluster, 1, 1) __launch_bounds__(kThreads, (G * C <= 32) ? 2 : 1)
     score_select_kernel(KvView kv, SelectArgs a, unsigned* err) {
   extern __shared__ float s_scores[];  // [max_blocks]; rank 0's copy holds every score
-  __shared__ uint32_t s_hist[2][256];
+  __shared__ uint32_t s_hist[3][kHistWords];
   __shared__ int s_warp[kWarps + 1];
-  __shared__ int s_pick[2];
 
   pdl_trigger();
   pdl_wait();
@@ -161,12 +158,12 @@ __global__ void __cluster_dims__(kSelectCluster, 1, 1) __launch_bounds__(kThread
       }
     }
   }
-  for (int i = tid; i < 512; i += kThreads) s_hist[i >> 8][i & 255] = 0u;
+  for (int i = tid; i < kHistWords; i += kThreads) s_hist[0][i] = 0u;
   cluster.sync();
   if (rank != 0) return;
 
   smooth_scores(s_scores, nb, kv.max_blocks, a, pair);
-  select_pair<kThreads>(s_scores, nb, L, B, a, pair, s_hist, s_warp, s_pick, err);
+  select_pair<kThreads>(s_scores, nb, L, B, a, pair, s_hist, s_warp, err);
 }
 
 // One CTA per (request, kv head): scores already in global memory (written by
@@ -176,9 +173,9 @@ __global__ __launch_bounds__(THREADS) void select_only_kernel(KvView kv, SelectA
                                                               unsigned* err) {
   constexpr int kWarps = THREADS / 32;
   extern __shared__ float s_scores[];
-  __shared__ uint32_t s_hist[2][256];
-  __shared__ int s_warp[kWarps + 1];
-  __shared__ int s_pick[2];
+  __shared__ uint32_t s_hist[3][kHistWords];
+  __shared__ int s_warp[kWarps];
+  __shared__ uint32_t s_range[2 * kWarps];
   pdl_trigger();
   pdl_wait();
   const int tid = threadIdx.x;
@@ -192,11 +189,29 @@ __global__ __launch_bounds__(THREADS) void select_only_kernel(KvView kv, SelectA
     nb = kv.max_blocks;
   }
   const float* src = scores + pair * kv.max_blocks;
-  for (int j = tid; j < nb; j += THREADS) s_scores[j] = src[j];
-  for (int i = tid; i < 512; i += THREADS) s_hist[i >> 8][i & 255] = 0u;
+  // the scores, and per warp the range of their keys
+  uint32_t lo = 0xffffffffu, hi = 0u;
+  for (int j0 = 0; j0 < nb; j0 += THREADS) {
+    const int j = j0 + tid;
+    if (j < nb) {
+      const float v = src[j];
+      s_scores[j] = v;
+      lo = min(lo, score_key(v));
+      hi = max(hi, score_key(v));
+    }
+  }
+  lo = __reduce_min_sync(0xffffffffu, lo);
+  hi = __reduce_max_sync(0xffffffffu, hi);
+  if ((tid & 31) == 0) {
+    s_range[2 * (tid >> 5)] = lo;
+    s_range[2 * (tid >> 5) + 1] = hi;
+  }
+  for (int i = tid; i < kHistWords; i += THREADS) s_hist[0][i] = 0u;
   __syncthreads();
+  const bool smoothed = a.history_weight != 0.0f && a.history != nullptr;  // the range no longer holds
   smooth_scores(s_scores, nb, kv.max_blocks, a, pair);
-  select_pair<THREADS>(s_scores, nb, L, B, a, pair, s_hist, s_warp, s_pick, err);
+  select_pair<THREADS>(s_scores, nb, L, B, a, pair, s_hist, s_warp, err, nullptr, smoothed ? nullptr : s_range,
+                       kWarps);
 }
 
 template <int C, int G, bool F32>

@@ -9,38 +9,6 @@
 namespace hs {
 namespace sel {
 
-// Exclusive prefix sum over a CTA of THREADS threads (at most 1024); `total`
-// receives the CTA-wide sum.  s_warp holds THREADS / 32 + 1 ints.
-template <int THREADS>
-__device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int& total) {
-  constexpr int kWarps = THREADS / 32;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int incl = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    int n = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += n;
-  }
-  if (lane == 31) s_warp[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    int w = lane < kWarps ? s_warp[lane] : 0;
-    int wi = w;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      int n = __shfl_up_sync(0xffffffffu, wi, o);
-      if (lane >= o) wi += n;
-    }
-    if (lane < kWarps) s_warp[lane] = wi - w;
-    if (lane == kWarps - 1) s_warp[kWarps] = wi;
-  }
-  __syncthreads();
-  const int excl = s_warp[warp] + incl - v;
-  total = s_warp[kWarps];
-  __syncthreads();
-  return excl;
-}
-
 // Score smoothing across decode steps ("SparDA" article §6.1): where the
 // previous step's smoothed score h of a block is a number, the score becomes
 // (1 - w) * s + w * h; a block without history keeps s.  The result is stored
@@ -59,16 +27,87 @@ __device__ __forceinline__ void smooth_scores(float* s_scores, int nb, int max_b
   __syncthreads();
 }
 
+// Histogram of one radix pass: 256 digit counters, one padding word after
+// every 8 so that the digit scan below reads without bank conflicts.
+constexpr int kHistWords = 256 + 32;
+__device__ __forceinline__ int hist_index(uint32_t digit) { return static_cast<int>(digit + (digit >> 3)); }
+
+// Digit scan of one radix pass, run by every warp on its own: the digit holding
+// the kk-th largest counted key (digits taken from 255 down) and that key's rank
+// within the digit.  Lane l owns digits 255-8l .. 248-8l.
+__device__ __forceinline__ void find_digit(const uint32_t* hist, int kk, int& digit, int& rank) {
+  const int lane = threadIdx.x & 31;
+  uint32_t hv[8];
+  int sum = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    hv[i] = hist[hist_index(255u - 8u * lane - i)];
+    sum += static_cast<int>(hv[i]);
+  }
+  int incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  int above = incl - sum, d = -1, r = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int h = static_cast<int>(hv[i]);
+    if (above < kk && kk <= above + h) {
+      d = 255 - 8 * lane - i;
+      r = kk - above;
+    }
+    above += h;
+  }
+  const int src = __ffs(__ballot_sync(0xffffffffu, d >= 0)) - 1;  // exactly one lane
+  digit = __shfl_sync(0xffffffffu, d, src & 31);
+  rank = __shfl_sync(0xffffffffu, r, src & 31);
+}
+
+// The same smoothing with the previous step's history already staged in shared
+// memory (s_prev, nb floats), for CTAs that select the same pair side by side:
+// the new history is stored only when `store`.  All threads of the CTA call it.
+__device__ __forceinline__ void smooth_staged(float* s_scores, const float* s_prev, int nb, int max_blocks,
+                                              const SelectArgs& a, int64_t pair, bool store) {
+  float* h = a.history + pair * max_blocks;
+  const float w = a.history_weight, keep = 1.0f - a.history_weight;
+  for (int j = threadIdx.x; j < nb; j += blockDim.x) {
+    const float old = s_prev[j];
+    const float v = old == old ? fmaf(w, old, keep * s_scores[j]) : s_scores[j];
+    s_scores[j] = v;
+    if (store) h[j] = v;
+  }
+  __syncthreads();
+}
+
 // Selection of one (request, kv head) from its block scores in shared memory,
 // by all THREADS threads of the CTA ("KV 稀疏化" wiki §2 sink/window, §5 top-k):
-// forced blocks in closed form, a 4-pass 8-bit radix select of the k-th largest
-// key among the other blocks (two histogram buffers, which must be zero on
-// entry), then one packed scan that places forced-or-above-threshold blocks and
-// the lowest-index threshold-equal blocks in ascending order.
+// forced blocks in closed form; the k-th largest key among the other blocks by
+// an 8-bit radix select (one pass per byte below the bytes that every key
+// shares, one CTA barrier per pass: every warp scans the histogram itself, and
+// three histogram buffers let the clearing of the next one ride on the current
+// pass); then forced-or-above-threshold blocks and the lowest-index
+// threshold-equal blocks are placed in ascending order with warp ballots and
+// one barrier.
+//   s_hist     three buffers of kHistWords; the first must be zero on entry,
+//              all are left dirty.
+//   s_warp     THREADS / 32 ints.
+//   s_out      (nullable, shared memory, capacity ints) receives the selected
+//              indices as well.
+//   key_range  (nullable) n_range pairs (min, max) of score_key over sets of
+//              blocks that together cover blocks [0, nb); with it the passes
+//              start at the first byte where the smallest and the largest key
+//              differ.
+//   store      false: nothing is written to global memory (sel, sel_count,
+//              error bits); another CTA stores the same selection.
+// Returns the number stored (min(selected, capacity)) to every thread.
 template <int THREADS>
-__device__ __forceinline__ void select_pair(const float* s_scores, int nb, int L, int B, const SelectArgs& a,
-                                            int64_t pair, uint32_t (*s_hist)[256], int* s_warp, int* s_pick,
-                                            unsigned* err) {
+__device__ __forceinline__ int select_pair(const float* s_scores, int nb, int L, int B, const SelectArgs& a,
+                                           int64_t pair, uint32_t (*s_hist)[kHistWords], int* s_warp,
+                                           unsigned* err, int* s_out = nullptr, const uint32_t* key_range = nullptr,
+                                           int n_range = 0, bool store = true) {
+  constexpr int kWarps = THREADS / 32;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int sink = a.sink_tokens, win = a.window_tokens, k = a.k_scored, cap = a.capacity;
   auto forced = [&](int j) -> bool {
@@ -80,111 +119,133 @@ __device__ __forceinline__ void select_pair(const float* s_scores, int nb, int L
   int w_first = nb;
   if (win > 0) w_first = (L - win <= 0) ? 0 : min(nb, (L - win) / B);
   const int nf = n_sink + max(0, nb - max(w_first, n_sink));
-  const bool take_all = nf + k >= nb;
-  const bool use_threshold = !take_all && k > 0;
   int32_t* out = a.sel + pair * cap;
+
+  if (nf + k >= nb) {  // every block is selected
+    for (int j = tid; j < cap; j += THREADS) {
+      if (store) out[j] = j < nb ? j : -1;
+      if (s_out && j < nb) s_out[j] = j;
+    }
+    if (tid == 0 && store) {
+      if (nb > cap) set_error(err, HS_EBIT_CAPACITY);
+      a.sel_count[pair] = min(nb, cap);
+    }
+    return min(nb, cap);
+  }
 
   uint32_t T = 0;
   int need_eq = 0;
-  if (use_threshold) {
-    // 4-pass 8-bit radix select of the k-th largest key among non-forced blocks;
-    // two histogram buffers so that clearing the next one rides on this pass
-    uint32_t prefix = 0, mask = 0;
-    int kk = k;  // rank (1-based) of the wanted key among keys matching `prefix`
-    int buf = 0;
-    for (int shift = 24; shift >= 0; shift -= 8, buf ^= 1) {
-      uint32_t* hist = s_hist[buf];
+  if (k > 0) {
+    uint32_t lo = 0u, hi = 0xffffffffu;
+    if (key_range) {
+      lo = 0xffffffffu;
+      hi = 0u;
+      for (int i = 0; i < n_range; ++i) {
+        lo = min(lo, key_range[2 * i]);
+        hi = max(hi, key_range[2 * i + 1]);
+      }
+    }
+    const uint32_t diff = lo ^ hi;
+    int shift = diff == 0u ? -8 : ((31 - __clz(diff)) & ~7);  // highest byte that differs
+    uint32_t mask = shift >= 24 ? 0u : (0xffffffffu << (shift + 8));
+    uint32_t prefix = hi & mask;
+    int kk = k;  // rank (1-based) of the wanted key among the keys matching prefix
+    for (int pass = 0; shift >= 0; shift -= 8, ++pass) {
+      uint32_t* hist = s_hist[pass % 3];
+      uint32_t* next = s_hist[(pass + 1) % 3];  // last read two passes ago
+      for (int i = tid; i < kHistWords; i += THREADS) next[i] = 0u;
       for (int j = tid; j < nb; j += THREADS) {
         if (forced(j)) continue;
         const uint32_t key = score_key(s_scores[j]);
-        if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+        if ((key & mask) == prefix) atomicAdd(&hist[hist_index((key >> shift) & 255u)], 1u);
       }
       __syncthreads();
-      if (warp == 0) {
-        // lane l owns digits 255-8l .. 248-8l; a warp scan from the top digit
-        // finds the bucket holding the kk-th largest key
-        uint32_t hv[8];
-        int sum = 0;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          hv[i] = hist[255 - 8 * lane - i];
-          sum += static_cast<int>(hv[i]);
-        }
-        int incl = sum;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int n = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += n;
-        }
-        int above = incl - sum;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int h = static_cast<int>(hv[i]);
-          if (above < kk && kk <= above + h) {
-            s_pick[0] = 255 - 8 * lane - i;
-            s_pick[1] = kk - above;
-          }
-          above += h;
-        }
-        uint32_t* other = s_hist[buf ^ 1];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) other[8 * lane + i] = 0u;
-      }
-      __syncthreads();
-      prefix |= static_cast<uint32_t>(s_pick[0]) << shift;
+      int digit, rank;
+      find_digit(hist, kk, digit, rank);
+      prefix |= static_cast<uint32_t>(digit) << shift;
       mask |= 255u << shift;
-      kk = s_pick[1];
+      kk = rank;
     }
     T = prefix;
     need_eq = kk;
   }
 
-  if (take_all) {
-    for (int j = tid; j < cap; j += THREADS) out[j] = j < nb ? j : -1;
-    if (tid == 0) {
-      if (nb > cap) set_error(err, HS_EBIT_CAPACITY);
-      a.sel_count[pair] = min(nb, cap);
-    }
-    return;
-  }
-  // contiguous index range per thread keeps the output ascending.  One packed
-  // scan gives, for every block, how many forced-or-above-threshold blocks and
-  // how many threshold-equal blocks precede it; an equal block is chosen while
-  // fewer than need_eq equal blocks precede it (lower index first).
-  const int per_t = ceil_div(nb, THREADS);
-  const int j0 = min(nb, tid * per_t), j1 = min(nb, j0 + per_t);
-  int gt_local = 0, eq_local = 0;
-  for (int j = j0; j < j1; ++j) {
+  // Placement: warp w takes the contiguous index range [w*R, (w+1)*R) in rounds
+  // of 32; per round, ballots of "forced or above T" and "equal to T" give each
+  // lane its position.  An equal block is chosen while fewer than need_eq
+  // equal blocks precede it (lower index first).
+  const int rounds = ceil_div(nb, 32 * kWarps);
+  const int base = warp * rounds * 32;
+  const unsigned below = (1u << lane) - 1u;
+  auto flags = [&](int j, bool& gt, bool& eq) {
+    gt = false;
+    eq = false;
+    if (j >= nb) return;
     if (forced(j)) {
-      ++gt_local;
-    } else if (use_threshold) {
+      gt = true;
+    } else if (k > 0) {
       const uint32_t key = score_key(s_scores[j]);
-      gt_local += key > T;
-      eq_local += key == T;
+      gt = key > T;
+      eq = key == T;
+    }
+  };
+  int gt_w = 0, eq_w = 0;
+  for (int r = 0; r < rounds; ++r) {
+    bool gt, eq;
+    flags(base + r * 32 + lane, gt, eq);
+    gt_w += __popc(__ballot_sync(0xffffffffu, gt));
+    eq_w += __popc(__ballot_sync(0xffffffffu, eq));
+  }
+  if (lane == 0) s_warp[warp] = (gt_w << 16) | eq_w;
+  __syncthreads();
+  int gt_b = 0, eq_b = 0, gt_t = 0, eq_t = 0;
+#pragma unroll 4
+  for (int w = 0; w < kWarps; ++w) {
+    const int v = s_warp[w];
+    if (w < warp) {
+      gt_b += v >> 16;
+      eq_b += v & 0xffff;
+    }
+    gt_t += v >> 16;
+    eq_t += v & 0xffff;
+  }
+  for (int r = 0; r < rounds; ++r) {
+    const int j = base + r * 32 + lane;
+    bool gt, eq;
+    flags(j, gt, eq);
+    const unsigned bg = __ballot_sync(0xffffffffu, gt), be = __ballot_sync(0xffffffffu, eq);
+    const int eq_before = eq_b + __popc(be & below);
+    if (gt || (eq && eq_before < need_eq)) {
+      const int pos = gt_b + __popc(bg & below) + min(eq_before, need_eq);  // chosen blocks before j
+      if (pos < cap) {
+        if (store) out[pos] = j;
+        if (s_out) s_out[pos] = j;
+      }
+    }
+    gt_b += __popc(bg);
+    eq_b += __popc(be);
+  }
+  const int total = gt_t + min(eq_t, need_eq);
+  if (store) {
+    for (int i = total + tid; i < cap; i += THREADS) out[i] = -1;
+    if (tid == 0) {
+      if (total > cap) set_error(err, HS_EBIT_CAPACITY);
+      a.sel_count[pair] = min(total, cap);
     }
   }
-  int packed_total;
-  const int packed = block_exclusive_scan<THREADS>((gt_local << 16) | eq_local, s_warp, packed_total);
-  int gt_b = packed >> 16, eq_b = packed & 0xffff;
-  const int total = (packed_total >> 16) + min(packed_total & 0xffff, need_eq);
-  for (int j = j0; j < j1; ++j) {
-    bool is_gt = forced(j), is_eq = false;
-    if (!is_gt && use_threshold) {
-      const uint32_t key = score_key(s_scores[j]);
-      is_gt = key > T;
-      is_eq = key == T;
-    }
-    if (is_gt || (is_eq && eq_b < need_eq)) {
-      const int pos = gt_b + min(eq_b, need_eq);  // chosen blocks before j
-      if (pos < cap) out[pos] = j;
-    }
-    gt_b += is_gt ? 1 : 0;
-    eq_b += is_eq ? 1 : 0;
-  }
-  for (int i = total + tid; i < cap; i += THREADS) out[i] = -1;
-  if (tid == 0) {
-    if (total > cap) set_error(err, HS_EBIT_CAPACITY);
-    a.sel_count[pair] = min(total, cap);
+  return min(total, cap);
+}
+
+// Per-warp (min, max) of score_key over the blocks of the calling warp's
+// lanes (valid = the lane holds a block): lane 0 stores the pair at
+// range[2 * slot].  All 32 lanes call it.
+__device__ __forceinline__ void warp_key_range(float score, bool valid, uint32_t* range, int slot) {
+  const uint32_t key = score_key(score);
+  const uint32_t lo = __reduce_min_sync(0xffffffffu, valid ? key : 0xffffffffu);
+  const uint32_t hi = __reduce_max_sync(0xffffffffu, valid ? key : 0u);
+  if ((threadIdx.x & 31) == 0) {
+    range[2 * slot] = lo;
+    range[2 * slot + 1] = hi;
   }
 }
 

@@ -31,14 +31,17 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 __device__ __forceinline__ void mbar_arrive_tx(uint32_t bar, uint32_t tx) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(tx) : "memory");
 }
+// The waiting thread is suspended until the phase completes or about 1 ms
+// has passed (the time-limit hint), so waiting warps take no issue slots
+// from the working ones.
 __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(1000000u)
       : "memory");
   return ok != 0;
 }
@@ -63,10 +66,10 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
                                           uint64_t limit_ns = 2000000000ull) {
   if (mbar_try(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  for (uint32_t i = 1;; ++i) {
+  for (;;) {
     if (mbar_try(bar, parity)) return true;
     if (*abort) return false;
-    if ((i & 255u) == 0 && globaltimer_ns() - t0 > limit_ns) {
+    if (globaltimer_ns() - t0 > limit_ns) {
       *abort = 1;
       return false;
     }
@@ -84,6 +87,11 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* map, int x
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
       : "memory");
+}
+// Fetches a tensor map (a __grid_constant__ kernel parameter) ahead of the
+// first copy that uses it.
+__device__ __forceinline__ void prefetch_tmap(const void* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 // 1-D bulk copy: dst, src and bytes multiples of 16
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {

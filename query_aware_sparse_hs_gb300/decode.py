@@ -20,7 +20,7 @@ class SparseDecode:
     def __init__(self, *, num_q_heads, num_kv_heads, head_dim, block_size, kv_dtype, batch,
                  max_blocks, sink_tokens, window_tokens, k_scored, capacity=None, scale=None,
                  out_is_fp32=False, algo="auto", blocks_per_split=0, score_smoothing=0.0,
-                 inline_merge=True, device="cuda"):
+                 inline_merge=True, fuse_step=True, device="cuda"):
         self.kv_dtype = kv_dtype
         self.shape = hs.attn_shape(num_q_heads, num_kv_heads, head_dim, block_size, kv_dtype)
         self.batch, self.max_blocks = int(batch), int(max_blocks)
@@ -53,7 +53,12 @@ class SparseDecode:
         self.results = torch.empty((ob16 + batch * num_q_heads * 4,), dtype=torch.uint8, device=dev)
         self.out = self.results[:ob].view(odt).view(batch, num_q_heads, head_dim)
         self.lse = self.results[ob16:].view(torch.float32).view(batch, num_q_heads)
-        ws = hs.hs_workspace_bytes(self.shape, batch, self.capacity, self.attn_params)
+        # one workspace serves the attention alone (from its start) and the
+        # combined selection + attention call
+        self.fuse_step = bool(fuse_step)
+        ws = max(hs.hs_workspace_bytes(self.shape, batch, self.capacity, self.attn_params),
+                 hs.hs_score_select_attend_workspace_bytes(self.shape, batch, max_blocks, self.capacity,
+                                                           self.attn_params))
         self.workspace = torch.empty((max(ws, 256),), dtype=torch.uint8, device=dev)
 
     def reset_score_history(self):
@@ -83,6 +88,13 @@ class SparseDecode:
             raise ValueError("a reused selection must have the same capacity")
         hs.hs_sparse_paged_decode_attn(self.shape, kv, q, src.sel, src.sel_count, self.capacity,
                                        self.attn_params, self.out, self.lse, self.workspace, stream)
+
+    def select_attend(self, kv: hs.PagedKV, q: torch.Tensor, keep_scores: bool = True, stream=None):
+        """select() then attend() as one library call (a single launch where
+        the shapes allow it)."""
+        hs.hs_score_select_attend(self.shape, kv, q, self.smin, self.smax, self.sel_params, self.sel,
+                                  self.sel_count, self.scores if keep_scores else None, self.attn_params,
+                                  self.out, self.lse, self.workspace, stream)
 
     def swap_in(self, hb: hs.HotBuffer, step: int, stats=None, stream=None):
         hs.hs_swapin_misses(self.shape, hb, self.sel, self.sel_count, self.capacity, step, stats, stream)
@@ -153,6 +165,9 @@ class SparseDecode:
             if hot is not None:
                 raise ValueError("the offload path selects every step")
             self.attend(kv, q, stream, selection=reuse)
+            return self.out, self.lse
+        if hot is None and self.fuse_step:
+            self.select_attend(kv, q, stream=stream)
             return self.out, self.lse
         self.select(kv, q, stream=stream)
         if hot is not None:

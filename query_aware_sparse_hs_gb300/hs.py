@@ -81,6 +81,13 @@ SYMBOLS = {
     "hs_sparse_paged_decode_attn": (c_int32, [POINTER(AttnShape), POINTER(PagedKV), c_void_p, c_void_p,
                                               c_void_p, c_int32, POINTER(AttnParams), c_void_p, c_void_p,
                                               c_void_p, c_size_t, c_void_p]),
+    "hs_score_select_attend_workspace_bytes": (c_size_t, [POINTER(AttnShape), c_int32, c_int32, c_int32,
+                                                          POINTER(AttnParams)]),
+    "hs_score_select_attend_fused": (c_int32, [POINTER(AttnShape), c_int32, c_int32, c_int32,
+                                               POINTER(AttnParams)]),
+    "hs_score_select_attend": (c_int32, [POINTER(AttnShape), POINTER(PagedKV), c_void_p, c_void_p, c_void_p,
+                                         POINTER(SelectParams), c_void_p, c_void_p, c_void_p, POINTER(AttnParams),
+                                         c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
     "hs_sparse_paged_decode_attn_noalloc": (c_int32, [POINTER(AttnShape), POINTER(PagedKV), c_void_p,
                                                       c_void_p, c_void_p, c_int32, POINTER(AttnParams),
                                                       c_void_p, c_void_p, c_void_p]),
@@ -215,6 +222,31 @@ def hs_sparse_paged_decode_attn(shape, kv, q, sel, sel_count, capacity, params, 
                                             _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes,
                                             _stream(stream)),
            "hs_sparse_paged_decode_attn")
+
+
+def hs_score_select_attend_workspace_bytes(shape: AttnShape, batch: int, max_blocks: int, capacity: int,
+                                           params: AttnParams) -> int:
+    return int(_lib.hs_score_select_attend_workspace_bytes(ctypes.byref(shape), batch, max_blocks, capacity,
+                                                           ctypes.byref(params)))
+
+
+def hs_score_select_attend_fused(shape: AttnShape, batch: int, max_blocks: int, capacity: int,
+                                 params: AttnParams) -> int:
+    """1: the combined call is one launch for this geometry on the current device; 0: separate launches."""
+    return int(_lib.hs_score_select_attend_fused(ctypes.byref(shape), batch, max_blocks, capacity,
+                                                 ctypes.byref(params)))
+
+
+def hs_score_select_attend(shape, kv, q, smin, smax, sel_params, sel, sel_count, scores, attn_params, out,
+                           lse=None, workspace=None, stream=None):
+    """Selection and attention of one decode step in one call (one launch where
+    the library can fuse them)."""
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(_lib.hs_score_select_attend(ctypes.byref(shape), ctypes.byref(kv), _ptr(q), _ptr(smin), _ptr(smax),
+                                       ctypes.byref(sel_params), _ptr(sel), _ptr(sel_count), _ptr(scores),
+                                       ctypes.byref(attn_params), _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes,
+                                       _stream(stream)),
+           "hs_score_select_attend")
 
 
 def hs_sparse_paged_decode_attn_noalloc(shape, kv, q, sel, sel_count, capacity, params, out, lse=None,

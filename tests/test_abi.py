@@ -133,3 +133,32 @@ def test_host_checks_of_the_overlap_and_merge_calls():
     st = lib.hs_sparse_paged_decode_attn(ctypes.byref(shape), ctypes.byref(kv), P, P, P, 8, ctypes.byref(params),
                                          P, None, None, 0, None)
     assert st == hs.HS_ERR_INVALID_ARG
+
+
+def test_host_checks_of_the_combined_call():
+    from query_aware_sparse_hs_gb300 import hs
+    lib = hs.library()
+    shape = hs.attn_shape(32, 4, 128, 64, "bf16")
+    params = hs.attn_params(0.088)
+    sp = hs.select_params(4, 256, 27, 33)
+    kv = hs.PagedKV()
+    P = 0x10000
+    kv.k_pages = kv.v_pages = kv.page_table = kv.seq_lens = P
+    kv.batch, kv.max_blocks, kv.num_pages = 8, 512, 4096
+    need = hs.hs_score_select_attend_workspace_bytes(shape, 8, 512, 32, params)
+    sel_ws = hs.hs_select_workspace_bytes(shape, 8, 512)
+    assert sel_ws == 8 * 4 * 512 * 4 and need > sel_ws
+    # no workspace for the selection's score buffer: refused before any device work
+    st = lib.hs_score_select_attend(ctypes.byref(shape), ctypes.byref(kv), P, P, P, ctypes.byref(sp), P, P, None,
+                                    ctypes.byref(params), P, None, None, 0, None)
+    assert st == hs.HS_ERR_WORKSPACE
+    # the selection's own checks come first: a capacity below the largest selection
+    small = hs.select_params(4, 256, 27, 8)
+    st = lib.hs_score_select_attend(ctypes.byref(shape), ctypes.byref(kv), P, P, P, ctypes.byref(small), P, P,
+                                    None, ctypes.byref(params), P, None, P, need, None)
+    assert st == hs.HS_ERR_CAPACITY
+    # the geometry query answers -1 for an invalid shape or CTA cap
+    bad = hs.attn_shape(32, 5, 128, 64, "bf16")
+    assert hs.hs_score_select_attend_fused(bad, 8, 512, 32, params) == -1
+    assert hs.hs_score_select_attend_fused(shape, 8, 512, 32, hs.attn_params(0.088, max_ctas=-1)) == -1
+    assert hs.hs_score_select_attend_workspace_bytes(bad, 8, 512, 32, params) == 0
