@@ -85,9 +85,9 @@ __device__ __forceinline__ void smooth_staged(float* s_scores, const float* s_pr
 // by all THREADS threads of the CTA ("KV 稀疏化" wiki §2 sink/window, §5 top-k):
 // forced blocks in closed form; the k-th largest key among the other blocks by
 // an 8-bit radix select (one pass per byte below the bytes that every key
-// shares, one CTA barrier per pass: every warp scans the histogram itself, and
-// three histogram buffers let the clearing of the next one ride on the current
-// pass); then forced-or-above-threshold blocks and the lowest-index
+// shares; three histogram buffers let the clearing of the next one ride on the
+// current pass; with up to 12 warps every warp scans the histogram itself, so
+// a pass takes one CTA barrier); then forced-or-above-threshold blocks and the lowest-index
 // threshold-equal blocks are placed in ascending order with warp ballots and
 // one barrier.
 //   s_hist     three buffers of kHistWords; the first must be zero on entry,
@@ -161,7 +161,22 @@ __device__ __forceinline__ int select_pair(const float* s_scores, int nb, int L,
       }
       __syncthreads();
       int digit, rank;
-      find_digit(hist, kk, digit, rank);
+      if constexpr (kWarps <= 12) {
+        find_digit(hist, kk, digit, rank);  // every warp on its own: no second barrier
+      } else {
+        // many warps: warp 0 scans and the others read its result
+        if (warp == 0) {
+          find_digit(hist, kk, digit, rank);
+          if (lane == 0) {
+            s_warp[0] = digit;
+            s_warp[1] = rank;
+          }
+        }
+        __syncthreads();
+        digit = s_warp[0];
+        rank = s_warp[1];
+        __syncthreads();  // s_warp is rewritten by the next pass or the placement
+      }
       prefix |= static_cast<uint32_t>(digit) << shift;
       mask |= 255u << shift;
       kk = rank;
