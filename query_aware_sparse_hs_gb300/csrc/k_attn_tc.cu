@@ -991,9 +991,10 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 
   // ---- phase 2: every CTA selects; rank 0 stores the selection ----
   if (smoothed) sel::smooth_staged(s_scores, s_prev, nb, a.max_blocks, sa, pair, rank == 0);
-  const int n = sel::select_pair<kThreadsB>(s_scores, nb, L, a.block, sa, pair, s_hist, s_warp, err, s_sel,
-                                            smoothed ? nullptr : s_range, 4 * ceil_div(nb, bound::kTile),
-                                            rank == 0);
+  static_assert(kThreadsB * 3 >= kFuseMaxBlocks, "three blocks per thread cover the pair");
+  const int n = sel::select_pair_regs<kThreadsB, 3>(s_scores, nb, L, a.block, sa, pair, s_hist, s_warp, err, s_sel,
+                                                    smoothed ? nullptr : s_range, 4 * ceil_div(nb, bound::kTile),
+                                                    rank == 0);
   __syncthreads();  // the shared copy of the selection is complete
   const int bpc = kChunk / a.block;
   const int per = split_len(n, bpc, a.splits, a.bps);

@@ -251,6 +251,142 @@ __device__ __forceinline__ int select_pair(const float* s_scores, int nb, int L,
   return min(total, cap);
 }
 
+// The same selection with the keys held in registers: thread t owns blocks
+// t*KPT .. t*KPT+KPT-1 (nb <= THREADS * KPT, THREADS / 32 <= 12), keys are
+// computed once, forced blocks are [0, sink blocks) and [first window block,
+// nb), and placement is one warp scan of per-thread counts plus one barrier.
+// Same arguments, result and tie rule as select_pair.
+template <int THREADS, int KPT>
+__device__ __forceinline__ int select_pair_regs(const float* s_scores, int nb, int L, int B, const SelectArgs& a,
+                                                int64_t pair, uint32_t (*s_hist)[kHistWords], int* s_warp,
+                                                unsigned* err, int* s_out, const uint32_t* key_range, int n_range,
+                                                bool store) {
+  constexpr int kWarps = THREADS / 32;
+  static_assert(kWarps <= 12 && KPT <= 16, "one barrier per pass needs few warps");
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int sink = a.sink_tokens, win = a.window_tokens, k = a.k_scored, cap = a.capacity;
+  const int n_sink = min(nb, ceil_div(sink, B));
+  int w_first = nb;
+  if (win > 0) w_first = (L - win <= 0) ? 0 : min(nb, (L - win) / B);
+  w_first = max(w_first, n_sink);
+  const int nf = n_sink + (nb - w_first);
+  int32_t* out = a.sel + pair * cap;
+
+  if (nf + k >= nb) {  // every block is selected
+    for (int j = tid; j < cap; j += THREADS) {
+      if (store) out[j] = j < nb ? j : -1;
+      if (s_out && j < nb) s_out[j] = j;
+    }
+    if (tid == 0 && store) {
+      if (nb > cap) set_error(err, HS_EBIT_CAPACITY);
+      a.sel_count[pair] = min(nb, cap);
+    }
+    return min(nb, cap);
+  }
+
+  const int j0 = tid * KPT;
+  uint32_t key[KPT];
+  unsigned cand = 0u, forc = 0u;  // per owned block: a candidate (scored) / forced
+#pragma unroll
+  for (int i = 0; i < KPT; ++i) {
+    const int j = j0 + i;
+    key[i] = 0u;
+    if (j < nb) {
+      if (j < n_sink || j >= w_first) {
+        forc |= 1u << i;
+      } else {
+        cand |= 1u << i;
+        key[i] = score_key(s_scores[j]);
+      }
+    }
+  }
+
+  uint32_t T = 0;
+  int need_eq = 0;
+  if (k > 0) {
+    uint32_t lo = 0u, hi = 0xffffffffu;
+    if (key_range) {
+      lo = 0xffffffffu;
+      hi = 0u;
+      for (int i = 0; i < n_range; ++i) {
+        lo = min(lo, key_range[2 * i]);
+        hi = max(hi, key_range[2 * i + 1]);
+      }
+    }
+    const uint32_t diff = lo ^ hi;
+    int shift = diff == 0u ? -8 : ((31 - __clz(diff)) & ~7);
+    uint32_t mask = shift >= 24 ? 0u : (0xffffffffu << (shift + 8));
+    uint32_t prefix = hi & mask;
+    int kk = k;
+    for (int pass = 0; shift >= 0; shift -= 8, ++pass) {
+      uint32_t* hist = s_hist[pass % 3];
+      uint32_t* next = s_hist[(pass + 1) % 3];  // last read two passes ago
+      for (int i = tid; i < kHistWords; i += THREADS) next[i] = 0u;
+#pragma unroll
+      for (int i = 0; i < KPT; ++i)
+        if (((cand >> i) & 1u) && (key[i] & mask) == prefix)
+          atomicAdd(&hist[hist_index((key[i] >> shift) & 255u)], 1u);
+      __syncthreads();
+      int digit, rank;
+      find_digit(hist, kk, digit, rank);
+      prefix |= static_cast<uint32_t>(digit) << shift;
+      mask |= 255u << shift;
+      kk = rank;
+    }
+    T = prefix;
+    need_eq = kk;
+  }
+
+  // placement: forced-or-above-threshold, then the lowest-index equal blocks
+  unsigned gt = forc, eq = 0u;
+#pragma unroll
+  for (int i = 0; i < KPT; ++i) {
+    if (k > 0 && ((cand >> i) & 1u)) {
+      gt |= (key[i] > T ? 1u : 0u) << i;
+      eq |= (key[i] == T ? 1u : 0u) << i;
+    }
+  }
+  const int mine = (__popc(gt) << 16) | __popc(eq);
+  int incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (lane == 31) s_warp[warp] = incl;
+  __syncthreads();
+  int before = incl - mine, total_packed = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    const int v = s_warp[w];
+    before += w < warp ? v : 0;
+    total_packed += v;
+  }
+  int gt_b = before >> 16, eq_b = before & 0xffff;
+#pragma unroll
+  for (int i = 0; i < KPT; ++i) {
+    const bool is_gt = (gt >> i) & 1u, is_eq = (eq >> i) & 1u;
+    if (is_gt || (is_eq && eq_b < need_eq)) {
+      const int pos = gt_b + min(eq_b, need_eq);
+      if (pos < cap) {
+        if (store) out[pos] = j0 + i;
+        if (s_out) s_out[pos] = j0 + i;
+      }
+    }
+    gt_b += is_gt ? 1 : 0;
+    eq_b += is_eq ? 1 : 0;
+  }
+  const int total = (total_packed >> 16) + min(total_packed & 0xffff, need_eq);
+  if (store) {
+    for (int i = total + tid; i < cap; i += THREADS) out[i] = -1;
+    if (tid == 0) {
+      if (total > cap) set_error(err, HS_EBIT_CAPACITY);
+      a.sel_count[pair] = min(total, cap);
+    }
+  }
+  return min(total, cap);
+}
+
 // Per-warp (min, max) of score_key over the blocks of the calling warp's
 // lanes (valid = the lane holds a block): lane 0 stores the pair at
 // range[2 * slot].  All 32 lanes call it.
