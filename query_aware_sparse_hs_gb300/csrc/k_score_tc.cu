@@ -248,8 +248,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncthreads();
       const bool smoothed = sa.history_weight != 0.0f && sa.history != nullptr;  // the range no longer holds
       sel::smooth_scores(s_scores, nb, a.max_blocks, sa, pair);
-      sel::select_pair<kThreads>(s_scores, nb, L, a.block, sa, pair, s_hist, s_warp, err, nullptr,
-                                 smoothed ? nullptr : s_range, kThreads / 32);
+      static_assert(kThreads * 6 >= 8 * kTile, "six blocks per thread cover up to 8 tiles");
+      sel::select_pair_regs<kThreads, 6>(s_scores, nb, L, a.block, sa, pair, s_hist, s_warp, err, nullptr,
+                                         smoothed ? nullptr : s_range, kThreads / 32, true);
     }
   }
   if (*abort_flag && tid == 0) set_error(err, HS_EBIT_TIMEOUT);

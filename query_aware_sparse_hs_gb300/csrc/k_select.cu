@@ -210,8 +210,10 @@ __global__ __launch_bounds__(THREADS) void select_only_kernel(KvView kv, SelectA
   __syncthreads();
   const bool smoothed = a.history_weight != 0.0f && a.history != nullptr;  // the range no longer holds
   smooth_scores(s_scores, nb, kv.max_blocks, a, pair);
-  select_pair<THREADS>(s_scores, nb, L, B, a, pair, s_hist, s_warp, err, nullptr, smoothed ? nullptr : s_range,
-                       kWarps);
+  // blocks per thread: up to 1024 blocks on 256 threads, up to kMaxSelectBlocks on 1024
+  constexpr int kKpt = THREADS >= 1024 ? kMaxSelectBlocks / 1024 : 1024 / THREADS;
+  select_pair_regs<THREADS, kKpt>(s_scores, nb, L, B, a, pair, s_hist, s_warp, err, nullptr,
+                                  smoothed ? nullptr : s_range, kWarps, true);
 }
 
 template <int C, int G, bool F32>

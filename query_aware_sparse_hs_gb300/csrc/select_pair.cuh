@@ -252,17 +252,18 @@ __device__ __forceinline__ int select_pair(const float* s_scores, int nb, int L,
 }
 
 // The same selection with the keys held in registers: thread t owns blocks
-// t*KPT .. t*KPT+KPT-1 (nb <= THREADS * KPT, THREADS / 32 <= 12), keys are
-// computed once, forced blocks are [0, sink blocks) and [first window block,
-// nb), and placement is one warp scan of per-thread counts plus one barrier.
-// Same arguments, result and tie rule as select_pair.
+// t*KPT .. t*KPT+KPT-1 (nb <= THREADS * KPT), keys are computed once, forced
+// blocks are [0, sink blocks) and [first window block, nb), and placement is
+// one warp scan of per-thread counts plus one barrier.  With up to 12 warps
+// every warp scans the radix histogram itself; with more, warp 0 scans and
+// broadcasts.  Same arguments, result and tie rule as select_pair.
 template <int THREADS, int KPT>
 __device__ __forceinline__ int select_pair_regs(const float* s_scores, int nb, int L, int B, const SelectArgs& a,
                                                 int64_t pair, uint32_t (*s_hist)[kHistWords], int* s_warp,
                                                 unsigned* err, int* s_out, const uint32_t* key_range, int n_range,
                                                 bool store) {
   constexpr int kWarps = THREADS / 32;
-  static_assert(kWarps <= 12 && KPT <= 16, "one barrier per pass needs few warps");
+  static_assert(KPT <= 32, "per-thread block masks are 32 bits");
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int sink = a.sink_tokens, win = a.window_tokens, k = a.k_scored, cap = a.capacity;
   const int n_sink = min(nb, ceil_div(sink, B));
@@ -328,7 +329,21 @@ __device__ __forceinline__ int select_pair_regs(const float* s_scores, int nb, i
           atomicAdd(&hist[hist_index((key[i] >> shift) & 255u)], 1u);
       __syncthreads();
       int digit, rank;
-      find_digit(hist, kk, digit, rank);
+      if constexpr (kWarps <= 12) {
+        find_digit(hist, kk, digit, rank);
+      } else {
+        if (warp == 0) {
+          find_digit(hist, kk, digit, rank);
+          if (lane == 0) {
+            s_warp[0] = digit;
+            s_warp[1] = rank;
+          }
+        }
+        __syncthreads();
+        digit = s_warp[0];
+        rank = s_warp[1];
+        __syncthreads();  // s_warp is rewritten by the next pass or the placement
+      }
       prefix |= static_cast<uint32_t>(digit) << shift;
       mask |= 255u << shift;
       kk = rank;
