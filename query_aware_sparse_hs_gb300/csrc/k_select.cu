@@ -168,7 +168,7 @@ __global__ void __cluster_dims__(kSelectCluster, 1, 1) __launch_bounds__(kThread
 
 // One CTA per (request, kv head): scores already in global memory (written by
 // the tensor-core scorer) -> selection.
-template <int THREADS>
+template <int THREADS, int KPT>
 __global__ __launch_bounds__(THREADS) void select_only_kernel(KvView kv, SelectArgs a, const float* scores,
                                                               unsigned* err) {
   constexpr int kWarps = THREADS / 32;
@@ -210,9 +210,7 @@ __global__ __launch_bounds__(THREADS) void select_only_kernel(KvView kv, SelectA
   __syncthreads();
   const bool smoothed = a.history_weight != 0.0f && a.history != nullptr;  // the range no longer holds
   smooth_scores(s_scores, nb, kv.max_blocks, a, pair);
-  // blocks per thread: up to 1024 blocks on 256 threads, up to kMaxSelectBlocks on 1024
-  constexpr int kKpt = THREADS >= 1024 ? kMaxSelectBlocks / 1024 : 1024 / THREADS;
-  select_pair_regs<THREADS, kKpt>(s_scores, nb, L, B, a, pair, s_hist, s_warp, err, nullptr,
+  select_pair_regs<THREADS, KPT>(s_scores, nb, L, B, a, pair, s_hist, s_warp, err, nullptr,
                                   smoothed ? nullptr : s_range, kWarps, true);
 }
 
@@ -247,9 +245,13 @@ cudaError_t launch_select_only(const KvView& kv, const SelectArgs& a, const floa
   const int pairs = kv.batch * kv.hkv;
   if (pairs == 0) return cudaSuccess;
   const size_t smem = static_cast<size_t>(kv.max_blocks) * sizeof(float);
-  // long requests: four times the threads, so each radix pass touches a
-  // quarter of the keys per thread
-  auto kern = kv.max_blocks > 1024 ? select_only_kernel<1024> : select_only_kernel<kThreads>;
+  // KPT consecutive blocks per thread (THREADS * KPT >= max_blocks): 256
+  // threads up to 1024 blocks, 1024 threads above, with as few blocks per
+  // thread as cover the request
+  auto kern = kv.max_blocks <= 1024   ? select_only_kernel<kThreads, 1024 / kThreads>
+              : kv.max_blocks <= 4096 ? select_only_kernel<1024, 4>
+              : kv.max_blocks <= 8192 ? select_only_kernel<1024, 8>
+                                      : select_only_kernel<1024, kMaxSelectBlocks / 1024>;
   const int threads = kv.max_blocks > 1024 ? 1024 : kThreads;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
