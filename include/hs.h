@@ -317,7 +317,8 @@ HS_API hs_status hs_score_select_attend(const hs_attn_shape* shape, const hs_pag
  * when attn_params has no split_counters and a pair has several splits) for
  * this geometry on the current device, 0 when it runs the separate launches,
  * -1 on invalid input or without a device.  Depends on the shape, batch,
- * max_blocks, capacity and attn_params only. */
+ * max_blocks, capacity and attn_params only (for page pools below 2^31
+ * token rows, the tensor-core attention's own limit). */
 HS_API int32_t hs_score_select_attend_fused(const hs_attn_shape* shape, int32_t batch, int32_t max_blocks,
                                             int32_t capacity, const hs_attn_params* attn_params);
 
