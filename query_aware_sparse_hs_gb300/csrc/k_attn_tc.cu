@@ -345,7 +345,6 @@ __device__ __forceinline__ void run_producer(const TcArgs& a, const Work& w, int
 // bf16 kernel: warps 0-7 are two softmax groups of 4 warps (group g takes the
 // chunks c with c % 2 == g, so two chunks are in the softmax stage at once),
 // warp 8 is the TMA producer, warps 9 and 10 the MMA issuers.
-constexpr int kGroups = 2;
 constexpr int kThreadsB = 352;
 constexpr int kProdB = 8, kMma1B = 9, kMma2B = 10;
 

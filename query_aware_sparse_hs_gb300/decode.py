@@ -17,6 +17,14 @@ _Q_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16, "fp8": torch.bfloat16}
 
 
 class SparseDecode:
+    """Buffers and calls of one decode step for one layer.
+
+    score_smoothing: weight of the previous step's block scores (0 = off).
+    inline_merge: give the tensor-core attention split counters so that it
+    merges its splits itself.  fuse_step: a step without a hot buffer or a
+    reused selection runs selection and attention as one library call
+    (hs_score_select_attend, a single launch where the geometry allows)."""
+
     def __init__(self, *, num_q_heads, num_kv_heads, head_dim, block_size, kv_dtype, batch,
                  max_blocks, sink_tokens, window_tokens, k_scored, capacity=None, scale=None,
                  out_is_fp32=False, algo="auto", blocks_per_split=0, score_smoothing=0.0,
