@@ -1,24 +1,39 @@
 """Throughput of one decode step of query-aware block-sparse paged attention.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload llama8b_bf16|fp8_g32|ragged_bf16|offload_bf16]
+                    [--workload all|offload_bf16|llama8b_bf16|ragged_bf16|fp8_g32]
+                    [--batch B] [--layers L] [--cpu-seconds S]
 
 A step = the whole per-step path of one layer over the batch: append of the
 newest token (written into its page, e4m3-quantised for the e4m3 cache, its
-block's summary widened), bound scoring + top-k selection,
-[swap-in for the offload workload], gather-attention with split-K, LSE merge.
-The default workload is the Llama-3-8B-like bf16 layer (8 requests x 32768
-tokens, 32 q / 4 kv heads, head_dim 128, 64-token blocks, 2048-token budget).
-Consecutive steps read distinct layer copies (32 layers, ~17 GB) so every step
-streams its K/V from HBM, not L2.  Steps are replayed from a CUDA graph.
+block's summary widened), bound scoring + top-k selection, [swap-in of the
+missing pages for the offload workload], gather-attention with split-K, LSE
+merge.
 
-Prints ONE JSON line (rank 0).  Multi-GPU: replicas (every rank runs the same
-per-GPU workload; no data-path collective), launched by torchrun.
+With ``--workload all`` (the default) every target workload is measured and ONE
+JSON line is printed (rank 0): its headline keys describe the largest workload,
+the HiSparse-style offload step (256 requests x 32768 tokens, a hot buffer of 64
+pages per (request, kv head), the rest of the cache in pinned host memory,
+64 decode steps with a drifting query); ``workloads`` holds one record with the
+same keys for each of the other three (the Llama-3-8B-like layer, the paged
+ragged batch and the e4m3 group-32 cache).  ``--workload NAME`` measures one
+workload and prints its record as the line.
+
+Exactly ``--steps`` steps are timed after exactly ``--warmup`` untimed steps.
+Resident workloads rotate distinct layer copies (together larger than L2) from
+step to step and replay their steps from CUDA graphs; the offload workload
+replays the decode steps of its drifting sequence (step 0, which refills the
+empty hot buffer, is run untimed before each pass).  Each record adds a
+``long_run`` figure over at least half a second of timed steps.
+
+Multi-GPU: replicas (every rank runs the same per-GPU workload; no data-path
+collective), launched by torchrun.
 """
 
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import math
 import os
@@ -36,6 +51,9 @@ sys.path.insert(0, ROOT)
 
 METRIC = "sparse decode-attn steps/s (batch×heads) and achieved HBM GB/s vs ~8 TB/s peak"
 UNIT = "head-steps/s"
+HEADLINE = "offload_bf16"
+SUB_WORKLOADS = ("llama8b_bf16", "ragged_bf16", "fp8_g32")
+LONG_RUN_S = 0.5
 
 
 # ----------------------------------------------------------------------------
@@ -73,17 +91,30 @@ def append_bytes_per_step(w) -> int:
     return int(w.batch * w.num_kv_heads * (src + token_bytes(w) + 2 * summary_bytes_per_block(w)))
 
 
+def select_bytes(w, total_blocks: int) -> int:
+    """Summaries of every block read once, q, the selection written."""
+    qb = w.batch * w.num_q_heads * w.head_dim * (4 if w.kv_dtype == "f32" else 2)
+    return int(total_blocks * summary_bytes_per_block(w) + qb + 4 * w.batch * w.num_kv_heads * w.capacity)
+
+
+# ----------------------------------------------------------------------------
+# launches of one step, as the library dispatches them
+# ----------------------------------------------------------------------------
+
+def _sms() -> int:
+    import torch
+    return torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+
+
 def select_launches(w) -> int:
     """Launches of bound scoring + selection: one fused cluster launch when
     every tile of every (request, kv head) fits one wave (tensor-core scoring,
     at most 8 tiles of 128 blocks per request), two with the tensor-core scorer
     otherwise, one on the CUDA-core path."""
-    import torch
-    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
     if not (w.kv_dtype != "f32" and w.head_dim == 128):
         return 1
     tiles = -(-w.max_blocks // 128)
-    return 1 if tiles <= 8 and w.batch * w.num_kv_heads * tiles <= sms else 2
+    return 1 if tiles <= 8 and w.batch * w.num_kv_heads * tiles <= _sms() else 2
 
 
 def fused_step(w, dec) -> bool:
@@ -94,43 +125,71 @@ def fused_step(w, dec) -> bool:
         dec.shape, w.batch, dec.max_blocks, dec.capacity, dec.attn_params) == 1
 
 
-def attn_splits(w, dec) -> int:
+def attn_splits(w, dec, params=None) -> int:
     from query_aware_sparse_hs_gb300 import hs
     per_split = w.batch * w.num_q_heads * (w.head_dim + 1) * 4
-    return hs.hs_workspace_bytes(dec.shape, w.batch, dec.capacity, dec.attn_params) // per_split
+    return hs.hs_workspace_bytes(dec.shape, w.batch, dec.capacity, params or dec.attn_params) // per_split
 
 
 def step_launches(w, dec, hot: bool = False, overlap: bool = False, allow_fused: bool = True) -> int:
     """Kernels of one step as the library dispatches them for this workload:
-    append (not on the offload path), then either the single scoring +
-    selection + attention launch, or bound scoring + selection
-    (select_launches), the swap-in (offload; with the copy overlapped: plan,
-    page copy, attention over the copied blocks, attention over the resident
-    blocks and the merge of the two) and attention; and the split merge unless
-    the tensor-core attention merges in the kernel or gives every pair one
-    split."""
-    import torch
-    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    either the single append + scoring + selection + attention launch (which
+    merges its splits inside its clusters), or the append (not on the
+    offload path), bound scoring + selection (select_launches), the swap-in
+    (offload; with the copy overlapped: plan, page copy, attention over the
+    copied blocks, attention over the resident blocks and the merge of the
+    two) and attention; and the split merge unless the tensor-core attention
+    merges in the kernel or gives every pair one split."""
     n = 0 if hot else 1
-    splits = attn_splits(w, dec)
     if not hot and allow_fused and fused_step(w, dec):
-        return n + 1 + (0 if splits <= 1 or dec.split_counters is not None else 1)
+        return 1  # the append runs inside the single launch
     n += select_launches(w)
+    tc = w.kv_dtype in ("bf16", "fp8") and w.head_dim == 128 and w.block_size in (16, 32, 64, 128)
     if hot and overlap:
-        return n + 5
+        # plan, page copy, attention over the copied blocks, attention over the
+        # hits (+ its split merge: no split counters there), merge of the parts
+        splits = attn_splits(w, dec, getattr(dec, "hit_params", None))
+        return n + 5 + (0 if (tc and splits <= 1) else 1)
+    splits = attn_splits(w, dec)
     n += 1 if hot else 0
     n += 1
-    tc = w.kv_dtype in ("bf16", "fp8") and w.head_dim == 128 and w.block_size in (16, 32, 64, 128)
     # the tensor-core kernel merges its splits itself when it has split
     # counters and every work item a CTA of its own
-    inline = tc and dec.split_counters is not None and w.batch * w.num_kv_heads * splits <= sms
+    inline = tc and dec.split_counters is not None and w.batch * w.num_kv_heads * splits <= _sms()
     return n + (0 if (tc and splits <= 1) or inline else 1)
 
 
-def select_bytes(w, total_blocks: int) -> int:
-    """Summaries of every block read once, q, the selection written."""
-    qb = w.batch * w.num_q_heads * w.head_dim * (4 if w.kv_dtype == "f32" else 2)
-    return int(total_blocks * summary_bytes_per_block(w) + qb + 4 * w.batch * w.num_kv_heads * w.capacity)
+# ----------------------------------------------------------------------------
+# DRAM traffic of the dominant kernel, from ncu captures (profiles/*.md)
+# ----------------------------------------------------------------------------
+
+# Per workload: the kernel, the DRAM bytes read + written by one captured launch
+# (ncu dram__bytes_read.sum + dram__bytes_write.sum), that launch's algorithmic
+# bytes, and a fingerprint of the CUDA sources the capture was taken on.  The
+# bench scales the captured traffic to the timed launch by its algorithmic
+# bytes (the units processed) and reports null once the sources have changed.
+NCU_TRAFFIC: dict = {}
+
+
+def source_fingerprint() -> str:
+    """SHA-256 (first 16 hex digits) over the library's CUDA sources and header."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "query_aware_sparse_hs_gb300", "csrc")
+    files = sorted(os.path.join(csrc, f) for f in os.listdir(csrc) if f.endswith((".cu", ".cuh", ".h")))
+    for p in files + [os.path.join(ROOT, "include", "hs.h")]:
+        h.update(os.path.basename(p).encode())
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_entry(workload: str, kernel: str, algorithmic: int) -> dict:
+    e = NCU_TRAFFIC.get((workload, kernel))
+    if not e or e["sources"] != source_fingerprint():
+        return {"traffic": None, "traffic_note": "no ncu capture of the current kernel sources"}
+    scaled = e["traffic"] * algorithmic / e["algorithmic"]
+    return {"traffic": int(round(scaled)), "traffic_over_algorithmic": e["traffic"] / e["algorithmic"],
+            "traffic_note": e["note"]}
 
 
 # ----------------------------------------------------------------------------
@@ -208,23 +267,32 @@ def barrier(world: int):
         dist.barrier()
 
 
+def split_counts(n: int, per: int) -> list:
+    """n steps as whole rotations of `per` steps and one partial rotation."""
+    return [per] * (n // per) + ([n % per] if n % per else [])
+
+
 # ----------------------------------------------------------------------------
 # CPU baseline / reference arm: the oracle as it stands, one (request, kv head)
 # pair of the same workload per step, single thread
 # ----------------------------------------------------------------------------
 
 class OracleStep:
+    """The oracle's per-step work for one (request, kv head) pair of the
+    workload: append the newest token (resident workloads), bound, select,
+    [hot-buffer step for the offload workload], attend."""
+
     def __init__(self, w, pairs: int = 4):
         import numpy as np
-        import torch
         import oracle as O
-        from synth import make_inputs
+        from synth import drift_queries, make_inputs
         self.O, self.np = O, np
         self.w = w
         wb = w.scaled(batch=1)  # the sampled pairs come from one request of the workload
         x = make_inputs(wb, device="cpu")
         self.pairs = []
         B = w.block_size
+        self.drift = drift_queries(wb, x["q"], w.decode_steps).float().numpy() if w.offload else None
         for kvh in range(min(pairs, w.num_kv_heads)):
             row = x["page_table"][0, kvh].numpy()
             L = int(x["seq_lens"][0])
@@ -245,42 +313,56 @@ class OracleStep:
             qg = x["q"][0, kvh * g:(kvh + 1) * g].float().numpy().astype(np.float64)
             newest = (O.gather_rows(x["k_pages"].float().numpy(), row, L, B)[L - 1:],
                       O.gather_rows(x["v_pages"].float().numpy(), row, L, B)[L - 1:])
-            self.pairs.append((K, V, smin, smax, qg, L, newest))
+            hb = O.HotBuffer(O.num_blocks(L, B), w.hot_slots) if w.offload else None
+            self.pairs.append((kvh, K, V, smin, smax, qg, L, newest, hb))
         self.i = 0
 
     def step(self):
-        """One pair's per-step work: append the newest token (e4m3: quantise
-        it) and rebuild its block's summary, score, select, attend."""
-        O, w = self.O, self.w
-        K, V, smin, smax, qg, L, newest = self.pairs[self.i % len(self.pairs)]
+        """One pair's per-step work.  Returns the query heads served."""
+        O, w, np = self.O, self.w, self.np
+        kvh, K, V, smin, smax, qg, L, newest, hb = self.pairs[self.i % len(self.pairs)]
+        t = self.i // len(self.pairs)
         self.i += 1
-        B = w.block_size
-        if w.kv_dtype == "fp8":
-            for rows, dst in zip(newest, (K, V)):
-                dst[L - 1:] = O.kv_values("fp8", *O.quantize_e4m3_g32(rows))
+        B, g = w.block_size, w.group
+        if w.offload:
+            # the drifting query of decode step t; the context is held fixed
+            t = t % w.decode_steps
+            qg = self.drift[t, 0, kvh * g:(kvh + 1) * g].astype(np.float64)
         else:
-            K[L - 1:], V[L - 1:] = O.kv_values(w.kv_dtype, newest[0]), O.kv_values(w.kv_dtype, newest[1])
-        j = (L - 1) // B
-        lo, hi = O.stored_summaries(*O.block_summaries(K[j * B:L], B), w.kv_dtype)
-        smin[j], smax[j] = lo[0], hi[0]
+            if w.kv_dtype == "fp8":
+                for rows, dst in zip(newest, (K, V)):
+                    dst[L - 1:] = O.kv_values("fp8", *O.quantize_e4m3_g32(rows))
+            else:
+                K[L - 1:], V[L - 1:] = O.kv_values(w.kv_dtype, newest[0]), O.kv_values(w.kv_dtype, newest[1])
+            j = (L - 1) // B
+            lo, hi = O.stored_summaries(*O.block_summaries(K[j * B:L], B), w.kv_dtype)
+            smin[j], smax[j] = lo[0], hi[0]
         _, score = O.bound_scores(qg, smin, smax)
         sel = O.select_blocks(score, O.forced_blocks(L, B, w.sink_tokens, w.window_tokens), w.k_scored)
+        if hb is not None:
+            hb.step(sel, t)
         O.sparse_attention(qg, K, V, sel, B, 1.0 / math.sqrt(w.head_dim))
-        return w.group  # query heads served
+        return g
 
 
-def cpu_baseline(w, seconds: float = 12.0) -> dict:
-    st = OracleStep(w)
-    st.step()
+def _oracle_steps(st, seconds: float):
     t0 = time.perf_counter()
     heads, n = 0, 0
     while time.perf_counter() - t0 < seconds:
         heads += st.step()
         n += 1
-    dt = time.perf_counter() - t0
+    return heads, n, time.perf_counter() - t0
+
+
+def cpu_baseline(w, seconds: float) -> dict:
+    st = OracleStep(w)
+    st.step()
+    heads, n, dt = _oracle_steps(st, seconds)
+    what = "bound + selection + hot-buffer step + attention" if w.offload else \
+        "append + bound + selection + attention"
     return {"value": heads / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{n} single-(request, kv head) steps of {w.name} (8 query heads each, "
-                      f"{w.ctx_max} tokens, append + bound + selection + attention), "
+            "sample": f"{n} single-(request, kv head) steps of {w.name} ({w.group} query heads each, "
+                      f"request 0's {w.ctx_max if w.ctx_min == w.ctx_max else 'sampled'} tokens, {what}), "
                       f"numpy float64, 1 thread, {dt:.1f} s"}
 
 
@@ -292,14 +374,11 @@ def _oracle_worker(args):
     st = OracleStep(WORKLOADS[name])
     st.i = seed
     st.step()
-    t0 = time.perf_counter()
-    heads = 0
-    while time.perf_counter() - t0 < seconds:
-        heads += st.step()
-    return heads, time.perf_counter() - t0
+    heads, _, dt = _oracle_steps(st, seconds)
+    return heads, dt
 
 
-def cpu_baseline_all_cores(w, seconds: float = 12.0) -> dict:
+def cpu_baseline_all_cores(w, seconds: float) -> dict:
     """The same oracle step on every host core: one process per core, each on
     its own (request, kv head) pairs (the pairs are independent).  Processes are
     started with 'spawn', so no CUDA state is inherited."""
@@ -311,8 +390,8 @@ def cpu_baseline_all_cores(w, seconds: float = 12.0) -> dict:
     heads = sum(r[0] for r in res)
     dt = max(r[1] for r in res)
     return {"value": heads / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{cores} processes x {seconds:.0f} s of single-(request, kv head) steps of {w.name} "
-                      f"(append + bound + selection + attention), numpy float64, 1 thread each"}
+            "sample": f"{cores} processes x {seconds:.0f} s of single-(request, kv head) steps of {w.name}, "
+                      f"numpy float64, 1 thread each"}
 
 
 def run_reference(args, w):
@@ -331,48 +410,64 @@ def run_reference(args, w):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / max(args.steps, 1),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": workload_config(w, layers=1),
+            "data": "synthetic", "config": workload_config(w),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": f"each step = one (request, kv head) pair of {w.name}, numpy float64, 1 thread"},
+                             "sample": f"each step = one (request, kv head) pair of {w.name}, numpy float64, "
+                                       f"1 thread"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
-def workload_config(w, layers: int) -> dict:
-    return {"workload": w.name, "batch": w.batch, "num_q_heads": w.num_q_heads,
-            "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size,
-            "kv_dtype": w.kv_dtype,
-            "context": w.ctx_max if w.ctx_min == w.ctx_max else [w.ctx_min, w.ctx_max],
-            "sink_tokens": w.sink_tokens, "window_tokens": w.window_tokens, "k_scored": w.k_scored,
-            "layer_copies": layers,
-            "l2": f"inputs larger than L2: {layers} distinct layer copies rotate step to step",
-            "parallelism": "replicas"}
+def workload_config(w, layers: int | None = None) -> dict:
+    c = {"workload": w.name, "batch": w.batch, "num_q_heads": w.num_q_heads,
+         "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size,
+         "kv_dtype": w.kv_dtype,
+         "context": w.ctx_max if w.ctx_min == w.ctx_max else [w.ctx_min, w.ctx_max],
+         "sink_tokens": w.sink_tokens, "window_tokens": w.window_tokens, "k_scored": w.k_scored,
+         "parallelism": "replicas"}
+    if w.offload:
+        c.update(hot_slots_per_stream=w.hot_slots, decode_steps=w.decode_steps,
+                 l2="inputs larger than L2: hot buffer 2.1 GB and summaries 268 MB read every step")
+    elif layers is not None:
+        c.update(layer_copies=layers, l2=f"inputs larger than L2: {layers} distinct layer copies rotate step to step")
+    return c
 
 
 # ----------------------------------------------------------------------------
 # GPU arm
 # ----------------------------------------------------------------------------
 
-# DRAM bytes (read + written) of one launch of the dominant kernel from an ncu
-# capture of the current kernel, keyed by (workload, single-launch step); a
-# workload without a capture of the current kernel reports null.
-NCU_TRAFFIC = {("llama8b_bf16", True): 42_193_664}
+class Graphs:
+    """CUDA graphs of `fn(i)` over step ranges, captured once per range."""
+
+    def __init__(self, stream, fn):
+        self.stream, self.fn, self.cache = stream, fn, {}
+
+    def get(self, first: int, n: int):
+        import torch
+        key = (first, n)
+        if key not in self.cache:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=self.stream):
+                for i in range(first, first + n):
+                    self.fn(i)
+            self.cache[key] = g
+        return self.cache[key]
 
 
-def run_ours(args, w):
-    import numpy as np
+def _events():
+    import torch
+    return torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+
+def measure_resident(args, w, dev, world) -> dict:
+    """One of the workloads whose whole cache is in HBM.  Steps rotate over
+    distinct layer copies and replay from CUDA graphs."""
     import torch
 
     from query_aware_sparse_hs_gb300 import hs
     from query_aware_sparse_hs_gb300.decode import SparseDecode
     from synth import make_layer, make_layout
-
-    rank, world, local = dist_env()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
 
     layout = make_layout(w, dev)
     layers = args.layers
@@ -428,70 +523,82 @@ def run_ours(args, w):
     stream = torch.cuda.Stream(device=dev)
     torch.cuda.current_stream().wait_stream(stream)
 
-    def one_step(i, q_override=None):
+    def one_step(i):
         li = i % layers
         lead = li - li % args.select_every  # layer whose selection this layer uses
-        d = decs[li]
-        d.step(kvs[li], qs[li] if q_override is None else q_override, new_kv=news[li],
-               reuse=None if lead == li else decs[lead], stream=stream)
+        decs[li].step(kvs[li], qs[li], new_kv=news[li], reuse=None if lead == li else decs[lead], stream=stream)
 
     # eager warm-up (module load, cluster attributes) before capture
     with torch.cuda.stream(stream):
         for i in range(layers):
             one_step(i)
     stream.synchronize()
+    steps_g = Graphs(stream, one_step)
 
-    def capture(fn, n):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for i in range(n):
-                fn(i)
-        return g
+    def run_steps(n):
+        """Exactly n steps: whole rotations over the layers, then a partial one."""
+        for c in split_counts(n, layers):
+            steps_g.get(0, c).replay()
 
-    g_step = capture(one_step, layers)
-
-    def replay(g, reps):
-        for _ in range(reps):
-            g.replay()
-
-    reps = max(1, math.ceil(args.steps / layers))
-    steps = reps * layers
-    wreps = max(1, math.ceil(args.warmup / layers))
+    # set-up, outside the W + K steps: every graph the warm-up, the timed
+    # steps and the long run replay is captured and launched once (its
+    # upload), so no capture or first launch falls into a timed region
     with torch.cuda.stream(stream):
-        replay(g_step, wreps)
+        for c in sorted(set(split_counts(args.warmup, layers) + split_counts(args.steps, layers) + [layers])):
+            steps_g.get(0, c).replay()
+    stream.synchronize()
+    with torch.cuda.stream(stream):
+        run_steps(args.warmup)
     stream.synchronize()
 
-    clocks = ClockSampler(local)
+    clocks = ClockSampler(dev.index)
     clocks.start()
     time.sleep(0.3)
     barrier(world)
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0, e1 = _events()
     with torch.cuda.stream(stream):
         e0.record(stream)
-        replay(g_step, reps)
+        run_steps(args.steps)
         e1.record(stream)
     stream.synchronize()
     torch.cuda.synchronize()
     barrier(world)
+    value, ms = whole_job_rate(args.steps * w.batch * w.num_q_heads, e0.elapsed_time(e1), world, dev)
+    ms_per_step = ms / args.steps
+    # a long run (at least half a second of timed steps) beside the exact-K figure
+    rot_ms = ms_per_step * layers
+    long_reps = max(1, math.ceil(LONG_RUN_S * 1e3 / max(rot_ms, 1e-3)))
+    full = steps_g.get(0, layers)
+    a, b = _events()
+    with torch.cuda.stream(stream):
+        a.record(stream)
+        for _ in range(long_reps):
+            full.replay()
+        b.record(stream)
+    stream.synchronize()
     clk = clocks.stop()
-    value, ms = whole_job_rate(steps * w.batch * w.num_q_heads, e0.elapsed_time(e1), world, dev)
-    ms_per_step = ms / steps
+    long_steps = long_reps * layers
+    long_ms = a.elapsed_time(b)
+    long_run = {"steps": long_steps, "seconds": long_ms / 1e3, "ms_per_step": long_ms / long_steps,
+                "value": long_steps * w.batch * w.num_q_heads / (long_ms / 1e3)}
 
     # ---- per-kernel times (each kernel alone, the same rotating layers) ----
-    def timed_graph(fn, n=layers, rr=None):
-        g = capture(fn, n)
+    def timed_graph(fn, rr=None):
+        g = Graphs(stream, fn).get(0, layers)
         with torch.cuda.stream(stream):
-            replay(g, 2)
+            g.replay()
+            g.replay()
         stream.synchronize()
-        rr = rr or max(3, min(reps, 200))
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        rr = rr or max(3, min(long_reps, 200))
+        x0, x1 = _events()
         with torch.cuda.stream(stream):
-            a.record(stream)
-            replay(g, rr)
-            b.record(stream)
+            x0.record(stream)
+            for _ in range(rr):
+                g.replay()
+            x1.record(stream)
         stream.synchronize()
-        return a.elapsed_time(b) * 1e3 / (rr * n)  # microseconds per launch
+        return x0.elapsed_time(x1) * 1e3 / (rr * layers)  # microseconds per launch
 
     def lead_of(li):
         return decs[li - li % args.select_every]
@@ -501,6 +608,9 @@ def run_ours(args, w):
     fused = fused_step(w, decs[0])
     t_fused = (timed_graph(lambda i: decs[i % layers].select_attend(kvs[i % layers], qs[i % layers], stream=stream))
                if fused else None)
+    t_decode = (timed_graph(lambda i: decs[i % layers].decode_step(kvs[i % layers], qs[i % layers], *news[i % layers],
+                                                                    stream=stream))
+                if fused else None)
     t_sel = timed_graph(lambda i: decs[i % layers].select(kvs[i % layers], qs[i % layers], stream=stream))
     t_app = timed_graph(lambda i: decs[i % layers].append(kvs[i % layers], *news[i % layers], stream))
     t_sum_full = timed_graph(lambda i: decs[i % layers].build_summaries(kvs[i % layers], 0, stream), rr=3)
@@ -511,10 +621,10 @@ def run_ours(args, w):
     sel = d0.sel.cpu().numpy()
     lens_np = lens.cpu().numpy()
     sel_tokens = 0
-    for b in range(w.batch):
-        L = int(lens_np[b])
+    for bq in range(w.batch):
+        L = int(lens_np[bq])
         for kvh in range(w.num_kv_heads):
-            for j in sel[b, kvh, :cnt[b, kvh]]:
+            for j in sel[bq, kvh, :cnt[bq, kvh]]:
                 sel_tokens += min(B, L - int(j) * B)
     pairs_blocks = int(cnt.sum())
     total_blocks = int(sum(w.num_kv_heads * ((int(L) + B - 1) // B) for L in lens_np))
@@ -528,9 +638,12 @@ def run_ours(args, w):
     # the dominant kernel: the single scoring + selection + attention launch
     # where the step uses it, else the attention launch (with its merge)
     if fused:
-        dom = {"kernel": "score_select_attend (one launch)", "bytes": a_bytes + s_bytes, "us": t_fused}
+        dom = {"kernel": "score_select_attn_kernel", "what": "decode_step: append + scoring + selection + "
+                                                             "attention + split merge in one launch",
+               "bytes": a_bytes + s_bytes + append_bytes, "us": t_decode}
     else:
-        dom = {"kernel": "sparse_paged_decode_attn", "bytes": a_bytes, "us": t_attn}
+        dom = {"kernel": "attn_tc_fp8_kernel" if w.kv_dtype == "fp8" else "attn_tc_kernel",
+               "what": "sparse_paged_decode_attn", "bytes": a_bytes, "us": t_attn}
     dom_gbs = dom["bytes"] / (dom["us"] * 1e-6) / 1e9
 
     # ---- end to end through the C ABI with host buffers ----
@@ -550,84 +663,86 @@ def run_ours(args, w):
         with torch.cuda.stream(drain):
             res_host[li].copy_(decs[li].results, non_blocking=True)
 
-    g_e2e = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_e2e, stream=stream):
-        for i in range(layers):
-            e2e_step(i)
-        stream.wait_stream(drain)  # every result is on the host when a replay ends
-    with torch.cuda.stream(stream):
-        replay(g_e2e, 2)
+    class E2EGraphs(Graphs):
+        def get(self, first, n):
+            key = (first, n)
+            if key not in self.cache:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=self.stream):
+                    for i in range(first, first + n):
+                        e2e_step(i)
+                    self.stream.wait_stream(drain)  # every result is on the host when the graph ends
+                self.cache[key] = g
+            return self.cache[key]
+
+    e2e_g = E2EGraphs(stream, None)
+
+    def run_e2e(n):
+        for c in split_counts(n, layers):
+            e2e_g.get(0, c).replay()
+
+    with torch.cuda.stream(stream):  # capture and upload, then the W warm-up steps
+        for c in sorted(set(split_counts(args.warmup, layers) + split_counts(args.steps, layers))):
+            e2e_g.get(0, c).replay()
+        run_e2e(args.warmup)
     stream.synchronize()
     barrier(world)
-    a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a, b_ = _events()
     with torch.cuda.stream(stream):
         a.record(stream)
-        replay(g_e2e, reps)
+        run_e2e(args.steps)
         b_.record(stream)
     stream.synchronize()
-    e2e_value, ms_e2e = whole_job_rate(steps * w.batch * w.num_q_heads, a.elapsed_time(b_), world, dev)
-    assert torch.equal(res_host[layers - 1], decs[layers - 1].results.cpu()), "results drained to the host differ"
+    e2e_value, ms_e2e = whole_job_rate(args.steps * w.batch * w.num_q_heads, a.elapsed_time(b_), world, dev)
+    last = (args.steps - 1) % layers
+    assert torch.equal(res_host[last], decs[last].results.cpu()), "results drained to the host differ"
     h2d = inputs[0].numel() * inputs[0].element_size()
     d2h = d0.results.numel()
 
     st_, bits = hs.hs_get_device_error()
     assert st_ == hs.HS_OK, (st_, bits)
-
-    if rank != 0:
-        return
-    cpu = cpu_baseline(w, seconds=args.cpu_seconds) if (world == 1 and args.cpu_seconds > 0) else None
-    cpu_all = (cpu_baseline_all_cores(w, seconds=args.cpu_seconds / 2)
-               if (world == 1 and args.cpu_seconds > 0) else None)
-    # layers that reuse a selection skip its launches
     # a layer that reuses a selection runs append + attention (+ merge)
     reuse_launches = step_launches(w, d0, allow_fused=False) - select_launches(w)
     launches_per_step = step_launches(w, d0) / args.select_every + reuse_launches * (1 - 1 / args.select_every)
-    line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
-        "warmup": wreps * layers, "ms_per_step": ms_per_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": w.kv_dtype, "data": "synthetic",
-        "config": dict(workload_config(w, layers), select_every=args.select_every),
+    rec = {
+        "value": value, "unit": UNIT, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "dtype": w.kv_dtype, "config": dict(workload_config(w, layers), select_every=args.select_every),
         "hbm_gbs_step": step_bytes / (ms_per_step * 1e-3) / 1e9,
-        "roofline": {"bound": "hbm", "kernel": dom["kernel"], "achieved": dom_gbs,
-                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": dom_gbs / peak,
-                     "traffic": NCU_TRAFFIC.get((w.name, fused)), "algorithmic_bytes_per_launch": dom["bytes"],
-                     "avg_launch_us": dom["us"]},
-        "kernels_us": {"append": t_app, "score_select_attend": t_fused, "score_select": t_sel,
+        "roofline": dict({"bound": "hbm", "kernel": dom["kernel"], "what": dom["what"], "achieved": dom_gbs,
+                          "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": dom_gbs / peak},
+                         **traffic_entry(w.name, dom["kernel"], dom["bytes"]),
+                         algorithmic_bytes_per_launch=dom["bytes"], avg_launch_us=dom["us"]),
+        "kernels_us": {"decode_step": t_decode, "append": t_app, "score_select_attend": t_fused, "score_select": t_sel,
                        "attention_with_merge": t_attn, "summary_build_full": t_sum_full},
-        "kernels_gbs": {"score_select_attend": dom_gbs if fused else None,
+        "kernels_gbs": {"decode_step": dom_gbs if fused else None,
                         "score_select": s_bytes / (t_sel * 1e-6) / 1e9,
                         "attention_with_merge": attn_gbs,
                         "summary_build_full": full_sum_bytes / (t_sum_full * 1e-6) / 1e9},
         "bytes_per_step": {"attention": a_bytes, "score_select": s_bytes, "append": int(append_bytes)},
-        "cpu_baseline": cpu,
-        "cpu_baseline_all_cores": cpu_all,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": ms_e2e / steps},
-        "gpu_launches": int(round(launches_per_step * steps)),
+                "ms_per_step": ms_e2e / args.steps},
+        "long_run": long_run,
+        "gpu_launches": int(round(launches_per_step * args.steps)),
         "clocks": clk,
     }
-    print(json.dumps(line), flush=True)
+    del decs, kvs, qs, news, inputs, keep, steps_g, e2e_g
+    return rec
 
 
-def run_offload(args, w):
+def measure_offload(args, w, dev, world) -> dict:
     """HiSparse workload: every step = score/select against the summaries of the
     whole cache, swap-in of the missing pages from the pinned host pool into the
-    hot device buffer, attention over the hot slots, merge.  A pass is the 64-step
-    drifting-query sequence; step 0 (empty buffer) is warm-up, steps 1..63 are
-    timed.  Reports the miss rate and the swap-in bandwidth next to the measured
-    host-to-device copy bandwidth."""
+    hot device buffer (overlapped with the attention over the blocks already
+    resident), attention over the hot slots, merge.  A pass is the 64-step
+    drifting-query sequence; step 0 (empty buffer) refills it untimed, steps
+    1..63 are the timed steps.  Reports the miss rate and the swap-in bandwidth
+    next to the measured host-to-device copy bandwidth."""
     import torch
 
     from query_aware_sparse_hs_gb300 import hs
     from query_aware_sparse_hs_gb300.decode import SparseDecode
     from synth import drift_queries, make_layer, make_layout
 
-    rank, world, local = dist_env()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
     B, D, S, hkv = w.block_size, w.head_dim, w.hot_slots, w.num_kv_heads
     nb, pairs, steps_seq = w.max_blocks, w.batch * w.num_kv_heads, w.decode_steps
     layout = make_layout(w, dev)
@@ -656,6 +771,10 @@ def run_offload(args, w):
     if args.swap_overlap:
         dec.enable_swap_overlap(args.swap_copy_ctas, args.swap_attn_ctas)
     stream = torch.cuda.Stream(device=dev)
+    # the query of the step being run: the end-to-end form copies each step's
+    # query from pinned host memory into this buffer; the resident form uses
+    # the device copy of the whole drift sequence
+    q_in = torch.empty_like(qs[0])
 
     def reset():
         table.fill_(-1)
@@ -663,65 +782,101 @@ def run_offload(args, w):
         last.fill_(-1)
         dec.reset_score_history()
 
-    def step(t, st=None):
-        dec.step(pool_kv, qs[t], hot=(hb, slot_kv, t, st), stream=stream)
+    def step(t, st=None, q=None):
+        dec.step(pool_kv, qs[t] if q is None else q, hot=(hb, slot_kv, t, st), stream=stream)
 
-    # warm-up pass (eager), then capture steps 1..63 of a pass
+    timed_per_pass = steps_seq - 1
+    # graphs over decode steps first..first+n-1 of a pass (first >= 1)
+    step_g = Graphs(stream, lambda t: step(t, stats))
+
+    def segments(start, n):
+        """Positions start..start+n-1 of the endless run of decode steps
+        (position p = decode step 1 + p % 63 of pass p // 63) as graph
+        segments (first step, count, refill before): a pass begins with an
+        untimed reset and step 0, the refill of the empty hot buffer."""
+        out, p, end = [], start, start + n
+        while p < end:
+            t = 1 + p % timed_per_pass
+            c = min(end - p, timed_per_pass - (t - 1))
+            out.append((t, c, t == 1))
+            p += c
+        return out
+
+    def run_segments(segs, graphs=step_g, timed=False):
+        """Replays the segments; returns the device time of their steps (ms)
+        when timed (the refills are outside the events)."""
+        total = 0.0
+        for first, cnt, refill in segs:
+            g = graphs.get(first, cnt)
+            with torch.cuda.stream(stream):
+                if refill:
+                    reset()
+                    step(0)
+                if timed:
+                    a, b = _events()
+                    a.record(stream)
+                g.replay()
+                if timed:
+                    b.record(stream)
+            if timed:
+                stream.synchronize()
+                total += a.elapsed_time(b)
+        stream.synchronize()
+        return total
+
+    def upload(segs, graphs=step_g):
+        """Set-up: capture each segment's graph and launch it once (its upload)
+        on a throw-away pass, so that no capture or first launch is timed."""
+        for first, cnt, _ in segs:
+            run_segments([(first, cnt, True)], graphs)
+
+    warm_segs = segments(0, args.warmup)
+    timed_segs = segments(args.warmup, args.steps)
+    long_start = -(-(args.warmup + args.steps) // timed_per_pass) * timed_per_pass
+    # eager pass (module load, attributes), then the graphs' set-up
     with torch.cuda.stream(stream):
         reset()
         for t in range(steps_seq):
             step(t, stats)
     stream.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=stream):
-        for t in range(1, steps_seq):
-            step(t, stats)
-    # the same steps with the swap-in and attention one after the other
-    side, dec.side_stream = getattr(dec, "side_stream", None), None
-    g_serial = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_serial, stream=stream):
-        for t in range(1, steps_seq):
-            step(t, stats)
-    dec.side_stream = side
-    timed_steps = steps_seq - 1
-    passes = max(1, math.ceil(args.steps / timed_steps))
-    warm_passes = max(1, math.ceil(args.warmup / timed_steps))
-
-    def run_pass(timed, graph=g):
-        with torch.cuda.stream(stream):
-            reset()
-            step(0)  # refills the empty buffer: warm-up, not timed
-            a = b = None
-            if timed:
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record(stream)
-            graph.replay()
-            if timed:
-                b.record(stream)
-        stream.synchronize()
-        return a.elapsed_time(b) if timed else 0.0
-
-    for _ in range(warm_passes):
-        run_pass(False)
+    upload(warm_segs + timed_segs + [(1, timed_per_pass, True)])
+    # the run: W warm-up steps, then exactly K timed steps that follow them
+    run_segments(warm_segs)
     stats.zero_()
-    clocks = ClockSampler(local)
+    clocks = ClockSampler(dev.index)
     clocks.start()
     time.sleep(0.3)
     barrier(world)
     torch.cuda.synchronize()
-    ms = sum(run_pass(True) for _ in range(passes))
+    ms = run_segments(timed_segs, timed=True)
     torch.cuda.synchronize()
     barrier(world)
-    clk = clocks.stop()
     st = stats.cpu().tolist()
-    steps = passes * timed_steps
-    serial_passes = max(1, min(passes, 4))
-    run_pass(False, g_serial)
-    ms_serial = sum(run_pass(True, g_serial) for _ in range(serial_passes)) / (serial_passes * timed_steps)
-    value, ms = whole_job_rate(steps * w.batch * w.num_q_heads, ms, world, dev)
-    ms_per_step = ms / steps
+    value, ms = whole_job_rate(args.steps * w.batch * w.num_q_heads, ms, world, dev)
+    ms_per_step = ms / args.steps
+    # long run: whole passes, at least half a second of timed steps
+    long_passes = max(1, math.ceil(LONG_RUN_S * 1e3 / max(ms_per_step * timed_per_pass, 1e-3)))
+    stats.zero_()
+    long_ms = run_segments(segments(long_start, long_passes * timed_per_pass), timed=True)
+    clk = clocks.stop()
+    long_steps = long_passes * timed_per_pass
+    st_long = stats.cpu().tolist()
+    long_run = {"steps": long_steps, "seconds": long_ms / 1e3, "ms_per_step": long_ms / long_steps,
+                "value": long_steps * w.batch * w.num_q_heads / (long_ms / 1e3),
+                "miss_rate": st_long[1] / max(1, st_long[0] + st_long[1]),
+                "what": f"{long_passes} whole passes of decode steps 1..{timed_per_pass}"}
 
-    # per-kernel times over one pass, each kernel bracketed by events (eager)
+    # the same steps with the swap-in and the attention one after the other
+    side, dec.side_stream = getattr(dec, "side_stream", None), None
+    serial_g = Graphs(stream, lambda t: step(t, stats))
+    serial_g.get(1, timed_per_pass)
+    dec.side_stream = side
+    run_segments(segments(0, timed_per_pass), serial_g)
+    ms_serial = run_segments(segments(0, timed_per_pass), serial_g, timed=True) / timed_per_pass
+
+    # per-kernel times over one pass, each call bracketed by events (eager,
+    # serial form); the pass's own swap-in statistics go with its times
+    stats_pass = torch.zeros(4, dtype=torch.int64, device=dev)
     ev = {k: [] for k in ("select", "swapin", "attention")}
     with torch.cuda.stream(stream):
         reset()
@@ -731,7 +886,7 @@ def run_offload(args, w):
             e[0].record(stream)
             dec.select(pool_kv, qs[t], stream=stream)
             e[1].record(stream)
-            dec.swap_in(hb, t, None, stream)
+            dec.swap_in(hb, t, stats_pass, stream)
             e[2].record(stream)
             dec.attend(slot_kv, qs[t], stream=stream)
             e[3].record(stream)
@@ -740,6 +895,42 @@ def run_offload(args, w):
             ev["attention"].append(e[2:4])
     stream.synchronize()
     t_us = {k: 1e3 * sum(a.elapsed_time(b) for a, b in v) / len(v) for k, v in ev.items()}
+    sel_blocks_step = int(dec.sel_count.sum().item())
+    st_pass = stats_pass.cpu().tolist()
+
+    # ---- end to end through the C ABI with host buffers: every step copies
+    # its query from pinned host memory and its results (out, lse) back ----
+    q_host = qs.cpu().pin_memory()
+    res_host = torch.empty((steps_seq, dec.results.numel()), dtype=torch.uint8).pin_memory()
+    drain = torch.cuda.Stream(device=dev)
+
+    def e2e_step(t):
+        q_in.copy_(q_host[t], non_blocking=True)
+        step(t, stats, q_in)
+        drain.wait_stream(stream)
+        with torch.cuda.stream(drain):
+            res_host[t].copy_(dec.results, non_blocking=True)
+
+    class E2EGraphs(Graphs):
+        def get(self, first, n):
+            key = (first, n)
+            if key not in self.cache:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=self.stream):
+                    for t in range(first, first + n):
+                        e2e_step(t)
+                    self.stream.wait_stream(drain)  # every result is on the host when the graph ends
+                self.cache[key] = g
+            return self.cache[key]
+
+    e2e_g = E2EGraphs(stream, None)
+    upload(warm_segs + timed_segs, e2e_g)
+    run_segments(warm_segs, e2e_g)
+    barrier(world)
+    ms_e2e = run_segments(timed_segs, e2e_g, timed=True)
+    e2e_value, ms_e2e = whole_job_rate(args.steps * w.batch * w.num_q_heads, ms_e2e, world, dev)
+    t_last = 1 + (args.warmup + args.steps - 1) % timed_per_pass
+    assert torch.equal(res_host[t_last], dec.results.cpu()), "results drained to the host differ"
     st_, bits = hs.hs_get_device_error()
     assert st_ == hs.HS_OK, (st_, bits)
 
@@ -748,59 +939,112 @@ def run_offload(args, w):
     dst = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
     link = 0.0
     for _ in range(5):
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a, b = _events()
         a.record()
         dst.copy_(src, non_blocking=True)
         b.record()
         torch.cuda.synchronize()
         link = max(link, (1 << 30) / (a.elapsed_time(b) * 1e-3) / 1e9)
+    del src, dst
 
     hits, misses, evictions, bytes_in = st
     page_bytes = B * token_bytes(w)  # K+V of one block
-    sel_tokens = int(dec.sel_count.sum().item()) * B
-    a_bytes = attn_bytes(w, sel_tokens, int(dec.sel_count.sum().item()))
+    a_bytes = attn_bytes(w, sel_blocks_step * B, sel_blocks_step)
+    s_bytes = select_bytes(w, pairs * nb)
     peak, peak_kind = load_peaks()
     attn_gbs = a_bytes / (t_us["attention"] * 1e-6) / 1e9
-    swap_bytes_step = bytes_in / steps
-    if rank != 0:
-        return
-    line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
-        "warmup": warm_passes * steps_seq, "ms_per_step": ms_per_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": w.kv_dtype, "data": "synthetic",
-        "config": dict(workload_config(w, 1), hot_slots_per_stream=S, decode_steps=steps_seq,
-                       l2="hot buffer 2.1 GB and summaries 268 MB per step, both above L2"),
-        "roofline": {"bound": "hbm", "kernel": "sparse_paged_decode_attn (hot slots)", "achieved": attn_gbs,
-                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": attn_gbs / peak,
-                     "traffic": None, "algorithmic_bytes_per_launch": a_bytes,
-                     "avg_launch_us": t_us["attention"]},
-        "swap": {"miss_rate": misses / max(1, hits + misses), "misses_per_step": misses / steps,
-                 "evictions_per_step": evictions / steps, "bytes_in_per_step": swap_bytes_step,
-                 "swapin_us": t_us["swapin"], "swapin_gbs": swap_bytes_step / (t_us["swapin"] * 1e-6) / 1e9,
+    swap_bytes_step = bytes_in / args.steps
+    pass_swap_bytes = st_pass[3] / timed_per_pass  # the eager pass whose swap-in was timed
+    rec = {
+        "value": value, "unit": UNIT, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "dtype": w.kv_dtype,
+        "config": dict(workload_config(w), overlapped_swap_in=bool(args.swap_overlap),
+                       score_smoothing=args.score_smoothing),
+        "hbm_gbs_step": (a_bytes + s_bytes) / (ms_per_step * 1e-3) / 1e9,
+        "roofline": dict({"bound": "hbm", "kernel": "attn_tc_kernel",
+                          "what": "sparse_paged_decode_attn over the hot slots (all selected blocks)",
+                          "achieved": attn_gbs, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                          "frac": attn_gbs / peak},
+                         **traffic_entry(w.name, "attn_tc_kernel", a_bytes),
+                         algorithmic_bytes_per_launch=a_bytes, avg_launch_us=t_us["attention"]),
+        "swap": {"miss_rate": misses / max(1, hits + misses), "misses_per_step": misses / args.steps,
+                 "evictions_per_step": evictions / args.steps, "bytes_in_per_step": swap_bytes_step,
+                 "timed_steps": f"the {args.steps} decode steps after {args.warmup} warm-up steps of the "
+                                f"{steps_seq}-step drifting sequence (step 0 of a pass refills the empty buffer, untimed)",
+                 "swapin_us_per_pass_step": t_us["swapin"],
+                 "swapin_bytes_per_pass_step": pass_swap_bytes,
+                 "miss_rate_pass": st_pass[1] / max(1, st_pass[0] + st_pass[1]),
+                 "swapin_gbs": pass_swap_bytes / (t_us["swapin"] * 1e-6) / 1e9,
                  "link_h2d_gbs_measured": link,
-                 "link_frac": swap_bytes_step / (t_us["swapin"] * 1e-6) / 1e9 / link,
+                 "link_frac": pass_swap_bytes / (t_us["swapin"] * 1e-6) / 1e9 / link,
                  "page_bytes": page_bytes},
-        "kernels_us": {"score_select": t_us["select"], "swapin": t_us["swapin"], "attention_with_merge": t_us["attention"]},
-        "score_smoothing": args.score_smoothing,
-        "swap_overlap": {"overlapped": bool(args.swap_overlap), "copy_ctas": args.swap_copy_ctas,
-                         "attn_ctas": args.swap_attn_ctas, "serial_ms_per_step": ms_serial},
-        "cpu_baseline": cpu_baseline(w, seconds=args.cpu_seconds) if (world == 1 and args.cpu_seconds > 0) else None,
-        "e2e": None,
-        "gpu_launches": step_launches(w, dec, hot=True, overlap=bool(args.swap_overlap)) * steps,
+        "kernels_us": {"score_select": t_us["select"], "swapin": t_us["swapin"],
+                       "attention_with_merge": t_us["attention"]},
+        "kernels_gbs": {"score_select": s_bytes / (t_us["select"] * 1e-6) / 1e9, "attention_with_merge": attn_gbs},
+        "bytes_per_step": {"attention": a_bytes, "score_select": s_bytes, "swap_in_host": int(swap_bytes_step)},
+        "serial_ms_per_step": ms_serial,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": q_in.numel() * q_in.element_size(),
+                "d2h_bytes_per_step": dec.results.numel(), "ms_per_step": ms_e2e / args.steps,
+                "note": "the swap-in's own reads of the pinned host pool are part of the step, not of these copies"},
+        "long_run": long_run,
+        "gpu_launches": step_launches(w, dec, hot=True, overlap=bool(args.swap_overlap)) * args.steps,
         "clocks": clk,
     }
+    del dec, hb, slot_kv, pool_kv, host_k, host_v, k_slots, v_slots, step_g, serial_g, e2e_g
+    return rec
+
+
+def run_ours(args, names):
+    import torch
+    from synth import WORKLOADS
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    recs = {}
+    for name in names:
+        w = WORKLOADS[name]
+        if args.batch > 0:
+            w = w.scaled(batch=args.batch)
+        rec = measure_offload(args, w, dev, world) if w.offload else measure_resident(args, w, dev, world)
+        import gc
+        gc.collect()
+        torch.cuda.empty_cache()
+        recs[name] = rec
+    if rank != 0:
+        return
+    if world == 1 and args.cpu_seconds > 0:
+        for name in names:
+            w = WORKLOADS[name]
+            recs[name]["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+        recs[names[0]]["cpu_baseline_all_cores"] = cpu_baseline_all_cores(WORKLOADS[names[0]], args.cpu_seconds)
+    head = recs[names[0]]
+    line = {"metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": head["dtype"], "data": "synthetic",
+            "config": head["config"]}
+    for k, v in head.items():
+        if k not in line and k not in ("steps", "warmup"):
+            line[k] = v
+    if len(names) > 1:
+        line["workloads"] = {n: recs[n] for n in names[1:]}
+        line["gpu_launches_all_workloads"] = sum(recs[n]["gpu_launches"] for n in names)
     print(json.dumps(line), flush=True)
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=32000)
-    ap.add_argument("--warmup", type=int, default=640)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="llama8b_bf16")
+    ap.add_argument("--workload", default="all", help="all, or one workload name")
+    ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling captures)")
     ap.add_argument("--layers", type=int, default=0, help="distinct layer copies (0 = fit ~24 GB, max 32)")
-    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--cpu-seconds", type=float, default=8.0)
     ap.add_argument("--select-every", type=int, default=1,
                     help="layers per selection: the first layer of each group selects, the others reuse it "
                          "(SparDA-style cross-layer reuse); 1 = every layer selects")
@@ -812,17 +1056,22 @@ def main():
     ap.add_argument("--swap-attn-ctas", type=int, default=0,
                     help="CTAs of the attention beside the copy (0 = the SMs the copy leaves)")
     args = ap.parse_args()
-    args.warmup = max(args.warmup, 3)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.steps < 1:
+        ap.error("--steps must be >= 1")
     if args.select_every < 1:
         ap.error("--select-every must be >= 1")
     from synth import WORKLOADS
-    w = WORKLOADS[args.workload]
+    names = [HEADLINE, *SUB_WORKLOADS] if args.workload == "all" else [args.workload]
+    for n in names:
+        if n not in WORKLOADS:
+            ap.error(f"unknown workload {n}")
     if args.impl == "reference":
-        run_reference(args, w)
-    elif w.offload:
-        run_offload(args, w)
+        w = WORKLOADS[names[0]]
+        run_reference(args, w.scaled(batch=args.batch) if args.batch > 0 else w)
     else:
-        run_ours(args, w)
+        run_ours(args, names)
 
 
 if __name__ == "__main__":

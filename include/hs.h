@@ -158,7 +158,14 @@ typedef struct hs_select_params {
  * them all into out/lse and sets the counter back to zero; no separate merge
  * kernel is launched (otherwise one is).  Every counter is zero again when the
  * call has completed; after HS_ERR_TIMEOUT, zero the array before reusing it.
- * NULL (and the CUDA-core kernel): the merge runs as a separate kernel. */
+ * NULL (and the CUDA-core kernel): the merge runs as a separate kernel.
+ * wait_limit_ns: bound, in nanoseconds, of every wait inside the tensor-core
+ * attention (and the single-launch step) for data, a product or another role
+ * of its CTA; 0 = the default of 2 s.  When a wait runs out the CTA stops all
+ * of its roles, lets the copies and products it already issued finish, frees
+ * its tensor memory and returns; the call's outputs are then undefined and
+ * hs_get_device_error reports HS_ERR_TIMEOUT.  A limit far below a launch's
+ * duration makes a wait run out on purpose (the bounded-wait test does). */
 typedef struct hs_attn_params {
   float scale;
   int32_t out_is_fp32;
@@ -166,6 +173,7 @@ typedef struct hs_attn_params {
   int32_t algo;
   int32_t max_ctas;
   uint32_t* split_counters;
+  uint32_t wait_limit_ns;
 } hs_attn_params;
 
 /* HiSparse hot buffer ([KVS] §7).  One stream per (request, kv head) owns
@@ -313,14 +321,34 @@ HS_API hs_status hs_score_select_attend(const hs_attn_shape* shape, const hs_pag
                                         const hs_attn_params* attn_params, void* out, float* lse_opt,
                                         void* workspace, size_t ws_bytes, hs_stream_t stream);
 
-/* 1 when hs_score_select_attend runs as a single launch (plus the split merge
- * when attn_params has no split_counters and a pair has several splits) for
- * this geometry on the current device, 0 when it runs the separate launches,
+/* 1 when hs_score_select_attend runs as a single launch for this geometry on
+ * the current device (its clusters merge their splits themselves, with or
+ * without split_counters), 0 when it runs the separate launches,
  * -1 on invalid input or without a device.  Depends on the shape, batch,
  * max_blocks, capacity and attn_params only (for page pools below 2^31
  * token rows, the tensor-core attention's own limit). */
 HS_API int32_t hs_score_select_attend_fused(const hs_attn_shape* shape, int32_t batch, int32_t max_blocks,
                                             int32_t capacity, const hs_attn_params* attn_params);
+
+/* One whole decode step of one layer: hs_append_token(shape, kv, new_k,
+ * new_v, smin, smax) followed by hs_score_select_attend(shape, kv, q, smin,
+ * smax, sel_params, ...), with the same argument rules, outputs and error bits
+ * ([KVS] §5: the newest token's block summary covers it before the query is
+ * scored; [KVS] §2 and §5 selection; [FLL] §2.2 attention).  new_k / new_v:
+ * [batch][Hkv][head_dim] in the source precision (bf16, or f32 for an f32
+ * cache), device, 16-byte aligned; each is written at position
+ * seq_lens[b] - 1 (the caller has advanced seq_lens and given a new block its
+ * page).  Where hs_score_select_attend is a single launch
+ * (hs_score_select_attend_fused), the append runs inside that launch: the CTA
+ * that scores the newest token's block writes the token into its page and
+ * widens the block's summary in the copy it scores and in smin/smax.
+ * Otherwise the append kernel runs first.  The K/V pages and smin/smax are
+ * written; the page pointers of kv are used for writing here. */
+HS_API hs_status hs_decode_step(const hs_attn_shape* shape, const hs_paged_kv* kv, const void* q,
+                                const void* new_k, const void* new_v, void* smin, void* smax,
+                                const hs_select_params* sel_params, int32_t* sel, int32_t* sel_count,
+                                float* scores_opt, const hs_attn_params* attn_params, void* out,
+                                float* lse_opt, void* workspace, size_t ws_bytes, hs_stream_t stream);
 
 /* HiSparse swap-in, [KVS] §7: for every (b, kvh), make each selected block
  * resident in the stream's hot slots.  Hits set last_used = step.  Misses are

@@ -220,6 +220,7 @@ hs_status prepare_attn(const hs_attn_shape* shape, const hs_paged_kv* kv, const 
   a.sms = ctas;
   if (params->split_counters && !aligned(params->split_counters, 4)) return HS_ERR_INVALID_ARG;
   a.counters = params->split_counters;
+  a.wait_ns = static_cast<uint64_t>(params->wait_limit_ns);
   a.q = q;
   a.sel = sel;
   a.sel_count = sel_count;
@@ -367,14 +368,23 @@ int32_t hs_score_select_attend_fused(const hs_attn_shape* shape, int32_t batch, 
   return score_select_attn_supported(v, a, d.sms) ? 1 : 0;
 }
 
-hs_status hs_score_select_attend(const hs_attn_shape* shape, const hs_paged_kv* kv, const void* q,
-                                 const void* smin, const void* smax, const hs_select_params* sel_params,
-                                 int32_t* sel, int32_t* sel_count, float* scores_opt,
-                                 const hs_attn_params* attn_params, void* out, float* lse_opt, void* workspace,
-                                 size_t ws_bytes, hs_stream_t stream) {
+}  // extern "C"
+
+namespace hs {
+namespace {
+
+// Selection and attention of one step, preceded by the append of the newest
+// token when new_k is given: one launch where the geometry allows, else the
+// separate launches in order.
+hs_status select_attend(const hs_attn_shape* shape, const hs_paged_kv* kv, const void* q, const void* new_k,
+                        const void* new_v, const void* smin, const void* smax, const hs_select_params* sel_params,
+                        int32_t* sel, int32_t* sel_count, float* scores_opt, const hs_attn_params* attn_params,
+                        void* out, float* lse_opt, void* workspace, size_t ws_bytes, cudaStream_t s) {
   SelectArgs sa;
   hs_status st = prepare_select(shape, kv, q, smin, smax, sel_params, sel, sel_count, scores_opt, &sa);
   if (st != HS_OK) return st;
+  if (new_k && (!new_v || !aligned(new_k, 16) || !aligned(new_v, 16))) return HS_ERR_INVALID_ARG;
+  if (new_k && static_cast<int64_t>(kv->batch) * shape->num_kv_heads > INT32_MAX) return HS_ERR_UNSUPPORTED;
   // workspace: the selection's score buffer first, the attention's partials after it
   const size_t sw = hs_select_workspace_bytes(shape, kv->batch, kv->max_blocks);
   if (sw > 0 && (!workspace || ws_bytes < sw || !aligned(workspace, 16))) return HS_ERR_WORKSPACE;
@@ -387,16 +397,44 @@ hs_status hs_score_select_attend(const hs_attn_shape* shape, const hs_paged_kv* 
                     &d, &a, &use_tc);
   if (st != HS_OK) return st;
   const KvView v = make_view(shape, kv);
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (use_tc && a.sms == d.sms && score_select_attn_supported(v, a, d.sms)) {
-    if (launch_score_select_attn(v, smin, smax, sa, a, d.err, s) != cudaSuccess) return HS_ERR_CUDA;
+    if (launch_score_select_attn(v, smin, smax, sa, a, d.err, s, new_k, new_v) != cudaSuccess) return HS_ERR_CUDA;
   } else {
+    if (new_k && launch_append(v, new_k, new_v, const_cast<void*>(smin), const_cast<void*>(smax), d.err, s) !=
+                     cudaSuccess)
+      return HS_ERR_CUDA;
     if ((st = run_select(v, sa, d, workspace, sw, s)) != HS_OK) return st;
     cudaError_t e = use_tc ? launch_attn_tc(v, a, d.err, s) : launch_attn_simt(v, a, d.err, s);
     if (e != cudaSuccess) return HS_ERR_CUDA;
   }
   if (a.merged) return HS_OK;
   return from_cuda(launch_merge(v, a, s));
+}
+
+}  // namespace
+}  // namespace hs
+
+extern "C" {
+
+hs_status hs_score_select_attend(const hs_attn_shape* shape, const hs_paged_kv* kv, const void* q,
+                                 const void* smin, const void* smax, const hs_select_params* sel_params,
+                                 int32_t* sel, int32_t* sel_count, float* scores_opt,
+                                 const hs_attn_params* attn_params, void* out, float* lse_opt, void* workspace,
+                                 size_t ws_bytes, hs_stream_t stream) {
+  return select_attend(shape, kv, q, nullptr, nullptr, smin, smax, sel_params, sel, sel_count, scores_opt,
+                       attn_params, out, lse_opt, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+hs_status hs_decode_step(const hs_attn_shape* shape, const hs_paged_kv* kv, const void* q, const void* new_k,
+                         const void* new_v, void* smin, void* smax, const hs_select_params* sel_params, int32_t* sel,
+                         int32_t* sel_count, float* scores_opt, const hs_attn_params* attn_params, void* out,
+                         float* lse_opt, void* workspace, size_t ws_bytes, hs_stream_t stream) {
+  hs_status st = check_shape(shape);
+  if (st != HS_OK) return st;
+  if ((st = check_kv(shape, kv, true)) != HS_OK) return st;
+  if (!new_k || !new_v) return HS_ERR_INVALID_ARG;
+  return select_attend(shape, kv, q, new_k, new_v, smin, smax, sel_params, sel, sel_count, scores_opt, attn_params,
+                       out, lse_opt, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
 static hs_status device_address(const void* p, const void** out) {

@@ -34,6 +34,7 @@ struct AttnArgs {
   int32_t splits;
   int32_t sms;  // multiprocessors of the current device (persistent grid size)
   int32_t merged = 0;  // set by a launcher that already wrote out / lse (fused merge)
+  uint64_t wait_ns = 0;  // bound of the tensor-core kernels' waits (0: the default 2 s)
 };
 
 struct HotView {
@@ -72,8 +73,11 @@ bool attn_tc_supported(const KvView& kv);
 // Bound scoring, selection and tensor-core attention in one cluster launch
 // (bf16, head_dim 128, g <= 8, every pair in one wave of at most 8 CTAs).
 bool score_select_attn_supported(const KvView& kv, const AttnArgs& a, int sms);
+// new_k / new_v (nullable): the newest token of every pair is appended first
+// (written into its page, its block's summary widened), as launch_append does.
 cudaError_t launch_score_select_attn(const KvView& kv, const void* smin, const void* smax, const SelectArgs& sa,
-                                     AttnArgs& a, unsigned* err, cudaStream_t st);
+                                     AttnArgs& a, unsigned* err, cudaStream_t st, const void* new_k = nullptr,
+                                     const void* new_v = nullptr);
 // LSE merge of `parts` partial results laid out [parts][rows][D] and [parts][rows].
 cudaError_t launch_merge_parts(int rows, int head_dim, int parts, const float* outs, const float* lses, void* out,
                                int out_f32, float* lse_out, cudaStream_t st);

@@ -74,6 +74,7 @@ struct TcArgs {
   int hkv, hq, group, block, max_blocks, capacity, bps, splits, items;
   int out_f32;
   float scale_log2;
+  uint64_t wait_ns;  // bound of every wait of the CTA's roles
 };
 
 template <int NH>
@@ -311,7 +312,7 @@ __device__ __forceinline__ void run_producer(const TcArgs& a, const Work& w, int
         int go = 0;
         if (lane == 0)
           go = !*abort_flag &&
-               (c < STAGES || mbar_wait(empty0 + 8 * (c % STAGES), ((c / STAGES) + 1) & 1, abort_flag));
+               (c < STAGES || mbar_wait(empty0 + 8 * (c % STAGES), ((c / STAGES) + 1) & 1, abort_flag, a.wait_ns));
         if (!__shfl_sync(0xffffffffu, go, 0)) {
           stop = true;
           break;
@@ -337,7 +338,7 @@ __device__ __forceinline__ void run_producer(const TcArgs& a, const Work& w, int
     // let every copy this CTA issued land before the CTA can exit
     for (int s = 0; s < STAGES && s < c; ++s) {
       const int last = c - 1 - ((c - 1 - s) % STAGES);
-      mbar_wait(full0 + 8 * s, (last / STAGES) & 1, abort_flag, 500000000ull);
+      mbar_drain(full0 + 8 * s, (last / STAGES) & 1);
     }
   }
 }
@@ -494,14 +495,14 @@ __device__ __forceinline__ void attn_bf16_cta(const CUtensorMap* tm_k_, const CU
         const int next = item + w.stride;
         const Item nit = next < a.items ? item_geom(a, next, bpc, w) : Item{};  // in flight meanwhile
         if (it.nch > 0 && first) {
-          ok = mbar_wait(q_full, qi & 1, abort_flag);
+          ok = mbar_wait(q_full, qi & 1, abort_flag, a.wait_ns);
           ++qi;
         }
         for (int ci = 0; ok && ci < it.nch; ++ci, ++c) {
           const int st = c % kStages, bb = c & 1;
           if (first) {
-            ok = mbar_wait(full_bar(st), (c / kStages) & 1, abort_flag) &&
-                 (c < 2 || mbar_wait(s_free(bb), ((c >> 1) + 1) & 1, abort_flag));
+            ok = mbar_wait(full_bar(st), (c / kStages) & 1, abort_flag, a.wait_ns) &&
+                 (c < 2 || mbar_wait(s_free(bb), ((c >> 1) + 1) & 1, abort_flag, a.wait_ns));
             if (!ok) break;
             tc_fence_after();
 #pragma unroll
@@ -512,8 +513,8 @@ __device__ __forceinline__ void attn_bf16_cta(const CUtensorMap* tm_k_, const CU
             }
             mma_commit(s_full(bb));
           } else {
-            ok = mbar_wait(p_full(bb), (c >> 1) & 1, abort_flag) &&
-                 (c < 2 || mbar_wait(o_free(bb), ((c >> 1) + 1) & 1, abort_flag));
+            ok = mbar_wait(p_full(bb), (c >> 1) & 1, abort_flag, a.wait_ns) &&
+                 (c < 2 || mbar_wait(o_free(bb), ((c >> 1) + 1) & 1, abort_flag, a.wait_ns));
             if (!ok) break;
             tc_fence_after();
 #pragma unroll
@@ -530,13 +531,10 @@ __device__ __forceinline__ void attn_bf16_cta(const CUtensorMap* tm_k_, const CU
         item = next;
         it = nit;
       }
-      if (!first) {
-        // every commit has landed before TMEM is released
-        for (int st = 0; st < kStages && st < c; ++st) {
-          const int last = c - 1 - ((c - 1 - st) % kStages);
-          mbar_wait(empty_bar(st), (last / kStages) & 1, abort_flag, 500000000ull);
-        }
-      }
+      // every product this thread issued is complete before TMEM is released
+      // (a commit arrives once all of the thread's earlier MMAs are done)
+      if (first && c > 0) mbar_drain(s_full((c - 1) & 1), ((c - 1) >> 1) & 1);
+      if (!first && c > 0) mbar_drain(empty_bar((c - 1) % kStages), ((c - 1) / kStages) & 1);
     }
   } else {
     // ================= softmax / correction: two groups of 4 warps =================
@@ -559,6 +557,10 @@ __device__ __forceinline__ void attn_bf16_cta(const CUtensorMap* tm_k_, const CU
                                                  ch * 8);
       }
     };
+    // A wait that runs out must not leave a barrier short: every wait's
+    // outcome is made uniform across the warp before the warp-wide TMEM loads,
+    // and across the group (or both groups) at each named barrier (bar.red.or),
+    // so that the threads of a group leave their loops at the same point.
     int c = 0;
     int item = w.first;
     Item it{};
@@ -567,7 +569,7 @@ __device__ __forceinline__ void attn_bf16_cta(const CUtensorMap* tm_k_, const CU
       it = item_geom(a, item, bpc, w);
       if (grp == 0) load_q(item, qv);
     }
-    for (; item < a.items && !*abort_flag;) {
+    while (item < a.items) {
       // the next item's geometry and query rows are fetched while this one runs
       const int next = item + w.stride;
       Item nit{};
@@ -595,9 +597,11 @@ __device__ __forceinline__ void attn_bf16_cta(const CUtensorMap* tm_k_, const CU
           oacc[h] = 0.0f;
           alpha_prev[h] = 1.0f;
         }
-        bool ok = true;
+        bool fail = false;  // this thread saw a wait run out (uniform per warp)
+        // O of an own chunk once its P.V product is complete; false (for the
+        // whole warp) when the wait ran out
         auto take_o = [&](int cc) -> bool {
-          if (!mbar_wait(o_full(grp), (cc >> 1) & 1, abort_flag)) return false;
+          if (!__all_sync(0xffffffffu, mbar_wait(o_full(grp), (cc >> 1) & 1, abort_flag, a.wait_ns))) return false;
           tc_fence_after();
           float ov[2 * NH];
           if constexpr (NH == 8) {
@@ -617,15 +621,20 @@ __device__ __forceinline__ void attn_bf16_cta(const CUtensorMap* tm_k_, const CU
         for (int cc = c0 + ((grp - c0) & 1); cc < c0 + it.nch; cc += 2) {
           const int s = cc % kStages;
           const int bi = t / B, tok = t - bi * B;
-          if (!mbar_wait(full_bar(s), (cc / kStages) & 1, abort_flag)) { ok = false; break; }
-          const int2 md = meta[s * 8 + bi];
+          bool ready = !fail && mbar_wait(full_bar(s), (cc / kStages) & 1, abort_flag, a.wait_ns);
+          const int2 md = ready ? meta[s * 8 + bi] : make_int2(-1, 0);
           const bool valid = md.x >= 0 && tok < md.y;
-          if (!mbar_wait(s_full(grp), (cc >> 1) & 1, abort_flag)) { ok = false; break; }
-          tc_fence_after();
+          ready = __all_sync(0xffffffffu, ready && mbar_wait(s_full(grp), (cc >> 1) & 1, abort_flag, a.wait_ns));
           float sv[16];
-          tmem_ld16(tmem + lane_base + grp * 16, sv);
-          tc_fence_before();
-          mbar_arrive(s_free(grp));
+          if (ready) {
+            tc_fence_after();
+            tmem_ld16(tmem + lane_base + grp * 16, sv);
+            tc_fence_before();
+            mbar_arrive(s_free(grp));
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) sv[i] = 0.0f;
+          }
           float x[NH], r[NH];
 #pragma unroll
           for (int h = 0; h < NH; ++h) {
@@ -636,7 +645,10 @@ __device__ __forceinline__ void attn_bf16_cta(const CUtensorMap* tm_k_, const CU
           float* rb = red + ((cc >> 1) & 1) * 4 * NH;  // alternate buffers: one barrier per chunk
           const float wmax = warp_reduce_scatter<NH, true>(r);
           if ((lane % (32 / NH)) == 0) rb[wq * NH + lane / (32 / NH)] = wmax;
-          named_barrier(bar, 128);
+          if (named_barrier_or(bar, 128, fail || !ready)) {
+            fail = true;
+            break;
+          }
           float alpha[NH], p[NH];
 #pragma unroll
           for (int h = 0; h < NH; ++h) {
@@ -650,51 +662,52 @@ __device__ __forceinline__ void attn_bf16_cta(const CUtensorMap* tm_k_, const CU
           // with one P buffer per group, the P.V product of this group's
           // previous chunk reads it: that product must be complete (and its O
           // taken) before P is rewritten
-          if (Ly::kPBufs == 2 && last_own >= 0 && !take_o(last_own)) { ok = false; break; }
-          // probabilities, split into bf16 high part + bf16 remainder
-          uint32_t hi2[NH / 2], lo2[NH / 2];
+          if (Ly::kPBufs == 2 && last_own >= 0 && !take_o(last_own)) fail = true;
+          if (!fail) {
+            // probabilities, split into bf16 high part + bf16 remainder
+            uint32_t hi2[NH / 2], lo2[NH / 2];
 #pragma unroll
-          for (int h = 0; h < NH; h += 2) {
-            const __nv_bfloat162 hi = __floats2bfloat162_rn(p[h], p[h + 1]);
-            const float2 hf = __bfloat1622float2(hi);
-            const __nv_bfloat162 lo = __floats2bfloat162_rn(p[h] - hf.x, p[h + 1] - hf.y);
-            hi2[h / 2] = *reinterpret_cast<const uint32_t*>(&hi);
-            lo2[h / 2] = *reinterpret_cast<const uint32_t*>(&lo);
-          }
-          {
-            constexpr int kPLbo = 8 * 2 * NH * 2;
-            uint8_t* prow = smem + Ly::kOffP + (cc % Ly::kPBufs) * Ly::kPBytes + (t >> 3) * kPLbo + (t & 7) * 16;
-#pragma unroll
-            for (int gi = 0; gi < NH / 8; ++gi) {
-              *reinterpret_cast<uint4*>(prow + gi * 128) =
-                  make_uint4(hi2[gi * 4], hi2[gi * 4 + 1], hi2[gi * 4 + 2], hi2[gi * 4 + 3]);
-              *reinterpret_cast<uint4*>(prow + (NH / 8 + gi) * 128) =
-                  make_uint4(lo2[gi * 4], lo2[gi * 4 + 1], lo2[gi * 4 + 2], lo2[gi * 4 + 3]);
+            for (int h = 0; h < NH; h += 2) {
+              const __nv_bfloat162 hi = __floats2bfloat162_rn(p[h], p[h + 1]);
+              const float2 hf = __bfloat1622float2(hi);
+              const __nv_bfloat162 lo = __floats2bfloat162_rn(p[h] - hf.x, p[h + 1] - hf.y);
+              hi2[h / 2] = *reinterpret_cast<const uint32_t*>(&hi);
+              lo2[h / 2] = *reinterpret_cast<const uint32_t*>(&lo);
             }
-          }
-          if (!valid) {
-            // rows of no token (past the request's end inside its last page, or of
-            // no loaded block): zero V so they contribute exactly nothing - P is 0
-            // there but the bytes in shared memory need not be finite
-            uint4 z = make_uint4(0, 0, 0, 0);
+            {
+              constexpr int kPLbo = 8 * 2 * NH * 2;
+              uint8_t* prow = smem + Ly::kOffP + (cc % Ly::kPBufs) * Ly::kPBytes + (t >> 3) * kPLbo + (t & 7) * 16;
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              uint4* row = reinterpret_cast<uint4*>(smem + s * kStageBytes + kTileBytes + h * kHalfBytes + t * 128);
-#pragma unroll
-              for (int i = 0; i < 8; ++i) row[i] = z;
+              for (int gi = 0; gi < NH / 8; ++gi) {
+                *reinterpret_cast<uint4*>(prow + gi * 128) =
+                    make_uint4(hi2[gi * 4], hi2[gi * 4 + 1], hi2[gi * 4 + 2], hi2[gi * 4 + 3]);
+                *reinterpret_cast<uint4*>(prow + (NH / 8 + gi) * 128) =
+                    make_uint4(lo2[gi * 4], lo2[gi * 4 + 1], lo2[gi * 4 + 2], lo2[gi * 4 + 3]);
+              }
             }
+            if (!valid) {
+              // rows of no token (past the request's end inside its last page, or of
+              // no loaded block): zero V so they contribute exactly nothing - P is 0
+              // there but the bytes in shared memory need not be finite
+              uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                uint4* row = reinterpret_cast<uint4*>(smem + s * kStageBytes + kTileBytes + h * kHalfBytes + t * 128);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) row[i] = z;
+              }
+            }
+            fence_async_smem();
+            mbar_arrive(p_full(grp));
+            // two P buffers per group: the product two own chunks back is done
+            // before its buffer is written again (next own chunk)
+            if (Ly::kPBufs == 4 && last_own >= 0 && !take_o(last_own)) fail = true;
           }
-          fence_async_smem();
-          mbar_arrive(p_full(grp));
-          // two P buffers per group: the product two own chunks back is done
-          // before its buffer is written again (next own chunk)
-          if (Ly::kPBufs == 4 && last_own >= 0 && !take_o(last_own)) { ok = false; break; }
 #pragma unroll
           for (int h = 0; h < NH; ++h) alpha_prev[h] = alpha[h];
           last_own = cc;
         }
         c = c0 + it.nch;
-        if (!ok) break;
         // the normaliser reduction overlaps the last P.V product
         float* rs = red + 8 * NH;
         {
@@ -704,12 +717,12 @@ __device__ __forceinline__ void attn_bf16_cta(const CUtensorMap* tm_k_, const CU
           const float wsum = warp_reduce_scatter<NH, false>(r);
           if ((lane % (32 / NH)) == 0) rs[wq * NH + lane / (32 / NH)] = wsum;
         }
-        named_barrier(bar, 128);
-        if (last_own >= 0 && !take_o(last_own)) break;
+        if (!fail && last_own >= 0 && !take_o(last_own)) fail = true;
+        fail = named_barrier_or(bar, 128, fail);
         // combine the two groups' states: group 1 publishes, group 0 merges and writes
         float* xm = xo + NH * 128;
         float* xl = xm + NH;
-        if (grp == 1) {
+        if (grp == 1 && !fail) {
 #pragma unroll
           for (int h = 0; h < NH; ++h) xo[h * 128 + t] = oacc[h];
 #pragma unroll
@@ -720,7 +733,8 @@ __device__ __forceinline__ void attn_bf16_cta(const CUtensorMap* tm_k_, const CU
             }
           }
         }
-        named_barrier(3, 256);
+        // both groups agree: after a wait ran out they leave the item loop together
+        if (named_barrier_or(3, 256, fail)) break;
         if (grp == 0) {
 #pragma unroll
           for (int h = 0; h < NH; ++h) {  // unrolled: the heads' chains overlap
@@ -817,7 +831,6 @@ template <int NH>
 struct FuseLayout {
   static constexpr int kOffF = (Layout<NH>::kBytes + 15) / 16 * 16;
   static constexpr int kOffBar = kOffF;       // tile full, q full, accumulator full
-  static constexpr int kOffMisc = kOffF + 32;  // abort flag
   static constexpr int kOffList = kOffF + 48;  // int2[kFuseList]: (page, valid tokens) of this CTA's split
   static constexpr int kOffPush = kOffList + kFuseList * 8;  // [kPushSlots][128] o, then [kPushSlots] lse
   static constexpr int kBytes = kOffPush + (kPushSlots * 129 * 4 + 15) / 16 * 16;
@@ -831,6 +844,15 @@ struct FuseArgs {
   const uint8_t* v_pages;
   int tiles;    // 128-block tiles per (request, kv head)
   int cluster;  // CTAs per (request, kv head)
+  // append (nullable new_k): the newest token of every pair, [batch][Hkv][128]
+  // bf16, is written at position seq_lens - 1 of the cache and widens its
+  // block's summary before the block is scored
+  const __nv_bfloat16* new_k;
+  const __nv_bfloat16* new_v;
+  __nv_bfloat16* k_pages_w;
+  __nv_bfloat16* v_pages_w;
+  __nv_bfloat16* smin_w;
+  __nv_bfloat16* smax_w;
 };
 
 // Sends a split's result for head h to the CTA that merges it: CTA h / hp,
@@ -865,7 +887,9 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   const uint32_t tile_full = sbase + FL::kOffBar, q_full = tile_full + 8, acc_full = tile_full + 16;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + FL::kOffMisc);
+  // one abort flag for all phases (the attention's), so that a wait that ran
+  // out in phase 1 also stops the attention of phase 3
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Layout<NH>::kOffMisc + 4);
   int2* s_list = reinterpret_cast<int2*>(smem + FL::kOffList);
   float* s_scores = reinterpret_cast<float*>(smem + kFScores);
   float* s_prev = reinterpret_cast<float*>(smem + kFPrev);
@@ -926,15 +950,49 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   const int32_t* pt = a.page_table + static_cast<int64_t>(pair) * a.max_blocks;
 
   // ---- phase 1: bound scores of tile `rank` ----
+  bool bound_issued = false;
   if (warp == kMma1B) {
-    if (lane == 0 && has_tile && mbar_wait(q_full, 0, abort_flag) && mbar_wait(tile_full, 0, abort_flag)) {
+    if (lane == 0 && has_tile && mbar_wait(q_full, 0, abort_flag, a.wait_ns) &&
+        mbar_wait(tile_full, 0, abort_flag, a.wait_ns)) {
       tc_fence_after();
       bound::issue_mmas(tmem, sbase + kFTile, sbase + kFQ);
       mma_commit(acc_full);
+      bound_issued = true;
     }
   } else if (warp < 4) {
+    if (has_tile) bound::write_q(smem + kFQ, a.q, static_cast<int64_t>(b) * a.hq + kvh * g, g, tid);
+    if (f.new_k && L > 0 && rank == (nb - 1) / bound::kTile) {
+      // append ("KV 稀疏化" wiki §5: the summary of the newest token's block
+      // covers it): thread t writes channel t of the token's K and V rows into
+      // its page and widens the block's min/max row, in the staged tile the
+      // MMAs read and in global memory (a token in row 0 starts the box)
+      const int jl = nb - 1, tok = (L - 1) - jl * a.block;
+      const int page = pt[jl];
+      const bool page_ok = page >= 0 && page < a.num_pages;
+      if (!page_ok && tid == 0) set_error(err, HS_EBIT_PAGE_RANGE);
+      const int64_t src = static_cast<int64_t>(pair) * kD + tid;
+      const __nv_bfloat16 kx = f.new_k[src], vx = f.new_v[src];
+      if (page_ok) {
+        const int64_t row = (static_cast<int64_t>(page) * a.block + tok) * kD + tid;
+        f.k_pages_w[row] = kx;
+        f.v_pages_w[row] = vx;
+      }
+      if (mbar_wait(tile_full, 0, abort_flag, a.wait_ns)) {
+        const int r = jl - rank * bound::kTile, h = tid >> 6, cc = tid & 63;
+        const uint32_t off = r * 128 + ((((cc >> 3) ^ (r & 7))) << 4) + (cc & 7) * 2;
+        __nv_bfloat16* mx = reinterpret_cast<__nv_bfloat16*>(smem + kFTile + h * bound::kHalf + off);
+        __nv_bfloat16* mn = reinterpret_cast<__nv_bfloat16*>(smem + kFTile + (2 + h) * bound::kHalf + off);
+        const float kf = __bfloat162float(kx);
+        *mn = tok == 0 ? kx : __float2bfloat16_rn(fminf(__bfloat162float(*mn), kf));  // exact: bf16 values
+        *mx = tok == 0 ? kx : __float2bfloat16_rn(fmaxf(__bfloat162float(*mx), kf));
+        const int64_t so = (static_cast<int64_t>(pair) * a.max_blocks + jl) * kD + tid;
+        f.smin_w[so] = *mn;
+        f.smax_w[so] = *mx;
+      }
+      // the rows written here are read by the copies (async proxy) of phase 3
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+    }
     if (has_tile) {
-      bound::write_q(smem + kFQ, a.q, static_cast<int64_t>(b) * a.hq + kvh * g, g, tid);
       fence_async_smem();
       mbar_arrive(q_full);
     }
@@ -968,7 +1026,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   cluster_wait();  // every CTA of the cluster runs: its shared memory is addressable
   if (warp < 4 && has_tile) {
     float best = -INFINITY;
-    if (mbar_wait(acc_full, 0, abort_flag)) {
+    if (__all_sync(0xffffffffu, mbar_wait(acc_full, 0, abort_flag, a.wait_ns))) {  // warp-wide TMEM load
       tc_fence_after();
       float u[16];
       tmem_ld16(tmem + (static_cast<uint32_t>(warp * 32) << 16), u);
@@ -981,11 +1039,13 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     if (j < nb && f.scores) f.scores[static_cast<int64_t>(pair) * a.max_blocks + j] = best;
     for (int r = 0; r < f.cluster; ++r) {  // every CTA of the cluster gets the tile's scores
       if (j < nb) cluster.map_shared_rank(s_scores, r)[j] = best;
-      sel::warp_key_range(best, j < nb, cluster.map_shared_rank(s_range, r), rank * 4 + warp);
+      sel::warp_key_range(best, j < nb && !sel::is_forced(j, L, a.block, sa.sink_tokens, sa.window_tokens),
+                          cluster.map_shared_rank(s_range, r), rank * 4 + warp);
     }
   }
   if (warp == kProdB && lane == 0 && rank < f.tiles)  // the tile has landed before the ring is reused
-    mbar_wait(tile_full, 0, abort_flag, 500000000ull);
+    mbar_drain(tile_full, 0);
+  if (bound_issued) mbar_drain(acc_full, 0);  // the bound product is done before TMEM is reused
   cluster.sync();  // every CTA holds all scores; no shared memory of another CTA is touched after this
 
   // ---- phase 2: every CTA selects; rank 0 stores the selection ----
@@ -1061,24 +1121,28 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 // ============================================================================
 // e4m3 K/V (one fp32 scale per 32 channels per token), head_dim 128, g <= 8.
 //
-// The e4m3 codes are exact in bf16, so the MMAs run on the codes and the scales
-// are applied in fp32 around them:
+// The e4m3 codes are exact in f16 (one conversion instruction per pair of
+// codes), so the MMAs run on f16 codes and the scales are applied in fp32
+// around them (q and the weights W enter as f16; both operands of every MMA
+// are f16):
 //   GEMM1  S'[tok][(grp, h)] = sum_{d in grp} code_k[tok][d] * q[h][d]   (N = 4 groups x 8 heads)
 //          S[tok][h] = sum_grp kscale[tok][grp] * S'[tok][(grp, h)]
 //   GEMM2  O'[d][(grp, hl, h)] = sum_tok code_v[tok][d] * W_hl[tok][(grp, h)],
-//          W = p[tok][h] * vscale[tok][grp] split into bf16 hi + lo (N = 64);
+//          W = p[tok][h] * vscale[tok][grp] split into f16 hi + lo (N = 64);
 //          channel d keeps the columns of its own group grp = d / 32.
-// TMA stages the raw codes and scales; the softmax warps convert each chunk's
-// codes to bf16 operand tiles (zero rows for tokens outside the request) and
-// release the stage.  K tile conversion of chunk c+1 overlaps the softmax of
-// chunk c; the V tile of chunk c is converted once GEMM2 of chunk c-1 is done.
+// TMA stages the raw codes and scales; two converter warpgroups turn each
+// chunk's codes into f16 operand tiles (zero rows for tokens outside the
+// request).  K tile conversion of chunk c+1 overlaps the softmax of chunk c;
+// the V tile of chunk c is converted once GEMM2 of chunk c-1 is done.  The
+// softmax warps publish P' of chunk c before they take the O' of chunk c-1,
+// so that wait is off their chain.
 // ============================================================================
 constexpr int kStages8 = 3;
 constexpr int kCodeBytes = kChunk * 128;          // 128 tokens x 128 codes
 constexpr int kScaleBytes = kChunk * 16;          // 128 tokens x 4 scales
 constexpr int kStage8Bytes = 2 * kCodeBytes + 2 * kScaleBytes;
 struct Layout8 {
-  static constexpr int kOffKbf = kStages8 * kStage8Bytes;  // bf16 K tile (2 halves, swizzled)
+  static constexpr int kOffKbf = kStages8 * kStage8Bytes;  // f16 K tile (2 halves, swizzled)
   static constexpr int kOffVbf = kOffKbf + kTileBytes;
   static constexpr int kQHalf = 32 * 128;                   // 32 rows (group x head) x 64 channels
   static constexpr int kOffQ = kOffVbf + kTileBytes;
@@ -1097,7 +1161,8 @@ struct Layout8 {
   static constexpr int kColO = 64;  // S' uses columns [0, 64)
 };
 
-// one token row of e4m3 codes -> bf16 row of a 128-byte-swizzled K-major tile
+// one token row of e4m3 codes -> f16 row of a 128-byte-swizzled K-major tile
+// (the conversion is exact)
 __device__ __forceinline__ void convert_row(const uint8_t* codes_row, uint8_t* tile, int t, bool valid) {
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
@@ -1108,18 +1173,28 @@ __device__ __forceinline__ void convert_row(const uint8_t* codes_row, uint8_t* t
     uint32_t w[8];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const float2 a = e4m3x2_to_float2(static_cast<uint16_t>(words[j] & 0xffffu));
-      const float2 b = e4m3x2_to_float2(static_cast<uint16_t>(words[j] >> 16));
-      const __nv_bfloat162 ab = __floats2bfloat162_rn(a.x, a.y);
-      const __nv_bfloat162 bb = __floats2bfloat162_rn(b.x, b.y);
-      w[2 * j] = *reinterpret_cast<const uint32_t*>(&ab);
-      w[2 * j + 1] = *reinterpret_cast<const uint32_t*>(&bb);
+      const __half2_raw a = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(words[j] & 0xffffu), __NV_E4M3);
+      const __half2_raw b = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(words[j] >> 16), __NV_E4M3);
+      w[2 * j] = static_cast<uint32_t>(a.x) | (static_cast<uint32_t>(a.y) << 16);
+      w[2 * j + 1] = static_cast<uint32_t>(b.x) | (static_cast<uint32_t>(b.y) << 16);
     }
     uint8_t* row = tile + (ch >> 2) * kHalfBytes + t * 128;
     const int lc = (ch & 3) * 2;
     *reinterpret_cast<uint4*>(row + (((lc) ^ (t & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
     *reinterpret_cast<uint4*>(row + (((lc + 1) ^ (t & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
   }
+}
+
+// bf16 pairs -> f16 pairs (exact for query values within the f16 range)
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
+  uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xffff0000u);
+    const __half2 h = __floats2half2_rn(lo, hi);
+    w[i] = *reinterpret_cast<const uint32_t*>(&h);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -1203,8 +1278,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp || warp == kMma2Warp) {
     if (lane == 0) {
       const bool first = warp == kMmaWarp;
-      constexpr uint32_t idesc1 = idesc_bf16(128, 32, false, false);
-      constexpr uint32_t idesc2 = idesc_bf16(128, 64, true, true);
+      constexpr uint32_t idesc1 = idesc_f16(128, 32, false, false);
+      constexpr uint32_t idesc2 = idesc_f16(128, 64, true, true);
       const uint64_t kdesc = smem_desc(sbase + Ly::kOffKbf, 16, 1024, 2);
       const uint64_t qdesc = smem_desc(sbase + Ly::kOffQ, 16, 1024, 2);
       const uint64_t vdesc = smem_desc(sbase + Ly::kOffVbf, kHalfBytes, 1024, 2);
@@ -1217,14 +1292,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int next = item + w.stride;
         const Item nit = next < a.items ? item_geom(a, next, bpc, w) : Item{};
         if (it.nch > 0 && first) {
-          ok = mbar_wait(q_full, qi & 1, abort_flag);
+          ok = mbar_wait(q_full, qi & 1, abort_flag, a.wait_ns);
           ++qi;
         }
         for (int ci = 0; ok && ci < it.nch; ++ci, ++c) {
           const int bb = c & 1;
           if (first) {
-            ok = mbar_wait(kconv_full, c & 1, abort_flag) &&
-                 (c < 2 || mbar_wait(s_free(bb), ((c >> 1) + 1) & 1, abort_flag));
+            ok = mbar_wait(kconv_full, c & 1, abort_flag, a.wait_ns) &&
+                 (c < 2 || mbar_wait(s_free(bb), ((c >> 1) + 1) & 1, abort_flag, a.wait_ns));
             if (!ok) break;
             tc_fence_after();
 #pragma unroll
@@ -1235,8 +1310,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             mma_commit(s_full(bb));
           } else {
-            ok = mbar_wait(p_full(bb), (c >> 1) & 1, abort_flag) && mbar_wait(vconv_full, c & 1, abort_flag) &&
-                 (c < 2 || mbar_wait(o_free(bb), ((c >> 1) + 1) & 1, abort_flag));
+            ok = mbar_wait(p_full(bb), (c >> 1) & 1, abort_flag, a.wait_ns) && mbar_wait(vconv_full, c & 1, abort_flag, a.wait_ns) &&
+                 (c < 2 || mbar_wait(o_free(bb), ((c >> 1) + 1) & 1, abort_flag, a.wait_ns));
             if (!ok) break;
             tc_fence_after();
 #pragma unroll
@@ -1252,7 +1327,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         item = next;
         it = nit;
       }
-      if (!first && last_g2 >= 0) mbar_wait(o_full(last_g2 & 1), (last_g2 >> 1) & 1, abort_flag, 500000000ull);
+      // every product this thread issued is complete before TMEM is released
+      if (first && c > 0) mbar_drain(s_full((c - 1) & 1), ((c - 1) >> 1) & 1);
+      if (!first && last_g2 >= 0) mbar_drain(o_full(last_g2 & 1), (last_g2 >> 1) & 1);
     }
   } else if (warp >= kConvWarp0 && warp < kConvVWarp0 + 4) {
     // ================= code conversion: e4m3 rows -> bf16 operand tiles =================
@@ -1267,9 +1344,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Item it = item_geom(a, item, bpc, w);
       for (int ci = 0; ci < it.nch; ++ci, ++c) {
         const int s = c % kStages8;
-        const bool prev_done = c == 0 || (is_k ? mbar_wait(s_full((c - 1) & 1), ((c - 1) >> 1) & 1, abort_flag)
-                                               : mbar_wait(o_full((c - 1) & 1), ((c - 1) >> 1) & 1, abort_flag));
-        if (!mbar_wait(full_bar(s), (c / kStages8) & 1, abort_flag) || !prev_done) {
+        const bool prev_done = c == 0 || (is_k ? mbar_wait(s_full((c - 1) & 1), ((c - 1) >> 1) & 1, abort_flag, a.wait_ns)
+                                               : mbar_wait(o_full((c - 1) & 1), ((c - 1) >> 1) & 1, abort_flag, a.wait_ns));
+        if (!mbar_wait(full_bar(s), (c / kStages8) & 1, abort_flag, a.wait_ns) || !prev_done) {
           ok = false;
           break;
         }
@@ -1298,37 +1375,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int grp = row >> 3, h = row & 7;
         v[i] = make_uint4(0, 0, 0, 0);
         if (h < g && half * 2 + (ch >> 2) == grp)
-          v[i] = *reinterpret_cast<const uint4*>(a.q + (static_cast<int64_t>(b) * a.hq + kvh * g + h) * kD +
-                                                 half * 64 + ch * 8);
+          v[i] = bf16x8_to_f16x8(*reinterpret_cast<const uint4*>(a.q + (static_cast<int64_t>(b) * a.hq + kvh * g + h) *
+                                                                        kD + half * 64 + ch * 8));
       }
     };
     int item = w.first;
     Item it{};
-    uint4 qv[4];
-    if (item < a.items) {
-      it = item_geom(a, item, bpc, w);
-      load_q(item, qv);
-    }
-    for (; item < a.items && !*abort_flag;) {
+    if (item < a.items) it = item_geom(a, item, bpc, w);
+    // as in the bf16 kernel, a wait that runs out is made uniform across the
+    // warp (warp-wide TMEM loads) and across the 128 threads at each named
+    // barrier (bar.red.or), so they all leave the loops at the same point
+    while (item < a.items) {
       const int next = item + w.stride;
-      Item nit{};
-      uint4 nqv[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) nqv[i] = make_uint4(0, 0, 0, 0);
-      if (next < a.items) {
-        nit = item_geom(a, next, bpc, w);
-        load_q(next, nqv);
-      }
+      const Item nit = next < a.items ? item_geom(a, next, bpc, w) : Item{};  // in flight meanwhile
       const int64_t row0 = (static_cast<int64_t>(it.b) * a.hq + it.kvh * g) * a.splits + it.split;
       if (it.nch == 0) {
         for (int h = 0; h < g; ++h) put_partial(a, row0, h, t, 0.0f, -INFINITY);
         if (a.splits > 1 && a.counters) merge_if_last(a, it, t, 1, s_last);
         item = next;
         it = nit;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) qv[i] = nqv[i];
         continue;
       }
+      // the item's query rows (not prefetched a whole item ahead: registers
+      // are the softmax warps' limit here)
+      uint4 qv[4];
+      load_q(item, qv);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int idx = t * 4 + i;
@@ -1338,7 +1409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_async_smem();
       mbar_arrive(q_full);
 
-      bool ok = true;
+      bool fail = false;  // this thread saw a wait run out (uniform per warp)
       float m[NH], lsum[NH], oacc[NH], alpha_prev[NH];
 #pragma unroll
       for (int h = 0; h < NH; ++h) {
@@ -1349,7 +1420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       auto take_o = [&](int cc) -> bool {
         const int bb = cc & 1;
-        if (!mbar_wait(o_full(bb), (cc >> 1) & 1, abort_flag)) return false;
+        if (!__all_sync(0xffffffffu, mbar_wait(o_full(bb), (cc >> 1) & 1, abort_flag, a.wait_ns))) return false;
         tc_fence_after();
         float ov[16];
         tmem_ld16(tmem + lane_base + Ly::kColO + bb * 64 + warp * 16, ov);  // channel t's group = warp
@@ -1359,38 +1430,49 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int h = 0; h < NH; ++h) oacc[h] = fmaf(oacc[h], alpha_prev[h], ov[h] + ov[NH + h]);
         return true;
       };
-      for (int ci = 0; ci < it.nch && ok; ++ci, ++c) {
-        const int bb = c & 1, s = c % kStages8;
+      const int c0 = c;
+      for (int ci = 0; ci < it.nch; ++ci) {
+        const int cc = c0 + ci, bb = cc & 1, s = cc % kStages8;
         // row t of the chunk: token t % B of its (t / B)-th block; its K and V
         // scales come from this chunk's stage
-        if (!mbar_wait(full_bar(s), (c / kStages8) & 1, abort_flag)) { ok = false; break; }
-        const int2 md = meta[s * 8 + t / B];
+        bool ready = !fail && mbar_wait(full_bar(s), (cc / kStages8) & 1, abort_flag, a.wait_ns);
+        const int2 md = ready ? meta[s * 8 + t / B] : make_int2(-1, 0);
         const bool valid_cur = md.x >= 0 && (t % B) < md.y;
         float ks_cur[4] = {0.f, 0.f, 0.f, 0.f};
         if (valid_cur) {
           const float4 sc = *reinterpret_cast<const float4*>(ks_stage(s) + t * 16);
           ks_cur[0] = sc.x; ks_cur[1] = sc.y; ks_cur[2] = sc.z; ks_cur[3] = sc.w;
         }
-        if (!mbar_wait(s_full(bb), (c >> 1) & 1, abort_flag)) { ok = false; break; }
-        tc_fence_after();
-        float sv[32];
-        tmem_ld16(tmem + lane_base + bb * 32, *reinterpret_cast<float(*)[16]>(sv));
-        tmem_ld16(tmem + lane_base + bb * 32 + 16, *reinterpret_cast<float(*)[16]>(sv + 16));
-        tc_fence_before();
-        mbar_arrive(s_free(bb));
+        ready = __all_sync(0xffffffffu, ready && mbar_wait(s_full(bb), (cc >> 1) & 1, abort_flag, a.wait_ns));
+        // S = sum over the 4 channel groups of kscale * S', two groups per TMEM load
         float x[NH];
 #pragma unroll
-        for (int h = 0; h < NH; ++h) {
-          const float sc = ks_cur[0] * sv[h] + ks_cur[1] * sv[8 + h] + ks_cur[2] * sv[16 + h] + ks_cur[3] * sv[24 + h];
-          x[h] = (valid_cur && h < g) ? sc * a.scale_log2 : -INFINITY;
+        for (int h = 0; h < NH; ++h) x[h] = 0.0f;
+        if (ready) {
+          tc_fence_after();
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            float sv[16];
+            tmem_ld16(tmem + lane_base + bb * 32 + half * 16, sv);
+#pragma unroll
+            for (int h = 0; h < NH; ++h)
+              x[h] = fmaf(ks_cur[2 * half + 1], sv[8 + h], fmaf(ks_cur[2 * half], sv[h], x[h]));
+          }
+          tc_fence_before();
+          mbar_arrive(s_free(bb));
         }
+#pragma unroll
+        for (int h = 0; h < NH; ++h) x[h] = (valid_cur && h < g) ? x[h] * a.scale_log2 : -INFINITY;
 #pragma unroll
         for (int h = 0; h < NH; ++h) {
           const float mx = warp_max(x[h]);
-          if (lane == 0) red[(c & 1) * 4 * NH + warp * NH + h] = mx;
+          if (lane == 0) red[(cc & 1) * 4 * NH + warp * NH + h] = mx;
         }
-        named_barrier(1, 128);
-        const float* rb = red + (c & 1) * 4 * NH;  // alternate buffers: one barrier per chunk
+        if (named_barrier_or(1, 128, fail || !ready)) {
+          fail = true;
+          break;
+        }
+        const float* rb = red + (cc & 1) * 4 * NH;  // alternate buffers: one barrier per chunk
         float alpha[NH], p[NH];
 #pragma unroll
         for (int h = 0; h < NH; ++h) {
@@ -1401,41 +1483,47 @@ __global__ void __launch_bounds__(kThreads, 1)
           p[h] = x[h] == -INFINITY ? 0.0f : exp2f(x[h] - mn);
           lsum[h] = fmaf(lsum[h], alpha[h], p[h]);
         }
-        if (ci > 0 && !take_o(c - 1)) { ok = false; break; }
-        const float4 vsc = valid_cur ? *reinterpret_cast<const float4*>(vs_stage(s) + t * 16) : make_float4(0, 0, 0, 0);
-        const float vs[4] = {vsc.x, vsc.y, vsc.z, vsc.w};
-        uint8_t* prow = smem + Ly::kOffP + bb * Ly::kPBytes + (t >> 3) * 1024 + (t & 7) * 16;
+        if (!fail) {
+          const float4 vsc =
+              valid_cur ? *reinterpret_cast<const float4*>(vs_stage(s) + t * 16) : make_float4(0, 0, 0, 0);
+          const float vs[4] = {vsc.x, vsc.y, vsc.z, vsc.w};
+          uint8_t* prow = smem + Ly::kOffP + bb * Ly::kPBytes + (t >> 3) * 1024 + (t & 7) * 16;
 #pragma unroll
-        for (int grp = 0; grp < 4; ++grp) {
-          uint32_t hi2[4], lo2[4];
+          for (int grp = 0; grp < 4; ++grp) {
+            uint32_t hi2[4], lo2[4];
 #pragma unroll
-          for (int h = 0; h < NH; h += 2) {
-            const float w0 = p[h] * vs[grp], w1 = p[h + 1] * vs[grp];
-            const __nv_bfloat162 hi = __floats2bfloat162_rn(w0, w1);
-            const float2 hf = __bfloat1622float2(hi);
-            const __nv_bfloat162 lo = __floats2bfloat162_rn(w0 - hf.x, w1 - hf.y);
-            hi2[h / 2] = *reinterpret_cast<const uint32_t*>(&hi);
-            lo2[h / 2] = *reinterpret_cast<const uint32_t*>(&lo);
+            for (int h = 0; h < NH; h += 2) {
+              const float w0 = p[h] * vs[grp], w1 = p[h + 1] * vs[grp];
+              const __half2 hi = __floats2half2_rn(w0, w1);
+              const float2 hf = __half22float2(hi);
+              const __half2 lo = __floats2half2_rn(w0 - hf.x, w1 - hf.y);
+              hi2[h / 2] = *reinterpret_cast<const uint32_t*>(&hi);
+              lo2[h / 2] = *reinterpret_cast<const uint32_t*>(&lo);
+            }
+            *reinterpret_cast<uint4*>(prow + (grp * 2) * 128) = make_uint4(hi2[0], hi2[1], hi2[2], hi2[3]);
+            *reinterpret_cast<uint4*>(prow + (grp * 2 + 1) * 128) = make_uint4(lo2[0], lo2[1], lo2[2], lo2[3]);
           }
-          *reinterpret_cast<uint4*>(prow + (grp * 2) * 128) = make_uint4(hi2[0], hi2[1], hi2[2], hi2[3]);
-          *reinterpret_cast<uint4*>(prow + (grp * 2 + 1) * 128) = make_uint4(lo2[0], lo2[1], lo2[2], lo2[3]);
+          fence_async_smem();
+          mbar_arrive(p_full(bb));
+          mbar_arrive(empty_bar(s));  // this group is done with the stage's meta and scales
+          // O' of the previous chunk, once P' of this one is out (P' of chunk c
+          // goes to buffer c & 1, last read by the product of chunk c - 2,
+          // whose O' this group took one chunk ago)
+          if (ci > 0 && !take_o(cc - 1)) fail = true;
         }
-        fence_async_smem();
-        mbar_arrive(p_full(bb));
-        mbar_arrive(empty_bar(s));  // this group is done with the stage's meta and scales
 #pragma unroll
         for (int h = 0; h < NH; ++h) alpha_prev[h] = alpha[h];
       }
-      if (!ok) break;
+      c = c0 + it.nch;
       // the normaliser reduction overlaps the last P.V product
 #pragma unroll
       for (int h = 0; h < NH; ++h) {
         const float s_ = warp_sum(lsum[h]);
         if (lane == 0) red[8 * NH + warp * NH + h] = s_;
       }
-      named_barrier(1, 128);
+      if (!fail && !take_o(c - 1)) fail = true;
+      if (named_barrier_or(1, 128, fail)) break;  // all 128 threads leave the item loop together
       const float* rs = red + 8 * NH;
-      if (!take_o(c - 1)) break;
       for (int h = 0; h < g && h < NH; ++h) {
         const float lt = rs[h] + rs[NH + h] + rs[2 * NH + h] + rs[3 * NH + h];
         put_partial(a, row0, h, t, lt > 0.0f ? oacc[h] / lt : 0.0f,
@@ -1445,8 +1533,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       named_barrier(1, 128);
       item = next;
       it = nit;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) qv[i] = nqv[i];
     }
   }
 
@@ -1530,6 +1616,7 @@ TcArgs make_args(const KvView& kv, const AttnArgs& aa) {
   a.splits = aa.splits;
   a.items = kv.batch * kv.hkv * aa.splits;
   a.scale_log2 = aa.scale * kLog2e;
+  a.wait_ns = aa.wait_ns > 0 ? aa.wait_ns : kWaitLimitNs;
   return a;
 }
 
@@ -1585,7 +1672,8 @@ bool score_select_attn_supported(const KvView& kv, const AttnArgs& aa, int sms) 
 }
 
 cudaError_t launch_score_select_attn(const KvView& kv, const void* smin, const void* smax, const SelectArgs& sa,
-                                     AttnArgs& aa, unsigned* err, cudaStream_t st) {
+                                     AttnArgs& aa, unsigned* err, cudaStream_t st, const void* new_k,
+                                     const void* new_v) {
   using FL = FuseLayout<8>;
   const int64_t pairs = static_cast<int64_t>(kv.batch) * kv.hkv;
   if (pairs == 0) return cudaSuccess;
@@ -1603,6 +1691,12 @@ cudaError_t launch_score_select_attn(const KvView& kv, const void* smin, const v
   f.v_pages = static_cast<const uint8_t*>(kv.v_pages);
   f.tiles = (kv.max_blocks + bound::kTile - 1) / bound::kTile;
   f.cluster = f.tiles > aa.splits ? f.tiles : aa.splits;
+  f.new_k = static_cast<const __nv_bfloat16*>(new_k);
+  f.new_v = static_cast<const __nv_bfloat16*>(new_v);
+  f.k_pages_w = static_cast<__nv_bfloat16*>(const_cast<void*>(kv.k_pages));
+  f.v_pages_w = static_cast<__nv_bfloat16*>(const_cast<void*>(kv.v_pages));
+  f.smin_w = static_cast<__nv_bfloat16*>(const_cast<void*>(smin));
+  f.smax_w = static_cast<__nv_bfloat16*>(const_cast<void*>(smax));
   auto kern = score_select_attn_kernel<8>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, FL::kAlloc);
   if (e != cudaSuccess) return e;

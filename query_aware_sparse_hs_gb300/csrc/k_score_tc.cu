@@ -44,24 +44,106 @@ constexpr int kOffBar = kOffQ + 2 * kQBytes;
 constexpr int kNumBars = 2 * kStages + 8;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kAlloc = 232448;
-static_assert(kOffMisc + 16 + 1024 <= kAlloc, "shared memory layout too large");
+static_assert(kOffMisc + 32 + 1024 <= kAlloc, "shared memory layout too large");
 constexpr int kTmemCols = 32;
 
 struct ScoreArgs {
   const __nv_bfloat16* q;
   const int32_t* seq_lens;
   float* scores;
-  int hkv, hq, group, block, max_blocks, tiles, items;
+  int batch, hkv, hq, group, block, max_blocks, tiles, items;
 };
 
-// tile `tile` of (request, kv head) `pair` holds blocks [tile*128, tile*128+128): valid if any is < N_b
-__device__ __forceinline__ bool tile_valid(const ScoreArgs& a, int item, int* pair, int* tile, int* nb) {
-  *pair = item / a.tiles;
-  *tile = item - *pair * a.tiles;
-  const int b = *pair / a.hkv;
+// Blocks of request b (every kv head of it has as many).
+__device__ __forceinline__ int request_blocks(const ScoreArgs& a, int b) {
   const int L = max(a.seq_lens[b], 0);
-  *nb = min((L + a.block - 1) / a.block, a.max_blocks);
-  return *tile * kTile < *nb;
+  return min((L + a.block - 1) / a.block, a.max_blocks);
+}
+
+// Position in the sequence of valid tiles (tile t of (request, kv head) pair
+// holds blocks [t*128, t*128+128); it is valid when one of them is < N_b),
+// taken pair by pair and tile by tile.
+struct TileCursor {
+  int pair, tile, nb;  // nb = blocks of the pair
+};
+
+__device__ __forceinline__ int tiles_of(int nb) { return (nb + kTile - 1) / kTile; }
+
+// The next valid tile (pairs without blocks are skipped; past the last pair
+// the cursor stays on a sentinel pair).
+__device__ __forceinline__ void next_tile(const ScoreArgs& a, TileCursor& c) {
+  if (++c.tile < tiles_of(c.nb)) return;
+  c.tile = 0;
+  const int pairs = a.batch * a.hkv;
+  do {
+    ++c.pair;
+    c.nb = c.pair < pairs ? request_blocks(a, c.pair / a.hkv) : kTile;
+  } while (c.nb == 0);
+}
+
+// The CTA's tiles: `count` consecutive valid tiles from `first`.
+struct TileRun {
+  TileCursor first;
+  int count;
+};
+
+// Without FUSE the valid tiles of all pairs are cut into gridDim.x contiguous
+// runs of (nearly) equal length, so that a CTA's tiles mostly share a pair
+// and its query operand.  Run by one warp; the result is in every lane.
+__device__ TileRun contiguous_run(const ScoreArgs& a) {
+  const int lane = threadIdx.x & 31;
+  int64_t total = 0;
+  for (int b0 = 0; b0 < a.batch; b0 += 32) {
+    const int b = b0 + lane;
+    total += warp_sum(static_cast<int64_t>(b < a.batch ? tiles_of(request_blocks(a, b)) : 0));
+  }
+  total *= a.hkv;
+  const int64_t start = total * blockIdx.x / gridDim.x, end = total * (blockIdx.x + 1) / gridDim.x;
+  TileRun r{{0, 0, 0}, static_cast<int>(end - start)};
+  if (r.count == 0) return r;
+  int64_t acc = 0;  // valid tiles of the requests before this round of 32
+  for (int b0 = 0; b0 < a.batch; b0 += 32) {
+    const int b = b0 + lane;
+    const int nb = b < a.batch ? request_blocks(a, b) : 0;
+    const int64_t tb = static_cast<int64_t>(tiles_of(nb)) * a.hkv;
+    int64_t incl = tb;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t n = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += n;
+    }
+    const int64_t lo = acc + incl - tb;
+    const unsigned hit = __ballot_sync(0xffffffffu, tb > 0 && start >= lo && start < lo + tb);
+    if (hit) {
+      const int src = __ffs(hit) - 1;
+      int pair = 0, tile = 0;
+      if (lane == src) {
+        const int t = tiles_of(nb);
+        const int64_t off = start - lo;
+        const int kvh = static_cast<int>(off / t);
+        tile = static_cast<int>(off - static_cast<int64_t>(kvh) * t);
+        pair = b * a.hkv + kvh;
+      }
+      r.first.pair = __shfl_sync(0xffffffffu, pair, src);
+      r.first.tile = __shfl_sync(0xffffffffu, tile, src);
+      r.first.nb = __shfl_sync(0xffffffffu, nb, src);
+      return r;
+    }
+    acc += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  r.count = 0;
+  return r;
+}
+
+// Moves a segment cursor (the first tile of a run of tiles of one pair, with
+// `left` tiles of the CTA's run from there on) to the next segment; false
+// when the run ends first.
+__device__ __forceinline__ bool next_segment(const ScoreArgs& a, TileCursor& c, int& left) {
+  left -= tiles_of(c.nb) - c.tile;
+  if (left <= 0) return false;
+  c.tile = tiles_of(c.nb) - 1;
+  next_tile(a, c);
+  return true;
 }
 
 // FUSE: launched as one cluster per (request, kv head) with one CTA per tile
@@ -114,49 +196,77 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   pdl_wait();  // q, the summaries and seq_lens of this step are complete
 
+  // the CTA's tiles: one per CTA with FUSE, else a contiguous run of valid tiles
+  int* s_run = reinterpret_cast<int*>(smem + kOffMisc + 16);
+  if (warp == 0) {
+    TileRun r;
+    if constexpr (FUSE) {
+      r.first.pair = blockIdx.x / a.tiles;
+      r.first.tile = blockIdx.x - r.first.pair * a.tiles;
+      r.first.nb = request_blocks(a, r.first.pair / a.hkv);
+      r.count = r.first.tile * kTile < r.first.nb ? 1 : 0;
+    } else {
+      r = contiguous_run(a);
+    }
+    if (lane == 0) {
+      s_run[0] = r.first.pair;
+      s_run[1] = r.first.tile;
+      s_run[2] = r.first.nb;
+      s_run[3] = r.count;
+    }
+  }
+  __syncthreads();
+  const TileCursor first{s_run[0], s_run[1], s_run[2]};
+  const int count = s_run[3];
+
+  // A segment is a run of the CTA's tiles of one pair; segment s's [Q+ | Q-]
+  // operand is in buffer s & 1, written by the epilogue warps a segment ahead.
   if (warp == kProducerWarp) {
     if (lane == 0) {
+      TileCursor cur = first;
       int n = 0;
-      for (int item = blockIdx.x; item < a.items && !*abort_flag; item += gridDim.x) {
-        int pair, tile, nb;
-        if (!tile_valid(a, item, &pair, &tile, &nb)) continue;
+      for (; n < count && !*abort_flag; ++n) {
         const int s = n % kStages;
         if (n >= kStages && !mbar_wait(empty_bar(s), ((n / kStages) + 1) & 1, abort_flag)) break;
         mbar_arrive_tx(full_bar(s), 4u * kHalf);
-        const int y = pair * a.max_blocks + tile * kTile;
+        const int y = cur.pair * a.max_blocks + cur.tile * kTile;
         const uint32_t st = sbase + s * kStageBytes;
         tma_load_2d(st, &tm_max, 0, y, full_bar(s));
         tma_load_2d(st + kHalf, &tm_max, 64, y, full_bar(s));
         tma_load_2d(st + 2 * kHalf, &tm_min, 0, y, full_bar(s));
         tma_load_2d(st + 3 * kHalf, &tm_min, 64, y, full_bar(s));
-        ++n;
+        next_tile(a, cur);
       }
       for (int s = 0; s < kStages && s < n; ++s) {  // every copy lands before exit
         const int last = n - 1 - ((n - 1 - s) % kStages);
-        mbar_wait(full_bar(s), (last / kStages) & 1, abort_flag, 500000000ull);
+        mbar_drain(full_bar(s), (last / kStages) & 1);
       }
     }
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
-      int n = 0;
-      for (int item = blockIdx.x; item < a.items && !*abort_flag; item += gridDim.x) {
-        int pair, tile, nb;
-        if (!tile_valid(a, item, &pair, &tile, &nb)) continue;
-        const int s = n % kStages, b = n & 1;
-        if (!mbar_wait(q_full(b), (n >> 1) & 1, abort_flag)) break;
+      TileCursor cur = first;
+      int n = 0, seg = 0;
+      for (; n < count && !*abort_flag; ++n) {
+        const int s = n % kStages, b = n & 1, qb = seg & 1;
+        if ((n == 0 || cur.tile == 0) && !mbar_wait(q_full(qb), (seg >> 1) & 1, abort_flag)) break;
         if (!mbar_wait(full_bar(s), (n / kStages) & 1, abort_flag)) break;
         if (n >= 2 && !mbar_wait(acc_free(b), ((n >> 1) + 1) & 1, abort_flag)) break;
         tc_fence_after();
-        bound::issue_mmas(tmem + b * 16, sbase + s * kStageBytes, sbase + kOffQ + b * kQBytes);
+        bound::issue_mmas(tmem + b * 16, sbase + s * kStageBytes, sbase + kOffQ + qb * kQBytes);
         mma_commit(acc_full(b));
         mma_commit(empty_bar(s));
-        mma_commit(q_free(b));
-        ++n;
+        next_tile(a, cur);
+        if (n + 1 == count || cur.tile == 0) {  // the segment's last tile: its operand buffer is free after it
+          mma_commit(q_free(qb));
+          ++seg;
+        }
       }
-      if (n > 0) mbar_wait(acc_full((n - 1) & 1), ((n - 1) >> 1) & 1, abort_flag, 500000000ull);
+      if (n > 0) mbar_drain(acc_full((n - 1) & 1), ((n - 1) >> 1) & 1);
     }
   } else {
-    // epilogue warps: Q operands and scores
+    // epilogue warps: Q operands and scores; a warp leaves the loop as a
+    // whole (its TMEM loads are warp-wide) once a wait has run out or the CTA
+    // is stopping
     const int t = tid;
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     const int g = a.group;
@@ -165,28 +275,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int bq = pair / a.hkv, kvh = pair - bq * a.hkv;
       bound::write_q(smem + kOffQ + b * kQBytes, a.q, static_cast<int64_t>(bq) * a.hq + kvh * g, g, t);
     };
-    int n = 0;
-    int item = blockIdx.x;
-    int pair = 0, tile = 0, nb = 0;
-    while (item < a.items && !tile_valid(a, item, &pair, &tile, &nb)) item += gridDim.x;
-    if (item < a.items) {
-      write_q(pair, 0);
+    TileCursor cur = first, qc = first;  // qc: first tile of the next segment whose operand is to be written
+    int qleft = count, q_done = 0, seg = 0;
+    bool more_q = count > 0;
+    if (more_q) {
+      write_q(qc.pair, 0);
       fence_async_smem();
       mbar_arrive(q_full(0));
+      q_done = 1;
+      more_q = next_segment(a, qc, qleft);
     }
-    while (item < a.items && !*abort_flag) {
-      // the next tile's operand is written while this tile is in flight
-      int nitem = item + gridDim.x, npair = 0, ntile = 0, nnb = 0;
-      while (nitem < a.items && !tile_valid(a, nitem, &npair, &ntile, &nnb)) nitem += gridDim.x;
-      if (nitem < a.items) {
-        const int b1 = (n + 1) & 1;
-        if (n + 1 >= 2 && !mbar_wait(q_free(b1), (((n + 1) >> 1) + 1) & 1, abort_flag)) break;
-        write_q(npair, b1);
-        fence_async_smem();
-        mbar_arrive(q_full(b1));
+    for (int n = 0; n < count; ++n) {
+      bool ok = !*abort_flag;
+      // the next segment's operand, once the MMAs of the segment before this one are done with its buffer
+      if (more_q && q_done == seg + 1) {
+        const int b1 = q_done & 1;
+        ok = __all_sync(0xffffffffu, ok && (q_done < 2 || mbar_wait(q_free(b1), ((q_done - 2) >> 1) & 1, abort_flag)));
+        if (ok) {
+          write_q(qc.pair, b1);
+          fence_async_smem();
+          mbar_arrive(q_full(b1));
+          ++q_done;
+          more_q = next_segment(a, qc, qleft);
+        }
       }
       const int b = n & 1;
-      if (!mbar_wait(acc_full(b), (n >> 1) & 1, abort_flag)) break;
+      if (!__all_sync(0xffffffffu, ok && mbar_wait(acc_full(b), (n >> 1) & 1, abort_flag))) break;
       tc_fence_after();
       float u[16];
       tmem_ld16(tmem + lane_base + b * 16, u);
@@ -196,13 +310,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int h = 0; h < 16; ++h)
         if (h < g) best = fmaxf(best, u[h]);
-      const int j = tile * kTile + t;
-      if (j < nb) a.scores[static_cast<int64_t>(pair) * a.max_blocks + j] = best;
-      item = nitem;
-      pair = npair;
-      tile = ntile;
-      nb = nnb;
-      ++n;
+      const int j = cur.tile * kTile + t;
+      if (j < cur.nb) a.scores[static_cast<int64_t>(cur.pair) * a.max_blocks + j] = best;
+      next_tile(a, cur);
+      if (cur.tile == 0) ++seg;
     }
   }
 
@@ -228,14 +339,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         nb = a.max_blocks;
       }
       const float* src = a.scores + static_cast<int64_t>(pair) * a.max_blocks;
-      uint32_t lo = 0xffffffffu, hi = 0u;  // per warp: the range of the keys
+      uint32_t lo = 0xffffffffu, hi = 0u;  // per warp: the range of the scored blocks' keys
       for (int j0 = 0; j0 < nb; j0 += kThreads) {
         const int j = j0 + tid;
         if (j < nb) {
           const float v = __ldcg(src + j);
           s_scores[j] = v;
-          lo = min(lo, score_key(v));
-          hi = max(hi, score_key(v));
+          if (!sel::is_forced(j, L, a.block, sa.sink_tokens, sa.window_tokens)) {
+            lo = min(lo, score_key(v));
+            hi = max(hi, score_key(v));
+          }
         }
       }
       lo = __reduce_min_sync(0xffffffffu, lo);
@@ -320,6 +433,7 @@ cudaError_t launch_score_tc(const KvView& kv, const void* q, const void* smin, c
   a.group = kv.group;
   a.block = kv.block;
   a.max_blocks = kv.max_blocks;
+  a.batch = kv.batch;
   a.tiles = (kv.max_blocks + kTile - 1) / kTile;
   a.items = kv.batch * kv.hkv * a.tiles;
   if (!fuse) {

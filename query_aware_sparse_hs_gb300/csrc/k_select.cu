@@ -189,15 +189,17 @@ __global__ __launch_bounds__(THREADS) void select_only_kernel(KvView kv, SelectA
     nb = kv.max_blocks;
   }
   const float* src = scores + pair * kv.max_blocks;
-  // the scores, and per warp the range of their keys
+  // the scores, and per warp the range of the keys of the scored (not forced) blocks
   uint32_t lo = 0xffffffffu, hi = 0u;
   for (int j0 = 0; j0 < nb; j0 += THREADS) {
     const int j = j0 + tid;
     if (j < nb) {
       const float v = src[j];
       s_scores[j] = v;
-      lo = min(lo, score_key(v));
-      hi = max(hi, score_key(v));
+      if (!is_forced(j, L, B, a.sink_tokens, a.window_tokens)) {
+        lo = min(lo, score_key(v));
+        hi = max(hi, score_key(v));
+      }
     }
   }
   lo = __reduce_min_sync(0xffffffffu, lo);

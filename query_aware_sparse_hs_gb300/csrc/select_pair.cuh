@@ -33,9 +33,9 @@ constexpr int kHistWords = 256 + 32;
 __device__ __forceinline__ int hist_index(uint32_t digit) { return static_cast<int>(digit + (digit >> 3)); }
 
 // Digit scan of one radix pass, run by every warp on its own: the digit holding
-// the kk-th largest counted key (digits taken from 255 down) and that key's rank
-// within the digit.  Lane l owns digits 255-8l .. 248-8l.
-__device__ __forceinline__ void find_digit(const uint32_t* hist, int kk, int& digit, int& rank) {
+// the kk-th largest counted key (digits taken from 255 down), that key's rank
+// within the digit and the digit's count.  Lane l owns digits 255-8l .. 248-8l.
+__device__ __forceinline__ void find_digit(const uint32_t* hist, int kk, int& digit, int& rank, int& count) {
   const int lane = threadIdx.x & 31;
   uint32_t hv[8];
   int sum = 0;
@@ -50,19 +50,21 @@ __device__ __forceinline__ void find_digit(const uint32_t* hist, int kk, int& di
     const int n = __shfl_up_sync(0xffffffffu, incl, o);
     if (lane >= o) incl += n;
   }
-  int above = incl - sum, d = -1, r = 0;
+  int above = incl - sum, d = -1, r = 0, n = 0;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int h = static_cast<int>(hv[i]);
     if (above < kk && kk <= above + h) {
       d = 255 - 8 * lane - i;
       r = kk - above;
+      n = h;
     }
     above += h;
   }
   const int src = __ffs(__ballot_sync(0xffffffffu, d >= 0)) - 1;  // exactly one lane
   digit = __shfl_sync(0xffffffffu, d, src & 31);
   rank = __shfl_sync(0xffffffffu, r, src & 31);
+  count = __shfl_sync(0xffffffffu, n, src & 31);
 }
 
 // The same smoothing with the previous step's history already staged in shared
@@ -160,13 +162,13 @@ __device__ __forceinline__ int select_pair(const float* s_scores, int nb, int L,
         if ((key & mask) == prefix) atomicAdd(&hist[hist_index((key >> shift) & 255u)], 1u);
       }
       __syncthreads();
-      int digit, rank;
+      int digit, rank, count;
       if constexpr (kWarps <= 12) {
-        find_digit(hist, kk, digit, rank);  // every warp on its own: no second barrier
+        find_digit(hist, kk, digit, rank, count);  // every warp on its own: no second barrier
       } else {
         // many warps: warp 0 scans and the others read its result
         if (warp == 0) {
-          find_digit(hist, kk, digit, rank);
+          find_digit(hist, kk, digit, rank, count);
           if (lane == 0) {
             s_warp[0] = digit;
             s_warp[1] = rank;
@@ -251,12 +253,32 @@ __device__ __forceinline__ int select_pair(const float* s_scores, int nb, int L,
   return min(total, cap);
 }
 
+// Whether block j of a request of L tokens is forced (sink or window).
+__device__ __forceinline__ bool is_forced(int j, int L, int B, int sink, int win) {
+  const int lo = j * B, hi = min(lo + B, L);
+  return lo < sink || (win > 0 && hi > L - win);
+}
+
 // The same selection with the keys held in registers: thread t owns blocks
 // t*KPT .. t*KPT+KPT-1 (nb <= THREADS * KPT), keys are computed once, forced
 // blocks are [0, sink blocks) and [first window block, nb), and placement is
-// one warp scan of per-thread counts plus one barrier.  With up to 12 warps
-// every warp scans the radix histogram itself; with more, warp 0 scans and
-// broadcasts.  Same arguments, result and tie rule as select_pair.
+// one warp scan of per-thread counts plus one barrier.  Same arguments, result
+// and tie rule as select_pair.
+//
+// The k-th largest candidate key is found by counting passes over the
+// candidates' own key range [lo, hi] rather than fixed bytes: a pass counts
+// the keys of the current range in 256 bins of width 2^sh (the smallest
+// power of two that covers the range in 256 bins) and keeps the bin that holds
+// the wanted key.  The search ends as soon as that bin's keys are all taken
+// (its count equals the rank still wanted: every key from the bin's lower
+// bound up is selected) or the bins are single keys (then ties take the lowest
+// indices).  Bound scores of one request sit in a narrow band, so the bins
+// spread them out (few shared-memory atomics meet on one counter) and one or
+// two passes usually settle the threshold.  With up to 12 warps every warp
+// scans the histogram itself; with more, warp 0 scans and broadcasts.
+//   key_range  (nullable) n_range pairs (min, max) of score_key covering every
+//              candidate (scored, not forced) block; without it the range is
+//              found here (one more barrier).
 template <int THREADS, int KPT>
 __device__ __forceinline__ int select_pair_regs(const float* s_scores, int nb, int L, int B, const SelectArgs& a,
                                                 int64_t pair, uint32_t (*s_hist)[kHistWords], int* s_warp,
@@ -302,54 +324,83 @@ __device__ __forceinline__ int select_pair_regs(const float* s_scores, int nb, i
     }
   }
 
-  uint32_t T = 0;
+  uint32_t T = 0;   // selected: key > T, then the first need_eq keys == T
   int need_eq = 0;
   if (k > 0) {
-    uint32_t lo = 0u, hi = 0xffffffffu;
+    uint32_t lo = 0xffffffffu, hi = 0u;
     if (key_range) {
-      lo = 0xffffffffu;
-      hi = 0u;
       for (int i = 0; i < n_range; ++i) {
         lo = min(lo, key_range[2 * i]);
         hi = max(hi, key_range[2 * i + 1]);
       }
+    } else {
+      // the candidates' range through the third histogram buffer, which the
+      // first pass does not touch (the second clears it after the first's barrier)
+      uint32_t l = 0xffffffffu, h = 0u;
+#pragma unroll
+      for (int i = 0; i < KPT; ++i)
+        if ((cand >> i) & 1u) {
+          l = min(l, key[i]);
+          h = max(h, key[i]);
+        }
+      l = __reduce_min_sync(0xffffffffu, l);
+      h = __reduce_max_sync(0xffffffffu, h);
+      uint32_t* scratch = s_hist[2];
+      if (lane == 0) {
+        scratch[2 * warp] = l;
+        scratch[2 * warp + 1] = h;
+      }
+      __syncthreads();
+#pragma unroll 4
+      for (int i = 0; i < kWarps; ++i) {
+        lo = min(lo, scratch[2 * i]);
+        hi = max(hi, scratch[2 * i + 1]);
+      }
     }
-    const uint32_t diff = lo ^ hi;
-    int shift = diff == 0u ? -8 : ((31 - __clz(diff)) & ~7);
-    uint32_t mask = shift >= 24 ? 0u : (0xffffffffu << (shift + 8));
-    uint32_t prefix = hi & mask;
-    int kk = k;
-    for (int pass = 0; shift >= 0; shift -= 8, ++pass) {
+    uint32_t base = lo, span = hi - lo;  // the current range: [base, base + span]
+    int kk = k;  // rank (1-based, from the top) of the wanted key within the range
+    for (int pass = 0;; ++pass) {
+      const int sh = max(0, 24 - __clz(span));  // bins of 2^sh keys: span >> sh < 256
       uint32_t* hist = s_hist[pass % 3];
       uint32_t* next = s_hist[(pass + 1) % 3];  // last read two passes ago
       for (int i = tid; i < kHistWords; i += THREADS) next[i] = 0u;
 #pragma unroll
       for (int i = 0; i < KPT; ++i)
-        if (((cand >> i) & 1u) && (key[i] & mask) == prefix)
-          atomicAdd(&hist[hist_index((key[i] >> shift) & 255u)], 1u);
+        if (((cand >> i) & 1u) && key[i] - base <= span) atomicAdd(&hist[hist_index((key[i] - base) >> sh)], 1u);
       __syncthreads();
-      int digit, rank;
+      int digit, rank, count;
       if constexpr (kWarps <= 12) {
-        find_digit(hist, kk, digit, rank);
+        find_digit(hist, kk, digit, rank, count);
       } else {
         if (warp == 0) {
-          find_digit(hist, kk, digit, rank);
+          find_digit(hist, kk, digit, rank, count);
           if (lane == 0) {
             s_warp[0] = digit;
             s_warp[1] = rank;
+            s_warp[2] = count;
           }
         }
         __syncthreads();
         digit = s_warp[0];
         rank = s_warp[1];
+        count = s_warp[2];
         __syncthreads();  // s_warp is rewritten by the next pass or the placement
       }
-      prefix |= static_cast<uint32_t>(digit) << shift;
-      mask |= 255u << shift;
+      const uint32_t bin_lo = base + (static_cast<uint32_t>(digit) << sh);
+      if (sh == 0) {  // single keys: ties take the lowest indices
+        T = bin_lo;
+        need_eq = rank;
+        break;
+      }
+      if (count == rank && bin_lo > 0u) {  // the whole bin is taken: every key >= bin_lo
+        T = bin_lo - 1u;
+        need_eq = 0;
+        break;
+      }
+      base = bin_lo;
+      span = (1u << sh) - 1u;
       kk = rank;
     }
-    T = prefix;
-    need_eq = kk;
   }
 
   // placement: forced-or-above-threshold, then the lowest-index equal blocks

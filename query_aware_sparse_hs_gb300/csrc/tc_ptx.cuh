@@ -31,17 +31,22 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 __device__ __forceinline__ void mbar_arrive_tx(uint32_t bar, uint32_t tx) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(tx) : "memory");
 }
-// The waiting thread is suspended until the phase completes or about 1 ms
-// has passed (the time-limit hint), so waiting warps take no issue slots
-// from the working ones.
-__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+// Default bound of every wait (2 s), and of the waits that let a stopping
+// CTA's own copies and MMAs finish before it exits (0.5 s).
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr uint64_t kDrainLimitNs = 500000000ull;
+
+// The waiting thread is suspended until the phase completes or about
+// `hint_ns` have passed (the time-limit hint, 1 ms unless a wait has a
+// shorter bound), so waiting warps take no issue slots from the working ones.
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity, uint32_t hint_ns = 1000000u) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity), "r"(1000000u)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
       : "memory");
   return ok != 0;
 }
@@ -60,19 +65,37 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
 }
 
 // Waits for the phase with the given parity to complete.  Gives up after
-// `limit_ns` of wall time or as soon as *abort is set; on a time-out it sets
-// *abort so every other role of the CTA stops too.  Returns false when it gave up.
+// `limit_ns` of wall time or as soon as *abort is set (at once when the phase
+// is not complete and *abort is set already); on a time-out it sets *abort so
+// every other role of the CTA stops too.  Returns false when it gave up.  A
+// phase that is complete already costs one non-blocking test.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
-                                          uint64_t limit_ns = 2000000000ull) {
-  if (mbar_try(bar, parity)) return true;
+                                          uint64_t limit_ns = kWaitLimitNs) {
+  if (mbar_test(bar, parity)) return true;
+  if (*abort) return false;
+  const uint32_t hint = limit_ns < 1000000ull ? static_cast<uint32_t>(limit_ns) : 1000000u;
+  if (mbar_try(bar, parity, hint)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
-    if (mbar_try(bar, parity)) return true;
     if (*abort) return false;
     if (globaltimer_ns() - t0 > limit_ns) {
       *abort = 1;
       return false;
     }
+    if (mbar_try(bar, parity, hint)) return true;
+  }
+}
+
+// Waits for the completion of copies or MMAs this CTA has already issued, so
+// that it never exits (or frees its TMEM) with them in flight.  Unlike
+// mbar_wait it ignores the abort flag: work in flight lands whether or not the
+// CTA is stopping.  Bounded by `limit_ns`; returns false if that passed.
+__device__ __forceinline__ bool mbar_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns = kDrainLimitNs) {
+  if (mbar_try(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    if (mbar_try(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
 
@@ -159,14 +182,36 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
   return d;
 }
 
-// Instruction descriptor of kind::f16 with bf16 A/B and f32 accumulation.
+// Instruction descriptor of kind::f16 with f32 accumulation and A and B both
+// bf16 (format code 1) or both f16 (format code 0).
+__host__ __device__ constexpr uint32_t idesc_kind_f16(int M, int N, bool a_mn_major, bool b_mn_major, bool bf16) {
+  return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | ((a_mn_major ? 1u : 0u) << 15) |
+         ((b_mn_major ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major, bool b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
-         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+  return idesc_kind_f16(M, N, a_mn_major, b_mn_major, true);
+}
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn_major, bool b_mn_major) {
+  return idesc_kind_f16(M, N, a_mn_major, b_mn_major, false);
 }
 
 __device__ __forceinline__ void named_barrier(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// The same barrier, also returning to every participant whether `pred` was
+// true for any of them (bar.red.or): the participants take one decision.
+__device__ __forceinline__ bool named_barrier_or(int id, int threads, bool pred) {
+  uint32_t any;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(any)
+      : "r"(pred ? 1u : 0u), "r"(id), "r"(threads)
+      : "memory");
+  return any != 0;
 }
 
 }  // namespace tc

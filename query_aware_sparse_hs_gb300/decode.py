@@ -97,6 +97,15 @@ class SparseDecode:
         hs.hs_sparse_paged_decode_attn(self.shape, kv, q, src.sel, src.sel_count, self.capacity,
                                        self.attn_params, self.out, self.lse, self.workspace, stream)
 
+    def decode_step(self, kv: hs.PagedKV, q: torch.Tensor, new_k: torch.Tensor, new_v: torch.Tensor,
+                    keep_scores: bool = True, stream=None):
+        """append() then select_attend() as one library call: the newest
+        token is appended inside the single step launch where the shapes allow
+        it."""
+        hs.hs_decode_step(self.shape, kv, q, new_k, new_v, self.smin, self.smax, self.sel_params, self.sel,
+                          self.sel_count, self.scores if keep_scores else None, self.attn_params, self.out, self.lse,
+                          self.workspace, stream)
+
     def select_attend(self, kv: hs.PagedKV, q: torch.Tensor, keep_scores: bool = True, stream=None):
         """select() then attend() as one library call (a single launch where
         the shapes allow it)."""
@@ -165,6 +174,12 @@ class SparseDecode:
         overlapped once enable_swap_overlap() was called).  ``reuse``: skip
         the scoring and selection and attend over the selection of ``reuse``
         (another decoder, or ``self`` to keep this decoder's previous one)."""
+        if new_kv is not None and hot is None and reuse is None and refresh_from_block is None and self.fuse_step:
+            # append, selection and attention in one library call (one launch where it fuses)
+            hs.hs_decode_step(self.shape, kv, q, new_kv[0], new_kv[1], self.smin, self.smax, self.sel_params,
+                              self.sel, self.sel_count, self.scores, self.attn_params, self.out, self.lse,
+                              self.workspace, stream)
+            return self.out, self.lse
         if new_kv is not None:
             self.append(kv, new_kv[0], new_kv[1], stream)
         if refresh_from_block is not None:

@@ -50,7 +50,8 @@ class SelectParams(ctypes.Structure):
 
 class AttnParams(ctypes.Structure):
     _fields_ = [("scale", c_float), ("out_is_fp32", c_int32), ("blocks_per_split", c_int32),
-                ("algo", c_int32), ("max_ctas", c_int32), ("split_counters", c_void_p)]
+                ("algo", c_int32), ("max_ctas", c_int32), ("split_counters", c_void_p),
+                ("wait_limit_ns", c_uint32)]
 
 
 class HotBuffer(ctypes.Structure):
@@ -88,6 +89,9 @@ SYMBOLS = {
     "hs_score_select_attend": (c_int32, [POINTER(AttnShape), POINTER(PagedKV), c_void_p, c_void_p, c_void_p,
                                          POINTER(SelectParams), c_void_p, c_void_p, c_void_p, POINTER(AttnParams),
                                          c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
+    "hs_decode_step": (c_int32, [POINTER(AttnShape), POINTER(PagedKV), c_void_p, c_void_p, c_void_p, c_void_p,
+                                 c_void_p, POINTER(SelectParams), c_void_p, c_void_p, c_void_p, POINTER(AttnParams),
+                                 c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
     "hs_sparse_paged_decode_attn_noalloc": (c_int32, [POINTER(AttnShape), POINTER(PagedKV), c_void_p,
                                                       c_void_p, c_void_p, c_int32, POINTER(AttnParams),
                                                       c_void_p, c_void_p, c_void_p]),
@@ -178,9 +182,11 @@ def select_params(sink_tokens, window_tokens, k_scored, capacity, history_weight
 
 
 def attn_params(scale, out_is_fp32=False, blocks_per_split=0, algo="auto", max_ctas=0,
-                split_counters=None) -> AttnParams:
+                split_counters=None, wait_limit_ns=0) -> AttnParams:
+    """wait_limit_ns: bound of the tensor-core kernels' waits (0 = 2 s)."""
     p = AttnParams(float(scale), 1 if out_is_fp32 else 0, int(blocks_per_split),
-                   ALGO[algo] if isinstance(algo, str) else int(algo), int(max_ctas), _ptr(split_counters))
+                   ALGO[algo] if isinstance(algo, str) else int(algo), int(max_ctas), _ptr(split_counters),
+                   int(wait_limit_ns))
     p._keep = split_counters
     return p
 
@@ -235,6 +241,18 @@ def hs_score_select_attend_fused(shape: AttnShape, batch: int, max_blocks: int, 
     """1: the combined call is one launch for this geometry on the current device; 0: separate launches."""
     return int(_lib.hs_score_select_attend_fused(ctypes.byref(shape), batch, max_blocks, capacity,
                                                  ctypes.byref(params)))
+
+
+def hs_decode_step(shape, kv, q, new_k, new_v, smin, smax, sel_params, sel, sel_count, scores, attn_params, out,
+                   lse=None, workspace=None, stream=None):
+    """Append of the newest token, selection and attention of one decode step
+    in one call (one launch where the library can fuse them)."""
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(_lib.hs_decode_step(ctypes.byref(shape), ctypes.byref(kv), _ptr(q), _ptr(new_k), _ptr(new_v), _ptr(smin),
+                               _ptr(smax), ctypes.byref(sel_params), _ptr(sel), _ptr(sel_count), _ptr(scores),
+                               ctypes.byref(attn_params), _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes,
+                               _stream(stream)),
+           "hs_decode_step")
 
 
 def hs_score_select_attend(shape, kv, q, smin, smax, sel_params, sel, sel_count, scores, attn_params, out,

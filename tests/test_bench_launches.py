@@ -29,7 +29,7 @@ def test_step_launches_follow_the_dispatch(monkeypatch):
     assert bench.attn_splits(w, dec) == 4
     monkeypatch.setattr(hs, "hs_score_select_attend_fused", lambda *a: 1)
     assert bench.fused_step(w, dec)
-    assert bench.step_launches(w, dec) == 2  # append + the step kernel
+    assert bench.step_launches(w, dec) == 1  # append, scoring, selection and attention in one launch
     # the same step without the single launch: append, scoring + selection in
     # one cluster launch, attention merging its splits itself
     assert bench.select_launches(w) == 1
@@ -40,6 +40,10 @@ def test_step_launches_follow_the_dispatch(monkeypatch):
     # without split counters the separate attention needs the merge launch
     dec.split_counters = None
     assert bench.step_launches(w, dec) == 4
+    # the single launch merges its splits inside its clusters, with or without counters
+    monkeypatch.setattr(hs, "hs_score_select_attend_fused", lambda *a: 1)
+    assert bench.step_launches(w, dec) == 1
+    monkeypatch.setattr(hs, "hs_score_select_attend_fused", lambda *a: 0)
     # a decoder that does not use the combined call never counts it
     dec.fuse_step = False
     monkeypatch.setattr(hs, "hs_score_select_attend_fused", lambda *a: 1)

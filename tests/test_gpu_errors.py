@@ -92,3 +92,55 @@ def test_select_workspace_when_no_score_buffer():
                             None, ws)
     assert torch.equal(dec.sel, ref)
     assert hs.hs_get_device_error() == (hs.HS_OK, 0)
+
+
+def _oracle_close(c, dec, tol=2e-3):
+    """Every (request, kv head) of the decoder's fp32 output against the oracle."""
+    from _parity import np32
+    out = np32(dec.out)
+    for b in range(c.w.batch):
+        for kvh in range(c.w.num_kv_heads):
+            r = c.oracle_pair(b, kvh)
+            g = c.w.group
+            assert dec.sel[b, kvh, :int(dec.sel_count[b, kvh])].tolist() == r["sel"]
+            assert np.abs(out[b, kvh * g:(kvh + 1) * g] - r["out"]).max() <= tol
+
+
+@pytest.mark.parametrize("single_launch", [False, True])
+def test_wait_that_runs_out_reports_timeout_then_the_next_call_is_exact(single_launch):
+    """The bounded waits of the tensor-core kernels: with a wait limit of 1 ns
+    (far below the time any copy or product takes) a wait runs out, the CTA
+    stops every role, lets the copies and products it issued land, frees its
+    tensor memory and returns; the host reads HS_ERR_TIMEOUT and the context
+    stays usable.  After the split counters are zeroed again (as the header
+    asks after a time-out) the next call with the default limit matches the
+    oracle."""
+    from query_aware_sparse_hs_gb300 import hs
+    c = _case()
+    dec = c.decoder(out_is_fp32=True)
+    dec.build_summaries(c.kv)
+    fused = hs.hs_score_select_attend_fused(dec.shape, c.w.batch, dec.max_blocks, dec.capacity, dec.attn_params)
+    assert fused == 1  # this geometry takes the single launch when asked to
+    short = hs.attn_params(dec.attn_params.scale, True, algo="tcgen05", split_counters=dec.split_counters,
+                           wait_limit_ns=1)
+    for _ in range(2):
+        if single_launch:
+            hs.hs_score_select_attend(dec.shape, c.kv, c.q, dec.smin, dec.smax, dec.sel_params, dec.sel,
+                                      dec.sel_count, None, short, dec.out, dec.lse, dec.workspace)
+        else:
+            dec.select(c.kv, c.q)
+            assert hs.hs_get_device_error() == (hs.HS_OK, 0)
+            hs.hs_sparse_paged_decode_attn(dec.shape, c.kv, c.q, dec.sel, dec.sel_count, dec.capacity, short,
+                                           dec.out, dec.lse, dec.workspace)
+        st, bits = hs.hs_get_device_error()
+        assert st == hs.HS_ERR_TIMEOUT and bits & hs.HS_EBIT_TIMEOUT, (st, bits)
+        dec.split_counters.zero_()
+    dec.out.fill_(float("nan"))
+    if single_launch:
+        dec.select_attend(c.kv, c.q)
+    else:
+        dec.select(c.kv, c.q)
+        dec.attend(c.kv, c.q)
+    assert hs.hs_get_device_error() == (hs.HS_OK, 0)
+    _oracle_close(c, dec)
+    assert int(dec.split_counters.abs().sum()) == 0
