@@ -517,8 +517,8 @@ def measure_resident(args, w, dev, world) -> dict:
         news.append(new_kv)
         keep.append((k, v, ks, vs))
     torch.cuda.synchronize()
-    st_, bits = hs.hs_get_device_error()
-    assert st_ == hs.HS_OK, (st_, bits)
+    st_, bits, where = hs.hs_get_device_error_detail()
+    assert st_ == hs.HS_OK, (st_, bits, where)
 
     stream = torch.cuda.Stream(device=dev)
     torch.cuda.current_stream().wait_stream(stream)
@@ -699,8 +699,8 @@ def measure_resident(args, w, dev, world) -> dict:
     h2d = inputs[0].numel() * inputs[0].element_size()
     d2h = d0.results.numel()
 
-    st_, bits = hs.hs_get_device_error()
-    assert st_ == hs.HS_OK, (st_, bits)
+    st_, bits, where = hs.hs_get_device_error_detail()
+    assert st_ == hs.HS_OK, (st_, bits, where)
     # a layer that reuses a selection runs append + attention (+ merge)
     reuse_launches = step_launches(w, d0, allow_fused=False) - select_launches(w)
     launches_per_step = step_launches(w, d0) / args.select_every + reuse_launches * (1 - 1 / args.select_every)
@@ -931,8 +931,8 @@ def measure_offload(args, w, dev, world) -> dict:
     e2e_value, ms_e2e = whole_job_rate(args.steps * w.batch * w.num_q_heads, ms_e2e, world, dev)
     t_last = 1 + (args.warmup + args.steps - 1) % timed_per_pass
     assert torch.equal(res_host[t_last], dec.results.cpu()), "results drained to the host differ"
-    st_, bits = hs.hs_get_device_error()
-    assert st_ == hs.HS_OK, (st_, bits)
+    st_, bits, where = hs.hs_get_device_error_detail()
+    assert st_ == hs.HS_OK, (st_, bits, where)
 
     # host -> device link bandwidth: 1 GiB from pinned memory, best of 5
     src = torch.empty(1 << 30, dtype=torch.uint8, pin_memory=True)

@@ -462,6 +462,18 @@ HS_API hs_status hs_sparse_paged_decode_attn_noalloc(const hs_attn_shape* shape,
  * synchronisation (an earlier kernel fault) returns HS_ERR_CUDA. */
 HS_API hs_status hs_get_device_error(hs_stream_t stream, uint32_t* bits_opt);
 
+/* hs_get_device_error, also returning in timeout_opt (nullable, 11 words) the
+ * first bounded wait that ran out since the last read: [0] the kernel (1 the
+ * tensor-core attention, 2 the single-launch step, 3 the e4m3 attention, 4 the
+ * tensor-core bound scoring; 0 = none), [1] its CTA index, [2] the wait:
+ * shared-memory address of the barrier (bits 0-17), the awaited parity (bit
+ * 18), the warp (bits 19-23), bit 31 set; [3..10] the progress of that CTA's
+ * roles in the attention kernels (chunks issued by the copy producer, by the
+ * S and by the O MMA thread, chunks done by softmax group 0 and 1, the
+ * producer's work item, the softmax warps' work item and its chunk count).
+ * For diagnosis only. */
+HS_API hs_status hs_get_device_error_detail(hs_stream_t stream, uint32_t* bits_opt, uint32_t* timeout_opt);
+
 #ifdef __cplusplus
 }
 #endif

@@ -8,7 +8,9 @@
 namespace hs {
 namespace {
 
-__device__ unsigned int g_error_word;  // HS_EBIT_* bits, cleared by hs_get_device_error
+// [0] HS_EBIT_* bits; [1..11] the first wait that ran out (kernel, CTA,
+// wait, the CTA's progress); cleared by hs_get_device_error
+__device__ unsigned int g_error_word[kErrorWords];
 
 constexpr int kMaxDevices = 64;
 unsigned* g_err_ptr[kMaxDevices];
@@ -597,16 +599,23 @@ hs_status hs_quantize_e4m3_g32(const void* src, int32_t src_is_fp32, int64_t row
 }
 
 hs_status hs_get_device_error(hs_stream_t stream, uint32_t* bits_opt) {
+  return hs_get_device_error_detail(stream, bits_opt, nullptr);
+}
+
+hs_status hs_get_device_error_detail(hs_stream_t stream, uint32_t* bits_opt, uint32_t* timeout_opt) {
   Device d;
   hs_status st = current_device(&d);
   if (st != HS_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(s) != cudaSuccess) return HS_ERR_CUDA;
-  unsigned bits = 0;
-  if (cudaMemcpyAsync(&bits, d.err, sizeof(bits), cudaMemcpyDeviceToHost, s) != cudaSuccess) return HS_ERR_CUDA;
-  if (cudaMemsetAsync(d.err, 0, sizeof(unsigned), s) != cudaSuccess) return HS_ERR_CUDA;
+  unsigned word[kErrorWords] = {};
+  if (cudaMemcpyAsync(word, d.err, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess) return HS_ERR_CUDA;
+  if (cudaMemsetAsync(d.err, 0, sizeof(word), s) != cudaSuccess) return HS_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return HS_ERR_CUDA;
+  const unsigned bits = word[0];
   if (bits_opt) *bits_opt = bits;
+  if (timeout_opt)
+    for (int i = 1; i < kErrorWords; ++i) timeout_opt[i - 1] = word[i];
   if (bits & (HS_EBIT_PAGE_RANGE | HS_EBIT_BLOCK_RANGE)) return HS_ERR_OUT_OF_RANGE;
   if (bits & HS_EBIT_CAPACITY) return HS_ERR_CAPACITY;
   if (bits & HS_EBIT_TIMEOUT) return HS_ERR_TIMEOUT;

@@ -37,6 +37,30 @@ __device__ __forceinline__ void set_error(unsigned* err, unsigned bit) {
   if (err) atomicOr(err, bit);
 }
 
+// Kernels that can report a wait that ran out, for the record below.
+enum TimeoutKernel : unsigned {
+  kTimeoutAttnBf16 = 1,
+  kTimeoutStepFused = 2,
+  kTimeoutAttnE4m3 = 3,
+  kTimeoutScore = 4,
+};
+
+// HS_EBIT_TIMEOUT plus, for the first CTA that reports one, a record of
+// where: err[1] = kernel, err[2] = CTA index, err[3] = the wait (the word a
+// bounded wait leaves next to the abort flag: barrier address, parity, warp),
+// err[4..11] = the CTA's progress words (nullable: zeros).
+constexpr int kErrorWords = 12;
+__device__ __forceinline__ void report_timeout(unsigned* err, unsigned kernel, unsigned wait_info,
+                                               const volatile int* progress = nullptr) {
+  if (!err) return;
+  atomicOr(err, HS_EBIT_TIMEOUT);
+  if (atomicCAS(err + 1, 0u, kernel) == 0u) {
+    err[2] = blockIdx.x;
+    err[3] = wait_info;
+    for (int i = 0; i < 8; ++i) err[4 + i] = progress ? static_cast<unsigned>(progress[i]) : 0u;
+  }
+}
+
 __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
   return __uint_as_float(static_cast<uint32_t>(b) << 16);
 }

@@ -89,11 +89,12 @@ struct Layout {
   static constexpr int kOffP = kOffQ + 2 * kQHalfBytes;
   static constexpr int kOffX = kOffP + kPBufs * kPBytes;      // group exchange: o[NH][128], m[NH], l[NH]
   static constexpr int kOffBar = kOffX + ((NH * 128 + 2 * NH) * 4 + 15) / 16 * 16;
-  static constexpr int kNumBars = 2 * kStages + 11;
+  static constexpr int kNumBars = 2 * kStages + 13;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kOffRed = kOffMisc + 16;
   static constexpr int kOffMeta = kOffRed + 2 * 3 * 4 * NH * 4;  // red: [group][3][4 warps][NH]; meta: [stage][8] (page, valid tokens)
-  static constexpr int kBytes = kOffMeta + kStages * 8 * 8;
+  static constexpr int kOffProg = kOffMeta + kStages * 8 * 8;     // progress words of the roles (for a time-out record)
+  static constexpr int kBytes = kOffProg + 32;
   // the layout plus 1 KB to align its base; what is left of the SM's shared
   // memory can hold a small CTA of another kernel (the overlapped page copy)
   static constexpr int kAlloc = (kBytes + 1024 + 127) / 128 * 128;
@@ -283,10 +284,11 @@ __device__ __forceinline__ int2 resolve_group(const TcArgs& a, const Item& it, i
 // so page-table lookups stay off the copy stream.  Each chunk's pages and
 // valid-token counts are published in meta[stage][8] for the softmax warps and
 // every lane issues the copies of its own block.
+// prog[0] / prog[5]: chunks issued so far / the item being issued.
 template <int STAGES, typename IssueFn>
 __device__ __forceinline__ void run_producer(const TcArgs& a, const Work& w, int bpc, uint32_t full0, uint32_t empty0,
                                              int2* meta, uint32_t bytes_per_block, volatile int* abort_flag,
-                                             unsigned* err, IssueFn issue) {
+                                             unsigned* err, volatile int* prog, IssueFn issue) {
   const int lane = threadIdx.x & 31;
   unsigned bad = 0;
   Item it;
@@ -326,6 +328,10 @@ __device__ __forceinline__ void run_producer(const TcArgs& a, const Work& w, int
         if (lane == 0) mbar_arrive_tx(full0 + 8 * s, tx);
         __syncwarp();
         if (mine && cur.x >= 0) issue(s, bi, cur.x);
+        if (lane == 0) {
+          prog[0] = c + 1;
+          prog[5] = item;
+        }
       }
       cur = nxt;
     }
@@ -379,6 +385,13 @@ __device__ __forceinline__ float warp_reduce_scatter(float (&v)[NH]) {
   return v[0];
 }
 
+// Barrier of P buffer b (the bf16 kernel has up to four P buffers; the first
+// two barriers keep their original slots).  One barrier per buffer: a buffer
+// is written again only after the product that read it has completed, so its
+// barrier is never two phases ahead of the MMA thread that waits on it (a
+// parity wait cannot tell phase n from phase n + 2).
+__host__ __device__ constexpr int p_full_index(int b) { return b < 2 ? 2 * kStages + 4 + b : 2 * kStages + 9 + b; }
+
 // Barrier initialisation (thread 0) and TMEM allocation (warp kMma1B) of a
 // bf16 attention CTA; the caller synchronises the CTA before any role starts.
 template <int NH>
@@ -394,12 +407,14 @@ __device__ __forceinline__ void attn_bf16_setup(uint8_t* smem) {
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar0 + 8 * (2 * kStages + b), 1);      // s_full
       mbar_init(bar0 + 8 * (2 * kStages + 2 + b), 128);  // s_free
-      mbar_init(bar0 + 8 * (2 * kStages + 4 + b), 128);  // p_full
       mbar_init(bar0 + 8 * (2 * kStages + 6 + b), 1);    // o_full
       mbar_init(bar0 + 8 * (2 * kStages + 8 + b), 128);  // o_free
     }
+    for (int b = 0; b < 4; ++b) mbar_init(bar0 + 8 * p_full_index(b), 128);  // p_full, one per P buffer
     mbar_init(bar0 + 8 * (2 * kStages + 10), 128);  // q_full
-    *reinterpret_cast<volatile int*>(smem + Ly::kOffMisc + 4) = 0;  // abort flag
+    *reinterpret_cast<volatile int*>(smem + Ly::kOffMisc + 4) = 0;   // abort flag
+    *reinterpret_cast<volatile int*>(smem + Ly::kOffMisc + 12) = 0;  // which wait ran out
+    for (int i = 0; i < 8; ++i) reinterpret_cast<volatile int*>(smem + Ly::kOffProg)[i] = 0;
     fence_barrier_init();
   }
   if (warp == kMma1B) {
@@ -431,13 +446,18 @@ __device__ __forceinline__ void attn_bf16_cta(const CUtensorMap* tm_k_, const CU
   auto empty_bar = [&](int s) { return bar0 + 8 * (kStages + s); };
   auto s_full = [&](int b) { return bar0 + 8 * (2 * kStages + b); };
   auto s_free = [&](int b) { return bar0 + 8 * (2 * kStages + 2 + b); };
-  auto p_full = [&](int b) { return bar0 + 8 * (2 * kStages + 4 + b); };
+  auto p_full = [&](int b) { return bar0 + 8 * p_full_index(b); };  // b = P buffer
   auto o_full = [&](int b) { return bar0 + 8 * (2 * kStages + 6 + b); };
   auto o_free = [&](int b) { return bar0 + 8 * (2 * kStages + 8 + b); };
   const uint32_t q_full = bar0 + 8 * (2 * kStages + 10);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Ly::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Ly::kOffMisc + 4);
   volatile int* s_last = reinterpret_cast<volatile int*>(smem + Ly::kOffMisc + 8);  // last split of an item
+  // progress of the roles, copied into the record of a wait that runs out:
+  // [0] chunks issued by the producer, [1] / [2] chunks issued by the S / O
+  // MMA thread, [3] / [4] chunks done by softmax group 0 / 1, [5] the
+  // producer's item, [6] the softmax groups' item, [7] its chunk count
+  volatile int* prog = reinterpret_cast<volatile int*>(smem + Ly::kOffProg);
   auto k_half = [&](int s, int h) { return sbase + s * kStageBytes + h * kHalfBytes; };
   auto v_half = [&](int s, int h) { return sbase + s * kStageBytes + kTileBytes + h * kHalfBytes; };
   auto q_half = [&](int h) { return sbase + Ly::kOffQ + h * kQHalfBytes; };
@@ -465,7 +485,7 @@ __device__ __forceinline__ void attn_bf16_cta(const CUtensorMap* tm_k_, const CU
   int2* meta = reinterpret_cast<int2*>(smem + Ly::kOffMeta);
   if (warp == kProdB) {
     // ================= TMA producer =================
-    run_producer<kStages>(a, w, bpc, full_bar(0), empty_bar(0), meta, 4u * B * 128u, abort_flag, err,
+    run_producer<kStages>(a, w, bpc, full_bar(0), empty_bar(0), meta, 4u * B * 128u, abort_flag, err, prog,
                           [&](int s, int bi, int page) {
                             const uint32_t row_off = bi * B * 128;
                             const int y = page * B;
@@ -512,8 +532,9 @@ __device__ __forceinline__ void attn_bf16_cta(const CUtensorMap* tm_k_, const CU
               mma_f16(tmem + bb * 16, kdesc + (koff >> 4), qdesc + (qoff >> 4), idesc1, k > 0 ? 1u : 0u);
             }
             mma_commit(s_full(bb));
+            prog[1] = c + 1;
           } else {
-            ok = mbar_wait(p_full(bb), (c >> 1) & 1, abort_flag, a.wait_ns) &&
+            ok = mbar_wait(p_full(c % Ly::kPBufs), (c / Ly::kPBufs) & 1, abort_flag, a.wait_ns) &&
                  (c < 2 || mbar_wait(o_free(bb), ((c >> 1) + 1) & 1, abort_flag, a.wait_ns));
             if (!ok) break;
             tc_fence_after();
@@ -526,6 +547,7 @@ __device__ __forceinline__ void attn_bf16_cta(const CUtensorMap* tm_k_, const CU
             }
             mma_commit(o_full(bb));
             mma_commit(empty_bar(st));
+            prog[2] = c + 1;
           }
         }
         item = next;
@@ -579,6 +601,10 @@ __device__ __forceinline__ void attn_bf16_cta(const CUtensorMap* tm_k_, const CU
         if (grp == 0) load_q(next, nqv);
       }
       const int64_t row0 = (static_cast<int64_t>(it.b) * a.hq + it.kvh * g) * a.splits + it.split;
+      if (tid == 0) {
+        prog[6] = item;
+        prog[7] = it.nch;
+      }
       if (it.nch > 0) {
         if (grp == 0) {
           // Q operand: 16 rows (heads, zero past g) x 128 channels, 128-byte swizzle
@@ -698,7 +724,8 @@ __device__ __forceinline__ void attn_bf16_cta(const CUtensorMap* tm_k_, const CU
               }
             }
             fence_async_smem();
-            mbar_arrive(p_full(grp));
+            mbar_arrive(p_full(cc % Ly::kPBufs));
+            if (t == 0) prog[3 + grp] = cc + 1;
             // two P buffers per group: the product two own chunks back is done
             // before its buffer is written again (next own chunk)
             if (Ly::kPBufs == 4 && last_own >= 0 && !take_o(last_own)) fail = true;
@@ -736,18 +763,32 @@ __device__ __forceinline__ void attn_bf16_cta(const CUtensorMap* tm_k_, const CU
         // both groups agree: after a wait ran out they leave the item loop together
         if (named_barrier_or(3, 256, fail)) break;
         if (grp == 0) {
+          // the two groups' combination: per head, the weights of the two
+          // states, 1 / l and the lse, computed once (thread h) into the
+          // chunk-max buffers (free after the chunk loop); then per channel
+          // two products and a scale
+          float* fac = red;  // [NH][4]
 #pragma unroll
-          for (int h = 0; h < NH; ++h) {  // unrolled: the heads' chains overlap
-            if (h < g) {
+          for (int h = 0; h < NH; ++h) {  // compile-time indices keep m[] in registers
+            if (t == h && h < g) {
               const float l0 = rs[h] + rs[NH + h] + rs[2 * NH + h] + rs[3 * NH + h];
               const float m1 = xm[h], l1 = xl[h];
               const float mx = fmaxf(m[h], m1);
               const float e0 = m[h] == -INFINITY ? 0.0f : exp2f(m[h] - mx);
               const float e1 = m1 == -INFINITY ? 0.0f : exp2f(m1 - mx);
               const float lt = l0 * e0 + l1 * e1;
-              const float ot = oacc[h] * e0 + xo[h * 128 + t] * e1;
-              const float o = lt > 0.0f ? ot / lt : 0.0f;
-              const float lse = lt > 0.0f ? (mx + log2f(lt)) * kLn2 : -INFINITY;
+              const float inv = lt > 0.0f ? 1.0f / lt : 0.0f;
+              fac[4 * h] = e0 * inv;
+              fac[4 * h + 1] = e1 * inv;
+              fac[4 * h + 3] = lt > 0.0f ? (mx + log2f(lt)) * kLn2 : -INFINITY;
+            }
+          }
+          named_barrier(bar, 128);
+#pragma unroll
+          for (int h = 0; h < NH; ++h) {
+            if (h < g) {
+              const float o = fmaf(oacc[h], fac[4 * h], xo[h * 128 + t] * fac[4 * h + 1]);
+              const float lse = fac[4 * h + 3];
               if constexpr (PART_SMEM) {
                 emit(h, t, o, lse);
               } else {
@@ -776,7 +817,8 @@ __device__ __forceinline__ void attn_bf16_cta(const CUtensorMap* tm_k_, const CU
   // ---- tear-down ----
   tc_fence_before();
   __syncthreads();
-  if (*abort_flag && tid == 0) set_error(err, HS_EBIT_TIMEOUT);
+  if (*abort_flag && tid == 0)
+    report_timeout(err, PART_SMEM ? kTimeoutStepFused : kTimeoutAttnBf16, static_cast<unsigned>(abort_flag[2]), prog);
   if (warp == kMma1B) {
     tc_fence_after();
     tmem_dealloc(tmem, Ly::kTmemCols);
@@ -919,7 +961,8 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     mbar_init(tile_full, 1);
     mbar_init(q_full, 128);
     mbar_init(acc_full, 1);
-    *abort_flag = 0;
+    abort_flag[0] = 0;
+    abort_flag[2] = 0;
   }
   attn_bf16_setup<NH>(smem);
   tc_fence_before();
@@ -1074,7 +1117,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     s_list[p - s0] = e;
   }
   if (bad) set_error(err, bad);
-  if (*abort_flag && tid == 0) set_error(err, HS_EBIT_TIMEOUT);
+  if (*abort_flag && tid == 0) report_timeout(err, kTimeoutStepFused, static_cast<unsigned>(abort_flag[2]));
   fence_async_smem();  // the scratch's generic writes before the ring's TMA writes
   __syncthreads();
 
@@ -1122,48 +1165,60 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 // e4m3 K/V (one fp32 scale per 32 channels per token), head_dim 128, g <= 8.
 //
 // The e4m3 codes are exact in f16 (one conversion instruction per pair of
-// codes), so the MMAs run on f16 codes and the scales are applied in fp32
-// around them (q and the weights W enter as f16; both operands of every MMA
-// are f16):
+// codes).  Both operands of every MMA are f16:
 //   GEMM1  S'[tok][(grp, h)] = sum_{d in grp} code_k[tok][d] * q[h][d]   (N = 4 groups x 8 heads)
-//          S[tok][h] = sum_grp kscale[tok][grp] * S'[tok][(grp, h)]
-//   GEMM2  O'[d][(grp, hl, h)] = sum_tok code_v[tok][d] * W_hl[tok][(grp, h)],
-//          W = p[tok][h] * vscale[tok][grp] split into f16 hi + lo (N = 64);
-//          channel d keeps the columns of its own group grp = d / 32.
-// TMA stages the raw codes and scales; two converter warpgroups turn each
-// chunk's codes into f16 operand tiles (zero rows for tokens outside the
-// request).  K tile conversion of chunk c+1 overlaps the softmax of chunk c;
-// the V tile of chunk c is converted once GEMM2 of chunk c-1 is done.  The
-// softmax warps publish P' of chunk c before they take the O' of chunk c-1,
-// so that wait is off their chain.
+//          S[tok][h] = sum_grp kscale[tok][grp] * S'[tok][(grp, h)]  (fp32: the K products are exact)
+//   GEMM2  O[d][(hl, h)] = sum_tok v[tok][d] * P_hl[tok][h],  N = 16,
+//          v = code_v * vscale rounded once to f16 (relative error <= 2^-12),
+//          P split into f16 hi + lo.
+// TMA stages the raw codes and scales (three stages).  One converter
+// warpgroup turns K codes into the f16 K tile once GEMM1 of the previous chunk
+// is done with it; another turns V codes and their scales into one of two f16
+// V tiles once GEMM2 of the chunk two back is done with it, so a stage is
+// released as soon as its K tile is scored.  The softmax warpgroup publishes P
+// of chunk c before it takes the O of chunk c-1.
 // ============================================================================
 constexpr int kStages8 = 3;
 constexpr int kCodeBytes = kChunk * 128;          // 128 tokens x 128 codes
 constexpr int kScaleBytes = kChunk * 16;          // 128 tokens x 4 scales
 constexpr int kStage8Bytes = 2 * kCodeBytes + 2 * kScaleBytes;
 struct Layout8 {
-  static constexpr int kOffKbf = kStages8 * kStage8Bytes;  // f16 K tile (2 halves, swizzled)
-  static constexpr int kOffVbf = kOffKbf + kTileBytes;
-  static constexpr int kQHalf = 32 * 128;                   // 32 rows (group x head) x 64 channels
-  static constexpr int kOffQ = kOffVbf + kTileBytes;
-  static constexpr int kPBytes = kChunk * 64 * 2;           // 128 tokens x 64 columns bf16
+  static constexpr int kOffKh = kStages8 * kStage8Bytes;    // f16 K tile (2 halves, swizzled)
+  static constexpr int kOffVh = kOffKh + kTileBytes;         // two f16 V tiles
+  static constexpr int kQHalf = 32 * 128;                    // 32 rows (group x head) x 64 channels
+  static constexpr int kOffQ = kOffVh + 2 * kTileBytes;
+  static constexpr int kPLbo = 8 * 16 * 2;                   // bytes between 8-token groups of P
+  static constexpr int kPBytes = kChunk * 16 * 2;            // 128 tokens x (hi, lo) x 8 heads, f16
   static constexpr int kOffP = kOffQ + 2 * kQHalf;
   static constexpr int kOffBar = kOffP + 2 * kPBytes;
-  static constexpr int kNumBars = 2 * kStages8 + 13;
+  static constexpr int kNumBars = 2 * kStages8 + 14;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kOffRed = kOffMisc + 16;
   static constexpr int kOffMeta = kOffRed + 3 * 4 * 8 * 4;
-  static constexpr int kBytes = kOffMeta + kStages8 * 8 * 8;
+  static constexpr int kOffProg = kOffMeta + kStages8 * 8 * 8;  // progress words (as in the bf16 kernel)
+  static constexpr int kBytes = kOffProg + 32;
   static constexpr int kAlloc = (kBytes + 1024 + 127) / 128 * 128;  // layout + base alignment
   static_assert(kAlloc <= 232448, "shared memory layout too large");
-  static_assert(kOffKbf % 1024 == 0 && kOffQ % 1024 == 0, "swizzled tiles need 1024-byte alignment");
-  static constexpr int kTmemCols = 256;
-  static constexpr int kColO = 64;  // S' uses columns [0, 64)
+  static_assert(kOffKh % 1024 == 0 && kOffVh % 1024 == 0 && kOffQ % 1024 == 0 && kOffP % 1024 == 0,
+                "swizzled tiles need 1024-byte alignment");
+  static constexpr int kTmemCols = 128;
+  static constexpr int kColO = 64;  // S' uses columns [0, 64), O [64, 96)
 };
 
 // one token row of e4m3 codes -> f16 row of a 128-byte-swizzled K-major tile
-// (the conversion is exact)
-__device__ __forceinline__ void convert_row(const uint8_t* codes_row, uint8_t* tile, int t, bool valid) {
+// (the conversion is exact); with SCALED, each code times its group's scale,
+// rounded once to f16
+template <bool SCALED>
+__device__ __forceinline__ void convert_row(const uint8_t* codes_row, const float* scales, uint8_t* tile, int t,
+                                            bool valid) {
+  float sc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  if (SCALED && valid) {
+    const float4 s4 = *reinterpret_cast<const float4*>(scales);
+    sc[0] = s4.x;
+    sc[1] = s4.y;
+    sc[2] = s4.z;
+    sc[3] = s4.w;
+  }
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int ch = (i + t) & 7;  // staggered so a warp's reads spread over the banks
@@ -1173,10 +1228,19 @@ __device__ __forceinline__ void convert_row(const uint8_t* codes_row, uint8_t* t
     uint32_t w[8];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const __half2_raw a = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(words[j] & 0xffffu), __NV_E4M3);
-      const __half2_raw b = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(words[j] >> 16), __NV_E4M3);
-      w[2 * j] = static_cast<uint32_t>(a.x) | (static_cast<uint32_t>(a.y) << 16);
-      w[2 * j + 1] = static_cast<uint32_t>(b.x) | (static_cast<uint32_t>(b.y) << 16);
+#pragma unroll
+      for (int hw = 0; hw < 2; ++hw) {
+        const __half2_raw r =
+            __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>((words[j] >> (16 * hw)) & 0xffffu), __NV_E4M3);
+        uint32_t bits = static_cast<uint32_t>(r.x) | (static_cast<uint32_t>(r.y) << 16);
+        if constexpr (SCALED) {
+          const float s = sc[ch >> 1];  // 16 codes per ch, 32 per scale group
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&bits));
+          const __half2 h = __floats2half2_rn(f.x * s, f.y * s);
+          bits = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        w[2 * j + hw] = bits;
+      }
     }
     uint8_t* row = tile + (ch >> 2) * kHalfBytes + t * 128;
     const int lc = (ch & 3) * 2;
@@ -1216,11 +1280,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto o_free = [&](int b) { return bar0 + 8 * (2 * kStages8 + 8 + b); };
   const uint32_t q_full = bar0 + 8 * (2 * kStages8 + 10);
   const uint32_t kconv_full = bar0 + 8 * (2 * kStages8 + 11);
-  const uint32_t vconv_full = bar0 + 8 * (2 * kStages8 + 12);
+  auto vconv_full = [&](int b) { return bar0 + 8 * (2 * kStages8 + 12 + b); };  // one per V tile
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Ly::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Ly::kOffMisc + 4);
   volatile int* s_last = reinterpret_cast<volatile int*>(smem + Ly::kOffMisc + 8);  // last split of an item
   float* red = reinterpret_cast<float*>(smem + Ly::kOffRed);
+  volatile int* prog = reinterpret_cast<volatile int*>(smem + Ly::kOffProg);
   auto kc_stage = [&](int s) { return smem + s * kStage8Bytes; };
   auto vc_stage = [&](int s) { return smem + s * kStage8Bytes + kCodeBytes; };
   auto ks_stage = [&](int s) { return smem + s * kStage8Bytes + 2 * kCodeBytes; };
@@ -1246,11 +1311,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(p_full(b), 128);
       mbar_init(o_full(b), 1);
       mbar_init(o_free(b), 128);
+      mbar_init(vconv_full(b), 128);
     }
     mbar_init(q_full, 128);
     mbar_init(kconv_full, 128);
-    mbar_init(vconv_full, 128);
-    *abort_flag = 0;
+    abort_flag[0] = 0;
+    abort_flag[2] = 0;
+    for (int i = 0; i < 8; ++i) reinterpret_cast<volatile int*>(smem + Ly::kOffProg)[i] = 0;
     fence_barrier_init();
   }
   if (warp == kMmaWarp) {
@@ -1266,7 +1333,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int2* meta = reinterpret_cast<int2*>(smem + Ly::kOffMeta);
   if (warp == kProducerWarp) {
     run_producer<kStages8>(a, w, bpc, full_bar(0), empty_bar(0), meta, 2u * B * 128u + 2u * B * 16u, abort_flag, err,
-                           [&](int s, int bi, int page) {
+                           prog, [&](int s, int bi, int page) {
                              const int y = page * B;
                              tma_load_2d(smem_u32(kc_stage(s)) + bi * B * 128, &tm_k, 0, y, full_bar(s));
                              tma_load_2d(smem_u32(vc_stage(s)) + bi * B * 128, &tm_v, 0, y, full_bar(s));
@@ -1279,12 +1346,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const bool first = warp == kMmaWarp;
       constexpr uint32_t idesc1 = idesc_f16(128, 32, false, false);
-      constexpr uint32_t idesc2 = idesc_f16(128, 64, true, true);
-      const uint64_t kdesc = smem_desc(sbase + Ly::kOffKbf, 16, 1024, 2);
+      constexpr uint32_t idesc2 = idesc_f16(128, 2 * NH, true, true);
+      const uint64_t kdesc = smem_desc(sbase + Ly::kOffKh, 16, 1024, 2);
       const uint64_t qdesc = smem_desc(sbase + Ly::kOffQ, 16, 1024, 2);
-      const uint64_t vdesc = smem_desc(sbase + Ly::kOffVbf, kHalfBytes, 1024, 2);
-      const uint64_t pdesc = smem_desc(sbase + Ly::kOffP, 1024, 128, 0);
-      int c = 0, qi = 0, last_g2 = -1;
+      const uint64_t vdesc = smem_desc(sbase + Ly::kOffVh, kHalfBytes, 1024, 2);
+      const uint64_t pdesc = smem_desc(sbase + Ly::kOffP, Ly::kPLbo, 128, 0);
+      int c = 0, qi = 0;
       int item = w.first;
       Item it = item < a.items ? item_geom(a, item, bpc, w) : Item{};
       bool ok = true;
@@ -1310,32 +1377,33 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             mma_commit(s_full(bb));
           } else {
-            ok = mbar_wait(p_full(bb), (c >> 1) & 1, abort_flag, a.wait_ns) && mbar_wait(vconv_full, c & 1, abort_flag, a.wait_ns) &&
+            ok = mbar_wait(p_full(bb), (c >> 1) & 1, abort_flag, a.wait_ns) &&
+                 mbar_wait(vconv_full(bb), (c >> 1) & 1, abort_flag, a.wait_ns) &&
                  (c < 2 || mbar_wait(o_free(bb), ((c >> 1) + 1) & 1, abort_flag, a.wait_ns));
             if (!ok) break;
             tc_fence_after();
 #pragma unroll
             for (int k = 0; k < kChunk / 16; ++k) {
-              const uint32_t poff = bb * Ly::kPBytes + k * 2048;
-              mma_f16(tmem + Ly::kColO + bb * 64, vdesc + ((k * 2048) >> 4), pdesc + (poff >> 4), idesc2,
-                      k > 0 ? 1u : 0u);
+              const uint32_t voff = bb * kTileBytes + k * 2048;
+              const uint32_t poff = bb * Ly::kPBytes + k * 2 * Ly::kPLbo;
+              mma_f16(tmem + Ly::kColO + bb * 16, vdesc + (voff >> 4), pdesc + (poff >> 4), idesc2, k > 0 ? 1u : 0u);
             }
             mma_commit(o_full(bb));
-            last_g2 = c;
           }
         }
         item = next;
         it = nit;
       }
       // every product this thread issued is complete before TMEM is released
+      // (a commit arrives once all of the thread's earlier MMAs are done)
       if (first && c > 0) mbar_drain(s_full((c - 1) & 1), ((c - 1) >> 1) & 1);
-      if (!first && last_g2 >= 0) mbar_drain(o_full(last_g2 & 1), (last_g2 >> 1) & 1);
+      if (!first && c > 0) mbar_drain(o_full((c - 1) & 1), ((c - 1) >> 1) & 1);
     }
   } else if (warp >= kConvWarp0 && warp < kConvVWarp0 + 4) {
-    // ================= code conversion: e4m3 rows -> bf16 operand tiles =================
-    // one warpgroup converts K of chunk c once the S' product of chunk c-1 is
-    // done with the K tile, the other V of chunk c once the P'.V product of
-    // chunk c-1 is done with the V tile; each then releases its part of the stage
+    // ================= code conversion: e4m3 rows -> f16 operand tiles =================
+    // K: chunk c into the K tile once the S' product of chunk c-1 is done with
+    // it; V: chunk c, scaled, into V tile c & 1 once the P.V product of chunk
+    // c-2 is done with it; each then releases its part of the stage
     const bool is_k = warp < kConvVWarp0;
     const int ct = tid - (is_k ? kConvWarp0 : kConvVWarp0) * 32;  // row of the chunk
     int c = 0;
@@ -1344,18 +1412,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Item it = item_geom(a, item, bpc, w);
       for (int ci = 0; ci < it.nch; ++ci, ++c) {
         const int s = c % kStages8;
-        const bool prev_done = c == 0 || (is_k ? mbar_wait(s_full((c - 1) & 1), ((c - 1) >> 1) & 1, abort_flag, a.wait_ns)
-                                               : mbar_wait(o_full((c - 1) & 1), ((c - 1) >> 1) & 1, abort_flag, a.wait_ns));
+        const bool prev_done =
+            is_k ? (c == 0 || mbar_wait(s_full((c - 1) & 1), ((c - 1) >> 1) & 1, abort_flag, a.wait_ns))
+                 : (c < 2 || mbar_wait(o_full(c & 1), ((c - 2) >> 1) & 1, abort_flag, a.wait_ns));
         if (!mbar_wait(full_bar(s), (c / kStages8) & 1, abort_flag, a.wait_ns) || !prev_done) {
           ok = false;
           break;
         }
         const int2 md = meta[s * 8 + ct / B];
         const bool valid = md.x >= 0 && (ct % B) < md.y;
-        convert_row((is_k ? kc_stage(s) : vc_stage(s)) + ct * 128, smem + (is_k ? Ly::kOffKbf : Ly::kOffVbf), ct,
-                    valid);
+        if (is_k) {
+          convert_row<false>(kc_stage(s) + ct * 128, nullptr, smem + Ly::kOffKh, ct, valid);
+        } else {
+          convert_row<true>(vc_stage(s) + ct * 128, reinterpret_cast<const float*>(vs_stage(s) + ct * 16),
+                            smem + Ly::kOffVh + (c & 1) * kTileBytes, ct, valid);
+        }
         fence_async_smem();
-        mbar_arrive(is_k ? kconv_full : vconv_full);
+        mbar_arrive(is_k ? kconv_full : vconv_full(c & 1));
         mbar_arrive(empty_bar(s));
       }
     }
@@ -1396,15 +1469,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         it = nit;
         continue;
       }
-      // the item's query rows (not prefetched a whole item ahead: registers
-      // are the softmax warps' limit here)
-      uint4 qv[4];
-      load_q(item, qv);
+      {  // the item's query rows
+        uint4 qv[4];
+        load_q(item, qv);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int idx = t * 4 + i;
-        const int half = idx >> 8, rem = idx & 255, row = rem >> 3, ch = rem & 7;
-        *reinterpret_cast<uint4*>(smem + Ly::kOffQ + half * Ly::kQHalf + row * 128 + ((ch ^ (row & 7)) << 4)) = qv[i];
+        for (int i = 0; i < 4; ++i) {
+          const int idx = t * 4 + i;
+          const int half = idx >> 8, rem = idx & 255, row = rem >> 3, ch = rem & 7;
+          *reinterpret_cast<uint4*>(smem + Ly::kOffQ + half * Ly::kQHalf + row * 128 + ((ch ^ (row & 7)) << 4)) =
+              qv[i];
+        }
       }
       fence_async_smem();
       mbar_arrive(q_full);
@@ -1423,7 +1497,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!__all_sync(0xffffffffu, mbar_wait(o_full(bb), (cc >> 1) & 1, abort_flag, a.wait_ns))) return false;
         tc_fence_after();
         float ov[16];
-        tmem_ld16(tmem + lane_base + Ly::kColO + bb * 64 + warp * 16, ov);  // channel t's group = warp
+        tmem_ld16(tmem + lane_base + Ly::kColO + bb * 16, ov);
         tc_fence_before();
         mbar_arrive(o_free(bb));
 #pragma unroll
@@ -1433,7 +1507,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int c0 = c;
       for (int ci = 0; ci < it.nch; ++ci) {
         const int cc = c0 + ci, bb = cc & 1, s = cc % kStages8;
-        // row t of the chunk: token t % B of its (t / B)-th block; its K and V
+        // row t of the chunk: token t % B of its (t / B)-th block; its K
         // scales come from this chunk's stage
         bool ready = !fail && mbar_wait(full_bar(s), (cc / kStages8) & 1, abort_flag, a.wait_ns);
         const int2 md = ready ? meta[s * 8 + t / B] : make_int2(-1, 0);
@@ -1445,7 +1519,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ready = __all_sync(0xffffffffu, ready && mbar_wait(s_full(bb), (cc >> 1) & 1, abort_flag, a.wait_ns));
         // S = sum over the 4 channel groups of kscale * S', two groups per TMEM load
-        float x[NH];
+        float x[NH], r[NH];
 #pragma unroll
         for (int h = 0; h < NH; ++h) x[h] = 0.0f;
         if (ready) {
@@ -1461,18 +1535,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_before();
           mbar_arrive(s_free(bb));
         }
-#pragma unroll
-        for (int h = 0; h < NH; ++h) x[h] = (valid_cur && h < g) ? x[h] * a.scale_log2 : -INFINITY;
+        if (ready) mbar_arrive(empty_bar(s));  // the stage's meta and K scales are read
 #pragma unroll
         for (int h = 0; h < NH; ++h) {
-          const float mx = warp_max(x[h]);
-          if (lane == 0) red[(cc & 1) * 4 * NH + warp * NH + h] = mx;
+          x[h] = (valid_cur && h < g) ? x[h] * a.scale_log2 : -INFINITY;
+          r[h] = x[h];
         }
+        // chunk max per head over the 128 rows: warp reduce-scatter, then the 4 warps
+        float* rb = red + (cc & 1) * 4 * NH;  // alternate buffers: one barrier per chunk
+        const float wmax = warp_reduce_scatter<NH, true>(r);
+        if ((lane % (32 / NH)) == 0) rb[warp * NH + lane / (32 / NH)] = wmax;
         if (named_barrier_or(1, 128, fail || !ready)) {
           fail = true;
           break;
         }
-        const float* rb = red + (cc & 1) * 4 * NH;  // alternate buffers: one barrier per chunk
         float alpha[NH], p[NH];
 #pragma unroll
         for (int h = 0; h < NH; ++h) {
@@ -1483,47 +1559,42 @@ __global__ void __launch_bounds__(kThreads, 1)
           p[h] = x[h] == -INFINITY ? 0.0f : exp2f(x[h] - mn);
           lsum[h] = fmaf(lsum[h], alpha[h], p[h]);
         }
-        if (!fail) {
-          const float4 vsc =
-              valid_cur ? *reinterpret_cast<const float4*>(vs_stage(s) + t * 16) : make_float4(0, 0, 0, 0);
-          const float vs[4] = {vsc.x, vsc.y, vsc.z, vsc.w};
-          uint8_t* prow = smem + Ly::kOffP + bb * Ly::kPBytes + (t >> 3) * 1024 + (t & 7) * 16;
+        // P of chunk c into buffer c & 1 (its last reader, the product of chunk
+        // c - 2, completed before this group took its O one chunk ago), as
+        // f16 high part + remainder
+        {
+          uint32_t hi2[NH / 2], lo2[NH / 2];
 #pragma unroll
-          for (int grp = 0; grp < 4; ++grp) {
-            uint32_t hi2[4], lo2[4];
-#pragma unroll
-            for (int h = 0; h < NH; h += 2) {
-              const float w0 = p[h] * vs[grp], w1 = p[h + 1] * vs[grp];
-              const __half2 hi = __floats2half2_rn(w0, w1);
-              const float2 hf = __half22float2(hi);
-              const __half2 lo = __floats2half2_rn(w0 - hf.x, w1 - hf.y);
-              hi2[h / 2] = *reinterpret_cast<const uint32_t*>(&hi);
-              lo2[h / 2] = *reinterpret_cast<const uint32_t*>(&lo);
-            }
-            *reinterpret_cast<uint4*>(prow + (grp * 2) * 128) = make_uint4(hi2[0], hi2[1], hi2[2], hi2[3]);
-            *reinterpret_cast<uint4*>(prow + (grp * 2 + 1) * 128) = make_uint4(lo2[0], lo2[1], lo2[2], lo2[3]);
+          for (int h = 0; h < NH; h += 2) {
+            const __half2 hi = __floats2half2_rn(p[h], p[h + 1]);
+            const float2 hf = __half22float2(hi);
+            const __half2 lo = __floats2half2_rn(p[h] - hf.x, p[h + 1] - hf.y);
+            hi2[h / 2] = *reinterpret_cast<const uint32_t*>(&hi);
+            lo2[h / 2] = *reinterpret_cast<const uint32_t*>(&lo);
           }
-          fence_async_smem();
-          mbar_arrive(p_full(bb));
-          mbar_arrive(empty_bar(s));  // this group is done with the stage's meta and scales
-          // O' of the previous chunk, once P' of this one is out (P' of chunk c
-          // goes to buffer c & 1, last read by the product of chunk c - 2,
-          // whose O' this group took one chunk ago)
-          if (ci > 0 && !take_o(cc - 1)) fail = true;
+          uint8_t* prow = smem + Ly::kOffP + bb * Ly::kPBytes + (t >> 3) * Ly::kPLbo + (t & 7) * 16;
+          *reinterpret_cast<uint4*>(prow) = make_uint4(hi2[0], hi2[1], hi2[2], hi2[3]);
+          *reinterpret_cast<uint4*>(prow + 128) = make_uint4(lo2[0], lo2[1], lo2[2], lo2[3]);
         }
+        fence_async_smem();
+        mbar_arrive(p_full(bb));
+        // O of the previous chunk, once P of this one is out
+        if (ci > 0 && !take_o(cc - 1)) fail = true;
 #pragma unroll
         for (int h = 0; h < NH; ++h) alpha_prev[h] = alpha[h];
       }
       c = c0 + it.nch;
       // the normaliser reduction overlaps the last P.V product
+      float* rs = red + 8 * NH;
+      {
+        float r[NH];
 #pragma unroll
-      for (int h = 0; h < NH; ++h) {
-        const float s_ = warp_sum(lsum[h]);
-        if (lane == 0) red[8 * NH + warp * NH + h] = s_;
+        for (int h = 0; h < NH; ++h) r[h] = lsum[h];
+        const float wsum = warp_reduce_scatter<NH, false>(r);
+        if ((lane % (32 / NH)) == 0) rs[warp * NH + lane / (32 / NH)] = wsum;
       }
       if (!fail && !take_o(c - 1)) fail = true;
       if (named_barrier_or(1, 128, fail)) break;  // all 128 threads leave the item loop together
-      const float* rs = red + 8 * NH;
       for (int h = 0; h < g && h < NH; ++h) {
         const float lt = rs[h] + rs[NH + h] + rs[2 * NH + h] + rs[3 * NH + h];
         put_partial(a, row0, h, t, lt > 0.0f ? oacc[h] / lt : 0.0f,
@@ -1538,7 +1609,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (*abort_flag && tid == 0) set_error(err, HS_EBIT_TIMEOUT);
+  if (*abort_flag && tid == 0) report_timeout(err, kTimeoutAttnE4m3, static_cast<unsigned>(abort_flag[2]), prog);
   if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, Ly::kTmemCols);

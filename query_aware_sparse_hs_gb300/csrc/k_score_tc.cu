@@ -183,7 +183,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(q_full(b), 128);
       mbar_init(q_free(b), 1);
     }
-    *abort_flag = 0;
+    abort_flag[0] = 0;
+    abort_flag[2] = 0;
     fence_barrier_init();
   }
   if (warp == kMmaWarp) {
@@ -366,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                          smoothed ? nullptr : s_range, kThreads / 32, true);
     }
   }
-  if (*abort_flag && tid == 0) set_error(err, HS_EBIT_TIMEOUT);
+  if (*abort_flag && tid == 0) report_timeout(err, kTimeoutScore, static_cast<unsigned>(abort_flag[2]));
   if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);

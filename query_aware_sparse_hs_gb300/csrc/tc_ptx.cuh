@@ -18,6 +18,12 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+__device__ __forceinline__ uint64_t sm_cycles() {
+  uint64_t c;
+  asm volatile("mov.u64 %0, %%clock64;" : "=l"(c));
+  return c;
+}
+
 // ---- mbarrier ----
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
@@ -64,10 +70,24 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Wall time and SM cycles of a bounded wait: it runs out only when both say
+// that `limit_ns` has passed (at least 2 cycles per nanosecond: the SM clock
+// is at most about 2.1 GHz), so neither a jump of the global timer nor a
+// slowed SM clock alone ends a wait early.
+struct WaitClock {
+  uint64_t t0, c0;
+  __device__ __forceinline__ WaitClock() : t0(globaltimer_ns()), c0(sm_cycles()) {}
+  __device__ __forceinline__ bool past(uint64_t limit_ns) const {
+    return globaltimer_ns() - t0 > limit_ns && sm_cycles() - c0 > 2 * limit_ns;
+  }
+};
+
 // Waits for the phase with the given parity to complete.  Gives up after
-// `limit_ns` of wall time or as soon as *abort is set (at once when the phase
+// `limit_ns` (WaitClock) or as soon as *abort is set (at once when the phase
 // is not complete and *abort is set already); on a time-out it sets *abort so
-// every other role of the CTA stops too.  Returns false when it gave up.  A
+// every other role of the CTA stops too, and leaves in abort[2] which wait
+// ran out: the barrier's shared-memory address (bits 0-17), the parity (bit
+// 18), the warp (bits 19-23), bit 31 set.  Returns false when it gave up.  A
 // phase that is complete already costs one non-blocking test.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
                                           uint64_t limit_ns = kWaitLimitNs) {
@@ -75,10 +95,12 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   if (*abort) return false;
   const uint32_t hint = limit_ns < 1000000ull ? static_cast<uint32_t>(limit_ns) : 1000000u;
   if (mbar_try(bar, parity, hint)) return true;
-  const uint64_t t0 = globaltimer_ns();
+  const WaitClock clk;
   for (;;) {
     if (*abort) return false;
-    if (globaltimer_ns() - t0 > limit_ns) {
+    if (clk.past(limit_ns)) {
+      abort[2] = static_cast<int>((bar & 0x3FFFFu) | ((parity & 1u) << 18) | (((threadIdx.x >> 5) & 31u) << 19) |
+                                  0x80000000u);
       *abort = 1;
       return false;
     }
@@ -92,10 +114,10 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 // CTA is stopping.  Bounded by `limit_ns`; returns false if that passed.
 __device__ __forceinline__ bool mbar_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns = kDrainLimitNs) {
   if (mbar_try(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
+  const WaitClock clk;
   for (;;) {
     if (mbar_try(bar, parity)) return true;
-    if (globaltimer_ns() - t0 > limit_ns) return false;
+    if (clk.past(limit_ns)) return false;
   }
 }
 

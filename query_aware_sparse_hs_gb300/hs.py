@@ -109,6 +109,7 @@ SYMBOLS = {
     "hs_quantize_e4m3_g32": (c_int32, [c_void_p, c_int32, c_int64, c_int32, c_void_p, c_void_p,
                                        c_void_p]),
     "hs_get_device_error": (c_int32, [c_void_p, POINTER(c_uint32)]),
+    "hs_get_device_error_detail": (c_int32, [c_void_p, POINTER(c_uint32), POINTER(c_uint32)]),
 }
 
 
@@ -341,3 +342,24 @@ def hs_get_device_error(stream=None) -> tuple[int, int]:
     bits = c_uint32(0)
     st = _lib.hs_get_device_error(_stream(stream), ctypes.byref(bits))
     return int(st), int(bits.value)
+
+
+TIMEOUT_KERNELS = {1: "tensor-core attention", 2: "single-launch step", 3: "e4m3 attention",
+                   4: "tensor-core bound scoring"}
+
+
+def hs_get_device_error_detail(stream=None) -> tuple[int, int, dict | None]:
+    """(status, bits, where) - where describes the first bounded wait that ran
+    out since the last read (None if none): kernel, CTA, barrier address,
+    parity, warp."""
+    bits = c_uint32(0)
+    rec = (c_uint32 * 11)()
+    st = _lib.hs_get_device_error_detail(_stream(stream), ctypes.byref(bits), rec)
+    where = None
+    if rec[0]:
+        w = rec[2]
+        names = ("issued", "mma_s", "mma_o", "softmax0", "softmax1", "producer_item", "softmax_item", "item_chunks")
+        where = {"kernel": TIMEOUT_KERNELS.get(rec[0], rec[0]), "cta": int(rec[1]), "barrier": w & 0x3FFFF,
+                 "parity": (w >> 18) & 1, "warp": (w >> 19) & 31,
+                 "progress": {n: int(ctypes.c_int32(rec[3 + i]).value) for i, n in enumerate(names)}}
+    return int(st), int(bits.value), where

@@ -132,8 +132,12 @@ def test_wait_that_runs_out_reports_timeout_then_the_next_call_is_exact(single_l
             assert hs.hs_get_device_error() == (hs.HS_OK, 0)
             hs.hs_sparse_paged_decode_attn(dec.shape, c.kv, c.q, dec.sel, dec.sel_count, dec.capacity, short,
                                            dec.out, dec.lse, dec.workspace)
-        st, bits = hs.hs_get_device_error()
+        st, bits, where = hs.hs_get_device_error_detail()
         assert st == hs.HS_ERR_TIMEOUT and bits & hs.HS_EBIT_TIMEOUT, (st, bits)
+        # the record of the first wait that ran out names the kernel and a warp of a CTA of it
+        assert where is not None, where
+        assert where["kernel"] == ("single-launch step" if single_launch else "tensor-core attention"), where
+        assert 0 <= where["warp"] < 11 and 0 <= where["cta"] < 1024, where
         dec.split_counters.zero_()
     dec.out.fill_(float("nan"))
     if single_launch:
