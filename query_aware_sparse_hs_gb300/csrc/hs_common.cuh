@@ -124,6 +124,18 @@ __host__ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b -
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// Lets `kern` take `dynamic` bytes of dynamic shared memory where that plus
+// its static shared memory passes the 48 KB a launch gets by default.
+template <typename... KArgs>
+cudaError_t allow_dynamic_smem(void (*kern)(KArgs...), size_t dynamic) {
+  if (dynamic <= 16 * 1024) return cudaSuccess;  // no kernel here has 32 KB of static shared memory
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+  if (e != cudaSuccess) return e;
+  if (dynamic + fa.sharedSizeBytes <= 48 * 1024) return cudaSuccess;
+  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(dynamic));
+}
+
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
                        Args&&... args) {

@@ -850,9 +850,14 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 //            stores it (and the history) - and resolves the blocks of its
 //            own split, whole 128-token chunks spread evenly over the splits,
 //            to (page, valid tokens).
-//   phase 3  CTA r is the attention CTA of split r (a one-item Work).
-// Nothing waits on another cluster, and no CTA touches another's shared
-// memory after the cluster barrier.
+//   phase 3  CTA r is the attention CTA of split r (a one-item Work); each
+//            head's result is pushed into the push buffer (kOffPush, used by
+//            nothing else) of the CTA of the cluster that merges that head.
+//   phase 4  after a second cluster barrier, which orders those pushes and
+//            keeps every CTA resident until they have landed, each CTA
+//            merges its heads from its own push buffer.
+// Nothing waits on another cluster.  Between the two cluster barriers a CTA
+// touches another's shared memory only through the phase-3 pushes.
 constexpr int kFuseMaxCluster = 8;
 constexpr int kFuseList = 256;   // selected blocks of one split held in shared memory
 constexpr int kPushSlots = 13;   // (split, head) results one CTA merges
@@ -1089,7 +1094,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   if (warp == kProdB && lane == 0 && rank < f.tiles)  // the tile has landed before the ring is reused
     mbar_drain(tile_full, 0);
   if (bound_issued) mbar_drain(acc_full, 0);  // the bound product is done before TMEM is reused
-  cluster.sync();  // every CTA holds all scores; no shared memory of another CTA is touched after this
+  cluster.sync();  // every CTA holds all scores; from here only phase 3's pushes reach another CTA's shared memory
 
   // ---- phase 2: every CTA selects; rank 0 stores the selection ----
   if (smoothed) sel::smooth_staged(s_scores, s_prev, nb, a.max_blocks, sa, pair, rank == 0);
@@ -1164,64 +1169,70 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 // ============================================================================
 // e4m3 K/V (one fp32 scale per 32 channels per token), head_dim 128, g <= 8.
 //
-// The e4m3 codes are exact in f16 (one conversion instruction per pair of
-// codes).  Both operands of every MMA are f16:
-//   GEMM1  S'[tok][(grp, h)] = sum_{d in grp} code_k[tok][d] * q[h][d]   (N = 4 groups x 8 heads)
-//          S[tok][h] = sum_grp kscale[tok][grp] * S'[tok][(grp, h)]  (fp32: the K products are exact)
-//   GEMM2  O[d][(hl, h)] = sum_tok v[tok][d] * P_hl[tok][h],  N = 16,
-//          v = code_v * vscale rounded once to f16 (relative error <= 2^-12),
-//          P split into f16 hi + lo.
-// TMA stages the raw codes and scales (three stages).  One converter
-// warpgroup turns K codes into the f16 K tile once GEMM1 of the previous chunk
-// is done with it; another turns V codes and their scales into one of two f16
-// V tiles once GEMM2 of the chunk two back is done with it, so a stage is
-// released as soon as its K tile is scored.  The softmax warpgroup publishes P
-// of chunk c before it takes the O of chunk c-1.
+// GEMM1 reads the K codes as TMA staged them (kind::f8f6f4, both operands
+// e4m3).  The query side is e4m3 too: each head's bf16 query row, times a
+// power of two 2^a_h that brings its largest entry into [128, 256), is split
+// into two e4m3 terms q1 + q2 whose sum is that row exactly (a bf16 value has
+// 8 significant bits, a term 4; entries below 2^-10 of 2^-a_h, where q2 is
+// subnormal, keep an error under 2^-10 * 2^-a_h).  Both terms accumulate
+// into the same columns:
+//   GEMM1  S'[tok][(grp, h)] = sum_{d in grp} code_k[tok][d] * (q1 + q2)[h][d]   (N = 4 groups x 8 heads)
+//          S[tok][h] = 2^-a_h * sum_grp kscale[tok][grp] * S'[tok][(grp, h)]
+//   GEMM2  O[d][(hl, h)] = sum_tok v[tok][d] * P_hl[tok][h],  N = 16, f16 operands,
+//          v = code_v * vscale in f16 (scale and product each rounded once:
+//          relative error <= 2^-10), P split into f16 hi + lo.
+// TMA stages the codes (K with the 128-byte swizzle the MMA reads) and the
+// scales, three stages.  Two converter warpgroups, two threads per row, turn
+// V codes times their scales into one of two f16 V tiles once GEMM2 of the
+// chunk two back is done with it.  The softmax warpgroup releases a stage
+// once GEMM1 of its chunk is complete and its K scales are read, and
+// publishes P of chunk c before it takes the O of chunk c-1.
 // ============================================================================
 constexpr int kStages8 = 3;
 constexpr int kCodeBytes = kChunk * 128;          // 128 tokens x 128 codes
 constexpr int kScaleBytes = kChunk * 16;          // 128 tokens x 4 scales
 constexpr int kStage8Bytes = 2 * kCodeBytes + 2 * kScaleBytes;
 struct Layout8 {
-  static constexpr int kOffKh = kStages8 * kStage8Bytes;    // f16 K tile (2 halves, swizzled)
-  static constexpr int kOffVh = kOffKh + kTileBytes;         // two f16 V tiles
-  static constexpr int kQHalf = 32 * 128;                    // 32 rows (group x head) x 64 channels
+  static constexpr int kOffVh = kStages8 * kStage8Bytes;     // two f16 V tiles
+  static constexpr int kQTerm = 32 * 128;                    // one e4m3 query term: 32 rows (group x head) x 128 codes
   static constexpr int kOffQ = kOffVh + 2 * kTileBytes;
   static constexpr int kPLbo = 8 * 16 * 2;                   // bytes between 8-token groups of P
   static constexpr int kPBytes = kChunk * 16 * 2;            // 128 tokens x (hi, lo) x 8 heads, f16
-  static constexpr int kOffP = kOffQ + 2 * kQHalf;
+  static constexpr int kOffP = kOffQ + 2 * kQTerm;
   static constexpr int kOffBar = kOffP + 2 * kPBytes;
-  static constexpr int kNumBars = 2 * kStages8 + 14;
+  static constexpr int kNumBars = 2 * kStages8 + 13;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kOffRed = kOffMisc + 16;
   static constexpr int kOffMeta = kOffRed + 3 * 4 * 8 * 4;
   static constexpr int kOffProg = kOffMeta + kStages8 * 8 * 8;  // progress words (as in the bf16 kernel)
-  static constexpr int kBytes = kOffProg + 32;
+  static constexpr int kOffQx = kOffProg + 32;                   // per head: the exponent a_h of the item's query
+  static constexpr int kBytes = kOffQx + 32;
   static constexpr int kAlloc = (kBytes + 1024 + 127) / 128 * 128;  // layout + base alignment
   static_assert(kAlloc <= 232448, "shared memory layout too large");
-  static_assert(kOffKh % 1024 == 0 && kOffVh % 1024 == 0 && kOffQ % 1024 == 0 && kOffP % 1024 == 0,
+  static_assert(kStage8Bytes % 1024 == 0 && kOffVh % 1024 == 0 && kOffQ % 1024 == 0 && kOffP % 1024 == 0,
                 "swizzled tiles need 1024-byte alignment");
   static constexpr int kTmemCols = 128;
   static constexpr int kColO = 64;  // S' uses columns [0, 64), O [64, 96)
 };
 
-// one token row of e4m3 codes -> f16 row of a 128-byte-swizzled K-major tile
-// (the conversion is exact); with SCALED, each code times its group's scale,
-// rounded once to f16
+// Half a token row of e4m3 codes (channels 64*cp .. 64*cp+63) -> f16 in a
+// 128-byte-swizzled K-major tile (the conversion is exact); with SCALED each
+// code is multiplied by its 32-channel group's scale in f16 (the scale and the
+// product each rounded once).  Two threads per row (r, cp = 0, 1); the
+// 16-byte segments are staggered so that eight consecutive threads touch
+// eight different bank groups on the loads and on the stores.
 template <bool SCALED>
-__device__ __forceinline__ void convert_row(const uint8_t* codes_row, const float* scales, uint8_t* tile, int t,
-                                            bool valid) {
-  float sc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-  if (SCALED && valid) {
-    const float4 s4 = *reinterpret_cast<const float4*>(scales);
-    sc[0] = s4.x;
-    sc[1] = s4.y;
-    sc[2] = s4.z;
-    sc[3] = s4.w;
+__device__ __forceinline__ void convert_half_row(const uint8_t* codes_row, const float* scales, uint8_t* tile, int r,
+                                                 int cp, bool valid) {
+  __half2 sc[2];
+  if constexpr (SCALED) {
+    const float2 s2 = valid ? *reinterpret_cast<const float2*>(scales + 2 * cp) : make_float2(0.0f, 0.0f);
+    sc[0] = __float2half2_rn(s2.x);
+    sc[1] = __float2half2_rn(s2.y);
   }
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int ch = (i + t) & 7;  // staggered so a warp's reads spread over the banks
+  for (int i = 0; i < 4; ++i) {
+    const int ch = 4 * cp + ((i + r + 2 * cp) & 3);  // 16-code segment of the row
     uint4 raw = make_uint4(0, 0, 0, 0);
     if (valid) raw = *reinterpret_cast<const uint4*>(codes_row + ch * 16);
     const uint32_t words[4] = {raw.x, raw.y, raw.z, raw.w};
@@ -1230,35 +1241,21 @@ __device__ __forceinline__ void convert_row(const uint8_t* codes_row, const floa
     for (int j = 0; j < 4; ++j) {
 #pragma unroll
       for (int hw = 0; hw < 2; ++hw) {
-        const __half2_raw r =
+        const __half2_raw h =
             __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>((words[j] >> (16 * hw)) & 0xffffu), __NV_E4M3);
-        uint32_t bits = static_cast<uint32_t>(r.x) | (static_cast<uint32_t>(r.y) << 16);
+        uint32_t bits = static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
         if constexpr (SCALED) {
-          const float s = sc[ch >> 1];  // 16 codes per ch, 32 per scale group
-          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&bits));
-          const __half2 h = __floats2half2_rn(f.x * s, f.y * s);
-          bits = *reinterpret_cast<const uint32_t*>(&h);
+          const __half2 v = __hmul2(*reinterpret_cast<const __half2*>(&bits), sc[(ch & 3) >> 1]);
+          bits = *reinterpret_cast<const uint32_t*>(&v);
         }
         w[2 * j + hw] = bits;
       }
     }
-    uint8_t* row = tile + (ch >> 2) * kHalfBytes + t * 128;
+    uint8_t* row = tile + (ch >> 2) * kHalfBytes + r * 128;
     const int lc = (ch & 3) * 2;
-    *reinterpret_cast<uint4*>(row + (((lc) ^ (t & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-    *reinterpret_cast<uint4*>(row + (((lc + 1) ^ (t & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
+    *reinterpret_cast<uint4*>(row + (((lc) ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint4*>(row + (((lc + 1) ^ (r & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
   }
-}
-
-// bf16 pairs -> f16 pairs (exact for query values within the f16 range)
-__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
-  uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xffff0000u);
-    const __half2 h = __floats2half2_rn(lo, hi);
-    w[i] = *reinterpret_cast<const uint32_t*>(&h);
-  }
-  return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -1279,8 +1276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto o_full = [&](int b) { return bar0 + 8 * (2 * kStages8 + 6 + b); };
   auto o_free = [&](int b) { return bar0 + 8 * (2 * kStages8 + 8 + b); };
   const uint32_t q_full = bar0 + 8 * (2 * kStages8 + 10);
-  const uint32_t kconv_full = bar0 + 8 * (2 * kStages8 + 11);
-  auto vconv_full = [&](int b) { return bar0 + 8 * (2 * kStages8 + 12 + b); };  // one per V tile
+  auto vconv_full = [&](int b) { return bar0 + 8 * (2 * kStages8 + 11 + b); };  // one per V tile
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Ly::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Ly::kOffMisc + 4);
   volatile int* s_last = reinterpret_cast<volatile int*>(smem + Ly::kOffMisc + 8);  // last split of an item
@@ -1311,10 +1307,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(p_full(b), 128);
       mbar_init(o_full(b), 1);
       mbar_init(o_free(b), 128);
-      mbar_init(vconv_full(b), 128);
+      mbar_init(vconv_full(b), 256);
     }
     mbar_init(q_full, 128);
-    mbar_init(kconv_full, 128);
     abort_flag[0] = 0;
     abort_flag[2] = 0;
     for (int i = 0; i < 8; ++i) reinterpret_cast<volatile int*>(smem + Ly::kOffProg)[i] = 0;
@@ -1345,9 +1340,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp || warp == kMma2Warp) {
     if (lane == 0) {
       const bool first = warp == kMmaWarp;
-      constexpr uint32_t idesc1 = idesc_f16(128, 32, false, false);
+      constexpr uint32_t idesc1 = idesc_e4m3(128, 32);
       constexpr uint32_t idesc2 = idesc_f16(128, 2 * NH, true, true);
-      const uint64_t kdesc = smem_desc(sbase + Ly::kOffKh, 16, 1024, 2);
+      const uint64_t kdesc = smem_desc(sbase, 16, 1024, 2);  // stage 0's K codes
       const uint64_t qdesc = smem_desc(sbase + Ly::kOffQ, 16, 1024, 2);
       const uint64_t vdesc = smem_desc(sbase + Ly::kOffVh, kHalfBytes, 1024, 2);
       const uint64_t pdesc = smem_desc(sbase + Ly::kOffP, Ly::kPLbo, 128, 0);
@@ -1365,15 +1360,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int ci = 0; ok && ci < it.nch; ++ci, ++c) {
           const int bb = c & 1;
           if (first) {
-            ok = mbar_wait(kconv_full, c & 1, abort_flag, a.wait_ns) &&
+            const int s = c % kStages8;
+            ok = mbar_wait(full_bar(s), (c / kStages8) & 1, abort_flag, a.wait_ns) &&
                  (c < 2 || mbar_wait(s_free(bb), ((c >> 1) + 1) & 1, abort_flag, a.wait_ns));
             if (!ok) break;
             tc_fence_after();
+            // two query terms x four K steps of 32 codes, into one accumulator
 #pragma unroll
-            for (int k = 0; k < kD / 16; ++k) {
-              const uint32_t koff = (k >> 2) * kHalfBytes + (k & 3) * 32;
-              const uint32_t qoff = (k >> 2) * Ly::kQHalf + (k & 3) * 32;
-              mma_f16(tmem + bb * 32, kdesc + (koff >> 4), qdesc + (qoff >> 4), idesc1, k > 0 ? 1u : 0u);
+            for (int k = 0; k < 8; ++k) {
+              const uint32_t koff = s * kStage8Bytes + (k & 3) * 32;
+              const uint32_t qoff = (k >> 2) * Ly::kQTerm + (k & 3) * 32;
+              mma_e4m3(tmem + bb * 32, kdesc + (koff >> 4), qdesc + (qoff >> 4), idesc1, k > 0 ? 1u : 0u);
             }
             mma_commit(s_full(bb));
           } else {
@@ -1400,35 +1397,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!first && c > 0) mbar_drain(o_full((c - 1) & 1), ((c - 1) >> 1) & 1);
     }
   } else if (warp >= kConvWarp0 && warp < kConvVWarp0 + 4) {
-    // ================= code conversion: e4m3 rows -> f16 operand tiles =================
-    // K: chunk c into the K tile once the S' product of chunk c-1 is done with
-    // it; V: chunk c, scaled, into V tile c & 1 once the P.V product of chunk
-    // c-2 is done with it; each then releases its part of the stage
-    const bool is_k = warp < kConvVWarp0;
-    const int ct = tid - (is_k ? kConvWarp0 : kConvVWarp0) * 32;  // row of the chunk
+    // ================= V conversion: e4m3 rows times scales -> f16 V tiles =================
+    // both converter warpgroups, two threads per row (one per 64-channel
+    // half): V of chunk c, scaled, into V tile c & 1 once the P.V product of
+    // chunk c-2 is done with it; then they release their part of the stage
+    const int ct = tid - kConvWarp0 * 32;  // 0..255
+    const int r = ct >> 1, cp = ct & 1;
     int c = 0;
     bool ok = true;
     for (int item = w.first; ok && item < a.items && !*abort_flag; item += w.stride) {
       const Item it = item_geom(a, item, bpc, w);
       for (int ci = 0; ci < it.nch; ++ci, ++c) {
         const int s = c % kStages8;
-        const bool prev_done =
-            is_k ? (c == 0 || mbar_wait(s_full((c - 1) & 1), ((c - 1) >> 1) & 1, abort_flag, a.wait_ns))
-                 : (c < 2 || mbar_wait(o_full(c & 1), ((c - 2) >> 1) & 1, abort_flag, a.wait_ns));
-        if (!mbar_wait(full_bar(s), (c / kStages8) & 1, abort_flag, a.wait_ns) || !prev_done) {
-          ok = false;
-          break;
-        }
-        const int2 md = meta[s * 8 + ct / B];
-        const bool valid = md.x >= 0 && (ct % B) < md.y;
-        if (is_k) {
-          convert_row<false>(kc_stage(s) + ct * 128, nullptr, smem + Ly::kOffKh, ct, valid);
-        } else {
-          convert_row<true>(vc_stage(s) + ct * 128, reinterpret_cast<const float*>(vs_stage(s) + ct * 16),
-                            smem + Ly::kOffVh + (c & 1) * kTileBytes, ct, valid);
-        }
+        ok = mbar_wait(full_bar(s), (c / kStages8) & 1, abort_flag, a.wait_ns) &&
+             (c < 2 || mbar_wait(o_full(c & 1), ((c - 2) >> 1) & 1, abort_flag, a.wait_ns));
+        if (!ok) break;
+        const int2 md = meta[s * 8 + r / B];
+        const bool valid = md.x >= 0 && (r % B) < md.y;
+        convert_half_row<true>(vc_stage(s) + r * 128, reinterpret_cast<const float*>(vs_stage(s) + r * 16),
+                               smem + Ly::kOffVh + (c & 1) * kTileBytes, r, cp, valid);
         fence_async_smem();
-        mbar_arrive(is_k ? kconv_full : vconv_full(c & 1));
+        mbar_arrive(vconv_full(c & 1));
         mbar_arrive(empty_bar(s));
       }
     }
@@ -1437,19 +1426,55 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     const int g = a.group;
     int c = 0;
-    // Q' operand: row (grp, h) holds head h's channels of group grp, zeros
-    // elsewhere; thread t owns four 16-byte pieces of it
-    auto load_q = [&](int item, uint4 (&v)[4]) {
+    // Query terms: row (grp, h) of each term holds head h's codes of channel
+    // group grp, zeros elsewhere; thread t writes row t >> 2, channels
+    // 32 (t & 3) .. 32 (t & 3) + 31 of both terms
+    int* s_qx = reinterpret_cast<int*>(smem + Ly::kOffQx);
+    auto write_q = [&](int item) {
       const int pair = item / a.splits, b = pair / a.hkv, kvh = pair - b * a.hkv;
+      const int row = t >> 2, cp = t & 3, grp = row >> 3, h = row & 7;
+      uint32_t w1[8], w2[8];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int idx = t * 4 + i;
-        const int half = idx >> 8, rem = idx & 255, row = rem >> 3, ch = rem & 7;
-        const int grp = row >> 3, h = row & 7;
-        v[i] = make_uint4(0, 0, 0, 0);
-        if (h < g && half * 2 + (ch >> 2) == grp)
-          v[i] = bf16x8_to_f16x8(*reinterpret_cast<const uint4*>(a.q + (static_cast<int64_t>(b) * a.hq + kvh * g + h) *
-                                                                        kD + half * 64 + ch * 8));
+      for (int i = 0; i < 8; ++i) w1[i] = w2[i] = 0u;
+      if (cp == grp && h < g) {
+        const uint4* qr = reinterpret_cast<const uint4*>(a.q + (static_cast<int64_t>(b) * a.hq + kvh * g + h) * kD);
+        uint32_t amax = 0u;  // bits of the largest |entry| (order of non-negative floats)
+#pragma unroll 4
+        for (int i = 0; i < 16; ++i) {
+          const uint4 v = qr[i];
+          amax = max(amax, max(max(v.x & 0x7fff7fffu, v.y & 0x7fff7fffu), max(v.z & 0x7fff7fffu, v.w & 0x7fff7fffu)) & 0xffff0000u);
+          amax = max(amax, max(max((v.x << 16) & 0x7fff0000u, (v.y << 16) & 0x7fff0000u),
+                               max((v.z << 16) & 0x7fff0000u, (v.w << 16) & 0x7fff0000u)));
+        }
+        // 2^ax brings the row's largest entry into [128, 256)
+        int ex = 0;
+        if (amax != 0u) frexpf(__uint_as_float(amax), &ex);
+        const int ax = amax != 0u ? 8 - ex : 0;
+        if (cp == 0) s_qx[h] = ax;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const uint32_t wq = reinterpret_cast<const uint32_t*>(qr + 4 * grp)[i];
+          const float y0 = ldexpf(__uint_as_float(wq << 16), ax), y1 = ldexpf(__uint_as_float(wq & 0xffff0000u), ax);
+          const __nv_fp8x2_storage_t c1 = __nv_cvt_float2_to_fp8x2(make_float2(y0, y1), __NV_SATFINITE, __NV_E4M3);
+          const __half2_raw h1 = __nv_cvt_fp8x2_to_halfraw2(c1, __NV_E4M3);
+          const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&h1));
+          const __nv_fp8x2_storage_t c2 =
+              __nv_cvt_float2_to_fp8x2(make_float2(y0 - f1.x, y1 - f1.y), __NV_SATFINITE, __NV_E4M3);
+          w1[i >> 1] |= static_cast<uint32_t>(c1) << (16 * (i & 1));
+          w2[i >> 1] |= static_cast<uint32_t>(c2) << (16 * (i & 1));
+        }
+      } else if (cp == grp && cp == 0) {
+        s_qx[h] = 0;
+      }
+      // 16-byte pieces 2cp, 2cp+1 of the row, 128-byte swizzle
+#pragma unroll
+      for (int term = 0; term < 2; ++term) {
+        uint8_t* rowp = smem + Ly::kOffQ + term * Ly::kQTerm + row * 128;
+        const uint32_t* wv = term ? w2 : w1;
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+          *reinterpret_cast<uint4*>(rowp + (((2 * cp + k) ^ (row & 7)) << 4)) =
+              make_uint4(wv[4 * k], wv[4 * k + 1], wv[4 * k + 2], wv[4 * k + 3]);
       }
     };
     int item = w.first;
@@ -1469,19 +1494,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         it = nit;
         continue;
       }
-      {  // the item's query rows
-        uint4 qv[4];
-        load_q(item, qv);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int idx = t * 4 + i;
-          const int half = idx >> 8, rem = idx & 255, row = rem >> 3, ch = rem & 7;
-          *reinterpret_cast<uint4*>(smem + Ly::kOffQ + half * Ly::kQHalf + row * 128 + ((ch ^ (row & 7)) << 4)) =
-              qv[i];
-        }
-      }
+      write_q(item);  // the item's query terms (GEMM1 of the previous item is complete)
       fence_async_smem();
       mbar_arrive(q_full);
+      named_barrier(1, 128);  // the exponents a_h are written
+      float sl[NH];  // log2(e) / sqrt(d) * 2^-a_h
+#pragma unroll
+      for (int h = 0; h < NH; ++h) sl[h] = h < g ? ldexpf(a.scale_log2, -s_qx[h]) : 0.0f;
 
       bool fail = false;  // this thread saw a wait run out (uniform per warp)
       float m[NH], lsum[NH], oacc[NH], alpha_prev[NH];
@@ -1538,7 +1557,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ready) mbar_arrive(empty_bar(s));  // the stage's meta and K scales are read
 #pragma unroll
         for (int h = 0; h < NH; ++h) {
-          x[h] = (valid_cur && h < g) ? x[h] * a.scale_log2 : -INFINITY;
+          x[h] = (valid_cur && h < g) ? x[h] * sl[h] : -INFINITY;
           r[h] = x[h];
         }
         // chunk max per head over the 128 rows: warp reduce-scatter, then the 4 warps
@@ -1648,8 +1667,9 @@ bool make_map(CUtensorMap* m, const void* base, int64_t rows, int block) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// e4m3 codes: [rows][128] bytes, box = one page of rows x 128 codes, no swizzle
-bool make_map_codes(CUtensorMap* m, const void* base, int64_t rows, int block) {
+// 2-D view of an e4m3 page pool [num_pages*B rows][128 codes]; box = one
+// page; swizzled (the layout the MMA reads) or plain rows
+bool make_map_codes(CUtensorMap* m, const void* base, int64_t rows, int block, bool swizzle) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(rows)};
@@ -1657,8 +1677,8 @@ bool make_map_codes(CUtensorMap* m, const void* base, int64_t rows, int block) {
   const cuuint32_t box[2] = {128, static_cast<cuuint32_t>(block)};
   const cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 TcArgs make_args(const KvView& kv, const AttnArgs& aa) {
@@ -1696,7 +1716,7 @@ cudaError_t launch_fp8(const KvView& kv, AttnArgs& aa, unsigned* err, cudaStream
   CUtensorMap mk, mv;
   const int64_t rows = kv.num_pages * kv.block;
   if (rows <= 0) return cudaErrorInvalidValue;
-  if (!make_map_codes(&mk, kv.k_pages, rows, kv.block) || !make_map_codes(&mv, kv.v_pages, rows, kv.block))
+  if (!make_map_codes(&mk, kv.k_pages, rows, kv.block, true) || !make_map_codes(&mv, kv.v_pages, rows, kv.block, false))
     return cudaErrorInvalidValue;
   const TcArgs a = make_args(kv, aa);
   if (a.items == 0) return cudaSuccess;

@@ -220,11 +220,7 @@ template <int C, int G, bool F32>
 cudaError_t launch_t(const KvView& kv, const SelectArgs& a, unsigned* err, cudaStream_t st) {
   const size_t smem = static_cast<size_t>(kv.max_blocks) * sizeof(float);
   auto kern = score_select_kernel<C, G, F32>;
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-  }
+  if (cudaError_t e = allow_dynamic_smem(kern, smem); e != cudaSuccess) return e;
   dim3 grid(kSelectCluster, kv.hkv, kv.batch);
   return launch_pdl(kern, grid, dim3(kThreads), smem, st, kv, a, err);
 }
@@ -255,10 +251,7 @@ cudaError_t launch_select_only(const KvView& kv, const SelectArgs& a, const floa
               : kv.max_blocks <= 8192 ? select_only_kernel<1024, 8>
                                       : select_only_kernel<1024, kMaxSelectBlocks / 1024>;
   const int threads = kv.max_blocks > 1024 ? 1024 : kThreads;
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-  }
+  if (cudaError_t e = allow_dynamic_smem(kern, smem); e != cudaSuccess) return e;
   return launch_pdl(kern, dim3(pairs), dim3(threads), smem, st, kv, a, scores, err);
 }
 

@@ -1,97 +1,90 @@
 // Per-block key summaries (Quest, "KV 稀疏化" wiki §5): channel-wise min and
-// max of K over each block's valid tokens.  Each lane owns D/32 consecutive
-// channels, so every token row is one coalesced warp load.  HBM-bound: one pass
-// over the K pages of the blocks asked for.
+// max of K over each block's valid tokens.  Each lane owns 16 bytes of
+// consecutive channels of a row, so one warp load reads whole consecutive
+// rows.  HBM-bound: one pass over the K pages of the blocks asked for.
 #include "hs_internal.h"
 
 namespace hs {
 namespace {
 
-template <int C, int KIND>
-struct RowLoad;
+// Each lane loads 16 bytes of a row (V channels), so a warp load covers RPL
+// consecutive rows of the page - one contiguous 512-byte span - and a lane
+// keeps U loads in flight before it uses any.
+template <int KIND>
+struct Elem;
+template <>
+struct Elem<HS_KV_F32> { static constexpr int kBytes = 4; };
+template <>
+struct Elem<HS_KV_BF16> { static constexpr int kBytes = 2; };
+template <>
+struct Elem<HS_KV_FP8E4M3_G32> { static constexpr int kBytes = 1; };
 
-// fp32 K
-template <int C>
-struct RowLoad<C, HS_KV_F32> {
-  static __device__ __forceinline__ void get(const KvView& kv, int64_t row, int d0, float (&x)[C]) {
-    const float* p = static_cast<const float*>(kv.k_pages) + row * kv.head_dim + d0;
-    if constexpr (C == 4) {
-      float4 v = __ldg(reinterpret_cast<const float4*>(p));
-      x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
-    } else {
-      float2 v = __ldg(reinterpret_cast<const float2*>(p));
-      x[0] = v.x; x[1] = v.y;
+// 16 bytes of one row -> min/max of its V channels into mn/mx
+template <int KIND, int V>
+__device__ __forceinline__ void fold(const uint4& raw, float s, float (&mn)[V], float (&mx)[V]) {
+  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+  if constexpr (KIND == HS_KV_F32) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const float x = __uint_as_float(w[c]);
+      mn[c] = fminf(mn[c], x); mx[c] = fmaxf(mx[c], x);
+    }
+  } else if constexpr (KIND == HS_KV_BF16) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const float lo = __uint_as_float(w[c] << 16), hi = __uint_as_float(w[c] & 0xffff0000u);
+      mn[2 * c] = fminf(mn[2 * c], lo); mx[2 * c] = fmaxf(mx[2 * c], lo);
+      mn[2 * c + 1] = fminf(mn[2 * c + 1], hi); mx[2 * c + 1] = fmaxf(mx[2 * c + 1], hi);
+    }
+  } else {
+    // e4m3 K: code value times the token's 32-channel group scale, in fp32
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const float2 x = e4m3x2_to_float2(static_cast<uint16_t>(w[c >> 1] >> (16 * (c & 1))));
+      const float a = x.x * s, b = x.y * s;
+      mn[2 * c] = fminf(mn[2 * c], a); mx[2 * c] = fmaxf(mx[2 * c], a);
+      mn[2 * c + 1] = fminf(mn[2 * c + 1], b); mx[2 * c + 1] = fmaxf(mx[2 * c + 1], b);
     }
   }
-};
-
-// bf16 K
-template <int C>
-struct RowLoad<C, HS_KV_BF16> {
-  static __device__ __forceinline__ void get(const KvView& kv, int64_t row, int d0, float (&x)[C]) {
-    const uint16_t* p = static_cast<const uint16_t*>(kv.k_pages) + row * kv.head_dim + d0;
-    if constexpr (C == 4) {
-      uint2 v = __ldg(reinterpret_cast<const uint2*>(p));
-      x[0] = __uint_as_float(v.x << 16); x[1] = __uint_as_float(v.x & 0xffff0000u);
-      x[2] = __uint_as_float(v.y << 16); x[3] = __uint_as_float(v.y & 0xffff0000u);
-    } else {
-      uint32_t v = __ldg(reinterpret_cast<const uint32_t*>(p));
-      x[0] = __uint_as_float(v << 16); x[1] = __uint_as_float(v & 0xffff0000u);
-    }
-  }
-};
-
-// e4m3 K: code value times the token's 32-channel group scale, in fp32
-template <int C>
-struct RowLoad<C, HS_KV_FP8E4M3_G32> {
-  static __device__ __forceinline__ void get(const KvView& kv, int64_t row, int d0, float (&x)[C]) {
-    const uint8_t* p = static_cast<const uint8_t*>(kv.k_pages) + row * kv.head_dim + d0;
-    const float s = __ldg(kv.k_scales + row * (kv.head_dim / kQuantGroup) + d0 / kQuantGroup);
-    if constexpr (C == 4) {
-      uint32_t v = __ldg(reinterpret_cast<const uint32_t*>(p));
-      float2 a = e4m3x2_to_float2(static_cast<uint16_t>(v & 0xffffu));
-      float2 b = e4m3x2_to_float2(static_cast<uint16_t>(v >> 16));
-      x[0] = a.x * s; x[1] = a.y * s; x[2] = b.x * s; x[3] = b.y * s;
-    } else {
-      uint16_t v = __ldg(reinterpret_cast<const unsigned short*>(p));
-      float2 a = e4m3x2_to_float2(v);
-      x[0] = a.x * s; x[1] = a.y * s;
-    }
-  }
-};
+}
 
 constexpr int kWarps = 8;
-constexpr int kRowsPerRound = 8;  // rows a warp has in flight
 
-// Warps per block: enough that each warp reads about 8 rows (B/8, from 1 to
-// 8); a CTA of 8 warps therefore covers 8 / wpb blocks.  Each warp loads all
-// the rows of a round before using any, so a block costs about one memory
-// latency; the warps' partial boxes are combined in shared memory.
-__host__ __device__ __forceinline__ int warps_per_block(int B) { return B >= 64 ? 8 : (B >= 8 ? B / 8 : 1); }
+// Warps per block: enough that each warp reads about one round of R rows per
+// block (from 1 to 8); a CTA of 8 warps covers 8 / wpb blocks, and the warps'
+// partial boxes are combined in shared memory.
+__host__ __device__ __forceinline__ int warps_per_block(int B, int R) { return B >= 8 * R ? 8 : (B >= R ? B / R : 1); }
 
-template <int C, int KIND>
+// rows in flight per lane: up to 8, no more than a block holds per warp load
+__host__ __forceinline__ int rounds_for(int B, int rpl) {
+  const int r = ceil_div(B, rpl);
+  return r >= 8 ? 8 : (r >= 4 ? 4 : (r >= 2 ? 2 : 1));
+}
+
+template <int D, int KIND, int U>
 __global__ __launch_bounds__(kWarps * 32) void summaries_kernel(KvView kv, int first_block,
                                                                void* smin, void* smax,
                                                                unsigned* err) {
-  constexpr int D = C * 32;
+  constexpr int E = Elem<KIND>::kBytes, V = 16 / E, LPR = D / V, RPL = 32 / LPR, R = RPL * U;
+  static_assert(D % V == 0 && 32 % LPR == 0, "a row is a whole number of 16-byte lanes");
   __shared__ float s_mn[kWarps][D], s_mx[kWarps][D];
   __shared__ int s_ok[kWarps];
   pdl_trigger();
   pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rs = lane / LPR, d0 = (lane % LPR) * V;
   const int b = blockIdx.z, kvh = blockIdx.y;
   const int B = kv.block;
-  const int wpb = warps_per_block(B), per_cta = kWarps / wpb;
-  const int j = first_block + blockIdx.x * per_cta + warp / wpb;
-  const int sub = warp % wpb;
+  const int wpb = warps_per_block(B, R), per_cta = kWarps / wpb;
+  const int bl = warp / wpb, sub = warp % wpb;
+  const int j = first_block + blockIdx.x * per_cta + bl;
   const int L = kv.seq_lens[b];
   const int nb = min(ceil_div(max(L, 0), B), kv.max_blocks);
   const int64_t pair = static_cast<int64_t>(b) * kv.hkv + kvh;
-  const int d0 = lane * C;
-  float mn[C], mx[C];
+  float mn[V], mx[V];
 #pragma unroll
-  for (int c = 0; c < C; ++c) { mn[c] = INFINITY; mx[c] = -INFINITY; }
-  bool ok = j < nb;
+  for (int c = 0; c < V; ++c) { mn[c] = INFINITY; mx[c] = -INFINITY; }
+  bool ok = bl < per_cta && j < nb;
   if (ok) {
     const int page = kv.page_table[pair * kv.max_blocks + j];
     if (page < 0 || page >= kv.num_pages) {
@@ -100,31 +93,43 @@ __global__ __launch_bounds__(kWarps * 32) void summaries_kernel(KvView kv, int f
     } else {
       const int valid = min(B, L - j * B);
       const int64_t row0 = static_cast<int64_t>(page) * B;
-      for (int t0 = sub; t0 < valid; t0 += wpb * kRowsPerRound) {
-        float x[kRowsPerRound][C];
+      const uint8_t* base = static_cast<const uint8_t*>(kv.k_pages) + d0 * E;
+      for (int t0 = sub * RPL; t0 < valid; t0 += wpb * R) {
+        uint4 raw[U];
+        float sc[U];
 #pragma unroll
-        for (int u = 0; u < kRowsPerRound; ++u) {
-          const int t = min(t0 + u * wpb, valid - 1);  // clamp: a repeated valid row changes nothing
-          RowLoad<C, KIND>::get(kv, row0 + t, d0, x[u]);
+        for (int u = 0; u < U; ++u) {
+          // clamp: a repeated valid row changes nothing
+          const int64_t row = row0 + min(t0 + u * wpb * RPL + rs, valid - 1);
+          raw[u] = __ldg(reinterpret_cast<const uint4*>(base + row * (D * E)));
+          if constexpr (KIND == HS_KV_FP8E4M3_G32) sc[u] = __ldg(kv.k_scales + row * (D / kQuantGroup) + d0 / kQuantGroup);
+          else sc[u] = 1.0f;
         }
 #pragma unroll
-        for (int u = 0; u < kRowsPerRound; ++u)
-#pragma unroll
-          for (int c = 0; c < C; ++c) { mn[c] = fminf(mn[c], x[u][c]); mx[c] = fmaxf(mx[c], x[u][c]); }
+        for (int u = 0; u < U; ++u) fold<KIND, V>(raw[u], sc[u], mn, mx);
       }
     }
   }
+  // the RPL row slots of the warp hold the same channels: combine them
 #pragma unroll
-  for (int c = 0; c < C; ++c) { s_mn[warp][d0 + c] = mn[c]; s_mx[warp][d0 + c] = mx[c]; }
+  for (int off = LPR; off < 32; off <<= 1)
+#pragma unroll
+    for (int c = 0; c < V; ++c) {
+      mn[c] = fminf(mn[c], __shfl_xor_sync(0xffffffffu, mn[c], off));
+      mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], off));
+    }
+  if (rs == 0)
+#pragma unroll
+    for (int c = 0; c < V; ++c) { s_mn[warp][d0 + c] = mn[c]; s_mx[warp][d0 + c] = mx[c]; }
   if (lane == 0) s_ok[warp] = ok ? 1 : 0;
   __syncthreads();
   for (int idx = threadIdx.x; idx < per_cta * D; idx += kWarps * 32) {
-    const int bl = idx / D, d = idx - bl * D;
-    const int w0 = bl * wpb;
+    const int cb = idx / D, d = idx - cb * D;
+    const int w0 = cb * wpb;
     if (!s_ok[w0]) continue;
     float lo = s_mn[w0][d], hi = s_mx[w0][d];
     for (int w = 1; w < wpb; ++w) { lo = fminf(lo, s_mn[w0 + w][d]); hi = fmaxf(hi, s_mx[w0 + w][d]); }
-    const int64_t o = (pair * kv.max_blocks + first_block + blockIdx.x * per_cta + bl) * D + d;
+    const int64_t o = (pair * kv.max_blocks + first_block + blockIdx.x * per_cta + cb) * D + d;
     if constexpr (KIND == HS_KV_F32) {
       static_cast<float*>(smin)[o] = lo;
       static_cast<float*>(smax)[o] = hi;
@@ -137,20 +142,35 @@ __global__ __launch_bounds__(kWarps * 32) void summaries_kernel(KvView kv, int f
   }
 }
 
-template <int C>
-cudaError_t launch_c(const KvView& kv, int first_block, int nblocks, void* smin, void* smax,
+template <int D, int KIND, int U>
+cudaError_t launch_u(const KvView& kv, int first_block, int nblocks, void* smin, void* smax,
                      unsigned* err, cudaStream_t st) {
-  const int per_cta = kWarps / warps_per_block(kv.block);
+  constexpr int RPL = 32 / (D * Elem<KIND>::kBytes / 16);
+  const int per_cta = kWarps / warps_per_block(kv.block, RPL * U);
   dim3 grid(ceil_div(nblocks, per_cta), kv.hkv, kv.batch);
-  switch (kv.kv_dtype) {
-    case HS_KV_F32:
-      return launch_pdl(summaries_kernel<C, HS_KV_F32>, grid, dim3(kWarps * 32), 0, st, kv, first_block, smin, smax, err);
-    case HS_KV_BF16:
-      return launch_pdl(summaries_kernel<C, HS_KV_BF16>, grid, dim3(kWarps * 32), 0, st, kv, first_block, smin, smax, err);
-    default:
-      return launch_pdl(summaries_kernel<C, HS_KV_FP8E4M3_G32>, grid, dim3(kWarps * 32), 0, st, kv, first_block, smin, smax, err);
+  return launch_pdl(summaries_kernel<D, KIND, U>, grid, dim3(kWarps * 32), 0, st, kv, first_block, smin, smax, err);
+}
+
+template <int D, int KIND>
+cudaError_t launch_k(const KvView& kv, int first_block, int nblocks, void* smin, void* smax,
+                     unsigned* err, cudaStream_t st) {
+  constexpr int RPL = 32 / (D * Elem<KIND>::kBytes / 16);
+  switch (rounds_for(kv.block, RPL)) {
+    case 8: return launch_u<D, KIND, 8>(kv, first_block, nblocks, smin, smax, err, st);
+    case 4: return launch_u<D, KIND, 4>(kv, first_block, nblocks, smin, smax, err, st);
+    case 2: return launch_u<D, KIND, 2>(kv, first_block, nblocks, smin, smax, err, st);
+    default: return launch_u<D, KIND, 1>(kv, first_block, nblocks, smin, smax, err, st);
   }
-  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_d(const KvView& kv, int first_block, int nblocks, void* smin, void* smax,
+                     unsigned* err, cudaStream_t st) {
+  switch (kv.kv_dtype) {
+    case HS_KV_F32: return launch_k<D, HS_KV_F32>(kv, first_block, nblocks, smin, smax, err, st);
+    case HS_KV_BF16: return launch_k<D, HS_KV_BF16>(kv, first_block, nblocks, smin, smax, err, st);
+    default: return launch_k<D, HS_KV_FP8E4M3_G32>(kv, first_block, nblocks, smin, smax, err, st);
+  }
 }
 
 }  // namespace
@@ -159,8 +179,8 @@ cudaError_t launch_summaries(const KvView& kv, int first_block, void* smin, void
                              unsigned* err, cudaStream_t st) {
   const int nblocks = kv.max_blocks - first_block;
   if (nblocks <= 0 || kv.batch == 0) return cudaSuccess;
-  return kv.head_dim == 128 ? launch_c<4>(kv, first_block, nblocks, smin, smax, err, st)
-                            : launch_c<2>(kv, first_block, nblocks, smin, smax, err, st);
+  return kv.head_dim == 128 ? launch_d<128>(kv, first_block, nblocks, smin, smax, err, st)
+                            : launch_d<64>(kv, first_block, nblocks, smin, smax, err, st);
 }
 
 }  // namespace hs

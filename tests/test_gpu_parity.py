@@ -227,6 +227,40 @@ def test_ties_break_to_lower_index_exactly(D):
             assert dec.sel[b, kvh, :n].tolist() == want
 
 
+@pytest.mark.parametrize("nb,k", [(8193, 37), (12001, 3000), (16384, 8000)])
+def test_selection_past_8192_blocks_matches_oracle(nb, k):
+    """The selection tier for 8193..16384 blocks per request (one 1024-thread
+    CTA per pair, 16 blocks a thread): integer-valued summaries and queries
+    make every score exact in fp32 and tie often, so scores and selection
+    must equal the oracle's bit for bit."""
+    from query_aware_sparse_hs_gb300.decode import SparseDecode
+    from query_aware_sparse_hs_gb300 import hs
+    gen = np.random.default_rng(nb)
+    batch, hkv, g, B, D = 1, 2, 4, 16, 128
+    L = nb * B - 5  # a ragged last block
+    dec = SparseDecode(num_q_heads=hkv * g, num_kv_heads=hkv, head_dim=D, block_size=B, kv_dtype="bf16",
+                       batch=batch, max_blocks=nb, sink_tokens=16, window_tokens=64, k_scored=k)
+    smin = gen.integers(-2, 1, (batch, hkv, nb, D)).astype(np.float32)
+    smax = smin + gen.integers(0, 2, (batch, hkv, nb, D)).astype(np.float32)
+    q = gen.integers(-1, 2, (batch, hkv * g, D)).astype(np.float32)
+    dec.smin.copy_(torch.from_numpy(smin).to(torch.bfloat16))
+    dec.smax.copy_(torch.from_numpy(smax).to(torch.bfloat16))
+    qd = torch.from_numpy(q).to(torch.bfloat16).cuda()
+    lens = torch.full((batch,), L, dtype=torch.int32, device="cuda")
+    table = torch.zeros((batch, hkv, nb), dtype=torch.int32, device="cuda")
+    dummy = torch.zeros((1, B, D), dtype=torch.bfloat16, device="cuda")
+    kv = hs.paged_kv(dummy, dummy, table, lens)
+    dec.select(kv, qd, keep_scores=True)
+    _err_clear()
+    F = O.forced_blocks(L, B, 16, 64)
+    for kvh in range(hkv):
+        _, score = O.bound_scores(q[0, kvh * g:(kvh + 1) * g].astype(np.float64), smin[0, kvh], smax[0, kvh])
+        assert np.array_equal(dec.scores[0, kvh].cpu().numpy(), score.astype(np.float32))
+        want = O.select_blocks(score, F, k)
+        n = int(dec.sel_count[0, kvh])
+        assert dec.sel[0, kvh, :n].tolist() == want
+
+
 def test_empty_and_tiny_requests():
     from _parity import Case
     w = WORKLOADS["ragged_bf16"].scaled(batch=4, ctx_min=40, ctx_max=40, k_scored=2)
