@@ -355,6 +355,13 @@ __device__ __forceinline__ void run_producer(const TcArgs& a, const Work& w, int
 constexpr int kThreadsB = 352;
 constexpr int kProdB = 8, kMma1B = 9, kMma2B = 10;
 
+// Lazy running max of the online softmax: a chunk moves a head's running max
+// m only when one of its logits (log2 units) exceeds m by more than this;
+// otherwise its probabilities 2^(x - m) stay <= 2^kLazyMax (within the range
+// of the bf16 / f16 P parts) and nothing is rescaled.  The result is the same
+// softmax: the offset cancels in the normalisation.
+constexpr float kLazyMax = 8.0f;
+
 // per-warp max (or sum) of each of the NH values a lane holds, over the warp's
 // 32 lanes, by halving exchanges: afterwards lane l holds the result of value
 // l / (32 / NH) (NH <= 32)
@@ -667,23 +674,37 @@ __device__ __forceinline__ void attn_bf16_cta(const CUtensorMap* tm_k_, const CU
             x[h] = (valid && h < g) ? sv[h] * a.scale_log2 : -INFINITY;
             r[h] = x[h];
           }
-          // chunk max per head over the 128 rows: warp reduce-scatter, then the 4 warps
-          float* rb = red + ((cc >> 1) & 1) * 4 * NH;  // alternate buffers: one barrier per chunk
-          const float wmax = warp_reduce_scatter<NH, true>(r);
-          if ((lane % (32 / NH)) == 0) rb[wq * NH + lane / (32 / NH)] = wmax;
-          if (named_barrier_or(bar, 128, fail || !ready)) {
-            fail = true;
-            break;
-          }
-          float alpha[NH], p[NH];
+          // the group's running max moves only when some row exceeds it by
+          // more than kLazyMax (one vote)
+          bool over = false;
 #pragma unroll
-          for (int h = 0; h < NH; ++h) {
-            const float cm = fmaxf(fmaxf(rb[h], rb[NH + h]), fmaxf(rb[2 * NH + h], rb[3 * NH + h]));
-            const float mn = fmaxf(m[h], cm);
-            alpha[h] = (mn == -INFINITY) ? 1.0f : exp2f(m[h] - mn);
-            m[h] = mn;
-            p[h] = x[h] == -INFINITY ? 0.0f : exp2f(x[h] - mn);
-            lsum[h] = fmaf(lsum[h], alpha[h], p[h]);
+          for (int h = 0; h < NH; ++h) over |= x[h] > m[h] + kLazyMax;
+          float alpha[NH], p[NH];
+          if (named_barrier_or(bar, 128, over || fail || !ready)) {
+            // chunk max per head over the 128 rows: warp reduce-scatter, then the 4 warps
+            float* rb = red + ((cc >> 1) & 1) * 4 * NH;  // alternate buffers: a barrier per chunk at least
+            const float wmax = warp_reduce_scatter<NH, true>(r);
+            if ((lane % (32 / NH)) == 0) rb[wq * NH + lane / (32 / NH)] = wmax;
+            if (named_barrier_or(bar, 128, fail || !ready)) {
+              fail = true;
+              break;
+            }
+#pragma unroll
+            for (int h = 0; h < NH; ++h) {
+              const float cm = fmaxf(fmaxf(rb[h], rb[NH + h]), fmaxf(rb[2 * NH + h], rb[3 * NH + h]));
+              const float mn = fmaxf(m[h], cm);
+              alpha[h] = (mn == -INFINITY) ? 1.0f : exp2f(m[h] - mn);
+              m[h] = mn;
+              p[h] = x[h] == -INFINITY ? 0.0f : exp2f(x[h] - mn);
+              lsum[h] = fmaf(lsum[h], alpha[h], p[h]);
+            }
+          } else {
+#pragma unroll
+            for (int h = 0; h < NH; ++h) {
+              alpha[h] = 1.0f;
+              p[h] = x[h] == -INFINITY ? 0.0f : exp2f(x[h] - m[h]);
+              lsum[h] += p[h];
+            }
           }
           // with one P buffer per group, the P.V product of this group's
           // previous chunk reads it: that product must be complete (and its O
@@ -1560,23 +1581,38 @@ __global__ void __launch_bounds__(kThreads, 1)
           x[h] = (valid_cur && h < g) ? x[h] * sl[h] : -INFINITY;
           r[h] = x[h];
         }
-        // chunk max per head over the 128 rows: warp reduce-scatter, then the 4 warps
-        float* rb = red + (cc & 1) * 4 * NH;  // alternate buffers: one barrier per chunk
-        const float wmax = warp_reduce_scatter<NH, true>(r);
-        if ((lane % (32 / NH)) == 0) rb[warp * NH + lane / (32 / NH)] = wmax;
-        if (named_barrier_or(1, 128, fail || !ready)) {
-          fail = true;
-          break;
-        }
-        float alpha[NH], p[NH];
+        // the running max moves only when some row of the chunk exceeds it by
+        // more than kLazyMax (one vote); otherwise P = 2^(x - m) <= 2^kLazyMax
+        // and nothing is rescaled
+        bool over = false;
 #pragma unroll
-        for (int h = 0; h < NH; ++h) {
-          const float cm = fmaxf(fmaxf(rb[h], rb[NH + h]), fmaxf(rb[2 * NH + h], rb[3 * NH + h]));
-          const float mn = fmaxf(m[h], cm);
-          alpha[h] = (mn == -INFINITY) ? 1.0f : exp2f(m[h] - mn);
-          m[h] = mn;
-          p[h] = x[h] == -INFINITY ? 0.0f : exp2f(x[h] - mn);
-          lsum[h] = fmaf(lsum[h], alpha[h], p[h]);
+        for (int h = 0; h < NH; ++h) over |= x[h] > m[h] + kLazyMax;
+        float alpha[NH], p[NH];
+        if (named_barrier_or(1, 128, over || fail || !ready)) {
+          // chunk max per head over the 128 rows: warp reduce-scatter, then the 4 warps
+          float* rb = red + (cc & 1) * 4 * NH;  // alternate buffers: a barrier per chunk at least
+          const float wmax = warp_reduce_scatter<NH, true>(r);
+          if ((lane % (32 / NH)) == 0) rb[warp * NH + lane / (32 / NH)] = wmax;
+          if (named_barrier_or(1, 128, fail || !ready)) {
+            fail = true;
+            break;
+          }
+#pragma unroll
+          for (int h = 0; h < NH; ++h) {
+            const float cm = fmaxf(fmaxf(rb[h], rb[NH + h]), fmaxf(rb[2 * NH + h], rb[3 * NH + h]));
+            const float mn = fmaxf(m[h], cm);
+            alpha[h] = (mn == -INFINITY) ? 1.0f : exp2f(m[h] - mn);
+            m[h] = mn;
+            p[h] = x[h] == -INFINITY ? 0.0f : exp2f(x[h] - mn);
+            lsum[h] = fmaf(lsum[h], alpha[h], p[h]);
+          }
+        } else {
+#pragma unroll
+          for (int h = 0; h < NH; ++h) {
+            alpha[h] = 1.0f;
+            p[h] = x[h] == -INFINITY ? 0.0f : exp2f(x[h] - m[h]);
+            lsum[h] += p[h];
+          }
         }
         // P of chunk c into buffer c & 1 (its last reader, the product of chunk
         // c - 2, completed before this group took its O one chunk ago), as
