@@ -41,12 +41,10 @@ using namespace tc;
 constexpr int kD = 128;
 constexpr int kChunk = 128;
 constexpr int kStages = 3;
-// e4m3 kernel roles: warps 0-3 softmax, 4-7 K code conversion, 8-11 V code
+// e4m3 kernel roles: warps 0-3 and 15-18 the two softmax groups, 4-11 V code
 // conversion, 12 TMA producer, 13 S' = K.Q'^T issuer (and TMEM owner),
 // 14 O' = V^T.P' issuer
-constexpr int kThreads = 480;
-constexpr int kConvWarp0 = 4;
-constexpr int kConvVWarp0 = 8;
+constexpr int kThreads = 608;
 constexpr int kProducerWarp = 12;
 constexpr int kMmaWarp = 13;
 constexpr int kMma2Warp = 14;
@@ -1195,36 +1193,43 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 // power of two 2^a_h that brings its largest entry into [128, 256), is split
 // into two e4m3 terms q1 + q2 whose sum is that row exactly (a bf16 value has
 // 8 significant bits, a term 4; entries below 2^-10 of 2^-a_h, where q2 is
-// subnormal, keep an error under 2^-10 * 2^-a_h).  Both terms accumulate
-// into the same columns:
-//   GEMM1  S'[tok][(grp, h)] = sum_{d in grp} code_k[tok][d] * (q1 + q2)[h][d]   (N = 4 groups x 8 heads)
-//          S[tok][h] = 2^-a_h * sum_grp kscale[tok][grp] * S'[tok][(grp, h)]
+// subnormal, keep an error under 2^-10 * 2^-a_h).  The terms are 64 rows of
+// one B operand, side by side in N:
+//   GEMM1  S'[tok][(term, grp, h)] = sum_{d in grp} code_k[tok][d] * q_term[h][d]
+//          (N = 2 terms x 4 groups x 8 heads, four MMAs of 32 codes)
+//          S[tok][h] = 2^-a_h * sum_grp kscale[tok][grp] * (S'[tok][(1, grp, h)] + S'[tok][(2, grp, h)])
 //   GEMM2  O[d][(hl, h)] = sum_tok v[tok][d] * P_hl[tok][h],  N = 16, f16 operands,
 //          v = code_v * vscale in f16 (scale and product each rounded once:
 //          relative error <= 2^-10), P split into f16 hi + lo.
 // TMA stages the codes (K with the 128-byte swizzle the MMA reads) and the
-// scales, three stages.  Two converter warpgroups, two threads per row, turn
+// scales, three stages.  Two converter warpgroups (two threads per row) turn
 // V codes times their scales into one of two f16 V tiles once GEMM2 of the
-// chunk two back is done with it.  The softmax warpgroup releases a stage
-// once GEMM1 of its chunk is complete and its K scales are read, and
-// publishes P of chunk c before it takes the O of chunk c-1.
+// chunk two back is done with it.  Two softmax groups of 4 warps take the
+// chunks alternately (group g the chunks c with c % 2 == g, with its own S,
+// O and running state, combined at the end of an item); a group releases a
+// stage once GEMM1 of its chunk is complete and its K scales are read, and
+// publishes P of chunk c (four P buffers) before it takes the O of its
+// previous chunk.
 // ============================================================================
 constexpr int kStages8 = 3;
 constexpr int kCodeBytes = kChunk * 128;          // 128 tokens x 128 codes
 constexpr int kScaleBytes = kChunk * 16;          // 128 tokens x 4 scales
 constexpr int kStage8Bytes = 2 * kCodeBytes + 2 * kScaleBytes;
+constexpr int kConv8Warp0 = 4;                    // warps 4-11 convert V; 0-3 and 15-18 are the softmax groups
 struct Layout8 {
   static constexpr int kOffVh = kStages8 * kStage8Bytes;     // two f16 V tiles
   static constexpr int kQTerm = 32 * 128;                    // one e4m3 query term: 32 rows (group x head) x 128 codes
   static constexpr int kOffQ = kOffVh + 2 * kTileBytes;
   static constexpr int kPLbo = 8 * 16 * 2;                   // bytes between 8-token groups of P
   static constexpr int kPBytes = kChunk * 16 * 2;            // 128 tokens x (hi, lo) x 8 heads, f16
+  static constexpr int kPBufs = 4;
   static constexpr int kOffP = kOffQ + 2 * kQTerm;
-  static constexpr int kOffBar = kOffP + 2 * kPBytes;
-  static constexpr int kNumBars = 2 * kStages8 + 13;
+  static constexpr int kOffBar = kOffP + kPBufs * kPBytes;
+  static constexpr int kNumBars = 2 * kStages8 + 15;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-  static constexpr int kOffRed = kOffMisc + 16;
-  static constexpr int kOffMeta = kOffRed + 3 * 4 * 8 * 4;
+  static constexpr int kOffRed = kOffMisc + 16;             // per group: 2 x [4 warps][8] maxima, [4][8] sums
+  static constexpr int kOffX = kOffRed + 2 * 3 * 4 * 8 * 4;  // group 1's o [8][128], m [8], l [8]
+  static constexpr int kOffMeta = kOffX + (8 * 128 + 16) * 4;
   static constexpr int kOffProg = kOffMeta + kStages8 * 8 * 8;  // progress words (as in the bf16 kernel)
   static constexpr int kOffQx = kOffProg + 32;                   // per head: the exponent a_h of the item's query
   static constexpr int kBytes = kOffQx + 32;
@@ -1232,31 +1237,35 @@ struct Layout8 {
   static_assert(kAlloc <= 232448, "shared memory layout too large");
   static_assert(kStage8Bytes % 1024 == 0 && kOffVh % 1024 == 0 && kOffQ % 1024 == 0 && kOffP % 1024 == 0,
                 "swizzled tiles need 1024-byte alignment");
-  static constexpr int kTmemCols = 128;
-  static constexpr int kColO = 64;  // S' uses columns [0, 64), O [64, 96)
+  static constexpr int kTmemCols = 256;
+  static constexpr int kColO = 128;  // S' of group g: columns [64 g, 64 g + 64); O of group g: [128 + 16 g, +16)
 };
 
-// Half a token row of e4m3 codes (channels 64*cp .. 64*cp+63) -> f16 in a
-// 128-byte-swizzled K-major tile (the conversion is exact); with SCALED each
-// code is multiplied by its 32-channel group's scale in f16 (the scale and the
-// product each rounded once).  Two threads per row (r, cp = 0, 1); the
-// 16-byte segments are staggered so that eight consecutive threads touch
-// eight different bank groups on the loads and on the stores.
-template <bool SCALED>
+// Half a token row of e4m3 codes (channels 64 cp .. 64 cp + 63) -> f16 in a
+// 128-byte-swizzled K-major tile, each code multiplied by its 32-channel
+// group's scale in f16 (the scale and the product each rounded once); zeros
+// for a row of no token.  Two threads per row (r, cp = 0, 1); the 16-byte
+// segments are staggered so that eight consecutive threads touch eight
+// different bank groups on the loads and on the stores.
 __device__ __forceinline__ void convert_half_row(const uint8_t* codes_row, const float* scales, uint8_t* tile, int r,
                                                  int cp, bool valid) {
   __half2 sc[2];
-  if constexpr (SCALED) {
+  {
     const float2 s2 = valid ? *reinterpret_cast<const float2*>(scales + 2 * cp) : make_float2(0.0f, 0.0f);
     sc[0] = __float2half2_rn(s2.x);
     sc[1] = __float2half2_rn(s2.y);
   }
+  // all four loads first: the tile stores below could alias them for all the
+  // compiler knows, so it would not move a load above an earlier store
+  uint4 raw[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    raw[i] = valid ? *reinterpret_cast<const uint4*>(codes_row + (4 * cp + ((i + r + 2 * cp) & 3)) * 16)
+                   : make_uint4(0, 0, 0, 0);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int ch = 4 * cp + ((i + r + 2 * cp) & 3);  // 16-code segment of the row
-    uint4 raw = make_uint4(0, 0, 0, 0);
-    if (valid) raw = *reinterpret_cast<const uint4*>(codes_row + ch * 16);
-    const uint32_t words[4] = {raw.x, raw.y, raw.z, raw.w};
+    const uint32_t words[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
     uint32_t w[8];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -1265,11 +1274,8 @@ __device__ __forceinline__ void convert_half_row(const uint8_t* codes_row, const
         const __half2_raw h =
             __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>((words[j] >> (16 * hw)) & 0xffffu), __NV_E4M3);
         uint32_t bits = static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
-        if constexpr (SCALED) {
-          const __half2 v = __hmul2(*reinterpret_cast<const __half2*>(&bits), sc[(ch & 3) >> 1]);
-          bits = *reinterpret_cast<const uint32_t*>(&v);
-        }
-        w[2 * j + hw] = bits;
+        const __half2 v = __hmul2(*reinterpret_cast<const __half2*>(&bits), sc[(ch & 3) >> 1]);
+        w[2 * j + hw] = *reinterpret_cast<const uint32_t*>(&v);
       }
     }
     uint8_t* row = tile + (ch >> 2) * kHalfBytes + r * 128;
@@ -1291,19 +1297,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar0 = sbase + Ly::kOffBar;
   auto full_bar = [&](int s) { return bar0 + 8 * s; };
   auto empty_bar = [&](int s) { return bar0 + 8 * (kStages8 + s); };
-  auto s_full = [&](int b) { return bar0 + 8 * (2 * kStages8 + b); };
-  auto s_free = [&](int b) { return bar0 + 8 * (2 * kStages8 + 2 + b); };
-  auto p_full = [&](int b) { return bar0 + 8 * (2 * kStages8 + 4 + b); };
-  auto o_full = [&](int b) { return bar0 + 8 * (2 * kStages8 + 6 + b); };
-  auto o_free = [&](int b) { return bar0 + 8 * (2 * kStages8 + 8 + b); };
-  const uint32_t q_full = bar0 + 8 * (2 * kStages8 + 10);
-  auto vconv_full = [&](int b) { return bar0 + 8 * (2 * kStages8 + 11 + b); };  // one per V tile
+  auto s_full = [&](int b) { return bar0 + 8 * (2 * kStages8 + b); };      // per group
+  auto s_free = [&](int b) { return bar0 + 8 * (2 * kStages8 + 2 + b); };  // per group
+  auto o_full = [&](int b) { return bar0 + 8 * (2 * kStages8 + 4 + b); };  // per group
+  auto o_free = [&](int b) { return bar0 + 8 * (2 * kStages8 + 6 + b); };  // per group
+  const uint32_t q_full = bar0 + 8 * (2 * kStages8 + 8);
+  auto vconv_full = [&](int b) { return bar0 + 8 * (2 * kStages8 + 9 + b); };  // per V tile
+  auto p_full = [&](int b) { return bar0 + 8 * (2 * kStages8 + 11 + b); };     // per P buffer
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Ly::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Ly::kOffMisc + 4);
   volatile int* s_last = reinterpret_cast<volatile int*>(smem + Ly::kOffMisc + 8);  // last split of an item
-  float* red = reinterpret_cast<float*>(smem + Ly::kOffRed);
   volatile int* prog = reinterpret_cast<volatile int*>(smem + Ly::kOffProg);
-  auto kc_stage = [&](int s) { return smem + s * kStage8Bytes; };
   auto vc_stage = [&](int s) { return smem + s * kStage8Bytes + kCodeBytes; };
   auto ks_stage = [&](int s) { return smem + s * kStage8Bytes + 2 * kCodeBytes; };
   auto vs_stage = [&](int s) { return smem + s * kStage8Bytes + 2 * kCodeBytes + kScaleBytes; };
@@ -1320,20 +1324,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < kStages8; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 384);  // released by both converting warpgroups and the softmax warps
+      mbar_init(empty_bar(s), 384);  // released by the converters and the chunk's softmax group
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(s_full(b), 1);
       mbar_init(s_free(b), 128);
-      mbar_init(p_full(b), 128);
       mbar_init(o_full(b), 1);
       mbar_init(o_free(b), 128);
       mbar_init(vconv_full(b), 256);
     }
+    for (int b = 0; b < Ly::kPBufs; ++b) mbar_init(p_full(b), 128);
     mbar_init(q_full, 128);
     abort_flag[0] = 0;
     abort_flag[2] = 0;
-    for (int i = 0; i < 8; ++i) reinterpret_cast<volatile int*>(smem + Ly::kOffProg)[i] = 0;
+    for (int i = 0; i < 8; ++i) prog[i] = 0;
     fence_barrier_init();
   }
   if (warp == kMmaWarp) {
@@ -1351,7 +1355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     run_producer<kStages8>(a, w, bpc, full_bar(0), empty_bar(0), meta, 2u * B * 128u + 2u * B * 16u, abort_flag, err,
                            prog, [&](int s, int bi, int page) {
                              const int y = page * B;
-                             tma_load_2d(smem_u32(kc_stage(s)) + bi * B * 128, &tm_k, 0, y, full_bar(s));
+                             tma_load_2d(sbase + s * kStage8Bytes + bi * B * 128, &tm_k, 0, y, full_bar(s));
                              tma_load_2d(smem_u32(vc_stage(s)) + bi * B * 128, &tm_v, 0, y, full_bar(s));
                              bulk_load(smem_u32(ks_stage(s)) + bi * B * 16, a.k_scales + static_cast<int64_t>(y) * 4,
                                        B * 16, full_bar(s));
@@ -1361,7 +1365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp || warp == kMma2Warp) {
     if (lane == 0) {
       const bool first = warp == kMmaWarp;
-      constexpr uint32_t idesc1 = idesc_e4m3(128, 32);
+      constexpr uint32_t idesc1 = idesc_e4m3(128, 64);
       constexpr uint32_t idesc2 = idesc_f16(128, 2 * NH, true, true);
       const uint64_t kdesc = smem_desc(sbase, 16, 1024, 2);  // stage 0's K codes
       const uint64_t qdesc = smem_desc(sbase + Ly::kOffQ, 16, 1024, 2);
@@ -1379,23 +1383,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++qi;
         }
         for (int ci = 0; ok && ci < it.nch; ++ci, ++c) {
-          const int bb = c & 1;
+          const int bb = c & 1;  // the chunk's softmax group
           if (first) {
             const int s = c % kStages8;
             ok = mbar_wait(full_bar(s), (c / kStages8) & 1, abort_flag, a.wait_ns) &&
                  (c < 2 || mbar_wait(s_free(bb), ((c >> 1) + 1) & 1, abort_flag, a.wait_ns));
             if (!ok) break;
             tc_fence_after();
-            // two query terms x four K steps of 32 codes, into one accumulator
+            // four K steps of 32 codes; both query terms (64 rows) in each
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              const uint32_t koff = s * kStage8Bytes + (k & 3) * 32;
-              const uint32_t qoff = (k >> 2) * Ly::kQTerm + (k & 3) * 32;
-              mma_e4m3(tmem + bb * 32, kdesc + (koff >> 4), qdesc + (qoff >> 4), idesc1, k > 0 ? 1u : 0u);
+            for (int k = 0; k < 4; ++k) {
+              const uint32_t koff = s * kStage8Bytes + k * 32;
+              mma_e4m3(tmem + bb * 64, kdesc + (koff >> 4), qdesc + ((k * 32) >> 4), idesc1, k > 0 ? 1u : 0u);
             }
             mma_commit(s_full(bb));
+            prog[1] = c + 1;
           } else {
-            ok = mbar_wait(p_full(bb), (c >> 1) & 1, abort_flag, a.wait_ns) &&
+            const int pb = c % Ly::kPBufs;
+            ok = mbar_wait(p_full(pb), (c / Ly::kPBufs) & 1, abort_flag, a.wait_ns) &&
                  mbar_wait(vconv_full(bb), (c >> 1) & 1, abort_flag, a.wait_ns) &&
                  (c < 2 || mbar_wait(o_free(bb), ((c >> 1) + 1) & 1, abort_flag, a.wait_ns));
             if (!ok) break;
@@ -1403,10 +1408,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int k = 0; k < kChunk / 16; ++k) {
               const uint32_t voff = bb * kTileBytes + k * 2048;
-              const uint32_t poff = bb * Ly::kPBytes + k * 2 * Ly::kPLbo;
+              const uint32_t poff = pb * Ly::kPBytes + k * 2 * Ly::kPLbo;
               mma_f16(tmem + Ly::kColO + bb * 16, vdesc + (voff >> 4), pdesc + (poff >> 4), idesc2, k > 0 ? 1u : 0u);
             }
             mma_commit(o_full(bb));
+            prog[2] = c + 1;
           }
         }
         item = next;
@@ -1417,12 +1423,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (first && c > 0) mbar_drain(s_full((c - 1) & 1), ((c - 1) >> 1) & 1);
       if (!first && c > 0) mbar_drain(o_full((c - 1) & 1), ((c - 1) >> 1) & 1);
     }
-  } else if (warp >= kConvWarp0 && warp < kConvVWarp0 + 4) {
+  } else if (warp >= kConv8Warp0 && warp < kConv8Warp0 + 8) {
     // ================= V conversion: e4m3 rows times scales -> f16 V tiles =================
-    // both converter warpgroups, two threads per row (one per 64-channel
-    // half): V of chunk c, scaled, into V tile c & 1 once the P.V product of
-    // chunk c-2 is done with it; then they release their part of the stage
-    const int ct = tid - kConvWarp0 * 32;  // 0..255
+    // threads (r, cp) convert half cp of row r of chunk c into V tile c & 1
+    // once the P.V product of chunk c-2 is done with it; then release their
+    // part of the stage
+    const int ct = tid - kConv8Warp0 * 32;  // 0..255
     const int r = ct >> 1, cp = ct & 1;
     int c = 0;
     bool ok = true;
@@ -1435,35 +1441,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         const int2 md = meta[s * 8 + r / B];
         const bool valid = md.x >= 0 && (r % B) < md.y;
-        convert_half_row<true>(vc_stage(s) + r * 128, reinterpret_cast<const float*>(vs_stage(s) + r * 16),
-                               smem + Ly::kOffVh + (c & 1) * kTileBytes, r, cp, valid);
+        convert_half_row(vc_stage(s) + r * 128, reinterpret_cast<const float*>(vs_stage(s) + r * 16),
+                         smem + Ly::kOffVh + (c & 1) * kTileBytes, r, cp, valid);
         fence_async_smem();
         mbar_arrive(vconv_full(c & 1));
         mbar_arrive(empty_bar(s));
       }
     }
   } else {
-    const int t = tid;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    // ================= softmax / correction: two groups of 4 warps =================
+    const int grp = warp < 4 ? 0 : 1;
+    const int wq = warp & 3;      // TMEM lane quarter
+    const int t = wq * 32 + lane;  // token row of S, channel of O
+    const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+    const int bar = 1 + grp;      // the group's named barrier; 3 = both groups
     const int g = a.group;
+    float* red = reinterpret_cast<float*>(smem + Ly::kOffRed) + grp * 3 * 4 * NH;
+    float* xo = reinterpret_cast<float*>(smem + Ly::kOffX);
+    float* xm = xo + NH * 128;
+    float* xl = xm + NH;
     int c = 0;
-    // Query terms: row (grp, h) of each term holds head h's codes of channel
-    // group grp, zeros elsewhere; thread t writes row t >> 2, channels
-    // 32 (t & 3) .. 32 (t & 3) + 31 of both terms
+    // Query terms (group 0): row (grp, h) of each term holds head h's codes of
+    // channel group grp, zeros elsewhere; thread t writes row t >> 2,
+    // channels 32 (t & 3) .. 32 (t & 3) + 31 of both terms
     int* s_qx = reinterpret_cast<int*>(smem + Ly::kOffQx);
     auto write_q = [&](int item) {
       const int pair = item / a.splits, b = pair / a.hkv, kvh = pair - b * a.hkv;
-      const int row = t >> 2, cp = t & 3, grp = row >> 3, h = row & 7;
+      const int row = t >> 2, cp = t & 3, cg = row >> 3, h = row & 7;
       uint32_t w1[8], w2[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) w1[i] = w2[i] = 0u;
-      if (cp == grp && h < g) {
+      if (cp == cg && h < g) {
         const uint4* qr = reinterpret_cast<const uint4*>(a.q + (static_cast<int64_t>(b) * a.hq + kvh * g + h) * kD);
         uint32_t amax = 0u;  // bits of the largest |entry| (order of non-negative floats)
 #pragma unroll 4
         for (int i = 0; i < 16; ++i) {
           const uint4 v = qr[i];
-          amax = max(amax, max(max(v.x & 0x7fff7fffu, v.y & 0x7fff7fffu), max(v.z & 0x7fff7fffu, v.w & 0x7fff7fffu)) & 0xffff0000u);
+          amax = max(amax, max(max(v.x & 0x7fff7fffu, v.y & 0x7fff7fffu), max(v.z & 0x7fff7fffu, v.w & 0x7fff7fffu)) &
+                               0xffff0000u);
           amax = max(amax, max(max((v.x << 16) & 0x7fff0000u, (v.y << 16) & 0x7fff0000u),
                                max((v.z << 16) & 0x7fff0000u, (v.w << 16) & 0x7fff0000u)));
         }
@@ -1474,8 +1489,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (cp == 0) s_qx[h] = ax;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const uint32_t wq = reinterpret_cast<const uint32_t*>(qr + 4 * grp)[i];
-          const float y0 = ldexpf(__uint_as_float(wq << 16), ax), y1 = ldexpf(__uint_as_float(wq & 0xffff0000u), ax);
+          const uint32_t wq2 = reinterpret_cast<const uint32_t*>(qr + 4 * cg)[i];
+          const float y0 = ldexpf(__uint_as_float(wq2 << 16), ax), y1 = ldexpf(__uint_as_float(wq2 & 0xffff0000u), ax);
           const __nv_fp8x2_storage_t c1 = __nv_cvt_float2_to_fp8x2(make_float2(y0, y1), __NV_SATFINITE, __NV_E4M3);
           const __half2_raw h1 = __nv_cvt_fp8x2_to_halfraw2(c1, __NV_E4M3);
           const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&h1));
@@ -1484,7 +1499,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           w1[i >> 1] |= static_cast<uint32_t>(c1) << (16 * (i & 1));
           w2[i >> 1] |= static_cast<uint32_t>(c2) << (16 * (i & 1));
         }
-      } else if (cp == grp && cp == 0) {
+      } else if (cp == cg && cp == 0) {
         s_qx[h] = 0;
       }
       // 16-byte pieces 2cp, 2cp+1 of the row, 128-byte swizzle
@@ -1501,29 +1516,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     int item = w.first;
     Item it{};
     if (item < a.items) it = item_geom(a, item, bpc, w);
-    // as in the bf16 kernel, a wait that runs out is made uniform across the
-    // warp (warp-wide TMEM loads) and across the 128 threads at each named
-    // barrier (bar.red.or), so they all leave the loops at the same point
+    // a wait that runs out is made uniform across the warp (warp-wide TMEM
+    // loads), across a group at its named barrier and across both groups at
+    // barrier 3 (bar.red.or), so that all leave the loops at the same point
     while (item < a.items) {
       const int next = item + w.stride;
       const Item nit = next < a.items ? item_geom(a, next, bpc, w) : Item{};  // in flight meanwhile
       const int64_t row0 = (static_cast<int64_t>(it.b) * a.hq + it.kvh * g) * a.splits + it.split;
       if (it.nch == 0) {
-        for (int h = 0; h < g; ++h) put_partial(a, row0, h, t, 0.0f, -INFINITY);
-        if (a.splits > 1 && a.counters) merge_if_last(a, it, t, 1, s_last);
+        if (grp == 0) {
+          for (int h = 0; h < g; ++h) put_partial(a, row0, h, t, 0.0f, -INFINITY);
+          if (a.splits > 1 && a.counters) merge_if_last(a, it, t, bar, s_last);
+        }
         item = next;
         it = nit;
         continue;
       }
-      write_q(item);  // the item's query terms (GEMM1 of the previous item is complete)
-      fence_async_smem();
-      mbar_arrive(q_full);
-      named_barrier(1, 128);  // the exponents a_h are written
+      if (grp == 0) {
+        write_q(item);  // the item's query terms (every GEMM1 of the previous item is complete)
+        fence_async_smem();
+        mbar_arrive(q_full);
+        if (t == 0) {
+          prog[6] = item;
+          prog[7] = it.nch;
+        }
+      }
+      named_barrier(3, 256);  // the exponents a_h are written
       float sl[NH];  // log2(e) / sqrt(d) * 2^-a_h
 #pragma unroll
       for (int h = 0; h < NH; ++h) sl[h] = h < g ? ldexpf(a.scale_log2, -s_qx[h]) : 0.0f;
 
-      bool fail = false;  // this thread saw a wait run out (uniform per warp)
+      bool fail = false;  // this thread saw a wait run out (uniform per group)
       float m[NH], lsum[NH], oacc[NH], alpha_prev[NH];
 #pragma unroll
       for (int h = 0; h < NH; ++h) {
@@ -1533,20 +1556,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         alpha_prev[h] = 1.0f;
       }
       auto take_o = [&](int cc) -> bool {
-        const int bb = cc & 1;
-        if (!__all_sync(0xffffffffu, mbar_wait(o_full(bb), (cc >> 1) & 1, abort_flag, a.wait_ns))) return false;
+        if (!__all_sync(0xffffffffu, mbar_wait(o_full(grp), (cc >> 1) & 1, abort_flag, a.wait_ns))) return false;
         tc_fence_after();
         float ov[16];
-        tmem_ld16(tmem + lane_base + Ly::kColO + bb * 16, ov);
+        tmem_ld16(tmem + lane_base + Ly::kColO + grp * 16, ov);
         tc_fence_before();
-        mbar_arrive(o_free(bb));
+        mbar_arrive(o_free(grp));
 #pragma unroll
         for (int h = 0; h < NH; ++h) oacc[h] = fmaf(oacc[h], alpha_prev[h], ov[h] + ov[NH + h]);
         return true;
       };
       const int c0 = c;
-      for (int ci = 0; ci < it.nch; ++ci) {
-        const int cc = c0 + ci, bb = cc & 1, s = cc % kStages8;
+      int last_own = -1;
+      for (int cc = c0 + ((grp - c0) & 1); cc < c0 + it.nch; cc += 2) {
+        const int s = cc % kStages8;
         // row t of the chunk: token t % B of its (t / B)-th block; its K
         // scales come from this chunk's stage
         bool ready = !fail && mbar_wait(full_bar(s), (cc / kStages8) & 1, abort_flag, a.wait_ns);
@@ -1557,43 +1580,43 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float4 sc = *reinterpret_cast<const float4*>(ks_stage(s) + t * 16);
           ks_cur[0] = sc.x; ks_cur[1] = sc.y; ks_cur[2] = sc.z; ks_cur[3] = sc.w;
         }
-        ready = __all_sync(0xffffffffu, ready && mbar_wait(s_full(bb), (cc >> 1) & 1, abort_flag, a.wait_ns));
-        // S = sum over the 4 channel groups of kscale * S', two groups per TMEM load
-        float x[NH], r[NH];
+        ready = __all_sync(0xffffffffu, ready && mbar_wait(s_full(grp), (cc >> 1) & 1, abort_flag, a.wait_ns));
+        // S = sum over the 4 channel groups of kscale * (S' of term 1 + S' of term 2)
+        float x[NH];
 #pragma unroll
         for (int h = 0; h < NH; ++h) x[h] = 0.0f;
         if (ready) {
           tc_fence_after();
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            float sv[16];
-            tmem_ld16(tmem + lane_base + bb * 32 + half * 16, sv);
+          for (int term = 0; term < 2; ++term) {
+            float sv[32];
+            tmem_ld32(tmem + lane_base + grp * 64 + term * 32, sv);
 #pragma unroll
-            for (int h = 0; h < NH; ++h)
-              x[h] = fmaf(ks_cur[2 * half + 1], sv[8 + h], fmaf(ks_cur[2 * half], sv[h], x[h]));
+            for (int cg = 0; cg < 4; ++cg)
+#pragma unroll
+              for (int h = 0; h < NH; ++h) x[h] = fmaf(ks_cur[cg], sv[cg * 8 + h], x[h]);
           }
           tc_fence_before();
-          mbar_arrive(s_free(bb));
+          mbar_arrive(s_free(grp));
+          mbar_arrive(empty_bar(s));  // the stage's K codes, meta and K scales are used
         }
-        if (ready) mbar_arrive(empty_bar(s));  // the stage's meta and K scales are read
 #pragma unroll
-        for (int h = 0; h < NH; ++h) {
-          x[h] = (valid_cur && h < g) ? x[h] * sl[h] : -INFINITY;
-          r[h] = x[h];
-        }
+        for (int h = 0; h < NH; ++h) x[h] = (valid_cur && h < g) ? x[h] * sl[h] : -INFINITY;
         // the running max moves only when some row of the chunk exceeds it by
         // more than kLazyMax (one vote); otherwise P = 2^(x - m) <= 2^kLazyMax
-        // and nothing is rescaled
         bool over = false;
 #pragma unroll
         for (int h = 0; h < NH; ++h) over |= x[h] > m[h] + kLazyMax;
         float alpha[NH], p[NH];
-        if (named_barrier_or(1, 128, over || fail || !ready)) {
+        if (named_barrier_or(bar, 128, over || fail || !ready)) {
           // chunk max per head over the 128 rows: warp reduce-scatter, then the 4 warps
-          float* rb = red + (cc & 1) * 4 * NH;  // alternate buffers: a barrier per chunk at least
+          float r[NH];
+#pragma unroll
+          for (int h = 0; h < NH; ++h) r[h] = x[h];
+          float* rb = red + ((cc >> 1) & 1) * 4 * NH;  // alternate buffers: a barrier per chunk at least
           const float wmax = warp_reduce_scatter<NH, true>(r);
-          if ((lane % (32 / NH)) == 0) rb[warp * NH + lane / (32 / NH)] = wmax;
-          if (named_barrier_or(1, 128, fail || !ready)) {
+          if ((lane % (32 / NH)) == 0) rb[wq * NH + lane / (32 / NH)] = wmax;
+          if (named_barrier_or(bar, 128, fail || !ready)) {
             fail = true;
             break;
           }
@@ -1614,8 +1637,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             lsum[h] += p[h];
           }
         }
-        // P of chunk c into buffer c & 1 (its last reader, the product of chunk
-        // c - 2, completed before this group took its O one chunk ago), as
+        // P of chunk cc into buffer cc % 4 (its last reader, the product of
+        // chunk cc - 4, completed before this group took that chunk's O), as
         // f16 high part + remainder
         {
           uint32_t hi2[NH / 2], lo2[NH / 2];
@@ -1627,16 +1650,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             hi2[h / 2] = *reinterpret_cast<const uint32_t*>(&hi);
             lo2[h / 2] = *reinterpret_cast<const uint32_t*>(&lo);
           }
-          uint8_t* prow = smem + Ly::kOffP + bb * Ly::kPBytes + (t >> 3) * Ly::kPLbo + (t & 7) * 16;
+          uint8_t* prow = smem + Ly::kOffP + (cc % Ly::kPBufs) * Ly::kPBytes + (t >> 3) * Ly::kPLbo + (t & 7) * 16;
           *reinterpret_cast<uint4*>(prow) = make_uint4(hi2[0], hi2[1], hi2[2], hi2[3]);
           *reinterpret_cast<uint4*>(prow + 128) = make_uint4(lo2[0], lo2[1], lo2[2], lo2[3]);
         }
         fence_async_smem();
-        mbar_arrive(p_full(bb));
-        // O of the previous chunk, once P of this one is out
-        if (ci > 0 && !take_o(cc - 1)) fail = true;
+        mbar_arrive(p_full(cc % Ly::kPBufs));
+        if (t == 0) prog[3 + grp] = cc + 1;
+        // O of this group's previous chunk, once P of this one is out
+        if (last_own >= 0 && !take_o(last_own)) fail = true;
 #pragma unroll
         for (int h = 0; h < NH; ++h) alpha_prev[h] = alpha[h];
+        last_own = cc;
       }
       c = c0 + it.nch;
       // the normaliser reduction overlaps the last P.V product
@@ -1646,17 +1671,47 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int h = 0; h < NH; ++h) r[h] = lsum[h];
         const float wsum = warp_reduce_scatter<NH, false>(r);
-        if ((lane % (32 / NH)) == 0) rs[warp * NH + lane / (32 / NH)] = wsum;
+        if ((lane % (32 / NH)) == 0) rs[wq * NH + lane / (32 / NH)] = wsum;
       }
-      if (!fail && !take_o(c - 1)) fail = true;
-      if (named_barrier_or(1, 128, fail)) break;  // all 128 threads leave the item loop together
-      for (int h = 0; h < g && h < NH; ++h) {
-        const float lt = rs[h] + rs[NH + h] + rs[2 * NH + h] + rs[3 * NH + h];
-        put_partial(a, row0, h, t, lt > 0.0f ? oacc[h] / lt : 0.0f,
-                    lt > 0.0f ? (m[h] + log2f(lt)) * kLn2 : -INFINITY);
+      if (!fail && last_own >= 0 && !take_o(last_own)) fail = true;
+      fail = named_barrier_or(bar, 128, fail);
+      // combine the two groups' states: group 1 publishes, group 0 merges and writes
+      if (grp == 1 && !fail) {
+#pragma unroll
+        for (int h = 0; h < NH; ++h) xo[h * 128 + t] = oacc[h];
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {  // compile-time indices keep m[] in registers
+          if (t == h) {
+            xm[h] = m[h];
+            xl[h] = rs[h] + rs[NH + h] + rs[2 * NH + h] + rs[3 * NH + h];
+          }
+        }
       }
-      if (a.splits > 1 && a.counters) merge_if_last(a, it, t, 1, s_last);
-      named_barrier(1, 128);
+      if (named_barrier_or(3, 256, fail)) break;  // both groups leave together after a wait ran out
+      if (grp == 0) {
+        float* fac = red;  // [NH][4], the chunk-max buffers are free after the chunk loop
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {  // compile-time indices keep m[] in registers
+          if (t == h && h < g) {
+            const float l0 = rs[h] + rs[NH + h] + rs[2 * NH + h] + rs[3 * NH + h];
+            const float m1 = xm[h], l1 = xl[h];
+            const float mx = fmaxf(m[h], m1);
+            const float e0 = m[h] == -INFINITY ? 0.0f : exp2f(m[h] - mx);
+            const float e1 = m1 == -INFINITY ? 0.0f : exp2f(m1 - mx);
+            const float lt = l0 * e0 + l1 * e1;
+            const float inv = lt > 0.0f ? 1.0f / lt : 0.0f;
+            fac[4 * h] = e0 * inv;
+            fac[4 * h + 1] = e1 * inv;
+            fac[4 * h + 3] = lt > 0.0f ? (mx + log2f(lt)) * kLn2 : -INFINITY;
+          }
+        }
+        named_barrier(bar, 128);
+#pragma unroll
+        for (int h = 0; h < NH; ++h)
+          if (h < g) put_partial(a, row0, h, t, fmaf(oacc[h], fac[4 * h], xo[h * 128 + t] * fac[4 * h + 1]), fac[4 * h + 3]);
+        if (a.splits > 1 && a.counters) merge_if_last(a, it, t, bar, s_last);
+      }
+      named_barrier(3, 256);  // the exchange buffer and s_qx are free again
       item = next;
       it = nit;
     }
