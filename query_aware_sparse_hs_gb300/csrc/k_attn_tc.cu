@@ -360,6 +360,15 @@ constexpr int kProdB = 8, kMma1B = 9, kMma2B = 10;
 // softmax: the offset cancels in the normalisation.
 constexpr float kLazyMax = 8.0f;
 
+// float -> unsigned key with the same order (-0 below +0; no NaN here), and back
+__device__ __forceinline__ uint32_t float_order_key(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float order_key_float(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
 // per-warp max (or sum) of each of the NH values a lane holds, over the warp's
 // 32 lanes, by halving exchanges: afterwards lane l holds the result of value
 // l / (32 / NH) (NH <= 32)
@@ -1231,12 +1240,13 @@ struct Layout8 {
   static constexpr int kOffX = kOffRed + 2 * 3 * 4 * 8 * 4;  // group 1's o [8][128], m [8], l [8]
   static constexpr int kOffMeta = kOffX + (8 * 128 + 16) * 4;
   static constexpr int kOffProg = kOffMeta + kStages8 * 8 * 8;  // progress words (as in the bf16 kernel)
-  static constexpr int kOffQx = kOffProg + 32;                   // per head: the exponent a_h of the item's query
-  static constexpr int kBytes = kOffQx + 32;
+  static constexpr int kOffQx = (kOffProg + 32 + 15) / 16 * 16;  // per head: the exponent a_h of the item's query,
+  static constexpr int kBytes = kOffQx + 64;                     // then the softmax scale times 2^-a_h (16-byte loads)
   static constexpr int kAlloc = (kBytes + 1024 + 127) / 128 * 128;  // layout + base alignment
   static_assert(kAlloc <= 232448, "shared memory layout too large");
   static_assert(kStage8Bytes % 1024 == 0 && kOffVh % 1024 == 0 && kOffQ % 1024 == 0 && kOffP % 1024 == 0,
                 "swizzled tiles need 1024-byte alignment");
+  static_assert(kOffQx % 16 == 0 && kOffMeta % 8 == 0 && kOffBar % 8 == 0, "vector accesses need alignment");
   static constexpr int kTmemCols = 256;
   static constexpr int kColO = 128;  // S' of group g: columns [64 g, 64 g + 64); O of group g: [128 + 16 g, +16)
 };
@@ -1486,7 +1496,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         int ex = 0;
         if (amax != 0u) frexpf(__uint_as_float(amax), &ex);
         const int ax = amax != 0u ? 8 - ex : 0;
-        if (cp == 0) s_qx[h] = ax;
+        if (cp == 0) {
+          s_qx[h] = ax;
+          reinterpret_cast<float*>(s_qx + 8)[h] = ldexpf(a.scale_log2, -ax);
+        }
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const uint32_t wq2 = reinterpret_cast<const uint32_t*>(qr + 4 * cg)[i];
@@ -1501,6 +1514,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else if (cp == cg && cp == 0) {
         s_qx[h] = 0;
+        reinterpret_cast<float*>(s_qx + 8)[h] = 0.0f;
       }
       // 16-byte pieces 2cp, 2cp+1 of the row, 128-byte swizzle
 #pragma unroll
@@ -1542,9 +1556,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       named_barrier(3, 256);  // the exponents a_h are written
-      float sl[NH];  // log2(e) / sqrt(d) * 2^-a_h
-#pragma unroll
-      for (int h = 0; h < NH; ++h) sl[h] = h < g ? ldexpf(a.scale_log2, -s_qx[h]) : 0.0f;
+      // per head log2(e) / sqrt(d) * 2^-a_h, read from shared memory at each chunk
+      const float* s_sl = reinterpret_cast<const float*>(s_qx + 8);
 
       bool fail = false;  // this thread saw a wait run out (uniform per group)
       float m[NH], lsum[NH], oacc[NH], alpha_prev[NH];
@@ -1600,8 +1613,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(s_free(grp));
           mbar_arrive(empty_bar(s));  // the stage's K codes, meta and K scales are used
         }
+        {
+          const float4 sa = *reinterpret_cast<const float4*>(s_sl), sb = *reinterpret_cast<const float4*>(s_sl + 4);
+          const float sl[NH] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
 #pragma unroll
-        for (int h = 0; h < NH; ++h) x[h] = (valid_cur && h < g) ? x[h] * sl[h] : -INFINITY;
+          for (int h = 0; h < NH; ++h) x[h] = (valid_cur && h < g) ? x[h] * sl[h] : -INFINITY;
+        }
         // the running max moves only when some row of the chunk exceeds it by
         // more than kLazyMax (one vote); otherwise P = 2^(x - m) <= 2^kLazyMax
         bool over = false;
@@ -1609,13 +1626,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int h = 0; h < NH; ++h) over |= x[h] > m[h] + kLazyMax;
         float alpha[NH], p[NH];
         if (named_barrier_or(bar, 128, over || fail || !ready)) {
-          // chunk max per head over the 128 rows: warp reduce-scatter, then the 4 warps
-          float r[NH];
-#pragma unroll
-          for (int h = 0; h < NH; ++h) r[h] = x[h];
+          // chunk max per head over the 128 rows: one warp reduction per head
+          // (on order-preserving integer keys), then the 4 warps
           float* rb = red + ((cc >> 1) & 1) * 4 * NH;  // alternate buffers: a barrier per chunk at least
-          const float wmax = warp_reduce_scatter<NH, true>(r);
-          if ((lane % (32 / NH)) == 0) rb[wq * NH + lane / (32 / NH)] = wmax;
+#pragma unroll
+          for (int h = 0; h < NH; ++h) {
+            const uint32_t k = __reduce_max_sync(0xffffffffu, float_order_key(x[h]));
+            if (lane == h) rb[wq * NH + h] = order_key_float(k);
+          }
           if (named_barrier_or(bar, 128, fail || !ready)) {
             fail = true;
             break;
