@@ -106,13 +106,29 @@ void split_geometry(const hs_attn_shape* s, int batch, int capacity, const hs_at
   if (bps <= 0) {
     const int64_t pairs = static_cast<int64_t>(batch) * s->num_kv_heads;
     const int64_t n_sm = sms > 0 ? sms : 148;
-    // few (request, kv head) pairs: one wave of CTAs, each pair split evenly;
-    // many pairs: about two items per SM
-    int64_t want = pairs <= 0 ? 1 : (pairs <= n_sm ? n_sm / pairs : (2 * n_sm + pairs - 1) / pairs);
-    if (want < 1) want = 1;
+    const int per_chunk = s->block_size < 128 ? 128 / s->block_size : 1;
+    const int64_t chunks = (cap + per_chunk - 1) / per_chunk;  // 128-token chunks of a full selection
+    // Splits per (request, kv head): the persistent CTAs take items in
+    // rounds, so the busiest CTA runs ceil(items / SMs) items; each costs its
+    // chunks plus about three chunks' worth of start-up, query load, state
+    // combination and output (measured: halving the items of the 16-token
+    // and e4m3 workloads pays more than the balance it costs).  The split
+    // count with the least such time wins, the fewest splits on a tie.
+    int64_t want = 1;
+    if (pairs > 0) {
+      int64_t best = -1;
+      const int64_t top = chunks < 32 ? chunks : 32;
+      for (int64_t sp = 1; sp <= top; ++sp) {
+        const int64_t rounds = (pairs * sp + n_sm - 1) / n_sm;
+        const int64_t cost = rounds * ((chunks + sp - 1) / sp + 3);
+        if (best < 0 || cost < best) {
+          best = cost;
+          want = sp;
+        }
+      }
+    }
     if (want > cap) want = cap;
     bps = static_cast<int>((cap + want - 1) / want);
-    const int per_chunk = s->block_size < 128 ? 128 / s->block_size : 1;
     bps = ((bps + per_chunk - 1) / per_chunk) * per_chunk;
   }
   *bps_out = bps;
