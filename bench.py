@@ -429,7 +429,8 @@ def workload_config(w, layers: int | None = None) -> dict:
         c.update(hot_slots_per_stream=w.hot_slots, decode_steps=w.decode_steps,
                  l2="inputs larger than L2: hot buffer 2.1 GB and summaries 268 MB read every step")
     elif layers is not None:
-        c.update(layer_copies=layers, l2=f"inputs larger than L2: {layers} distinct layer copies rotate step to step")
+        c.update(layer_copies=layers, l2=f"inputs larger than L2: {layers} distinct layer copies rotate step to step",
+                 early_summaries=layers > 1)
     return c
 
 
@@ -506,10 +507,12 @@ def measure_resident(args, w, dev, world) -> dict:
             del k, v
             k, v = kc, vc
         kv = hs.paged_kv(k, v, table, lens, ks, vs)
+        # layers are stepped in turn, so with two or more the kernel before a
+        # layer's step never writes that layer's summaries
         dec = SparseDecode(num_q_heads=w.num_q_heads, num_kv_heads=w.num_kv_heads, head_dim=D,
                            block_size=B, kv_dtype=w.kv_dtype, batch=w.batch, max_blocks=w.max_blocks,
                            sink_tokens=w.sink_tokens, window_tokens=w.window_tokens,
-                           k_scored=w.k_scored, device=dev)
+                           k_scored=w.k_scored, early_summaries=layers > 1, device=dev)
         dec.build_summaries(kv)
         decs.append(dec)
         kvs.append(kv)

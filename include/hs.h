@@ -165,7 +165,14 @@ typedef struct hs_select_params {
  * of its roles, lets the copies and products it already issued finish, frees
  * its tensor memory and returns; the call's outputs are then undefined and
  * hs_get_device_error reports HS_ERR_TIMEOUT.  A limit far below a launch's
- * duration makes a wait run out on purpose (the bounded-wait test does). */
+ * duration makes a wait run out on purpose (the bounded-wait test does).
+ * flags: HS_ATTN_EARLY_SUMMARIES = the caller guarantees that smin/smax are
+ * not written by the kernel launched just before on the same stream (they
+ * were complete before it started), so the single-launch step
+ * (hs_decode_step, hs_score_select_attend when fused) may start copying its
+ * summary tiles while that kernel finishes, instead of after it.  Every other
+ * input is still read only after it.  0 = no such guarantee. */
+#define HS_ATTN_EARLY_SUMMARIES 1u
 typedef struct hs_attn_params {
   float scale;
   int32_t out_is_fp32;
@@ -174,6 +181,7 @@ typedef struct hs_attn_params {
   int32_t max_ctas;
   uint32_t* split_counters;
   uint32_t wait_limit_ns;
+  uint32_t flags;
 } hs_attn_params;
 
 /* HiSparse hot buffer ([KVS] §7).  One stream per (request, kv head) owns

@@ -239,6 +239,7 @@ hs_status prepare_attn(const hs_attn_shape* shape, const hs_paged_kv* kv, const 
   if (params->split_counters && !aligned(params->split_counters, 4)) return HS_ERR_INVALID_ARG;
   a.counters = params->split_counters;
   a.wait_ns = static_cast<uint64_t>(params->wait_limit_ns);
+  a.early_summaries = (params->flags & HS_ATTN_EARLY_SUMMARIES) != 0;
   a.q = q;
   a.sel = sel;
   a.sel_count = sel_count;

@@ -35,6 +35,7 @@ struct AttnArgs {
   int32_t sms;  // multiprocessors of the current device (persistent grid size)
   int32_t merged = 0;  // set by a launcher that already wrote out / lse (fused merge)
   uint64_t wait_ns = 0;  // bound of the tensor-core kernels' waits (0: the default 2 s)
+  bool early_summaries = false;  // HS_ATTN_EARLY_SUMMARIES
 };
 
 struct HotView {

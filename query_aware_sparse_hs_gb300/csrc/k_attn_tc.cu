@@ -919,6 +919,7 @@ struct FuseArgs {
   const uint8_t* v_pages;
   int tiles;    // 128-block tiles per (request, kv head)
   int cluster;  // CTAs per (request, kv head)
+  int early;    // the summary tile may be copied before the previous kernel completes
   // append (nullable new_k): the newest token of every pair, [batch][Hkv][128]
   // bf16, is written at position seq_lens - 1 of the cache and widens its
   // block's summary before the block is scored
@@ -1003,11 +1004,10 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<uint32_t*>(smem + Layout<NH>::kOffMisc);
   cluster_arrive_relaxed();  // completes once every CTA of the cluster runs
-  pdl_wait();  // q, the summaries, seq_lens, the page table and the history of this step are complete
-
   // the summary tile is requested before the request's length is known (rows
-  // past its blocks are never used)
-  if (warp == kProdB && lane == 0 && rank < f.tiles) {
+  // past its blocks are never used); with f.early before the previous kernel
+  // has completed (the caller guarantees that it does not write them)
+  auto load_tile = [&]() {
     mbar_arrive_tx(tile_full, bound::kTileBytes);
     const int y = pair * a.max_blocks + rank * bound::kTile;
     const uint32_t st = sbase + kFTile;
@@ -1015,7 +1015,10 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     tma_load_2d(st + bound::kHalf, &tm_smax, 64, y, tile_full);
     tma_load_2d(st + 2 * bound::kHalf, &tm_smin, 0, y, tile_full);
     tma_load_2d(st + 3 * bound::kHalf, &tm_smin, 64, y, tile_full);
-  }
+  };
+  if (f.early && warp == kProdB && lane == 0 && rank < f.tiles) load_tile();
+  pdl_wait();  // q, the summaries, seq_lens, the page table and the history of this step are complete
+  if (!f.early && warp == kProdB && lane == 0 && rank < f.tiles) load_tile();
   const int L = max(a.seq_lens[b], 0);
   int nb = (L + a.block - 1) / a.block;
   if (nb > a.max_blocks) {
@@ -1886,6 +1889,7 @@ cudaError_t launch_score_select_attn(const KvView& kv, const void* smin, const v
     return cudaErrorInvalidValue;
   const TcArgs a = make_args(kv, aa);
   FuseArgs f;
+  f.early = aa.early_summaries ? 1 : 0;
   f.scores = sa.scores;
   f.k_pages = static_cast<const uint8_t*>(kv.k_pages);
   f.v_pages = static_cast<const uint8_t*>(kv.v_pages);

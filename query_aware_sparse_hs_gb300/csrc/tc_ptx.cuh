@@ -89,12 +89,11 @@ struct WaitClock {
 // ran out: the barrier's shared-memory address (bits 0-17), the parity (bit
 // 18), the warp (bits 19-23), bit 31 set.  Returns false when it gave up.  A
 // phase that is complete already costs one non-blocking test.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
-                                          uint64_t limit_ns = kWaitLimitNs) {
-  if (mbar_test(bar, parity)) return true;
-  if (*abort) return false;
-  const uint32_t hint = limit_ns < 1000000ull ? static_cast<uint32_t>(limit_ns) : 1000000u;
-  if (mbar_try(bar, parity, hint)) return true;
+// The rest of a wait whose first suspension ended without the phase: kept
+// out of line, so that the many inlined waits of a kernel carry only their
+// common path (a kernel's code is fetched into each SM's instruction cache).
+static __device__ __noinline__ bool mbar_wait_rest(uint32_t bar, uint32_t parity, volatile int* abort, uint64_t limit_ns,
+                                            uint32_t hint) {
   const WaitClock clk;
   for (;;) {
     if (*abort) return false;
@@ -108,17 +107,29 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
+                                          uint64_t limit_ns = kWaitLimitNs) {
+  if (mbar_test(bar, parity)) return true;
+  if (*abort) return false;
+  const uint32_t hint = limit_ns < 1000000ull ? static_cast<uint32_t>(limit_ns) : 1000000u;
+  if (mbar_try(bar, parity, hint)) return true;
+  return mbar_wait_rest(bar, parity, abort, limit_ns, hint);
+}
+
 // Waits for the completion of copies or MMAs this CTA has already issued, so
 // that it never exits (or frees its TMEM) with them in flight.  Unlike
 // mbar_wait it ignores the abort flag: work in flight lands whether or not the
 // CTA is stopping.  Bounded by `limit_ns`; returns false if that passed.
-__device__ __forceinline__ bool mbar_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns = kDrainLimitNs) {
-  if (mbar_try(bar, parity)) return true;
+static __device__ __noinline__ bool mbar_drain_rest(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
   const WaitClock clk;
   for (;;) {
     if (mbar_try(bar, parity)) return true;
     if (clk.past(limit_ns)) return false;
   }
+}
+__device__ __forceinline__ bool mbar_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns = kDrainLimitNs) {
+  if (mbar_try(bar, parity)) return true;
+  return mbar_drain_rest(bar, parity, limit_ns);
 }
 
 // ---- async proxy fences ----

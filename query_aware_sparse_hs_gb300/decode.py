@@ -23,12 +23,15 @@ class SparseDecode:
     inline_merge: give the tensor-core attention split counters so that it
     merges its splits itself.  fuse_step: a step without a hot buffer or a
     reused selection runs selection and attention as one library call
-    (hs_score_select_attend, a single launch where the geometry allows)."""
+    (hs_score_select_attend, a single launch where the geometry allows).
+    early_summaries: this layer's summaries are never written by the kernel
+    launched just before its step (e.g. layers stepped in turn), so the
+    single-launch step may start reading them early (HS_ATTN_EARLY_SUMMARIES)."""
 
     def __init__(self, *, num_q_heads, num_kv_heads, head_dim, block_size, kv_dtype, batch,
                  max_blocks, sink_tokens, window_tokens, k_scored, capacity=None, scale=None,
                  out_is_fp32=False, algo="auto", blocks_per_split=0, score_smoothing=0.0,
-                 inline_merge=True, fuse_step=True, device="cuda"):
+                 inline_merge=True, fuse_step=True, early_summaries=False, device="cuda"):
         self.kv_dtype = kv_dtype
         self.shape = hs.attn_shape(num_q_heads, num_kv_heads, head_dim, block_size, kv_dtype)
         self.batch, self.max_blocks = int(batch), int(max_blocks)
@@ -46,7 +49,8 @@ class SparseDecode:
         self.split_counters = (torch.zeros(batch * num_kv_heads, dtype=torch.int32, device=dev)
                                if inline_merge else None)
         self.attn_params = hs.attn_params(scale if scale is not None else 1.0 / math.sqrt(head_dim),
-                                          out_is_fp32, blocks_per_split, algo, split_counters=self.split_counters)
+                                          out_is_fp32, blocks_per_split, algo, split_counters=self.split_counters,
+                                          early_summaries=early_summaries)
         sdt = _SUMMARY_DTYPE[kv_dtype]
         self.smin = torch.empty((batch, num_kv_heads, max_blocks, head_dim), dtype=sdt, device=dev)
         self.smax = torch.empty_like(self.smin)

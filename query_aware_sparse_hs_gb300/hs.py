@@ -21,6 +21,7 @@ HS_OK, HS_ERR_INVALID_ARG, HS_ERR_UNSUPPORTED, HS_ERR_CUDA = 0, 1, 2, 3
 HS_ERR_OUT_OF_RANGE, HS_ERR_CAPACITY, HS_ERR_TIMEOUT, HS_ERR_WORKSPACE = 4, 5, 6, 7
 HS_ERR_SCRATCH_LIMIT = 8
 HS_NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
+HS_ATTN_EARLY_SUMMARIES = 1
 HS_EBIT_PAGE_RANGE, HS_EBIT_CAPACITY, HS_EBIT_TIMEOUT, HS_EBIT_BLOCK_RANGE = 0x1, 0x2, 0x4, 0x8
 KV_DTYPES = {"f32": 0, "bf16": 1, "fp8": 2}
 ALGO = {"auto": 0, "simt": 1, "tcgen05": 2}
@@ -51,7 +52,7 @@ class SelectParams(ctypes.Structure):
 class AttnParams(ctypes.Structure):
     _fields_ = [("scale", c_float), ("out_is_fp32", c_int32), ("blocks_per_split", c_int32),
                 ("algo", c_int32), ("max_ctas", c_int32), ("split_counters", c_void_p),
-                ("wait_limit_ns", c_uint32)]
+                ("wait_limit_ns", c_uint32), ("flags", c_uint32)]
 
 
 class HotBuffer(ctypes.Structure):
@@ -183,11 +184,13 @@ def select_params(sink_tokens, window_tokens, k_scored, capacity, history_weight
 
 
 def attn_params(scale, out_is_fp32=False, blocks_per_split=0, algo="auto", max_ctas=0,
-                split_counters=None, wait_limit_ns=0) -> AttnParams:
-    """wait_limit_ns: bound of the tensor-core kernels' waits (0 = 2 s)."""
+                split_counters=None, wait_limit_ns=0, early_summaries=False) -> AttnParams:
+    """wait_limit_ns: bound of the tensor-core kernels' waits (0 = 2 s).
+    early_summaries: HS_ATTN_EARLY_SUMMARIES (smin/smax are not written by the
+    kernel launched just before the call on its stream)."""
     p = AttnParams(float(scale), 1 if out_is_fp32 else 0, int(blocks_per_split),
                    ALGO[algo] if isinstance(algo, str) else int(algo), int(max_ctas), _ptr(split_counters),
-                   int(wait_limit_ns))
+                   int(wait_limit_ns), HS_ATTN_EARLY_SUMMARIES if early_summaries else 0)
     p._keep = split_counters
     return p
 

@@ -109,3 +109,42 @@ def test_decode_step_checks_its_arguments():
                           d.attn_params, d.out, d.lse, d.workspace)
     assert e.value.status == hs.HS_ERR_INVALID_ARG
     assert hs.hs_get_device_error() == (hs.HS_OK, 0)
+
+
+def test_decode_step_with_early_summaries_equals_without():
+    """HS_ATTN_EARLY_SUMMARIES (the step may copy its summary tiles before the
+    previous kernel completes; the caller guarantees that kernel does not write
+    them): two layers stepped in turn, so the kernel before each step is the
+    other layer's.  Every output equals, bit for bit, that of the same steps
+    without the flag."""
+    from _parity import Case
+    from query_aware_sparse_hs_gb300 import hs
+    w = CASES["llama_mid_block"][0]
+    results = []
+    for early in (False, True):
+        runs = []
+        for layer in range(2):
+            x = make_inputs(w)
+            if layer:
+                x["q"] = x["q"].flip(-1).contiguous()
+            c = Case(w, x, tail_nan=False)
+            d = c.decoder(out_is_fp32=True, early_summaries=early)
+            d.build_summaries(hs.paged_kv(c.k_pages, c.v_pages, c.page_table, (c.seq_lens - 1).clamp(min=0)))
+            runs.append((c, d))
+        new_k, new_v = _new_token(w, 99)
+        dk, dv = new_k.cuda(), new_v.cuda()
+        for _ in range(3):  # layer 0, layer 1, layer 0, ...
+            for c, d in runs:
+                d.decode_step(c.kv, c.q, dk, dv)
+        torch.cuda.synchronize()
+        assert hs.hs_get_device_error() == (hs.HS_OK, 0)
+        results.append([(d.out.clone(), d.lse.clone(), d.sel.clone(), d.sel_count.clone(), d.smin.clone(), d.smax.clone())
+                        for _, d in runs])
+    lens = runs[0][0].lens
+    for a, b in zip(*results):
+        for x, y in zip(a[:4], b[:4]):
+            assert torch.equal(x, y)
+        for bi, L in enumerate(lens):  # summary rows of blocks past a request's end are never written
+            nb = O.num_blocks(L, w.block_size)
+            for x, y in zip(a[4:], b[4:]):
+                assert torch.equal(x[bi, :, :nb], y[bi, :, :nb]), bi
