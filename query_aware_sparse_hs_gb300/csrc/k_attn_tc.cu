@@ -797,12 +797,18 @@ __device__ __forceinline__ void attn_bf16_cta(const CUtensorMap* tm_k_, const CU
           // two products and a scale
           float* fac = red;  // [NH][4]
 #pragma unroll
-          for (int h = 0; h < NH; ++h) {  // compile-time indices keep m[] in registers
-            if (t == h && h < g) {
+          {
+            // thread h < g takes head h: its running max picked out of m[] with
+            // compile-time indices (m[] stays in registers), the arithmetic once
+            const int h = t;
+            float m0 = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < NH; ++i) m0 = (i == h) ? m[i] : m0;
+            if (h < g && h < NH) {
               const float l0 = rs[h] + rs[NH + h] + rs[2 * NH + h] + rs[3 * NH + h];
               const float m1 = xm[h], l1 = xl[h];
-              const float mx = fmaxf(m[h], m1);
-              const float e0 = m[h] == -INFINITY ? 0.0f : exp2f(m[h] - mx);
+              const float mx = fmaxf(m0, m1);
+              const float e0 = m0 == -INFINITY ? 0.0f : exp2f(m0 - mx);
               const float e1 = m1 == -INFINITY ? 0.0f : exp2f(m1 - mx);
               const float lt = l0 * e0 + l1 * e1;
               const float inv = lt > 0.0f ? 1.0f / lt : 0.0f;
@@ -1712,12 +1718,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (grp == 0) {
         float* fac = red;  // [NH][4], the chunk-max buffers are free after the chunk loop
 #pragma unroll
-        for (int h = 0; h < NH; ++h) {  // compile-time indices keep m[] in registers
-          if (t == h && h < g) {
+        {
+          // thread h < g takes head h: its running max picked out of m[] with
+          // compile-time indices (m[] stays in registers), the arithmetic once
+          const int h = t;
+          float m0 = -INFINITY;
+#pragma unroll
+          for (int i = 0; i < NH; ++i) m0 = (i == h) ? m[i] : m0;
+          if (h < g && h < NH) {
             const float l0 = rs[h] + rs[NH + h] + rs[2 * NH + h] + rs[3 * NH + h];
             const float m1 = xm[h], l1 = xl[h];
-            const float mx = fmaxf(m[h], m1);
-            const float e0 = m[h] == -INFINITY ? 0.0f : exp2f(m[h] - mx);
+            const float mx = fmaxf(m0, m1);
+            const float e0 = m0 == -INFINITY ? 0.0f : exp2f(m0 - mx);
             const float e1 = m1 == -INFINITY ? 0.0f : exp2f(m1 - mx);
             const float lt = l0 * e0 + l1 * e1;
             const float inv = lt > 0.0f ? 1.0f / lt : 0.0f;
