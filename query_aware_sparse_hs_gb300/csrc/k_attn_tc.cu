@@ -43,11 +43,14 @@ constexpr int kChunk = 128;
 constexpr int kStages = 3;
 // e4m3 kernel roles: warps 0-3 and 15-18 the two softmax groups, 4-11 V code
 // conversion, 12 TMA producer, 13 S' = K.Q'^T issuer (and TMEM owner),
-// 14 O' = V^T.P' issuer
-constexpr int kThreads = 608;
+// 14 and 19 the O' = V^T.P' issuers of the even and the odd chunks (an MMA
+// takes its issuing thread ~70 cycles, so a chunk's eight P.V products are
+// issued while the other group's are)
+constexpr int kThreads = 640;
 constexpr int kProducerWarp = 12;
 constexpr int kMmaWarp = 13;
 constexpr int kMma2Warp = 14;
+constexpr int kMma3Warp = 19;
 constexpr int kHalfBytes = kChunk * 128;   // 128 rows x 64 bf16
 constexpr int kTileBytes = 2 * kHalfBytes;  // one K or V chunk
 constexpr int kStageBytes = 2 * kTileBytes;
@@ -203,7 +206,7 @@ __device__ __forceinline__ void merge_if_last(const TcArgs& a, const Item& it, i
     const int64_t orow = static_cast<int64_t>(it.b) * a.hq + static_cast<int64_t>(it.kvh) * g + h;
     const int64_t r0 = orow * S;
     float M = -INFINITY;
-#pragma unroll 4
+#pragma unroll 1
     for (int s = 0; s < S; ++s) M = fmaxf(M, __ldcg(a.ws_lse + r0 + s));
     float acc[8];
 #pragma unroll
@@ -211,7 +214,7 @@ __device__ __forceinline__ void merge_if_last(const TcArgs& a, const Item& it, i
     float lse = -INFINITY;
     if (M != -INFINITY) {
       float tot = 0.0f;
-#pragma unroll 2
+#pragma unroll 1
       for (int s = 0; s < S; ++s) {
         const float w = expf(__ldcg(a.ws_lse + r0 + s) - M);
         const float4* src = reinterpret_cast<const float4*>(a.ws_o + (r0 + s) * kD + c0);
@@ -1381,9 +1384,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                              bulk_load(smem_u32(vs_stage(s)) + bi * B * 16, a.v_scales + static_cast<int64_t>(y) * 4,
                                        B * 16, full_bar(s));
                            });
-  } else if (warp == kMmaWarp || warp == kMma2Warp) {
+  } else if (warp == kMmaWarp || warp == kMma2Warp || warp == kMma3Warp) {
     if (lane == 0) {
       const bool first = warp == kMmaWarp;
+      const int par = warp == kMma2Warp ? 0 : 1;  // a P.V issuer's chunk parity
       constexpr uint32_t idesc1 = idesc_e4m3(128, 64);
       constexpr uint32_t idesc2 = idesc_f16(128, 2 * NH, true, true);
       const uint64_t kdesc = smem_desc(sbase, 16, 1024, 2);  // stage 0's K codes
@@ -1418,6 +1422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(s_full(bb));
             prog[1] = c + 1;
           } else {
+            if (bb != par) continue;
             const int pb = c % Ly::kPBufs;
             ok = mbar_wait(p_full(pb), (c / Ly::kPBufs) & 1, abort_flag, a.wait_ns) &&
                  mbar_wait(vconv_full(bb), (c >> 1) & 1, abort_flag, a.wait_ns) &&
@@ -1440,7 +1445,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // every product this thread issued is complete before TMEM is released
       // (a commit arrives once all of the thread's earlier MMAs are done)
       if (first && c > 0) mbar_drain(s_full((c - 1) & 1), ((c - 1) >> 1) & 1);
-      if (!first && c > 0) mbar_drain(o_full((c - 1) & 1), ((c - 1) >> 1) & 1);
+      if (!first) {
+        const int last = ((c - 1) & 1) == par ? c - 1 : c - 2;  // this issuer's last chunk
+        if (last >= 0) mbar_drain(o_full(par), (last >> 1) & 1);
+      }
     }
   } else if (warp >= kConv8Warp0 && warp < kConv8Warp0 + 8) {
     // ================= V conversion: e4m3 rows times scales -> f16 V tiles =================
