@@ -1224,29 +1224,30 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 //          relative error <= 2^-10), P split into f16 hi + lo.
 // TMA stages the codes (K with the 128-byte swizzle the MMA reads) and the
 // scales, three stages.  Two converter warpgroups (two threads per row) turn
-// V codes times their scales into one of two f16 V tiles once GEMM2 of the
-// chunk two back is done with it.  Two softmax groups of 4 warps take the
+// V codes times their scales into one of three f16 V tiles once GEMM2 of the
+// chunk three back is done with it (each tile has its own free barrier).  Two softmax groups of 4 warps take the
 // chunks alternately (group g the chunks c with c % 2 == g, with its own S,
 // O and running state, combined at the end of an item); a group releases a
 // stage once GEMM1 of its chunk is complete and its K scales are read, and
-// publishes P of chunk c (four P buffers) before it takes the O of its
-// previous chunk.
+// takes the O of its previous chunk before it writes P of chunk c into its
+// own P buffer.
 // ============================================================================
 constexpr int kStages8 = 3;
+constexpr int kVTiles = 3;                        // f16 V tiles: chunk c converts into tile c % 3
 constexpr int kCodeBytes = kChunk * 128;          // 128 tokens x 128 codes
 constexpr int kScaleBytes = kChunk * 16;          // 128 tokens x 4 scales
 constexpr int kStage8Bytes = 2 * kCodeBytes + 2 * kScaleBytes;
 constexpr int kConv8Warp0 = 4;                    // warps 4-11 convert V; 0-3 and 15-18 are the softmax groups
 struct Layout8 {
-  static constexpr int kOffVh = kStages8 * kStage8Bytes;     // two f16 V tiles
+  static constexpr int kOffVh = kStages8 * kStage8Bytes;     // kVTiles f16 V tiles
   static constexpr int kQTerm = 32 * 128;                    // one e4m3 query term: 32 rows (group x head) x 128 codes
-  static constexpr int kOffQ = kOffVh + 2 * kTileBytes;
+  static constexpr int kOffQ = kOffVh + kVTiles * kTileBytes;
   static constexpr int kPLbo = 8 * 16 * 2;                   // bytes between 8-token groups of P
   static constexpr int kPBytes = kChunk * 16 * 2;            // 128 tokens x (hi, lo) x 8 heads, f16
-  static constexpr int kPBufs = 4;
+  static constexpr int kPBufs = 2;                           // one per softmax group
   static constexpr int kOffP = kOffQ + 2 * kQTerm;
   static constexpr int kOffBar = kOffP + kPBufs * kPBytes;
-  static constexpr int kNumBars = 2 * kStages8 + 15;
+  static constexpr int kNumBars = 2 * kStages8 + 9 + 2 * kVTiles + kPBufs;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kOffRed = kOffMisc + 16;             // per group: 2 x [4 warps][8] maxima, [4][8] sums
   static constexpr int kOffX = kOffRed + 2 * 3 * 4 * 8 * 4;  // group 1's o [8][128], m [8], l [8]
@@ -1324,8 +1325,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto o_full = [&](int b) { return bar0 + 8 * (2 * kStages8 + 4 + b); };  // per group
   auto o_free = [&](int b) { return bar0 + 8 * (2 * kStages8 + 6 + b); };  // per group
   const uint32_t q_full = bar0 + 8 * (2 * kStages8 + 8);
-  auto vconv_full = [&](int b) { return bar0 + 8 * (2 * kStages8 + 9 + b); };  // per V tile
-  auto p_full = [&](int b) { return bar0 + 8 * (2 * kStages8 + 11 + b); };     // per P buffer
+  auto vconv_full = [&](int b) { return bar0 + 8 * (2 * kStages8 + 9 + b); };            // per V tile
+  auto vfree = [&](int b) { return bar0 + 8 * (2 * kStages8 + 9 + kVTiles + b); };        // per V tile
+  auto p_full = [&](int b) { return bar0 + 8 * (2 * kStages8 + 9 + 2 * kVTiles + b); };  // per P buffer
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Ly::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Ly::kOffMisc + 4);
   volatile int* s_last = reinterpret_cast<volatile int*>(smem + Ly::kOffMisc + 8);  // last split of an item
@@ -1353,7 +1355,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(s_free(b), 128);
       mbar_init(o_full(b), 1);
       mbar_init(o_free(b), 128);
+    }
+    for (int b = 0; b < kVTiles; ++b) {
       mbar_init(vconv_full(b), 256);
+      mbar_init(vfree(b), 1);
     }
     for (int b = 0; b < Ly::kPBufs; ++b) mbar_init(p_full(b), 128);
     mbar_init(q_full, 128);
@@ -1423,19 +1428,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             prog[1] = c + 1;
           } else {
             if (bb != par) continue;
-            const int pb = c % Ly::kPBufs;
+            const int pb = c % Ly::kPBufs, vt = c % kVTiles;
             ok = mbar_wait(p_full(pb), (c / Ly::kPBufs) & 1, abort_flag, a.wait_ns) &&
-                 mbar_wait(vconv_full(bb), (c >> 1) & 1, abort_flag, a.wait_ns) &&
+                 mbar_wait(vconv_full(vt), (c / kVTiles) & 1, abort_flag, a.wait_ns) &&
                  (c < 2 || mbar_wait(o_free(bb), ((c >> 1) + 1) & 1, abort_flag, a.wait_ns));
             if (!ok) break;
             tc_fence_after();
 #pragma unroll
             for (int k = 0; k < kChunk / 16; ++k) {
-              const uint32_t voff = bb * kTileBytes + k * 2048;
+              const uint32_t voff = vt * kTileBytes + k * 2048;
               const uint32_t poff = pb * Ly::kPBytes + k * 2 * Ly::kPLbo;
               mma_f16(tmem + Ly::kColO + bb * 16, vdesc + (voff >> 4), pdesc + (poff >> 4), idesc2, k > 0 ? 1u : 0u);
             }
             mma_commit(o_full(bb));
+            mma_commit(vfree(vt));
             prog[2] = c + 1;
           }
         }
@@ -1452,8 +1458,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= kConv8Warp0 && warp < kConv8Warp0 + 8) {
     // ================= V conversion: e4m3 rows times scales -> f16 V tiles =================
-    // threads (r, cp) convert half cp of row r of chunk c into V tile c & 1
-    // once the P.V product of chunk c-2 is done with it; then release their
+    // threads (r, cp) convert half cp of row r of chunk c into V tile c % 3
+    // once the P.V product of chunk c-3 is done with it; then release their
     // part of the stage
     const int ct = tid - kConv8Warp0 * 32;  // 0..255
     const int r = ct >> 1, cp = ct & 1;
@@ -1463,15 +1469,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Item it = item_geom(a, item, bpc, w);
       for (int ci = 0; ci < it.nch; ++ci, ++c) {
         const int s = c % kStages8;
+        const int vt = c % kVTiles;  // its last reader, the P.V product of chunk c - 3
         ok = mbar_wait(full_bar(s), (c / kStages8) & 1, abort_flag, a.wait_ns) &&
-             (c < 2 || mbar_wait(o_full(c & 1), ((c - 2) >> 1) & 1, abort_flag, a.wait_ns));
+             (c < kVTiles || mbar_wait(vfree(vt), ((c / kVTiles) - 1) & 1, abort_flag, a.wait_ns));
         if (!ok) break;
         const int2 md = meta[s * 8 + r / B];
         const bool valid = md.x >= 0 && (r % B) < md.y;
         convert_half_row(vc_stage(s) + r * 128, reinterpret_cast<const float*>(vs_stage(s) + r * 16),
-                         smem + Ly::kOffVh + (c & 1) * kTileBytes, r, cp, valid);
+                         smem + Ly::kOffVh + vt * kTileBytes, r, cp, valid);
         fence_async_smem();
-        mbar_arrive(vconv_full(c & 1));
+        mbar_arrive(vconv_full(vt));
         mbar_arrive(empty_bar(s));
       }
     }
@@ -1672,9 +1679,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             lsum[h] += p[h];
           }
         }
-        // P of chunk cc into buffer cc % 4 (its last reader, the product of
-        // chunk cc - 4, completed before this group took that chunk's O), as
-        // f16 high part + remainder
+        // O of this group's previous chunk: its P.V product is then complete,
+        // and with it the last read of this group's P buffer
+        if (last_own >= 0 && !take_o(last_own)) fail = true;
+        // P of chunk cc into the group's buffer, as f16 high part + remainder
         {
           uint32_t hi2[NH / 2], lo2[NH / 2];
 #pragma unroll
@@ -1692,8 +1700,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_async_smem();
         mbar_arrive(p_full(cc % Ly::kPBufs));
         if (t == 0) prog[3 + grp] = cc + 1;
-        // O of this group's previous chunk, once P of this one is out
-        if (last_own >= 0 && !take_o(last_own)) fail = true;
 #pragma unroll
         for (int h = 0; h < NH; ++h) alpha_prev[h] = alpha[h];
         last_own = cc;
