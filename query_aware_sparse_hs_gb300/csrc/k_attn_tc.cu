@@ -352,9 +352,10 @@ __device__ __forceinline__ void run_producer(const TcArgs& a, const Work& w, int
 
 // bf16 kernel: warps 0-7 are two softmax groups of 4 warps (group g takes the
 // chunks c with c % 2 == g, so two chunks are in the softmax stage at once),
-// warp 8 is the TMA producer, warps 9 and 10 the MMA issuers.
-constexpr int kThreadsB = 352;
-constexpr int kProdB = 8, kMma1B = 9, kMma2B = 10;
+// warp 8 is the TMA producer, warp 9 issues S = K.Q^T, warps 10 and 11 issue
+// O = V^T.P of the even and the odd chunks.
+constexpr int kThreadsB = 384;
+constexpr int kProdB = 8, kMma1B = 9, kMma2B = 10, kMma3B = 11;
 
 // Lazy running max of the online softmax: a chunk moves a head's running max
 // m only when one of its logits (log2 units) exceeds m by more than this;
@@ -511,12 +512,14 @@ __device__ __forceinline__ void attn_bf16_cta(const CUtensorMap* tm_k_, const CU
                             tma_load_2d(v_half(s, 0) + row_off, &tm_v, 0, y, full_bar(s));
                             tma_load_2d(v_half(s, 1) + row_off, &tm_v, 64, y, full_bar(s));
                           });
-  } else if (warp == kMma1B || warp == kMma2B) {
-    // ================= MMA issuers: one thread for S = K.Q^T, one for O = V^T.P =================
-    // (issuing a GEMM's 8 tcgen05.mma takes a few hundred ns, so the two GEMMs
-    // of a chunk are issued from two threads instead of one after the other)
+  } else if (warp == kMma1B || warp == kMma2B || warp == kMma3B) {
+    // ================= MMA issuers: one thread for S = K.Q^T, two for O = V^T.P =================
+    // (an MMA takes its issuing thread ~70 cycles, a GEMM's eight a few hundred
+    // ns, so S and O are issued from different threads, and the O products of
+    // the two softmax groups' chunks from one thread each)
     if (lane == 0) {
       const bool first = warp == kMma1B;
+      const int par = warp == kMma2B ? 0 : 1;  // an O issuer's chunk parity
       constexpr uint32_t idesc1 = idesc_bf16(128, 16, false, false);
       constexpr uint32_t idesc2 = idesc_bf16(128, 2 * NH, true, true);
       constexpr uint32_t kPLbo = 8 * 2 * NH * 2;  // bytes between 8-token groups of P
@@ -551,6 +554,7 @@ __device__ __forceinline__ void attn_bf16_cta(const CUtensorMap* tm_k_, const CU
             mma_commit(s_full(bb));
             prog[1] = c + 1;
           } else {
+            if (bb != par) continue;
             ok = mbar_wait(p_full(c % Ly::kPBufs), (c / Ly::kPBufs) & 1, abort_flag, a.wait_ns) &&
                  (c < 2 || mbar_wait(o_free(bb), ((c >> 1) + 1) & 1, abort_flag, a.wait_ns));
             if (!ok) break;
@@ -573,9 +577,12 @@ __device__ __forceinline__ void attn_bf16_cta(const CUtensorMap* tm_k_, const CU
       // every product this thread issued is complete before TMEM is released
       // (a commit arrives once all of the thread's earlier MMAs are done)
       if (first && c > 0) mbar_drain(s_full((c - 1) & 1), ((c - 1) >> 1) & 1);
-      if (!first && c > 0) mbar_drain(empty_bar((c - 1) % kStages), ((c - 1) / kStages) & 1);
+      if (!first) {
+        const int last = ((c - 1) & 1) == par ? c - 1 : c - 2;  // this issuer's last chunk
+        if (last >= 0) mbar_drain(empty_bar(last % kStages), (last / kStages) & 1);
+      }
     }
-  } else {
+  } else if (warp < 8) {
     // ================= softmax / correction: two groups of 4 warps =================
     const int grp = warp >> 2;       // group: owns the chunks with c % 2 == grp, S/P/O buffer grp
     const int wq = warp & 3;         // TMEM lane quarter
@@ -799,7 +806,6 @@ __device__ __forceinline__ void attn_bf16_cta(const CUtensorMap* tm_k_, const CU
           // chunk-max buffers (free after the chunk loop); then per channel
           // two products and a scale
           float* fac = red;  // [NH][4]
-#pragma unroll
           {
             // thread h < g takes head h: its running max picked out of m[] with
             // compile-time indices (m[] stays in registers), the arithmetic once
@@ -1731,7 +1737,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (named_barrier_or(3, 256, fail)) break;  // both groups leave together after a wait ran out
       if (grp == 0) {
         float* fac = red;  // [NH][4], the chunk-max buffers are free after the chunk loop
-#pragma unroll
         {
           // thread h < g takes head h: its running max picked out of m[] with
           // compile-time indices (m[] stays in registers), the arithmetic once
