@@ -299,7 +299,7 @@ hs_status hs_build_block_summaries(const hs_attn_shape* shape, const hs_paged_kv
   Device d;
   if ((st = current_device(&d)) != HS_OK) return st;
   const KvView v = make_view(shape, kv);
-  return from_cuda(launch_summaries(v, first_block, smin, smax, d.err,
+  return from_cuda(launch_summaries(v, first_block, smin, smax, d.err, d.sms,
                                     reinterpret_cast<cudaStream_t>(stream)));
 }
 

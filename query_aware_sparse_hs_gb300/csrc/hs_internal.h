@@ -57,7 +57,7 @@ struct HotView {
 cudaError_t launch_append(const KvView& kv, const void* new_k, const void* new_v, void* smin, void* smax,
                           unsigned* err, cudaStream_t st);
 cudaError_t launch_summaries(const KvView& kv, int first_block, void* smin, void* smax,
-                             unsigned* err, cudaStream_t st);
+                             unsigned* err, int sms, cudaStream_t st);
 cudaError_t launch_score_select(const KvView& kv, const SelectArgs& a, unsigned* err,
                                 cudaStream_t st);
 bool score_tc_supported(const KvView& kv);

@@ -361,3 +361,41 @@ def test_fp8_attention_over_every_code():
             qg = x["q"][b, kvh * g:(kvh + 1) * g].float().numpy().astype(np.float64)
             ref, _ = O.sparse_attention(qg, K, V, sel[b, kvh, :cnt[b, kvh]].tolist(), B, 1 / math.sqrt(D))
             assert np.abs(out[b, kvh * g:(kvh + 1) * g] - ref).max() <= 2e-3, (b, kvh)
+
+
+def test_fp8_summaries_every_code_small_and_large_scales():
+    """e4m3 summaries over every non-NaN code with group scales from 1e-6 to
+    4000 (products from subnormal to about 1.8e6): the builder's fp32
+    dequantisation and outward bf16 rounding must equal the oracle's boxes bit
+    for bit."""
+    from query_aware_sparse_hs_gb300 import hs
+    from query_aware_sparse_hs_gb300.decode import SparseDecode
+    w = WORKLOADS["fp8_g32"].scaled(batch=2, ctx_min=3000, ctx_max=4133, k_scored=20)
+    x = make_inputs(w)
+    B, D, hkv = w.block_size, w.head_dim, w.num_kv_heads
+    P = x["k_pages"].shape[0]
+    gen = torch.Generator().manual_seed(23)
+    allowed = torch.tensor([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=torch.uint8)
+    codes = allowed[torch.randint(len(allowed), (P, B, D), generator=gen)]
+    # log-uniform scales over 1e-6 .. 4000, so both sides of 256 occur in every block
+    scales = torch.exp(torch.rand((P, B, D // 32), generator=gen) * (math.log(4000.0) - math.log(1e-6)) +
+                       math.log(1e-6)).float()
+    dev = torch.device("cuda")
+    kv = hs.paged_kv(codes.to(dev), codes.to(dev), x["page_table"].to(dev), x["seq_lens"].to(dev),
+                     scales.to(dev), scales.to(dev))
+    dec = SparseDecode(num_q_heads=w.num_q_heads, num_kv_heads=hkv, head_dim=D, block_size=B, kv_dtype="fp8",
+                       batch=w.batch, max_blocks=w.max_blocks, sink_tokens=w.sink_tokens,
+                       window_tokens=w.window_tokens, k_scored=w.k_scored)
+    dec.build_summaries(kv)
+    _err_clear()
+    smin, smax = dec.smin.float().cpu().numpy(), dec.smax.float().cpu().numpy()
+    table = x["page_table"].numpy()
+    for b in range(w.batch):
+        L = int(x["seq_lens"][b])
+        nb = O.num_blocks(L, B)
+        for kvh in range(hkv):
+            row = table[b, kvh]
+            K = O.kv_values("fp8", O.gather_rows(codes.numpy(), row, L, B), O.gather_rows(scales.numpy(), row, L, B))
+            lo, hi = O.stored_summaries(*O.block_summaries(K, B), "fp8")
+            assert np.array_equal(smin[b, kvh, :nb], lo.astype(np.float32)), (b, kvh)
+            assert np.array_equal(smax[b, kvh, :nb], hi.astype(np.float32)), (b, kvh)
