@@ -724,7 +724,8 @@ def measure_resident(args, w, dev, world) -> dict:
     st_, bits, where = hs.hs_get_device_error_detail()
     assert st_ == hs.HS_OK, (st_, bits, where)
     # a layer that reuses a selection runs append + attention (+ merge)
-    reuse_launches = step_launches(w, d0, allow_fused=False) - select_launches(w)
+    reuse_launches = (1 if fused_step(w, d0) else
+                      step_launches(w, d0, allow_fused=False) - select_launches(w))
     launches_per_step = step_launches(w, d0) / args.select_every + reuse_launches * (1 - 1 / args.select_every)
     rec = {
         "value": value, "unit": UNIT, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,

@@ -358,6 +358,23 @@ HS_API hs_status hs_decode_step(const hs_attn_shape* shape, const hs_paged_kv* k
                                 float* scores_opt, const hs_attn_params* attn_params, void* out,
                                 float* lse_opt, void* workspace, size_t ws_bytes, hs_stream_t stream);
 
+/* One decode step of a layer that reuses another layer's selection ([SPD]
+ * §3.1: the mask chosen at a shallow layer serves the deeper ones):
+ * hs_append_token(shape, kv, new_k,
+ * new_v, smin, smax) followed by hs_sparse_paged_decode_attn(shape, kv, q,
+ * sel, sel_count, capacity, attn_params, ...), with the same argument rules,
+ * outputs and error bits; sel / sel_count are read only.  Where
+ * hs_score_select_attend_fused holds for (shape, batch, max_blocks, capacity,
+ * attn_params) it is one launch: the single-launch step without its scoring
+ * and selection phases (the append, then the attention of each split over
+ * the given selection, merged in the cluster); otherwise the append kernel and
+ * the attention run in turn.  The K/V pages and smin/smax are written. */
+HS_API hs_status hs_decode_step_reuse(const hs_attn_shape* shape, const hs_paged_kv* kv, const void* q,
+                                      const void* new_k, const void* new_v, void* smin, void* smax,
+                                      const int32_t* sel, const int32_t* sel_count, int32_t capacity,
+                                      const hs_attn_params* attn_params, void* out, float* lse_opt,
+                                      void* workspace, size_t ws_bytes, hs_stream_t stream);
+
 /* HiSparse swap-in, [KVS] §7: for every (b, kvh), make each selected block
  * resident in the stream's hot slots.  Hits set last_used = step.  Misses are
  * taken in ascending block order; each goes to the lowest free slot, else to

@@ -456,6 +456,43 @@ hs_status hs_decode_step(const hs_attn_shape* shape, const hs_paged_kv* kv, cons
                        out, lse_opt, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
+hs_status hs_decode_step_reuse(const hs_attn_shape* shape, const hs_paged_kv* kv, const void* q, const void* new_k,
+                               const void* new_v, void* smin, void* smax, const int32_t* sel,
+                               const int32_t* sel_count, int32_t capacity, const hs_attn_params* attn_params,
+                               void* out, float* lse_opt, void* workspace, size_t ws_bytes, hs_stream_t stream) {
+  using namespace hs;
+  hs_status st = check_shape(shape);
+  if (st != HS_OK) return st;
+  if ((st = check_kv(shape, kv, true)) != HS_OK) return st;
+  if (!new_k || !new_v || !aligned(new_k, 16) || !aligned(new_v, 16)) return HS_ERR_INVALID_ARG;
+  if (!smin || !smax || !aligned(smin, 16) || !aligned(smax, 16)) return HS_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(kv->batch) * shape->num_kv_heads > INT32_MAX) return HS_ERR_UNSUPPORTED;
+  Device d;
+  AttnArgs a;
+  bool use_tc = false;
+  st = prepare_attn(shape, kv, q, sel, sel_count, capacity, attn_params, out, lse_opt, workspace, ws_bytes, &d, &a,
+                    &use_tc);
+  if (st != HS_OK) return st;
+  const KvView v = make_view(shape, kv);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (use_tc && a.sms == d.sms && score_select_attn_supported(v, a, d.sms)) {
+    SelectArgs sa{};
+    sa.q = q;
+    sa.smin = smin;
+    sa.smax = smax;
+    sa.sel = const_cast<int32_t*>(sel);  // read only: the reused selection
+    sa.sel_count = const_cast<int32_t*>(sel_count);
+    sa.capacity = capacity;
+    if (launch_score_select_attn(v, smin, smax, sa, a, d.err, s, new_k, new_v, true) != cudaSuccess) return HS_ERR_CUDA;
+  } else {
+    if (launch_append(v, new_k, new_v, smin, smax, d.err, s) != cudaSuccess) return HS_ERR_CUDA;
+    cudaError_t e = use_tc ? launch_attn_tc(v, a, d.err, s) : launch_attn_simt(v, a, d.err, s);
+    if (e != cudaSuccess) return HS_ERR_CUDA;
+  }
+  if (a.merged) return HS_OK;
+  return from_cuda(launch_merge(v, a, s));
+}
+
 static hs_status device_address(const void* p, const void** out) {
   if (!p) {
     *out = nullptr;

@@ -76,9 +76,11 @@ bool attn_tc_supported(const KvView& kv);
 bool score_select_attn_supported(const KvView& kv, const AttnArgs& a, int sms);
 // new_k / new_v (nullable): the newest token of every pair is appended first
 // (written into its page, its block's summary widened), as launch_append does.
+// reuse: no scoring or selection; the attention takes the selection in
+// sa.sel / sa.sel_count (capacity sa.capacity) as given.
 cudaError_t launch_score_select_attn(const KvView& kv, const void* smin, const void* smax, const SelectArgs& sa,
                                      AttnArgs& a, unsigned* err, cudaStream_t st, const void* new_k = nullptr,
-                                     const void* new_v = nullptr);
+                                     const void* new_v = nullptr, bool reuse = false);
 // LSE merge of `parts` partial results laid out [parts][rows][D] and [parts][rows].
 cudaError_t launch_merge_parts(int rows, int head_dim, int parts, const float* outs, const float* lses, void* out,
                                int out_f32, float* lse_out, cudaStream_t st);

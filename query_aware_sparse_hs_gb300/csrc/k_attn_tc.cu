@@ -935,6 +935,10 @@ struct FuseArgs {
   int tiles;    // 128-block tiles per (request, kv head)
   int cluster;  // CTAs per (request, kv head)
   int early;    // the summary tile may be copied before the previous kernel completes
+  // reuse: no scoring and no selection; the step attends over the selection
+  // given in sa.sel / sa.sel_count (another layer's), read after the
+  // dependency wait (the append still runs)
+  int reuse;
   // append (nullable new_k): the newest token of every pair, [batch][Hkv][128]
   // bf16, is written at position seq_lens - 1 of the cache and widens its
   // block's summary before the block is scored
@@ -1031,16 +1035,17 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     tma_load_2d(st + 2 * bound::kHalf, &tm_smin, 0, y, tile_full);
     tma_load_2d(st + 3 * bound::kHalf, &tm_smin, 64, y, tile_full);
   };
-  if (f.early && warp == kProdB && lane == 0 && rank < f.tiles) load_tile();
+  const bool tile_loaded = !f.reuse && rank < f.tiles;
+  if (f.early && warp == kProdB && lane == 0 && tile_loaded) load_tile();
   pdl_wait();  // q, the summaries, seq_lens, the page table and the history of this step are complete
-  if (!f.early && warp == kProdB && lane == 0 && rank < f.tiles) load_tile();
+  if (!f.early && warp == kProdB && lane == 0 && tile_loaded) load_tile();
   const int L = max(a.seq_lens[b], 0);
   int nb = (L + a.block - 1) / a.block;
   if (nb > a.max_blocks) {
     if (tid == 0 && rank == 0) set_error(err, HS_EBIT_BLOCK_RANGE);
     nb = a.max_blocks;
   }
-  const bool has_tile = rank < f.tiles && rank * bound::kTile < nb;
+  const bool has_tile = tile_loaded && rank * bound::kTile < nb;
   const int32_t* pt = a.page_table + static_cast<int64_t>(pair) * a.max_blocks;
 
   // ---- phase 1: bound scores of tile `rank` ----
@@ -1055,7 +1060,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     }
   } else if (warp < 4) {
     if (has_tile) bound::write_q(smem + kFQ, a.q, static_cast<int64_t>(b) * a.hq + kvh * g, g, tid);
-    if (f.new_k && L > 0 && rank == (nb - 1) / bound::kTile) {
+    if (f.new_k && L > 0 && rank == (f.reuse ? 0 : (nb - 1) / bound::kTile)) {
       // append ("KV 稀疏化" wiki §5: the summary of the newest token's block
       // covers it): thread t writes channel t of the token's K and V rows into
       // its page and widens the block's min/max row, in the staged tile the
@@ -1071,7 +1076,12 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         f.k_pages_w[row] = kx;
         f.v_pages_w[row] = vx;
       }
-      if (mbar_wait(tile_full, 0, abort_flag, a.wait_ns)) {
+      const int64_t so = (static_cast<int64_t>(pair) * a.max_blocks + jl) * kD + tid;
+      if (f.reuse) {  // no staged tile: the block's row of smin/smax in global memory
+        const float kf = __bfloat162float(kx);
+        f.smin_w[so] = tok == 0 ? kx : __float2bfloat16_rn(fminf(__bfloat162float(f.smin_w[so]), kf));
+        f.smax_w[so] = tok == 0 ? kx : __float2bfloat16_rn(fmaxf(__bfloat162float(f.smax_w[so]), kf));
+      } else if (mbar_wait(tile_full, 0, abort_flag, a.wait_ns)) {
         const int r = jl - rank * bound::kTile, h = tid >> 6, cc = tid & 63;
         const uint32_t off = r * 128 + ((((cc >> 3) ^ (r & 7))) << 4) + (cc & 7) * 2;
         __nv_bfloat16* mx = reinterpret_cast<__nv_bfloat16*>(smem + kFTile + h * bound::kHalf + off);
@@ -1079,7 +1089,6 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         const float kf = __bfloat162float(kx);
         *mn = tok == 0 ? kx : __float2bfloat16_rn(fminf(__bfloat162float(*mn), kf));  // exact: bf16 values
         *mx = tok == 0 ? kx : __float2bfloat16_rn(fmaxf(__bfloat162float(*mx), kf));
-        const int64_t so = (static_cast<int64_t>(pair) * a.max_blocks + jl) * kD + tid;
         f.smin_w[so] = *mn;
         f.smax_w[so] = *mx;
       }
@@ -1091,10 +1100,17 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       mbar_arrive(q_full);
     }
   } else if (warp < 8) {
-    // the pair's page-table row and score history, cleared histograms
+    // the pair's page-table row and score history, cleared histograms; with
+    // reuse the given selection and its count
     const int t = tid - 128;
     for (int j = t; j < nb; j += 128) s_pt[j] = pt[j];
-    if (smoothed) {
+    if (f.reuse) {
+      const int cnt = max(0, min(sa.sel_count[pair], sa.capacity));
+      const int32_t* src = sa.sel + static_cast<int64_t>(pair) * sa.capacity;
+      for (int j = t; j < cnt; j += 128) s_sel[j] = src[j];
+      if (t == 0) s_warp[0] = cnt;
+    }
+    if (smoothed && !f.reuse) {
       const float* h = sa.history + static_cast<int64_t>(pair) * a.max_blocks;
       for (int j = t; j < nb; j += 128) s_prev[j] = h[j];
     }
@@ -1137,18 +1153,25 @@ __global__ void __launch_bounds__(kThreadsB, 1)
                           cluster.map_shared_rank(s_range, r), rank * 4 + warp);
     }
   }
-  if (warp == kProdB && lane == 0 && rank < f.tiles)  // the tile has landed before the ring is reused
+  if (warp == kProdB && lane == 0 && tile_loaded)  // the tile has landed before the ring is reused
     mbar_drain(tile_full, 0);
   if (bound_issued) mbar_drain(acc_full, 0);  // the bound product is done before TMEM is reused
-  cluster.sync();  // every CTA holds all scores; from here only phase 3's pushes reach another CTA's shared memory
+  if (!f.reuse)
+    cluster.sync();  // every CTA holds all scores; from here only phase 3's pushes reach another CTA's shared memory
+  else
+    __syncthreads();  // the reused selection and the page-table row are staged
 
-  // ---- phase 2: every CTA selects; rank 0 stores the selection ----
-  if (smoothed) sel::smooth_staged(s_scores, s_prev, nb, a.max_blocks, sa, pair, rank == 0);
-  static_assert(kThreadsB * 3 >= kFuseMaxBlocks, "three blocks per thread cover the pair");
-  const int n = sel::select_pair_regs<kThreadsB, 3>(s_scores, nb, L, a.block, sa, pair, s_hist, s_warp, err, s_sel,
-                                                    smoothed ? nullptr : s_range, 4 * ceil_div(nb, bound::kTile),
-                                                    rank == 0);
-  __syncthreads();  // the shared copy of the selection is complete
+  // ---- phase 2: every CTA selects (rank 0 stores the selection), or takes the reused one ----
+  int n;
+  if (f.reuse) {
+    n = s_warp[0];
+  } else {
+    if (smoothed) sel::smooth_staged(s_scores, s_prev, nb, a.max_blocks, sa, pair, rank == 0);
+    static_assert(kThreadsB * 3 >= kFuseMaxBlocks, "three blocks per thread cover the pair");
+    n = sel::select_pair_regs<kThreadsB, 3>(s_scores, nb, L, a.block, sa, pair, s_hist, s_warp, err, s_sel,
+                                            smoothed ? nullptr : s_range, 4 * ceil_div(nb, bound::kTile), rank == 0);
+  }
+  __syncthreads();  // the shared copy of the selection is complete (s_warp is free again)
   const int bpc = kChunk / a.block;
   const int per = split_len(n, bpc, a.splits, a.bps);
   const int s0 = min(n, rank * per), s1 = min(n, s0 + per);
@@ -1907,7 +1930,7 @@ bool score_select_attn_supported(const KvView& kv, const AttnArgs& aa, int sms) 
 
 cudaError_t launch_score_select_attn(const KvView& kv, const void* smin, const void* smax, const SelectArgs& sa,
                                      AttnArgs& aa, unsigned* err, cudaStream_t st, const void* new_k,
-                                     const void* new_v) {
+                                     const void* new_v, bool reuse) {
   using FL = FuseLayout<8>;
   const int64_t pairs = static_cast<int64_t>(kv.batch) * kv.hkv;
   if (pairs == 0) return cudaSuccess;
@@ -1921,6 +1944,7 @@ cudaError_t launch_score_select_attn(const KvView& kv, const void* smin, const v
   const TcArgs a = make_args(kv, aa);
   FuseArgs f;
   f.early = aa.early_summaries ? 1 : 0;
+  f.reuse = reuse ? 1 : 0;
   f.scores = sa.scores;
   f.k_pages = static_cast<const uint8_t*>(kv.k_pages);
   f.v_pages = static_cast<const uint8_t*>(kv.v_pages);

@@ -110,6 +110,17 @@ class SparseDecode:
                           self.sel_count, self.scores if keep_scores else None, self.attn_params, self.out, self.lse,
                           self.workspace, stream)
 
+    def decode_step_reuse(self, kv: hs.PagedKV, q: torch.Tensor, new_k: torch.Tensor, new_v: torch.Tensor,
+                          selection, stream=None):
+        """append() then attend(selection=...) as one library call: a layer
+        that reuses another layer's selection runs as the single step launch
+        without its scoring and selection where the shapes allow it."""
+        if selection.capacity != self.capacity:
+            raise ValueError("a reused selection must have the same capacity")
+        hs.hs_decode_step_reuse(self.shape, kv, q, new_k, new_v, self.smin, self.smax, selection.sel,
+                                selection.sel_count, self.capacity, self.attn_params, self.out, self.lse,
+                                self.workspace, stream)
+
     def select_attend(self, kv: hs.PagedKV, q: torch.Tensor, keep_scores: bool = True, stream=None):
         """select() then attend() as one library call (a single launch where
         the shapes allow it)."""
@@ -183,6 +194,10 @@ class SparseDecode:
             hs.hs_decode_step(self.shape, kv, q, new_kv[0], new_kv[1], self.smin, self.smax, self.sel_params,
                               self.sel, self.sel_count, self.scores, self.attn_params, self.out, self.lse,
                               self.workspace, stream)
+            return self.out, self.lse
+        if new_kv is not None and hot is None and reuse is not None and refresh_from_block is None and self.fuse_step:
+            # append and attention over the reused selection in one library call
+            self.decode_step_reuse(kv, q, new_kv[0], new_kv[1], reuse, stream)
             return self.out, self.lse
         if new_kv is not None:
             self.append(kv, new_kv[0], new_kv[1], stream)

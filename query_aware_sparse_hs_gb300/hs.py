@@ -93,6 +93,9 @@ SYMBOLS = {
     "hs_decode_step": (c_int32, [POINTER(AttnShape), POINTER(PagedKV), c_void_p, c_void_p, c_void_p, c_void_p,
                                  c_void_p, POINTER(SelectParams), c_void_p, c_void_p, c_void_p, POINTER(AttnParams),
                                  c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
+    "hs_decode_step_reuse": (c_int32, [POINTER(AttnShape), POINTER(PagedKV), c_void_p, c_void_p, c_void_p,
+                                       c_void_p, c_void_p, c_void_p, c_void_p, c_int32, POINTER(AttnParams),
+                                       c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
     "hs_sparse_paged_decode_attn_noalloc": (c_int32, [POINTER(AttnShape), POINTER(PagedKV), c_void_p,
                                                       c_void_p, c_void_p, c_int32, POINTER(AttnParams),
                                                       c_void_p, c_void_p, c_void_p]),
@@ -257,6 +260,19 @@ def hs_decode_step(shape, kv, q, new_k, new_v, smin, smax, sel_params, sel, sel_
                                ctypes.byref(attn_params), _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes,
                                _stream(stream)),
            "hs_decode_step")
+
+
+def hs_decode_step_reuse(shape, kv, q, new_k, new_v, smin, smax, sel, sel_count, capacity, attn_params, out,
+                         lse=None, workspace=None, stream=None):
+    """Append of the newest token and attention over another layer's selection
+    (sel / sel_count, read only) in one call (one launch where the library can
+    fuse them)."""
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(_lib.hs_decode_step_reuse(ctypes.byref(shape), ctypes.byref(kv), _ptr(q), _ptr(new_k), _ptr(new_v),
+                                     _ptr(smin), _ptr(smax), _ptr(sel), _ptr(sel_count), int(capacity),
+                                     ctypes.byref(attn_params), _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes,
+                                     _stream(stream)),
+           "hs_decode_step_reuse")
 
 
 def hs_score_select_attend(shape, kv, q, smin, smax, sel_params, sel, sel_count, scores, attn_params, out,

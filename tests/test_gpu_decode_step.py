@@ -148,3 +148,43 @@ def test_decode_step_with_early_summaries_equals_without():
             nb = O.num_blocks(L, w.block_size)
             for x, y in zip(a[4:], b[4:]):
                 assert torch.equal(x[bi, :, :nb], y[bi, :, :nb]), bi
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_decode_step_reuse_equals_append_then_attention(name):
+    """A layer that reuses another layer's selection: hs_decode_step_reuse
+    (one launch where the step fuses) must equal, bit for bit, the append
+    followed by the attention over that selection - pages, summaries, output
+    and lse - and leave the reused selection untouched."""
+    from _parity import Case
+    from query_aware_sparse_hs_gb300 import hs
+    w, _ = CASES[name]
+    x = make_inputs(w)
+    c = Case(w, x, tail_nan=False)
+    lead = c.decoder(out_is_fp32=True)
+    lead.build_summaries(c.kv)
+    lead.select(c.kv, c.q)  # the selection the deeper layer reuses
+    sel0, cnt0 = lead.sel.clone(), lead.sel_count.clone()
+    new_k, new_v = _new_token(w, 31 + len(name))
+    dk, dv = new_k.cuda(), new_v.cuda()
+    q2 = c.q.flip(-1).contiguous()  # the reusing layer's own query
+    pages_a = (c.k_pages.clone(), c.v_pages.clone())
+    pages_b = (c.k_pages.clone(), c.v_pages.clone())
+    kv_a = hs.paged_kv(*pages_a, c.page_table, c.seq_lens)
+    kv_b = hs.paged_kv(*pages_b, c.page_table, c.seq_lens)
+    one, ref = c.decoder(out_is_fp32=True), c.decoder(out_is_fp32=True)
+    before = (c.seq_lens - 1).clamp(min=0).contiguous()
+    one.build_summaries(hs.paged_kv(*pages_a, c.page_table, before))
+    ref.build_summaries(hs.paged_kv(*pages_b, c.page_table, before))
+    one.decode_step_reuse(kv_a, q2, dk, dv, lead)
+    ref.append(kv_b, dk, dv)
+    ref.attend(kv_b, q2, selection=lead)
+    torch.cuda.synchronize()
+    assert hs.hs_get_device_error() == (hs.HS_OK, 0)
+    assert torch.equal(one.out, ref.out) and torch.equal(one.lse, ref.lse)
+    assert torch.equal(pages_a[0], pages_b[0]) and torch.equal(pages_a[1], pages_b[1])
+    for b, L in enumerate(c.lens):  # rows of blocks past a request's end are never written
+        nb = O.num_blocks(L, w.block_size)
+        assert torch.equal(one.smin[b, :, :nb], ref.smin[b, :, :nb]), b
+        assert torch.equal(one.smax[b, :, :nb], ref.smax[b, :, :nb]), b
+    assert torch.equal(lead.sel, sel0) and torch.equal(lead.sel_count, cnt0)
