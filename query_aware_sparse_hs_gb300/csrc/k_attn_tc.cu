@@ -303,14 +303,22 @@ __device__ __forceinline__ void run_producer(const TcArgs& a, const Work& w, int
     int next_item = item;
     Item nit = it;
     for (int g = 0; g < ngroups && !stop; ++g) {
+      // the next group (of this item, or the first of the next item) is
+      // looked up once this group's first chunks fill the ring, so that its
+      // dependent loads overlap the copies in flight instead of delaying them
       int2 nxt = make_int2(-1, 0);
-      if (g + 1 < ngroups) {
-        nxt = resolve_group(a, it, (g + 1) * 32, &bad, w);
-      } else {
-        next_item = find_item(a, bpc, item + w.stride, &nit, w);
-        if (next_item < a.items) nxt = resolve_group(a, nit, 0, &bad, w);
-      }
+      bool looked = false;
+      auto look_ahead = [&]() {
+        if (g + 1 < ngroups) {
+          nxt = resolve_group(a, it, (g + 1) * 32, &bad, w);
+        } else {
+          next_item = find_item(a, bpc, item + w.stride, &nit, w);
+          if (next_item < a.items) nxt = resolve_group(a, nit, 0, &bad, w);
+        }
+        looked = true;
+      };
       const int gchunks = min(32 / bpc, (nblk - g * 32 + bpc - 1) / bpc);
+      const int look_at = min(gchunks, STAGES) - 1;
       for (int k = 0; k < gchunks; ++k, ++c) {
         int go = 0;
         if (lane == 0)
@@ -333,7 +341,9 @@ __device__ __forceinline__ void run_producer(const TcArgs& a, const Work& w, int
           prog[0] = c + 1;
           prog[5] = item;
         }
+        if (k == look_at) look_ahead();
       }
+      if (!looked && !stop) look_ahead();  // a group shorter than the ring
       cur = nxt;
     }
     item = next_item;
@@ -1524,59 +1534,81 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* xm = xo + NH * 128;
     float* xl = xm + NH;
     int c = 0;
-    // Query terms (group 0): row (grp, h) of each term holds head h's codes of
-    // channel group grp, zeros elsewhere; thread t writes row t >> 2,
-    // channels 32 (t & 3) .. 32 (t & 3) + 31 of both terms
+    // Query terms: row (cg, h) of each term holds head h's codes of channel
+    // group cg, zeros elsewhere.  The zeros are written once; per item warp 0
+    // (lane 4h + cg: head h, channel group cg) loads its 32 channels, takes
+    // the head's largest entry over the four lanes of the head, and writes
+    // the two 16-byte pieces of its row in both terms.
     int* s_qx = reinterpret_cast<int*>(smem + Ly::kOffQx);
-    auto write_q = [&](int item) {
+    if (grp == 0) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        reinterpret_cast<uint4*>(smem + Ly::kOffQ)[t * 4 + i] = make_uint4(0, 0, 0, 0);
+      if (t < 8 && t >= g) {
+        s_qx[t] = 0;
+        reinterpret_cast<float*>(s_qx + 8)[t] = 0.0f;
+      }
+      named_barrier(bar, 128);  // the zeros are in place before warp 0 writes its pieces
+    }
+    auto write_q = [&](int item) {  // warp 0 of group 0
       const int pair = item / a.splits, b = pair / a.hkv, kvh = pair - b * a.hkv;
-      const int row = t >> 2, cp = t & 3, cg = row >> 3, h = row & 7;
+      const int h = lane >> 2, cg = lane & 3;
+      uint4 v[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) v[i] = make_uint4(0, 0, 0, 0);
+      if (h < g) {
+        const uint4* qr =
+            reinterpret_cast<const uint4*>(a.q + (static_cast<int64_t>(b) * a.hq + kvh * g + h) * kD + 32 * cg);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = qr[i];
+      }
+      uint32_t amax = 0u;  // bits of the largest |entry| (order of non-negative floats)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        amax = max(amax, max(max(v[i].x & 0x7fff7fffu, v[i].y & 0x7fff7fffu),
+                             max(v[i].z & 0x7fff7fffu, v[i].w & 0x7fff7fffu)) & 0xffff0000u);
+        amax = max(amax, max(max((v[i].x << 16) & 0x7fff0000u, (v[i].y << 16) & 0x7fff0000u),
+                             max((v[i].z << 16) & 0x7fff0000u, (v[i].w << 16) & 0x7fff0000u)));
+      }
+      amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+      amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+      if (h >= g) return;
+      // 2^ax brings the head's largest entry into [128, 256)
+      int ex = 0;
+      if (amax != 0u) frexpf(__uint_as_float(amax), &ex);
+      const int ax = amax != 0u ? 8 - ex : 0;
+      if (cg == 0) {
+        s_qx[h] = ax;
+        reinterpret_cast<float*>(s_qx + 8)[h] = ldexpf(a.scale_log2, -ax);
+      }
       uint32_t w1[8], w2[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) w1[i] = w2[i] = 0u;
-      if (cp == cg && h < g) {
-        const uint4* qr = reinterpret_cast<const uint4*>(a.q + (static_cast<int64_t>(b) * a.hq + kvh * g + h) * kD);
-        uint32_t amax = 0u;  // bits of the largest |entry| (order of non-negative floats)
-#pragma unroll 4
-        for (int i = 0; i < 16; ++i) {
-          const uint4 v = qr[i];
-          amax = max(amax, max(max(v.x & 0x7fff7fffu, v.y & 0x7fff7fffu), max(v.z & 0x7fff7fffu, v.w & 0x7fff7fffu)) &
-                               0xffff0000u);
-          amax = max(amax, max(max((v.x << 16) & 0x7fff0000u, (v.y << 16) & 0x7fff0000u),
-                               max((v.z << 16) & 0x7fff0000u, (v.w << 16) & 0x7fff0000u)));
+      for (int i = 0; i < 16; ++i) {
+        const uint4 vv = v[i >> 2];
+        const uint32_t wq2 = (i & 3) == 0 ? vv.x : (i & 3) == 1 ? vv.y : (i & 3) == 2 ? vv.z : vv.w;
+        const float y0 = ldexpf(__uint_as_float(wq2 << 16), ax), y1 = ldexpf(__uint_as_float(wq2 & 0xffff0000u), ax);
+        const __nv_fp8x2_storage_t c1 = __nv_cvt_float2_to_fp8x2(make_float2(y0, y1), __NV_SATFINITE, __NV_E4M3);
+        const __half2_raw h1 = __nv_cvt_fp8x2_to_halfraw2(c1, __NV_E4M3);
+        const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&h1));
+        const __nv_fp8x2_storage_t c2 =
+            __nv_cvt_float2_to_fp8x2(make_float2(y0 - f1.x, y1 - f1.y), __NV_SATFINITE, __NV_E4M3);
+        if ((i & 1) == 0) {
+          w1[i >> 1] = static_cast<uint32_t>(c1);
+          w2[i >> 1] = static_cast<uint32_t>(c2);
+        } else {
+          w1[i >> 1] |= static_cast<uint32_t>(c1) << 16;
+          w2[i >> 1] |= static_cast<uint32_t>(c2) << 16;
         }
-        // 2^ax brings the row's largest entry into [128, 256)
-        int ex = 0;
-        if (amax != 0u) frexpf(__uint_as_float(amax), &ex);
-        const int ax = amax != 0u ? 8 - ex : 0;
-        if (cp == 0) {
-          s_qx[h] = ax;
-          reinterpret_cast<float*>(s_qx + 8)[h] = ldexpf(a.scale_log2, -ax);
-        }
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const uint32_t wq2 = reinterpret_cast<const uint32_t*>(qr + 4 * cg)[i];
-          const float y0 = ldexpf(__uint_as_float(wq2 << 16), ax), y1 = ldexpf(__uint_as_float(wq2 & 0xffff0000u), ax);
-          const __nv_fp8x2_storage_t c1 = __nv_cvt_float2_to_fp8x2(make_float2(y0, y1), __NV_SATFINITE, __NV_E4M3);
-          const __half2_raw h1 = __nv_cvt_fp8x2_to_halfraw2(c1, __NV_E4M3);
-          const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&h1));
-          const __nv_fp8x2_storage_t c2 =
-              __nv_cvt_float2_to_fp8x2(make_float2(y0 - f1.x, y1 - f1.y), __NV_SATFINITE, __NV_E4M3);
-          w1[i >> 1] |= static_cast<uint32_t>(c1) << (16 * (i & 1));
-          w2[i >> 1] |= static_cast<uint32_t>(c2) << (16 * (i & 1));
-        }
-      } else if (cp == cg && cp == 0) {
-        s_qx[h] = 0;
-        reinterpret_cast<float*>(s_qx + 8)[h] = 0.0f;
       }
-      // 16-byte pieces 2cp, 2cp+1 of the row, 128-byte swizzle
+      // 16-byte pieces 2cg, 2cg+1 of row cg * 8 + h, 128-byte swizzle
+      const int row = cg * 8 + h;
 #pragma unroll
       for (int term = 0; term < 2; ++term) {
         uint8_t* rowp = smem + Ly::kOffQ + term * Ly::kQTerm + row * 128;
         const uint32_t* wv = term ? w2 : w1;
 #pragma unroll
         for (int k = 0; k < 2; ++k)
-          *reinterpret_cast<uint4*>(rowp + (((2 * cp + k) ^ (row & 7)) << 4)) =
+          *reinterpret_cast<uint4*>(rowp + (((2 * cg + k) ^ (row & 7)) << 4)) =
               make_uint4(wv[4 * k], wv[4 * k + 1], wv[4 * k + 2], wv[4 * k + 3]);
       }
     };
@@ -1600,7 +1632,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         continue;
       }
       if (grp == 0) {
-        write_q(item);  // the item's query terms (every GEMM1 of the previous item is complete)
+        if (wq == 0) write_q(item);  // the item's query terms (every GEMM1 of the previous item is complete)
         fence_async_smem();
         mbar_arrive(q_full);
         if (t == 0) {
