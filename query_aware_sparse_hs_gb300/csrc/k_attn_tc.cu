@@ -132,7 +132,19 @@ __device__ __forceinline__ int split_len(int cnt, int bpc, int splits, int bps) 
   return min(per, bps);
 }
 
-__device__ __forceinline__ Item item_geom(const TcArgs& a, int item, int bpc, const Work& w) {
+// The two global reads an item's geometry depends on (its pair's selection
+// count and request length), separate from the arithmetic on them, so that a
+// loop can issue them an item ahead and use them an item later.
+struct ItemPre {
+  int cnt, L;
+};
+__device__ __forceinline__ ItemPre item_pre(const TcArgs& a, int item, const Work& w) {
+  if (w.list) return ItemPre{0, 0};
+  const int pair = item / a.splits;
+  return ItemPre{a.sel_count[pair], a.seq_lens[pair / a.hkv]};
+}
+
+__device__ __forceinline__ Item item_geom_from(const TcArgs& a, int item, int bpc, const Work& w, ItemPre pre) {
   Item it;
   it.pair = item / a.splits;
   it.split = item - it.pair * a.splits;
@@ -143,17 +155,21 @@ __device__ __forceinline__ Item item_geom(const TcArgs& a, int item, int bpc, co
     it.s1 = w.s1;
     it.L = w.L;
   } else {
-    int cnt = a.sel_count[it.pair];
+    int cnt = pre.cnt;
     cnt = max(0, min(cnt, a.capacity));
     const int per = split_len(cnt, bpc, a.splits, a.bps);
     it.s0 = it.split * per;
     it.s1 = min(cnt, it.s0 + per);
-    it.L = a.seq_lens[it.b];
+    it.L = pre.L;
   }
   const int nblk = it.s1 - it.s0;
   it.nch = nblk > 0 ? (nblk + bpc - 1) / bpc : 0;
   it.nb = min((max(it.L, 0) + a.block - 1) / a.block, a.max_blocks);
   return it;
+}
+
+__device__ __forceinline__ Item item_geom(const TcArgs& a, int item, int bpc, const Work& w) {
+  return item_geom_from(a, item, bpc, w, item_pre(a, item, w));
 }
 
 
@@ -628,10 +644,11 @@ __device__ __forceinline__ void attn_bf16_cta(const CUtensorMap* tm_k_, const CU
     while (item < a.items) {
       // the next item's geometry and query rows are fetched while this one runs
       const int next = item + w.stride;
-      Item nit{};
+      // (the next item's geometry is only computed at the end of this one)
+      ItemPre npre{0, 0};
       uint4 nqv[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
       if (next < a.items) {
-        nit = item_geom(a, next, bpc, w);
+        npre = item_pre(a, next, w);
         if (grp == 0) load_q(next, nqv);
       }
       const int64_t row0 = (static_cast<int64_t>(it.b) * a.hq + it.kvh * g) * a.splits + it.split;
@@ -837,16 +854,19 @@ __device__ __forceinline__ void attn_bf16_cta(const CUtensorMap* tm_k_, const CU
             }
           }
           named_barrier(bar, 128);
+          // one copy of the output code for all heads: head h's accumulator
+          // picked out of oacc[] with compile-time indices
+#pragma unroll 1
+          for (int h = 0; h < g && h < NH; ++h) {
+            float oh = oacc[0];
 #pragma unroll
-          for (int h = 0; h < NH; ++h) {
-            if (h < g) {
-              const float o = fmaf(oacc[h], fac[4 * h], xo[h * 128 + t] * fac[4 * h + 1]);
-              const float lse = fac[4 * h + 3];
-              if constexpr (PART_SMEM) {
-                emit(h, t, o, lse);
-              } else {
-                put_partial(a, row0, h, t, o, lse);
-              }
+            for (int i = 1; i < NH; ++i) oh = (i == h) ? oacc[i] : oh;
+            const float o = fmaf(oh, fac[4 * h], xo[h * 128 + t] * fac[4 * h + 1]);
+            const float lse = fac[4 * h + 3];
+            if constexpr (PART_SMEM) {
+              emit(h, t, o, lse);
+            } else {
+              put_partial(a, row0, h, t, o, lse);
             }
           }
           if (!PART_SMEM && a.splits > 1 && a.counters) merge_if_last(a, it, t, bar, s_last);
@@ -861,7 +881,7 @@ __device__ __forceinline__ void attn_bf16_cta(const CUtensorMap* tm_k_, const CU
         }
       }
       item = next;
-      it = nit;
+      it = next < a.items ? item_geom_from(a, next, bpc, w, npre) : Item{};
       qv[0] = nqv[0];
       qv[1] = nqv[1];
     }
@@ -1620,7 +1640,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // barrier 3 (bar.red.or), so that all leave the loops at the same point
     while (item < a.items) {
       const int next = item + w.stride;
-      const Item nit = next < a.items ? item_geom(a, next, bpc, w) : Item{};  // in flight meanwhile
+      // the next item's two reads are issued now, its geometry computed at the end
+      const ItemPre npre = next < a.items ? item_pre(a, next, w) : ItemPre{0, 0};
       const int64_t row0 = (static_cast<int64_t>(it.b) * a.hq + it.kvh * g) * a.splits + it.split;
       if (it.nch == 0) {
         if (grp == 0) {
@@ -1628,7 +1649,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (a.splits > 1 && a.counters) merge_if_last(a, it, t, bar, s_last);
         }
         item = next;
-        it = nit;
+        it = next < a.items ? item_geom_from(a, next, bpc, w, npre) : Item{};
         continue;
       }
       if (grp == 0) {
@@ -1813,14 +1834,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         named_barrier(bar, 128);
+        // one copy of the output code for all heads: head h's accumulator
+        // picked out of oacc[] with compile-time indices
+#pragma unroll 1
+        for (int h = 0; h < g && h < NH; ++h) {
+          float oh = oacc[0];
 #pragma unroll
-        for (int h = 0; h < NH; ++h)
-          if (h < g) put_partial(a, row0, h, t, fmaf(oacc[h], fac[4 * h], xo[h * 128 + t] * fac[4 * h + 1]), fac[4 * h + 3]);
+          for (int i = 1; i < NH; ++i) oh = (i == h) ? oacc[i] : oh;
+          put_partial(a, row0, h, t, fmaf(oh, fac[4 * h], xo[h * 128 + t] * fac[4 * h + 1]), fac[4 * h + 3]);
+        }
         if (a.splits > 1 && a.counters) merge_if_last(a, it, t, bar, s_last);
       }
       named_barrier(3, 256);  // the exchange buffer and s_qx are free again
       item = next;
-      it = nit;
+      it = next < a.items ? item_geom_from(a, next, bpc, w, npre) : Item{};
     }
   }
 
