@@ -641,6 +641,7 @@ __device__ __forceinline__ void attn_bf16_cta(const CUtensorMap* tm_k_, const CU
       it = item_geom(a, item, bpc, w);
       if (grp == 0) load_q(item, qv);
     }
+    bool q_ready = false;  // this item's Q operand was written during the previous item's epilogue
     while (item < a.items) {
       // the next item's geometry and query rows are fetched while this one runs
       const int next = item + w.stride;
@@ -656,16 +657,19 @@ __device__ __forceinline__ void attn_bf16_cta(const CUtensorMap* tm_k_, const CU
         prog[6] = item;
         prog[7] = it.nch;
       }
-      if (it.nch > 0) {
-        if (grp == 0) {
-          // Q operand: 16 rows (heads, zero past g) x 128 channels, 128-byte swizzle
-          const int n = t >> 3, ch = t & 7;
+      // Q operand: 16 rows (heads, zero past g) x 128 channels, 128-byte swizzle
+      auto write_q = [&](const uint4 (&v)[2]) {
+        const int n = t >> 3, ch = t & 7;
 #pragma unroll
-          for (int h = 0; h < 2; ++h)
-            *reinterpret_cast<uint4*>(smem + Ly::kOffQ + h * kQHalfBytes + n * 128 + ((ch ^ (n & 7)) << 4)) = qv[h];
-          fence_async_smem();
-          mbar_arrive(q_full);
-        }
+        for (int h = 0; h < 2; ++h)
+          *reinterpret_cast<uint4*>(smem + Ly::kOffQ + h * kQHalfBytes + n * 128 + ((ch ^ (n & 7)) << 4)) = v[h];
+        fence_async_smem();
+        mbar_arrive(q_full);
+      };
+      Item nit{};  // the next item, computed once this item's chunks are done
+      bool q_next = false;
+      if (it.nch > 0) {
+        if (grp == 0 && !q_ready) write_q(qv);
         float m[NH], lsum[NH], oacc[NH], alpha_prev[NH];
 #pragma unroll
         for (int h = 0; h < NH; ++h) {
@@ -800,6 +804,13 @@ __device__ __forceinline__ void attn_bf16_cta(const CUtensorMap* tm_k_, const CU
           last_own = cc;
         }
         c = c0 + it.nch;
+        // both groups have read every S of this item, so the Q operand is
+        // free: the next item's query goes in now and its first products run
+        // during this item's epilogue
+        fail = named_barrier_or(3, 256, fail);
+        if (next < a.items) nit = item_geom_from(a, next, bpc, w, npre);
+        q_next = !fail && next < a.items && nit.nch > 0;
+        if (q_next && grp == 0) write_q(nqv);
         // the normaliser reduction overlaps the last P.V product
         float* rs = red + 8 * NH;
         {
@@ -881,7 +892,8 @@ __device__ __forceinline__ void attn_bf16_cta(const CUtensorMap* tm_k_, const CU
         }
       }
       item = next;
-      it = next < a.items ? item_geom_from(a, next, bpc, w, npre) : Item{};
+      it = (it.nch > 0 || next >= a.items) ? nit : item_geom_from(a, next, bpc, w, npre);
+      q_ready = q_next;
       qv[0] = nqv[0];
       qv[1] = nqv[1];
     }
