@@ -88,9 +88,9 @@ struct Layout {
   static constexpr int kPBufs = NH <= 8 ? 4 : 2;
   static constexpr int kOffQ = kStages * kStageBytes;
   static constexpr int kOffP = kOffQ + 2 * kQHalfBytes;
-  static constexpr int kOffX = kOffP + kPBufs * kPBytes;      // group exchange: o[NH][128], m[NH], l[NH]
+  static constexpr int kOffX = kOffP + kPBufs * kPBytes;  // group hand-over: o[NH][128], m[NH], 2 words
   static constexpr int kOffBar = kOffX + ((NH * 128 + 2 * NH) * 4 + 15) / 16 * 16;
-  static constexpr int kNumBars = 2 * kStages + 13;
+  static constexpr int kNumBars = 2 * kStages + 16;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kOffRed = kOffMisc + 16;
   static constexpr int kOffMeta = kOffRed + 2 * 3 * 4 * NH * 4;  // red: [group][3][4 warps][NH]; meta: [stage][8] (page, valid tokens)
@@ -456,6 +456,9 @@ __device__ __forceinline__ void attn_bf16_setup(uint8_t* smem) {
     }
     for (int b = 0; b < 4; ++b) mbar_init(bar0 + 8 * p_full_index(b), 128);  // p_full, one per P buffer
     mbar_init(bar0 + 8 * (2 * kStages + 10), 128);  // q_full
+    mbar_init(bar0 + 8 * (2 * kStages + 13), 1);    // q_free
+    mbar_init(bar0 + 8 * (2 * kStages + 14), 128);  // x_full
+    mbar_init(bar0 + 8 * (2 * kStages + 15), 128);  // x_free
     *reinterpret_cast<volatile int*>(smem + Ly::kOffMisc + 4) = 0;   // abort flag
     *reinterpret_cast<volatile int*>(smem + Ly::kOffMisc + 12) = 0;  // which wait ran out
     for (int i = 0; i < 8; ++i) reinterpret_cast<volatile int*>(smem + Ly::kOffProg)[i] = 0;
@@ -494,9 +497,14 @@ __device__ __forceinline__ void attn_bf16_cta(const CUtensorMap* tm_k_, const CU
   auto o_full = [&](int b) { return bar0 + 8 * (2 * kStages + 6 + b); };
   auto o_free = [&](int b) { return bar0 + 8 * (2 * kStages + 8 + b); };
   const uint32_t q_full = bar0 + 8 * (2 * kStages + 10);
+  // q_free: every S product of an item is complete (the Q operand may be
+  // rewritten); x_full / x_free: an item's state handed from one softmax
+  // group to the other / read by it
+  const uint32_t q_free = bar0 + 8 * (2 * kStages + 13);
+  const uint32_t x_full = bar0 + 8 * (2 * kStages + 14);
+  const uint32_t x_free = bar0 + 8 * (2 * kStages + 15);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Ly::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Ly::kOffMisc + 4);
-  volatile int* s_last = reinterpret_cast<volatile int*>(smem + Ly::kOffMisc + 8);  // last split of an item
   // progress of the roles, copied into the record of a wait that runs out:
   // [0] chunks issued by the producer, [1] / [2] chunks issued by the S / O
   // MMA thread, [3] / [4] chunks done by softmax group 0 / 1, [5] the
@@ -553,7 +561,7 @@ __device__ __forceinline__ void attn_bf16_cta(const CUtensorMap* tm_k_, const CU
       const uint64_t qdesc = smem_desc(q_half(0), 16, 1024, 2);
       const uint64_t vdesc = smem_desc(v_half(0, 0), kHalfBytes, 1024, 2);
       const uint64_t pdesc = smem_desc(p_buf(0), kPLbo, 128, 0);
-      int c = 0, qi = 0;
+      int c = 0, qi = 0, qc = 0;
       int item = w.first;
       Item it = item < a.items ? item_geom(a, item, bpc, w) : Item{};
       bool ok = true;
@@ -579,6 +587,10 @@ __device__ __forceinline__ void attn_bf16_cta(const CUtensorMap* tm_k_, const CU
             }
             mma_commit(s_full(bb));
             prog[1] = c + 1;
+            if (ci == it.nch - 1) {
+              mma_commit(q_free);  // the item's last S product: its Q operand is free
+              ++qc;
+            }
           } else {
             if (bb != par) continue;
             ok = mbar_wait(p_full(c % Ly::kPBufs), (c / Ly::kPBufs) & 1, abort_flag, a.wait_ns) &&
@@ -603,6 +615,7 @@ __device__ __forceinline__ void attn_bf16_cta(const CUtensorMap* tm_k_, const CU
       // every product this thread issued is complete before TMEM is released
       // (a commit arrives once all of the thread's earlier MMAs are done)
       if (first && c > 0) mbar_drain(s_full((c - 1) & 1), ((c - 1) >> 1) & 1);
+      if (first && qc > 0) mbar_drain(q_free, (qc - 1) & 1);
       if (!first) {
         const int last = ((c - 1) & 1) == par ? c - 1 : c - 2;  // this issuer's last chunk
         if (last >= 0) mbar_drain(empty_bar(last % kStages), (last / kStages) & 1);
@@ -617,7 +630,13 @@ __device__ __forceinline__ void attn_bf16_cta(const CUtensorMap* tm_k_, const CU
     const int bar = 1 + grp;         // named barrier of the group
     const int g = a.group;
     float* red = reinterpret_cast<float*>(smem + Ly::kOffRed) + grp * 12 * NH;  // [3][4 warps][NH]
-    float* xo = reinterpret_cast<float*>(smem + Ly::kOffX);                    // [NH][128] + m[NH] + l[NH]
+    float* rs = red + 8 * NH;                                                  // this group's normaliser parts
+    const float* rs_other = reinterpret_cast<const float*>(smem + Ly::kOffRed) + (1 - grp) * 12 * NH + 8 * NH;
+    // hand-over of an item's state between the groups: o[NH][128], m[NH],
+    // then one last-split word per group
+    float* xo = reinterpret_cast<float*>(smem + Ly::kOffX);
+    float* xm = xo + NH * 128;
+    volatile int* my_last = reinterpret_cast<volatile int*>(xm + NH) + grp;
     auto load_q = [&](int item, uint4 (&v)[2]) {
       const int pair = item / a.splits, b = pair / a.hkv, kvh = pair - b * a.hkv;
       const int n = t >> 3, ch = t & 7;
@@ -629,47 +648,59 @@ __device__ __forceinline__ void attn_bf16_cta(const CUtensorMap* tm_k_, const CU
                                                  ch * 8);
       }
     };
-    // A wait that runs out must not leave a barrier short: every wait's
-    // outcome is made uniform across the warp before the warp-wide TMEM loads,
-    // and across the group (or both groups) at each named barrier (bar.red.or),
-    // so that the threads of a group leave their loops at the same point.
+    // Q operand: 16 rows (heads, zero past g) x 128 channels, 128-byte swizzle
+    auto write_q = [&](const uint4 (&v)[2]) {
+      const int n = t >> 3, ch = t & 7;
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+        *reinterpret_cast<uint4*>(smem + Ly::kOffQ + h * kQHalfBytes + n * 128 + ((ch ^ (n & 7)) << 4)) = v[h];
+      fence_async_smem();
+      mbar_arrive(q_full);
+    };
+    // An item ends with a hand-over instead of a CTA-wide barrier: the group
+    // that takes the next item's first chunk (the starter) writes that item's
+    // query once every S product of this one is complete (q_free), publishes
+    // its state (o, m and its normaliser parts) and goes on; the other group
+    // combines both states and writes the result meanwhile.  Waits across the
+    // groups are bounded mbarrier waits; inside a group, every wait's outcome
+    // is made uniform (warp vote, then bar.red.or at the group's named
+    // barriers) so that the group's threads leave their loops together.
     int c = 0;
+    int e = 0;  // items with chunks so far: the phase of q_free, x_full and x_free
     int item = w.first;
     Item it{};
     uint4 qv[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
     if (item < a.items) {
       it = item_geom(a, item, bpc, w);
-      if (grp == 0) load_q(item, qv);
+      if (grp == 0) load_q(item, qv);  // the first item starts with chunk 0, group 0's
     }
-    bool q_ready = false;  // this item's Q operand was written during the previous item's epilogue
+    bool q_ready = false;  // this item's query was written at the end of the previous one
+    bool fail = false;     // this thread saw a wait run out (uniform per warp)
     while (item < a.items) {
-      // the next item's geometry and query rows are fetched while this one runs
+      // the next item's geometry reads and query rows are issued while this one runs
       const int next = item + w.stride;
-      // (the next item's geometry is only computed at the end of this one)
+      const int c0 = c;
+      const bool starter = grp == ((c0 + it.nch) & 1);
       ItemPre npre{0, 0};
       uint4 nqv[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
       if (next < a.items) {
         npre = item_pre(a, next, w);
-        if (grp == 0) load_q(next, nqv);
+        if (starter) load_q(next, nqv);
       }
       const int64_t row0 = (static_cast<int64_t>(it.b) * a.hq + it.kvh * g) * a.splits + it.split;
       if (tid == 0) {
         prog[6] = item;
         prog[7] = it.nch;
       }
-      // Q operand: 16 rows (heads, zero past g) x 128 channels, 128-byte swizzle
-      auto write_q = [&](const uint4 (&v)[2]) {
-        const int n = t >> 3, ch = t & 7;
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-          *reinterpret_cast<uint4*>(smem + Ly::kOffQ + h * kQHalfBytes + n * 128 + ((ch ^ (n & 7)) << 4)) = v[h];
-        fence_async_smem();
-        mbar_arrive(q_full);
-      };
       Item nit{};  // the next item, computed once this item's chunks are done
       bool q_next = false;
       if (it.nch > 0) {
-        if (grp == 0 && !q_ready) write_q(qv);
+        if (grp == (c0 & 1) && !q_ready) {
+          if (e == 0 || __all_sync(0xffffffffu, mbar_wait(q_free, (e - 1) & 1, abort_flag, a.wait_ns)))
+            write_q(qv);
+          else
+            fail = true;
+        }
         float m[NH], lsum[NH], oacc[NH], alpha_prev[NH];
 #pragma unroll
         for (int h = 0; h < NH; ++h) {
@@ -678,7 +709,6 @@ __device__ __forceinline__ void attn_bf16_cta(const CUtensorMap* tm_k_, const CU
           oacc[h] = 0.0f;
           alpha_prev[h] = 1.0f;
         }
-        bool fail = false;  // this thread saw a wait run out (uniform per warp)
         // O of an own chunk once its P.V product is complete; false (for the
         // whole warp) when the wait ran out
         auto take_o = [&](int cc) -> bool {
@@ -697,7 +727,6 @@ __device__ __forceinline__ void attn_bf16_cta(const CUtensorMap* tm_k_, const CU
           for (int h = 0; h < NH; ++h) oacc[h] = fmaf(oacc[h], alpha_prev[h], ov[h] + ov[NH + h]);
           return true;
         };
-        const int c0 = c;
         int last_own = -1;
         for (int cc = c0 + ((grp - c0) & 1); cc < c0 + it.nch; cc += 2) {
           const int s = cc % kStages;
@@ -804,56 +833,64 @@ __device__ __forceinline__ void attn_bf16_cta(const CUtensorMap* tm_k_, const CU
           last_own = cc;
         }
         c = c0 + it.nch;
-        // both groups have read every S of this item, so the Q operand is
-        // free: the next item's query goes in now and its first products run
-        // during this item's epilogue
-        fail = named_barrier_or(3, 256, fail);
         if (next < a.items) nit = item_geom_from(a, next, bpc, w, npre);
-        q_next = !fail && next < a.items && nit.nch > 0;
-        if (q_next && grp == 0) write_q(nqv);
-        // the normaliser reduction overlaps the last P.V product
-        float* rs = red + 8 * NH;
+        // the normaliser parts (one per warp and head)
+        float wsum;
         {
           float r[NH];
 #pragma unroll
           for (int h = 0; h < NH; ++h) r[h] = lsum[h];
-          const float wsum = warp_reduce_scatter<NH, false>(r);
-          if ((lane % (32 / NH)) == 0) rs[wq * NH + lane / (32 / NH)] = wsum;
+          wsum = warp_reduce_scatter<NH, false>(r);
         }
-        if (!fail && last_own >= 0 && !take_o(last_own)) fail = true;
-        fail = named_barrier_or(bar, 128, fail);
-        // combine the two groups' states: group 1 publishes, group 0 merges and writes
-        float* xm = xo + NH * 128;
-        float* xl = xm + NH;
-        if (grp == 1 && !fail) {
-#pragma unroll
-          for (int h = 0; h < NH; ++h) xo[h * 128 + t] = oacc[h];
-#pragma unroll
-          for (int h = 0; h < NH; ++h) {  // compile-time indices keep m[] in registers
-            if (t == h) {
-              xm[h] = m[h];
-              xl[h] = rs[h] + rs[NH + h] + rs[2 * NH + h] + rs[3 * NH + h];
-            }
+        // (the hand-over buffers - xo, xm and both groups' normaliser
+        // parts - are free once the previous item's combination has read them)
+        if (starter) {
+          // the next item's query first, once this item's S products are
+          // complete, so that its first products overlap the rest
+          q_next = next < a.items && nit.nch > 0;
+          if (q_next) {
+            if (!fail && __all_sync(0xffffffffu, mbar_wait(q_free, e & 1, abort_flag, a.wait_ns)))
+              write_q(nqv);
+            else
+              fail = true;
           }
-        }
-        // both groups agree: after a wait ran out they leave the item loop together
-        if (named_barrier_or(3, 256, fail)) break;
-        if (grp == 0) {
-          // the two groups' combination: per head, the weights of the two
-          // states, 1 / l and the lse, computed once (thread h) into the
-          // chunk-max buffers (free after the chunk loop); then per channel
-          // two products and a scale
+          // then publish and go on (a warp whose wait ran out leaves at the
+          // group's next named barrier, with the others)
+          if (!fail && last_own >= 0 && !take_o(last_own)) fail = true;
+          if (!fail && e > 0 && !__all_sync(0xffffffffu, mbar_wait(x_free, (e - 1) & 1, abort_flag, a.wait_ns)))
+            fail = true;
+          if (!fail) {
+            if ((lane % (32 / NH)) == 0) rs[wq * NH + lane / (32 / NH)] = wsum;
+#pragma unroll
+            for (int h = 0; h < NH; ++h) xo[h * 128 + t] = oacc[h];
+#pragma unroll
+            for (int h = 0; h < NH; ++h)  // compile-time indices keep m[] in registers
+              if (t == h) xm[h] = m[h];
+            mbar_arrive(x_full);
+          }
+        } else {
+          if (!fail && last_own >= 0 && !take_o(last_own)) fail = true;
+          if (!fail && e > 0 && !__all_sync(0xffffffffu, mbar_wait(x_free, (e - 1) & 1, abort_flag, a.wait_ns)))
+            fail = true;
+          if (!fail && (lane % (32 / NH)) == 0) rs[wq * NH + lane / (32 / NH)] = wsum;
+          // x_full: the other group's state is in; the barrier also orders
+          // this group's normaliser parts
+          fail = named_barrier_or(bar, 128, fail || !mbar_wait(x_full, e & 1, abort_flag, a.wait_ns));
+          if (fail) break;
+          // per head, once (thread h): the weights of the two states, 1 / l
+          // and the lse, into this group's chunk-max buffer (no thread of the
+          // group writes it again before the group's next vote barrier, which
+          // every thread reaches only after the output below)
           float* fac = red;  // [NH][4]
           {
-            // thread h < g takes head h: its running max picked out of m[] with
-            // compile-time indices (m[] stays in registers), the arithmetic once
             const int h = t;
             float m0 = -INFINITY;
 #pragma unroll
-            for (int i = 0; i < NH; ++i) m0 = (i == h) ? m[i] : m0;
+            for (int i = 0; i < NH; ++i) m0 = (i == h) ? m[i] : m0;  // compile-time indices keep m[] in registers
             if (h < g && h < NH) {
               const float l0 = rs[h] + rs[NH + h] + rs[2 * NH + h] + rs[3 * NH + h];
-              const float m1 = xm[h], l1 = xl[h];
+              const float m1 = xm[h];
+              const float l1 = rs_other[h] + rs_other[NH + h] + rs_other[2 * NH + h] + rs_other[3 * NH + h];
               const float mx = fmaxf(m0, m1);
               const float e0 = m0 == -INFINITY ? 0.0f : exp2f(m0 - mx);
               const float e1 = m1 == -INFINITY ? 0.0f : exp2f(m1 - mx);
@@ -864,9 +901,10 @@ __device__ __forceinline__ void attn_bf16_cta(const CUtensorMap* tm_k_, const CU
               fac[4 * h + 3] = lt > 0.0f ? (mx + log2f(lt)) * kLn2 : -INFINITY;
             }
           }
-          named_barrier(bar, 128);
-          // one copy of the output code for all heads: head h's accumulator
-          // picked out of oacc[] with compile-time indices
+          fail = named_barrier_or(bar, 128, fail);
+          if (fail) break;
+          // per channel two products; one copy of the code for all heads
+          // (head h's accumulator picked out of oacc[] with compile-time indices)
 #pragma unroll 1
           for (int h = 0; h < g && h < NH; ++h) {
             float oh = oacc[0];
@@ -880,15 +918,16 @@ __device__ __forceinline__ void attn_bf16_cta(const CUtensorMap* tm_k_, const CU
               put_partial(a, row0, h, t, o, lse);
             }
           }
-          if (!PART_SMEM && a.splits > 1 && a.counters) merge_if_last(a, it, t, bar, s_last);
+          mbar_arrive(x_free);
+          if (!PART_SMEM && a.splits > 1 && a.counters) merge_if_last(a, it, t, bar, my_last);
         }
-        named_barrier(3, 256);  // the exchange buffer is free again
+        ++e;
       } else if (grp == 0) {
         if constexpr (PART_SMEM) {
           for (int h = 0; h < g; ++h) emit(h, t, 0.0f, -INFINITY);
         } else {
           for (int h = 0; h < g; ++h) put_partial(a, row0, h, t, 0.0f, -INFINITY);
-          if (a.splits > 1 && a.counters) merge_if_last(a, it, t, bar, s_last);
+          if (a.splits > 1 && a.counters) merge_if_last(a, it, t, bar, my_last);
         }
       }
       item = next;

@@ -22,6 +22,9 @@ CASES = {
     "d64_g16_bf16": WORKLOADS["llama8b_bf16"].scaled(batch=2, num_q_heads=32, num_kv_heads=2,
                                                      head_dim=64, block_size=32, ctx_min=1000,
                                                      ctx_max=1500, k_scored=9),
+    # 16 query heads per kv head at head_dim 128: the tensor-core attention's 16-head variant
+    "d128_g16_bf16": WORKLOADS["llama8b_bf16"].scaled(batch=2, num_q_heads=32, num_kv_heads=2,
+                                                      ctx_min=3000, ctx_max=4133, k_scored=20),
 }
 
 
