@@ -457,6 +457,14 @@ def workload_config(w, layers: int | None = None) -> dict:
 # GPU arm
 # ----------------------------------------------------------------------------
 
+def attn_work(dec) -> dict:
+    """How the tensor-core attention divides its work (hs_attn_geometry):
+    balanced chunk ranges of chunks_per_cta chunks, or equal splits per pair."""
+    from query_aware_sparse_hs_gb300 import hs
+    splits, per = hs.hs_attn_geometry(dec.shape, dec.batch, dec.capacity, dec.attn_params)
+    return {"mode": "balanced_ranges" if per > 0 else "equal_splits", "splits": splits, "chunks_per_cta": per}
+
+
 class Graphs:
     """CUDA graphs of `fn(i)` over step ranges, captured once per range."""
 
@@ -729,7 +737,8 @@ def measure_resident(args, w, dev, world) -> dict:
     launches_per_step = step_launches(w, d0) / args.select_every + reuse_launches * (1 - 1 / args.select_every)
     rec = {
         "value": value, "unit": UNIT, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
-        "dtype": w.kv_dtype, "config": dict(workload_config(w, layers), select_every=args.select_every),
+        "dtype": w.kv_dtype, "config": dict(workload_config(w, layers), select_every=args.select_every,
+                                            attn_work=attn_work(d0)),
         "hbm_gbs_step": step_bytes / (ms_per_step * 1e-3) / 1e9,
         "roofline": dict({"bound": "hbm", "kernel": dom["kernel"], "what": dom["what"], "achieved": dom_gbs,
                           "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": dom_gbs / peak},

@@ -152,7 +152,8 @@ typedef struct hs_select_params {
  * shared memory, so nothing else fits on an SM it occupies.
  * split_counters (nullable): device array of at least batch * Hkv uint32, all
  * zero before the first call that uses it.  When given, and the tensor-core
- * kernel runs every work item on a CTA of its own, it merges the splits itself
+ * kernel runs every work item on a CTA of its own or cuts the work into
+ * balanced chunk ranges (below), it merges the splits itself
  * ([FLL] §2.2 log-sum-exp): each split of a (request, kv head) writes its
  * partial result and counts itself in, and the split that arrives last merges
  * them all into out/lse and sets the counter back to zero; no separate merge
@@ -171,8 +172,18 @@ typedef struct hs_select_params {
  * were complete before it started), so the single-launch step
  * (hs_decode_step, hs_score_select_attend when fused) may start copying its
  * summary tiles while that kernel finishes, instead of after it.  Every other
- * input is still read only after it.  0 = no such guarantee. */
+ * input is still read only after it.  0 = no such guarantee.
+ * Balanced chunk ranges (tensor-core kernel, split_counters given,
+ * blocks_per_split 0): the 128-token chunks of every (request, kv head)'s
+ * full selection are laid end to end and cut into equal runs, one per CTA,
+ * so that no SM idles while another still has a whole item to go; a pair
+ * whose chunks fall into several runs is merged in place as above.  The
+ * library takes them when its cost estimate favours them over equal splits
+ * per pair; HS_ATTN_RANGES takes them whenever they apply, HS_ATTN_NO_RANGES
+ * never (hs_attn_geometry reports the choice). */
 #define HS_ATTN_EARLY_SUMMARIES 1u
+#define HS_ATTN_RANGES 2u
+#define HS_ATTN_NO_RANGES 4u
 typedef struct hs_attn_params {
   float scale;
   int32_t out_is_fp32;
@@ -229,6 +240,14 @@ HS_API int32_t hs_version(void);
  * floats of output and one float of log-sum-exp).  0 on invalid input. */
 HS_API size_t hs_workspace_bytes(const hs_attn_shape* shape, int32_t batch, int32_t capacity,
                           const hs_attn_params* params);
+
+/* How the tensor-core attention divides its work for this geometry on the
+ * current device: *splits = partial results per (request, kv head) at most,
+ * *chunks_per_cta = the length of a balanced chunk range (0 = equal splits
+ * per pair instead).  Returns 0, or -1 on invalid input or without a device
+ * (outputs untouched).  The CUDA-core kernel always uses equal splits. */
+HS_API int32_t hs_attn_geometry(const hs_attn_shape* shape, int32_t batch, int32_t capacity,
+                                const hs_attn_params* params, int32_t* splits, int32_t* chunks_per_cta);
 
 /* Per-block key summaries, [KVS] §5 Quest: for every request b, kv head kvh and
  * block j with first_block <= j < N_b, smin/smax[b][kvh][j][d] = min/max over

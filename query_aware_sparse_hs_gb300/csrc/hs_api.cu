@@ -100,9 +100,13 @@ int max_selected(const hs_attn_shape* s, int max_blocks, int sink, int window, i
 // Split-K geometry: how many selected blocks one CTA work item takes, a whole
 // number of 128-token chunks where blocks are shorter.
 void split_geometry(const hs_attn_shape* s, int batch, int capacity, const hs_attn_params* p,
-                    int sms, int* bps_out, int* splits_out) {
+                    int sms, int* bps_out, int* splits_out, AttnArgs* stream) {
   const int cap = capacity > 0 ? capacity : 1;
   int bps = p ? p->blocks_per_split : 0;
+  if (stream) {
+    stream->stream_per = 0;
+    stream->stream_n = 0;
+  }
   if (bps <= 0) {
     const int64_t pairs = static_cast<int64_t>(batch) * s->num_kv_heads;
     const int64_t n_sm = sms > 0 ? sms : 148;
@@ -114,9 +118,8 @@ void split_geometry(const hs_attn_shape* s, int batch, int capacity, const hs_at
     // combination and output (measured: halving the items of the 16-token
     // and e4m3 workloads pays more than the balance it costs).  The split
     // count with the least such time wins, the fewest splits on a tie.
-    int64_t want = 1;
+    int64_t want = 1, best = -1;
     if (pairs > 0) {
-      int64_t best = -1;
       const int64_t top = chunks < 32 ? chunks : 32;
       for (int64_t sp = 1; sp <= top; ++sp) {
         const int64_t rounds = (pairs * sp + n_sm - 1) / n_sm;
@@ -125,6 +128,30 @@ void split_geometry(const hs_attn_shape* s, int batch, int capacity, const hs_at
           best = cost;
           want = sp;
         }
+      }
+    }
+    // Balanced chunk ranges (the tensor-core kernels, which then merge the
+    // segments of a pair in place, so only with split counters): every CTA
+    // takes an equal run of the pairs' chunks laid end to end, touching at
+    // most ceil(per / chunks) + 1 pairs.  Taken only when cheaper than the
+    // best uniform split, at a measured cost per item: three chunks for the
+    // bf16 kernel, eight for the e4m3 one, whose item start and end (query
+    // terms, state combination, in-place merge) are not overlapped with the
+    // next item (the e4m3 workload, 128 pairs of 33 chunks: 53 us in ranges
+    // of 28 chunks against 43 us in whole pairs).
+    const uint32_t flags = p ? p->flags : 0u;
+    if (stream && pairs > 0 && p && p->split_counters && !(flags & HS_ATTN_NO_RANGES)) {
+      const int64_t total = pairs * chunks;
+      const int64_t per = (total + n_sm - 1) / n_sm;
+      const int64_t items = (per + chunks - 1) / chunks + 1;
+      const int64_t segs = (chunks - 1 + per - 1) / per + 1;  // the most CTAs one pair's chunks touch
+      const int64_t item_cost = s->kv_dtype == HS_KV_FP8E4M3_G32 ? 8 : 3;
+      if (((flags & HS_ATTN_RANGES) || per + item_cost * items < best) && total + per < (int64_t(1) << 30)) {
+        stream->stream_per = static_cast<int32_t>(per);
+        stream->stream_n = static_cast<int32_t>(chunks);
+        *bps_out = cap;
+        *splits_out = static_cast<int>(segs);
+        return;
       }
     }
     if (want > cap) want = cap;
@@ -139,6 +166,19 @@ size_t workspace_for(const hs_attn_shape* s, int batch, int splits) {
   const size_t rows = static_cast<size_t>(batch) * s->num_q_heads * splits;
   const size_t bytes = rows * (s->head_dim + 1) * sizeof(float);
   return (bytes + 255) & ~static_cast<size_t>(255);
+}
+
+// Partial workspace an attention call may need: the larger of the uniform
+// splits and the tensor-core kernels' geometry (which kernel runs depends on
+// the pointers given at call time).
+size_t attn_workspace_need(const hs_attn_shape* s, int batch, int capacity, const hs_attn_params* p, int ctas) {
+  int bps, splits;
+  split_geometry(s, batch, capacity, p, ctas, &bps, &splits, nullptr);
+  const size_t uniform = workspace_for(s, batch, splits);
+  AttnArgs t;
+  split_geometry(s, batch, capacity, p, ctas, &bps, &splits, &t);
+  const size_t tc = workspace_for(s, batch, splits);
+  return uniform > tc ? uniform : tc;
 }
 
 hs_status from_cuda(cudaError_t e) { return e == cudaSuccess ? HS_OK : HS_ERR_CUDA; }
@@ -232,7 +272,7 @@ hs_status prepare_attn(const hs_attn_shape* shape, const hs_paged_kv* kv, const 
     *use_tc = attn_tc_supported(v);
   }
   AttnArgs& a = *out_args;
-  split_geometry(shape, kv->batch, capacity, params, ctas, &a.blocks_per_split, &a.splits);
+  split_geometry(shape, kv->batch, capacity, params, ctas, &a.blocks_per_split, &a.splits, *use_tc ? &a : nullptr);
   const size_t need = workspace_for(shape, kv->batch, a.splits);
   if (need > 0 && (!workspace || ws_bytes < need || !aligned(workspace, 16))) return HS_ERR_WORKSPACE;
   a.sms = ctas;
@@ -277,15 +317,26 @@ const char* hs_status_string(hs_status s) {
 
 int32_t hs_version(void) { return 1; }
 
+int32_t hs_attn_geometry(const hs_attn_shape* shape, int32_t batch, int32_t capacity,
+                         const hs_attn_params* params, int32_t* splits, int32_t* chunks_per_cta) {
+  if (check_shape(shape) != HS_OK || batch < 0 || capacity < 1 || !params || !splits || !chunks_per_cta) return -1;
+  if (params->blocks_per_split < 0 || params->max_ctas < 0) return -1;
+  Device d;
+  if (current_device(&d) != HS_OK) return -1;
+  AttnArgs a;
+  split_geometry(shape, batch, capacity, params, attn_ctas(d.sms, params), &a.blocks_per_split, &a.splits, &a);
+  *splits = a.splits;
+  *chunks_per_cta = a.stream_per;
+  return 0;
+}
+
 size_t hs_workspace_bytes(const hs_attn_shape* shape, int32_t batch, int32_t capacity,
                           const hs_attn_params* params) {
   if (check_shape(shape) != HS_OK || batch < 0 || capacity < 0) return 0;
   Device d{};
   int sms = 148;
   if (current_device(&d) == HS_OK) sms = d.sms;
-  int bps, splits;
-  split_geometry(shape, batch, capacity, params, attn_ctas(sms, params), &bps, &splits);
-  return workspace_for(shape, batch, splits);
+  return attn_workspace_need(shape, batch, capacity, params, attn_ctas(sms, params));
 }
 
 hs_status hs_build_block_summaries(const hs_attn_shape* shape, const hs_paged_kv* kv,
@@ -383,7 +434,7 @@ int32_t hs_score_select_attend_fused(const hs_attn_shape* shape, int32_t batch, 
   v.kv_dtype = shape->kv_dtype;
   if (!attn_tc_supported(v)) return 0;
   AttnArgs a;
-  split_geometry(shape, batch, capacity, params, d.sms, &a.blocks_per_split, &a.splits);
+  split_geometry(shape, batch, capacity, params, d.sms, &a.blocks_per_split, &a.splits, &a);
   return score_select_attn_supported(v, a, d.sms) ? 1 : 0;
 }
 
@@ -718,9 +769,7 @@ extern "C" hs_status hs_sparse_paged_decode_attn_noalloc(const hs_attn_shape* sh
   if (params->blocks_per_split < 0) return HS_ERR_INVALID_ARG;
   Device d;
   if ((st = current_device(&d)) != HS_OK) return st;
-  int bps = 0, splits = 0;
-  split_geometry(shape, kv->batch, capacity, params, attn_ctas(d.sms, params), &bps, &splits);
-  const size_t need = workspace_for(shape, kv->batch, splits);
+  const size_t need = attn_workspace_need(shape, kv->batch, capacity, params, attn_ctas(d.sms, params));
   if (need > HS_NOALLOC_SCRATCH_BYTES) return HS_ERR_SCRATCH_LIMIT;
   void* scratch = nullptr;
   if ((st = scratch_address(d.id, &scratch)) != HS_OK) return st;

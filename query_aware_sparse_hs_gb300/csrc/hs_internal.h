@@ -32,6 +32,10 @@ struct AttnArgs {
   float* ws_lse;  // [batch][hq][splits]
   int32_t blocks_per_split;
   int32_t splits;
+  // balanced chunk ranges (tensor-core kernels, with split counters): the
+  // pairs' chunks end to end, stream_per per CTA; 0 = uniform splits
+  int32_t stream_per = 0;
+  int32_t stream_n = 0;  // chunks of a full selection per pair
   int32_t sms;  // multiprocessors of the current device (persistent grid size)
   int32_t merged = 0;  // set by a launcher that already wrote out / lse (fused merge)
   uint64_t wait_ns = 0;  // bound of the tensor-core kernels' waits (0: the default 2 s)

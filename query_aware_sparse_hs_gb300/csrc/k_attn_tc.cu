@@ -73,6 +73,12 @@ struct TcArgs {
   unsigned* counters;  // split arrivals per pair (null: a separate merge kernel runs)
   int64_t num_pages;
   int hkv, hq, group, block, max_blocks, capacity, bps, splits, items;
+  // balanced chunk ranges (stream_per > 0): the pairs' chunks (stream_n per
+  // pair, a full selection) laid end to end and cut into one range of
+  // stream_per chunks per CTA; an item is then a pair (items = pairs), its
+  // part inside the CTA's range one segment, and splits the most segments a
+  // pair can have (the partial workspace stride)
+  int stream_per, stream_n;
   int out_f32;
   float scale_log2;
   uint64_t wait_ns;  // bound of every wait of the CTA's roles
@@ -106,23 +112,54 @@ struct Layout {
 
 struct Item {
   int pair, split, b, kvh, s0, s1, nch, L, nb;
+  int nseg;  // the pair's splits (segments): 1 = this item writes the output itself
 };
 
 // The work items of one CTA and where their selected blocks come from.  A
-// persistent launch takes items first, first + stride, ... and resolves the
-// global selection through the page table; a CTA of the fused scoring +
-// selection + attention launch takes one item, whose (page, valid tokens)
-// list rank 0 of its cluster has already resolved into this CTA's shared
-// memory: list[i] is position s0 + i of the pair's selection, positions
-// [s0, s1) are the item's, and L is the request's length.
+// persistent launch takes items first, first + stride, ... (below end) and
+// resolves the global selection through the page table; a CTA of the fused
+// scoring + selection + attention launch takes one item, whose (page, valid
+// tokens) list rank 0 of its cluster has already resolved into this CTA's
+// shared memory: list[i] is position s0 + i of the pair's selection,
+// positions [s0, s1) are the item's, and L is the request's length.
 struct Work {
   int first, stride;
   const int2* list;
   int s0, s1, L;
+  int end;
+  static constexpr bool kRanges = false;
+};
+// The same with balanced chunk ranges (a compile-time mode, so that each
+// kernel carries the item geometry of one mode only).
+struct RangeWork : Work {
+  static constexpr bool kRanges = true;
 };
 
-__device__ __forceinline__ Work persistent_work() {
-  return Work{static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), nullptr, 0, 0, 0};
+// With balanced chunk ranges the CTA takes the pairs its range touches, in
+// order; otherwise every gridDim.x-th item.
+template <class W>
+__device__ __forceinline__ W persistent_work(const TcArgs& a) {
+  W w;
+  w.list = nullptr;
+  w.s0 = w.s1 = w.L = 0;
+  if constexpr (W::kRanges) {  // (the chunk total stays below 2^30, so int holds every index)
+    const int lo = static_cast<int>(blockIdx.x) * a.stream_per;
+    const int hi = min(lo + a.stream_per, a.items * a.stream_n);
+    w.first = lo / a.stream_n;
+    w.stride = 1;
+    w.end = hi > lo ? (hi - 1) / a.stream_n + 1 : w.first;
+  } else {
+    w.first = static_cast<int>(blockIdx.x);
+    w.stride = static_cast<int>(gridDim.x);
+    w.end = a.items;
+  }
+  return w;
+}
+
+template <class W>
+__device__ __forceinline__ int item_pair(const TcArgs& a, int item) {
+  if constexpr (W::kRanges) return item;
+  return item / a.splits;
 }
 
 // Selected blocks per split of a pair with cnt selected blocks: its whole
@@ -138,16 +175,19 @@ __device__ __forceinline__ int split_len(int cnt, int bpc, int splits, int bps) 
 struct ItemPre {
   int cnt, L;
 };
-__device__ __forceinline__ ItemPre item_pre(const TcArgs& a, int item, const Work& w) {
+template <class W>
+__device__ __forceinline__ ItemPre item_pre(const TcArgs& a, int item, const W& w) {
   if (w.list) return ItemPre{0, 0};
-  const int pair = item / a.splits;
+  const int pair = item_pair<W>(a, item);
   return ItemPre{a.sel_count[pair], a.seq_lens[pair / a.hkv]};
 }
 
-__device__ __forceinline__ Item item_geom_from(const TcArgs& a, int item, int bpc, const Work& w, ItemPre pre) {
+template <class W>
+__device__ __forceinline__ Item item_geom_from(const TcArgs& a, int item, int bpc, const W& w, ItemPre pre) {
   Item it;
-  it.pair = item / a.splits;
+  it.pair = item_pair<W>(a, item);
   it.split = item - it.pair * a.splits;
+  it.nseg = a.splits;
   it.b = it.pair / a.hkv;
   it.kvh = it.pair - it.b * a.hkv;
   if (w.list) {
@@ -157,9 +197,23 @@ __device__ __forceinline__ Item item_geom_from(const TcArgs& a, int item, int bp
   } else {
     int cnt = pre.cnt;
     cnt = max(0, min(cnt, a.capacity));
-    const int per = split_len(cnt, bpc, a.splits, a.bps);
-    it.s0 = it.split * per;
-    it.s1 = min(cnt, it.s0 + per);
+    if constexpr (W::kRanges) {
+      // the part of the pair's chunks [base, base + stream_n) inside this
+      // CTA's range; the pair's segments are the ranges it touches
+      const int base = it.pair * a.stream_n;
+      const int lo = static_cast<int>(blockIdx.x) * a.stream_per;
+      const int c_lo = max(lo - base, 0);
+      const int c_hi = min(lo + a.stream_per - base, a.stream_n);
+      const int first_cta = base / a.stream_per;
+      it.split = static_cast<int>(blockIdx.x) - first_cta;
+      it.nseg = (base + a.stream_n - 1) / a.stream_per - first_cta + 1;
+      it.s0 = min(cnt, c_lo * bpc);
+      it.s1 = min(cnt, c_hi * bpc);
+    } else {
+      const int per = split_len(cnt, bpc, a.splits, a.bps);
+      it.s0 = it.split * per;
+      it.s1 = min(cnt, it.s0 + per);
+    }
     it.L = pre.L;
   }
   const int nblk = it.s1 - it.s0;
@@ -168,7 +222,8 @@ __device__ __forceinline__ Item item_geom_from(const TcArgs& a, int item, int bp
   return it;
 }
 
-__device__ __forceinline__ Item item_geom(const TcArgs& a, int item, int bpc, const Work& w) {
+template <class W>
+__device__ __forceinline__ Item item_geom(const TcArgs& a, int item, int bpc, const W& w) {
   return item_geom_from(a, item, bpc, w, item_pre(a, item, w));
 }
 
@@ -176,16 +231,16 @@ __device__ __forceinline__ Item item_geom(const TcArgs& a, int item, int bpc, co
 // A split's result: with one split per (request, kv head) it is the final
 // output (written directly, no merge pass); otherwise it goes to the partial
 // workspace for the log-sum-exp merge.
-__device__ __forceinline__ void put_partial(const TcArgs& a, int64_t row0, int h, int t, float o, float lse) {
-  if (a.splits == 1) {
-    const int64_t orow = row0 + h;  // row0 = (b * hq + kvh * g) * splits with splits == 1
+__device__ __forceinline__ void put_partial(const TcArgs& a, const Item& it, int h, int t, float o, float lse) {
+  const int64_t orow = static_cast<int64_t>(it.b) * a.hq + static_cast<int64_t>(it.kvh) * a.group + h;
+  if (it.nseg == 1) {
     if (a.out_f32)
       static_cast<float*>(a.out)[orow * kD + t] = o;
     else
       static_cast<__nv_bfloat16*>(a.out)[orow * kD + t] = __float2bfloat16_rn(o);
     if (a.lse_out && t == 0) a.lse_out[orow] = lse;
   } else {
-    const int64_t row = row0 + static_cast<int64_t>(h) * a.splits;
+    const int64_t row = orow * a.splits + it.split;
     a.ws_o[row * kD + t] = o;
     if (t == 0) a.ws_lse[row] = lse;
   }
@@ -209,18 +264,18 @@ __device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned* p, unsigned v
 __device__ __forceinline__ void merge_if_last(const TcArgs& a, const Item& it, int t, int bar_id,
                                               volatile int* s_last) {
   named_barrier(bar_id, 128);  // every writer's partial stores are issued
-  if (t == 0) *s_last = atom_add_acq_rel_gpu(a.counters + it.pair, 1u) == static_cast<unsigned>(a.splits - 1);
+  if (t == 0) *s_last = atom_add_acq_rel_gpu(a.counters + it.pair, 1u) == static_cast<unsigned>(it.nseg - 1);
   named_barrier(bar_id, 128);
   const bool last = *s_last != 0;
   named_barrier(bar_id, 128);  // s_last may be rewritten by the next item
   if (!last) return;
-  const int g = a.group, S = a.splits;
+  const int g = a.group, S = it.nseg;
   const int c0 = (t & 15) * 8;
   for (int h0 = 0; h0 < g; h0 += 8) {
     const int h = h0 + (t >> 4);
     if (h >= g) continue;
     const int64_t orow = static_cast<int64_t>(it.b) * a.hq + static_cast<int64_t>(it.kvh) * g + h;
-    const int64_t r0 = orow * S;
+    const int64_t r0 = orow * a.splits;  // the pair's segments, stride splits
     float M = -INFINITY;
 #pragma unroll 1
     for (int s = 0; s < S; ++s) M = fmaxf(M, __ldcg(a.ws_lse + r0 + s));
@@ -263,9 +318,10 @@ __device__ __forceinline__ void merge_if_last(const TcArgs& a, const Item& it, i
   if (t == 0) a.counters[it.pair] = 0u;
 }
 
-// First item at or after `item` (stepping by w.stride) that has chunks; a.items if none.
-__device__ __forceinline__ int find_item(const TcArgs& a, int bpc, int item, Item* it, const Work& w) {
-  for (; item < a.items; item += w.stride) {
+// First item at or after `item` (stepping by w.stride) that has chunks; w.end or past if none.
+template <class W>
+__device__ __forceinline__ int find_item(const TcArgs& a, int bpc, int item, Item* it, const W& w) {
+  for (; item < w.end; item += w.stride) {
     *it = item_geom(a, item, bpc, w);
     if (it->nch > 0) break;
   }
@@ -302,18 +358,18 @@ __device__ __forceinline__ int2 resolve_group(const TcArgs& a, const Item& it, i
 // valid-token counts are published in meta[stage][8] for the softmax warps and
 // every lane issues the copies of its own block.
 // prog[0] / prog[5]: chunks issued so far / the item being issued.
-template <int STAGES, typename IssueFn>
-__device__ __forceinline__ void run_producer(const TcArgs& a, const Work& w, int bpc, uint32_t full0, uint32_t empty0,
+template <int STAGES, class W, typename IssueFn>
+__device__ __forceinline__ void run_producer(const TcArgs& a, const W& w, int bpc, uint32_t full0, uint32_t empty0,
                                              int2* meta, uint32_t bytes_per_block, volatile int* abort_flag,
                                              unsigned* err, volatile int* prog, IssueFn issue) {
   const int lane = threadIdx.x & 31;
   unsigned bad = 0;
   Item it;
   int item = find_item(a, bpc, w.first, &it, w);
-  int2 cur = item < a.items ? resolve_group(a, it, 0, &bad, w) : make_int2(-1, 0);
+  int2 cur = item < w.end ? resolve_group(a, it, 0, &bad, w) : make_int2(-1, 0);
   int c = 0;
   bool stop = false;
-  while (item < a.items && !stop) {
+  while (item < w.end && !stop) {
     const int nblk = it.s1 - it.s0;
     const int ngroups = (nblk + 31) / 32;
     int next_item = item;
@@ -329,7 +385,7 @@ __device__ __forceinline__ void run_producer(const TcArgs& a, const Work& w, int
           nxt = resolve_group(a, it, (g + 1) * 32, &bad, w);
         } else {
           next_item = find_item(a, bpc, item + w.stride, &nit, w);
-          if (next_item < a.items) nxt = resolve_group(a, nit, 0, &bad, w);
+          if (next_item < w.end) nxt = resolve_group(a, nit, 0, &bad, w);
         }
         looked = true;
       };
@@ -478,9 +534,9 @@ struct NoEmit {};
 // goes to the output (one split) or the partial workspace, or, with an Emit
 // other than NoEmit, to emit(h, channel, o, lse) for the caller's merge.  Run
 // by all kThreadsB threads.
-template <int NH, bool SETUP = true, class Emit = NoEmit>
+template <int NH, bool SETUP = true, class Emit = NoEmit, class W = Work>
 __device__ __forceinline__ void attn_bf16_cta(const CUtensorMap* tm_k_, const CUtensorMap* tm_v_, const TcArgs& a,
-                                              const Work& w, unsigned* err, const Emit& emit = Emit{}) {
+                                              const W& w, unsigned* err, const Emit& emit = Emit{}) {
   constexpr bool PART_SMEM = !std::is_same<Emit, NoEmit>::value;
   using Ly = Layout<NH>;
   const CUtensorMap& tm_k = *tm_k_;
@@ -563,11 +619,11 @@ __device__ __forceinline__ void attn_bf16_cta(const CUtensorMap* tm_k_, const CU
       const uint64_t pdesc = smem_desc(p_buf(0), kPLbo, 128, 0);
       int c = 0, qi = 0, qc = 0;
       int item = w.first;
-      Item it = item < a.items ? item_geom(a, item, bpc, w) : Item{};
+      Item it = item < w.end ? item_geom(a, item, bpc, w) : Item{};
       bool ok = true;
-      while (ok && item < a.items && !*abort_flag) {
+      while (ok && item < w.end && !*abort_flag) {
         const int next = item + w.stride;
-        const Item nit = next < a.items ? item_geom(a, next, bpc, w) : Item{};  // in flight meanwhile
+        const Item nit = next < w.end ? item_geom(a, next, bpc, w) : Item{};  // in flight meanwhile
         if (it.nch > 0 && first) {
           ok = mbar_wait(q_full, qi & 1, abort_flag, a.wait_ns);
           ++qi;
@@ -638,7 +694,7 @@ __device__ __forceinline__ void attn_bf16_cta(const CUtensorMap* tm_k_, const CU
     float* xm = xo + NH * 128;
     volatile int* my_last = reinterpret_cast<volatile int*>(xm + NH) + grp;
     auto load_q = [&](int item, uint4 (&v)[2]) {
-      const int pair = item / a.splits, b = pair / a.hkv, kvh = pair - b * a.hkv;
+      const int pair = item_pair<W>(a, item), b = pair / a.hkv, kvh = pair - b * a.hkv;
       const int n = t >> 3, ch = t & 7;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -670,24 +726,23 @@ __device__ __forceinline__ void attn_bf16_cta(const CUtensorMap* tm_k_, const CU
     int item = w.first;
     Item it{};
     uint4 qv[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
-    if (item < a.items) {
+    if (item < w.end) {
       it = item_geom(a, item, bpc, w);
       if (grp == 0) load_q(item, qv);  // the first item starts with chunk 0, group 0's
     }
     bool q_ready = false;  // this item's query was written at the end of the previous one
     bool fail = false;     // this thread saw a wait run out (uniform per warp)
-    while (item < a.items) {
+    while (item < w.end) {
       // the next item's geometry reads and query rows are issued while this one runs
       const int next = item + w.stride;
       const int c0 = c;
       const bool starter = grp == ((c0 + it.nch) & 1);
       ItemPre npre{0, 0};
       uint4 nqv[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
-      if (next < a.items) {
+      if (next < w.end) {
         npre = item_pre(a, next, w);
         if (starter) load_q(next, nqv);
       }
-      const int64_t row0 = (static_cast<int64_t>(it.b) * a.hq + it.kvh * g) * a.splits + it.split;
       if (tid == 0) {
         prog[6] = item;
         prog[7] = it.nch;
@@ -833,7 +888,7 @@ __device__ __forceinline__ void attn_bf16_cta(const CUtensorMap* tm_k_, const CU
           last_own = cc;
         }
         c = c0 + it.nch;
-        if (next < a.items) nit = item_geom_from(a, next, bpc, w, npre);
+        if (next < w.end) nit = item_geom_from(a, next, bpc, w, npre);
         // the normaliser parts (one per warp and head)
         float wsum;
         {
@@ -847,7 +902,7 @@ __device__ __forceinline__ void attn_bf16_cta(const CUtensorMap* tm_k_, const CU
         if (starter) {
           // the next item's query first, once this item's S products are
           // complete, so that its first products overlap the rest
-          q_next = next < a.items && nit.nch > 0;
+          q_next = next < w.end && nit.nch > 0;
           if (q_next) {
             if (!fail && __all_sync(0xffffffffu, mbar_wait(q_free, e & 1, abort_flag, a.wait_ns)))
               write_q(nqv);
@@ -915,23 +970,23 @@ __device__ __forceinline__ void attn_bf16_cta(const CUtensorMap* tm_k_, const CU
             if constexpr (PART_SMEM) {
               emit(h, t, o, lse);
             } else {
-              put_partial(a, row0, h, t, o, lse);
+              put_partial(a, it, h, t, o, lse);
             }
           }
           mbar_arrive(x_free);
-          if (!PART_SMEM && a.splits > 1 && a.counters) merge_if_last(a, it, t, bar, my_last);
+          if (!PART_SMEM && it.nseg > 1 && a.counters) merge_if_last(a, it, t, bar, my_last);
         }
         ++e;
       } else if (grp == 0) {
         if constexpr (PART_SMEM) {
           for (int h = 0; h < g; ++h) emit(h, t, 0.0f, -INFINITY);
         } else {
-          for (int h = 0; h < g; ++h) put_partial(a, row0, h, t, 0.0f, -INFINITY);
-          if (a.splits > 1 && a.counters) merge_if_last(a, it, t, bar, my_last);
+          for (int h = 0; h < g; ++h) put_partial(a, it, h, t, 0.0f, -INFINITY);
+          if (it.nseg > 1 && a.counters) merge_if_last(a, it, t, bar, my_last);
         }
       }
       item = next;
-      it = (it.nch > 0 || next >= a.items) ? nit : item_geom_from(a, next, bpc, w, npre);
+      it = (it.nch > 0 || next >= w.end) ? nit : item_geom_from(a, next, bpc, w, npre);
       q_ready = q_next;
       qv[0] = nqv[0];
       qv[1] = nqv[1];
@@ -949,11 +1004,11 @@ __device__ __forceinline__ void attn_bf16_cta(const CUtensorMap* tm_k_, const CU
   }
 }
 
-template <int NH>
+template <int NH, class W>
 __global__ void __launch_bounds__(kThreadsB, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                    TcArgs a, unsigned* err) {
-  attn_bf16_cta<NH>(&tm_k, &tm_v, a, persistent_work(), err);
+  attn_bf16_cta<NH, true, NoEmit, W>(&tm_k, &tm_v, a, persistent_work<W>(a), err);
 }
 
 
@@ -1280,7 +1335,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   // the push buffer of the CTA that merges that head ----
   const int hp = (g + f.cluster - 1) / f.cluster;  // heads merged per CTA
   float* push = reinterpret_cast<float*>(smem + FL::kOffPush);
-  const Work w{rank < a.splits ? pair * a.splits + rank : a.items, a.items, s_list, s0, s1, L};
+  const Work w{rank < a.splits ? pair * a.splits + rank : a.items, a.items, s_list, s0, s1, L, a.items};
   attn_bf16_cta<NH, false, ClusterPush>(&tm_k, &tm_v, a, w, err, ClusterPush{push, hp, rank});
 
   // ---- phase 4: the splits' log-sum-exp merge inside the cluster
@@ -1418,12 +1473,13 @@ __device__ __forceinline__ void convert_half_row(const uint8_t* codes_row, const
   }
 }
 
+template <class W>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                        TcArgs a, unsigned* err) {
   using Ly = Layout8;
   constexpr int NH = 8;
-  const Work w = persistent_work();
+  const W w = persistent_work<W>(a);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -1511,11 +1567,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pdesc = smem_desc(sbase + Ly::kOffP, Ly::kPLbo, 128, 0);
       int c = 0, qi = 0;
       int item = w.first;
-      Item it = item < a.items ? item_geom(a, item, bpc, w) : Item{};
+      Item it = item < w.end ? item_geom(a, item, bpc, w) : Item{};
       bool ok = true;
-      while (ok && item < a.items && !*abort_flag) {
+      while (ok && item < w.end && !*abort_flag) {
         const int next = item + w.stride;
-        const Item nit = next < a.items ? item_geom(a, next, bpc, w) : Item{};
+        const Item nit = next < w.end ? item_geom(a, next, bpc, w) : Item{};
         if (it.nch > 0 && first) {
           ok = mbar_wait(q_full, qi & 1, abort_flag, a.wait_ns);
           ++qi;
@@ -1575,7 +1631,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = ct >> 1, cp = ct & 1;
     int c = 0;
     bool ok = true;
-    for (int item = w.first; ok && item < a.items && !*abort_flag; item += w.stride) {
+    for (int item = w.first; ok && item < w.end && !*abort_flag; item += w.stride) {
       const Item it = item_geom(a, item, bpc, w);
       for (int ci = 0; ci < it.nch; ++ci, ++c) {
         const int s = c % kStages8;
@@ -1622,7 +1678,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       named_barrier(bar, 128);  // the zeros are in place before warp 0 writes its pieces
     }
     auto write_q = [&](int item) {  // warp 0 of group 0
-      const int pair = item / a.splits, b = pair / a.hkv, kvh = pair - b * a.hkv;
+      const int pair = item_pair<W>(a, item), b = pair / a.hkv, kvh = pair - b * a.hkv;
       const int h = lane >> 2, cg = lane & 3;
       uint4 v[4];
 #pragma unroll
@@ -1685,22 +1741,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     int item = w.first;
     Item it{};
-    if (item < a.items) it = item_geom(a, item, bpc, w);
+    if (item < w.end) it = item_geom(a, item, bpc, w);
     // a wait that runs out is made uniform across the warp (warp-wide TMEM
     // loads), across a group at its named barrier and across both groups at
     // barrier 3 (bar.red.or), so that all leave the loops at the same point
-    while (item < a.items) {
+    while (item < w.end) {
       const int next = item + w.stride;
       // the next item's two reads are issued now, its geometry computed at the end
-      const ItemPre npre = next < a.items ? item_pre(a, next, w) : ItemPre{0, 0};
-      const int64_t row0 = (static_cast<int64_t>(it.b) * a.hq + it.kvh * g) * a.splits + it.split;
+      const ItemPre npre = next < w.end ? item_pre(a, next, w) : ItemPre{0, 0};
       if (it.nch == 0) {
         if (grp == 0) {
-          for (int h = 0; h < g; ++h) put_partial(a, row0, h, t, 0.0f, -INFINITY);
-          if (a.splits > 1 && a.counters) merge_if_last(a, it, t, bar, s_last);
+          for (int h = 0; h < g; ++h) put_partial(a, it, h, t, 0.0f, -INFINITY);
+          if (it.nseg > 1 && a.counters) merge_if_last(a, it, t, bar, s_last);
         }
         item = next;
-        it = next < a.items ? item_geom_from(a, next, bpc, w, npre) : Item{};
+        it = next < w.end ? item_geom_from(a, next, bpc, w, npre) : Item{};
         continue;
       }
       if (grp == 0) {
@@ -1892,13 +1947,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           float oh = oacc[0];
 #pragma unroll
           for (int i = 1; i < NH; ++i) oh = (i == h) ? oacc[i] : oh;
-          put_partial(a, row0, h, t, fmaf(oh, fac[4 * h], xo[h * 128 + t] * fac[4 * h + 1]), fac[4 * h + 3]);
+          put_partial(a, it, h, t, fmaf(oh, fac[4 * h], xo[h * 128 + t] * fac[4 * h + 1]), fac[4 * h + 3]);
         }
-        if (a.splits > 1 && a.counters) merge_if_last(a, it, t, bar, s_last);
+        if (it.nseg > 1 && a.counters) merge_if_last(a, it, t, bar, s_last);
       }
       named_barrier(3, 256);  // the exchange buffer and s_qx are free again
       item = next;
-      it = next < a.items ? item_geom_from(a, next, bpc, w, npre) : Item{};
+      it = next < w.end ? item_geom_from(a, next, bpc, w, npre) : Item{};
     }
   }
 
@@ -1981,12 +2036,21 @@ TcArgs make_args(const KvView& kv, const AttnArgs& aa) {
   a.capacity = aa.capacity;
   a.bps = aa.blocks_per_split;
   a.splits = aa.splits;
-  a.items = kv.batch * kv.hkv * aa.splits;
+  a.stream_per = aa.stream_per;
+  a.stream_n = aa.stream_n;
+  a.items = kv.batch * kv.hkv * (aa.stream_per > 0 ? 1 : aa.splits);
   a.scale_log2 = aa.scale * kLog2e;
   a.wait_ns = aa.wait_ns > 0 ? aa.wait_ns : kWaitLimitNs;
   return a;
 }
 
+
+// Persistent grid: one CTA per balanced range, else min(items, CTAs allowed).
+int attn_grid(const TcArgs& a, int sms) {
+  if (a.stream_per > 0)
+    return static_cast<int>((static_cast<int64_t>(a.items) * a.stream_n + a.stream_per - 1) / a.stream_per);
+  return a.items < sms ? a.items : sms;
+}
 
 cudaError_t launch_fp8(const KvView& kv, AttnArgs& aa, unsigned* err, cudaStream_t st) {
   CUtensorMap mk, mv;
@@ -1996,14 +2060,16 @@ cudaError_t launch_fp8(const KvView& kv, AttnArgs& aa, unsigned* err, cudaStream
     return cudaErrorInvalidValue;
   const TcArgs a = make_args(kv, aa);
   if (a.items == 0) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(attn_tc_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       Layout8::kAlloc);
+  auto kern = a.stream_per > 0 ? attn_tc_fp8_kernel<RangeWork> : attn_tc_fp8_kernel<Work>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Layout8::kAlloc);
   if (e != cudaSuccess) return e;
-  const int grid = a.items < aa.sms ? a.items : aa.sms;
+  const int grid = attn_grid(a, aa.sms);
   TcArgs b = a;
-  if (a.items > grid) b.counters = nullptr;  // CTAs with several items: the merge kernel is cheaper
+  // CTAs with several uniform splits: the merge kernel is cheaper (balanced
+  // ranges always merge in place)
+  if (a.stream_per == 0 && a.items > grid) b.counters = nullptr;
   aa.merged = aa.splits == 1 || b.counters != nullptr;
-  return launch_pdl(attn_tc_fp8_kernel, dim3(grid), dim3(kThreads), Layout8::kAlloc, st, mk, mv, b, err);
+  return launch_pdl(kern, dim3(grid), dim3(kThreads), Layout8::kAlloc, st, mk, mv, b, err);
 }
 
 template <int NH>
@@ -2016,12 +2082,14 @@ cudaError_t launch_nh(const KvView& kv, AttnArgs& aa, unsigned* err, cudaStream_
     return cudaErrorInvalidValue;
   const TcArgs a = make_args(kv, aa);
   if (a.items == 0) return cudaSuccess;
-  auto kern = attn_tc_kernel<NH>;
+  auto kern = a.stream_per > 0 ? attn_tc_kernel<NH, RangeWork> : attn_tc_kernel<NH, Work>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::kAlloc);
   if (e != cudaSuccess) return e;
-  const int grid = a.items < aa.sms ? a.items : aa.sms;
+  const int grid = attn_grid(a, aa.sms);
   TcArgs b = a;
-  if (a.items > grid) b.counters = nullptr;  // CTAs with several items: the merge kernel is cheaper
+  // CTAs with several uniform splits: the merge kernel is cheaper (balanced
+  // ranges always merge in place)
+  if (a.stream_per == 0 && a.items > grid) b.counters = nullptr;
   aa.merged = aa.splits == 1 || b.counters != nullptr;
   return launch_pdl(kern, dim3(grid), dim3(kThreadsB), Ly::kAlloc, st, mk, mv, b, err);
 }
@@ -2029,7 +2097,7 @@ cudaError_t launch_nh(const KvView& kv, AttnArgs& aa, unsigned* err, cudaStream_
 }  // namespace
 
 bool score_select_attn_supported(const KvView& kv, const AttnArgs& aa, int sms) {
-  if (kv.kv_dtype != HS_KV_BF16 || kv.group > 8 || !attn_tc_supported(kv)) return false;
+  if (kv.kv_dtype != HS_KV_BF16 || kv.group > 8 || aa.stream_per > 0 || !attn_tc_supported(kv)) return false;
   const int tiles = (kv.max_blocks + bound::kTile - 1) / bound::kTile;
   const int f = tiles > aa.splits ? tiles : aa.splits;
   const int64_t pairs = static_cast<int64_t>(kv.batch) * kv.hkv;

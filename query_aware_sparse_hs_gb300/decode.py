@@ -26,12 +26,14 @@ class SparseDecode:
     (hs_score_select_attend, a single launch where the geometry allows).
     early_summaries: this layer's summaries are never written by the kernel
     launched just before its step (e.g. layers stepped in turn), so the
-    single-launch step may start reading them early (HS_ATTN_EARLY_SUMMARIES)."""
+    single-launch step may start reading them early (HS_ATTN_EARLY_SUMMARIES).
+    ranges: balanced chunk ranges of the tensor-core attention (True = always
+    where they apply, False = never, None = the library's cost estimate)."""
 
     def __init__(self, *, num_q_heads, num_kv_heads, head_dim, block_size, kv_dtype, batch,
                  max_blocks, sink_tokens, window_tokens, k_scored, capacity=None, scale=None,
                  out_is_fp32=False, algo="auto", blocks_per_split=0, score_smoothing=0.0,
-                 inline_merge=True, fuse_step=True, early_summaries=False, device="cuda"):
+                 inline_merge=True, fuse_step=True, early_summaries=False, ranges=None, device="cuda"):
         self.kv_dtype = kv_dtype
         self.shape = hs.attn_shape(num_q_heads, num_kv_heads, head_dim, block_size, kv_dtype)
         self.batch, self.max_blocks = int(batch), int(max_blocks)
@@ -50,7 +52,7 @@ class SparseDecode:
                                if inline_merge else None)
         self.attn_params = hs.attn_params(scale if scale is not None else 1.0 / math.sqrt(head_dim),
                                           out_is_fp32, blocks_per_split, algo, split_counters=self.split_counters,
-                                          early_summaries=early_summaries)
+                                          early_summaries=early_summaries, ranges=ranges)
         sdt = _SUMMARY_DTYPE[kv_dtype]
         self.smin = torch.empty((batch, num_kv_heads, max_blocks, head_dim), dtype=sdt, device=dev)
         self.smax = torch.empty_like(self.smin)

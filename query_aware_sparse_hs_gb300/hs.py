@@ -22,6 +22,8 @@ HS_ERR_OUT_OF_RANGE, HS_ERR_CAPACITY, HS_ERR_TIMEOUT, HS_ERR_WORKSPACE = 4, 5, 6
 HS_ERR_SCRATCH_LIMIT = 8
 HS_NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
 HS_ATTN_EARLY_SUMMARIES = 1
+HS_ATTN_RANGES = 2
+HS_ATTN_NO_RANGES = 4
 HS_EBIT_PAGE_RANGE, HS_EBIT_CAPACITY, HS_EBIT_TIMEOUT, HS_EBIT_BLOCK_RANGE = 0x1, 0x2, 0x4, 0x8
 KV_DTYPES = {"f32": 0, "bf16": 1, "fp8": 2}
 ALGO = {"auto": 0, "simt": 1, "tcgen05": 2}
@@ -72,6 +74,8 @@ SYMBOLS = {
     "hs_status_string": (ctypes.c_char_p, [c_int32]),
     "hs_version": (c_int32, []),
     "hs_workspace_bytes": (c_size_t, [POINTER(AttnShape), c_int32, c_int32, POINTER(AttnParams)]),
+    "hs_attn_geometry": (c_int32, [POINTER(AttnShape), c_int32, c_int32, POINTER(AttnParams),
+                                   POINTER(c_int32), POINTER(c_int32)]),
     "hs_select_workspace_bytes": (c_size_t, [POINTER(AttnShape), c_int32, c_int32]),
     "hs_build_block_summaries": (c_int32, [POINTER(AttnShape), POINTER(PagedKV), c_int32, c_void_p,
                                            c_void_p, c_void_p]),
@@ -187,19 +191,31 @@ def select_params(sink_tokens, window_tokens, k_scored, capacity, history_weight
 
 
 def attn_params(scale, out_is_fp32=False, blocks_per_split=0, algo="auto", max_ctas=0,
-                split_counters=None, wait_limit_ns=0, early_summaries=False) -> AttnParams:
+                split_counters=None, wait_limit_ns=0, early_summaries=False, ranges=None) -> AttnParams:
     """wait_limit_ns: bound of the tensor-core kernels' waits (0 = 2 s).
     early_summaries: HS_ATTN_EARLY_SUMMARIES (smin/smax are not written by the
-    kernel launched just before the call on its stream)."""
+    kernel launched just before the call on its stream).  ranges: True =
+    HS_ATTN_RANGES, False = HS_ATTN_NO_RANGES, None = the library's choice."""
+    flags = (HS_ATTN_EARLY_SUMMARIES if early_summaries else 0) | \
+        {None: 0, True: HS_ATTN_RANGES, False: HS_ATTN_NO_RANGES}[ranges]
     p = AttnParams(float(scale), 1 if out_is_fp32 else 0, int(blocks_per_split),
                    ALGO[algo] if isinstance(algo, str) else int(algo), int(max_ctas), _ptr(split_counters),
-                   int(wait_limit_ns), HS_ATTN_EARLY_SUMMARIES if early_summaries else 0)
+                   int(wait_limit_ns), flags)
     p._keep = split_counters
     return p
 
 
 def hs_workspace_bytes(shape: AttnShape, batch: int, capacity: int, params: AttnParams) -> int:
     return int(_lib.hs_workspace_bytes(ctypes.byref(shape), batch, capacity, ctypes.byref(params)))
+
+
+def hs_attn_geometry(shape: AttnShape, batch: int, capacity: int, params: AttnParams):
+    """(splits, chunks_per_cta) of the tensor-core attention; chunks_per_cta 0 = equal splits."""
+    sp, per = c_int32(0), c_int32(0)
+    if _lib.hs_attn_geometry(ctypes.byref(shape), batch, capacity, ctypes.byref(params), ctypes.byref(sp),
+                             ctypes.byref(per)) != 0:
+        raise HSError(HS_ERR_INVALID_ARG, "hs_attn_geometry")
+    return sp.value, per.value
 
 
 def hs_select_workspace_bytes(shape: AttnShape, batch: int, max_blocks: int) -> int:

@@ -155,6 +155,49 @@ def test_end_to_end_bf16_output(cases, name):
             assert np.all(np.abs(out[b, kvh * g:(kvh + 1) * g] - ref) <= tol), (b, kvh)
 
 
+@pytest.mark.parametrize("max_ctas", [3, 7, 0])
+@pytest.mark.parametrize("name", ["llama_bf16_tail", "ragged_bf16", "fp8_tail", "long_b16_bf16", "d128_g16_bf16"])
+def test_attention_balanced_ranges(cases, name, max_ctas):
+    """Balanced chunk ranges (HS_ATTN_RANGES): the pairs' chunks end to end,
+    cut into one equal run per CTA, a pair spread over several runs merged in
+    place.  Few CTAs make runs that cover several whole pairs and pairs that
+    span three runs.  Same oracle bound as the equal splits; the split
+    counters are back at zero afterwards."""
+    from _parity import TOL
+    from query_aware_sparse_hs_gb300 import hs
+    c = cases[name]
+    w = c.w
+    dec = c.decoder(out_is_fp32=True, algo="tcgen05")
+    dec.attn_params = hs.attn_params(dec.attn_params.scale, True, 0, "tcgen05", max_ctas=max_ctas,
+                                     split_counters=dec.split_counters, ranges=True)
+    splits, per = hs.hs_attn_geometry(dec.shape, w.batch, dec.capacity, dec.attn_params)
+    assert per > 0 and splits >= 1
+    dec.workspace = torch.empty((hs.hs_workspace_bytes(dec.shape, w.batch, dec.capacity, dec.attn_params),),
+                                dtype=torch.uint8, device=dec.workspace.device)
+    sel = np.full((w.batch, w.num_kv_heads, dec.capacity), -1, dtype=np.int32)
+    cnt = np.zeros((w.batch, w.num_kv_heads), dtype=np.int32)
+    ref_out = np.zeros((w.batch, w.num_q_heads, w.head_dim))
+    ref_lse = np.zeros((w.batch, w.num_q_heads))
+    g = w.group
+    for b in range(w.batch):
+        for kvh in range(w.num_kv_heads):
+            r = c.oracle_pair(b, kvh)
+            sel[b, kvh, :len(r["sel"])] = r["sel"]
+            cnt[b, kvh] = len(r["sel"])
+            ref_out[b, kvh * g:(kvh + 1) * g] = r["out"]
+            ref_lse[b, kvh * g:(kvh + 1) * g] = r["lse"]
+    dec.sel.copy_(torch.from_numpy(sel))
+    dec.sel_count.copy_(torch.from_numpy(cnt))
+    for _ in range(2):  # the second call checks that the counters were re-armed
+        dec.out.zero_()
+        dec.attend(c.kv, c.q)
+        _err_clear()
+        tol = TOL["fp8_dequant"] if w.kv_dtype == "fp8" else TOL[w.kv_dtype]
+        assert np.abs(dec.out.cpu().numpy() - ref_out).max() <= tol
+        assert np.abs(dec.lse.cpu().numpy() - ref_lse).max() <= 1e-4
+        assert int(dec.split_counters.abs().sum()) == 0
+
+
 def test_k_covers_everything_is_dense_attention():
     """With k at least the block count the result is dense softmax attention."""
     from _parity import Case
