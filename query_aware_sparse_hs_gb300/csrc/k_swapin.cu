@@ -287,8 +287,8 @@ constexpr int kSub = 64;  // token rows of a block staged in shared memory at a 
 template <int KIND>
 constexpr int elem_size() { return KIND == HS_KV_F32 ? 4 : (KIND == HS_KV_BF16 ? 2 : 1); }
 
-// Dynamic shared memory of the attending copy kernel: K and V rows of a
-// sub-block (+ e4m3 scales), q of the group, and the scores/probabilities.
+// Dynamic shared memory of the copied-blocks attention: K and V rows of a
+// sub-block (+ e4m3 scales) and q of the group.
 // K/V rows are staged with a stride of one row plus four elements, so that
 // threads reading four consecutive elements of consecutive rows hit distinct
 // banks.
@@ -303,8 +303,7 @@ struct AttendSmem {
   static constexpr int kOffKs = (kOffV + kSub * kStride + 15) / 16 * 16;
   static constexpr int kOffVs = kOffKs + kSub * kScaleRow;
   static constexpr int kOffQ = (kOffVs + kSub * kScaleRow + 15) / 16 * 16;
-  static constexpr int kOffP = kOffQ + kMaxGroup * D * 4;
-  static constexpr int kBytes = kOffP + kMaxGroup * kSub * 4;
+  static constexpr int kBytes = kOffQ + kMaxGroup * D * 4;
 };
 
 // Channel d of staged row t, as the attention sees it (e4m3: code * scale).
@@ -395,9 +394,11 @@ __global__ __launch_bounds__(kCopyThreads, 1) void swapin_copy_kernel(HotView hb
 // Attention of one stream's query heads over the blocks of its miss list,
 // read from the slots the copy filled.  One CTA per stream (streams without
 // misses only write lse = -inf).  Per block, in pieces of up to kSub valid
-// tokens: the rows are staged in shared memory (16-byte loads, padded rows);
-// thread (head, token) takes a dot product; one warp per head updates the
-// running max and sum; thread (head, channel) accumulates p * v.
+// tokens, the rows are staged in shared memory (16-byte loads, padded rows);
+// then each warp takes whole heads (warp w: heads w, w + 8) with no further
+// barrier: lane t scores tokens t and t + 32, the warp's shuffles give the
+// running max and sum, and lane t accumulates p * v for channels
+// [C t, C t + C).
 template <int C, int KIND>
 __global__ __launch_bounds__(kAttnThreads) void copied_blocks_attn_kernel(HotView hb,
                                                                          const int32_t* __restrict__ miss_sel,
@@ -405,11 +406,11 @@ __global__ __launch_bounds__(kAttnThreads) void copied_blocks_attn_kernel(HotVie
                                                                          int capacity, MissAttn ma, unsigned* err) {
   using Ly = AttendSmem<C, KIND>;
   constexpr int D = C * 32;
-  constexpr int kAcc = (kMaxGroup * D + kAttnThreads - 1) / kAttnThreads;
-  __shared__ float s_m[kMaxGroup], s_l[kMaxGroup], s_alpha[kMaxGroup];
+  constexpr int kWarps = kAttnThreads / 32;
+  constexpr int kHpw = (kMaxGroup + kWarps - 1) / kWarps;  // heads per warp
+  static_assert(kSub == 64, "two token rows per lane");
   extern __shared__ __align__(16) uint8_t dyn[];
   float* s_q = reinterpret_cast<float*>(dyn + Ly::kOffQ);
-  float* s_p = reinterpret_cast<float*>(dyn + Ly::kOffP);
   pdl_trigger();
   pdl_wait();
   const int pair = blockIdx.x;
@@ -429,17 +430,19 @@ __global__ __launch_bounds__(kAttnThreads) void copied_blocks_attn_kernel(HotVie
   const int32_t* pt = hb.page_table + static_cast<int64_t>(pair) * hb.max_blocks;
   const int L = ma.seq_lens[b];
   const int B = hb.block;
-  float acc[kAcc];
-#pragma unroll
-  for (int i = 0; i < kAcc; ++i) acc[i] = 0.0f;
-  if (tid < g) {
-    s_m[tid] = -INFINITY;
-    s_l[tid] = 0.0f;
-  }
   for (int i = tid; i < g * D; i += kAttnThreads) {
     const int64_t e = qrow0 * D + i;  // heads of the group are consecutive rows
     s_q[i] = KIND == HS_KV_F32 ? static_cast<const float*>(ma.q)[e]
                                : bf16_bits_to_float(static_cast<const uint16_t*>(ma.q)[e]);
+  }
+  // per head of this warp: running max and sum (log2 units), p * v of its C channels
+  float m[kHpw], l[kHpw], acc[kHpw][C];
+#pragma unroll
+  for (int k = 0; k < kHpw; ++k) {
+    m[k] = -INFINITY;
+    l[k] = 0.0f;
+#pragma unroll
+    for (int c = 0; c < C; ++c) acc[k][c] = 0.0f;
   }
   const float* ksc = reinterpret_cast<const float*>(dyn + Ly::kOffKs);
   const float* vsc = reinterpret_cast<const float*>(dyn + Ly::kOffVs);
@@ -452,7 +455,7 @@ __global__ __launch_bounds__(kAttnThreads) void copied_blocks_attn_kernel(HotVie
     const int64_t row0 = (static_cast<int64_t>(pair) * S + sl) * B;
     for (int r0 = 0; r0 < nv; r0 += kSub) {
       const int rows = min(kSub, nv - r0);
-      __syncthreads();  // previous piece done with the staging, s_p and s_alpha
+      __syncthreads();  // every warp is done with the previous piece (and q is in)
       {  // stage K and V rows (and scales): 16-byte loads, 4-byte stores into the padded rows
         constexpr int kVecRow = Ly::kRowBytes / 16;
         const int vec = rows * kVecRow;
@@ -481,71 +484,67 @@ __global__ __launch_bounds__(kAttnThreads) void copied_blocks_attn_kernel(HotVie
         }
       }
       __syncthreads();
-      // scores: thread (h, t) takes the dot product of head h with token t
-      for (int idx = tid; idx < g * kSub; idx += kAttnThreads) {
-        const int h = idx / kSub, t = idx - h * kSub;
-        if (t < rows) {
-          const float4* qv = reinterpret_cast<const float4*>(s_q + h * D);
-          float a0 = 0.0f, a1 = 0.0f;
-#pragma unroll 8
-          for (int d4 = 0; d4 < D / 4; ++d4) {
-            const float4 k4 = staged_val4<C, KIND>(dyn + Ly::kOffK, ksc, t, d4 * 4);
-            const float4 q4 = qv[d4];
-            a0 = fmaf(q4.x, k4.x, a0);
-            a1 = fmaf(q4.y, k4.y, a1);
-            a0 = fmaf(q4.z, k4.z, a0);
-            a1 = fmaf(q4.w, k4.w, a1);
-          }
-          s_p[h * kSub + t] = (a0 + a1) * ma.scale_log2;
-        }
-      }
-      __syncthreads();
-      // running max / sum per head; s_p becomes p = 2^(s - m)
-      for (int h = warp; h < g; h += kAttnThreads / 32) {
-        float mb = -INFINITY;
-        for (int t = lane; t < rows; t += 32) mb = fmaxf(mb, s_p[h * kSub + t]);
-        mb = warp_max(mb);
-        const float m_old = s_m[h];
-        const float m_new = fmaxf(m_old, mb);
-        float sum = 0.0f;
-        for (int t = lane; t < rows; t += 32) {
-          const float pv = exp2f(s_p[h * kSub + t] - m_new);
-          s_p[h * kSub + t] = pv;
-          sum += pv;
-        }
-        sum = warp_sum(sum);
-        if (lane == 0) {
-          const float alpha = m_old == -INFINITY ? 0.0f : exp2f(m_old - m_new);
-          s_alpha[h] = alpha;
-          s_l[h] = s_l[h] * alpha + sum;
-          s_m[h] = m_new;
-        }
-      }
-      __syncthreads();
-      // o[h][d] = o[h][d] * alpha_h + sum_t p[h][t] v[t][d]
 #pragma unroll
-      for (int ai = 0; ai < kAcc; ++ai) {
-        const int idx = tid + ai * kAttnThreads;
-        if (idx < g * D) {
-          const int h = idx / D, d = idx - h * D;
-          float a = acc[ai] * s_alpha[h];
-          for (int t = 0; t < rows; ++t) a = fmaf(s_p[h * kSub + t], staged_val<C, KIND>(dyn + Ly::kOffV, vsc, t, d), a);
-          acc[ai] = a;
+      for (int k = 0; k < kHpw; ++k) {
+        const int h = warp + k * kWarps;
+        if (h >= g) break;  // the same for the whole warp
+        const float4* qv = reinterpret_cast<const float4*>(s_q + h * D);
+        // scores of tokens lane and lane + 32 (two chains each)
+        const int t0 = min(lane, rows - 1), t1 = min(lane + 32, rows - 1);
+        float a0 = 0.0f, a1 = 0.0f, b0 = 0.0f, b1 = 0.0f;
+#pragma unroll 8
+        for (int d4 = 0; d4 < D / 4; ++d4) {
+          const float4 q4 = qv[d4];
+          const float4 x = staged_val4<C, KIND>(dyn + Ly::kOffK, ksc, t0, d4 * 4);
+          const float4 y = staged_val4<C, KIND>(dyn + Ly::kOffK, ksc, t1, d4 * 4);
+          a0 = fmaf(q4.x, x.x, a0);
+          a1 = fmaf(q4.y, x.y, a1);
+          a0 = fmaf(q4.z, x.z, a0);
+          a1 = fmaf(q4.w, x.w, a1);
+          b0 = fmaf(q4.x, y.x, b0);
+          b1 = fmaf(q4.y, y.y, b1);
+          b0 = fmaf(q4.z, y.z, b0);
+          b1 = fmaf(q4.w, y.w, b1);
+        }
+        const float s0 = lane < rows ? (a0 + a1) * ma.scale_log2 : -INFINITY;
+        const float s1 = lane + 32 < rows ? (b0 + b1) * ma.scale_log2 : -INFINITY;
+        const float mn = fmaxf(m[k], warp_max(fmaxf(s0, s1)));
+        const float alpha = m[k] == -INFINITY ? 0.0f : exp2f(m[k] - mn);
+        const float p0 = s0 == -INFINITY ? 0.0f : exp2f(s0 - mn);
+        const float p1 = s1 == -INFINITY ? 0.0f : exp2f(s1 - mn);
+        l[k] = l[k] * alpha + warp_sum(p0 + p1);
+        m[k] = mn;
+#pragma unroll
+        for (int cc = 0; cc < C; ++cc) acc[k][cc] *= alpha;
+        // p * v: token t's probability from lane t % 32
+        for (int t = 0; t < rows; ++t) {
+          const float pt_ = __shfl_sync(0xffffffffu, t < 32 ? p0 : p1, t & 31);
+          if constexpr (C == 4) {
+            const float4 v4 = staged_val4<C, KIND>(dyn + Ly::kOffV, vsc, t, lane * 4);
+            acc[k][0] = fmaf(pt_, v4.x, acc[k][0]);
+            acc[k][1] = fmaf(pt_, v4.y, acc[k][1]);
+            acc[k][2] = fmaf(pt_, v4.z, acc[k][2]);
+            acc[k][3] = fmaf(pt_, v4.w, acc[k][3]);
+          } else {
+#pragma unroll
+            for (int cc = 0; cc < C; ++cc)
+              acc[k][cc] = fmaf(pt_, staged_val<C, KIND>(dyn + Ly::kOffV, vsc, t, lane * C + cc), acc[k][cc]);
+          }
         }
       }
     }
   }
-  __syncthreads();
-  // normalised output and lse of every query head of the stream
+  // normalised output and lse of this warp's heads
 #pragma unroll
-  for (int ai = 0; ai < kAcc; ++ai) {
-    const int idx = tid + ai * kAttnThreads;
-    if (idx < g * D) {
-      const int h = idx / D, d = idx - h * D;
-      const float l = s_l[h];
-      if (l > 0.0f) ma.out[(qrow0 + h) * D + d] = acc[ai] / l;
-      if (d == 0) ma.lse[qrow0 + h] = l > 0.0f ? (s_m[h] + log2f(l)) * 0.6931471805599453f : -INFINITY;
+  for (int k = 0; k < kHpw; ++k) {
+    const int h = warp + k * kWarps;
+    if (h >= g) break;
+    const float lk = l[k];
+    if (lk > 0.0f) {
+#pragma unroll
+      for (int cc = 0; cc < C; ++cc) ma.out[(qrow0 + h) * D + lane * C + cc] = acc[k][cc] / lk;
     }
+    if (lane == 0) ma.lse[qrow0 + h] = lk > 0.0f ? (m[k] + log2f(lk)) * 0.6931471805599453f : -INFINITY;
   }
   (void)err;
 }
