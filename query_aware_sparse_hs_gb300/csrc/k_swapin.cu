@@ -341,54 +341,154 @@ __device__ __forceinline__ float4 staged_val4(const uint8_t* rows, const float* 
 }
 
 // Copy only: the pages of the miss lists written by swapin_plan_kernel, whose
-// slots the page table now names.  Persistent: CTA c takes streams c, c+grid, ...
+// slots the page table now names.  The misses of all streams, in stream
+// order, are cut into one equal share per CTA, so that every CTA keeps its
+// 16-byte host loads in flight however the misses fall on the streams (a CTA
+// per stream in turn would wait out a host round trip per stream).  Each CTA
+// finds its share with two passes over the miss counts (total, then the
+// prefix of the streams it touches), resolves up to kCopyBatch misses at a
+// time to (stream, block, slot) and copies them with all its threads.
+__device__ __forceinline__ int clamp_misses(int n, int capacity, int S) {
+  n = n < 0 ? 0 : (n > capacity ? capacity : n);
+  return n > S ? S : n;
+}
+
 __global__ __launch_bounds__(kCopyThreads, 1) void swapin_copy_kernel(HotView hb, const int32_t* __restrict__ miss_sel,
                                                                       const int32_t* __restrict__ miss_count,
                                                                       int capacity, hs_swap_stats* stats,
                                                                       unsigned* err) {
-  __shared__ int s_j[kCopyBatch];
-  __shared__ int s_s[kCopyBatch];
-  __shared__ int s_n;
+  __shared__ int s_p[kCopyBatch];  // stream of each miss of the window (-1: skipped)
+  __shared__ int s_j[kCopyBatch];  // its block, then (resolved) its pool page offset
+  __shared__ int s_s[kCopyBatch];  // its slot
+  __shared__ int s_warp[kCopyThreads / 32];
   // No early trigger: CTAs of a dependent launched early would wait on SMs
   // that the attention running beside the copy needs.
   pdl_wait();  // (a no-op unless launched as a programmatic dependent)
   const int pairs = hb.batch * hb.hkv;
   const int S = hb.slots;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int kW = kCopyThreads / 32;
+  // inclusive block scan of one value per thread (the tile's running sum is in *tot)
+  auto block_scan = [&](int v, long long* tot) -> int {
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) s_warp[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+      int wv = lane < kW ? s_warp[lane] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, wv, o);
+        if (lane >= o) wv += y;
+      }
+      if (lane < kW) s_warp[lane] = wv;
+    }
+    __syncthreads();
+    const int incl = x + (warp > 0 ? s_warp[warp - 1] : 0);
+    *tot = s_warp[kW - 1];
+    __syncthreads();  // s_warp is reused by the next tile
+    return incl;
+  };
+  // pass 1: all misses
+  long long total = 0;
+  for (int p0 = 0; p0 < pairs; p0 += kCopyThreads) {
+    const int p = p0 + tid;
+    long long t;
+    block_scan(p < pairs ? clamp_misses(miss_count[p], capacity, S) : 0, &t);
+    total += t;
+  }
+  const long long lo = total * blockIdx.x / gridDim.x, hi = total * (blockIdx.x + 1) / gridDim.x;
+  const int64_t page_bytes = page_bytes_of(hb);
+  const int vpp = static_cast<int>(page_bytes / 16);
   unsigned long long pages = 0;
-  for (int pair = blockIdx.x; pair < pairs; pair += gridDim.x) {
-    int n = miss_count[pair];
-    n = n < 0 ? 0 : (n > capacity ? capacity : n);
-    n = n > S ? S : n;
-    const int64_t row = static_cast<int64_t>(pair) * capacity;
-    const int32_t* pt = hb.page_table + static_cast<int64_t>(pair) * hb.max_blocks;
-    for (int i0 = 0; i0 < n; i0 += kCopyBatch) {  // n is uniform across the CTA
-      if (threadIdx.x == 0) s_n = 0;
-      __syncthreads();
-      const int i = i0 + static_cast<int>(threadIdx.x);
-      if (threadIdx.x < kCopyBatch && i < n) {
-        const int j = miss_sel[row + i];
-        if (j < 0 || j >= hb.max_blocks) {
-          set_error(err, HS_EBIT_BLOCK_RANGE);
-        } else {
-          const int sl = pt[j] - pair * S;
-          if (sl < 0 || sl >= S) {
-            set_error(err, HS_EBIT_PAGE_RANGE);
-          } else {
-            const int k = atomicAdd(&s_n, 1);
-            s_j[k] = j;
-            s_s[k] = sl;
+  for (long long w0 = lo; w0 < hi; w0 += kCopyBatch) {
+    const long long w1 = min(hi, w0 + kCopyBatch);
+    const int m = static_cast<int>(w1 - w0);
+    // pass 2: the streams whose misses fall in [w0, w1) list them
+    long long carry = 0;
+    for (int p0 = 0; p0 < pairs && carry < w1; p0 += kCopyThreads) {
+      const int p = p0 + tid;
+      const int n = p < pairs ? clamp_misses(miss_count[p], capacity, S) : 0;
+      long long t;
+      const long long pre = carry + block_scan(n, &t) - n;  // misses before stream p
+      for (long long k = max(pre, w0); k < min(pre + n, w1); ++k) {
+        s_p[k - w0] = p;
+        s_j[k - w0] = static_cast<int>(k - pre);  // index in the stream's miss list
+      }
+      carry += t;
+    }
+    __syncthreads();
+    // resolve: block and slot of each miss of the window
+    for (int e = tid; e < m; e += kCopyThreads) {
+      const int p = s_p[e];
+      const int j = miss_sel[static_cast<int64_t>(p) * capacity + s_j[e]];
+      int sl = -1;
+      if (j < 0 || j >= hb.max_blocks) {
+        set_error(err, HS_EBIT_BLOCK_RANGE);
+      } else {
+        sl = hb.page_table[static_cast<int64_t>(p) * hb.max_blocks + j] - p * S;
+        if (sl < 0 || sl >= S) {
+          set_error(err, HS_EBIT_PAGE_RANGE);
+          sl = -1;
+        }
+      }
+      s_j[e] = j;
+      s_s[e] = sl;
+      if (sl < 0) s_p[e] = -1;
+    }
+    __syncthreads();
+    // copy: K then V of every miss, kCopyUnroll 16-byte host loads in flight per thread
+    const int64_t vtot = static_cast<int64_t>(m) * vpp * 2;
+    for (int64_t v0 = tid; v0 < vtot; v0 += static_cast<int64_t>(kCopyThreads) * kCopyUnroll) {
+      uint4 buf[kCopyUnroll];
+      uint4* dst[kCopyUnroll];
+#pragma unroll
+      for (int u = 0; u < kCopyUnroll; ++u) {
+        const int64_t v = v0 + static_cast<int64_t>(u) * kCopyThreads;
+        dst[u] = nullptr;
+        if (v < vtot) {
+          const int which = v >= static_cast<int64_t>(m) * vpp;  // 0 = K, 1 = V
+          const int w = static_cast<int>(v - which * static_cast<int64_t>(m) * vpp);
+          const int e = w / vpp, off = w - e * vpp;
+          const int p = s_p[e];
+          if (p >= 0) {
+            const uint4* src = reinterpret_cast<const uint4*>(
+                                   static_cast<const char*>(which ? hb.host_v : hb.host_k) +
+                                   (static_cast<int64_t>(p) * hb.max_blocks + s_j[e]) * page_bytes) + off;
+            dst[u] = reinterpret_cast<uint4*>(static_cast<char*>(which ? hb.v_slots : hb.k_slots) +
+                                              (static_cast<int64_t>(p) * S + s_s[e]) * page_bytes) + off;
+            buf[u] = __ldcs(src);
           }
         }
       }
-      __syncthreads();
-      const int m = s_n;
-      copy_pages(hb, pair, m, [&](int c) { return s_j[c]; }, [&](int c) { return s_s[c]; });
-      pages += m;
-      __syncthreads();  // s_j/s_s/s_n are refilled next round
+#pragma unroll
+      for (int u = 0; u < kCopyUnroll; ++u)
+        if (dst[u]) *dst[u] = buf[u];
     }
+    if (hb.kv_dtype == HS_KV_FP8E4M3_G32) {
+      const int spp = hb.block * (hb.head_dim / kQuantGroup);  // scales per page
+      for (int v = tid; v < 2 * m * spp; v += kCopyThreads) {
+        const int which = v >= m * spp;
+        const int w = v - which * m * spp;
+        const int e = w / spp, off = w - e * spp;
+        const int p = s_p[e];
+        if (p < 0) continue;
+        const float* src = (which ? hb.host_v_scales : hb.host_k_scales) +
+                           (static_cast<int64_t>(p) * hb.max_blocks + s_j[e]) * spp + off;
+        float* dst = (which ? hb.v_slot_scales : hb.k_slot_scales) + (static_cast<int64_t>(p) * S + s_s[e]) * spp + off;
+        *dst = __ldcs(src);
+      }
+    }
+    if (stats && tid == 0)
+      for (int e = 0; e < m; ++e) pages += s_p[e] >= 0 ? 1 : 0;
+    __syncthreads();  // the window's lists are refilled next
   }
-  if (stats && threadIdx.x == 0 && pages)
-    atomicAdd(&stats->bytes_in, pages * 2ull * static_cast<unsigned long long>(page_bytes_of(hb) + scale_bytes_of(hb)));
+  if (stats && pages)
+    atomicAdd(&stats->bytes_in, pages * 2ull * static_cast<unsigned long long>(page_bytes + scale_bytes_of(hb)));
 }
 
 // Attention of one stream's query heads over the blocks of its miss list,
