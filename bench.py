@@ -131,6 +131,23 @@ def attn_splits(w, dec, params=None) -> int:
     return hs.hs_workspace_bytes(dec.shape, w.batch, dec.capacity, params or dec.attn_params) // per_split
 
 
+def merge_launches(w, dec, params) -> int:
+    """1 when the attention's split partials go through the separate merge
+    kernel: not with one split, nor when the tensor-core kernel merges them in
+    place (split counters, and every work item a CTA of its own or balanced
+    chunk ranges)."""
+    from query_aware_sparse_hs_gb300 import hs
+    tc = w.kv_dtype in ("bf16", "fp8") and w.head_dim == 128 and w.block_size in (16, 32, 64, 128)
+    if not tc:
+        return 0 if attn_splits(w, dec, params) <= 1 else 1
+    splits, per = hs.hs_attn_geometry(dec.shape, w.batch, dec.capacity, params)
+    if splits <= 1 or per > 0:
+        return 0
+    ctas = params.max_ctas if 0 < params.max_ctas < _sms() else _sms()
+    inline = dec.split_counters is not None and w.batch * w.num_kv_heads * splits <= ctas
+    return 0 if inline else 1
+
+
 def step_launches(w, dec, hot: bool = False, overlap: bool = False, allow_fused: bool = True) -> int:
     """Kernels of one step as the library dispatches them for this workload:
     either the single append + scoring + selection + attention launch (which
@@ -138,25 +155,19 @@ def step_launches(w, dec, hot: bool = False, overlap: bool = False, allow_fused:
     offload path), bound scoring + selection (select_launches), the swap-in
     (offload; with the copy overlapped: plan, page copy, attention over the
     copied blocks, attention over the resident blocks and the merge of the
-    two) and attention; and the split merge unless the tensor-core attention
-    merges in the kernel or gives every pair one split."""
+    two) and attention; and the split merge unless the attention merges its
+    splits itself (merge_launches)."""
     n = 0 if hot else 1
     if not hot and allow_fused and fused_step(w, dec):
         return 1  # the append runs inside the single launch
     n += select_launches(w)
-    tc = w.kv_dtype in ("bf16", "fp8") and w.head_dim == 128 and w.block_size in (16, 32, 64, 128)
     if hot and overlap:
         # plan, page copy, attention over the copied blocks, attention over the
-        # hits (+ its split merge: no split counters there), merge of the parts
-        splits = attn_splits(w, dec, getattr(dec, "hit_params", None))
-        return n + 5 + (0 if (tc and splits <= 1) else 1)
-    splits = attn_splits(w, dec)
+        # hits (+ its split merge), merge of the parts
+        return n + 5 + merge_launches(w, dec, dec.hit_params)
     n += 1 if hot else 0
     n += 1
-    # the tensor-core kernel merges its splits itself when it has split
-    # counters and every work item a CTA of its own
-    inline = tc and dec.split_counters is not None and w.batch * w.num_kv_heads * splits <= _sms()
-    return n + (0 if (tc and splits <= 1) or inline else 1)
+    return n + merge_launches(w, dec, dec.attn_params)
 
 
 # ----------------------------------------------------------------------------
@@ -1084,7 +1095,7 @@ def main():
                     help="offload workload: weight of the previous step's block scores (0.3 in the SparDA article)")
     ap.add_argument("--swap-overlap", type=int, default=1,
                     help="offload workload: 1 = page copy overlapped with attention over the hits, 0 = one after the other")
-    ap.add_argument("--swap-copy-ctas", type=int, default=24, help="CTAs (SMs) of the overlapped page copy")
+    ap.add_argument("--swap-copy-ctas", type=int, default=12, help="CTAs (SMs) of the overlapped page copy")
     ap.add_argument("--swap-attn-ctas", type=int, default=0,
                     help="CTAs of the attention beside the copy (0 = the SMs the copy leaves)")
     args = ap.parse_args()

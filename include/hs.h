@@ -244,8 +244,9 @@ HS_API size_t hs_workspace_bytes(const hs_attn_shape* shape, int32_t batch, int3
 /* How the tensor-core attention divides its work for this geometry on the
  * current device: *splits = partial results per (request, kv head) at most,
  * *chunks_per_cta = the length of a balanced chunk range (0 = equal splits
- * per pair instead).  Returns 0, or -1 on invalid input or without a device
- * (outputs untouched).  The CUDA-core kernel always uses equal splits. */
+ * per pair instead).  Returns 0, or -1 on invalid input (outputs untouched).
+ * Without a device it assumes 148 SMs, as hs_workspace_bytes does.  The
+ * CUDA-core kernel always uses equal splits. */
 HS_API int32_t hs_attn_geometry(const hs_attn_shape* shape, int32_t batch, int32_t capacity,
                                 const hs_attn_params* params, int32_t* splits, int32_t* chunks_per_cta);
 

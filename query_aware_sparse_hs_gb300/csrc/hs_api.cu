@@ -321,10 +321,11 @@ int32_t hs_attn_geometry(const hs_attn_shape* shape, int32_t batch, int32_t capa
                          const hs_attn_params* params, int32_t* splits, int32_t* chunks_per_cta) {
   if (check_shape(shape) != HS_OK || batch < 0 || capacity < 1 || !params || !splits || !chunks_per_cta) return -1;
   if (params->blocks_per_split < 0 || params->max_ctas < 0) return -1;
-  Device d;
-  if (current_device(&d) != HS_OK) return -1;
+  Device d{};
+  int sms = 148;  // without a device: as hs_workspace_bytes
+  if (current_device(&d) == HS_OK) sms = d.sms;
   AttnArgs a;
-  split_geometry(shape, batch, capacity, params, attn_ctas(d.sms, params), &a.blocks_per_split, &a.splits, &a);
+  split_geometry(shape, batch, capacity, params, attn_ctas(sms, params), &a.blocks_per_split, &a.splits, &a);
   *splits = a.splits;
   *chunks_per_cta = a.stream_per;
   return 0;

@@ -18,6 +18,7 @@
 // other SMs (they touch disjoint slots: victims are never in the current
 // selection).
 #include "hs_internal.h"
+#include "tc_ptx.cuh"
 
 namespace hs {
 namespace {
@@ -283,6 +284,7 @@ struct MissAttn {
 
 constexpr int kMaxGroup = 16;
 constexpr int kSub = 64;  // token rows of a block staged in shared memory at a time
+constexpr int kMissWin = 64;  // misses of a stream resolved at a time by the copied-blocks attention
 
 template <int KIND>
 constexpr int elem_size() { return KIND == HS_KV_F32 ? 4 : (KIND == HS_KV_BF16 ? 2 : 1); }
@@ -530,11 +532,24 @@ __global__ __launch_bounds__(kAttnThreads) void copied_blocks_attn_kernel(HotVie
   const int32_t* pt = hb.page_table + static_cast<int64_t>(pair) * hb.max_blocks;
   const int L = ma.seq_lens[b];
   const int B = hb.block;
-  for (int i = tid; i < g * D; i += kAttnThreads) {
-    const int64_t e = qrow0 * D + i;  // heads of the group are consecutive rows
-    s_q[i] = KIND == HS_KV_F32 ? static_cast<const float*>(ma.q)[e]
-                               : bf16_bits_to_float(static_cast<const uint16_t*>(ma.q)[e]);
+  {  // q of the group (consecutive rows): every load of a thread in flight before its first store
+    constexpr int kQPer = (kMaxGroup * D + kAttnThreads - 1) / kAttnThreads;
+    float qv[kQPer];
+#pragma unroll
+    for (int u = 0; u < kQPer; ++u) {
+      const int i = tid + u * kAttnThreads;
+      const int64_t e = qrow0 * D + i;
+      qv[u] = i >= g * D ? 0.0f
+                         : (KIND == HS_KV_F32 ? static_cast<const float*>(ma.q)[e]
+                                              : bf16_bits_to_float(static_cast<const uint16_t*>(ma.q)[e]));
+    }
+#pragma unroll
+    for (int u = 0; u < kQPer; ++u)
+      if (tid + u * kAttnThreads < g * D) s_q[tid + u * kAttnThreads] = qv[u];
   }
+  // the stream's misses resolved up front, kMissWin at a time: block and slot
+  // (-1: skipped, reported by the copy)
+  __shared__ int s_mj[kMissWin], s_ms[kMissWin];
   // per head of this warp: running max and sum (log2 units), p * v of its C channels
   float m[kHpw], l[kHpw], acc[kHpw][C];
 #pragma unroll
@@ -547,10 +562,22 @@ __global__ __launch_bounds__(kAttnThreads) void copied_blocks_attn_kernel(HotVie
   const float* ksc = reinterpret_cast<const float*>(dyn + Ly::kOffKs);
   const float* vsc = reinterpret_cast<const float*>(dyn + Ly::kOffVs);
   for (int c = 0; c < n; ++c) {
-    const int j = miss_sel[row + c];
-    if (j < 0 || j >= hb.max_blocks) continue;  // reported by the copy
-    const int sl = pt[j] - pair * S;
-    if (sl < 0 || sl >= S) continue;
+    if (c % kMissWin == 0) {
+      __syncthreads();  // the previous window is used up
+      if (tid < kMissWin && c + tid < n) {
+        const int j = miss_sel[row + c + tid];
+        int sl = -1;
+        if (j >= 0 && j < hb.max_blocks) {
+          sl = pt[j] - pair * S;
+          if (sl >= S) sl = -1;
+        }
+        s_mj[tid] = j;
+        s_ms[tid] = sl < 0 ? -1 : sl;
+      }
+      __syncthreads();
+    }
+    const int j = s_mj[c % kMissWin], sl = s_ms[c % kMissWin];
+    if (sl < 0) continue;  // the same for every thread
     const int nv = min(B, L - j * B);  // valid tokens of the block (uniform)
     const int64_t row0 = (static_cast<int64_t>(pair) * S + sl) * B;
     for (int r0 = 0; r0 < nv; r0 += kSub) {
@@ -563,15 +590,25 @@ __global__ __launch_bounds__(kAttnThreads) void copied_blocks_attn_kernel(HotVie
                                                          (row0 + r0) * Ly::kRowBytes);
         const uint4* vs = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(hb.v_slots) +
                                                          (row0 + r0) * Ly::kRowBytes);
-        for (int v = tid; v < 2 * vec; v += kAttnThreads) {
+        constexpr int kPer = (2 * kSub * kVecRow + kAttnThreads - 1) / kAttnThreads;
+        uint4 xs[kPer];
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {  // every load of a thread in flight before its first store
+          const int v = tid + u * kAttnThreads;
           const int w = v < vec ? v : v - vec;
-          const uint4 x = v < vec ? ks[w] : vs[w];
+          if (v < 2 * vec) xs[u] = v < vec ? ks[w] : vs[w];
+        }
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+          const int v = tid + u * kAttnThreads;
+          if (v >= 2 * vec) break;
+          const int w = v < vec ? v : v - vec;
           uint32_t* dst = reinterpret_cast<uint32_t*>(dyn + (v < vec ? Ly::kOffK : Ly::kOffV) +
                                                       (w / kVecRow) * Ly::kStride + (w % kVecRow) * 16);
-          dst[0] = x.x;
-          dst[1] = x.y;
-          dst[2] = x.z;
-          dst[3] = x.w;
+          dst[0] = xs[u].x;
+          dst[1] = xs[u].y;
+          dst[2] = xs[u].z;
+          dst[3] = xs[u].w;
         }
         if constexpr (KIND == HS_KV_FP8E4M3_G32) {
           constexpr int G = D / kQuantGroup;
@@ -649,6 +686,253 @@ __global__ __launch_bounds__(kAttnThreads) void copied_blocks_attn_kernel(HotVie
   (void)err;
 }
 
+// The same for bf16 K/V and head_dim 128 on the tensor cores (warp-level
+// mma.sync m16n8k16, bf16 products exact, fp32 accumulation): the copied
+// blocks are a few hundred scattered tiles, too small for a tcgen05 pipeline.
+// One CTA of 4 warps per stream; warp w takes tokens [16 w, 16 w + 16) of
+// every 64-token piece of every missed block: S (16 padded heads x 16 tokens)
+// = Q.K^T over 8 k-steps of 16 channels, the online softmax per head row
+// (quad shuffles), then O (16 heads x 128 channels) += P.V with P as bf16
+// high part + remainder (the S accumulators are the A fragments of P).  The
+// warps' states are combined through shared memory at the end.
+constexpr int kMmaWarps = 4;
+constexpr int kMmaRow = 128 * 2 + 16;  // staged row: 128 bf16 + 16 bytes (ldmatrix rows hit distinct banks)
+constexpr int kMmaStage = 16 * kMmaRow;  // one warp's 16 rows of K (or V)
+constexpr int kMmaSmem = 16 * kMmaRow + kMmaWarps * 2 * kMmaStage;  // Q, then per warp K and V
+static_assert(kMmaSmem >= kMmaWarps * (16 * 128 + 32) * 4, "the warps' states fit the staging area");
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+// D += A.B, m16n8k16, bf16 inputs, fp32 accumulators
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+  asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+               "{%0, %1, %2, %3};"
+               : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+               : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// 16-byte global -> shared copy, the bytes past src_bytes zero-filled
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+__global__ __launch_bounds__(kMmaWarps * 32) void copied_blocks_attn_mma_kernel(HotView hb,
+                                                                               const int32_t* __restrict__ miss_sel,
+                                                                               const int32_t* __restrict__ miss_count,
+                                                                               int capacity, MissAttn ma,
+                                                                               unsigned* err) {
+  constexpr int D = 128;
+  extern __shared__ __align__(16) uint8_t dyn[];
+  __shared__ int s_mj[kMissWin], s_ms[kMissWin];
+  pdl_trigger();
+  pdl_wait();
+  const int pair = blockIdx.x;
+  const int S = hb.slots;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = ma.group;
+  const int b = pair / hb.hkv, kvh = pair - b * hb.hkv;
+  const int64_t qrow0 = static_cast<int64_t>(b) * ma.hq + static_cast<int64_t>(kvh) * g;
+  int n = miss_count[pair];
+  n = n < 0 ? 0 : (n > capacity ? capacity : n);
+  n = n > S ? S : n;
+  if (n == 0) {
+    if (tid < g) ma.lse[qrow0 + tid] = -INFINITY;
+    return;
+  }
+  const int64_t row = static_cast<int64_t>(pair) * capacity;
+  const int32_t* pt = hb.page_table + static_cast<int64_t>(pair) * hb.max_blocks;
+  const int L = ma.seq_lens[b];
+  const int B = hb.block;
+  const uint32_t sq = tc::smem_u32(dyn);
+  uint8_t* kst = dyn + 16 * kMmaRow + warp * 2 * kMmaStage;  // this warp's K rows, then its V rows
+  uint8_t* vst = kst + kMmaStage;
+  {  // Q of the group, 16 rows (zero past g), bf16
+    const int r = tid >> 3, seg = tid & 7;  // 128 threads: row r (0..15), 16-byte segments seg and seg + 8
+    uint4 x0 = make_uint4(0, 0, 0, 0), x1 = x0;
+    if (r < g) {
+      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(ma.q) + (qrow0 + r) * D);
+      x0 = src[seg];
+      x1 = src[seg + 8];
+    }
+    *reinterpret_cast<uint4*>(dyn + r * kMmaRow + seg * 16) = x0;
+    *reinterpret_cast<uint4*>(dyn + r * kMmaRow + (seg + 8) * 16) = x1;
+  }
+  const int q4 = lane & 3, r8 = lane >> 2;  // fragment coordinates
+  float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.0f, 0.0f};  // rows r8, r8 + 8
+  float o[16][4];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
+  for (int c = 0; c < n; ++c) {
+    if (c % kMissWin == 0) {
+      __syncthreads();  // the previous window is used up (and Q is in)
+      if (tid < kMissWin && c + tid < n) {
+        const int j = miss_sel[row + c + tid];
+        int sl = -1;
+        if (j >= 0 && j < hb.max_blocks) {
+          sl = pt[j] - pair * S;
+          if (sl >= S) sl = -1;
+        }
+        s_mj[tid] = j;
+        s_ms[tid] = sl < 0 ? -1 : sl;
+      }
+      __syncthreads();
+    }
+    const int j = s_mj[c % kMissWin], sl = s_ms[c % kMissWin];
+    if (sl < 0) continue;  // reported by the copy; the same for every thread
+    const int nv = min(B, L - j * B);  // valid tokens of the block
+    const int64_t row0 = (static_cast<int64_t>(pair) * S + sl) * B;
+    for (int r0 = 0; r0 < nv; r0 += 64) {
+      const int t0 = r0 + 16 * warp;  // this warp's first token of the piece
+      const int rows = min(16, nv - t0);
+      if (rows <= 0) continue;  // the same for the whole warp
+      {  // stage this warp's 16 K and V rows by asynchronous copies (zero fill past the valid tokens)
+        const uint8_t* kg = static_cast<const uint8_t*>(hb.k_slots) + (row0 + t0) * (D * 2);
+        const uint8_t* vg = static_cast<const uint8_t*>(hb.v_slots) + (row0 + t0) * (D * 2);
+        __syncwarp();  // every lane is done with the previous piece's rows
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {  // 16 rows x 16 segments; lane takes segment lane & 15 of rows 2u + (lane >> 4)
+          const int rr = 2 * u + (lane >> 4), seg = lane & 15;
+          const int bytes = rr < rows ? 16 : 0;
+          const int rs = rr < rows ? rr : 0;  // (a valid address even when nothing is read)
+          cp_async16(tc::smem_u32(kst + rr * kMmaRow + seg * 16), kg + rs * (D * 2) + seg * 16, bytes);
+          cp_async16(tc::smem_u32(vst + rr * kMmaRow + seg * 16), vg + rs * (D * 2) + seg * 16, bytes);
+        }
+        cp_async_wait_all();
+        __syncwarp();
+      }
+      // S = Q.K^T: 16 heads x 16 tokens (two n-tiles of 8 tokens)
+      float sc[2][4];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.0f;
+      const uint32_t kbase = tc::smem_u32(kst);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
+        ldsm_x4(sq + ((lane & 7) + ((lane >> 3) & 1) * 8) * kMmaRow + (16 * ks + (lane >> 4) * 8) * 2, a0, a1, a2, a3);
+        ldsm_x4(kbase + ((lane & 7) + (lane >> 4) * 8) * kMmaRow + (16 * ks + ((lane >> 3) & 1) * 8) * 2, b0, b1, b2,
+                b3);
+        mma_bf16_16816(sc[0], a0, a1, a2, a3, b0, b1);
+        mma_bf16_16816(sc[1], a0, a1, a2, a3, b2, b3);
+      }
+      // online softmax per head row (rows r8 and r8 + 8; tokens 8 i + 2 q4 + {0, 1})
+      float alpha[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float x[4];
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int tok = 8 * i + 2 * q4 + e;
+            x[2 * i + e] = tok < rows ? sc[i][2 * h + e] * ma.scale_log2 : -INFINITY;
+          }
+        float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const float mn = fmaxf(m[h], mx);
+        alpha[h] = m[h] == -INFINITY ? (mn == -INFINITY ? 1.0f : 0.0f) : exp2f(m[h] - mn);
+        float sum = 0.0f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          x[k] = x[k] == -INFINITY ? 0.0f : exp2f(x[k] - mn);
+          sum += x[k];
+        }
+        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+        l[h] = l[h] * alpha[h] + sum;
+        m[h] = mn;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          sc[i][2 * h] = x[2 * i];
+          sc[i][2 * h + 1] = x[2 * i + 1];
+        }
+      }
+      // P as A fragments (bf16 high part + remainder)
+      uint32_t ph[4], pl[4];
+      {
+        const float pv[4][2] = {{sc[0][0], sc[0][1]}, {sc[0][2], sc[0][3]}, {sc[1][0], sc[1][1]}, {sc[1][2], sc[1][3]}};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const __nv_bfloat162 hi = __floats2bfloat162_rn(pv[k][0], pv[k][1]);
+          const float2 hf = __bfloat1622float2(hi);
+          ph[k] = *reinterpret_cast<const uint32_t*>(&hi);
+          pl[k] = pack_bf16(pv[k][0] - hf.x, pv[k][1] - hf.y);
+        }
+      }
+      // O = O * alpha + P.V over the 16 channel tiles
+      const uint32_t vbase = tc::smem_u32(vst);
+#pragma unroll
+      for (int dt = 0; dt < 16; dt += 2) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(vbase + ((lane & 7) + ((lane >> 3) & 1) * 8) * kMmaRow + (8 * dt + (lane >> 4) * 8) * 2, b0, b1, b2,
+                  b3);
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          float (&od)[4] = o[dt + e];
+          od[0] *= alpha[0];
+          od[1] *= alpha[0];
+          od[2] *= alpha[1];
+          od[3] *= alpha[1];
+          const uint32_t bb0 = e ? b2 : b0, bb1 = e ? b3 : b1;
+          mma_bf16_16816(od, ph[0], ph[1], ph[2], ph[3], bb0, bb1);
+          mma_bf16_16816(od, pl[0], pl[1], pl[2], pl[3], bb0, bb1);
+        }
+      }
+    }
+  }
+  // combine the four warps' states through shared memory: per warp o [16][128], m [16], l [16]
+  __syncthreads();  // every warp is done with its staging rows
+  float* xo = reinterpret_cast<float*>(dyn);
+  float* xm = xo + kMmaWarps * 16 * 128;
+  float* xl = xm + kMmaWarps * 16;
+#pragma unroll
+  for (int dt = 0; dt < 16; ++dt) {
+    const int d = 8 * dt + 2 * q4;
+    float* w0 = xo + (warp * 16 + r8) * 128 + d;
+    w0[0] = o[dt][0];
+    w0[1] = o[dt][1];
+    w0[8 * 128] = o[dt][2];
+    w0[8 * 128 + 1] = o[dt][3];
+  }
+  if (q4 == 0) {
+    xm[warp * 16 + r8] = m[0];
+    xm[warp * 16 + r8 + 8] = m[1];
+    xl[warp * 16 + r8] = l[0];
+    xl[warp * 16 + r8 + 8] = l[1];
+  }
+  __syncthreads();
+  // thread t: channel t of every head of the group
+  for (int h = 0; h < g; ++h) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kMmaWarps; ++w) M = fmaxf(M, xm[w * 16 + h]);
+    float lt = 0.0f, acc = 0.0f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kMmaWarps; ++w) {
+        const float mw = xm[w * 16 + h];
+        const float sw = mw == -INFINITY ? 0.0f : exp2f(mw - M);
+        lt = fmaf(xl[w * 16 + h], sw, lt);
+        acc = fmaf(xo[(w * 16 + h) * 128 + tid], sw, acc);
+      }
+    }
+    if (lt > 0.0f) ma.out[(qrow0 + h) * D + tid] = acc / lt;
+    if (tid == 0) ma.lse[qrow0 + h] = lt > 0.0f ? (M + log2f(lt)) * 0.6931471805599453f : -INFINITY;
+  }
+  (void)err;
+}
+
 }  // namespace
 
 template <int C, int KIND>
@@ -701,7 +985,13 @@ cudaError_t launch_swapin_copy(const HotView& hb, const int32_t* miss_sel, const
   ma.group = attn->hq / hb.hkv;
   if (hb.head_dim == 128) {
     if (hb.kv_dtype == HS_KV_F32) return launch_attend<4, HS_KV_F32>(hb, miss_sel, miss_count, capacity, ma, err, st);
-    if (hb.kv_dtype == HS_KV_BF16) return launch_attend<4, HS_KV_BF16>(hb, miss_sel, miss_count, capacity, ma, err, st);
+    if (hb.kv_dtype == HS_KV_BF16) {
+      cudaError_t e2 = cudaFuncSetAttribute(copied_blocks_attn_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            kMmaSmem);
+      if (e2 != cudaSuccess) return e2;
+      return launch_pdl(copied_blocks_attn_mma_kernel, dim3(hb.batch * hb.hkv), dim3(kMmaWarps * 32), kMmaSmem, st,
+                        hb, miss_sel, miss_count, capacity, ma, err);
+    }
     return launch_attend<4, HS_KV_FP8E4M3_G32>(hb, miss_sel, miss_count, capacity, ma, err, st);
   }
   if (hb.kv_dtype == HS_KV_F32) return launch_attend<2, HS_KV_F32>(hb, miss_sel, miss_count, capacity, ma, err, st);

@@ -133,7 +133,7 @@ class SparseDecode:
     def swap_in(self, hb: hs.HotBuffer, step: int, stats=None, stream=None):
         hs.hs_swapin_misses(self.shape, hb, self.sel, self.sel_count, self.capacity, step, stats, stream)
 
-    def enable_swap_overlap(self, copy_ctas: int = 24, attn_ctas: int = 0):
+    def enable_swap_overlap(self, copy_ctas: int = 12, attn_ctas: int = 0):
         """Allocates what the overlapped swap-in step needs: hit and miss lists,
         two fp32 partial results, a side stream for the page copy.  The copy
         kernel runs ``copy_ctas`` CTAs, each on an SM of its own; the attention
@@ -154,7 +154,10 @@ class SparseDecode:
         self.part_out = torch.empty((2, b, hq, d), dtype=torch.float32, device=dev)
         self.part_lse = torch.empty((2, b, hq), dtype=torch.float32, device=dev)
         p = self.attn_params
-        self.hit_params = hs.attn_params(p.scale, True, p.blocks_per_split, p.algo, max_ctas=attn_ctas)
+        # (with the split counters the attention over the hits can cut its
+        # work into balanced chunk ranges over the CTAs it is given)
+        self.hit_params = hs.attn_params(p.scale, True, p.blocks_per_split, p.algo, max_ctas=attn_ctas,
+                                         split_counters=self.split_counters)
         ws = hs.hs_workspace_bytes(self.shape, self.batch, self.capacity, self.hit_params)
         if ws > self.workspace.numel():
             self.workspace = torch.empty((ws,), dtype=torch.uint8, device=dev)

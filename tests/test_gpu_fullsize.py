@@ -115,7 +115,7 @@ def test_full_size_offload_steps(overlap):
     hot-buffer tables of sampled pairs follow the oracle's simulator exactly over
     several drifting decode steps, and the attention on the hot slots matches -
     with the swap-in in one call, and overlapped (page copy and attention over
-    the copied blocks on 24 SMs beside attention over the resident blocks)."""
+    the copied blocks on 12 SMs beside attention over the resident blocks)."""
     from query_aware_sparse_hs_gb300 import hs
     from query_aware_sparse_hs_gb300.decode import SparseDecode
     from _parity import tie_window_ok
