@@ -39,8 +39,11 @@ __device__ __forceinline__ unsigned long long umin64(unsigned long long a, unsig
 struct PlanSmem {
   int owner[kMaxSlots];
   int last[kMaxSlots];
+  int sel[kMaxSlots];  // the stream's selection
   unsigned char prot[kMaxSlots];
-  unsigned char hit[kMaxSlots];  // per selection entry: resident at entry
+  // per selection entry: 1 = resident at entry, 2 = a page-table entry out of
+  // the stream's slots (skipped by the victim walk), 0 = to be brought in
+  unsigned char hit[kMaxSlots];
   int copy_j[kMaxSlots];
   int copy_s[kMaxSlots];
   int ncopy, hits, evict;
@@ -74,12 +77,17 @@ __device__ int plan_stream(const HotView& hb, const int32_t* my_sel, int cnt, in
   // hits: stamp and protect
   for (int i = tid; i < cnt; i += blockDim.x) {
     const int j = my_sel[i];
+    sm.sel[i] = j;
     sm.hit[i] = 0;
     if (j < 0 || j >= hb.max_blocks) continue;
     const int g = pt[j];
     if (g >= 0) {
       const int s = g - base;
-      if (s < 0 || s >= S) { set_error(err, HS_EBIT_PAGE_RANGE); continue; }
+      if (s < 0 || s >= S) {
+        set_error(err, HS_EBIT_PAGE_RANGE);
+        sm.hit[i] = 2;
+        continue;
+      }
       sm.prot[s] = 1;
       sm.last[s] = step;
       sm.hit[i] = 1;
@@ -88,15 +96,16 @@ __device__ int plan_stream(const HotView& hb, const int32_t* my_sel, int cnt, in
   }
   __syncthreads();
 
-  // misses, in ascending block order
+  // misses, in ascending block order (from shared memory only: a miss's
+  // page-table entry is -1 until this walk assigns it a slot)
   if (warp == 0) {
     for (int i = 0; i < cnt; ++i) {
-      const int j = my_sel[i];
+      const int j = sm.sel[i];
       if (j < 0 || j >= hb.max_blocks) {
         if (lane == 0) set_error(err, HS_EBIT_BLOCK_RANGE);
         continue;
       }
-      if (pt[j] >= 0) continue;  // a hit
+      if (sm.hit[i]) continue;  // resident (or an entry out of the stream's slots)
       // victim key: (class, last_used, slot); class 0 = free, 1 = evictable, 3 = protected
       unsigned long long best = ~0ull;
       for (int s = lane; s < S; s += 32) {
@@ -243,8 +252,8 @@ __global__ __launch_bounds__(kThreads) void swapin_plan_kernel(HotView hb, const
       const int i = i0 + lane;
       const int j = i < cnt ? my_sel[i] : -1;
       const bool valid = i < cnt && j >= 0 && j < hb.max_blocks;
-      const bool h = valid && sm.hit[i];
-      const bool m = valid && !sm.hit[i];
+      const bool h = valid && sm.hit[i] == 1;
+      const bool m = valid && sm.hit[i] != 1;
       const unsigned bh = __ballot_sync(0xffffffffu, h), bm = __ballot_sync(0xffffffffu, m);
       const unsigned below = (1u << lane) - 1u;
       if (h) hit_sel[row + nh + __popc(bh & below)] = j;
