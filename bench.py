@@ -162,9 +162,13 @@ def step_launches(w, dec, hot: bool = False, overlap: bool = False, allow_fused:
         return 1  # the append runs inside the single launch
     n += select_launches(w)
     if hot and overlap:
-        # plan, page copy, attention over the copied blocks, attention over the
-        # hits (+ its split merge), merge of the parts
-        return n + 5 + merge_launches(w, dec, dec.hit_params)
+        # plan (inside the selection's launch when the scorer takes its own
+        # launch and a request has at most 1024 blocks), page copy, attention
+        # over the copied blocks, attention over the hits (+ its split merge),
+        # merge of the parts
+        plan_in_select = (select_launches(w) == 2 and w.kv_dtype == "bf16" and w.head_dim == 128
+                          and w.max_blocks <= 1024)
+        return n + (4 if plan_in_select else 5) + merge_launches(w, dec, dec.hit_params)
     n += 1 if hot else 0
     n += 1
     return n + merge_launches(w, dec, dec.attn_params)

@@ -433,6 +433,20 @@ HS_API hs_status hs_swapin_plan(const hs_attn_shape* shape, const hs_hot_buffer*
                                 const int32_t* sel_count, int32_t capacity, int32_t step, int32_t* hit_sel,
                                 int32_t* hit_count, int32_t* miss_sel, int32_t* miss_count,
                                 hs_swap_stats* stats_opt, hs_stream_t stream);
+/* hs_score_select_topk(shape, kv, q, smin, smax, sel_params, sel, sel_count,
+ * scores_opt, workspace, ws_bytes) followed by hs_swapin_plan(shape, hb, sel,
+ * sel_count, sel_params->capacity, step, hit_sel, hit_count, miss_sel,
+ * miss_count, stats_opt): the same outputs, argument rules and error bits as
+ * those two calls ([KVS] §5 selection, §7 hot buffer), and hb->batch must
+ * equal kv->batch.  With tensor-core scoring in more than one wave and at most
+ * 1024 blocks per request, each stream's plan runs in the selection's launch,
+ * right after its selection. */
+HS_API hs_status hs_score_select_swapin_plan(const hs_attn_shape* shape, const hs_paged_kv* kv, const void* q,
+                                             const void* smin, const void* smax, const hs_select_params* sel_params,
+                                             int32_t* sel, int32_t* sel_count, float* scores_opt, void* workspace,
+                                             size_t ws_bytes, const hs_hot_buffer* hb, int32_t step,
+                                             int32_t* hit_sel, int32_t* hit_count, int32_t* miss_sel,
+                                             int32_t* miss_count, hs_swap_stats* stats_opt, hs_stream_t stream);
 HS_API hs_status hs_swapin_copy(const hs_attn_shape* shape, const hs_hot_buffer* hb, const int32_t* miss_sel,
                                 const int32_t* miss_count, int32_t capacity, int32_t max_ctas,
                                 hs_swap_stats* stats_opt, hs_stream_t stream);

@@ -639,6 +639,40 @@ hs_status hs_swapin_plan(const hs_attn_shape* shape, const hs_hot_buffer* hb, co
                                       stats_opt, d.err, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+hs_status hs_score_select_swapin_plan(const hs_attn_shape* shape, const hs_paged_kv* kv, const void* q,
+                                      const void* smin, const void* smax, const hs_select_params* sel_params,
+                                      int32_t* sel, int32_t* sel_count, float* scores_opt, void* workspace,
+                                      size_t ws_bytes, const hs_hot_buffer* hb, int32_t step, int32_t* hit_sel,
+                                      int32_t* hit_count, int32_t* miss_sel, int32_t* miss_count,
+                                      hs_swap_stats* stats_opt, hs_stream_t stream) {
+  SelectArgs a;
+  hs_status st = prepare_select(shape, kv, q, smin, smax, sel_params, sel, sel_count, scores_opt, &a);
+  if (st != HS_OK) return st;
+  if (!hit_sel || !hit_count || !miss_sel || !miss_count) return HS_ERR_INVALID_ARG;
+  if (hit_sel == sel || miss_sel == sel || hit_sel == miss_sel) return HS_ERR_INVALID_ARG;
+  HotView hv;
+  if ((st = hot_view(shape, hb, &hv)) != HS_OK) return st;
+  if (hb->batch != kv->batch) return HS_ERR_INVALID_ARG;
+  Device d;
+  if ((st = current_device(&d)) != HS_OK) return st;
+  const KvView v = make_view(shape, kv);
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (score_tc_supported(v) && !score_select_fused_supported(v, d.sms) && select_plan_supported(v, hv)) {
+    float* buf = a.scores;
+    if (!buf) {
+      const size_t need = static_cast<size_t>(v.batch) * v.hkv * v.max_blocks * sizeof(float);
+      if (!workspace || ws_bytes < need || !aligned(workspace, 16)) return HS_ERR_WORKSPACE;
+      buf = static_cast<float*>(workspace);
+    }
+    if (launch_score_tc(v, a.q, a.smin, a.smax, buf, d.sms, d.err, cs) != cudaSuccess) return HS_ERR_CUDA;
+    const PlanArgs pa{hv, step, hit_sel, hit_count, miss_sel, miss_count, stats_opt};
+    return from_cuda(launch_select_plan(v, a, buf, pa, d.err, cs));
+  }
+  if ((st = run_select(v, a, d, workspace, ws_bytes, cs)) != HS_OK) return st;
+  return from_cuda(launch_swapin_plan(hv, sel, sel_count, a.capacity, step, hit_sel, hit_count, miss_sel, miss_count,
+                                      stats_opt, d.err, cs));
+}
+
 hs_status hs_swapin_copy(const hs_attn_shape* shape, const hs_hot_buffer* hb, const int32_t* miss_sel,
                          const int32_t* miss_count, int32_t capacity, int32_t max_ctas,
                          hs_swap_stats* stats_opt, hs_stream_t stream) {

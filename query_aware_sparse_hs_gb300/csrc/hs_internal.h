@@ -95,6 +95,22 @@ cudaError_t launch_swapin(const HotView& hb, const int32_t* sel, const int32_t* 
 cudaError_t launch_swapin_plan(const HotView& hb, const int32_t* sel, const int32_t* sel_count, int capacity,
                                int step, int32_t* hit_sel, int32_t* hit_count, int32_t* miss_sel,
                                int32_t* miss_count, hs_swap_stats* stats, unsigned* err, cudaStream_t st);
+// The hot-buffer plan run by the selection launch right after each stream's
+// selection (the same outputs as launch_swapin_plan).
+struct PlanArgs {
+  HotView hb;
+  int32_t step;
+  int32_t* hit_sel;
+  int32_t* hit_count;
+  int32_t* miss_sel;
+  int32_t* miss_count;
+  hs_swap_stats* stats;  // nullable
+};
+// false when the geometry needs the separate launches (more than 1024 blocks
+// per request or slots per stream)
+bool select_plan_supported(const KvView& kv, const HotView& hb);
+cudaError_t launch_select_plan(const KvView& kv, const SelectArgs& a, const float* scores, const PlanArgs& pa,
+                               unsigned* err, cudaStream_t st);
 // Attention over the blocks a page copy brings in (q rows of the stream's query heads).
 struct MissAttnArgs {
   const void* q;

@@ -17,6 +17,7 @@
 
 #include "hs_internal.h"
 #include "select_pair.cuh"
+#include "swapin_plan.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -166,18 +167,16 @@ __global__ void __cluster_dims__(kSelectCluster, 1, 1) __launch_bounds__(kThread
   select_pair<kThreads>(s_scores, nb, L, B, a, pair, s_hist, s_warp, err);
 }
 
-// One CTA per (request, kv head): scores already in global memory (written by
-// the tensor-core scorer) -> selection.
+// The selection of one (request, kv head) from its scores in global memory
+// (written by the tensor-core scorer), by all THREADS threads of the CTA.
 template <int THREADS, int KPT>
-__global__ __launch_bounds__(THREADS) void select_only_kernel(KvView kv, SelectArgs a, const float* scores,
-                                                              unsigned* err) {
+__device__ __forceinline__ void select_from_scores(const KvView& kv, const SelectArgs& a, const float* scores,
+                                                   unsigned* err) {
   constexpr int kWarps = THREADS / 32;
   extern __shared__ float s_scores[];
   __shared__ uint32_t s_hist[3][kHistWords];
   __shared__ int s_warp[kWarps];
   __shared__ uint32_t s_range[2 * kWarps];
-  pdl_trigger();
-  pdl_wait();
   const int tid = threadIdx.x;
   const int64_t pair = blockIdx.x;
   const int b = static_cast<int>(pair / kv.hkv);
@@ -214,6 +213,33 @@ __global__ __launch_bounds__(THREADS) void select_only_kernel(KvView kv, SelectA
   smooth_scores(s_scores, nb, kv.max_blocks, a, pair);
   select_pair_regs<THREADS, KPT>(s_scores, nb, L, B, a, pair, s_hist, s_warp, err, nullptr,
                                   smoothed ? nullptr : s_range, kWarps, true);
+}
+
+// One CTA per (request, kv head): scores -> selection.
+template <int THREADS, int KPT>
+__global__ __launch_bounds__(THREADS) void select_only_kernel(KvView kv, SelectArgs a, const float* scores,
+                                                              unsigned* err) {
+  pdl_trigger();
+  pdl_wait();
+  select_from_scores<THREADS, KPT>(kv, a, scores, err);
+}
+
+// The same, then the HiSparse hot-buffer plan of the stream ("KV 稀疏化" wiki
+// §7) on the selection this CTA has just written: one launch instead of the
+// selection and hs_swapin_plan's kernel, with the same outputs.
+template <int THREADS, int KPT>
+__global__ __launch_bounds__(THREADS) void select_plan_kernel(KvView kv, SelectArgs a, const float* scores,
+                                                              PlanArgs pa, unsigned* err) {
+  __shared__ plan::PlanSmem sm;
+  pdl_trigger();
+  pdl_wait();
+  select_from_scores<THREADS, KPT>(kv, a, scores, err);
+  __syncthreads();  // the stream's selection, written to global memory by this CTA, is complete
+  const int pair = blockIdx.x;
+  const int32_t* my_sel = a.sel + static_cast<int64_t>(pair) * a.capacity;
+  const int cnt = plan::plan_stream(pa.hb, my_sel, a.sel_count[pair], a.capacity, pa.step, pair, sm, err);
+  plan::write_lists(pa.hb, my_sel, cnt, a.capacity, pair, sm, pa.hit_sel, pa.hit_count, pa.miss_sel, pa.miss_count,
+                    pa.stats);
 }
 
 template <int C, int G, bool F32>
@@ -253,6 +279,21 @@ cudaError_t launch_select_only(const KvView& kv, const SelectArgs& a, const floa
   const int threads = kv.max_blocks > 1024 ? 1024 : kThreads;
   if (cudaError_t e = allow_dynamic_smem(kern, smem); e != cudaSuccess) return e;
   return launch_pdl(kern, dim3(pairs), dim3(threads), smem, st, kv, a, scores, err);
+}
+
+bool select_plan_supported(const KvView& kv, const HotView& hb) {
+  return kv.max_blocks <= 1024 && hb.slots <= plan::kMaxSlots;
+}
+
+cudaError_t launch_select_plan(const KvView& kv, const SelectArgs& a, const float* scores, const PlanArgs& pa,
+                               unsigned* err, cudaStream_t st) {
+  const int pairs = kv.batch * kv.hkv;
+  if (pairs == 0) return cudaSuccess;
+  if (!select_plan_supported(kv, pa.hb)) return cudaErrorInvalidValue;
+  const size_t smem = static_cast<size_t>(kv.max_blocks) * sizeof(float);
+  auto kern = select_plan_kernel<kThreads, 1024 / kThreads>;
+  if (cudaError_t e = allow_dynamic_smem(kern, smem); e != cudaSuccess) return e;
+  return launch_pdl(kern, dim3(pairs), dim3(kThreads), smem, st, kv, a, scores, pa, err);
 }
 
 cudaError_t launch_score_select(const KvView& kv, const SelectArgs& a, unsigned* err,

@@ -164,14 +164,16 @@ class SparseDecode:
         self.side_stream = torch.cuda.Stream(device=dev)
 
     def swap_in_overlapped(self, hb: hs.HotBuffer, slot_kv: hs.PagedKV, q: torch.Tensor, step: int,
-                           stats=None, stream=None):
+                           stats=None, stream=None, planned=False):
         """Swap-in and attention with the page copy overlapped: plan (hit and
-        miss lists) -> [side stream: copy the missed pages and attend over
-        them] | attention over the hits -> LSE merge of the two parts into
-        ``out``/``lse``.  Needs enable_swap_overlap() first."""
+        miss lists; already made when ``planned``) -> [side stream: copy the
+        missed pages and attend over them] | attention over the hits -> LSE
+        merge of the two parts into ``out``/``lse``.  Needs
+        enable_swap_overlap() first."""
         main = stream if stream is not None else torch.cuda.current_stream(self.sel.device)
-        hs.hs_swapin_plan(self.shape, hb, self.sel, self.sel_count, self.capacity, step, self.hit_sel,
-                          self.hit_count, self.miss_sel, self.miss_count, stats, main)
+        if not planned:
+            hs.hs_swapin_plan(self.shape, hb, self.sel, self.sel_count, self.capacity, step, self.hit_sel,
+                              self.hit_count, self.miss_sel, self.miss_count, stats, main)
         side = self.side_stream
         side.wait_stream(main)
         hs.hs_swapin_copy_attend(self.shape, hb, slot_kv.seq_lens, q, self.miss_sel, self.miss_count, self.capacity,
@@ -215,6 +217,15 @@ class SparseDecode:
             return self.out, self.lse
         if hot is None and self.fuse_step:
             self.select_attend(kv, q, stream=stream)
+            return self.out, self.lse
+        if hot is not None and getattr(self, "side_stream", None) is not None:
+            # selection and the swap-in plan (one launch where it fits), then the overlapped copy
+            hb, slot_kv, step_idx, stats = hot
+            hs.hs_score_select_swapin_plan(self.shape, kv, q, self.smin, self.smax, self.sel_params, self.sel,
+                                           self.sel_count, hb, step_idx, self.hit_sel, self.hit_count,
+                                           self.miss_sel, self.miss_count, scores=self.scores, stats=stats,
+                                           stream=stream)
+            self.swap_in_overlapped(hb, slot_kv, q, step_idx, stats, stream, planned=True)
             return self.out, self.lse
         self.select(kv, q, stream=stream)
         if hot is not None:

@@ -107,6 +107,10 @@ SYMBOLS = {
                                    c_int32, c_void_p, c_void_p]),
     "hs_swapin_plan": (c_int32, [POINTER(AttnShape), POINTER(HotBuffer), c_void_p, c_void_p, c_int32, c_int32,
                                  c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
+    "hs_score_select_swapin_plan": (c_int32, [POINTER(AttnShape), POINTER(PagedKV), c_void_p, c_void_p, c_void_p,
+                                              POINTER(SelectParams), c_void_p, c_void_p, c_void_p, c_void_p,
+                                              c_size_t, POINTER(HotBuffer), c_int32, c_void_p, c_void_p, c_void_p,
+                                              c_void_p, c_void_p, c_void_p]),
     "hs_swapin_copy": (c_int32, [POINTER(AttnShape), POINTER(HotBuffer), c_void_p, c_void_p, c_int32, c_int32,
                                  c_void_p, c_void_p]),
     "hs_swapin_copy_attend": (c_int32, [POINTER(AttnShape), POINTER(HotBuffer), c_void_p, c_void_p, c_void_p,
@@ -338,6 +342,18 @@ def hs_swapin_plan(shape, hb, sel, sel_count, capacity, step, hit_sel, hit_count
                                int(step), _ptr(hit_sel), _ptr(hit_count), _ptr(miss_sel), _ptr(miss_count),
                                _ptr(stats), _stream(stream)),
            "hs_swapin_plan")
+
+
+def hs_score_select_swapin_plan(shape, kv, q, smin, smax, params, sel, sel_count, hb, step, hit_sel, hit_count,
+                                miss_sel, miss_count, scores=None, workspace=None, stats=None, stream=None):
+    """hs_score_select_topk then hs_swapin_plan, each stream's plan in the selection's launch where it fits."""
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(_lib.hs_score_select_swapin_plan(ctypes.byref(shape), ctypes.byref(kv), _ptr(q), _ptr(smin), _ptr(smax),
+                                            ctypes.byref(params), _ptr(sel), _ptr(sel_count), _ptr(scores),
+                                            _ptr(workspace), ws_bytes, ctypes.byref(hb), int(step), _ptr(hit_sel),
+                                            _ptr(hit_count), _ptr(miss_sel), _ptr(miss_count), _ptr(stats),
+                                            _stream(stream)),
+           "hs_score_select_swapin_plan")
 
 
 def hs_swapin_copy(shape, hb, miss_sel, miss_count, capacity, max_ctas=0, stats=None, stream=None):

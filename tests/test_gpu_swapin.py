@@ -254,3 +254,53 @@ def test_plan_then_copy_equals_the_one_call_swapin():
         for a, b in zip(st1, st2):
             assert torch.equal(a, b), t
     assert torch.equal(stats1, stats2)
+
+
+def test_select_plan_in_one_launch_equals_the_two_calls():
+    """hs_score_select_swapin_plan (each stream's plan in the selection's
+    launch once the scoring takes more than one wave) leaves the same
+    selection, hit and miss lists, tables and statistics as
+    hs_score_select_topk followed by hs_swapin_plan, over drifting steps."""
+    from query_aware_sparse_hs_gb300 import hs
+    from query_aware_sparse_hs_gb300.decode import SparseDecode
+    # 160 (request, kv head) pairs of one 128-block tile: more than one wave of the scorer
+    w, x = _setup("bf16", batch=40, blocks=48, slots=16, k_scored=7)
+    dev = torch.device("cuda")
+    B, D, S, hkv, nb = w.block_size, w.head_dim, w.hot_slots, w.num_kv_heads, w.max_blocks
+    hk, hv, _, _ = _pool(w, x)
+    lens = x["seq_lens"].to(dev)
+    pool_kv = hs.paged_kv(hk, hv, x["page_table"].to(dev), lens)
+    pairs = w.batch * hkv
+
+    def side():
+        t = torch.full((w.batch, hkv, nb), -1, dtype=torch.int32, device=dev)
+        o = torch.full((w.batch, hkv, S), -1, dtype=torch.int32, device=dev)
+        l = torch.full((w.batch, hkv, S), -1, dtype=torch.int32, device=dev)
+        k = torch.zeros((pairs * S, B, D), dtype=torch.bfloat16, device=dev)
+        d = SparseDecode(num_q_heads=w.num_q_heads, num_kv_heads=hkv, head_dim=D, block_size=B, kv_dtype="bf16",
+                         batch=w.batch, max_blocks=nb, sink_tokens=w.sink_tokens, window_tokens=w.window_tokens,
+                         k_scored=w.k_scored)
+        d.build_summaries(pool_kv)
+        lists = [torch.full_like(d.sel, -1) for _ in range(2)] + [torch.zeros_like(d.sel_count) for _ in range(2)]
+        return hs.hot_buffer(t, o, l, k, torch.zeros_like(k), hk, hv, S), (t, o, l), d, lists, \
+            torch.zeros(4, dtype=torch.int64, device=dev)
+
+    hb1, tab1, d1, l1, st1 = side()
+    hb2, tab2, d2, l2, st2 = side()
+    qs = drift_queries(w, x["q"], 6)
+    for t in range(6):
+        q = qs[t]
+        d1.select(pool_kv, q)
+        hs.hs_swapin_plan(d1.shape, hb1, d1.sel, d1.sel_count, d1.capacity, t, l1[0], l1[2], l1[1], l1[3], st1)
+        hs.hs_score_select_swapin_plan(d2.shape, pool_kv, q, d2.smin, d2.smax, d2.sel_params, d2.sel, d2.sel_count,
+                                       hb2, t, l2[0], l2[2], l2[1], l2[3], scores=d2.scores, stats=st2)
+        st, bits = hs.hs_get_device_error()
+        assert st == 0, bits
+        assert torch.equal(d1.sel, d2.sel) and torch.equal(d1.sel_count, d2.sel_count), t
+        assert torch.equal(d1.scores, d2.scores), t
+        for a, b in zip(l1, l2):
+            assert torch.equal(a, b), t
+        for a, b in zip(tab1, tab2):
+            assert torch.equal(a, b), t
+    assert torch.equal(st1, st2)
+    assert int(st1[1]) > 0  # the drift brought misses in
