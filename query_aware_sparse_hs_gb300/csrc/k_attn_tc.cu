@@ -328,49 +328,35 @@ __device__ __forceinline__ int find_item(const TcArgs& a, int bpc, int item, Ite
   return item;
 }
 
-// Lane's block of the group of 32 selected positions starting at `gbase`
-// (lane i: position gbase + i) in three steps, so that a caller can spread
-// the two dependent global reads over other work: the selection entry, the
-// page-table entry, then the checks giving (page, valid tokens), page -1 past
-// the item or for a bad entry.
-__device__ __forceinline__ int group_sel(const TcArgs& a, const Item& it, int gbase, const Work& w) {
-  if (w.list) return -1;
-  const int pos = it.s0 + gbase + (threadIdx.x & 31);
-  return pos < it.s1 && pos < a.capacity ? a.sel[static_cast<int64_t>(it.pair) * a.capacity + pos] : -1;
-}
-__device__ __forceinline__ int group_page(const TcArgs& a, const Item& it, int j, const Work& w) {
-  if (w.list || j < 0 || j >= it.nb) return -1;
-  return a.page_table[static_cast<int64_t>(it.pair) * a.max_blocks + j];
-}
-__device__ __forceinline__ int2 group_finish(const TcArgs& a, const Item& it, int gbase, int j, int page,
-                                             unsigned* bad, const Work& w) {
+// Lane's block of the group of 32 selected positions starting at `gbase`:
+// (page, valid tokens), page -1 past the item or for a bad entry.  The
+// selection entry is read without waiting for the item's count.
+__device__ __forceinline__ int2 resolve_group(const TcArgs& a, const Item& it, int gbase, unsigned* bad,
+                                              const Work& w) {
   const int lane = threadIdx.x & 31;
   if (w.list) return it.s0 + gbase + lane < it.s1 ? w.list[gbase + lane] : make_int2(-1, 0);
-  if (it.s0 + gbase + lane >= it.s1) return make_int2(-1, 0);
+  const int pos = it.s0 + gbase + lane;
+  const int64_t row = static_cast<int64_t>(it.pair) * a.capacity;
+  const int j = pos < a.capacity ? a.sel[row + pos] : -1;
+  if (pos >= it.s1) return make_int2(-1, 0);
   if (j < 0 || j >= it.nb) {
     *bad |= HS_EBIT_BLOCK_RANGE;
     return make_int2(-1, 0);
   }
+  const int page = a.page_table[static_cast<int64_t>(it.pair) * a.max_blocks + j];
   if (page < 0 || page >= a.num_pages) {
     *bad |= HS_EBIT_PAGE_RANGE;
     return make_int2(-1, 0);
   }
   return make_int2(page, min(a.block, it.L - j * a.block));
 }
-__device__ __forceinline__ int2 resolve_group(const TcArgs& a, const Item& it, int gbase, unsigned* bad,
-                                              const Work& w) {
-  const int j = group_sel(a, it, gbase, w);
-  return group_finish(a, it, gbase, j, group_page(a, it, j, w), bad, w);
-}
 
 // TMA producer warp (all 32 lanes).  An item's selected blocks are resolved 32
-// at a time (lane i: block i of the group); the next group - of this item or
-// the first of the next one - is resolved in steps taken between this group's
-// chunk issues, each step using what a load of the step before brought, so
-// the producer never waits on a dependent global read (selection entry, then
-// page-table entry; the next item's count and length first).  Each chunk's
-// pages and valid-token counts are published in meta[stage][8] for the
-// softmax warps and every lane issues the copies of its own block.
+// at a time (lane i: block i of the group) and the next group - of this item or
+// of the next one - is looked up while the current group's chunks are issued,
+// so page-table lookups stay off the copy stream.  Each chunk's pages and
+// valid-token counts are published in meta[stage][8] for the softmax warps and
+// every lane issues the copies of its own block.
 // prog[0] / prog[5]: chunks issued so far / the item being issued.
 template <int STAGES, class W, typename IssueFn>
 __device__ __forceinline__ void run_producer(const TcArgs& a, const W& w, int bpc, uint32_t full0, uint32_t empty0,
@@ -389,64 +375,47 @@ __device__ __forceinline__ void run_producer(const TcArgs& a, const W& w, int bp
     int next_item = item;
     Item nit = it;
     for (int g = 0; g < ngroups && !stop; ++g) {
-      const bool same = g + 1 < ngroups;  // the next group is in this item
-      const int gb = same ? (g + 1) * 32 : 0;
-      const int cand = item + w.stride;
-      ItemPre npre{0, 0};
-      int jn = -1, pn = -1, ph = 0;
-      const int nph = same ? 3 : 4;
+      // the next group (of this item, or the first of the next item) is
+      // looked up once this group's first chunks fill the ring, so that its
+      // dependent loads overlap the copies in flight instead of delaying them
       int2 nxt = make_int2(-1, 0);
-      auto step = [&]() {
-        if (same) {
-          if (ph == 0) jn = group_sel(a, it, gb, w);
-          else if (ph == 1) pn = group_page(a, it, jn, w);
-          else nxt = group_finish(a, it, gb, jn, pn, &bad, w);
-        } else if (ph == 0) {
-          if (cand < w.end) npre = item_pre(a, cand, w);
-        } else if (ph == 1) {
-          next_item = w.end;
-          if (cand < w.end) {
-            nit = item_geom_from(a, cand, bpc, w, npre);
-            next_item = nit.nch > 0 ? cand : find_item(a, bpc, cand + w.stride, &nit, w);
-          }
-          if (next_item < w.end) jn = group_sel(a, nit, 0, w);
-        } else if (ph == 2) {
-          if (next_item < w.end) pn = group_page(a, nit, jn, w);
-        } else if (next_item < w.end) {
-          nxt = group_finish(a, nit, 0, jn, pn, &bad, w);
+      bool looked = false;
+      auto look_ahead = [&]() {
+        if (g + 1 < ngroups) {
+          nxt = resolve_group(a, it, (g + 1) * 32, &bad, w);
+        } else {
+          next_item = find_item(a, bpc, item + w.stride, &nit, w);
+          if (next_item < w.end) nxt = resolve_group(a, nit, 0, &bad, w);
         }
-        ++ph;
+        looked = true;
       };
-      // one pass: a step before the group's first chunk (its loads go out
-      // before the copies), then one after each chunk, the rest after the last
       const int gchunks = min(32 / bpc, (nblk - g * 32 + bpc - 1) / bpc);
-      for (int k = -1; k < gchunks || ph < nph; ++k) {
-        if (k >= 0 && k < gchunks) {
-          int go = 0;
-          if (lane == 0)
-            go = !*abort_flag &&
-                 (c < STAGES || mbar_wait(empty0 + 8 * (c % STAGES), ((c / STAGES) + 1) & 1, abort_flag, a.wait_ns));
-          if (!__shfl_sync(0xffffffffu, go, 0)) {
-            stop = true;
-            break;
-          }
-          const int s = c % STAGES;
-          const int bi = lane - k * bpc;
-          const bool mine = bi >= 0 && bi < bpc;
-          if (mine) meta[s * 8 + bi] = cur;
-          const uint32_t tx = __reduce_add_sync(0xffffffffu, (mine && cur.x >= 0) ? bytes_per_block : 0u);
-          __syncwarp();
-          if (lane == 0) mbar_arrive_tx(full0 + 8 * s, tx);
-          __syncwarp();
-          if (mine && cur.x >= 0) issue(s, bi, cur.x);
-          if (lane == 0) {
-            prog[0] = c + 1;
-            prog[5] = item;
-          }
-          ++c;
+      const int look_at = min(gchunks, STAGES) - 1;
+      for (int k = 0; k < gchunks; ++k, ++c) {
+        int go = 0;
+        if (lane == 0)
+          go = !*abort_flag &&
+               (c < STAGES || mbar_wait(empty0 + 8 * (c % STAGES), ((c / STAGES) + 1) & 1, abort_flag, a.wait_ns));
+        if (!__shfl_sync(0xffffffffu, go, 0)) {
+          stop = true;
+          break;
         }
-        if (ph < nph) step();
+        const int s = c % STAGES;
+        const int bi = lane - k * bpc;
+        const bool mine = bi >= 0 && bi < bpc;
+        if (mine) meta[s * 8 + bi] = cur;
+        const uint32_t tx = __reduce_add_sync(0xffffffffu, (mine && cur.x >= 0) ? bytes_per_block : 0u);
+        __syncwarp();
+        if (lane == 0) mbar_arrive_tx(full0 + 8 * s, tx);
+        __syncwarp();
+        if (mine && cur.x >= 0) issue(s, bi, cur.x);
+        if (lane == 0) {
+          prog[0] = c + 1;
+          prog[5] = item;
+        }
+        if (k == look_at) look_ahead();
       }
+      if (!looked && !stop) look_ahead();  // a group shorter than the ring
       cur = nxt;
     }
     item = next_item;
