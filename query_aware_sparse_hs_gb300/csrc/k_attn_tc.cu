@@ -1434,26 +1434,29 @@ struct Layout8 {
 // group's scale in f16 (the scale and the product each rounded once); zeros
 // for a row of no token.  Two threads per row (r, cp = 0, 1); the 16-byte
 // segments are staggered so that eight consecutive threads touch eight
-// different bank groups on the loads and on the stores.
-__device__ __forceinline__ void convert_half_row(const uint8_t* codes_row, const float* scales, uint8_t* tile, int r,
-                                                 int cp, bool valid) {
-  __half2 sc[2];
-  {
-    const float2 s2 = valid ? *reinterpret_cast<const float2*>(scales + 2 * cp) : make_float2(0.0f, 0.0f);
-    sc[0] = __float2half2_rn(s2.x);
-    sc[1] = __float2half2_rn(s2.y);
-  }
-  // all four loads first: the tile stores below could alias them for all the
-  // compiler knows, so it would not move a load above an earlier store
+// different bank groups on the loads and on the stores.  In two parts: the
+// codes and scales out of the stage into registers (after which the stage
+// may be refilled), then the conversion into the tile.
+struct HalfRow {
   uint4 raw[4];
+  float2 s2;
+};
+__device__ __forceinline__ HalfRow load_half_row(const uint8_t* codes_row, const float* scales, int r, int cp,
+                                                 bool valid) {
+  HalfRow h;
+  h.s2 = valid ? *reinterpret_cast<const float2*>(scales + 2 * cp) : make_float2(0.0f, 0.0f);
 #pragma unroll
   for (int i = 0; i < 4; ++i)
-    raw[i] = valid ? *reinterpret_cast<const uint4*>(codes_row + (4 * cp + ((i + r + 2 * cp) & 3)) * 16)
-                   : make_uint4(0, 0, 0, 0);
+    h.raw[i] = valid ? *reinterpret_cast<const uint4*>(codes_row + (4 * cp + ((i + r + 2 * cp) & 3)) * 16)
+                     : make_uint4(0, 0, 0, 0);
+  return h;
+}
+__device__ __forceinline__ void store_half_row(const HalfRow& hr, uint8_t* tile, int r, int cp) {
+  const __half2 sc[2] = {__float2half2_rn(hr.s2.x), __float2half2_rn(hr.s2.y)};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int ch = 4 * cp + ((i + r + 2 * cp) & 3);  // 16-code segment of the row
-    const uint32_t words[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+    const uint32_t words[4] = {hr.raw[i].x, hr.raw[i].y, hr.raw[i].z, hr.raw[i].w};
     uint32_t w[8];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -1624,9 +1627,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= kConv8Warp0 && warp < kConv8Warp0 + 8) {
     // ================= V conversion: e4m3 rows times scales -> f16 V tiles =================
-    // threads (r, cp) convert half cp of row r of chunk c into V tile c % 3
-    // once the P.V product of chunk c-3 is done with it; then release their
-    // part of the stage
+    // threads (r, cp) take half cp of row r of chunk c out of the stage,
+    // release their part of it, and convert it into V tile c % 3 once the
+    // P.V product of chunk c-3 is done with that tile
     const int ct = tid - kConv8Warp0 * 32;  // 0..255
     const int r = ct >> 1, cp = ct & 1;
     int c = 0;
@@ -1636,16 +1639,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int ci = 0; ci < it.nch; ++ci, ++c) {
         const int s = c % kStages8;
         const int vt = c % kVTiles;  // its last reader, the P.V product of chunk c - 3
-        ok = mbar_wait(full_bar(s), (c / kStages8) & 1, abort_flag, a.wait_ns) &&
-             (c < kVTiles || mbar_wait(vfree(vt), ((c / kVTiles) - 1) & 1, abort_flag, a.wait_ns));
+        ok = mbar_wait(full_bar(s), (c / kStages8) & 1, abort_flag, a.wait_ns);
         if (!ok) break;
         const int2 md = meta[s * 8 + r / B];
         const bool valid = md.x >= 0 && (r % B) < md.y;
-        convert_half_row(vc_stage(s) + r * 128, reinterpret_cast<const float*>(vs_stage(s) + r * 16),
-                         smem + Ly::kOffVh + vt * kTileBytes, r, cp, valid);
+        const HalfRow hr = load_half_row(vc_stage(s) + r * 128, reinterpret_cast<const float*>(vs_stage(s) + r * 16),
+                                         r, cp, valid);
+        mbar_arrive(empty_bar(s));  // (the arrival's release orders the reads above before the stage's refill)
+        ok = c < kVTiles || mbar_wait(vfree(vt), ((c / kVTiles) - 1) & 1, abort_flag, a.wait_ns);
+        if (!ok) break;
+        store_half_row(hr, smem + Ly::kOffVh + vt * kTileBytes, r, cp);
         fence_async_smem();
         mbar_arrive(vconv_full(vt));
-        mbar_arrive(empty_bar(s));
       }
     }
   } else {
