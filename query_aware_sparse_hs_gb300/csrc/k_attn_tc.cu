@@ -1388,17 +1388,19 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 //          v = code_v * vscale in f16 (scale and product each rounded once:
 //          relative error <= 2^-10), P split into f16 hi + lo.
 // TMA stages the codes (K with the 128-byte swizzle the MMA reads) and the
-// scales, three stages.  Two converter warpgroups (two threads per row) turn
-// V codes times their scales into one of three f16 V tiles once GEMM2 of the
-// chunk three back is done with it (each tile has its own free barrier).  Two softmax groups of 4 warps take the
+// scales, four stages.  Two converter warpgroups (two threads per row) turn
+// V codes times their scales into one of two f16 V tiles once GEMM2 of the
+// chunk two back is done with it (each tile has its own free barrier).  The
+// ring is the deeper of the two: the loads in flight set the chunk rate, and
+// a V tile is free again soon after its product is issued.  Two softmax groups of 4 warps take the
 // chunks alternately (group g the chunks c with c % 2 == g, with its own S,
 // O and running state, combined at the end of an item); a group releases a
 // stage once GEMM1 of its chunk is complete and its K scales are read, and
 // takes the O of its previous chunk before it writes P of chunk c into its
 // own P buffer.
 // ============================================================================
-constexpr int kStages8 = 3;
-constexpr int kVTiles = 3;                        // f16 V tiles: chunk c converts into tile c % 3
+constexpr int kStages8 = 4;
+constexpr int kVTiles = 2;                        // f16 V tiles: chunk c converts into tile c % 2
 constexpr int kCodeBytes = kChunk * 128;          // 128 tokens x 128 codes
 constexpr int kScaleBytes = kChunk * 16;          // 128 tokens x 4 scales
 constexpr int kStage8Bytes = 2 * kCodeBytes + 2 * kScaleBytes;
@@ -1415,8 +1417,10 @@ struct Layout8 {
   static constexpr int kNumBars = 2 * kStages8 + 9 + 2 * kVTiles + kPBufs;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kOffRed = kOffMisc + 16;             // per group: 2 x [4 warps][8] maxima, [4][8] sums
-  static constexpr int kOffX = kOffRed + 2 * 3 * 4 * 8 * 4;  // group 1's o [8][128], m [8], l [8]
-  static constexpr int kOffMeta = kOffX + (8 * 128 + 16) * 4;
+  // (group 1's o [8][128] is handed to group 0 at the end of an item in its
+  // own P buffer, its m [8] and l [8] in its chunk-max buffers: both are free
+  // once the group's last P.V product is taken)
+  static constexpr int kOffMeta = kOffRed + 2 * 3 * 4 * 8 * 4;
   static constexpr int kOffProg = kOffMeta + kStages8 * 8 * 8;  // progress words (as in the bf16 kernel)
   static constexpr int kOffQx = (kOffProg + 32 + 15) / 16 * 16;  // per head: the exponent a_h of the item's query,
   static constexpr int kBytes = kOffQx + 64;                     // then the softmax scale times 2^-a_h (16-byte loads)
@@ -1628,8 +1632,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= kConv8Warp0 && warp < kConv8Warp0 + 8) {
     // ================= V conversion: e4m3 rows times scales -> f16 V tiles =================
     // threads (r, cp) take half cp of row r of chunk c out of the stage,
-    // release their part of it, and convert it into V tile c % 3 once the
-    // P.V product of chunk c-3 is done with that tile
+    // release their part of it, and convert it into V tile c % 2 once the
+    // P.V product of chunk c-2 is done with that tile
     const int ct = tid - kConv8Warp0 * 32;  // 0..255
     const int r = ct >> 1, cp = ct & 1;
     int c = 0;
@@ -1638,7 +1642,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Item it = item_geom(a, item, bpc, w);
       for (int ci = 0; ci < it.nch; ++ci, ++c) {
         const int s = c % kStages8;
-        const int vt = c % kVTiles;  // its last reader, the P.V product of chunk c - 3
+        const int vt = c % kVTiles;  // its last reader, the P.V product of chunk c - 2
         ok = mbar_wait(full_bar(s), (c / kStages8) & 1, abort_flag, a.wait_ns);
         if (!ok) break;
         const int2 md = meta[s * 8 + r / B];
@@ -1662,8 +1666,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int bar = 1 + grp;      // the group's named barrier; 3 = both groups
     const int g = a.group;
     float* red = reinterpret_cast<float*>(smem + Ly::kOffRed) + grp * 3 * 4 * NH;
-    float* xo = reinterpret_cast<float*>(smem + Ly::kOffX);
-    float* xm = xo + NH * 128;
+    float* xo = reinterpret_cast<float*>(smem + Ly::kOffP + Ly::kPBytes);  // group 1's P buffer
+    float* xm = reinterpret_cast<float*>(smem + Ly::kOffRed) + 3 * 4 * NH;  // group 1's chunk maxima
     float* xl = xm + NH;
     int c = 0;
     // Query terms: row (cg, h) of each term holds head h's codes of channel
