@@ -198,6 +198,42 @@ def test_attention_balanced_ranges(cases, name, max_ctas):
         assert int(dec.split_counters.abs().sum()) == 0
 
 
+@pytest.mark.parametrize("name", ["llama_bf16_tail", "ragged_bf16", "fp8_tail"])
+def test_attention_equal_splits_several_items_per_cta(cases, name):
+    """Equal splits on three CTAs: each CTA takes many work items in turn, so
+    every item boundary inside the tensor-core kernels (the next query, the
+    two softmax groups' states combined, the exchange buffers reused) runs
+    between items of different pairs.  Same oracle bound as the other cases."""
+    from _parity import TOL
+    from query_aware_sparse_hs_gb300 import hs
+    c = cases[name]
+    w = c.w
+    dec = c.decoder(out_is_fp32=True, algo="tcgen05")
+    dec.attn_params = hs.attn_params(dec.attn_params.scale, True, 0, "tcgen05", max_ctas=3,
+                                     split_counters=dec.split_counters, ranges=False)
+    splits, per = hs.hs_attn_geometry(dec.shape, w.batch, dec.capacity, dec.attn_params)
+    assert per == 0 and splits >= 1  # equal splits, not chunk ranges
+    dec.workspace = torch.empty((hs.hs_workspace_bytes(dec.shape, w.batch, dec.capacity, dec.attn_params),),
+                                dtype=torch.uint8, device=dec.workspace.device)
+    dec.build_summaries(c.kv)
+    dec.select(c.kv, c.q)
+    dec.attend(c.kv, c.q)
+    _err_clear()
+    sel, cnt = dec.sel.cpu().numpy(), dec.sel_count.cpu().numpy()
+    out, lse = dec.out.cpu().numpy(), dec.lse.cpu().numpy()
+    g = w.group
+    scale = 1.0 / math.sqrt(w.head_dim)
+    tol = TOL["fp8_dequant"] if w.kv_dtype == "fp8" else TOL[w.kv_dtype]
+    for b in range(w.batch):
+        for kvh in range(w.num_kv_heads):
+            got = sel[b, kvh, :cnt[b, kvh]].tolist()  # the oracle's attention over the kernel's selection
+            ref_out, ref_lse = O.sparse_attention(c.q_group(b, kvh), c.logical(b, kvh, "k"), c.logical(b, kvh, "v"),
+                                                  got, w.block_size, scale)
+            assert np.abs(out[b, kvh * g:(kvh + 1) * g] - ref_out).max() <= tol, (b, kvh)
+            assert np.abs(lse[b, kvh * g:(kvh + 1) * g] - ref_lse).max() <= 1e-4, (b, kvh)
+    assert int(dec.split_counters.abs().sum()) == 0
+
+
 def test_k_covers_everything_is_dense_attention():
     """With k at least the block count the result is dense softmax attention."""
     from _parity import Case
