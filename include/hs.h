@@ -145,7 +145,11 @@ typedef struct hs_select_params {
  * blocks_per_split: selected blocks handled by one CTA before the LSE merge;
  * 0 = chosen by the library from the SMs the call may use.  algo: 0 =
  * automatic, 1 = CUDA-core kernel (every dtype), 2 = tensor-core (tcgen05)
- * kernel (bf16 and e4m3 only; HS_ERR_UNSUPPORTED otherwise).  max_ctas: 0 =
+ * kernel (bf16 and e4m3 only; HS_ERR_UNSUPPORTED otherwise).  The e4m3
+ * tensor-core kernel forms each V value, code times scale, in f16 (as it does
+ * the products with P), so it needs |code * scale| <= 65504 (a V scale up to
+ * 146 for codes up to 448); beyond that its output is not finite.  The
+ * CUDA-core kernel forms them in fp32.  max_ctas: 0 =
  * the tensor-core kernel runs one CTA on every SM; n > 0 = at most n CTAs (and
  * the automatic split for n SMs), leaving the other SMs to work launched
  * beside it, such as hs_swapin_copy.  Each of its CTAs takes a whole SM's
